@@ -1,0 +1,68 @@
+// Internal declarations shared by the translation units of libpg.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pg.h"
+
+namespace pg {
+
+// ---------------------------------------------------------------- host helpers
+
+// Remember a CUDA error for pg_last_cuda_error() and map it to PG_ERR_CUDA.
+pg_status cuda_fail(cudaError_t err);
+
+// Check the last launch; counts `n` launches on success.
+pg_status after_launch(int n);
+
+// Streaming multiprocessor count and compute capability of the current device.
+int sm_count();
+int device_cc();
+
+// Device address of this library's device-side error word (current device).
+int* device_error_word();
+
+// Validated table geometry (what pg_table_geometry reports).
+struct Geometry {
+  uint64_t rows;
+  uint32_t row_bytes;
+  uint32_t e_width;
+  int O;      // orders
+  int H;      // heads per order (flat and toy: 1)
+  int W;      // 64-bit sign words per (order, head)
+};
+pg_status validate_desc(const pg_table_desc* d, Geometry* g);
+
+// ---------------------------------------------------------------- hashing
+
+constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
+constexpr uint32_t kPad = 0xFFFFFFFFu;
+
+__host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Flat index of multiplier (kind, o, k, j) in HashParams::mult.
+__host__ __device__ __forceinline__ int mult_index(int kind, int o, int k, int j) {
+  return ((kind * PG_MAX_ORDERS + o) * PG_MAX_HEADS + k) * 4 + j;
+}
+constexpr int kNumMult = 3 * PG_MAX_ORDERS * PG_MAX_HEADS * 4;
+
+// Everything a hashing kernel needs, passed by value (kernel parameter space).
+struct HashParams {
+  uint64_t mult[kNumMult];                        // odd multipliers m_{kind,o,k,j}
+  uint32_t divisor[PG_MAX_ORDERS][PG_MAX_HEADS];  // Engram M_{o,k}; flat R_o and PageGram P_o at [o][0]
+  uint32_t base[PG_MAX_ORDERS][PG_MAX_HEADS];     // first row of (o,k) (Engram) or of order o at [o][0]
+  int32_t order_n[PG_MAX_ORDERS];                 // n of order index o
+  int32_t O, H, K, S, W, r;
+  int32_t mode, hash_kind;
+  uint32_t vocab;
+  uint32_t toy_m;
+};
+
+void fill_hash_params(const pg_table_desc* d, const Geometry& g, HashParams* p);
+
+}  // namespace pg

@@ -1,0 +1,735 @@
+// Projection and gates (sm_103a).
+//
+//   v = W_V e_t, k^(m) = W_K^(m) e_t (one fused GEMM over [W_V; W_K^(1..M)], Engram notes
+//   (arXiv 2601.07372) section 3.4), then
+//   scalar gate   x + g v                                   PageGram report section 3.1
+//   context gate  alpha = sigmoid(RMSNorm(h)^T RMSNorm(k) / sqrt(d))   Engram notes 3.3/3.4
+//
+// bf16: a persistent tcgen05 GEMM. One CTA per SM, 6 warps:
+//   warp 0      TMA producer: 128x64 A (e) and BNx64 B (W) tiles, 128-byte swizzle,
+//               into a 4-stage shared-memory ring (mbarrier full/empty pairs)
+//   warp 1      allocates 2*BN TMEM columns (two fp32 accumulators) and issues
+//               tcgen05.mma (M=128, N=BN, K=16) from one thread; tcgen05.commit
+//               frees smem stages and publishes finished accumulators
+//   warps 2..5  epilogue: tcgen05.ld 32x32b (thread = output row), gate math, stores;
+//               context-gate tiles reduce per-row partial sums instead of storing
+// The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
+// fp32: a register-tiled SIMT FFMA GEMM (fp32 tolerance 1e-5 rules out TF32).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "pg_internal.cuh"
+
+namespace pg {
+namespace {
+
+// ==================================================================== PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after ~1 s
+
+// Waits for the phase of `parity` to complete; false after the time limit or when
+// another role of the CTA has already given up (`abort`).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D(tmem) (+)= A(smem desc) x B(smem desc)^T, bf16 in, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on `bar` when all previously issued tcgen05.mma of this thread complete.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) for a K-major operand tile written
+// by TMA with 128-byte swizzle: rows of 64 bf16 (128 B), 8-row atoms of 1024 B.
+//   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4 (unused here)
+//   bits 32-45 stride byte offset >> 4 (1024 B between 8-row atoms)
+//   bits 46-47 descriptor version 1    bits 61-63 layout: 2 = 128-byte swizzle
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+  uint64_t d = static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9,
+// 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 w, float* f) {
+  f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(w.z << 16); f[5] = __uint_as_float(w.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(w.w << 16); f[7] = __uint_as_float(w.w & 0xFFFF0000u);
+}
+
+// ==================================================================== tcgen05 GEMM
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kABytes = kBM * kBK * 2;
+
+struct GemmArgs {
+  int N;          // rows of e (tokens)
+  int Din;        // reduction length
+  int Dcols;      // rows of W = output columns of the GEMM ((1+M)*d)
+  int d;          // model width
+  int M;          // branches (context gate)
+  float g;        // scalar gate
+  const __nv_bfloat16* x;    // [N, d] residual (scalar gate)
+  const __nv_bfloat16* h;    // [M, N, d] branch states (context gate)
+  const float* gamma_h;      // [d]
+  const float* gamma_k;      // [d]
+  __nv_bfloat16* v_out;      // [N, d]
+  float* partials;           // [M, d/BN, 3, N] (context gate)
+  int* err_word;
+};
+
+struct GemmBarriers {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int BN>
+constexpr size_t gemm_smem_bytes() {
+  return 1024 /* alignment slack */ + kStages * (kABytes + BN * kBK * 2) + sizeof(GemmBarriers);
+}
+
+template <int BN, int GATE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const GemmArgs args) {
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN);
+  constexpr uint32_t kTmemCols = 2 * BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  GemmBarriers* bars = reinterpret_cast<GemmBarriers*>(sB + kStages * kBBytes);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&bars->tmem_full[a]), 1);
+      mbar_init(smem_u32(&bars->tmem_empty[a]), 4 * 32);
+    }
+    mbar_init(smem_u32(&bars->mma_done), 1);
+    bars->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  const int num_m = (args.N + kBM - 1) / kBM;
+  const int num_n = args.Dcols / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = args.Din / kBK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&map_a);
+      tma_prefetch_map(&map_b);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t issued = 0;  // bit s: stage s holds a load nobody has consumed yet (error path)
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bars->full[stage]);
+          mbar_expect_tx(full, kABytes + kBBytes);
+          tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
+          tma_load_2d(smem_u32(sB + stage * kBBytes), &map_b, full, kb * kBK, n_blk * BN);
+          issued |= 1u << stage;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        atomicOr(args.err_word, 1);
+        *abort = 1;
+        // Let copies already in flight land before the CTA can exit (bounded).
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) {
+            const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(&bars->full[s]), par) && globaltimer() - t0 < kWaitLimitNs) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&bars->full[stage]), phase, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a0 = sw128_desc(smem_u32(sA + stage * kABytes));
+          const uint64_t b0 = sw128_desc(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // advance 16 elements = 32 bytes = 2 units
+            umma_bf16(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc, (kb | k) != 0);
+          umma_commit(smem_u32(&bars->empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&bars->tmem_full[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) {
+        atomicOr(args.err_word, 2);
+        *abort = 1;
+      }
+      // Every MMA this thread issued has finished before TMEM can be released.
+      umma_commit(smem_u32(&bars->mma_done));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&bars->mma_done), 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    const int tpb = args.d / BN;  // tiles per branch (context gate)
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
+      if (!mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int row = m_blk * kBM + row_in_tile;
+      const bool live = row < args.N;
+      const int n0 = n_blk * BN;
+      const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>(acc * BN);
+      if (GATE != PG_GATE_CONTEXT || n0 < args.d) {
+        // v (or x + g v) columns [n0, n0 + BN) of this row
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_base + c, r);
+          tmem_ld_wait();
+          if (live) {
+            const size_t off = static_cast<size_t>(row) * args.d + n0 + c;
+            uint4* dst = reinterpret_cast<uint4*>(args.v_out + off);
+            if (GATE == PG_GATE_SCALAR) {
+              const uint4* xs = reinterpret_cast<const uint4*>(args.x + off);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float xf[8];
+                unpack_bf16x8(__ldg(xs + q), xf);
+                float o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = fmaf(args.g, __uint_as_float(r[8 * q + i]), xf[i]);
+                dst[q] = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                                    pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(
+                    pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
+                    pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                    pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                    pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+            }
+          }
+        }
+      } else {
+        // k^(m) columns: per-row partial sums for the gate of branch m
+        const int m = n0 / args.d - 1;
+        const int kc = n0 - (m + 1) * args.d;  // column inside the branch
+        const int tb = kc / BN;
+        float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
+        const __nv_bfloat16* hrow = args.h + (static_cast<size_t>(m) * args.N + (live ? row : 0)) * args.d;
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_base + c, r);
+          tmem_ld_wait();
+          if (live) {
+            const uint4* hs = reinterpret_cast<const uint4*>(hrow + kc + c);
+            const float4* gh = reinterpret_cast<const float4*>(args.gamma_h + kc + c);
+            const float4* gk = reinterpret_cast<const float4*>(args.gamma_k + kc + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float hf[8];
+              unpack_bf16x8(__ldg(hs + q), hf);
+              const float4 gh0 = __ldg(gh + 2 * q), gh1 = __ldg(gh + 2 * q + 1);
+              const float4 gk0 = __ldg(gk + 2 * q), gk1 = __ldg(gk + 2 * q + 1);
+              const float ghv[8] = {gh0.x, gh0.y, gh0.z, gh0.w, gh1.x, gh1.y, gh1.z, gh1.w};
+              const float gkv[8] = {gk0.x, gk0.y, gk0.z, gk0.w, gk1.x, gk1.y, gk1.z, gk1.w};
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float kv = __uint_as_float(r[8 * q + i]);
+                s_kk = fmaf(kv, kv, s_kk);
+                s_hh = fmaf(hf[i], hf[i], s_hh);
+                s_hk = fmaf(ghv[i] * gkv[i] * hf[i], kv, s_hk);
+              }
+            }
+          }
+        }
+        if (live) {
+          float* p = args.partials + (static_cast<size_t>(m * tpb + tb) * 3) * args.N + row;
+          p[0] = s_hk;
+          p[args.N] = s_kk;
+          p[2 * static_cast<size_t>(args.N)] = s_hh;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      atomicOr(args.err_word, 4);
+      *abort = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// alpha[m, t] from the per-tile partial sums (summed in tile order: deterministic).
+__global__ void __launch_bounds__(256) alpha_finalize_kernel(const float* __restrict__ partials, int M,
+                                                             int tpb, int N, int d, float eps,
+                                                             float* __restrict__ alpha) {
+  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<int64_t>(M) * N) return;
+  const int m = static_cast<int>(idx / N);
+  const int row = static_cast<int>(idx - static_cast<int64_t>(m) * N);
+  float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
+  for (int tb = 0; tb < tpb; ++tb) {
+    const float* p = partials + (static_cast<size_t>(m * tpb + tb) * 3) * N + row;
+    s_hk += p[0];
+    s_kk += p[N];
+    s_hh += p[2 * static_cast<size_t>(N)];
+  }
+  const float inv_d = 1.0f / static_cast<float>(d);
+  const float rh = sqrtf(s_hh * inv_d + eps);
+  const float rk = sqrtf(s_kk * inv_d + eps);
+  const float s = s_hk / (rh * rk * sqrtf(static_cast<float>(d)));
+  alpha[idx] = 1.0f / (1.0f + expf(-s));
+}
+
+// ==================================================================== fp32 SIMT GEMM
+
+constexpr int kSimtTile = 64;
+constexpr int kSimtK = 16;
+
+// out[N, Dout] = A[N, Din] B[Dout, Din]^T (+ gate); 256 threads, 4x4 outputs each.
+template <int GATE>
+__global__ void __launch_bounds__(256) simt_gemm_f32_kernel(const float* __restrict__ A,
+                                                            const float* __restrict__ Bw, int N,
+                                                            int Din, int Dout, const float* __restrict__ x,
+                                                            float g, float* __restrict__ out) {
+  __shared__ float As[kSimtK][kSimtTile + 4];
+  __shared__ float Bs[kSimtK][kSimtTile + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * kSimtTile, n0 = blockIdx.x * kSimtTile;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < Din; k0 += kSimtK) {
+    for (int i = threadIdx.x; i < kSimtTile * kSimtK; i += 256) {
+      const int r = i / kSimtK, kk = i - (i / kSimtK) * kSimtK;
+      As[kk][r] = (m0 + r < N && k0 + kk < Din) ? A[static_cast<size_t>(m0 + r) * Din + k0 + kk] : 0.f;
+      Bs[kk][r] = (n0 + r < Dout && k0 + kk < Din) ? Bw[static_cast<size_t>(n0 + r) * Din + k0 + kk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kSimtK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = As[kk][ty + 16 * i];
+        b[i] = Bs[kk][tx + 16 * i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = m0 + ty + 16 * i, c = n0 + tx + 16 * j;
+      if (r < N && c < Dout) {
+        const size_t off = static_cast<size_t>(r) * Dout + c;
+        out[off] = GATE == PG_GATE_SCALAR ? fmaf(g, acc[i][j], x[off]) : acc[i][j];
+      }
+    }
+}
+
+// ==================================================================== identity projection
+
+// W == NULL (Din == d): v = e, or x + g e for the scalar gate; 8 elements per thread.
+template <typename T, int GATE>
+__global__ void __launch_bounds__(256) identity_gate_kernel(const T* __restrict__ e, const T* __restrict__ x,
+                                                            float g, T* __restrict__ out, int64_t n) {
+  for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 8; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x * 8) {
+    if constexpr (sizeof(T) == 2) {
+      const uint4 ev = *reinterpret_cast<const uint4*>(e + i);
+      float ef[8], o[8];
+      unpack_bf16x8(ev, ef);
+      if (GATE == PG_GATE_SCALAR) {
+        float xf[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(x + i), xf);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o[q] = fmaf(g, ef[q], xf[q]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o[q] = ef[q];
+      }
+      *reinterpret_cast<uint4*>(out + i) = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
+                                                      pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        out[i + q] = GATE == PG_GATE_SCALAR ? fmaf(g, e[i + q], x[i + q]) : e[i + q];
+    }
+  }
+}
+
+// ==================================================================== host side
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row-major), box [box_rows, 64] with 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int GATE>
+pg_status launch_tc(const void* e, const void* W, const GemmArgs& a, cudaStream_t stream) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, e, a.N, a.Din, kBM) || !make_map(&mb, W, a.Dcols, a.Din, BN))
+    return PG_ERR_UNSUPPORTED;
+  auto kern = tc_gemm_kernel<BN, GATE>;
+  const size_t smem = gemm_smem_bytes<BN>();
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return cuda_fail(err);
+  const int tiles = ((a.N + kBM - 1) / kBM) * (a.Dcols / BN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  kern<<<grid, kGemmThreads, smem, stream>>>(ma, mb, a);
+  return after_launch(1);
+}
+
+template <int BN>
+pg_status dispatch_tc(int gate, const void* e, const void* W, const GemmArgs& a, cudaStream_t stream) {
+  if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE>(e, W, a, stream);
+  if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR>(e, W, a, stream);
+  return launch_tc<BN, PG_GATE_CONTEXT>(e, W, a, stream);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace pg
+
+extern "C" {
+
+pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t dtype,
+                                         int32_t gate_kind, size_t* bytes) {
+  if (!bytes) return PG_ERR_NULL;
+  if (N < 0 || Din < 1 || d < 1 || M < 0) return PG_ERR_SHAPE;
+  *bytes = 0;
+  if (gate_kind == PG_GATE_CONTEXT && dtype == PG_BF16) {
+    const int bn = (d % 256 == 0) ? 256 : 128;
+    *bytes = static_cast<size_t>(M) * (d / bn) * 3 * static_cast<size_t>(N) * sizeof(float);
+  }
+  return PG_OK;
+}
+
+pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t dtype, const void* e,
+                          const void* W, int32_t gate_kind, float g, const void* x_resid, const void* h,
+                          const float* gamma_h, const float* gamma_k, float eps, void* v_out,
+                          float* alpha_out, void* workspace, size_t workspace_bytes, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (N < 0 || Din < 1 || d < 1 || M < 0) return PG_ERR_SHAPE;
+  if (gate_kind < PG_GATE_NONE || gate_kind > PG_GATE_CONTEXT) return PG_ERR_SHAPE;
+  if (dtype != PG_F32 && dtype != PG_BF16) return PG_ERR_DTYPE;
+  if (gate_kind != PG_GATE_CONTEXT && M != 0) return PG_ERR_SHAPE;
+  if (gate_kind == PG_GATE_CONTEXT && M < 1) return PG_ERR_SHAPE;
+  if (N == 0) return PG_OK;
+  if (!e || !v_out) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_SCALAR && !x_resid) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_CONTEXT && (!W || !h || !gamma_h || !gamma_k || !alpha_out)) return PG_ERR_NULL;
+  if (!aligned16(e) || !aligned16(v_out) || (x_resid && !aligned16(x_resid))) return PG_ERR_ALIGN;
+  if (static_cast<int64_t>(N) * (d > Din ? d : Din) >= (1ll << 40)) return PG_ERR_SHAPE;
+  if (sm_count() == 0) return cuda_fail(cudaGetLastError());
+
+  if (!W) {  // identity projection: a flat table's e_t is already d wide
+    if (Din != d) return PG_ERR_SHAPE;
+    if (d % 8) return PG_ERR_UNSUPPORTED;
+    const int64_t n = static_cast<int64_t>(N) * d;
+    const int64_t want = (n / 8 + 255) / 256;
+    const int blocks = static_cast<int>(want < sm_count() * 8ll ? want : sm_count() * 8ll);
+    if (dtype == PG_BF16) {
+      auto* eb = static_cast<const __nv_bfloat16*>(e);
+      auto* xb = static_cast<const __nv_bfloat16*>(x_resid);
+      auto* ob = static_cast<__nv_bfloat16*>(v_out);
+      if (gate_kind == PG_GATE_SCALAR) identity_gate_kernel<__nv_bfloat16, PG_GATE_SCALAR><<<blocks, 256, 0, stream>>>(eb, xb, g, ob, n);
+      else identity_gate_kernel<__nv_bfloat16, PG_GATE_NONE><<<blocks, 256, 0, stream>>>(eb, xb, g, ob, n);
+    } else {
+      auto* ef = static_cast<const float*>(e);
+      auto* xf = static_cast<const float*>(x_resid);
+      auto* of = static_cast<float*>(v_out);
+      if (gate_kind == PG_GATE_SCALAR) identity_gate_kernel<float, PG_GATE_SCALAR><<<blocks, 256, 0, stream>>>(ef, xf, g, of, n);
+      else identity_gate_kernel<float, PG_GATE_NONE><<<blocks, 256, 0, stream>>>(ef, xf, g, of, n);
+    }
+    return after_launch(1);
+  }
+
+  if (dtype == PG_F32) {
+    if (gate_kind == PG_GATE_CONTEXT) return PG_ERR_UNSUPPORTED;
+    dim3 grid((d + kSimtTile - 1) / kSimtTile, (N + kSimtTile - 1) / kSimtTile);
+    auto* A = static_cast<const float*>(e);
+    auto* B = static_cast<const float*>(W);
+    auto* x = static_cast<const float*>(x_resid);
+    auto* out = static_cast<float*>(v_out);
+    if (gate_kind == PG_GATE_SCALAR) simt_gemm_f32_kernel<PG_GATE_SCALAR><<<grid, 256, 0, stream>>>(A, B, N, Din, d, x, g, out);
+    else simt_gemm_f32_kernel<PG_GATE_NONE><<<grid, 256, 0, stream>>>(A, B, N, Din, d, x, g, out);
+    return after_launch(1);
+  }
+
+  // bf16 tensor-core path
+  if (device_cc() != 103 && device_cc() != 100) return PG_ERR_DEVICE;
+  if (Din % kBK != 0 || d % 128 != 0) return PG_ERR_UNSUPPORTED;
+  if (!aligned16(W) || (h && !aligned16(h))) return PG_ERR_ALIGN;
+  const int bn = (d % 256 == 0) ? 256 : 128;
+  GemmArgs a;
+  a.N = N;
+  a.Din = Din;
+  a.Dcols = (gate_kind == PG_GATE_CONTEXT ? (1 + M) : 1) * d;
+  a.d = d;
+  a.M = M;
+  a.g = g;
+  a.x = static_cast<const __nv_bfloat16*>(x_resid);
+  a.h = static_cast<const __nv_bfloat16*>(h);
+  a.gamma_h = gamma_h;
+  a.gamma_k = gamma_k;
+  a.v_out = static_cast<__nv_bfloat16*>(v_out);
+  a.partials = static_cast<float*>(workspace);
+  a.err_word = device_error_word();
+  if (!a.err_word) return cuda_fail(cudaGetLastError());
+  if (gate_kind == PG_GATE_CONTEXT) {
+    size_t need = 0;
+    pg_project_gate_workspace_size(N, Din, d, M, dtype, gate_kind, &need);
+    if (!workspace || workspace_bytes < need) return PG_ERR_WORKSPACE;
+    if (!aligned16(workspace) || !aligned16(gamma_h) || !aligned16(gamma_k)) return PG_ERR_ALIGN;
+  }
+  pg_status st = bn == 256 ? dispatch_tc<256>(gate_kind, e, W, a, stream)
+                           : dispatch_tc<128>(gate_kind, e, W, a, stream);
+  if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
+  const int64_t total = static_cast<int64_t>(M) * N;
+  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
+      a.partials, M, d / bn, N, d, eps, alpha_out);
+  return after_launch(1);
+}
+
+}  // extern "C"

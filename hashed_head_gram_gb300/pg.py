@@ -1,0 +1,216 @@
+"""Thin Python binding of libpg.so (include/pg.h): argument marshalling only.
+
+Every function takes torch tensors that live on the current CUDA device, passes
+their data pointers and sizes through the C ABI, and raises PgError on a non-zero
+status. All computation happens in the library's CUDA kernels; nothing here
+computes or falls back to anything. When libpg.so is missing the import fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpg.so")
+
+PG_ABI_VERSION = 1
+PG_HASH_VERSION = 1
+PG_MAX_ORDERS = 4
+PG_MAX_HEADS = 16
+PG_NO_ROW = 0xFFFFFFFF
+FLAT, ENGRAM, PAGEGRAM = 0, 1, 2
+HASH_MULXOR, HASH_TOY = 0, 1
+F32, BF16, NF4 = 0, 1, 2
+GATE_NONE, GATE_SCALAR, GATE_CONTEXT = 0, 1, 2
+
+STATUS = {0: "PG_OK", 1: "PG_ERR_NULL", 2: "PG_ERR_SHAPE", 3: "PG_ERR_DTYPE", 4: "PG_ERR_RANGE",
+          5: "PG_ERR_ALIGN", 6: "PG_ERR_UNSUPPORTED", 7: "PG_ERR_VERSION", 8: "PG_ERR_WORKSPACE",
+          9: "PG_ERR_CUDA", 10: "PG_ERR_DEVICE"}
+
+
+class PgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.pg_status_str(status).decode() if _lib is not None else ""
+        extra = f", cuda error {_lib.pg_last_cuda_error()}" if status == 9 and _lib is not None else ""
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({msg}{extra})")
+
+
+class TableDesc(ctypes.Structure):
+    _fields_ = [
+        ("abi_version", ctypes.c_uint32),
+        ("hash_version", ctypes.c_uint32),
+        ("mode", ctypes.c_int32),
+        ("hash_kind", ctypes.c_int32),
+        ("num_orders", ctypes.c_int32),
+        ("orders", ctypes.c_int32 * PG_MAX_ORDERS),
+        ("K", ctypes.c_int32),
+        ("S", ctypes.c_int32),
+        ("r", ctypes.c_int32),
+        ("pages", ctypes.c_uint32 * PG_MAX_ORDERS),
+        ("rows", (ctypes.c_uint32 * PG_MAX_HEADS) * PG_MAX_ORDERS),
+        ("row_dtype", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("hash_seed", ctypes.c_uint64),
+        ("vocab", ctypes.c_uint32),
+        ("canon_vocab", ctypes.c_uint32),
+    ]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libpg.so is not built ({_LIB_PATH}); run `python -m hashed_head_gram_gb300.build`")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, u32, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64,
+                                  ctypes.c_float, ctypes.c_size_t)
+    dp = ctypes.POINTER(TableDesc)
+    L.pg_status_str.restype = ctypes.c_char_p
+    L.pg_status_str.argtypes = [ctypes.c_int]
+    L.pg_abi_version.restype = u32
+    L.pg_last_cuda_error.restype = i32
+    L.pg_launch_count.restype = u64
+    L.pg_device_error.restype = ctypes.c_int
+    L.pg_device_error.argtypes = [ctypes.POINTER(i32), i32]
+    L.pg_table_geometry.restype = ctypes.c_int
+    L.pg_table_geometry.argtypes = [dp, ctypes.POINTER(u64), ctypes.POINTER(u32), ctypes.POINTER(u32)]
+    L.pg_canon_hash.restype = ctypes.c_int
+    L.pg_canon_hash.argtypes = [dp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
+    L.pg_gather_sign_concat.restype = ctypes.c_int
+    L.pg_gather_sign_concat.argtypes = [dp, vp, i32, i32, vp, vp, u64, vp, i32, vp, vp]
+    L.pg_project_gate_workspace_size.restype = ctypes.c_int
+    L.pg_project_gate_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    L.pg_project_gate.restype = ctypes.c_int
+    L.pg_project_gate.argtypes = [i32, i32, i32, i32, i32, vp, vp, i32, f32, vp, vp, vp, vp, f32, vp, vp,
+                                  vp, sz, vp]
+    L.pg_conv_residual.restype = ctypes.c_int
+    L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp]
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PgError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def table_desc(spec, vocab: int, canon_vocab: Optional[int] = None) -> TableDesc:
+    """Descriptor for a workloads.TableSpec (or any object with its fields)."""
+    d = TableDesc()
+    d.abi_version = PG_ABI_VERSION
+    d.hash_version = PG_HASH_VERSION
+    d.mode = spec.mode
+    d.hash_kind = spec.hash_kind
+    d.num_orders = len(spec.orders)
+    for i, n in enumerate(spec.orders):
+        d.orders[i] = n
+    d.K, d.S, d.r = spec.K, spec.S, spec.r
+    for i, p in enumerate(spec.pages):
+        d.pages[i] = p
+    for i, rr in enumerate(spec.rows):
+        for k, m in enumerate(rr):
+            d.rows[i][k] = m
+    d.row_dtype = spec.row_dtype
+    d.hash_seed = spec.hash_seed & 0xFFFFFFFFFFFFFFFF
+    d.vocab = vocab
+    d.canon_vocab = canon_vocab if canon_vocab is not None else vocab
+    return d
+
+
+def table_geometry(desc: TableDesc):
+    rows, rb, ew = ctypes.c_uint64(), ctypes.c_uint32(), ctypes.c_uint32()
+    _check(_lib.pg_table_geometry(ctypes.byref(desc), ctypes.byref(rows), ctypes.byref(rb), ctypes.byref(ew)),
+           "pg_table_geometry")
+    return rows.value, rb.value, ew.value
+
+
+def canon_hash(desc: TableDesc, tokens: torch.Tensor, rows_out: torch.Tensor,
+               canon_map: Optional[torch.Tensor] = None, canon_out: Optional[torch.Tensor] = None,
+               sign_out: Optional[torch.Tensor] = None, err_index: Optional[torch.Tensor] = None,
+               stream=None):
+    B, L = tokens.shape
+    _check(_lib.pg_canon_hash(ctypes.byref(desc), _ptr(tokens), B, L, _ptr(canon_map), _ptr(canon_out),
+                              _ptr(rows_out), _ptr(sign_out), _ptr(err_index), _stream(stream)),
+           "pg_canon_hash")
+
+
+def gather_sign_concat(desc: TableDesc, tokens: torch.Tensor, table: torch.Tensor, e_out: torch.Tensor,
+                       out_dtype: int, canon_map: Optional[torch.Tensor] = None,
+                       err_index: Optional[torch.Tensor] = None, stream=None):
+    B, L = tokens.shape
+    nbytes = table.numel() * table.element_size()
+    _check(_lib.pg_gather_sign_concat(ctypes.byref(desc), _ptr(tokens), B, L, _ptr(canon_map), _ptr(table),
+                                      nbytes, _ptr(e_out), out_dtype, _ptr(err_index), _stream(stream)),
+           "pg_gather_sign_concat")
+
+
+def workspace_size(N: int, Din: int, d: int, M: int, dtype: int, gate_kind: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.pg_project_gate_workspace_size(N, Din, d, M, dtype, gate_kind, ctypes.byref(n)),
+           "pg_project_gate_workspace_size")
+    return n.value
+
+
+def project_gate(e: torch.Tensor, W: Optional[torch.Tensor], d: int, gate_kind: int, v_out: torch.Tensor,
+                 dtype: int, M: int = 0, g: float = 0.0, x_resid: Optional[torch.Tensor] = None,
+                 h: Optional[torch.Tensor] = None, gamma_h: Optional[torch.Tensor] = None,
+                 gamma_k: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                 alpha_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 stream=None):
+    N, Din = e.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pg_project_gate(N, Din, d, M, dtype, _ptr(e), _ptr(W), gate_kind, g, _ptr(x_resid), _ptr(h),
+                                _ptr(gamma_h), _ptr(gamma_k), eps, _ptr(v_out), _ptr(alpha_out),
+                                _ptr(workspace), ws_bytes, _stream(stream)),
+           "pg_project_gate")
+
+
+def conv_residual(B: int, L: int, d: int, M: int, dtype: int, v: torch.Tensor, alpha: torch.Tensor,
+                  gamma_c: torch.Tensor, conv_w: torch.Tensor, H: torch.Tensor, dilation: int = 3,
+                  eps: float = 1e-6, stream=None):
+    ks = conv_w.shape[1]
+    _check(_lib.pg_conv_residual(B, L, d, M, dtype, _ptr(v), _ptr(alpha), _ptr(gamma_c), _ptr(conv_w), ks,
+                                 dilation, eps, _ptr(H), _stream(stream)),
+           "pg_conv_residual")
+
+
+def launch_count() -> int:
+    return int(_lib.pg_launch_count())
+
+
+def device_error(clear: bool = False) -> int:
+    code = ctypes.c_int32()
+    _check(_lib.pg_device_error(ctypes.byref(code), 1 if clear else 0), "pg_device_error")
+    return code.value
+
+
+def dtype_code(t: torch.dtype) -> int:
+    return {torch.float32: F32, torch.bfloat16: BF16}[t]
+
+
+__all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
+           "workspace_size", "project_gate", "conv_residual", "launch_count", "device_error", "lib",
+           "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
+           "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

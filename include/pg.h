@@ -1,0 +1,235 @@
+/*
+ * pg.h -- C ABI of libpg.so, the GB300 (sm_103a) hashed multi-head N-gram lookup.
+ *
+ * The lookup, per token t of a [B, L] batch (sources by page title and section):
+ *   1. canonical IDs x'_t = P[x_t]            Engram notes (arXiv 2601.07372) 3.2
+ *   2. suffix n-grams g_{t,n}, n in orders    PageGram report 2.1; Engram notes 3.2
+ *   3. multiply-XOR hash per (order, head)    Engram notes 3.2
+ *   4. row index in one of three layouts      PageGram report 2.1 (flat), 2.2 (multi-head,
+ *                                             prime subtables), 3.1 (page-local row_{n,k})
+ *   5. gather of the 2K head rows (f32, bf16 or NF4 34-byte rows, PageGram report 3.3)
+ *   6. +-1 hash sign masks, concat e_t = ||_n ||_k s_{n,k} * row  (PageGram report 2.2, 3.1)
+ *   7. projection W_V e_t (fused with M per-branch W_K, Engram notes 3.4), scalar gate
+ *      x + g e (PageGram report 3.1) or RMSNorm-sigmoid gate alpha (Engram notes 3.3)
+ *   8. causal depthwise conv + SiLU + residual into the branch states (Engram notes 3.3)
+ *
+ * Conventions for every call:
+ *  - Pointers named as device memory must point to memory of the current CUDA
+ *    device; all of it is owned by the caller. No call allocates memory that
+ *    outlives the call, and no call frees anything.
+ *  - Tensors are dense, row-major, with no padding between rows.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream): it returns after enqueueing its kernels. Host-side checks
+ *    run first; when one fails the call returns its status and enqueues nothing.
+ *  - Nothing traps or hangs on the device. Device-side waits are bounded; when one
+ *    gives up the kernel records a code readable through pg_device_error().
+ *  - Hash definition (hash_version 1; the pages name only "a multiply-XOR hash"):
+ *      mix64 = splitmix64 output function (Steele, Lea & Flood 2014),
+ *      G = 0x9E3779B97F4A7C15,
+ *      multiplier m_{f,j} = mix64(seed + G*(1 + (((kind*4 + o)*64 + k)*4 + j))) | 1,
+ *        kind 0 = page hash b_n, 1 = head hash (u_{n,k}, phi_{n,k}, flat h_n), 2 = sign,
+ *      n-gram c_j = x'_{t-j} (j < n), or 0xFFFFFFFF before the start of the sequence,
+ *      h_f = XOR_j c_j * m_{f,j} (mod 2^64), H_f = low 32 bits of h_f ^ (h_f >> 32),
+ *      flat      row = base_n + H_{1,o,0} mod R_n
+ *      Engram    row = base_{n,k} + H_{1,o,k} mod M_{n,k}   (subtables order-major, head-major)
+ *      PageGram  row = base_n + ((H_{0,o,0} mod P_n) K + k) S + (H_{1,o,k} mod S)
+ *      sign word q of (o,k) = mix64(h_{2,o,k} + G*(q+1)); element i of the head is
+ *        negated iff bit i%64 of word i/64 is set (flat: k = 0 and i < d).
+ */
+#ifndef PG_H_
+#define PG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without including the CUDA headers. */
+typedef struct CUstream_st* pg_stream_t;
+
+#define PG_ABI_VERSION 1u
+#define PG_HASH_VERSION 1u
+#define PG_MAX_ORDERS 4
+#define PG_MAX_HEADS 16
+#define PG_NO_ROW 0xFFFFFFFFu     /* rows_out entry for "no row" (toy hash at t = 0) */
+
+typedef enum {
+  PG_OK = 0,
+  PG_ERR_NULL = 1,         /* a required pointer is NULL */
+  PG_ERR_SHAPE = 2,        /* a size is out of range or inconsistent */
+  PG_ERR_DTYPE = 3,        /* unsupported dtype or dtype combination */
+  PG_ERR_RANGE = 4,        /* table smaller than its descriptor needs, or >= 2^32 rows */
+  PG_ERR_ALIGN = 5,        /* a pointer is not aligned as the call requires */
+  PG_ERR_UNSUPPORTED = 6,  /* well-formed request this build does not implement */
+  PG_ERR_VERSION = 7,      /* descriptor abi_version / hash_version not supported */
+  PG_ERR_WORKSPACE = 8,    /* workspace missing or smaller than the size query says */
+  PG_ERR_CUDA = 9,         /* a CUDA runtime call failed; see pg_last_cuda_error() */
+  PG_ERR_DEVICE = 10       /* current device cannot run the kernel (needs sm_103a) */
+} pg_status;
+
+enum { PG_FLAT = 0, PG_ENGRAM = 1, PG_PAGEGRAM = 2 };
+enum { PG_HASH_MULXOR = 0, PG_HASH_TOY = 1 };
+enum { PG_F32 = 0, PG_BF16 = 1, PG_NF4 = 2 };
+enum { PG_GATE_NONE = 0, PG_GATE_SCALAR = 1, PG_GATE_CONTEXT = 2 };
+
+/*
+ * Table descriptor (plain data; fill every field).
+ *  abi_version, hash_version  PG_ABI_VERSION, PG_HASH_VERSION
+ *  mode        PG_FLAT | PG_ENGRAM | PG_PAGEGRAM
+ *  hash_kind   PG_HASH_MULXOR, or PG_HASH_TOY: the Engram explainer's teaching bucket
+ *              (3a + b) mod m ("Hash 冲突是什么样？"), flat mode, one order n = 2,
+ *              m = rows[0][0]; pg_canon_hash only.
+ *  num_orders, orders[]  n-gram orders, strictly increasing, each in [1, 4]
+ *  K           heads per order (multi-head modes), 1..16; flat: 1
+ *  S           PageGram slots per head per page (>= 1); ignored otherwise
+ *  r           head width (flat: the row width, = d)
+ *  pages[o]    PageGram P_n for order index o
+ *  rows[o][k]  Engram M_{n,k} for order index o, head k; flat R_n in rows[o][0]
+ *  row_dtype   PG_F32 | PG_BF16 | PG_NF4 (NF4: r = 64, 34-byte rows: bytes 0..31
+ *              hold codes, element 2i in the low nibble of byte i, 2i+1 in the high
+ *              nibble; bytes 32..33 an fp16 scale, little-endian)
+ *  hash_seed   seeds the hash family
+ *  vocab       V: token IDs must lie in [0, V)
+ *  canon_vocab V' (informational; the canonical map's values are used as given)
+ */
+typedef struct {
+  uint32_t abi_version;
+  uint32_t hash_version;
+  int32_t mode;
+  int32_t hash_kind;
+  int32_t num_orders;
+  int32_t orders[PG_MAX_ORDERS];
+  int32_t K;
+  int32_t S;
+  int32_t r;
+  uint32_t pages[PG_MAX_ORDERS];
+  uint32_t rows[PG_MAX_ORDERS][PG_MAX_HEADS];
+  int32_t row_dtype;
+  int32_t reserved;
+  uint64_t hash_seed;
+  uint32_t vocab;
+  uint32_t canon_vocab;
+} pg_table_desc;
+
+/* Message for a status code (static storage). */
+const char* pg_status_str(pg_status status);
+
+/* PG_ABI_VERSION of the loaded library. */
+uint32_t pg_abi_version(void);
+
+/* Last CUDA error code a pg_* call on this host thread met (0 if none). */
+int32_t pg_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pg_launch_count(void);
+
+/*
+ * Device-side error word of the current device: 0, or the OR of codes of bounded
+ * waits that gave up (1 = TMA producer, 2 = MMA issuer, 4 = epilogue). Synchronizes
+ * the device. With clear != 0 the word is reset to 0.
+ */
+pg_status pg_device_error(int32_t* code, int32_t clear);
+
+/*
+ * Table geometry of a descriptor: number of stored rows (the table's first
+ * dimension), bytes per row, and the width of e_t (O*K*r, or r for flat).
+ * Any out pointer may be NULL. Validates the descriptor (PG_ERR_VERSION,
+ * PG_ERR_SHAPE, PG_ERR_DTYPE, PG_ERR_RANGE).
+ */
+pg_status pg_table_geometry(const pg_table_desc* desc, uint64_t* rows, uint32_t* row_bytes,
+                            uint32_t* e_width);
+
+/*
+ * pg_canon_hash -- steps 1-4 plus sign words, written out (the addresses depend on
+ * token IDs only, so they can be computed before the forward pass: PageGram report
+ * 3.3 "prefetch"; Engram notes 3.5).
+ *  tokens     device int32 [B, L]
+ *  canon_map  device uint32 [vocab], or NULL for the identity map
+ *  canon_out  device uint32 [B*L] (x'_t), or NULL
+ *  rows_out   device uint32 [B*L, O, H], H = K (flat and toy: 1)
+ *  sign_out   device uint64 [B*L, O, H, ceil(r/64)], or NULL (toy: all zero)
+ *  err_index  device int32 [1], or NULL: set to the smallest flat index of a token
+ *             outside [0, vocab) that the call read, else -1 (written on `stream`).
+ *             Such a token is read as ID 0 and the call continues.
+ * B, L >= 0 (B*L < 2^31); B*L == 0 enqueues nothing.
+ */
+pg_status pg_canon_hash(const pg_table_desc* desc, const int32_t* tokens, int32_t B, int32_t L,
+                        const uint32_t* canon_map, uint32_t* canon_out, uint32_t* rows_out,
+                        uint64_t* sign_out, int32_t* err_index, pg_stream_t stream);
+
+/*
+ * pg_gather_sign_concat -- steps 1-6 fused: hashes and row indices are computed in
+ * registers, the rows gathered with 16-byte loads (PageGram: one warp serves a
+ * token's K*S page blocks, one contiguous segment per order), NF4 rows dequantised
+ * in registers (level[code] * float(scale), one fp32 multiply, round-to-nearest-even),
+ * signs applied and the heads written concatenated.
+ *  table      device memory, table_bytes long (>= rows * row_bytes), 16-byte aligned
+ *  e_out      device [B*L, e_width] of out_dtype; multi-head column block
+ *             (o*K + k)*r holds head (o, k); flat: e = s_0*T[row_0] + s_1*T[row_1] + ...
+ *             summed in fp32 in order of increasing n, then rounded to out_dtype
+ *  out_dtype  f32 rows -> PG_F32; bf16 rows -> PG_BF16 or PG_F32; NF4 -> PG_BF16 or PG_F32
+ *  err_index  as in pg_canon_hash
+ * PG_HASH_TOY is not accepted here (PG_ERR_UNSUPPORTED).
+ */
+pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens, int32_t B,
+                                int32_t L, const uint32_t* canon_map, const void* table,
+                                uint64_t table_bytes, void* e_out, int32_t out_dtype,
+                                int32_t* err_index, pg_stream_t stream);
+
+/*
+ * Workspace bytes pg_project_gate needs for these arguments (0 when none).
+ */
+pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int32_t M,
+                                         int32_t dtype, int32_t gate_kind, size_t* bytes);
+
+/*
+ * pg_project_gate -- step 7 (PageGram report 2.2 and 3.1; Engram notes 3.3, 3.4).
+ *  e      device [N, Din] (dtype)
+ *  W      device [(1+M)*d, Din] (dtype): W_V rows, then W_K^(1..M) rows. May be NULL
+ *         with Din == d and gate NONE or SCALAR: identity (a flat table's e_t is already
+ *         d wide, PageGram report 2.1).
+ *  gate_kind
+ *    PG_GATE_NONE     v_out[N, d] = e W_V^T                       (M must be 0)
+ *    PG_GATE_SCALAR   v_out[N, d] = x_resid + g * (e W_V^T)       (x_resid [N, d]; M = 0)
+ *    PG_GATE_CONTEXT  v_out[N, d] = e W_V^T and, for each branch m,
+ *                     alpha_out[m, t] = sigmoid(RMSNorm(h^(m)_t) . RMSNorm(W_K^(m) e_t) / sqrt(d))
+ *                     with RMSNorm(z) = z / sqrt(mean(z^2) + eps) * gamma (gamma_h for h,
+ *                     gamma_k for k; fp32 [d]); h device [M, N, d]; alpha_out fp32 [M, N]
+ *  dtype  PG_F32: fp32 SIMT FFMA path (gates NONE and SCALAR).
+ *         PG_BF16: tcgen05 tensor-core path, fp32 accumulation, bf16 results; requires
+ *         Din % 64 == 0, d % 128 == 0, 16-byte aligned e and W. Identity (W == NULL)
+ *         works for both dtypes.
+ *  workspace  device, >= pg_project_gate_workspace_size() bytes, 16-byte aligned
+ *             (only the context gate uses it; its contents are scratch).
+ * N == 0 enqueues nothing. x_resid / h / v_out must not overlap e or W.
+ */
+pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t dtype,
+                          const void* e, const void* W, int32_t gate_kind, float g,
+                          const void* x_resid, const void* h, const float* gamma_h,
+                          const float* gamma_k, float eps, void* v_out, float* alpha_out,
+                          void* workspace, size_t workspace_bytes, pg_stream_t stream);
+
+/*
+ * pg_conv_residual -- step 8 (Engram notes 3.3 and 3.1, explainer's causal conv):
+ * for each branch m and position t of each sequence,
+ *   u = alpha[m, t] * v_t;  z = RMSNorm(u) with gamma_c;
+ *   c_t = sum_{j < kernel_size} conv_w[:, j] * z_{t - j*dilation}   (zero before t = 0)
+ *   H[m, t] <- H[m, t] + SiLU(c_t) + u
+ *  v      device [B*L, d] (dtype), alpha device fp32 [M, B*L]
+ *  gamma_c, conv_w  device fp32 [d], [d, kernel_size] (shared by the branches)
+ *  H      device [M, B*L, d] (dtype), updated in place
+ *  dtype PG_BF16 or PG_F32; d % 8 == 0, d <= 8192; kernel_size in [1, 4];
+ *  dilation in [1, 8]; v and H 16-byte aligned.
+ */
+pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M, int32_t dtype,
+                           const void* v, const float* alpha, const float* gamma_c,
+                           const float* conv_w, int32_t kernel_size, int32_t dilation,
+                           float eps, void* H, pg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PG_H_ */

@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: libpg.so builds, loads, exports every function that
+include/pg.h declares, and its host-side checks answer before any CUDA work."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from hashed_head_gram_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pg.h")
+
+
+@pytest.fixture(scope="module")
+def pg():
+    from hashed_head_gram_gb300.build import build
+    build()
+    from hashed_head_gram_gb300 import pg as mod
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_lookup_calls():
+    names = declared_functions()
+    for n in ("pg_canon_hash", "pg_gather_sign_concat", "pg_project_gate", "pg_conv_residual"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(pg):
+    lib_path = os.path.join(ROOT, "hashed_head_gram_gb300", "libpg.so")
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (pg_[a-z0-9_]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert getattr(pg.lib(), n) is not None
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "pg.h"\nint main(void){pg_table_desc d; (void)d; return (int)sizeof(d) > 0 ? 0 : 1;}\n')
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I" + os.path.join(ROOT, "include"),
+                           "-c", str(src), "-o", str(tmp_path / "t.o")])
+
+
+def test_descriptor_layout_matches_the_header(pg, tmp_path):
+    src = tmp_path / "sz.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "pg.h"\n'
+                   'int main(void){printf("%zu %zu %zu %zu\\n", sizeof(pg_table_desc),'
+                   ' offsetof(pg_table_desc, hash_seed), offsetof(pg_table_desc, rows),'
+                   ' offsetof(pg_table_desc, canon_vocab)); return 0;}\n')
+    exe = tmp_path / "sz"
+    subprocess.check_call(["gcc", "-I" + os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    size, seed_off, rows_off, cv_off = map(int, subprocess.check_output([str(exe)]).split())
+    T = pg.TableDesc
+    assert ctypes.sizeof(T) == size and T.hash_seed.offset == seed_off
+    assert T.rows.offset == rows_off and T.canon_vocab.offset == cv_off
+
+
+def test_status_strings_and_version(pg):
+    L = pg.lib()
+    assert L.pg_abi_version() == 1
+    for s in range(11):
+        assert L.pg_status_str(s)
+    assert L.pg_status_str(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_geometry_of_every_workload(pg, cfg):
+    w = W.make_workload(cfg)
+    for spec in w.tables:
+        rows, rb, ew = pg.table_geometry(pg.table_desc(spec, w.vocab, w.canon_vocab))
+        assert (rows, rb, ew) == (spec.table_rows, spec.row_bytes, spec.e_width)
+
+
+def test_descriptor_validation(pg):
+    spec = W.make_workload(2).tables[0]
+    cases = []
+    d = pg.table_desc(spec, 50304); d.abi_version = 9; cases.append((d, 7))
+    d = pg.table_desc(spec, 50304); d.orders[1] = 2; cases.append((d, 2))           # not increasing
+    d = pg.table_desc(spec, 50304); d.K = 17; cases.append((d, 2))
+    d = pg.table_desc(spec, 50304); d.pages[0] = 0; cases.append((d, 2))
+    d = pg.table_desc(spec, 50304); d.row_dtype = 7; cases.append((d, 3))
+    d = pg.table_desc(spec, 50304); d.row_dtype = 2; d.r = 80; cases.append((d, 3))  # NF4 needs r = 64
+    d = pg.table_desc(spec, 50304); d.pages[0] = 0xFFFFFFF; cases.append((d, 4))     # >= 2^32 rows
+    d = pg.table_desc(spec, 50304); d.vocab = 0; cases.append((d, 2))
+    for desc, want in cases:
+        with pytest.raises(pg.PgError) as ex:
+            pg.table_geometry(desc)
+        assert ex.value.status == want
+
+
+def test_calls_reject_null_pointers_on_the_host(pg):
+    L = pg.lib()
+    spec = W.make_workload(2).tables[0]
+    d = pg.table_desc(spec, 50304)
+    assert L.pg_gather_sign_concat(ctypes.byref(d), None, 2, 3, None, None, 0, None, 1, None, None) == 1
+    assert L.pg_canon_hash(ctypes.byref(d), None, 2, 3, None, None, None, None, None, None) == 1
+    assert L.pg_canon_hash(ctypes.byref(d), None, -1, 3, None, None, None, None, None, None) == 2
+    assert L.pg_project_gate(4, 64, 128, 0, 1, None, None, 0, 0.0, None, None, None, None, 1e-6, None, None,
+                             None, 0, None) == 1
+    assert L.pg_project_gate(4, 64, 128, 1, 1, None, None, 0, 0.0, None, None, None, None, 1e-6, None, None,
+                             None, 0, None) == 2                                   # M with gate NONE
+    assert L.pg_conv_residual(1, 4, 12, 1, 1, None, None, None, None, 4, 3, 1e-6, None, None) == 2  # d % 8
+    assert L.pg_conv_residual(1, 4, 16, 1, 1, None, None, None, None, 4, 3, 1e-6, None, None) == 1
+
+
+def test_workspace_size_query(pg):
+    assert pg.workspace_size(32768, 1280, 2560, 4, pg.BF16, pg.GATE_CONTEXT) == 4 * 10 * 3 * 32768 * 4
+    assert pg.workspace_size(65536, 1024, 768, 0, pg.BF16, pg.GATE_SCALAR) == 0

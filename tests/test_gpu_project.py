@@ -1,0 +1,170 @@
+"""GPU parity of pg_project_gate (SIMT fp32 and tcgen05 bf16 paths) and
+pg_conv_residual against the fp64 oracle, within the stated rel-L2 tolerances."""
+import numpy as np
+import pytest
+import torch
+
+from hashed_head_gram_gb300 import workloads as W
+from oracle import dense
+from tests._helpers import BF16_TOL, F32_TOL, rel_l2, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _pg():
+    from hashed_head_gram_gb300 import pg
+    return pg
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+def _e_bf16(N, Din, seed):
+    # e_t-like values: int8/64 with random signs (exact in bf16)
+    return (torch.randint(-128, 128, (N, Din), generator=_gen(seed)).float() / 64).to(torch.bfloat16)
+
+
+def test_simt_fp32_projection_config1(cuda):
+    pg = _pg()
+    N, Din, d = 4096, 1024, 256                   # the tiny workload's full size
+    e = torch.randint(-128, 128, (N, Din), generator=_gen(1)).float() / 64
+    Wv = torch.randn(d, Din, generator=_gen(2)) * 0.02
+    v = torch.empty(N, d, device=cuda)
+    pg.project_gate(e.to(cuda), Wv.to(cuda), d, pg.GATE_NONE, v, pg.F32)
+    ref = dense.project(e.double().numpy(), Wv.double().numpy())
+    assert rel_l2(to_f64(v), ref) <= F32_TOL
+    x = torch.randn(N, d, generator=_gen(3))
+    out = torch.empty(N, d, device=cuda)
+    pg.project_gate(e.to(cuda), Wv.to(cuda), d, pg.GATE_SCALAR, out, pg.F32, g=0.5, x_resid=x.to(cuda))
+    assert rel_l2(to_f64(out), dense.scalar_gate(x.double().numpy(), ref, 0.5)) <= F32_TOL
+
+
+@pytest.mark.parametrize("N,Din,d", [(429, 1024, 768), (128, 64, 128), (1000, 1280, 256), (77, 192, 384)])
+def test_tcgen05_projection(cuda, N, Din, d):
+    pg = _pg()
+    e = _e_bf16(N, Din, 4)
+    Wv = (torch.randn(d, Din, generator=_gen(5)) * 0.02).to(torch.bfloat16)
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    pg.project_gate(e.to(cuda), Wv.to(cuda), d, pg.GATE_NONE, v, pg.BF16)
+    torch.cuda.synchronize()
+    assert pg.device_error() == 0
+    ref = dense.project(e.double().numpy(), Wv.double().numpy())
+    err = rel_l2(to_f64(v), ref)
+    assert err <= BF16_TOL
+    assert err <= 4e-3        # bf16 output rounding dominates; fp32 accumulation
+    x = torch.randn(N, d, generator=_gen(6)).to(torch.bfloat16)
+    out = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    pg.project_gate(e.to(cuda), Wv.to(cuda), d, pg.GATE_SCALAR, out, pg.BF16, g=0.5, x_resid=x.to(cuda))
+    torch.cuda.synchronize()
+    assert rel_l2(to_f64(out), dense.scalar_gate(x.double().numpy(), ref, 0.5)) <= BF16_TOL
+
+
+@pytest.mark.parametrize("N,Din,d,M", [(300, 1280, 2560, 4), (129, 128, 256, 2), (64, 64, 384, 1)])
+def test_tcgen05_context_gate(cuda, N, Din, d, M):
+    pg = _pg()
+    e = _e_bf16(N, Din, 7)
+    Wm = (torch.randn((1 + M) * d, Din, generator=_gen(8)) * 0.02).to(torch.bfloat16)
+    h = torch.randn(M, N, d, generator=_gen(9)).to(torch.bfloat16)
+    gh = torch.rand(d, generator=_gen(10)) + 0.5
+    gk = torch.rand(d, generator=_gen(11)) + 0.5
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    alpha = torch.empty(M, N, device=cuda)
+    ws = torch.empty(pg.workspace_size(N, Din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4, device=cuda)
+    pg.project_gate(e.to(cuda), Wm.to(cuda), d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=h.to(cuda),
+                    gamma_h=gh.to(cuda), gamma_k=gk.to(cuda), eps=1e-6, alpha_out=alpha, workspace=ws)
+    torch.cuda.synchronize()
+    assert pg.device_error() == 0
+    v_ref, a_ref = dense.engram_gate(e.double().numpy(), Wm.double().numpy(), h.double().numpy(),
+                                     gh.double().numpy(), gk.double().numpy(), 1e-6, M)
+    assert rel_l2(to_f64(v), v_ref) <= BF16_TOL
+    assert rel_l2(to_f64(alpha), a_ref) <= BF16_TOL
+    assert np.abs(to_f64(alpha) - a_ref).max() < 1e-3
+
+
+def test_context_gate_rejects_small_workspace(cuda):
+    pg = _pg()
+    N, Din, d, M = 64, 64, 256, 2
+    e = torch.zeros(N, Din, dtype=torch.bfloat16, device=cuda)
+    Wm = torch.zeros((1 + M) * d, Din, dtype=torch.bfloat16, device=cuda)
+    h = torch.zeros(M, N, d, dtype=torch.bfloat16, device=cuda)
+    g1 = torch.ones(d, device=cuda)
+    need = pg.workspace_size(N, Din, d, M, pg.BF16, pg.GATE_CONTEXT)
+    ws = torch.empty(need // 4 - 1, device=cuda)
+    with pytest.raises(pg.PgError) as ex:
+        pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, torch.empty(N, d, dtype=torch.bfloat16, device=cuda),
+                        pg.BF16, M=M, h=h, gamma_h=g1, gamma_k=g1, alpha_out=torch.empty(M, N, device=cuda),
+                        workspace=ws)
+    assert ex.value.status == 8
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_identity_projection_for_flat_tables(cuda, dtype):
+    pg = _pg()
+    N, d = 333, 768
+    e = (torch.randint(-128, 128, (N, d), generator=_gen(12)).float() / 64).to(dtype)
+    x = torch.randn(N, d, generator=_gen(13)).to(dtype)
+    out = torch.empty(N, d, dtype=dtype, device=cuda)
+    pg.project_gate(e.to(cuda), None, d, pg.GATE_SCALAR, out, pg.dtype_code(dtype), g=0.5, x_resid=x.to(cuda))
+    ref = dense.scalar_gate(x.double().numpy(), e.double().numpy(), 0.5)
+    assert rel_l2(to_f64(out), ref) <= (BF16_TOL if dtype == torch.bfloat16 else F32_TOL)
+
+
+def _conv_case(B, L, d, M, seed, zero_w=False, dtype=torch.bfloat16):
+    g = _gen(seed)
+    v = torch.randn(B * L, d, generator=g).to(dtype)
+    alpha = torch.rand(M, B * L, generator=g)
+    gc = torch.rand(d, generator=g) + 0.5
+    w = torch.zeros(d, 4) if zero_w else torch.randn(d, 4, generator=g) * 0.25
+    H = torch.randn(M, B * L, d, generator=g).to(dtype)
+    return v, alpha, gc, w, H
+
+
+@pytest.mark.parametrize("B,L,d,M,dtype", [(2, 75, 2560, 4, torch.bfloat16), (3, 16, 64, 2, torch.bfloat16),
+                                           (1, 40, 256, 3, torch.float32), (2, 9, 512, 1, torch.bfloat16)])
+def test_conv_residual(cuda, B, L, d, M, dtype):
+    pg = _pg()
+    v, alpha, gc, w, H = _conv_case(B, L, d, M, 14, dtype=dtype)
+    Hd = H.to(cuda)
+    pg.conv_residual(B, L, d, M, pg.dtype_code(dtype), v.to(cuda), alpha.to(cuda), gc.to(cuda), w.to(cuda), Hd,
+                     dilation=3, eps=1e-6)
+    ref = dense.conv_residual(v.double().numpy().reshape(B, L, d), alpha.double().numpy().reshape(M, B, L),
+                              gc.double().numpy(), w.double().numpy(), 3, 1e-6,
+                              H.double().numpy().reshape(M, B, L, d))
+    tol = BF16_TOL if dtype == torch.bfloat16 else F32_TOL * 10
+    assert rel_l2(to_f64(Hd).reshape(M, B, L, d), ref) <= tol
+    # the update itself (H_new - H) is also close: a stricter view of the same output
+    upd = to_f64(Hd).reshape(M, B, L, d) - H.double().numpy().reshape(M, B, L, d)
+    assert rel_l2(upd, ref - H.double().numpy().reshape(M, B, L, d)) <= (5e-2 if dtype == torch.bfloat16 else 1e-4)
+
+
+def test_zero_table_leaves_H_bit_identical(cuda):
+    # e = 0 -> v = 0, alpha = 1/2 exactly, Y = 0: H is unchanged bit for bit
+    # (PageGram report appendix D/E check 3).
+    pg = _pg()
+    N, Din, d, M, B, L = 96, 128, 256, 2, 2, 48
+    e = torch.zeros(N, Din, dtype=torch.bfloat16, device=cuda)
+    Wm = (torch.randn((1 + M) * d, Din, generator=_gen(15)) * 0.02).to(torch.bfloat16).to(cuda)
+    H = torch.randn(M, N, d, generator=_gen(16)).to(torch.bfloat16).to(cuda)
+    H0 = H.clone()
+    g1 = torch.ones(d, device=cuda)
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    alpha = torch.empty(M, N, device=cuda)
+    ws = torch.empty(pg.workspace_size(N, Din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4, device=cuda)
+    pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=H, gamma_h=g1, gamma_k=g1, alpha_out=alpha,
+                    workspace=ws)
+    pg.conv_residual(B, L, d, M, pg.BF16, v, alpha, g1, torch.randn(d, 4, device=cuda), H)
+    torch.cuda.synchronize()
+    assert (v.float() == 0).all() and (alpha == 0.5).all()
+    assert torch.equal(H.view(torch.int16), H0.view(torch.int16))
+
+
+def test_zero_conv_is_the_identity_path(cuda):
+    pg = _pg()
+    B, L, d, M = 2, 30, 128, 2
+    v, alpha, gc, w, H = _conv_case(B, L, d, M, 17, zero_w=True, dtype=torch.float32)
+    Hd = torch.zeros_like(H).to(cuda)
+    pg.conv_residual(B, L, d, M, pg.F32, v.to(cuda), alpha.to(cuda), gc.to(cuda), w.to(cuda), Hd)
+    ref = alpha.double().numpy()[..., None] * v.double().numpy()[None]
+    assert np.array_equal(to_f64(Hd), (alpha[..., None] * v[None]).double().numpy())  # fp32 u = alpha * v
+    assert rel_l2(to_f64(Hd), ref) <= 1e-7
