@@ -1,0 +1,521 @@
+#!/usr/bin/env python3
+"""Benchmark of the hashed multi-head N-gram lookup on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--config C]
+
+A step is one pass of the whole lookup over one batch of the workload (default:
+the PageGram 200M-parameter bf16 table, 64 x 1024 Zipf(1.1) tokens): canonical IDs,
+n-grams, hashes and rows, gather + sign + concat (pg_gather_sign_concat), then the
+W_V projection with the scalar gate x + g v (pg_project_gate, tcgen05). With
+--config 5 the step is the Engram-27B-shaped module (gather, fused W_V + 4 W_K with
+the RMSNorm-sigmoid gate, causal conv + residual).
+
+Rank 0 prints one JSON line. Under torchrun each rank runs its own batch (seeded by
+rank; no collective on the data path) and the timing is the max over ranks.
+--impl reference times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "N-gram memory lookup tokens/s (1 GB300) and % of HBM / tensor roofline"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- rank / sharding helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / seconds_max
+
+
+# ---------------------------------------------------------------- peaks and clocks
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed loop runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        load = [r for r in rows if r[2] > 0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i, flag in enumerate(r[3][1:5]) if flag.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(load)}
+
+
+# ---------------------------------------------------------------- the GPU path
+
+class Pipeline:
+    """Resident inputs and outputs of one workload; step() launches the whole path."""
+
+    def __init__(self, cfg: int, dev, rank: int):
+        import numpy as np
+        import torch
+
+        from hashed_head_gram_gb300 import pg, workloads as W
+
+        self.pg, self.W, self.torch, self.np = pg, W, torch, np
+        self.cfg = cfg
+        w = self.w = W.make_workload(cfg)
+        spec = self.spec = w.tables[0]
+        self.desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+        self.dev = dev
+        tokens = W.make_tokens(w, rank=rank)
+        self.tokens_host = torch.from_numpy(tokens).pin_memory()
+        self.tokens = self.tokens_host.to(dev)
+        cmap = W.make_canon_map(w)
+        self.cmap = None if cmap is None else torch.from_numpy(cmap.view(np.int32)).to(dev)
+        self.table = W.make_table(w, spec, dev)
+        dn = self.dn = W.make_dense(w, dev)
+        self.N, self.din, self.d = w.N, spec.e_width, w.d
+        self.e = torch.empty(self.N, self.din, dtype=torch.bfloat16, device=dev)
+        if w.gate == W.GATE_SCALAR:
+            self.out = torch.empty(self.N, self.d, dtype=torch.bfloat16, device=dev)
+            self.x_host = dn["x"].cpu().pin_memory()
+        else:
+            self.v = torch.empty(self.N, self.d, dtype=torch.bfloat16, device=dev)
+            self.alpha = torch.empty(w.M, self.N, device=dev)
+            nws = pg.workspace_size(self.N, self.din, self.d, w.M, pg.BF16, pg.GATE_CONTEXT)
+            self.ws = torch.empty(nws // 4, device=dev)
+            self.H0 = dn["H"].clone()
+        self.out_host = torch.empty(self.N, self.d, dtype=torch.bfloat16).pin_memory()
+
+    def gather(self):
+        self.pg.gather_sign_concat(self.desc, self.tokens, self.table, self.e, self.pg.BF16, canon_map=self.cmap)
+
+    def project(self):
+        pg, w, dn = self.pg, self.w, self.dn
+        if w.gate == self.W.GATE_SCALAR:
+            pg.project_gate(self.e, dn["W"], self.d, pg.GATE_SCALAR, self.out, pg.BF16, g=w.g, x_resid=dn["x"])
+        else:
+            pg.project_gate(self.e, dn["W"], self.d, pg.GATE_CONTEXT, self.v, pg.BF16, M=w.M, h=dn["H"],
+                            gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=self.alpha,
+                            workspace=self.ws)
+
+    def conv(self):
+        pg, w, dn = self.pg, self.w, self.dn
+        pg.conv_residual(w.B, w.L, self.d, w.M, pg.BF16, self.v, self.alpha, dn["gamma_c"], dn["conv_w"], dn["H"],
+                         dilation=w.dilation, eps=w.eps)
+
+    def stages(self):
+        st = [("gather_sign_concat", self.gather), ("project_gate", self.project)]
+        if self.w.gate == self.W.GATE_CONTEXT:
+            st.append(("conv_residual", self.conv))
+        return st
+
+    def result_tensor(self):
+        return self.out if self.w.gate == self.W.GATE_SCALAR else self.dn["H"]
+
+    # algorithmic work per launch ("Roofline")
+    def algorithmic(self, name):
+        N, din, d, w = self.N, self.din, self.d, self.w
+        if name == "gather_sign_concat":
+            # 2K rows x row bytes (sector-rounded for NF4) + token ID + e_t write, per token
+            rb = self.spec.row_bytes if self.spec.row_dtype != self.W.DT_NF4 else 64
+            per = len(self.spec.orders) * self.spec.K * rb + 4 + din * 2
+            return "hbm", per * N
+        if name == "project_gate":
+            cols = d * (1 + w.M)
+            return "tensor", 2.0 * N * din * cols
+        # conv: read v, read + write H for every branch
+        return "hbm", N * (d * 2 + 2 * w.M * d * 2)
+
+
+def compulsory_gather_bytes(p) -> float:
+    """Distinct 32-byte table sectors the batch touches (rows from pg_canon_hash on
+    the GPU) + token IDs + the e_t write: a lower bound on the gather's DRAM traffic."""
+    torch, pg = p.torch, p.pg
+    rows = torch.empty(p.N, len(p.spec.orders), p.spec.K, dtype=torch.int32, device=p.dev)
+    pg.canon_hash(p.desc, p.tokens, rows, canon_map=p.cmap)
+    r = rows.view(-1).to(torch.int64) & 0xFFFFFFFF
+    rb = p.spec.row_bytes
+    first = (r * rb) // 32
+    last = (r * rb + rb - 1) // 32
+    span = torch.arange((rb + 31) // 32 + 1, device=p.dev)
+    cand = first.unsqueeze(1) + span
+    cand = cand[cand <= last.unsqueeze(1)]
+    distinct = int(torch.unique(cand).numel())
+    return distinct * 32.0 + p.N * 4 + p.N * p.din * 2
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def run_gpu(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from hashed_head_gram_gb300 import pg
+
+    p = Pipeline(args.config, dev, rank)
+    stream = torch.cuda.current_stream()
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stages = p.stages()
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        for _, fn in stages:
+            fn()
+        flush_l2(flush)
+    torch.cuda.synchronize()
+    if p.w.gate != p.W.GATE_SCALAR:
+        p.dn["H"].copy_(p.H0)
+    torch.cuda.synchronize()
+
+    # ---- device-timed loop: events around every stage of every step, L2 flushed between steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    launches0 = pg.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            for j, (_, fn) in enumerate(stages):
+                fn()
+                ev[i][j + 1].record(stream)
+            flush_l2(flush)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    launches = pg.launch_count() - launches0
+    stage_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(len(stages))]
+    step_ms = [sum(stage_ms[j][i] for j in range(len(stages))) for i in range(args.steps)]
+    total_s = reduce_max(sum(step_ms) / 1e3, world)
+    value = whole_job_rate(p.N * args.steps, world, total_s)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e_ms = []
+    h2d = p.tokens_host.numel() * 4 + (p.x_host.numel() * 2 if hasattr(p, "x_host") else 0)
+    res = p.result_tensor()
+    res_host = p.out_host if res.numel() == p.out_host.numel() else torch.empty_like(res, device="cpu").pin_memory()
+    barrier(world)
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 200))
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        e0[i].record(stream)
+        p.tokens.copy_(p.tokens_host, non_blocking=True)
+        if hasattr(p, "x_host"):
+            p.dn["x"].copy_(p.x_host, non_blocking=True)
+        for _, fn in stages:
+            fn()
+        res_host.copy_(res, non_blocking=True)
+        e1[i].record(stream)
+        flush_l2(flush)
+    torch.cuda.synchronize()
+    e2e_ms = [e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)]
+    e2e_s = reduce_max(sum(e2e_ms) / 1e3, world)
+    e2e_value = whole_job_rate(p.N * e2e_steps, world, e2e_s)
+    d2h = res.numel() * res.element_size()
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    means = {name: statistics.mean(stage_ms[j]) for j, (name, _) in enumerate(stages)}
+    dom = max(means, key=means.get)
+    bound, work = p.algorithmic(dom)
+    dur_s = means[dom] / 1e3
+    traffic = traffic_of(args.config, dom)
+    if bound == "hbm":
+        achieved, peak, unit = work / dur_s / 1e9, float(peaks["hbm_gbs"]), "GB/s"
+    else:
+        achieved, peak, unit = work / dur_s / 1e12, float(peaks["bf16_tflops"]), "TFLOP/s"
+    kernels = {}
+    for j, (name, _) in enumerate(stages):
+        b, wk = p.algorithmic(name)
+        ms = means[name]
+        if b == "hbm":
+            kernels[name] = {"ms": round(ms, 5), "GB/s": round(wk / (ms / 1e3) / 1e9, 1),
+                             "frac_hbm": round(wk / (ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
+        else:
+            kernels[name] = {"ms": round(ms, 5), "TFLOP/s": round(wk / (ms / 1e3) / 1e12, 1),
+                             "frac_tensor": round(wk / (ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]), 4)}
+    comp = compulsory_gather_bytes(p)
+    g_ms = means["gather_sign_concat"]
+    kernels["gather_sign_concat"]["compulsory_bytes"] = comp
+    kernels["gather_sign_concat"]["frac_hbm_compulsory"] = round(comp / (g_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(step_ms), 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded Zipf token IDs, int8/64 table values, N(0,0.02) weights, N(0,1) states",
+            "config": workload_config(p.w, world),
+            "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})"},
+            "kernels": kernels,
+            "clocks": clocks,
+            "wall_s_timed_loop": round(t_wall, 4),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ncu-measured DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum),
+# keyed by (workload, stage), with the sha256 prefix of the kernel's source file at the
+# time of the capture; reported only while the source is unchanged (profiles/ holds the
+# captures).
+TRAFFIC = {
+    (2, "gather_sign_concat"): ("pg_lookup.cu", "7f257e0f89cf21f7", 185.324800e6),
+    (2, "project_gate"): ("pg_project.cu", "3df1f560fb1667a6", 305.980160e6),
+}
+
+
+def traffic_of(cfg, stage):
+    import hashlib
+    entry = TRAFFIC.get((cfg, stage))
+    if entry is None:
+        return None
+    src, sha, nbytes = entry
+    path = os.path.join(ROOT, "hashed_head_gram_gb300", "csrc", src)
+    try:
+        with open(path, "rb") as f:
+            now = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return nbytes if now == sha else None
+
+
+def workload_config(w, world):
+    t = w.tables[0]
+    desc = {2: "PageGram 200M-parameter bf16 table: P_n = 48,823 / 48,821 pages, K=8, S=4, r=64; "
+               "Zipf(1.1) IDs over 50,304; W_V 1024->768; scalar gate g=0.5",
+            5: "Engram-27B-shaped module: 16 prime subtables ~2.2266M rows, r=80, bf16; Zipf(1.05) over 128k "
+               "with canonical folding; fused W_V + 4 W_K (1280 -> 12800); RMSNorm-sigmoid gate; causal "
+               "depthwise conv k=4 dilation 3 + SiLU + residual into 4 branches of d=2560"}.get(w.cfg_id, w.name)
+    return {"workload": f"{w.name} (config {w.cfg_id}): {desc}", "batch": f"{w.B}x{w.L}", "tokens_per_gpu": w.N,
+            "table_bytes": t.table_bytes, "parallelism": f"dp{world} (independent batches, no collective)",
+            "l2": "flushed between timed steps (256 MiB write); table and activations > L2"}
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+def _oracle_sample(cfg: int, ntok: int):
+    """Runs the oracle over the first `ntok` tokens of the workload; returns seconds."""
+    import numpy as np
+    import torch
+
+    from hashed_head_gram_gb300 import workloads as W
+    from oracle import dense, oracle as orc
+
+    w = W.make_workload(cfg)
+    spec = w.tables[0]
+    tokens = W.make_tokens(w)
+    cmap = W.make_canon_map(w)
+    L = w.L
+    nseq = max(1, (ntok + L - 1) // L)
+    tok = tokens[:nseq]
+    which = np.arange(min(ntok, nseq * L), dtype=np.int64)
+    table = _cpu_table(w, spec)
+    dn = _cpu_dense(w)
+    t0 = time.perf_counter()
+    canon, rows, signs, bad = orc.index(spec, tok, cmap, w.vocab, which)
+    rowdata = orc.fetch_rows(table, rows)
+    e = orc.assemble(spec, rows, rowdata, signs, orc.BF16)
+    ef = orc.bf16_bits_to_f64(e)
+    if w.gate == W.GATE_SCALAR:
+        v = dense.project(ef, dn["W"])
+        dense.scalar_gate(dn["x"][:len(which)], v, w.g)
+    else:
+        v, a = dense.engram_gate(ef, dn["W"], dn["H"][:, :len(which)], dn["gh"], dn["gk"], w.eps, w.M)
+        n = len(which) // L * L
+        if n:
+            dense.conv_residual(v[:n].reshape(-1, L, w.d), a[:, :n].reshape(w.M, -1, L), dn["gc"], dn["cw"],
+                                w.dilation, w.eps, dn["H"][:, :n].reshape(w.M, -1, L, w.d))
+    return time.perf_counter() - t0, len(which)
+
+
+_CPU_CACHE = {}
+
+
+def _cpu_table(w, spec):
+    """Host copy of the table rows. The table tensor is generated on the CPU with the
+    same seeded generator kind the tests use (only the rows are needed)."""
+    import numpy as np
+    from hashed_head_gram_gb300 import workloads as W
+    key = ("t", w.cfg_id)
+    if key not in _CPU_CACHE:
+        if spec.table_bytes > (8 << 30):
+            raise RuntimeError("table too large for the CPU baseline leg")
+        t = W.make_table(w, spec, "cpu")
+        _CPU_CACHE[key] = t.view(__import__("torch").uint8).reshape(spec.table_rows, spec.row_bytes).numpy()
+    return _CPU_CACHE[key]
+
+
+def _cpu_dense(w):
+    from hashed_head_gram_gb300 import workloads as W
+    key = ("d", w.cfg_id)
+    if key not in _CPU_CACHE:
+        dn = W.make_dense(w, "cpu")
+        out = {"W": dn["W"].double().numpy()}
+        if "x" in dn:
+            out["x"] = dn["x"].double().numpy()
+        if "H" in dn:
+            out.update(H=dn["H"][:, :8192].double().numpy(), gh=dn["gamma_h"].double().numpy(),
+                       gk=dn["gamma_k"].double().numpy(), gc=dn["gamma_c"].double().numpy(),
+                       cw=dn["conv_w"].double().numpy())
+        _CPU_CACHE[key] = out
+    return _CPU_CACHE[key]
+
+
+def cpu_baseline(cfg: int, seconds: float):
+    """The oracle as it stands on the host cores, on a bounded sample of the workload."""
+    dt, n = _oracle_sample(cfg, 1024)                     # calibration
+    want = int(max(1024, min(1 << 16, n * seconds / max(dt, 1e-3))))
+    dt, n = _oracle_sample(cfg, want)
+    return {"value": round(n / dt, 1), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n} tokens of the workload batch; C stages single-threaded, numpy fp64 "
+                      f"projection/gate on the BLAS thread pool (up to {os.cpu_count()} cores); {dt:.2f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    dt1, n1 = _oracle_sample(args.config, 256)
+    budget = 60.0                                         # seconds for the whole run
+    per_step = max(64, min(1 << 14, int(n1 * budget / max((args.steps + args.warmup) * dt1, 1e-6))))
+    for _ in range(args.warmup):
+        _oracle_sample(args.config, per_step)
+    total_t, total_n = 0.0, 0
+    for _ in range(args.steps):
+        dt, n = _oracle_sample(args.config, per_step)
+        total_t += dt
+        total_n += n
+    value = total_n / total_t
+    from hashed_head_gram_gb300 import workloads as W
+    w = W.make_workload(args.config)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_t / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same seeded workload as the GPU arm)", "config": workload_config(w, 1),
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"{per_step} tokens per step from the workload batch"},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 5])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
