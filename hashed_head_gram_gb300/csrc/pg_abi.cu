@@ -192,6 +192,7 @@ const char* pg_status_str(pg_status s) {
     case PG_ERR_WORKSPACE: return "workspace missing or too small";
     case PG_ERR_CUDA: return "a CUDA runtime call failed";
     case PG_ERR_DEVICE: return "the current device cannot run this kernel (needs sm_103a)";
+    case PG_ERR_SCRATCH_LIMIT: return "request needs more scratch than the library's static scratch holds";
   }
   return "unknown status";
 }

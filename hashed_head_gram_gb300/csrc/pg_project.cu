@@ -19,6 +19,8 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "pg_internal.cuh"
 
 namespace pg {
@@ -733,3 +735,51 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
 }
 
 }  // extern "C"
+
+// ==================================================================== no-allocation variant
+
+namespace pg {
+namespace {
+
+// Scratch of pg_project_gate_context_noalloc: per-row partial sums of the context
+// gate. Device code never names it; host code passes its per-device address.
+static __device__ __align__(256) float g_noalloc_scratch[PG_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int kScratchDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kScratchDevices];
+
+// Device address of the scratch array on the current device (looked up once per device).
+pg_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (dev < 0 || dev >= kScratchDevices) return PG_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (err != cudaSuccess) return cuda_fail(err);
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return PG_OK;
+}
+
+}  // namespace
+}  // namespace pg
+
+extern "C" pg_status pg_project_gate_context_noalloc(int32_t N, int32_t Din, int32_t d, int32_t M,
+                                                     const void* e, const void* W, const void* h,
+                                                     const float* gamma_h, const float* gamma_k, float eps,
+                                                     void* v_out, float* alpha_out, pg_stream_t stream) {
+  size_t need = 0;
+  pg_status st = pg_project_gate_workspace_size(N, Din, d, M, PG_BF16, PG_GATE_CONTEXT, &need);
+  if (st != PG_OK) return st;
+  if (need > PG_NOALLOC_SCRATCH_BYTES) return PG_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  st = pg::noalloc_scratch(&scratch);
+  if (st != PG_OK) return st;
+  return pg_project_gate(N, Din, d, M, PG_BF16, e, W, PG_GATE_CONTEXT, 0.0f, nullptr, h, gamma_h, gamma_k,
+                         eps, v_out, alpha_out, scratch, PG_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -27,7 +27,7 @@ GATE_NONE, GATE_SCALAR, GATE_CONTEXT = 0, 1, 2
 
 STATUS = {0: "PG_OK", 1: "PG_ERR_NULL", 2: "PG_ERR_SHAPE", 3: "PG_ERR_DTYPE", 4: "PG_ERR_RANGE",
           5: "PG_ERR_ALIGN", 6: "PG_ERR_UNSUPPORTED", 7: "PG_ERR_VERSION", 8: "PG_ERR_WORKSPACE",
-          9: "PG_ERR_CUDA", 10: "PG_ERR_DEVICE"}
+          9: "PG_ERR_CUDA", 10: "PG_ERR_DEVICE", 11: "PG_ERR_SCRATCH_LIMIT"}
 
 
 class PgError(RuntimeError):
@@ -84,6 +84,8 @@ def _load():
     L.pg_project_gate.restype = ctypes.c_int
     L.pg_project_gate.argtypes = [i32, i32, i32, i32, i32, vp, vp, i32, f32, vp, vp, vp, vp, f32, vp, vp,
                                   vp, sz, vp]
+    L.pg_project_gate_context_noalloc.restype = ctypes.c_int
+    L.pg_project_gate_context_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp, vp, vp]
     L.pg_conv_residual.restype = ctypes.c_int
     L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp]
     return L
@@ -187,6 +189,18 @@ def project_gate(e: torch.Tensor, W: Optional[torch.Tensor], d: int, gate_kind: 
            "pg_project_gate")
 
 
+def project_gate_context_noalloc(e: torch.Tensor, W: torch.Tensor, d: int, M: int, h: torch.Tensor,
+                                 gamma_h: torch.Tensor, gamma_k: torch.Tensor, v_out: torch.Tensor,
+                                 alpha_out: torch.Tensor, eps: float = 1e-6, stream=None):
+    """Context-gate projection with the library's static scratch (no workspace, no
+    allocation); for callers that cannot allocate device memory."""
+    N, Din = e.shape
+    _check(_lib.pg_project_gate_context_noalloc(N, Din, d, M, _ptr(e), _ptr(W), _ptr(h), _ptr(gamma_h),
+                                                _ptr(gamma_k), eps, _ptr(v_out), _ptr(alpha_out),
+                                                _stream(stream)),
+           "pg_project_gate_context_noalloc")
+
+
 def conv_residual(B: int, L: int, d: int, M: int, dtype: int, v: torch.Tensor, alpha: torch.Tensor,
                   gamma_c: torch.Tensor, conv_w: torch.Tensor, H: torch.Tensor, dilation: int = 3,
                   eps: float = 1e-6, stream=None):
@@ -211,6 +225,6 @@ def dtype_code(t: torch.dtype) -> int:
 
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
-           "workspace_size", "project_gate", "conv_residual", "launch_count", "device_error", "lib",
+           "workspace_size", "project_gate", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

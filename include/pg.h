@@ -66,7 +66,8 @@ typedef enum {
   PG_ERR_VERSION = 7,      /* descriptor abi_version / hash_version not supported */
   PG_ERR_WORKSPACE = 8,    /* workspace missing or smaller than the size query says */
   PG_ERR_CUDA = 9,         /* a CUDA runtime call failed; see pg_last_cuda_error() */
-  PG_ERR_DEVICE = 10       /* current device cannot run the kernel (needs sm_103a) */
+  PG_ERR_DEVICE = 10,      /* current device cannot run the kernel (needs sm_103a) */
+  PG_ERR_SCRATCH_LIMIT = 11 /* request needs more than the library's static scratch */
 } pg_status;
 
 enum { PG_FLAT = 0, PG_ENGRAM = 1, PG_PAGEGRAM = 2 };
@@ -227,6 +228,40 @@ pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M, int32_t d
                            const void* v, const float* alpha, const float* gamma_c,
                            const float* conv_w, int32_t kernel_size, int32_t dilation,
                            float eps, void* H, pg_stream_t stream);
+
+/*
+ * pg_project_gate_context_noalloc -- the context-gate projection of pg_project_gate
+ * (gate PG_GATE_CONTEXT, dtype PG_BF16) for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point: it exists for the host side only.
+ *
+ * Some callers cannot call cudaMalloc: a serving runtime that hands all device memory
+ * to its own pool at start-up, or a plug-in whose host gives it no allocator and does
+ * not allow the device-wide synchronisation that cudaMalloc / cudaFree may cause. They
+ * cannot provide the workspace pg_project_gate needs, so this call uses scratch held
+ * by the library instead: a file-scope device array of PG_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) that every GPU which loads libpg.so keeps until the process exits.
+ *
+ * Arguments, results and errors are those of pg_project_gate with gate_kind =
+ * PG_GATE_CONTEXT, dtype = PG_BF16, g and x_resid unused. In addition:
+ *  - the call allocates nothing and frees nothing (no cudaMalloc, cudaFree or other
+ *    allocating routine);
+ *  - PG_ERR_SCRATCH_LIMIT when the scratch it needs, M * (d / BN) * 3 * N * 4 bytes with
+ *    BN = 256 if d % 256 == 0 else 128, exceeds PG_NOALLOC_SCRATCH_BYTES (at d = 2560,
+ *    M = 4: N <= 34,952 tokens); nothing is enqueued then;
+ *  - the first call on a device looks up the scratch array's device address on that
+ *    device (cudaGetSymbolAddress, with the device current); make that first call before
+ *    any stream capture;
+ *  - every call on a device shares the one array and overwrites all of the scratch it
+ *    uses before reading it (no part has to start at zero); calls whose kernels overlap
+ *    on the GPU (other streams, other host threads) race on it and must be ordered by
+ *    the caller.
+ */
+#define PG_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pg_status pg_project_gate_context_noalloc(int32_t N, int32_t Din, int32_t d, int32_t M,
+                                          const void* e, const void* W, const void* h,
+                                          const float* gamma_h, const float* gamma_k, float eps,
+                                          void* v_out, float* alpha_out, pg_stream_t stream);
 
 #ifdef __cplusplus
 }
