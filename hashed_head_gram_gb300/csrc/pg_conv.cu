@@ -5,11 +5,15 @@
 // section 3.1: H^(m) <- H^(m) + Y. The explainer's "一次 lookup 经过哪些步骤？" requires
 // the conv to be causal.
 //
-// One block per (sequence, run of kRun positions), d/8 threads: thread i owns channels
-// [8i, 8i+8). Since u = alpha v, RMSNorm(u) = f v gamma with the per-(branch, position)
-// scalar f = alpha / sqrt(alpha^2 mean(v^2) + eps), so the block first reduces sum(v^2)
-// for its positions and their causal halo, then every thread walks its positions:
-// c = sum_j w[:, j] f_{t-j dil} gamma v_{t-j dil};  H += SiLU(c) + alpha_t v_t.
+// Since u = alpha v, RMSNorm(u) = f v gamma with the per-(branch, position) scalar
+// f = alpha / sqrt(alpha^2 mean(v^2) + eps). A block owns runs of kRun positions of one
+// sequence (persistent grid) and d/8 threads, thread i owning channels [8i, 8i+8):
+//   1. one warp per position reduces sum(v^2) over the run and its causal halo;
+//   2. f and alpha per (branch, position) go to shared memory;
+//   3. every thread walks its positions: c = sum_j (w[:, j] gamma) f_{t-j dil} v_{t-j dil},
+//      H[m, t] += SiLU(c) + alpha_t v_t for all M branches, whose H loads issue together.
+// DRAM traffic per token: v once (2d bytes; the taps re-read it from L1/L2) and H read +
+// written once per branch (2 * M * 2d bytes).
 #include <cuda_bf16.h>
 
 #include "pg_internal.cuh"
@@ -17,18 +21,26 @@
 namespace pg {
 namespace {
 
-constexpr int kRun = 16;        // positions per block
+constexpr int kRun = 32;        // positions per run
 constexpr int kMaxHalo = 24;    // (kernel_size - 1) * dilation <= 3 * 8
 constexpr int kMaxBranches = 8;
 constexpr int kMaxPos = kRun + kMaxHalo;
+constexpr int kTaps = 4;
 
 template <typename T>
 struct Vec8;
 
 template <>
 struct Vec8<__nv_bfloat16> {
-  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* f) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
+  using Raw = uint4;
+  static __device__ __forceinline__ Raw zero() { return make_uint4(0, 0, 0, 0); }
+  static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+  }
+  static __device__ __forceinline__ Raw load_rw(const __nv_bfloat16* p) {
+    return *reinterpret_cast<const uint4*>(p);
+  }
+  static __device__ __forceinline__ void unpack(const Raw& w, float* f) {
     f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
     f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
     f[4] = __uint_as_float(w.z << 16); f[5] = __uint_as_float(w.z & 0xFFFF0000u);
@@ -47,9 +59,19 @@ struct Vec8<__nv_bfloat16> {
 
 template <>
 struct Vec8<float> {
-  static __device__ __forceinline__ void load(const float* p, float* f) {
-    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  struct Raw {
+    float4 a, b;
+  };
+  static __device__ __forceinline__ Raw zero() { return Raw{make_float4(0, 0, 0, 0), make_float4(0, 0, 0, 0)}; }
+  static __device__ __forceinline__ Raw load(const float* p) {
+    return Raw{__ldg(reinterpret_cast<const float4*>(p)), __ldg(reinterpret_cast<const float4*>(p + 4))};
+  }
+  static __device__ __forceinline__ Raw load_rw(const float* p) {
+    return Raw{*reinterpret_cast<const float4*>(p), *reinterpret_cast<const float4*>(p + 4)};
+  }
+  static __device__ __forceinline__ void unpack(const Raw& r, float* f) {
+    f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
+    f[4] = r.b.x; f[5] = r.b.y; f[6] = r.b.z; f[7] = r.b.w;
   }
   static __device__ __forceinline__ void store(float* p, const float* f) {
     *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
@@ -57,109 +79,140 @@ struct Vec8<float> {
   }
 };
 
-template <typename T>
-__global__ void __launch_bounds__(1024) conv_residual_kernel(
-    int B, int L, int d, int M, const T* __restrict__ v, const float* __restrict__ alpha,
-    const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks, int dil, float eps,
-    T* __restrict__ H) {
-  __shared__ float s_red[kMaxPos][32];
-  __shared__ float s_f[kMaxBranches][kMaxPos];
-  __shared__ float s_a[kMaxBranches][kMaxPos];
+// SiLU(c) = c * sigmoid(c) with sigmoid(c) = (1 + tanh(c/2)) / 2: one MUFU operation.
+__device__ __forceinline__ float silu(float c) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * c));
+  return c * fmaf(0.5f, t, 0.5f);
+}
 
-  const int runs = (L + kRun - 1) / kRun;
-  const int b = blockIdx.x / runs;
-  const int t0 = (blockIdx.x - b * runs) * kRun;
-  const int t1 = min(t0 + kRun, L);
-  const int halo = (ks - 1) * dil;
-  const int p0 = max(0, t0 - halo);
-  const int npos = t1 - p0;
+template <typename T, int MB>
+__global__ void __launch_bounds__(512) conv_residual_kernel(
+    int L, int d, int M_rt, int64_t N, const T* __restrict__ v, const float* __restrict__ alpha,
+    const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks, int dil, float eps,
+    T* __restrict__ H, int runs_per_seq, int total_runs) {
+  constexpr int MMAX = MB > 0 ? MB : kMaxBranches;
+  const int M = MB > 0 ? MB : M_rt;
+  __shared__ float s_ms[kMaxPos];
+  __shared__ float s_f[MMAX][kMaxPos];
+  __shared__ float s_a[MMAX][kMaxPos];
+
   const int c0 = threadIdx.x * 8;
   const bool active = c0 < d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = (blockDim.x + 31) >> 5;
-  const int64_t seq0 = static_cast<int64_t>(b) * L;
-  const int64_t N = static_cast<int64_t>(B) * L;
-
-  // ---- sum(v^2) per position (positions p0 .. t1-1)
-  for (int i = 0; i < npos; ++i) {
-    float s = 0.f;
-    if (active) {
-      float x[8];
-      Vec8<T>::load(v + (seq0 + p0 + i) * d + c0, x);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) s = fmaf(x[q], x[q], s);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) s_red[i][warp] = s;
-  }
-  __syncthreads();
+  const int nwarps = blockDim.x >> 5;
+  const int chunks = d >> 3;
+  const int halo = (ks - 1) * dil;
   const float inv_d = 1.0f / static_cast<float>(d);
-  for (int idx = threadIdx.x; idx < M * npos; idx += blockDim.x) {
-    const int m = idx / npos, i = idx - (idx / npos) * npos;
-    float ms = 0.f;
-    for (int w = 0; w < nwarps; ++w) ms += s_red[i][w];
-    ms *= inv_d;
-    const float a = alpha[static_cast<int64_t>(m) * N + seq0 + p0 + i];
-    s_a[m][i] = a;
-    s_f[m][i] = a / sqrtf(a * a * ms + eps);
-  }
-  __syncthreads();
-  if (!active) return;
 
-  float gam[8], w[4][8];
-  {
-    const float4 g0 = *reinterpret_cast<const float4*>(gamma_c + c0);
-    const float4 g1 = *reinterpret_cast<const float4*>(gamma_c + c0 + 4);
-    gam[0] = g0.x; gam[1] = g0.y; gam[2] = g0.z; gam[3] = g0.w;
-    gam[4] = g1.x; gam[5] = g1.y; gam[6] = g1.z; gam[7] = g1.w;
+  // conv taps with the RMSNorm gain folded in: wg[j][q] = w[c0+q, j] * gamma[c0+q]
+  float wg[kTaps][8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+  for (int q = 0; q < 8; ++q) {
+    const float g = active ? gamma_c[c0 + q] : 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) w[j][q] = j < ks ? conv_w[(c0 + q) * ks + j] : 0.f;
+    for (int j = 0; j < kTaps; ++j) wg[j][q] = (active && j < ks) ? conv_w[(c0 + q) * ks + j] * g : 0.f;
   }
 
-  for (int t = t0; t < t1; ++t) {
-    float vt[4][8];  // v at t - j*dil (zeros before the start of the sequence)
+  for (int run = blockIdx.x; run < total_runs; run += gridDim.x) {
+    const int b = run / runs_per_seq;
+    const int t0 = (run - b * runs_per_seq) * kRun;
+    const int t1 = min(t0 + kRun, L);
+    const int p0 = max(0, t0 - halo);
+    const int npos = t1 - p0;
+    const int64_t seq0 = static_cast<int64_t>(b) * L;
+
+    // 1. mean(v^2) per position, one warp per position
+    for (int i = warp; i < npos; i += nwarps) {
+      const T* row = v + (seq0 + p0 + i) * d;
+      float s = 0.f;
+      for (int q = lane; q < chunks; q += 32) {
+        float x[8];
+        Vec8<T>::unpack(Vec8<T>::load(row + 8 * q), x);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int p = t - j * dil;
-      if (j < ks && p >= 0) {
-        Vec8<T>::load(v + (seq0 + p) * d + c0, vt[j]);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) vt[j][q] *= gam[q];
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) vt[j][q] = 0.f;
+        for (int k = 0; k < 8; ++k) s = fmaf(x[k], x[k], s);
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane == 0) s_ms[i] = s * inv_d;
     }
-    float vraw[8];
-    Vec8<T>::load(v + (seq0 + t) * d + c0, vraw);
-    for (int m = 0; m < M; ++m) {
-      float conv[8];
+    __syncthreads();
+    // 2. alpha and f = alpha / sqrt(alpha^2 mean(v^2) + eps) per (branch, position)
+    for (int idx = threadIdx.x; idx < M * npos; idx += blockDim.x) {
+      const int m = idx / npos, i = idx - (idx / npos) * npos;
+      const float a = alpha[m * N + seq0 + p0 + i];
+      s_a[m][i] = a;
+      s_f[m][i] = a * rsqrtf(a * a * s_ms[i] + eps);
+    }
+    __syncthreads();
+
+    // 3. conv + SiLU + residual, all branches of a position together
+    if (active) {
+      for (int t = t0; t < t1; ++t) {
+        typename Vec8<T>::Raw vraw[kTaps];  // tap rows stay packed; unpacked per branch
 #pragma unroll
-      for (int q = 0; q < 8; ++q) conv[q] = 0.f;
+        for (int j = 0; j < kTaps; ++j) {
+          const int p = t - j * dil;
+          vraw[j] = (j < ks && p >= 0) ? Vec8<T>::load(v + (seq0 + p) * d + c0) : Vec8<T>::zero();
+        }
+        typename Vec8<T>::Raw hraw[MMAX];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int p = t - j * dil;
-        if (j < ks && p >= 0) {
-          const float f = s_f[m][p - p0];
+        for (int m = 0; m < MMAX; ++m)
+          if (m < M) hraw[m] = Vec8<T>::load_rw(H + (m * N + seq0 + t) * d + c0);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) conv[q] = fmaf(w[j][q] * f, vt[j][q], conv[q]);
+        for (int m = 0; m < MMAX; ++m) {
+          if (m >= M) continue;
+          float fj[kTaps];
+#pragma unroll
+          for (int j = 0; j < kTaps; ++j) {
+            const int p = t - j * dil;
+            fj[j] = (j < ks && p >= 0) ? s_f[m][p - p0] : 0.f;
+          }
+          const float a = s_a[m][t - p0];
+          float h[8], c[8], x[8];
+          Vec8<T>::unpack(hraw[m], h);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) c[q] = 0.f;
+#pragma unroll
+          for (int j = kTaps - 1; j >= 0; --j) {
+            Vec8<T>::unpack(vraw[j], x);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) c[q] = fmaf(wg[j][q] * fj[j], x[q], c[q]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) h[q] = h[q] + (silu(c[q]) + a * x[q]);  // x = v_t (tap 0)
+          Vec8<T>::store(H + (m * N + seq0 + t) * d + c0, h);
         }
       }
-      const float a = s_a[m][t - p0];
-      T* hp = H + (static_cast<int64_t>(m) * N + seq0 + t) * d + c0;
-      float hv[8];
-      Vec8<T>::load(hp, hv);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float c = conv[q];
-        const float silu = c / (1.0f + __expf(-c));
-        hv[q] = hv[q] + (silu + a * vraw[q]);
-      }
-      Vec8<T>::store(hp, hv);
     }
+    __syncthreads();
+  }
+}
+
+template <typename T>
+pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, const float* gamma_c,
+                 const float* conv_w, int ks, int dil, float eps, void* H, cudaStream_t stream) {
+  const int threads = ((d / 8) + 31) / 32 * 32;
+  const int runs_per_seq = (L + kRun - 1) / kRun;
+  const int64_t total = static_cast<int64_t>(B) * runs_per_seq;
+  if (total >= (1ll << 31)) return PG_ERR_SHAPE;
+  const int64_t N = static_cast<int64_t>(B) * L;
+  auto run = [&](auto kern) -> pg_status {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+    const int grid = static_cast<int>(total < cap ? total : cap);
+    kern<<<grid, threads, 0, stream>>>(L, d, M, N, static_cast<const T*>(v), alpha, gamma_c, conv_w, ks, dil,
+                                       eps, static_cast<T*>(H), runs_per_seq, static_cast<int>(total));
+    return after_launch(1);
+  };
+  switch (M) {
+    case 1: return run(conv_residual_kernel<T, 1>);
+    case 2: return run(conv_residual_kernel<T, 2>);
+    case 4: return run(conv_residual_kernel<T, 4>);
+    default: return run(conv_residual_kernel<T, 0>);
   }
 }
 
@@ -173,25 +226,14 @@ extern "C" pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M
   using namespace pg;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (B < 0 || L < 0 || d < 8 || d % 8 || d > 8192 || M < 1 || M > kMaxBranches) return PG_ERR_SHAPE;
-  if (kernel_size < 1 || kernel_size > 4 || dilation < 1 || dilation > 8) return PG_ERR_SHAPE;
+  if (kernel_size < 1 || kernel_size > kTaps || dilation < 1 || dilation > 8) return PG_ERR_SHAPE;
   if (dtype != PG_BF16 && dtype != PG_F32) return PG_ERR_DTYPE;
   if (static_cast<int64_t>(B) * L == 0) return PG_OK;
   if (static_cast<int64_t>(B) * L >= (1ll << 31)) return PG_ERR_SHAPE;
   if (!v || !alpha || !gamma_c || !conv_w || !H) return PG_ERR_NULL;
-  if ((reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(H) |
-       reinterpret_cast<uintptr_t>(gamma_c)) & 15u)
-    return PG_ERR_ALIGN;
-  const int threads = ((d / 8) + 31) / 32 * 32;
-  const int runs = (L + kRun - 1) / kRun;
-  const int64_t blocks = static_cast<int64_t>(B) * runs;
-  if (blocks >= (1ll << 31)) return PG_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(H)) & 15u) return PG_ERR_ALIGN;
+  if (sm_count() == 0) return cuda_fail(cudaGetLastError());
   if (dtype == PG_BF16)
-    conv_residual_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        B, L, d, M, static_cast<const __nv_bfloat16*>(v), alpha, gamma_c, conv_w, kernel_size, dilation,
-        eps, static_cast<__nv_bfloat16*>(H));
-  else
-    conv_residual_kernel<float><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        B, L, d, M, static_cast<const float*>(v), alpha, gamma_c, conv_w, kernel_size, dilation, eps,
-        static_cast<float*>(H));
-  return after_launch(1);
+    return launch<__nv_bfloat16>(B, L, d, M, v, alpha, gamma_c, conv_w, kernel_size, dilation, eps, H, stream);
+  return launch<float>(B, L, d, M, v, alpha, gamma_c, conv_w, kernel_size, dilation, eps, H, stream);
 }

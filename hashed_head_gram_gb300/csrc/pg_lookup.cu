@@ -1,16 +1,16 @@
 // Hashing and gather kernels of the N-gram lookup (sm_103a).
 //
 // pg_canon_hash          one thread per (token, order, head): writes x'_t, rows, sign words.
-// pg_gather_sign_concat  one warp per token (grid-stride, persistent grid):
-//   phase A  lanes 0..3 read the token window and canonicalise it; lane l owns item
-//            l = (order o, head k), whose multipliers it computed once at kernel start,
-//            and hashes it to a row (+ the 64-bit sign hash); sign words follow.
-//   phase B  the token's rows are streamed in 16-byte chunks: chunk c covers bytes
-//            [16c, 16c+16) of the token's concatenated e_t, so every warp store writes
-//            512 contiguous bytes and every load reads 16 bytes of one row. In PageGram
-//            mode all K rows of an order lie in one K*S-row page block (4 KiB for
-//            bf16 r=64, S=4; 1088 B for NF4), so each order is served from one
-//            contiguous segment (PageGram tech report, section 3.1).
+// pg_gather_sign_concat  persistent grid of 256-thread blocks:
+//   Each warp takes batches of tb tokens (2 for K = 8 heads x 2 orders), independently:
+//   phase A  one lane per (token, item = (order o, head k)): canonical window, the page /
+//            head / sign multiply-XOR hashes, the row (remainders by direct computation)
+//            and the sign words, into the warp's double-buffered shared memory;
+//   phase B  the batch is streamed in 16-byte chunks, 8 per lane: chunk c of a token covers
+//            bytes [16c, 16c+16) of its concatenated e_t, so 32 consecutive chunks are 512
+//            contiguous bytes of e_t and 4 whole 128-byte rows of one page (PageGram: all K
+//            rows of an order lie in one K*S-row page block, PageGram report section 3.1);
+//   phase A of the warp's next batch runs while phase B's loads are in flight.
 // Sources: PageGram report sections 2.1, 2.2, 3.1, 3.3; Engram notes (arXiv 2601.07372)
 // section 3.2.
 #include <cuda_bf16.h>
@@ -20,10 +20,6 @@
 
 namespace pg {
 namespace {
-
-constexpr int kWarps = 8;            // warps per block of the gather kernel
-constexpr int kMaxItems = 32;        // (order, head) items per token in the gather kernel
-constexpr int kMaxSignWords = 128;   // items * sign words per token in the gather kernel
 
 // NF4 levels: normal quantiles at evenly spaced probabilities (7 negative, exact zero,
 // 8 positive; outermost probability 1 - (1/30 + 1/32)/2), scaled to [-1, 1]; the
@@ -114,10 +110,48 @@ __global__ void __launch_bounds__(256) canon_hash_kernel(
 
 // ------------------------------------------------------------------ K2: fused gather
 
-struct WarpScratch {
-  uint32_t row[kMaxItems];
-  uint64_t hsign[kMaxItems];
-  uint64_t sign[kMaxSignWords];
+constexpr int kThreads = 256;       // threads per gather block
+constexpr int kChunksPerThread = 8; // 16-byte chunks (or NF4 tasks) per lane per warp batch
+constexpr int kMaxItems = 32;       // (order, head) items per token
+constexpr int kMaxSignWords = 128;  // items * sign words per token
+
+// Remainder by direct computation (Lemire, Kaser & Kurz, "Faster remainder by direct
+// computation", Software: Practice and Experience 2019): with c = ceil(2^64 / d),
+// a mod d = floor(((c * a) mod 2^64) * d / 2^64), exact for all 32-bit a and d >= 1
+// (d = 1 gives c = 0 and the remainder 0).
+__host__ __device__ __forceinline__ uint64_t fastmod_constant(uint32_t d) { return ~0ull / d + 1ull; }
+
+__device__ __forceinline__ uint32_t fastmod(uint32_t a, uint64_t c, uint32_t d) {
+  return static_cast<uint32_t>(__umul64hi(c * a, d));
+}
+
+// Per-item constants in shared memory.
+struct ItemConst {
+  uint64_t mp[4], mh[4], ms[4];  // multipliers: page hash, head hash, sign hash
+  uint64_t fm_main, fm_slot;     // fastmod constants of div_main and S
+  uint32_t div_main;             // P_n (PageGram), M_{n,k} (Engram), R_n (flat)
+  uint32_t slots;                // S (PageGram), 1 otherwise
+  uint32_t stride;               // K * S (PageGram)
+  uint32_t base;                 // row of (page 0, head k, slot 0) / subtable start
+  int32_t n;                     // n-gram order
+  int32_t pad;
+};
+
+struct GatherGeom {
+  int64_t N;            // tokens
+  uint32_t L;           // sequence length
+  uint64_t fm_L;        // fastmod constant of L
+  int items;            // O * H
+  int W;                // sign words per item
+  int tb;               // tokens per batch
+  int per_tok;          // chunks (or NF4 tasks) per token
+  uint32_t tok_magic;   // floor(c / per_tok) = umulhi(c, tok_magic)
+  uint32_t items_magic; // floor(p / items) = umulhi(p, items_magic)
+  uint32_t rc;          // 16-byte chunks per stored row (multi-head f32/bf16), or per row (flat)
+  uint32_t rc_magic;
+  uint32_t row_bytes;
+  uint32_t e_bytes;     // bytes of one token's e_t
+  int64_t nbatch;
 };
 
 __device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
@@ -161,235 +195,221 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Registers are capped so that NCH <= 4 variants keep 32 warps per SM resident.
-template <int ROWT, int OUTT, bool FLAT, int NCH>
-__global__ void __launch_bounds__(kWarps * 32, NCH <= 4 ? 4 : (NCH <= 8 ? 2 : 1)) gather_kernel(
-    const __grid_constant__ HashParams P, uint64_t seed, const int32_t* __restrict__ tokens,
-    int64_t B, int64_t L, const uint32_t* __restrict__ canon_map,
-    const uint8_t* __restrict__ table, uint32_t row_bytes, uint32_t rc, uint32_t rc_magic,
-    uint8_t* __restrict__ e_out, uint32_t e_bytes, int32_t* err) {
-  __shared__ WarpScratch scratch[kWarps];
+// Phase A: rows and sign words of every (token, item) of one warp batch, one lane each.
+__device__ __forceinline__ void hash_batch(const ItemConst* __restrict__ ic, const GatherGeom& g, int mode,
+                                           int64_t batch, int lane, const int32_t* __restrict__ tokens,
+                                           const uint32_t* __restrict__ canon_map, uint32_t vocab,
+                                           uint32_t* s_rows, uint64_t* s_signs, int32_t* err) {
+  const int p = lane;
+  if (p >= g.tb * g.items) return;
+  const int s = static_cast<int>(__umulhi(static_cast<uint32_t>(p), g.items_magic));
+  const int item = p - s * g.items;
+  const int64_t tok = batch * g.tb + s;
+  if (tok >= g.N) return;
+  const ItemConst& it = ic[item];
+  const uint32_t t = fastmod(static_cast<uint32_t>(tok), g.fm_L, g.L);
+  uint64_t hp = 0, hh = 0, hs = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j < it.n) {
+      const uint64_t c = (t >= static_cast<uint32_t>(j)) ? canon_token(tokens, canon_map, vocab, tok - j, err) : kPad;
+      hp ^= c * it.mp[j];
+      hh ^= c * it.mh[j];
+      hs ^= c * it.ms[j];
+    }
+  }
+  uint32_t row;
+  if (mode == PG_PAGEGRAM)
+    row = it.base + fastmod(fold32(hp), it.fm_main, it.div_main) * it.stride +
+          fastmod(fold32(hh), it.fm_slot, it.slots);
+  else
+    row = it.base + fastmod(fold32(hh), it.fm_main, it.div_main);
+  s_rows[p] = row;
+  for (int q = 0; q < g.W; ++q) s_signs[p * g.W + q] = mix64(hs + kGolden * static_cast<uint64_t>(q + 1));
+}
+
+template <int ROWT, int OUTT, bool FLAT>
+__global__ void __launch_bounds__(kThreads, 2) gather_kernel(
+    const __grid_constant__ HashParams P, uint64_t seed, const GatherGeom g, const int32_t* __restrict__ tokens,
+    const uint32_t* __restrict__ canon_map, const uint8_t* __restrict__ table, uint8_t* __restrict__ e_out,
+    int32_t* err) {
+  constexpr int NCH = kChunksPerThread;
+  constexpr int kWarpsPerBlock = kThreads / 32;
+  __shared__ ItemConst s_ic[kMaxItems];
   __shared__ float s_nf4[16];
+  // per warp, double-buffered: rows [2][32], sign words [2][kMaxSignWords]
+  __shared__ uint32_t s_rows_all[kWarpsPerBlock][2][32];
+  __shared__ uint64_t s_signs_all[kWarpsPerBlock][2][kMaxSignWords];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  WarpScratch& ws = scratch[warp];
+
+  // Per-item constants: multipliers (from the seed), divisors, fastmod constants.
+  if (threadIdx.x < g.items) {
+    const int item = threadIdx.x;
+    const int o = item / P.H, k = item - o * P.H;
+    ItemConst& it = s_ic[item];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      it.mp[j] = multiplier(seed, 0, o, 0, j);
+      it.mh[j] = multiplier(seed, 1, o, k, j);
+      it.ms[j] = multiplier(seed, 2, o, k, j);
+    }
+    const bool paged = P.mode == PG_PAGEGRAM;
+    it.div_main = paged ? P.divisor[o][0] : P.divisor[o][P.mode == PG_ENGRAM ? k : 0];
+    it.slots = paged ? static_cast<uint32_t>(P.S) : 1u;
+    it.stride = paged ? static_cast<uint32_t>(P.K * P.S) : 0u;
+    it.base = paged ? P.base[o][0] + static_cast<uint32_t>(k * P.S) : P.base[o][P.mode == PG_ENGRAM ? k : 0];
+    it.fm_main = fastmod_constant(it.div_main);
+    it.fm_slot = fastmod_constant(it.slots);
+    it.n = P.order_n[o];
+  }
   if (ROWT == PG_NF4 && threadIdx.x < 16) s_nf4[threadIdx.x] = __uint_as_float(c_nf4_bits[threadIdx.x]);
   __syncthreads();
 
-  const int items = P.O * P.H;
-  const int W = P.W;
-  // This lane's item and its multipliers (fixed for the whole kernel).
-  const bool has_item = lane < items;
-  const int io = has_item ? lane / P.H : 0;
-  const int ik = has_item ? lane - io * P.H : 0;
-  const int n = P.order_n[io];
-  int nmax = 0;
-  for (int o = 0; o < P.O; ++o) nmax = max(nmax, P.order_n[o]);
-  uint64_t mp[4], mh[4], ms[4];
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
+  if (first < g.nbatch)
+    hash_batch(s_ic, g, P.mode, first, lane, tokens, canon_map, P.vocab, s_rows_all[warp][0],
+               s_signs_all[warp][0], err);
+  __syncwarp();
+  const int chunks = g.tb * g.per_tok;
+  int cur = 0;
+  for (int64_t batch = first; batch < g.nbatch; batch += nwarps) {
+    const uint32_t* rows = s_rows_all[warp][cur];
+    const uint64_t* signs = s_signs_all[warp][cur];
+    // ---- phase B, issue: loads of this batch's chunks
+    uint4 v[NCH];
+    uint32_t bits[NCH];
+    uint32_t aux[NCH];   // NF4: scale bits
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    mp[j] = multiplier(seed, 0, io, 0, j);
-    mh[j] = multiplier(seed, 1, io, ik, j);
-    ms[j] = multiplier(seed, 2, io, ik, j);
-  }
-  // Row of this lane's item = lane_base + (H_page mod div_main) * stride + H_head mod S
-  // (PageGram), or lane_base + H_head mod div_main (Engram, flat).
-  const bool paged = P.mode == PG_PAGEGRAM;
-  const uint32_t div_main = paged ? P.divisor[io][0] : P.divisor[io][P.mode == PG_ENGRAM ? ik : 0];
-  const uint32_t slots = static_cast<uint32_t>(P.S);
-  const uint32_t stride = static_cast<uint32_t>(P.K) * slots;
-  const uint32_t lane_base = paged ? P.base[io][0] + static_cast<uint32_t>(ik) * slots
-                                   : P.base[io][P.mode == PG_ENGRAM ? ik : 0];
-
-  const int64_t N = B * L;
-  const int64_t warp_stride = static_cast<int64_t>(gridDim.x) * kWarps;
-  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kWarps + warp; tok < N; tok += warp_stride) {
-    const int64_t b = tok / L, t = tok - b * L;
-    // ---- phase A: window, hashes, rows, sign words
-    uint32_t cj = kPad;
-    if (lane < nmax && t - lane >= 0) cj = canon_token(tokens, canon_map, P.vocab, tok - lane, err);
-    uint32_t c[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) c[j] = __shfl_sync(0xffffffffu, cj, j);
-    if (has_item) {
-      uint64_t hp = 0, hh = 0, hs = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (j < n) {
-          const uint64_t cv = c[j];
-          hp ^= cv * mp[j];
-          hh ^= cv * mh[j];
-          hs ^= cv * ms[j];
-        }
-      const uint32_t h32 = fold32(hh);
-      ws.row[lane] = paged ? lane_base + (fold32(hp) % div_main) * stride + h32 % slots
-                           : lane_base + h32 % div_main;
-      ws.hsign[lane] = hs;
-    }
-    __syncwarp();
-    for (int s = lane; s < items * W; s += 32) {
-      const int it = s / W;
-      ws.sign[s] = mix64(ws.hsign[it] + kGolden * static_cast<uint64_t>(s - it * W + 1));
-    }
-    __syncwarp();
-
-    // ---- phase B: gather, dequantise, sign, concat (or flat sum)
-    uint8_t* out_tok = e_out + static_cast<uint64_t>(tok) * e_bytes;
-    if constexpr (FLAT) {
-      // rc chunks of 16 bytes per row; every order contributes to every chunk.
-      constexpr int E = ROWT == PG_F32 ? 4 : 8;   // elements per chunk
-#pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int cidx = lane + 32 * i;
-        if (cidx < static_cast<int>(rc)) {
-          float acc[E];
-          for (int o = 0; o < P.O; ++o) {
-            const uint4 v = ldg_stream(table + static_cast<uint64_t>(ws.row[o]) * row_bytes +
-                                       static_cast<uint32_t>(cidx) * 16u);
-            const int e0 = cidx * E;
-            const uint32_t bits =
-                static_cast<uint32_t>(ws.sign[o * W + (e0 >> 6)] >> (e0 & 63)) & ((1u << E) - 1u);
-            float x[E];
-            if constexpr (ROWT == PG_F32) {
-              const uint4 f = xor4(v, f32_sign_mask(bits));
-              x[0] = __uint_as_float(f.x); x[1] = __uint_as_float(f.y);
-              x[2] = __uint_as_float(f.z); x[3] = __uint_as_float(f.w);
-            } else {
-              const uint4 f = xor4(v, bf16_sign_mask(bits));
-              x[0] = bf16_lo(f.x); x[1] = bf16_hi(f.x); x[2] = bf16_lo(f.y); x[3] = bf16_hi(f.y);
-              x[4] = bf16_lo(f.z); x[5] = bf16_hi(f.z); x[6] = bf16_lo(f.w); x[7] = bf16_hi(f.w);
-            }
-#pragma unroll
-            for (int q = 0; q < E; ++q) acc[q] = (o == 0) ? x[q] : __fadd_rn(acc[q], x[q]);
-          }
-          if constexpr (OUTT == PG_F32) {
-#pragma unroll
-            for (int q = 0; q < E; q += 4)
-              *reinterpret_cast<uint4*>(out_tok + (static_cast<uint32_t>(cidx) * E + q) * 4u) =
-                  make_uint4(__float_as_uint(acc[q]), __float_as_uint(acc[q + 1]),
-                             __float_as_uint(acc[q + 2]), __float_as_uint(acc[q + 3]));
+    for (int i = 0; i < NCH; ++i) {
+      const uint32_t c = lane + 32 * i;
+      if (c < static_cast<uint32_t>(chunks)) {
+        const uint32_t s = __umulhi(c, g.tok_magic);
+        const uint32_t cc = c - s * g.per_tok;
+        if (batch * g.tb + s < g.N) {
+          if constexpr (FLAT) {
+            // chunk cc of the d-wide row, for every order: loaded and summed at use
+            v[i] = make_uint4(0, 0, 0, 0);
+            bits[i] = 0;
+          } else if constexpr (ROWT == PG_NF4) {
+            const uint32_t it = cc >> 3, piece = cc & 7u;
+            const uint8_t* rowp = table + static_cast<uint64_t>(rows[s * g.items + it]) * 34u;
+            v[i].x = static_cast<uint32_t>(ldg_u16(rowp + 4 * piece)) |
+                     (static_cast<uint32_t>(ldg_u16(rowp + 4 * piece + 2)) << 16);
+            aux[i] = ldg_u16(rowp + 32);
+            bits[i] = static_cast<uint32_t>(signs[(s * g.items + it) * g.W] >> (piece * 8)) & 0xFFu;
           } else {
-            uint4 o4;
-            o4.x = pack_bf16(acc[0], acc[1]);
-            o4.y = pack_bf16(acc[2], acc[3]);
-            o4.z = pack_bf16(acc[4], acc[5]);
-            o4.w = pack_bf16(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(out_tok + static_cast<uint32_t>(cidx) * 16u) = o4;
+            constexpr int E = ROWT == PG_F32 ? 4 : 8;
+            const uint32_t it = g.rc == 1u ? cc : __umulhi(cc, g.rc_magic);
+            const uint32_t piece = cc - it * g.rc;
+            v[i] = ldg_stream(table + static_cast<uint64_t>(rows[s * g.items + it]) * g.row_bytes + piece * 16u);
+            const uint32_t e0 = piece * E;
+            bits[i] = static_cast<uint32_t>(signs[(s * g.items + it) * g.W + (e0 >> 6)] >> (e0 & 63)) &
+                      ((1u << E) - 1u);
           }
         }
       }
-    } else if constexpr (ROWT == PG_NF4) {
-      // task c = (item, piece of 8 elements); codes at bytes [4*piece, 4*piece + 4) of
-      // the 34-byte row (2-byte aligned), scale at bytes 32..33.
-      const int tasks = items * 8;
-      uint32_t codes[NCH];
-      uint16_t sbits[NCH];
-      uint32_t bits[NCH];
+    }
+    // ---- phase A of the next batch while the loads are in flight
+    const int64_t next = batch + nwarps;
+    if (next < g.nbatch)
+      hash_batch(s_ic, g, P.mode, next, lane, tokens, canon_map, P.vocab, s_rows_all[warp][cur ^ 1],
+                 s_signs_all[warp][cur ^ 1], err);
+    // ---- phase B, finish: dequantise, sign, (sum), store
 #pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int cidx = lane + 32 * i;
-        if (cidx < tasks) {
-          const int it = cidx >> 3, piece = cidx & 7;
-          const uint8_t* rowp = table + static_cast<uint64_t>(ws.row[it]) * 34u;
-          const uint32_t lo = ldg_u16(rowp + 4 * piece);
-          const uint32_t hi = ldg_u16(rowp + 4 * piece + 2);
-          codes[i] = lo | (hi << 16);
-          sbits[i] = ldg_u16(rowp + 32);
-          bits[i] = static_cast<uint32_t>(ws.sign[it * W] >> (piece * 8)) & 0xFFu;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const int cidx = lane + 32 * i;
-        if (cidx < tasks) {
-          const float scale = __half2float(__ushort_as_half(sbits[i]));
-          float x[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float v = s_nf4[(codes[i] >> (4 * q)) & 15u] * scale;
-            x[q] = ((bits[i] >> q) & 1u) ? -v : v;
-          }
-          if constexpr (OUTT == PG_F32) {
-            uint8_t* dst = out_tok + static_cast<uint32_t>(cidx) * 32u;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
-                                                        __float_as_uint(x[2]), __float_as_uint(x[3]));
-            *reinterpret_cast<uint4*>(dst + 16) = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
-                                                             __float_as_uint(x[6]), __float_as_uint(x[7]));
-          } else {
-            uint4 o4;
-            o4.x = pack_bf16(x[0], x[1]);
-            o4.y = pack_bf16(x[2], x[3]);
-            o4.z = pack_bf16(x[4], x[5]);
-            o4.w = pack_bf16(x[6], x[7]);
-            *reinterpret_cast<uint4*>(out_tok + static_cast<uint32_t>(cidx) * 16u) = o4;
-          }
-        }
-      }
-    } else {
-      // multi-head f32 / bf16 rows: chunk c = (item, piece); item = c / rc.
-      constexpr int E = ROWT == PG_F32 ? 4 : 8;
-      const int chunks = items * static_cast<int>(rc);
-      uint4 v[NCH];
-      uint32_t bits[NCH];
-#pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const uint32_t cidx = static_cast<uint32_t>(lane + 32 * i);
-        if (cidx < static_cast<uint32_t>(chunks)) {
-          const uint32_t it = rc == 1u ? cidx : __umulhi(cidx, rc_magic);
-          const uint32_t piece = cidx - it * rc;
-          v[i] = ldg_stream(table + static_cast<uint64_t>(ws.row[it]) * row_bytes + piece * 16u);
-          const uint32_t e0 = piece * E;
-          bits[i] = static_cast<uint32_t>(ws.sign[it * W + (e0 >> 6)] >> (e0 & 63)) & ((1u << E) - 1u);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < NCH; ++i) {
-        const uint32_t cidx = static_cast<uint32_t>(lane + 32 * i);
-        if (cidx < static_cast<uint32_t>(chunks)) {
+    for (int i = 0; i < NCH; ++i) {
+      const uint32_t c = lane + 32 * i;
+      if (c >= static_cast<uint32_t>(chunks)) continue;
+      const uint32_t s = __umulhi(c, g.tok_magic);
+      const uint32_t cc = c - s * g.per_tok;
+      const int64_t tok = batch * g.tb + s;
+      if (tok >= g.N) continue;
+      uint8_t* out_tok = e_out + static_cast<uint64_t>(tok) * g.e_bytes;
+      if constexpr (FLAT) {
+        constexpr int E = ROWT == PG_F32 ? 4 : 8;
+        const int O = g.items;
+        float acc[E];
+        for (int o = 0; o < O; ++o) {
+          const uint4 x4 = ldg_stream(table + static_cast<uint64_t>(rows[s * O + o]) * g.row_bytes + cc * 16u);
+          const uint32_t e0 = cc * E;
+          const uint32_t b = static_cast<uint32_t>(signs[(s * O + o) * g.W + (e0 >> 6)] >> (e0 & 63)) &
+                             ((1u << E) - 1u);
+          float x[E];
           if constexpr (ROWT == PG_F32) {
-            *reinterpret_cast<uint4*>(out_tok + cidx * 16u) = xor4(v[i], f32_sign_mask(bits[i]));
-          } else if constexpr (OUTT == PG_BF16) {
-            *reinterpret_cast<uint4*>(out_tok + cidx * 16u) = xor4(v[i], bf16_sign_mask(bits[i]));
+            const uint4 f = xor4(x4, f32_sign_mask(b));
+            x[0] = __uint_as_float(f.x); x[1] = __uint_as_float(f.y);
+            x[2] = __uint_as_float(f.z); x[3] = __uint_as_float(f.w);
           } else {
-            const uint4 f = xor4(v[i], bf16_sign_mask(bits[i]));
-            uint8_t* dst = out_tok + cidx * 32u;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(f.x << 16, f.x & 0xFFFF0000u,
-                                                        f.y << 16, f.y & 0xFFFF0000u);
-            *reinterpret_cast<uint4*>(dst + 16) = make_uint4(f.z << 16, f.z & 0xFFFF0000u,
-                                                             f.w << 16, f.w & 0xFFFF0000u);
+            const uint4 f = xor4(x4, bf16_sign_mask(b));
+            x[0] = bf16_lo(f.x); x[1] = bf16_hi(f.x); x[2] = bf16_lo(f.y); x[3] = bf16_hi(f.y);
+            x[4] = bf16_lo(f.z); x[5] = bf16_hi(f.z); x[6] = bf16_lo(f.w); x[7] = bf16_hi(f.w);
           }
+#pragma unroll
+          for (int q = 0; q < E; ++q) acc[q] = (o == 0) ? x[q] : __fadd_rn(acc[q], x[q]);
         }
+        if constexpr (OUTT == PG_F32) {
+#pragma unroll
+          for (int q = 0; q < E; q += 4)
+            *reinterpret_cast<uint4*>(out_tok + (cc * E + q) * 4u) =
+                make_uint4(__float_as_uint(acc[q]), __float_as_uint(acc[q + 1]), __float_as_uint(acc[q + 2]),
+                           __float_as_uint(acc[q + 3]));
+        } else {
+          *reinterpret_cast<uint4*>(out_tok + cc * 16u) =
+              make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                         pack_bf16(acc[6], acc[7]));
+        }
+      } else if constexpr (ROWT == PG_NF4) {
+        const float scale = __half2float(__ushort_as_half(static_cast<unsigned short>(aux[i])));
+        float x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float val = s_nf4[(v[i].x >> (4 * q)) & 15u] * scale;
+          x[q] = ((bits[i] >> q) & 1u) ? -val : val;
+        }
+        if constexpr (OUTT == PG_F32) {
+          uint8_t* dst = out_tok + cc * 32u;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                                                      __float_as_uint(x[2]), __float_as_uint(x[3]));
+          *reinterpret_cast<uint4*>(dst + 16) = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
+                                                           __float_as_uint(x[6]), __float_as_uint(x[7]));
+        } else {
+          *reinterpret_cast<uint4*>(out_tok + cc * 16u) =
+              make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                         pack_bf16(x[6], x[7]));
+        }
+      } else if constexpr (ROWT == PG_F32) {
+        *reinterpret_cast<uint4*>(out_tok + cc * 16u) = xor4(v[i], f32_sign_mask(bits[i]));
+      } else if constexpr (OUTT == PG_BF16) {
+        *reinterpret_cast<uint4*>(out_tok + cc * 16u) = xor4(v[i], bf16_sign_mask(bits[i]));
+      } else {
+        const uint4 f = xor4(v[i], bf16_sign_mask(bits[i]));
+        uint8_t* dst = out_tok + cc * 32u;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(f.x << 16, f.x & 0xFFFF0000u, f.y << 16, f.y & 0xFFFF0000u);
+        *reinterpret_cast<uint4*>(dst + 16) =
+            make_uint4(f.z << 16, f.z & 0xFFFF0000u, f.w << 16, f.w & 0xFFFF0000u);
       }
     }
     __syncwarp();
+    cur ^= 1;
   }
 }
 
-using GatherFn = void (*)(const HashParams, uint64_t, const int32_t*, int64_t, int64_t,
-                          const uint32_t*, const uint8_t*, uint32_t, uint32_t, uint32_t, uint8_t*,
-                          uint32_t, int32_t*);
+using GatherFn = void (*)(const HashParams, uint64_t, const GatherGeom, const int32_t*, const uint32_t*,
+                          const uint8_t*, uint8_t*, int32_t*);
 
-template <int ROWT, int OUTT, bool FLAT>
-GatherFn pick_nch(int nch) {
-  if (nch <= 2) return gather_kernel<ROWT, OUTT, FLAT, 2>;
-  if (nch <= 4) return gather_kernel<ROWT, OUTT, FLAT, 4>;
-  if (nch <= 8) return gather_kernel<ROWT, OUTT, FLAT, 8>;
-  if (nch <= 16) return gather_kernel<ROWT, OUTT, FLAT, 16>;
-  return nullptr;
-}
-
-GatherFn pick_gather(int row_dtype, int out_dtype, bool flat, int nch) {
+GatherFn pick_gather(int row_dtype, int out_dtype, bool flat) {
   if (flat) {
-    if (row_dtype == PG_F32 && out_dtype == PG_F32) return pick_nch<PG_F32, PG_F32, true>(nch);
-    if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return pick_nch<PG_BF16, PG_BF16, true>(nch);
-    if (row_dtype == PG_BF16 && out_dtype == PG_F32) return pick_nch<PG_BF16, PG_F32, true>(nch);
+    if (row_dtype == PG_F32 && out_dtype == PG_F32) return gather_kernel<PG_F32, PG_F32, true>;
+    if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return gather_kernel<PG_BF16, PG_BF16, true>;
+    if (row_dtype == PG_BF16 && out_dtype == PG_F32) return gather_kernel<PG_BF16, PG_F32, true>;
     return nullptr;
   }
-  if (row_dtype == PG_F32 && out_dtype == PG_F32) return pick_nch<PG_F32, PG_F32, false>(nch);
-  if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return pick_nch<PG_BF16, PG_BF16, false>(nch);
-  if (row_dtype == PG_BF16 && out_dtype == PG_F32) return pick_nch<PG_BF16, PG_F32, false>(nch);
-  if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return pick_nch<PG_NF4, PG_BF16, false>(nch);
-  if (row_dtype == PG_NF4 && out_dtype == PG_F32) return pick_nch<PG_NF4, PG_F32, false>(nch);
+  if (row_dtype == PG_F32 && out_dtype == PG_F32) return gather_kernel<PG_F32, PG_F32, false>;
+  if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return gather_kernel<PG_BF16, PG_BF16, false>;
+  if (row_dtype == PG_BF16 && out_dtype == PG_F32) return gather_kernel<PG_BF16, PG_F32, false>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_kernel<PG_NF4, PG_BF16, false>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_kernel<PG_NF4, PG_F32, false>;
   return nullptr;
 }
 
@@ -438,8 +458,8 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
                                 int32_t* err_index, pg_stream_t stream_) {
   using namespace pg;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  Geometry g;
-  pg_status st = validate_desc(desc, &g);
+  Geometry geo;
+  pg_status st = validate_desc(desc, &geo);
   if (st != PG_OK) return st;
   if (desc->hash_kind != PG_HASH_MULXOR) return PG_ERR_UNSUPPORTED;
   if (B < 0 || L < 0) return PG_ERR_SHAPE;
@@ -447,41 +467,59 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   if (N >= (1ll << 31)) return PG_ERR_SHAPE;
   if (N == 0) return PG_OK;
   if (!tokens || !table || !e_out) return PG_ERR_NULL;
-  if (table_bytes < g.rows * g.row_bytes) return PG_ERR_RANGE;
+  if (table_bytes < geo.rows * geo.row_bytes) return PG_ERR_RANGE;
   if (reinterpret_cast<uintptr_t>(table) % 16 || reinterpret_cast<uintptr_t>(e_out) % 16)
     return PG_ERR_ALIGN;
   if (out_dtype != PG_F32 && out_dtype != PG_BF16) return PG_ERR_DTYPE;
   const bool flat = desc->mode == PG_FLAT;
-  const int items = g.O * g.H;
-  if (items > kMaxItems || items * g.W > kMaxSignWords) return PG_ERR_UNSUPPORTED;
-  if (desc->row_dtype != PG_NF4 && g.row_bytes % 16) return PG_ERR_UNSUPPORTED;
-  uint32_t rc = desc->row_dtype == PG_NF4 ? 8u : g.row_bytes / 16u;
-  int nch;
-  if (flat) nch = (static_cast<int>(rc) + 31) / 32;
-  else nch = (items * static_cast<int>(rc) + 31) / 32;
-  GatherFn fn = pick_gather(desc->row_dtype, out_dtype, flat, nch);
+  const int items = geo.O * geo.H;
+  if (items > kMaxItems || items * geo.W > kMaxSignWords) return PG_ERR_UNSUPPORTED;
+  if (desc->row_dtype != PG_NF4 && geo.row_bytes % 16) return PG_ERR_UNSUPPORTED;
+  GatherFn fn = pick_gather(desc->row_dtype, out_dtype, flat);
   if (!fn) return desc->row_dtype == PG_F32 && out_dtype == PG_BF16 ? PG_ERR_DTYPE : PG_ERR_UNSUPPORTED;
-  const uint32_t out_size = out_dtype == PG_F32 ? 4u : 2u;
-  const uint32_t e_bytes = g.e_width * out_size;
-  // item = umulhi(chunk, magic) = floor(chunk / rc), exact while chunk * rc < 2^32
-  const uint32_t rc_magic = rc == 1u ? 0u : static_cast<uint32_t>((1ull << 32) / rc + 1ull);
+
+  GatherGeom g;
+  g.N = N;
+  g.L = static_cast<uint32_t>(L);
+  g.fm_L = fastmod_constant(g.L);
+  g.items = items;
+  g.W = geo.W;
+  g.rc = desc->row_dtype == PG_NF4 ? 8u : geo.row_bytes / 16u;
+  g.per_tok = flat ? static_cast<int>(g.rc) : items * static_cast<int>(g.rc);
+  if (g.per_tok < 2) return PG_ERR_UNSUPPORTED;  // 16-byte flat rows: no workload uses them
+  // a warp batch: tb tokens whose (token, item) pairs fit the 32 lanes and whose chunks
+  // fit 8 per lane
+  int tb = 32 * kChunksPerThread / g.per_tok;
+  if (tb > 32 / items) tb = 32 / items;
+  if (tb < 1) return PG_ERR_UNSUPPORTED;  // one token's row bytes exceed a batch
+  g.tb = tb;
+  // floor(x / n) = umulhi(x, floor(2^32 / n) + 1), exact while x * n < 2^32 (x < 2^11 here)
+  g.tok_magic = static_cast<uint32_t>((1ull << 32) / static_cast<uint32_t>(g.per_tok) + 1ull);
+  g.items_magic = static_cast<uint32_t>((1ull << 32) / static_cast<uint32_t>(items) + 1ull);
+  g.rc_magic = g.rc == 1u ? 0u : static_cast<uint32_t>((1ull << 32) / g.rc + 1ull);
+  g.row_bytes = geo.row_bytes;
+  g.e_bytes = geo.e_width * (out_dtype == PG_F32 ? 4u : 2u);
+  g.nbatch = (N + tb - 1) / tb;
+
   const int nsm = sm_count();
   if (nsm == 0) return cuda_fail(cudaGetLastError());
   st = prepare_err(err_index, stream);
   if (st != PG_OK) return st;
   HashParams P;
-  fill_hash_params(desc, g, &P);
+  fill_hash_params(desc, geo, &P);
+  if (tb * items * geo.W > kMaxSignWords) return PG_ERR_UNSUPPORTED;
+  const size_t dyn = 0;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, reinterpret_cast<const void*>(fn), kWarps * 32, 0);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(fn),
+                                                                kThreads, dyn);
   if (e != cudaSuccess) return cuda_fail(e);
   if (per_sm < 1) per_sm = 1;
-  const int64_t want = (N + kWarps - 1) / kWarps;
-  const int blocks = static_cast<int>(want < static_cast<int64_t>(nsm) * per_sm ? want
-                                                                              : static_cast<int64_t>(nsm) * per_sm);
-  fn<<<blocks, kWarps * 32, 0, stream>>>(P, desc->hash_seed, tokens, B, L, canon_map,
-                                         static_cast<const uint8_t*>(table), g.row_bytes, rc, rc_magic,
-                                         static_cast<uint8_t*>(e_out), e_bytes, err_index);
+  const int64_t cap = static_cast<int64_t>(nsm) * per_sm;
+  const int64_t want = (g.nbatch + kThreads / 32 - 1) / (kThreads / 32);
+  const int blocks = static_cast<int>(want < cap ? want : cap);
+  fn<<<blocks, kThreads, dyn, stream>>>(P, desc->hash_seed, g, tokens, canon_map,
+                                        static_cast<const uint8_t*>(table), static_cast<uint8_t*>(e_out),
+                                        err_index);
   return after_launch(1);
 }
 
