@@ -150,6 +150,29 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// TMA store of a 2-D box from shared memory (bulk group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until the committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format) for a K-major operand tile written
 // by TMA with 128-byte swizzle: rows of 64 bf16 (128 B), 8-row atoms of 1024 B.
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4 (unused here)
@@ -188,8 +211,11 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 w, float* f) {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 224;   // 7 warps: A/B producer, MMA, operand producer, 4 x epilogue
 constexpr int kABytes = kBM * kBK * 2;
+constexpr int kEpiCols = 32;        // columns per epilogue sub-tile
+constexpr int kEpiStages = 4;       // epilogue shared-memory ring
+constexpr int kEpiBytes = kBM * kEpiCols * 2;
 
 struct GemmArgs {
   int N;          // rows of e (tokens)
@@ -198,11 +224,8 @@ struct GemmArgs {
   int d;          // model width
   int M;          // branches (context gate)
   float g;        // scalar gate
-  const __nv_bfloat16* x;    // [N, d] residual (scalar gate)
-  const __nv_bfloat16* h;    // [M, N, d] branch states (context gate)
   const float* gamma_h;      // [d]
   const float* gamma_k;      // [d]
-  __nv_bfloat16* v_out;      // [N, d]
   float* partials;           // [M, d/BN, 3, N] (context gate)
   int* err_word;
 };
@@ -212,6 +235,9 @@ struct GemmBarriers {
   uint64_t empty[kStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t epi_full[kEpiStages];   // operand sub-tile landed (or slot handed over)
+  uint64_t epi_done[kEpiStages];   // all 128 epilogue threads finished with the slot
+  uint64_t epi_empty[kEpiStages];  // slot free again (its TMA store finished reading)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -219,22 +245,33 @@ struct GemmBarriers {
 
 template <int BN>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 /* alignment slack */ + kStages * (kABytes + BN * kBK * 2) + sizeof(GemmBarriers);
+  return 1024 /* alignment slack */ + kStages * (kABytes + BN * kBK * 2) + kEpiStages * kEpiBytes +
+         sizeof(GemmBarriers);
+}
+
+// Epilogue operands and results move through 128 x 32 bf16 sub-tiles (64 bytes per row)
+// written / read by TMA with 64-byte swizzle: 16-byte chunk c of row r sits at
+// r * 64 + ((c ^ ((r >> 1) & 3)) * 16), so the 32 rows of a warp hit every bank.
+__device__ __forceinline__ uint32_t epi_offset(int row, int chunk) {
+  return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
 template <int BN, int GATE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
+                   const __grid_constant__ CUtensorMap map_v, const GemmArgs args) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN);
   constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr int kSub = BN / kEpiCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  GemmBarriers* bars = reinterpret_cast<GemmBarriers*>(sB + kStages * kBBytes);
+  uint8_t* sE = sB + kStages * kBBytes;
+  GemmBarriers* bars = reinterpret_cast<GemmBarriers*>(sE + kEpiStages * kEpiBytes);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -248,6 +285,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&bars->tmem_full[a]), 1);
       mbar_init(smem_u32(&bars->tmem_empty[a]), 4 * 32);
+    }
+    for (int s = 0; s < kEpiStages; ++s) {
+      mbar_init(smem_u32(&bars->epi_full[s]), 1);
+      mbar_init(smem_u32(&bars->epi_done[s]), 4 * 32);
+      mbar_init(smem_u32(&bars->epi_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars->mma_done), 1);
     bars->abort = 0;
@@ -269,7 +311,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_kb = args.Din / kBK;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ A/B TMA producer
     if (lane == 0) {
       tma_prefetch_map(&map_a);
       tma_prefetch_map(&map_b);
@@ -355,100 +397,154 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       while (!mbar_try_wait(smem_u32(&bars->mma_done), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ epilogue operand producer
+    if (lane == 0) {
+      if (GATE == PG_GATE_SCALAR) tma_prefetch_map(&map_x);
+      if (GATE == PG_GATE_CONTEXT) tma_prefetch_map(&map_h);
+      uint32_t seq = 0;
+      bool ok = true;
+      uint32_t issued = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
+        const int n0 = n_blk * BN, m0 = m_blk * kBM;
+        const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
+        for (int j = 0; j < kSub; ++j, ++seq) {
+          const int slot = static_cast<int>(seq % kEpiStages);
+          const uint32_t ph = (seq / kEpiStages) & 1u;
+          if (!mbar_wait(smem_u32(&bars->epi_empty[slot]), ph ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bars->epi_full[slot]);
+          const uint32_t dst = smem_u32(sE + slot * kEpiBytes);
+          if (GATE == PG_GATE_SCALAR) {
+            mbar_expect_tx(full, kEpiBytes);
+            tma_load_2d(dst, &map_x, full, n0 + j * kEpiCols, m0);
+            issued |= 1u << slot;
+          } else if (is_k) {
+            const int m = n0 / args.d - 1;
+            const int kc = n0 - (m + 1) * args.d;
+            mbar_expect_tx(full, kEpiBytes);
+            tma_load_2d(dst, &map_h, full, kc + j * kEpiCols, m * args.N + m0);
+            issued |= 1u << slot;
+          } else {
+            mbar_arrive(full);   // output staging only: hand the free slot over
+          }
+        }
+      }
+      if (!ok) {
+        atomicOr(args.err_word, 8);
+        *abort = 1;
+        for (int s = 0; s < kEpiStages; ++s)
+          if (issued & (1u << s)) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < kWaitLimitNs / 4 &&
+                   !mbar_try_wait(smem_u32(&bars->epi_full[s]), ((seq - 1 - ((seq - 1 - s) % kEpiStages)) / kEpiStages) & 1u)) {
+            }
+          }
+      }
+    }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 3..6)
+    const int epi = threadIdx.x - 3 * 32;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t seq = 0;
     bool ok = true;
     const int tpb = args.d / BN;  // tiles per branch (context gate)
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
       if (!mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int row = m_blk * kBM + row_in_tile;
+      const int m0 = m_blk * kBM;
+      const int row = m0 + row_in_tile;
       const bool live = row < args.N;
       const int n0 = n_blk * BN;
-      const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                              static_cast<uint32_t>(acc * BN);
-      if (GATE != PG_GATE_CONTEXT || n0 < args.d) {
-        // v (or x + g v) columns [n0, n0 + BN) of this row
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(t_base + c, r);
-          tmem_ld_wait();
-          if (live) {
-            const size_t off = static_cast<size_t>(row) * args.d + n0 + c;
-            uint4* dst = reinterpret_cast<uint4*>(args.v_out + off);
+      const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
+      const int m_br = is_k ? n0 / args.d - 1 : 0;
+      const int kc = is_k ? n0 - (m_br + 1) * args.d : 0;
+      const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
+      for (int j = 0; j < kSub; ++j, ++seq) {
+        const int slot = static_cast<int>(seq % kEpiStages);
+        const uint32_t ph = (seq / kEpiStages) & 1u;
+        if (!mbar_wait(smem_u32(&bars->epi_full[slot]), ph, abort)) {
+          ok = false;
+          break;
+        }
+        uint32_t r[32];
+        tmem_ld32(t_base + static_cast<uint32_t>(j * kEpiCols), r);
+        tmem_ld_wait();
+        uint8_t* slot_p = sE + slot * kEpiBytes;
+        if (is_k) {
+          const float4* gh = reinterpret_cast<const float4*>(args.gamma_h + kc + j * kEpiCols);
+          const float4* gk = reinterpret_cast<const float4*>(args.gamma_k + kc + j * kEpiCols);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float hf[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_p + epi_offset(row_in_tile, c)), hf);
+            const float4 gh0 = __ldg(gh + 2 * c), gh1 = __ldg(gh + 2 * c + 1);
+            const float4 gk0 = __ldg(gk + 2 * c), gk1 = __ldg(gk + 2 * c + 1);
+            const float ghv[8] = {gh0.x, gh0.y, gh0.z, gh0.w, gh1.x, gh1.y, gh1.z, gh1.w};
+            const float gkv[8] = {gk0.x, gk0.y, gk0.z, gk0.w, gk1.x, gk1.y, gk1.z, gk1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float kv = __uint_as_float(r[8 * c + i]);
+              s_kk = fmaf(kv, kv, s_kk);
+              s_hh = fmaf(hf[i], hf[i], s_hh);
+              s_hk = fmaf(ghv[i] * gkv[i] * hf[i], kv, s_hk);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4* p = reinterpret_cast<uint4*>(slot_p + epi_offset(row_in_tile, c));
+            float o[8];
             if (GATE == PG_GATE_SCALAR) {
-              const uint4* xs = reinterpret_cast<const uint4*>(args.x + off);
+              float xf[8];
+              unpack_bf16x8(*p, xf);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                float xf[8];
-                unpack_bf16x8(__ldg(xs + q), xf);
-                float o[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = fmaf(args.g, __uint_as_float(r[8 * q + i]), xf[i]);
-                dst[q] = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                                    pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
-              }
+              for (int i = 0; i < 8; ++i) o[i] = fmaf(args.g, __uint_as_float(r[8 * c + i]), xf[i]);
             } else {
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(
-                    pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
-                    pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                    pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                    pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+              for (int i = 0; i < 8; ++i) o[i] = __uint_as_float(r[8 * c + i]);
             }
+            *p = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+                            pack_bf16(o[6], o[7]));
           }
+          fence_proxy_async_smem();
         }
-      } else {
-        // k^(m) columns: per-row partial sums for the gate of branch m
-        const int m = n0 / args.d - 1;
-        const int kc = n0 - (m + 1) * args.d;  // column inside the branch
-        const int tb = kc / BN;
-        float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
-        const __nv_bfloat16* hrow = args.h + (static_cast<size_t>(m) * args.N + (live ? row : 0)) * args.d;
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(t_base + c, r);
-          tmem_ld_wait();
-          if (live) {
-            const uint4* hs = reinterpret_cast<const uint4*>(hrow + kc + c);
-            const float4* gh = reinterpret_cast<const float4*>(args.gamma_h + kc + c);
-            const float4* gk = reinterpret_cast<const float4*>(args.gamma_k + kc + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float hf[8];
-              unpack_bf16x8(__ldg(hs + q), hf);
-              const float4 gh0 = __ldg(gh + 2 * q), gh1 = __ldg(gh + 2 * q + 1);
-              const float4 gk0 = __ldg(gk + 2 * q), gk1 = __ldg(gk + 2 * q + 1);
-              const float ghv[8] = {gh0.x, gh0.y, gh0.z, gh0.w, gh1.x, gh1.y, gh1.z, gh1.w};
-              const float gkv[8] = {gk0.x, gk0.y, gk0.z, gk0.w, gk1.x, gk1.y, gk1.z, gk1.w};
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float kv = __uint_as_float(r[8 * q + i]);
-                s_kk = fmaf(kv, kv, s_kk);
-                s_hh = fmaf(hf[i], hf[i], s_hh);
-                s_hk = fmaf(ghv[i] * gkv[i] * hf[i], kv, s_hk);
-              }
-            }
+        mbar_arrive(smem_u32(&bars->epi_done[slot]));
+        if (epi == 0) {
+          // the slot goes back to the producer once every thread is done with it and,
+          // for outputs, once its TMA store has read it
+          if (!mbar_wait(smem_u32(&bars->epi_done[slot]), ph, abort)) {
+            ok = false;
+            break;
           }
-        }
-        if (live) {
-          float* p = args.partials + (static_cast<size_t>(m * tpb + tb) * 3) * args.N + row;
-          p[0] = s_hk;
-          p[args.N] = s_kk;
-          p[2 * static_cast<size_t>(args.N)] = s_hh;
+          if (!is_k) {
+            tma_store_2d(&map_v, smem_u32(slot_p), n0 + j * kEpiCols, m0);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(smem_u32(&bars->epi_empty[slot]));
         }
       }
+      if (!ok) break;
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
+      if (is_k && live) {
+        float* p = args.partials + (static_cast<size_t>(m_br * tpb + kc / BN) * 3) * args.N + row;
+        p[0] = s_hk;
+        p[args.N] = s_kk;
+        p[2 * static_cast<size_t>(args.N)] = s_hh;
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -456,6 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       atomicOr(args.err_word, 4);
       *abort = 1;
     }
+    if (epi == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -590,24 +687,43 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (row-major), box [box_rows, 64] with 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D bf16 tensor [rows, cols] (row-major), box [box_rows, box_cols].
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+struct GemmPtrs {
+  const void* e;
+  const void* W;
+  const void* x;
+  const void* h;
+  void* v;
+};
+
 template <int BN, int GATE>
-pg_status launch_tc(const void* e, const void* W, const GemmArgs& a, cudaStream_t stream) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, e, a.N, a.Din, kBM) || !make_map(&mb, W, a.Dcols, a.Din, BN))
+pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream) {
+  CUtensorMap ma, mb, mx, mh, mv;
+  if (!make_map(&ma, ptr.e, a.N, a.Din, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mb, ptr.W, a.Dcols, a.Din, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mv, ptr.v, a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
+    return PG_ERR_UNSUPPORTED;
+  // operand maps that a gate does not use alias the output map (never read)
+  mx = mv;
+  mh = mv;
+  if (GATE == PG_GATE_SCALAR && !make_map(&mx, ptr.x, a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
+    return PG_ERR_UNSUPPORTED;
+  if (GATE == PG_GATE_CONTEXT &&
+      !make_map(&mh, ptr.h, static_cast<uint64_t>(a.M) * a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
   auto kern = tc_gemm_kernel<BN, GATE>;
   const size_t smem = gemm_smem_bytes<BN>();
@@ -616,15 +732,15 @@ pg_status launch_tc(const void* e, const void* W, const GemmArgs& a, cudaStream_
   if (err != cudaSuccess) return cuda_fail(err);
   const int tiles = ((a.N + kBM - 1) / kBM) * (a.Dcols / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  kern<<<grid, kGemmThreads, smem, stream>>>(ma, mb, a);
+  kern<<<grid, kGemmThreads, smem, stream>>>(ma, mb, mx, mh, mv, a);
   return after_launch(1);
 }
 
 template <int BN>
-pg_status dispatch_tc(int gate, const void* e, const void* W, const GemmArgs& a, cudaStream_t stream) {
-  if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE>(e, W, a, stream);
-  if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR>(e, W, a, stream);
-  return launch_tc<BN, PG_GATE_CONTEXT>(e, W, a, stream);
+pg_status dispatch_tc(int gate, const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream) {
+  if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE>(ptr, a, stream);
+  if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR>(ptr, a, stream);
+  return launch_tc<BN, PG_GATE_CONTEXT>(ptr, a, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -711,12 +827,11 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   a.d = d;
   a.M = M;
   a.g = g;
-  a.x = static_cast<const __nv_bfloat16*>(x_resid);
-  a.h = static_cast<const __nv_bfloat16*>(h);
   a.gamma_h = gamma_h;
   a.gamma_k = gamma_k;
-  a.v_out = static_cast<__nv_bfloat16*>(v_out);
   a.partials = static_cast<float*>(workspace);
+  if (gate_kind == PG_GATE_CONTEXT && static_cast<int64_t>(M) * N >= (1ll << 31)) return PG_ERR_SHAPE;
+  const GemmPtrs ptrs{e, W, x_resid, h, v_out};
   a.err_word = device_error_word();
   if (!a.err_word) return cuda_fail(cudaGetLastError());
   if (gate_kind == PG_GATE_CONTEXT) {
@@ -725,8 +840,8 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
     if (!workspace || workspace_bytes < need) return PG_ERR_WORKSPACE;
     if (!aligned16(workspace) || !aligned16(gamma_h) || !aligned16(gamma_k)) return PG_ERR_ALIGN;
   }
-  pg_status st = bn == 256 ? dispatch_tc<256>(gate_kind, e, W, a, stream)
-                           : dispatch_tc<128>(gate_kind, e, W, a, stream);
+  pg_status st = bn == 256 ? dispatch_tc<256>(gate_kind, ptrs, a, stream)
+                           : dispatch_tc<128>(gate_kind, ptrs, a, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
   const int64_t total = static_cast<int64_t>(M) * N;
   alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
