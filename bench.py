@@ -6,7 +6,8 @@
 A step is one pass of the whole lookup over one batch of the workload (default:
 the PageGram 200M-parameter bf16 table, 64 x 1024 Zipf(1.1) tokens): canonical IDs,
 n-grams, hashes and rows, gather + sign + concat (pg_gather_sign_concat), then the
-W_V projection with the scalar gate x + g v (pg_project_gate, tcgen05). With
+W_V projection with the scalar gate x + g v (pg_project_gate, tcgen05); --path fused
+runs both in one kernel (pg_lookup_project_gate) and the other path is timed too. With
 --config 5 the step is the Engram-27B-shaped module (gather, fused W_V + 4 W_K with
 the RMSNorm-sigmoid gate, causal conv + residual).
 
@@ -183,8 +184,25 @@ class Pipeline:
         pg.conv_residual(w.B, w.L, self.d, w.M, pg.BF16, self.v, self.alpha, dn["gamma_c"], dn["conv_w"], dn["H"],
                          dilation=w.dilation, eps=w.eps)
 
-    def stages(self):
-        st = [("gather_sign_concat", self.gather), ("project_gate", self.project)]
+    def fused(self):
+        pg, w, dn = self.pg, self.w, self.dn
+        if w.gate == self.W.GATE_SCALAR:
+            pg.lookup_project_gate(self.desc, self.tokens, self.table, dn["W"], self.d, pg.GATE_SCALAR, self.out,
+                                   canon_map=self.cmap, g=w.g, x_resid=dn["x"])
+        else:
+            pg.lookup_project_gate(self.desc, self.tokens, self.table, dn["W"], self.d, pg.GATE_CONTEXT, self.v,
+                                   canon_map=self.cmap, M=w.M, h=dn["H"], gamma_h=dn["gamma_h"],
+                                   gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=self.alpha, workspace=self.ws)
+
+    def can_fuse(self):
+        sp = self.spec
+        return sp.mode != self.W.MODE_FLAT and sp.row_dtype == self.W.DT_BF16 and sp.r == 64
+
+    def stages(self, fused=True):
+        if fused and self.can_fuse():
+            st = [("lookup_project_gate", self.fused)]
+        else:
+            st = [("gather_sign_concat", self.gather), ("project_gate", self.project)]
         if self.w.gate == self.W.GATE_CONTEXT:
             st.append(("conv_residual", self.conv))
         return st
@@ -200,7 +218,7 @@ class Pipeline:
             rb = self.spec.row_bytes if self.spec.row_dtype != self.W.DT_NF4 else 64
             per = len(self.spec.orders) * self.spec.K * rb + 4 + din * 2
             return "hbm", per * N
-        if name == "project_gate":
+        if name in ("project_gate", "lookup_project_gate"):
             cols = d * (1 + w.M)
             return "tensor", 2.0 * N * din * cols
         # conv: read v, read + write H for every branch
@@ -228,6 +246,20 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def time_stages(stages, steps, stream, flush):
+    """CUDA-event durations (ms) of every stage of `steps` steps; L2 flushed between steps."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn()
+            ev[i][j + 1].record(stream)
+        flush_l2(flush)
+    torch.cuda.synchronize()
+    return [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)] for j in range(len(stages))]
+
+
 def run_gpu(args):
     import torch
 
@@ -242,7 +274,7 @@ def run_gpu(args):
     p = Pipeline(args.config, dev, rank)
     stream = torch.cuda.current_stream()
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    stages = p.stages()
+    stages = p.stages(fused=args.path == "fused")
 
     # ---- warm-up
     for _ in range(args.warmup):
@@ -255,23 +287,15 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     # ---- device-timed loop: events around every stage of every step, L2 flushed between steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     launches0 = pg.launch_count()
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t_wall = time.perf_counter()
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            for j, (_, fn) in enumerate(stages):
-                fn()
-                ev[i][j + 1].record(stream)
-            flush_l2(flush)
-        torch.cuda.synchronize()
+        stage_ms = time_stages(stages, args.steps, stream, flush)
         t_wall = time.perf_counter() - t_wall
     barrier(world)
     launches = pg.launch_count() - launches0
-    stage_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(len(stages))]
     step_ms = [sum(stage_ms[j][i] for j in range(len(stages))) for i in range(args.steps)]
     total_s = reduce_max(sum(step_ms) / 1e3, world)
     value = whole_job_rate(p.N * args.steps, world, total_s)
@@ -324,9 +348,26 @@ def run_gpu(args):
             kernels[name] = {"ms": round(ms, 5), "TFLOP/s": round(wk / (ms / 1e3) / 1e12, 1),
                              "frac_tensor": round(wk / (ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]), 4)}
     comp = compulsory_gather_bytes(p)
-    g_ms = means["gather_sign_concat"]
-    kernels["gather_sign_concat"]["compulsory_bytes"] = comp
-    kernels["gather_sign_concat"]["frac_hbm_compulsory"] = round(comp / (g_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+    if "gather_sign_concat" in means:
+        g_ms = means["gather_sign_concat"]
+        kernels["gather_sign_concat"]["compulsory_bytes"] = comp
+        kernels["gather_sign_concat"]["frac_hbm_compulsory"] = round(
+            comp / (g_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+    if "lookup_project_gate" in means:
+        # e_t never reaches memory: table sectors + IDs + the epilogue operand in + the output
+        fb = comp - p.N * p.din * 2 + p.N * p.d * 2 * (2 if p.w.gate == p.W.GATE_SCALAR else 1 + 2 * p.w.M)
+        f_ms = means["lookup_project_gate"]
+        kernels["lookup_project_gate"]["compulsory_bytes"] = fb
+        kernels["lookup_project_gate"]["GB/s_compulsory"] = round(fb / (f_ms / 1e3) / 1e9, 1)
+        kernels["lookup_project_gate"]["frac_hbm_compulsory"] = round(
+            fb / (f_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+    other = None
+    if p.can_fuse():
+        ost = p.stages(fused=args.path != "fused")
+        o_ms = time_stages(ost, max(3, args.steps // 4), stream, flush)
+        other = {"path": "fused" if args.path != "fused" else "two_kernel",
+                 "ms_per_step": round(sum(statistics.mean(x) for x in o_ms), 5),
+                 "kernels": {name: round(statistics.mean(o_ms[j]), 5) for j, (name, _) in enumerate(ost)}}
 
     clocks = clk.summary()
     if rank == 0:
@@ -343,6 +384,8 @@ def run_gpu(args):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})"},
             "kernels": kernels,
+            "path": args.path if p.can_fuse() else "two_kernel",
+            "other_path": other,
             "clocks": clocks,
             "wall_s_timed_loop": round(t_wall, 4),
         }
@@ -505,6 +548,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 5])
+    ap.add_argument("--path", choices=["two_kernel", "fused"], default="two_kernel",
+                    help="two_kernel: pg_gather_sign_concat + pg_project_gate; fused: pg_lookup_project_gate "
+                         "(r = 64 bf16 tables); the other one is timed too and reported as other_path")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -16,7 +16,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "pg_internal.cuh"
+#include "pg_hash.cuh"
 
 namespace pg {
 namespace {
@@ -29,25 +29,8 @@ __constant__ uint32_t c_nf4_bits[16] = {
     0xbdba7869u, 0x00000000u, 0x3da2fb01u, 0x3e24cadfu, 0x3e7c04dau, 0x3ead0336u,
     0x3ee1a4b5u, 0x3f1007a9u, 0x3f3913b0u, 0x3f800000u};
 
-__device__ __forceinline__ uint32_t fold32(uint64_t h) { return static_cast<uint32_t>(h ^ (h >> 32)); }
 
-__device__ __forceinline__ uint64_t multiplier(uint64_t seed, int kind, int o, int k, int j) {
-  const uint64_t fid = static_cast<uint64_t>(((kind * 4 + o) * 64 + k) * 4 + j);
-  return mix64(seed + kGolden * (1ull + fid)) | 1ull;
-}
 
-// Reads the canonical ID of token `src` (flat index); out-of-range IDs are reported
-// through err (smallest flat index wins) and read as ID 0.
-__device__ __forceinline__ uint32_t canon_token(const int32_t* __restrict__ tokens,
-                                                const uint32_t* __restrict__ canon_map,
-                                                uint32_t vocab, int64_t src, int32_t* err) {
-  int32_t x = __ldg(tokens + src);
-  if (x < 0 || static_cast<uint32_t>(x) >= vocab) {
-    if (err) atomicMin(reinterpret_cast<unsigned int*>(err), static_cast<unsigned int>(src));
-    x = 0;
-  }
-  return canon_map ? __ldg(canon_map + x) : static_cast<uint32_t>(x);
-}
 
 // Row of item (o, k) from its head (and page) hash; `hh` = H of the head hash,
 // `hp` = H of the page hash (PageGram only).
@@ -115,27 +98,7 @@ constexpr int kChunksPerThread = 8; // 16-byte chunks (or NF4 tasks) per lane pe
 constexpr int kMaxItems = 32;       // (order, head) items per token
 constexpr int kMaxSignWords = 128;  // items * sign words per token
 
-// Remainder by direct computation (Lemire, Kaser & Kurz, "Faster remainder by direct
-// computation", Software: Practice and Experience 2019): with c = ceil(2^64 / d),
-// a mod d = floor(((c * a) mod 2^64) * d / 2^64), exact for all 32-bit a and d >= 1
-// (d = 1 gives c = 0 and the remainder 0).
-__host__ __device__ __forceinline__ uint64_t fastmod_constant(uint32_t d) { return ~0ull / d + 1ull; }
 
-__device__ __forceinline__ uint32_t fastmod(uint32_t a, uint64_t c, uint32_t d) {
-  return static_cast<uint32_t>(__umul64hi(c * a, d));
-}
-
-// Per-item constants in shared memory.
-struct ItemConst {
-  uint64_t mp[4], mh[4], ms[4];  // multipliers: page hash, head hash, sign hash
-  uint64_t fm_main, fm_slot;     // fastmod constants of div_main and S
-  uint32_t div_main;             // P_n (PageGram), M_{n,k} (Engram), R_n (flat)
-  uint32_t slots;                // S (PageGram), 1 otherwise
-  uint32_t stride;               // K * S (PageGram)
-  uint32_t base;                 // row of (page 0, head k, slot 0) / subtable start
-  int32_t n;                     // n-gram order
-  int32_t pad;
-};
 
 struct GatherGeom {
   int64_t N;            // tokens
@@ -168,24 +131,12 @@ __device__ __forceinline__ uint16_t ldg_u16(const void* ptr) {
   return v;
 }
 
-// XOR masks that negate 8 packed bf16 (two per 32-bit word) from 8 sign bits.
-__device__ __forceinline__ uint4 bf16_sign_mask(uint32_t bits) {
-  uint4 m;
-  m.x = ((bits & 1u) << 15) | ((bits & 2u) << 30);
-  m.y = ((bits & 4u) << 13) | ((bits & 8u) << 28);
-  m.z = ((bits & 16u) << 11) | ((bits & 32u) << 26);
-  m.w = ((bits & 64u) << 9) | ((bits & 128u) << 24);
-  return m;
-}
 
 // XOR masks that negate 4 fp32 from 4 sign bits.
 __device__ __forceinline__ uint4 f32_sign_mask(uint32_t bits) {
   return make_uint4((bits & 1u) << 31, (bits & 2u) << 30, (bits & 4u) << 29, (bits & 8u) << 28);
 }
 
-__device__ __forceinline__ uint4 xor4(uint4 a, uint4 b) {
-  return make_uint4(a.x ^ b.x, a.y ^ b.y, a.z ^ b.z, a.w ^ b.w);
-}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -206,25 +157,9 @@ __device__ __forceinline__ void hash_batch(const ItemConst* __restrict__ ic, con
   const int item = p - s * g.items;
   const int64_t tok = batch * g.tb + s;
   if (tok >= g.N) return;
-  const ItemConst& it = ic[item];
   const uint32_t t = fastmod(static_cast<uint32_t>(tok), g.fm_L, g.L);
-  uint64_t hp = 0, hh = 0, hs = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j < it.n) {
-      const uint64_t c = (t >= static_cast<uint32_t>(j)) ? canon_token(tokens, canon_map, vocab, tok - j, err) : kPad;
-      hp ^= c * it.mp[j];
-      hh ^= c * it.mh[j];
-      hs ^= c * it.ms[j];
-    }
-  }
-  uint32_t row;
-  if (mode == PG_PAGEGRAM)
-    row = it.base + fastmod(fold32(hp), it.fm_main, it.div_main) * it.stride +
-          fastmod(fold32(hh), it.fm_slot, it.slots);
-  else
-    row = it.base + fastmod(fold32(hh), it.fm_main, it.div_main);
-  s_rows[p] = row;
+  uint64_t hs;
+  s_rows[p] = item_row(ic[item], mode, tokens, canon_map, vocab, tok, t, err, &hs);
   for (int q = 0; q < g.W; ++q) s_signs[p * g.W + q] = mix64(hs + kGolden * static_cast<uint64_t>(q + 1));
 }
 
@@ -243,26 +178,7 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
 
-  // Per-item constants: multipliers (from the seed), divisors, fastmod constants.
-  if (threadIdx.x < g.items) {
-    const int item = threadIdx.x;
-    const int o = item / P.H, k = item - o * P.H;
-    ItemConst& it = s_ic[item];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      it.mp[j] = multiplier(seed, 0, o, 0, j);
-      it.mh[j] = multiplier(seed, 1, o, k, j);
-      it.ms[j] = multiplier(seed, 2, o, k, j);
-    }
-    const bool paged = P.mode == PG_PAGEGRAM;
-    it.div_main = paged ? P.divisor[o][0] : P.divisor[o][P.mode == PG_ENGRAM ? k : 0];
-    it.slots = paged ? static_cast<uint32_t>(P.S) : 1u;
-    it.stride = paged ? static_cast<uint32_t>(P.K * P.S) : 0u;
-    it.base = paged ? P.base[o][0] + static_cast<uint32_t>(k * P.S) : P.base[o][P.mode == PG_ENGRAM ? k : 0];
-    it.fm_main = fastmod_constant(it.div_main);
-    it.fm_slot = fastmod_constant(it.slots);
-    it.n = P.order_n[o];
-  }
+  if (threadIdx.x < g.items) init_item_const(s_ic[threadIdx.x], P, seed, threadIdx.x);
   if (ROWT == PG_NF4 && threadIdx.x < 16) s_nf4[threadIdx.x] = __uint_as_float(c_nf4_bits[threadIdx.x]);
   __syncthreads();
 

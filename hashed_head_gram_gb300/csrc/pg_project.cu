@@ -21,7 +21,7 @@
 
 #include <mutex>
 
-#include "pg_internal.cuh"
+#include "pg_hash.cuh"
 
 namespace pg {
 namespace {
@@ -212,10 +212,37 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kGemmThreads = 224;   // 7 warps: A/B producer, MMA, operand producer, 4 x epilogue
+constexpr int kFusedThreads = 480;  // + 8 gather warps producing the A operand
+constexpr int kGatherWarp0 = 7;
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kEpiCols = 32;        // columns per epilogue sub-tile
-constexpr int kEpiStages = 4;       // epilogue shared-memory ring
+constexpr int kEpiStagesMax = 4;    // epilogue shared-memory ring (3 slots in the fused kernel)
 constexpr int kEpiBytes = kBM * kEpiCols * 2;
+constexpr int kFusedItems = 32;     // (order, head) items of the fused kernel
+
+template <bool GATHER>
+__host__ __device__ constexpr int epi_stages() { return GATHER ? 3 : 4; }
+
+// What the gather warps of the fused kernel need (empty in the plain GEMM).
+struct FusedGather {
+  HashParams P;
+  uint64_t seed;
+  const int32_t* tokens;
+  const uint32_t* canon_map;
+  const uint8_t* table;
+  uint32_t L;
+  uint64_t fm_L;
+  int32_t* err;
+};
+struct NoGather {};
+template <bool GATHER>
+struct GatherParam {
+  using type = NoGather;
+};
+template <>
+struct GatherParam<true> {
+  using type = FusedGather;
+};
 
 struct GemmArgs {
   int N;          // rows of e (tokens)
@@ -235,18 +262,18 @@ struct GemmBarriers {
   uint64_t empty[kStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
-  uint64_t epi_full[kEpiStages];   // operand sub-tile landed (or slot handed over)
-  uint64_t epi_done[kEpiStages];   // all 128 epilogue threads finished with the slot
-  uint64_t epi_empty[kEpiStages];  // slot free again (its TMA store finished reading)
+  uint64_t epi_full[kEpiStagesMax];   // operand sub-tile landed (or slot handed over)
+  uint64_t epi_done[kEpiStagesMax];   // all 128 epilogue threads finished with the slot
+  uint64_t epi_empty[kEpiStagesMax];  // slot free again (its TMA store finished reading)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
-template <int BN>
+template <int BN, bool GATHER>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 /* alignment slack */ + kStages * (kABytes + BN * kBK * 2) + kEpiStages * kEpiBytes +
-         sizeof(GemmBarriers);
+  return 1024 /* alignment slack */ + kStages * (kABytes + BN * kBK * 2) + epi_stages<GATHER>() * kEpiBytes +
+         sizeof(GemmBarriers) + (GATHER ? kFusedItems * sizeof(ItemConst) : 0);
 }
 
 // Epilogue operands and results move through 128 x 32 bf16 sub-tiles (64 bytes per row)
@@ -256,11 +283,16 @@ __device__ __forceinline__ uint32_t epi_offset(int row, int chunk) {
   return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
-template <int BN, int GATE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// GATHER: the A operand (e_t) is not read from global memory; 8 gather warps build each
+// 128 x 64 A tile in shared memory from the table (k-block kb = head (o, k) of r = 64),
+// exactly as pg_gather_sign_concat would have written it.
+template <int BN, int GATE, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
-                   const __grid_constant__ CUtensorMap map_v, const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap map_v, const GemmArgs args,
+                   const __grid_constant__ typename GatherParam<GATHER>::type gat) {
+  constexpr int kEpiStages = epi_stages<GATHER>();
   constexpr int kBBytes = BN * kBK * 2;
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN);
   constexpr uint32_t kTmemCols = 2 * BN;
@@ -272,6 +304,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sB = smem + kStages * kABytes;
   uint8_t* sE = sB + kStages * kBBytes;
   GemmBarriers* bars = reinterpret_cast<GemmBarriers*>(sE + kEpiStages * kEpiBytes);
+  ItemConst* s_ic = reinterpret_cast<ItemConst*>(bars + 1);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -279,7 +312,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->full[s]), 1);
+      // the TMA expect-tx arrival, plus the 64 gather threads that build the A tile
+      mbar_init(smem_u32(&bars->full[s]), GATHER ? 1 + 64 : 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -300,6 +334,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  if constexpr (GATHER) {
+    if (threadIdx.x >= 32 * kGatherWarp0 && threadIdx.x - 32 * kGatherWarp0 < gat.P.O * gat.P.H)
+      init_item_const(s_ic[threadIdx.x - 32 * kGatherWarp0], gat.P, gat.seed, threadIdx.x - 32 * kGatherWarp0);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -313,7 +351,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ A/B TMA producer
     if (lane == 0) {
-      tma_prefetch_map(&map_a);
+      if (!GATHER) tma_prefetch_map(&map_a);
       tma_prefetch_map(&map_b);
       int stage = 0;
       uint32_t phase = 0;
@@ -327,8 +365,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const uint32_t full = smem_u32(&bars->full[stage]);
-          mbar_expect_tx(full, kABytes + kBBytes);
-          tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
+          mbar_expect_tx(full, GATHER ? kBBytes : kABytes + kBBytes);
+          if (!GATHER) tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
           tma_load_2d(smem_u32(sB + stage * kBBytes), &map_b, full, kb * kBK, n_blk * BN);
           issued |= 1u << stage;
           if (++stage == kStages) {
@@ -443,6 +481,95 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    !mbar_try_wait(smem_u32(&bars->epi_full[s]), ((seq - 1 - ((seq - 1 - s) % kEpiStages)) / kEpiStages) & 1u)) {
             }
           }
+      }
+    }
+  } else if (GATHER && warp >= kGatherWarp0) {
+    if constexpr (GATHER) {
+      // ---------------------------------------------------------- A-operand gather (warps 7..14)
+      // Pair p of warps builds every A tile of ring stage p; warp `half` of the pair covers
+      // tokens [64 half, 64 half + 64) of the 128-token block. Lane l hashes tokens l and
+      // l + 32 of its half for head kb, then 8 lanes per row move 16-byte chunks: chunk
+      // (token, piece) -> A-tile row `token`, physical chunk piece ^ (row & 7) (128-byte
+      // swizzle, the layout the TMA would have written).
+      const int gw = warp - kGatherWarp0;
+      const int pair = gw >> 1, half = gw & 1;
+      const int piece = lane & 7, sub = lane >> 3;
+      const int stage = pair;
+      // rows and sign words of tokens (64 half + lane) and (+32) of one k-block
+      auto hash_rows = [&](int tile, int kb, uint32_t& ra, uint32_t& rb, uint64_t& sa, uint64_t& sb) {
+        const int m0 = (tile / num_n) * kBM;
+        const ItemConst& it = s_ic[kb];
+        const int64_t ta = static_cast<int64_t>(m0) + 64 * half + lane, tb = ta + 32;
+        uint64_t hs;
+        ra = rb = 0;
+        sa = sb = 0;
+        if (ta < args.N) {
+          ra = item_row(it, gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, ta,
+                        fastmod(static_cast<uint32_t>(ta), gat.fm_L, gat.L), gat.err, &hs);
+          sa = mix64(hs + kGolden);
+        }
+        if (tb < args.N) {
+          rb = item_row(it, gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, tb,
+                        fastmod(static_cast<uint32_t>(tb), gat.fm_L, gat.L), gat.err, &hs);
+          sb = mix64(hs + kGolden);
+        }
+      };
+      // this pair's k-blocks: sequence numbers q = pair, pair + 4, ... over the CTA's tiles
+      int tile = blockIdx.x, kb = pair;
+      while (kb >= num_kb && tile < num_tiles) {
+        kb -= num_kb;
+        tile += gridDim.x;
+      }
+      uint32_t q = pair;
+      uint32_t ra, rb;
+      uint64_t sa, sb;
+      if (tile < num_tiles) hash_rows(tile, kb, ra, rb, sa, sb);
+      bool ok = true;
+      while (tile < num_tiles) {
+        // 1. loads of this k-block (they do not need the stage to be free)
+        uint4 v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int src = 4 * (i & 7) + sub;
+          const uint32_t r = __shfl_sync(0xffffffffu, i < 8 ? ra : rb, src);
+          v[i] = __ldg(reinterpret_cast<const uint4*>(gat.table + static_cast<uint64_t>(r) * 128u + piece * 16));
+        }
+        // 2. hash the next k-block of this pair while the loads are in flight
+        int ntile = tile, nkb = kb + 4;
+        while (nkb >= num_kb && ntile < num_tiles) {
+          nkb -= num_kb;
+          ntile += gridDim.x;
+        }
+        uint32_t na = 0, nb = 0;
+        uint64_t nsa = 0, nsb = 0;
+        if (ntile < num_tiles) hash_rows(ntile, nkb, na, nb, nsa, nsb);
+        // 3. wait for the stage, then sign-flip and store into the swizzled A tile
+        if (!mbar_wait(smem_u32(&bars->empty[stage]), ((q >> 2) & 1u) ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_tile = sA + stage * kABytes;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int src = 4 * (i & 7) + sub;
+          const uint64_t sw = __shfl_sync(0xffffffffu, i < 8 ? sa : sb, src);
+          const uint32_t bits = static_cast<uint32_t>(sw >> (8 * piece)) & 0xFFu;
+          const int row = 64 * half + (i < 8 ? 0 : 32) + src;
+          *reinterpret_cast<uint4*>(a_tile + row * 128 + ((piece ^ (row & 7)) << 4)) = xor4(v[i], bf16_sign_mask(bits));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bars->full[stage]));
+        tile = ntile;
+        kb = nkb;
+        q += 4;
+        ra = na;
+        rb = nb;
+        sa = nsa;
+        sb = nsb;
+      }
+      if (!ok) {
+        atomicOr(args.err_word, 16);
+        *abort = 1;
       }
     }
   } else {
@@ -710,14 +837,16 @@ struct GemmPtrs {
   void* v;
 };
 
-template <int BN, int GATE>
-pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream) {
+template <int BN, int GATE, bool GATHER = false>
+pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
+                    const typename GatherParam<GATHER>::type& gat = {}) {
   CUtensorMap ma, mb, mx, mh, mv;
-  if (!make_map(&ma, ptr.e, a.N, a.Din, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if ((!GATHER && !make_map(&ma, ptr.e, a.N, a.Din, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) ||
       !make_map(&mb, ptr.W, a.Dcols, a.Din, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mv, ptr.v, a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
-  // operand maps that a gate does not use alias the output map (never read)
+  // maps that this launch does not use alias the output map (never read)
+  if (GATHER) ma = mv;
   mx = mv;
   mh = mv;
   if (GATE == PG_GATE_SCALAR && !make_map(&mx, ptr.x, a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -725,14 +854,14 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream)
   if (GATE == PG_GATE_CONTEXT &&
       !make_map(&mh, ptr.h, static_cast<uint64_t>(a.M) * a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
-  auto kern = tc_gemm_kernel<BN, GATE>;
-  const size_t smem = gemm_smem_bytes<BN>();
+  auto kern = tc_gemm_kernel<BN, GATE, GATHER>;
+  const size_t smem = gemm_smem_bytes<BN, GATHER>();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return cuda_fail(err);
   const int tiles = ((a.N + kBM - 1) / kBM) * (a.Dcols / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  kern<<<grid, kGemmThreads, smem, stream>>>(ma, mb, mx, mh, mv, a);
+  kern<<<grid, GATHER ? kFusedThreads : kGemmThreads, smem, stream>>>(ma, mb, mx, mh, mv, a, gat);
   return after_launch(1);
 }
 
@@ -741,6 +870,14 @@ pg_status dispatch_tc(int gate, const GemmPtrs& ptr, const GemmArgs& a, cudaStre
   if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE>(ptr, a, stream);
   if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR>(ptr, a, stream);
   return launch_tc<BN, PG_GATE_CONTEXT>(ptr, a, stream);
+}
+
+template <int BN>
+pg_status dispatch_fused(int gate, const GemmPtrs& ptr, const GemmArgs& a, const FusedGather& gat,
+                         cudaStream_t stream) {
+  if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE, true>(ptr, a, stream, gat);
+  if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR, true>(ptr, a, stream, gat);
+  return launch_tc<BN, PG_GATE_CONTEXT, true>(ptr, a, stream, gat);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -850,6 +987,86 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
 }
 
 }  // extern "C"
+
+// ==================================================================== fused lookup + projection
+
+extern "C" pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int32_t* tokens, int32_t B,
+                                            int32_t L, const uint32_t* canon_map, const void* table,
+                                            uint64_t table_bytes, int32_t d, int32_t M, const void* W,
+                                            int32_t gate_kind, float g, const void* x_resid, const void* h,
+                                            const float* gamma_h, const float* gamma_k, float eps, void* v_out,
+                                            float* alpha_out, void* workspace, size_t workspace_bytes,
+                                            int32_t* err_index, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  Geometry geo;
+  pg_status st = validate_desc(desc, &geo);
+  if (st != PG_OK) return st;
+  if (desc->hash_kind != PG_HASH_MULXOR || desc->mode == PG_FLAT) return PG_ERR_UNSUPPORTED;
+  if (desc->row_dtype != PG_BF16 || desc->r != kBK) return PG_ERR_UNSUPPORTED;
+  const int items = geo.O * geo.H;
+  if (items > kFusedItems) return PG_ERR_UNSUPPORTED;
+  if (B < 0 || L < 0 || d < 1 || M < 0) return PG_ERR_SHAPE;
+  if (gate_kind < PG_GATE_NONE || gate_kind > PG_GATE_CONTEXT) return PG_ERR_SHAPE;
+  if (gate_kind != PG_GATE_CONTEXT && M != 0) return PG_ERR_SHAPE;
+  if (gate_kind == PG_GATE_CONTEXT && M < 1) return PG_ERR_SHAPE;
+  const int64_t N = static_cast<int64_t>(B) * L;
+  if (N >= (1ll << 31)) return PG_ERR_SHAPE;
+  if (N == 0) return PG_OK;
+  if (!tokens || !table || !W || !v_out) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_SCALAR && !x_resid) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_CONTEXT && (!h || !gamma_h || !gamma_k || !alpha_out)) return PG_ERR_NULL;
+  if (table_bytes < geo.rows * geo.row_bytes) return PG_ERR_RANGE;
+  if (!aligned16(table) || !aligned16(W) || !aligned16(v_out) || (x_resid && !aligned16(x_resid)) ||
+      (h && !aligned16(h)))
+    return PG_ERR_ALIGN;
+  if (d % 128 != 0) return PG_ERR_UNSUPPORTED;
+  if (gate_kind == PG_GATE_CONTEXT && static_cast<int64_t>(M) * N >= (1ll << 31)) return PG_ERR_SHAPE;
+  if (sm_count() == 0) return cuda_fail(cudaGetLastError());
+  if (device_cc() != 103 && device_cc() != 100) return PG_ERR_DEVICE;
+  const int din = items * kBK;
+  if (gate_kind == PG_GATE_CONTEXT) {
+    size_t need = 0;
+    pg_project_gate_workspace_size(static_cast<int32_t>(N), din, d, M, PG_BF16, gate_kind, &need);
+    if (!workspace || workspace_bytes < need) return PG_ERR_WORKSPACE;
+    if (!aligned16(workspace) || !aligned16(gamma_h) || !aligned16(gamma_k)) return PG_ERR_ALIGN;
+  }
+  if (err_index) {
+    if (reinterpret_cast<uintptr_t>(err_index) % 4) return PG_ERR_ALIGN;
+    cudaError_t e = cudaMemsetAsync(err_index, 0xFF, sizeof(int32_t), stream);  // reads as -1
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  const int bn = (d % 256 == 0) ? 256 : 128;
+  GemmArgs a;
+  a.N = static_cast<int>(N);
+  a.Din = din;
+  a.Dcols = (gate_kind == PG_GATE_CONTEXT ? (1 + M) : 1) * d;
+  a.d = d;
+  a.M = M;
+  a.g = g;
+  a.gamma_h = gamma_h;
+  a.gamma_k = gamma_k;
+  a.partials = static_cast<float*>(workspace);
+  a.err_word = device_error_word();
+  if (!a.err_word) return cuda_fail(cudaGetLastError());
+  FusedGather gat;
+  fill_hash_params(desc, geo, &gat.P);
+  gat.seed = desc->hash_seed;
+  gat.tokens = tokens;
+  gat.canon_map = canon_map;
+  gat.table = static_cast<const uint8_t*>(table);
+  gat.L = static_cast<uint32_t>(L);
+  gat.fm_L = fastmod_constant(gat.L);
+  gat.err = err_index;
+  const GemmPtrs ptrs{nullptr, W, x_resid, h, v_out};
+  st = bn == 256 ? dispatch_fused<256>(gate_kind, ptrs, a, gat, stream)
+                 : dispatch_fused<128>(gate_kind, ptrs, a, gat, stream);
+  if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
+  const int64_t total = static_cast<int64_t>(M) * N;
+  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
+      a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out);
+  return after_launch(1);
+}
 
 // ==================================================================== no-allocation variant
 

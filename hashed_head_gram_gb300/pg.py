@@ -84,6 +84,9 @@ def _load():
     L.pg_project_gate.restype = ctypes.c_int
     L.pg_project_gate.argtypes = [i32, i32, i32, i32, i32, vp, vp, i32, f32, vp, vp, vp, vp, f32, vp, vp,
                                   vp, sz, vp]
+    L.pg_lookup_project_gate.restype = ctypes.c_int
+    L.pg_lookup_project_gate.argtypes = [dp, vp, i32, i32, vp, vp, u64, i32, i32, vp, i32, f32, vp, vp, vp, vp,
+                                         f32, vp, vp, vp, sz, vp, vp]
     L.pg_project_gate_context_noalloc.restype = ctypes.c_int
     L.pg_project_gate_context_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp, vp, vp]
     L.pg_conv_residual.restype = ctypes.c_int
@@ -189,6 +192,24 @@ def project_gate(e: torch.Tensor, W: Optional[torch.Tensor], d: int, gate_kind: 
            "pg_project_gate")
 
 
+def lookup_project_gate(desc: TableDesc, tokens: torch.Tensor, table: torch.Tensor, W: torch.Tensor, d: int,
+                        gate_kind: int, v_out: torch.Tensor, canon_map: Optional[torch.Tensor] = None, M: int = 0,
+                        g: float = 0.0, x_resid: Optional[torch.Tensor] = None, h: Optional[torch.Tensor] = None,
+                        gamma_h: Optional[torch.Tensor] = None, gamma_k: Optional[torch.Tensor] = None,
+                        eps: float = 1e-6, alpha_out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, err_index: Optional[torch.Tensor] = None,
+                        stream=None):
+    """gather_sign_concat + project_gate in one kernel (e_t never leaves shared memory)."""
+    B, L = tokens.shape
+    nbytes = table.numel() * table.element_size()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pg_lookup_project_gate(ctypes.byref(desc), _ptr(tokens), B, L, _ptr(canon_map), _ptr(table),
+                                       nbytes, d, M, _ptr(W), gate_kind, g, _ptr(x_resid), _ptr(h), _ptr(gamma_h),
+                                       _ptr(gamma_k), eps, _ptr(v_out), _ptr(alpha_out), _ptr(workspace),
+                                       ws_bytes, _ptr(err_index), _stream(stream)),
+           "pg_lookup_project_gate")
+
+
 def project_gate_context_noalloc(e: torch.Tensor, W: torch.Tensor, d: int, M: int, h: torch.Tensor,
                                  gamma_h: torch.Tensor, gamma_k: torch.Tensor, v_out: torch.Tensor,
                                  alpha_out: torch.Tensor, eps: float = 1e-6, stream=None):
@@ -225,6 +246,6 @@ def dtype_code(t: torch.dtype) -> int:
 
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
-           "workspace_size", "project_gate", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
+           "workspace_size", "project_gate", "lookup_project_gate", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

@@ -230,6 +230,27 @@ pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M, int32_t d
                            float eps, void* H, pg_stream_t stream);
 
 /*
+ * pg_lookup_project_gate -- steps 1-7 in one kernel: pg_gather_sign_concat followed by
+ * pg_project_gate, without writing e_t to memory. The projection is the fused W_V (+ M
+ * W_K) GEMM of the Engram notes section 3.4 fed straight by the lookup of section 3.2 /
+ * PageGram report section 3.1: each 64-column k-block of e_t is one head (o, k) of 128
+ * tokens, gathered, sign-flipped and laid out in shared memory by dedicated warps and
+ * consumed there by the tensor cores.
+ *  Tables: PG_ENGRAM or PG_PAGEGRAM mode, PG_BF16 rows, r = 64, O*K <= 32 (Din = O*K*64).
+ *  desc .. table_bytes, err_index   as in pg_gather_sign_concat
+ *  d .. workspace_bytes             as in pg_project_gate with dtype PG_BF16
+ * Results are bit-identical to the two-call sequence (same values, same accumulation
+ * order). B*L == 0 enqueues nothing.
+ */
+pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int32_t* tokens, int32_t B, int32_t L,
+                                 const uint32_t* canon_map, const void* table, uint64_t table_bytes,
+                                 int32_t d, int32_t M, const void* W, int32_t gate_kind, float g,
+                                 const void* x_resid, const void* h, const float* gamma_h,
+                                 const float* gamma_k, float eps, void* v_out, float* alpha_out,
+                                 void* workspace, size_t workspace_bytes, int32_t* err_index,
+                                 pg_stream_t stream);
+
+/*
  * pg_project_gate_context_noalloc -- the context-gate projection of pg_project_gate
  * (gate PG_GATE_CONTEXT, dtype PG_BF16) for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point: it exists for the host side only.
