@@ -79,6 +79,17 @@ struct Vec8<float> {
   }
 };
 
+// Asynchronous 16-byte global -> shared copies of one thread (L1 bypassed); a thread
+// waits only for its own copies, so no block-wide barrier is involved.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // SiLU(c) = c * sigmoid(c) with sigmoid(c) = (1 + tanh(c/2)) / 2: one MUFU operation.
 __device__ __forceinline__ float silu(float c) {
   float t;
@@ -86,7 +97,8 @@ __device__ __forceinline__ float silu(float c) {
   return c * fmaf(0.5f, t, 0.5f);
 }
 
-template <typename T, int MB>
+// PF: positions of H prefetched ahead of the one being computed (per thread, cp.async).
+template <typename T, int MB, int PF>
 __global__ void __launch_bounds__(512) conv_residual_kernel(
     int L, int d, int M_rt, int64_t N, const T* __restrict__ v, const float* __restrict__ alpha,
     const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks, int dil, float eps,
@@ -96,6 +108,11 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
   __shared__ float s_ms[kMaxPos];
   __shared__ float s_f[MMAX][kMaxPos];
   __shared__ float s_a[MMAX][kMaxPos];
+  // H prefetch ring: [PF][M][threads] chunks of 8 channels (16 B bf16 / 32 B fp32)
+  extern __shared__ __align__(16) uint8_t s_ring[];
+  using Raw = typename Vec8<T>::Raw;
+  Raw* ring = reinterpret_cast<Raw*>(s_ring);
+  auto ring_at = [&](int slot, int m) -> Raw* { return ring + (slot * MMAX + m) * blockDim.x + threadIdx.x; };
 
   const int c0 = threadIdx.x * 8;
   const bool active = c0 < d;
@@ -146,7 +163,25 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
     }
     __syncthreads();
 
-    // 3. conv + SiLU + residual, all branches of a position together
+    // 3. conv + SiLU + residual, all branches of a position together; H for the next PF
+    //    positions is already on its way into this thread's ring slots.
+    auto prefetch = [&](int t) {
+      if (active && t < t1) {
+        const int slot = (t - t0) % PF;
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) {
+          if (m >= M) continue;
+          const T* src = H + (m * N + seq0 + t) * d + c0;
+          Raw* dst = ring_at(slot, m);
+#pragma unroll
+          for (int k = 0; k < static_cast<int>(sizeof(Raw) / 16); ++k)
+            cp_async16(reinterpret_cast<uint8_t*>(dst) + 16 * k, reinterpret_cast<const uint8_t*>(src) + 16 * k);
+        }
+      }
+      cp_async_commit();
+    };
+#pragma unroll 1
+    for (int i = 0; i < PF; ++i) prefetch(t0 + i);
     if (active) {
       for (int t = t0; t < t1; ++t) {
         typename Vec8<T>::Raw vraw[kTaps];  // tap rows stay packed; unpacked per branch
@@ -155,10 +190,8 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
           const int p = t - j * dil;
           vraw[j] = (j < ks && p >= 0) ? Vec8<T>::load(v + (seq0 + p) * d + c0) : Vec8<T>::zero();
         }
-        typename Vec8<T>::Raw hraw[MMAX];
-#pragma unroll
-        for (int m = 0; m < MMAX; ++m)
-          if (m < M) hraw[m] = Vec8<T>::load_rw(H + (m * N + seq0 + t) * d + c0);
+        cp_async_wait<PF - 1>();   // this thread's copies for position t have landed
+        const int slot = (t - t0) % PF;
 #pragma unroll
         for (int m = 0; m < MMAX; ++m) {
           if (m >= M) continue;
@@ -170,7 +203,7 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
           }
           const float a = s_a[m][t - p0];
           float h[8], c[8], x[8];
-          Vec8<T>::unpack(hraw[m], h);
+          Vec8<T>::unpack(*ring_at(slot, m), h);
 #pragma unroll
           for (int q = 0; q < 8; ++q) c[q] = 0.f;
 #pragma unroll
@@ -183,8 +216,10 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
           for (int q = 0; q < 8; ++q) h[q] = h[q] + (silu(c[q]) + a * x[q]);  // x = v_t (tap 0)
           Vec8<T>::store(H + (m * N + seq0 + t) * d + c0, h);
         }
+        prefetch(t + PF);   // reuses the slot just read
       }
     }
+    cp_async_wait<0>();
     __syncthreads();
   }
 }
@@ -197,22 +232,29 @@ pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, 
   const int64_t total = static_cast<int64_t>(B) * runs_per_seq;
   if (total >= (1ll << 31)) return PG_ERR_SHAPE;
   const int64_t N = static_cast<int64_t>(B) * L;
-  auto run = [&](auto kern) -> pg_status {
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+  auto run = [&](auto kern, int mmax, int pf) -> pg_status {
+    const size_t ring = static_cast<size_t>(pf) * mmax * threads * (sizeof(T) * 8);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring));
     if (e != cudaSuccess) return cuda_fail(e);
-    if (per_sm < 1) per_sm = 1;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, ring);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm < 1) return PG_ERR_UNSUPPORTED;
     const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
     const int grid = static_cast<int>(total < cap ? total : cap);
-    kern<<<grid, threads, 0, stream>>>(L, d, M, N, static_cast<const T*>(v), alpha, gamma_c, conv_w, ks, dil,
-                                       eps, static_cast<T*>(H), runs_per_seq, static_cast<int>(total));
+    kern<<<grid, threads, ring, stream>>>(L, d, M, N, static_cast<const T*>(v), alpha, gamma_c, conv_w, ks, dil,
+                                          eps, static_cast<T*>(H), runs_per_seq, static_cast<int>(total));
     return after_launch(1);
   };
+  // prefetch depth: 4 positions while the ring fits in 192 KB of shared memory, else 1
+  const bool deep = 4ull * (M == 1 || M == 2 || M == 4 ? M : kMaxBranches) * threads * sizeof(T) * 8 <= (192u << 10);
   switch (M) {
-    case 1: return run(conv_residual_kernel<T, 1>);
-    case 2: return run(conv_residual_kernel<T, 2>);
-    case 4: return run(conv_residual_kernel<T, 4>);
-    default: return run(conv_residual_kernel<T, 0>);
+    case 1: return deep ? run(conv_residual_kernel<T, 1, 4>, 1, 4) : run(conv_residual_kernel<T, 1, 1>, 1, 1);
+    case 2: return deep ? run(conv_residual_kernel<T, 2, 4>, 2, 4) : run(conv_residual_kernel<T, 2, 1>, 2, 1);
+    case 4: return deep ? run(conv_residual_kernel<T, 4, 4>, 4, 4) : run(conv_residual_kernel<T, 4, 1>, 4, 1);
+    default:
+      return deep ? run(conv_residual_kernel<T, 0, 4>, kMaxBranches, 4)
+                  : run(conv_residual_kernel<T, 0, 1>, kMaxBranches, 1);
   }
 }
 

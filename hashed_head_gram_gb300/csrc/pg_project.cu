@@ -160,6 +160,11 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// Waits until all but the most recent committed bulk store group have read shared memory.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Waits until the committed bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -581,6 +586,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     uint32_t acc_phase = 0;
     uint32_t seq = 0;
     bool ok = true;
+    int pending = -1;             // slot whose TMA store may still be reading (thread epi == 0)
     const int tpb = args.d / BN;  // tiles per branch (context gate)
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
@@ -658,9 +664,19 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
           if (!is_k) {
             tma_store_2d(&map_v, smem_u32(slot_p), n0 + j * kEpiCols, m0);
             bulk_commit();
-            bulk_wait_read_all();
+            if (pending >= 0) {   // one store stays in flight; the one before it is done reading
+              bulk_wait_read_all_but_one();
+              mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+            }
+            pending = slot;
+          } else {
+            if (pending >= 0) {
+              bulk_wait_read_all();
+              mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+              pending = -1;
+            }
+            mbar_arrive(smem_u32(&bars->epi_empty[slot]));
           }
-          mbar_arrive(smem_u32(&bars->epi_empty[slot]));
         }
       }
       if (!ok) break;
@@ -679,7 +695,10 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       atomicOr(args.err_word, 4);
       *abort = 1;
     }
-    if (epi == 0) bulk_wait_all();
+    if (epi == 0) {
+      bulk_wait_all();
+      if (pending >= 0) mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+    }
   }
 
   tc_fence_before();
