@@ -10,8 +10,10 @@
 // sequence (persistent grid) and d/8 threads, thread i owning channels [8i, 8i+8):
 //   1. one warp per position reduces sum(v^2) over the run and its causal halo;
 //   2. f and alpha per (branch, position) go to shared memory;
-//   3. every thread walks its positions: c = sum_j (w[:, j] gamma) f_{t-j dil} v_{t-j dil},
-//      H[m, t] += SiLU(c) + alpha_t v_t for all M branches, whose H loads issue together.
+//   3. every thread walks its positions by residue class mod dil (so the 4 taps form a
+//      window sliding one row per step): c = sum_j f_{t-j dil} (w[:, j] gamma) v_{t-j dil},
+//      H[m, t] += SiLU(c) + alpha_t v_t for all M branches, in packed fp32x2 arithmetic,
+//      with H of the next positions prefetched into shared memory by cp.async.
 // DRAM traffic per token: v once (2d bytes; the taps re-read it from L1/L2) and H read +
 // written once per branch (2 * M * 2d bytes).
 #include <cuda_bf16.h>
@@ -90,11 +92,39 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// SiLU(c) = c * sigmoid(c) with sigmoid(c) = (1 + tanh(c/2)) / 2: one MUFU operation.
-__device__ __forceinline__ float silu(float c) {
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * c));
-  return c * fmaf(0.5f, t, 0.5f);
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic: two lanes per instruction).
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// SiLU(c) = c * sigmoid(c) with sigmoid(c) = (1 + tanh(c/2)) / 2 (one MUFU operation per
+// element), on a packed pair.
+__device__ __forceinline__ uint64_t silu2(uint64_t c) {
+  float c0, c1, t0, t1;
+  upk(mul2(c, pk(0.5f, 0.5f)), c0, c1);
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(c0));
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(c1));
+  return mul2(c, fma2(pk(0.5f, 0.5f), pk(t0, t1), pk(0.5f, 0.5f)));
 }
 
 // PF: positions of H prefetched ahead of the one being computed (per thread, cp.async).
@@ -163,60 +193,97 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
     }
     __syncthreads();
 
-    // 3. conv + SiLU + residual, all branches of a position together; H for the next PF
-    //    positions is already on its way into this thread's ring slots.
-    auto prefetch = [&](int t) {
-      if (active && t < t1) {
-        const int slot = (t - t0) % PF;
+    // 3. conv + SiLU + residual. Positions are walked by residue class mod dil, so the taps
+    //    of t (t, t - dil, t - 2 dil, t - 3 dil) form a window that slides by one row per
+    //    step; H of the next PF positions in walking order is already on its way into this
+    //    thread's ring slots (one cp.async group per position).
+    int pr = 0, pi = 0, ps = 0;  // prefetch cursor: position t0 + pr + dil * pi, sequence ps
+    auto prefetch_next = [&]() {
+      if (pr < dil && t0 + pr < t1) {
+        if (active) {
+          const int t = t0 + pr + dil * pi;
+          const int slot = ps % PF;
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m) {
-          if (m >= M) continue;
-          const T* src = H + (m * N + seq0 + t) * d + c0;
-          Raw* dst = ring_at(slot, m);
+          for (int m = 0; m < MMAX; ++m) {
+            if (m >= M) continue;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(H + (m * N + seq0 + t) * d + c0);
+            uint8_t* dst = reinterpret_cast<uint8_t*>(ring_at(slot, m));
 #pragma unroll
-          for (int k = 0; k < static_cast<int>(sizeof(Raw) / 16); ++k)
-            cp_async16(reinterpret_cast<uint8_t*>(dst) + 16 * k, reinterpret_cast<const uint8_t*>(src) + 16 * k);
+            for (int k = 0; k < static_cast<int>(sizeof(Raw) / 16); ++k) cp_async16(dst + 16 * k, src + 16 * k);
+          }
+        }
+        ++pi;
+        if (t0 + pr + dil * pi >= t1) {
+          ++pr;
+          pi = 0;
         }
       }
       cp_async_commit();
+      ++ps;
     };
 #pragma unroll 1
-    for (int i = 0; i < PF; ++i) prefetch(t0 + i);
-    if (active) {
-      for (int t = t0; t < t1; ++t) {
-        typename Vec8<T>::Raw vraw[kTaps];  // tap rows stay packed; unpacked per branch
+    for (int i = 0; i < PF; ++i) prefetch_next();
+    int s = 0;  // sequence index of the position being computed
+    for (int r = 0; r < dil && t0 + r < t1; ++r) {
+      float win[kTaps][8];  // v at t - j dil, zero before the start of the sequence
 #pragma unroll
-        for (int j = 0; j < kTaps; ++j) {
-          const int p = t - j * dil;
-          vraw[j] = (j < ks && p >= 0) ? Vec8<T>::load(v + (seq0 + p) * d + c0) : Vec8<T>::zero();
+      for (int j = 0; j < kTaps; ++j) {
+        const int p = t0 + r - j * dil;
+        if (active && j < ks && p >= 0) {
+          Vec8<T>::unpack(Vec8<T>::load(v + (seq0 + p) * d + c0), win[j]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) win[j][q] = 0.f;
         }
+      }
+      for (int t = t0 + r; t < t1; t += dil, ++s) {
+        const bool has_next = active && t + dil < t1;
+        Raw nxt = Vec8<T>::zero();
+        if (has_next) nxt = Vec8<T>::load(v + (seq0 + t + dil) * d + c0);   // next window row, early
         cp_async_wait<PF - 1>();   // this thread's copies for position t have landed
-        const int slot = (t - t0) % PF;
+        if (active) {
+          const int slot = s % PF;
+          uint64_t prod[kTaps][4];   // (w[:, j] gamma) * v_{t - j dil}, packed pairs
 #pragma unroll
-        for (int m = 0; m < MMAX; ++m) {
-          if (m >= M) continue;
-          float fj[kTaps];
+          for (int j = 0; j < kTaps; ++j)
 #pragma unroll
-          for (int j = 0; j < kTaps; ++j) {
-            const int p = t - j * dil;
-            fj[j] = (j < ks && p >= 0) ? s_f[m][p - p0] : 0.f;
+            for (int q = 0; q < 4; ++q)
+              prod[j][q] = mul2(pk(wg[j][2 * q], wg[j][2 * q + 1]), pk(win[j][2 * q], win[j][2 * q + 1]));
+          uint64_t vt[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) vt[q] = pk(win[0][2 * q], win[0][2 * q + 1]);
+#pragma unroll
+          for (int m = 0; m < MMAX; ++m) {
+            if (m >= M) continue;
+            uint64_t fj[kTaps];
+#pragma unroll
+            for (int j = 0; j < kTaps; ++j) {
+              const int p = t - j * dil;
+              const float f = (j < ks && p >= 0) ? s_f[m][p - p0] : 0.f;
+              fj[j] = pk(f, f);
+            }
+            const float a = s_a[m][t - p0];
+            const uint64_t aa = pk(a, a);
+            float h[8];
+            Vec8<T>::unpack(*ring_at(slot, m), h);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint64_t c = mul2(fj[0], prod[0][q]);
+#pragma unroll
+              for (int j = 1; j < kTaps; ++j) c = fma2(fj[j], prod[j][q], c);
+              const uint64_t y = fma2(aa, vt[q], silu2(c));           // SiLU(c) + alpha v_t
+              upk(add2(pk(h[2 * q], h[2 * q + 1]), y), h[2 * q], h[2 * q + 1]);
+            }
+            Vec8<T>::store(H + (m * N + seq0 + t) * d + c0, h);
           }
-          const float a = s_a[m][t - p0];
-          float h[8], c[8], x[8];
-          Vec8<T>::unpack(*ring_at(slot, m), h);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) c[q] = 0.f;
-#pragma unroll
-          for (int j = kTaps - 1; j >= 0; --j) {
-            Vec8<T>::unpack(vraw[j], x);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) c[q] = fmaf(wg[j][q] * fj[j], x[q], c[q]);
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) h[q] = h[q] + (silu(c[q]) + a * x[q]);  // x = v_t (tap 0)
-          Vec8<T>::store(H + (m * N + seq0 + t) * d + c0, h);
         }
-        prefetch(t + PF);   // reuses the slot just read
+        prefetch_next();
+        // slide the window by one row (t -> t + dil)
+#pragma unroll
+        for (int j = kTaps - 1; j > 0; --j)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) win[j][q] = win[j - 1][q];
+        Vec8<T>::unpack(nxt, win[0]);
       }
     }
     cp_async_wait<0>();
