@@ -147,15 +147,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Phase A: rows and sign words of every (token, item) of one warp batch, one lane each.
+template <int ITEMS, int TB>
 __device__ __forceinline__ void hash_batch(const ItemConst* __restrict__ ic, const GatherGeom& g, int mode,
                                            int64_t batch, int lane, const int32_t* __restrict__ tokens,
                                            const uint32_t* __restrict__ canon_map, uint32_t vocab,
                                            uint32_t* s_rows, uint64_t* s_signs, int32_t* err) {
   const int p = lane;
-  if (p >= g.tb * g.items) return;
-  const int s = static_cast<int>(__umulhi(static_cast<uint32_t>(p), g.items_magic));
-  const int item = p - s * g.items;
-  const int64_t tok = batch * g.tb + s;
+  const int items = ITEMS ? ITEMS : g.items;
+  const int tb = ITEMS ? TB : g.tb;
+  if (p >= tb * items) return;
+  const int s = ITEMS ? p / ITEMS : static_cast<int>(__umulhi(static_cast<uint32_t>(p), g.items_magic));
+  const int item = p - s * items;
+  const int64_t tok = batch * tb + s;
   if (tok >= g.N) return;
   const uint32_t t = fastmod(static_cast<uint32_t>(tok), g.fm_L, g.L);
   uint64_t hs;
@@ -163,12 +166,28 @@ __device__ __forceinline__ void hash_batch(const ItemConst* __restrict__ ic, con
   for (int q = 0; q < g.W; ++q) s_signs[p * g.W + q] = mix64(hs + kGolden * static_cast<uint64_t>(q + 1));
 }
 
-template <int ROWT, int OUTT, bool FLAT>
-__global__ void __launch_bounds__(kThreads, 2) gather_kernel(
+// Warp-batch geometry: tb tokens whose (token, item) pairs fit 32 lanes and whose chunks
+// fit kChunksPerThread per lane (the host computes the same numbers).
+__host__ __device__ constexpr int batch_tokens(int per_tok, int items) {
+  return (32 * kChunksPerThread / per_tok) < (32 / items) ? (32 * kChunksPerThread / per_tok) : (32 / items);
+}
+
+// RC (16-byte chunks per row, or 8-element NF4 tasks per row) and ITEMS (items per token)
+// fixed at compile time turn the chunk -> (token, item, piece) mapping into shifts for the
+// layouts the workloads use; RC = ITEMS = 0 is the general, runtime-geometry version.
+template <int ROWT, int OUTT, bool FLAT, int RC, int ITEMS>
+__global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gather_kernel(
     const __grid_constant__ HashParams P, uint64_t seed, const GatherGeom g, const int32_t* __restrict__ tokens,
     const uint32_t* __restrict__ canon_map, const uint8_t* __restrict__ table, uint8_t* __restrict__ e_out,
     int32_t* err) {
-  constexpr int NCH = kChunksPerThread;
+  constexpr bool CT = RC > 0 && ITEMS > 0;
+  constexpr int PT = CT ? (FLAT ? RC : ITEMS * RC) : 1;
+  constexpr int TBC = CT ? batch_tokens(PT, ITEMS) : 1;
+  constexpr int NCH = CT ? (TBC * PT + 31) / 32 : kChunksPerThread;
+  const int per_tok = CT ? PT : g.per_tok;
+  const int items = CT ? ITEMS : g.items;
+  const int tb = CT ? TBC : g.tb;
+  const uint32_t rc = CT ? RC : g.rc;
   constexpr int kWarpsPerBlock = kThreads / 32;
   __shared__ ItemConst s_ic[kMaxItems];
   __shared__ float s_nf4[16];
@@ -185,10 +204,10 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
   if (first < g.nbatch)
-    hash_batch(s_ic, g, P.mode, first, lane, tokens, canon_map, P.vocab, s_rows_all[warp][0],
-               s_signs_all[warp][0], err);
+    hash_batch<ITEMS, TBC>(s_ic, g, P.mode, first, lane, tokens, canon_map, P.vocab, s_rows_all[warp][0],
+                           s_signs_all[warp][0], err);
   __syncwarp();
-  const int chunks = g.tb * g.per_tok;
+  const int chunks = tb * per_tok;
   int cur = 0;
   for (int64_t batch = first; batch < g.nbatch; batch += nwarps) {
     const uint32_t* rows = s_rows_all[warp][cur];
@@ -201,27 +220,28 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(
     for (int i = 0; i < NCH; ++i) {
       const uint32_t c = lane + 32 * i;
       if (c < static_cast<uint32_t>(chunks)) {
-        const uint32_t s = __umulhi(c, g.tok_magic);
-        const uint32_t cc = c - s * g.per_tok;
-        if (batch * g.tb + s < g.N) {
+        const uint32_t s = CT ? c / PT : __umulhi(c, g.tok_magic);
+        const uint32_t cc = c - s * per_tok;
+        if (batch * tb + s < g.N) {
           if constexpr (FLAT) {
             // chunk cc of the d-wide row, for every order: loaded and summed at use
             v[i] = make_uint4(0, 0, 0, 0);
             bits[i] = 0;
           } else if constexpr (ROWT == PG_NF4) {
             const uint32_t it = cc >> 3, piece = cc & 7u;
-            const uint8_t* rowp = table + static_cast<uint64_t>(rows[s * g.items + it]) * 34u;
+            const uint8_t* rowp = table + static_cast<uint64_t>(rows[s * items + it]) * 34u;
             v[i].x = static_cast<uint32_t>(ldg_u16(rowp + 4 * piece)) |
                      (static_cast<uint32_t>(ldg_u16(rowp + 4 * piece + 2)) << 16);
             aux[i] = ldg_u16(rowp + 32);
-            bits[i] = static_cast<uint32_t>(signs[(s * g.items + it) * g.W] >> (piece * 8)) & 0xFFu;
+            bits[i] = static_cast<uint32_t>(signs[(s * items + it) * g.W] >> (piece * 8)) & 0xFFu;
           } else {
             constexpr int E = ROWT == PG_F32 ? 4 : 8;
-            const uint32_t it = g.rc == 1u ? cc : __umulhi(cc, g.rc_magic);
-            const uint32_t piece = cc - it * g.rc;
-            v[i] = ldg_stream(table + static_cast<uint64_t>(rows[s * g.items + it]) * g.row_bytes + piece * 16u);
+            const uint32_t it = CT ? cc / RC : (rc == 1u ? cc : __umulhi(cc, g.rc_magic));
+            const uint32_t piece = cc - it * rc;
+            v[i] = ldg_stream(table + static_cast<uint64_t>(rows[s * items + it]) * (CT ? RC * 16u : g.row_bytes) +
+                              piece * 16u);
             const uint32_t e0 = piece * E;
-            bits[i] = static_cast<uint32_t>(signs[(s * g.items + it) * g.W + (e0 >> 6)] >> (e0 & 63)) &
+            bits[i] = static_cast<uint32_t>(signs[(s * items + it) * g.W + (e0 >> 6)] >> (e0 & 63)) &
                       ((1u << E) - 1u);
           }
         }
@@ -230,24 +250,25 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(
     // ---- phase A of the next batch while the loads are in flight
     const int64_t next = batch + nwarps;
     if (next < g.nbatch)
-      hash_batch(s_ic, g, P.mode, next, lane, tokens, canon_map, P.vocab, s_rows_all[warp][cur ^ 1],
-                 s_signs_all[warp][cur ^ 1], err);
+      hash_batch<ITEMS, TBC>(s_ic, g, P.mode, next, lane, tokens, canon_map, P.vocab, s_rows_all[warp][cur ^ 1],
+                             s_signs_all[warp][cur ^ 1], err);
     // ---- phase B, finish: dequantise, sign, (sum), store
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
       const uint32_t c = lane + 32 * i;
       if (c >= static_cast<uint32_t>(chunks)) continue;
-      const uint32_t s = __umulhi(c, g.tok_magic);
-      const uint32_t cc = c - s * g.per_tok;
-      const int64_t tok = batch * g.tb + s;
+      const uint32_t s = CT ? c / PT : __umulhi(c, g.tok_magic);
+      const uint32_t cc = c - s * per_tok;
+      const int64_t tok = batch * tb + s;
       if (tok >= g.N) continue;
       uint8_t* out_tok = e_out + static_cast<uint64_t>(tok) * g.e_bytes;
       if constexpr (FLAT) {
         constexpr int E = ROWT == PG_F32 ? 4 : 8;
-        const int O = g.items;
+        const int O = items;
         float acc[E];
         for (int o = 0; o < O; ++o) {
-          const uint4 x4 = ldg_stream(table + static_cast<uint64_t>(rows[s * O + o]) * g.row_bytes + cc * 16u);
+          const uint4 x4 =
+              ldg_stream(table + static_cast<uint64_t>(rows[s * O + o]) * (CT ? RC * 16u : g.row_bytes) + cc * 16u);
           const uint32_t e0 = cc * E;
           const uint32_t b = static_cast<uint32_t>(signs[(s * O + o) * g.W + (e0 >> 6)] >> (e0 & 63)) &
                              ((1u << E) - 1u);
@@ -314,19 +335,41 @@ __global__ void __launch_bounds__(kThreads, 2) gather_kernel(
 using GatherFn = void (*)(const HashParams, uint64_t, const GatherGeom, const int32_t*, const uint32_t*,
                           const uint8_t*, uint8_t*, int32_t*);
 
-GatherFn pick_gather(int row_dtype, int out_dtype, bool flat) {
+template <int RC, int ITEMS>
+GatherFn pick_layout(int row_dtype, int out_dtype, bool flat) {
   if (flat) {
-    if (row_dtype == PG_F32 && out_dtype == PG_F32) return gather_kernel<PG_F32, PG_F32, true>;
-    if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return gather_kernel<PG_BF16, PG_BF16, true>;
-    if (row_dtype == PG_BF16 && out_dtype == PG_F32) return gather_kernel<PG_BF16, PG_F32, true>;
+    if (row_dtype == PG_F32 && out_dtype == PG_F32) return gather_kernel<PG_F32, PG_F32, true, RC, ITEMS>;
+    if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return gather_kernel<PG_BF16, PG_BF16, true, RC, ITEMS>;
+    if (row_dtype == PG_BF16 && out_dtype == PG_F32) return gather_kernel<PG_BF16, PG_F32, true, RC, ITEMS>;
     return nullptr;
   }
-  if (row_dtype == PG_F32 && out_dtype == PG_F32) return gather_kernel<PG_F32, PG_F32, false>;
-  if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return gather_kernel<PG_BF16, PG_BF16, false>;
-  if (row_dtype == PG_BF16 && out_dtype == PG_F32) return gather_kernel<PG_BF16, PG_F32, false>;
-  if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_kernel<PG_NF4, PG_BF16, false>;
-  if (row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_kernel<PG_NF4, PG_F32, false>;
+  if (row_dtype == PG_F32 && out_dtype == PG_F32) return gather_kernel<PG_F32, PG_F32, false, RC, ITEMS>;
+  if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return gather_kernel<PG_BF16, PG_BF16, false, RC, ITEMS>;
+  if (row_dtype == PG_BF16 && out_dtype == PG_F32) return gather_kernel<PG_BF16, PG_F32, false, RC, ITEMS>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_kernel<PG_NF4, PG_BF16, false, RC, ITEMS>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_kernel<PG_NF4, PG_F32, false, RC, ITEMS>;
   return nullptr;
+}
+
+// Compile-time layouts: r = 64 rows (bf16 / NF4: 8 chunks; fp32: 16) and r = 80 bf16 (10)
+// with 2 orders x 8 heads; flat d = 768 bf16 (96 chunks) and d = 256 fp32 (64).
+GatherFn pick_gather(int row_dtype, int out_dtype, bool flat, uint32_t rc, int items) {
+  const bool bb = row_dtype == PG_BF16 && out_dtype == PG_BF16;
+  const bool bf = row_dtype == PG_BF16 && out_dtype == PG_F32;
+  const bool ff = row_dtype == PG_F32 && out_dtype == PG_F32;
+  if (!flat && items == 16) {
+    if (rc == 8 && bb) return gather_kernel<PG_BF16, PG_BF16, false, 8, 16>;
+    if (rc == 8 && bf) return gather_kernel<PG_BF16, PG_F32, false, 8, 16>;
+    if (rc == 8 && row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_kernel<PG_NF4, PG_BF16, false, 8, 16>;
+    if (rc == 8 && row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_kernel<PG_NF4, PG_F32, false, 8, 16>;
+    if (rc == 10 && bb) return gather_kernel<PG_BF16, PG_BF16, false, 10, 16>;
+    if (rc == 16 && ff) return gather_kernel<PG_F32, PG_F32, false, 16, 16>;
+  }
+  if (flat && items == 2) {
+    if (rc == 96 && bb) return gather_kernel<PG_BF16, PG_BF16, true, 96, 2>;
+    if (rc == 64 && ff) return gather_kernel<PG_F32, PG_F32, true, 64, 2>;
+  }
+  return pick_layout<0, 0>(row_dtype, out_dtype, flat);
 }
 
 pg_status prepare_err(int32_t* err_index, cudaStream_t stream) {
@@ -391,7 +434,8 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   const int items = geo.O * geo.H;
   if (items > kMaxItems || items * geo.W > kMaxSignWords) return PG_ERR_UNSUPPORTED;
   if (desc->row_dtype != PG_NF4 && geo.row_bytes % 16) return PG_ERR_UNSUPPORTED;
-  GatherFn fn = pick_gather(desc->row_dtype, out_dtype, flat);
+  const uint32_t rc_host = desc->row_dtype == PG_NF4 ? 8u : geo.row_bytes / 16u;
+  GatherFn fn = pick_gather(desc->row_dtype, out_dtype, flat, rc_host, items);
   if (!fn) return desc->row_dtype == PG_F32 && out_dtype == PG_BF16 ? PG_ERR_DTYPE : PG_ERR_UNSUPPORTED;
 
   GatherGeom g;
@@ -405,8 +449,7 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   if (g.per_tok < 2) return PG_ERR_UNSUPPORTED;  // 16-byte flat rows: no workload uses them
   // a warp batch: tb tokens whose (token, item) pairs fit the 32 lanes and whose chunks
   // fit 8 per lane
-  int tb = 32 * kChunksPerThread / g.per_tok;
-  if (tb > 32 / items) tb = 32 / items;
+  const int tb = batch_tokens(g.per_tok, items);
   if (tb < 1) return PG_ERR_UNSUPPORTED;  // one token's row bytes exceed a batch
   g.tb = tb;
   // floor(x / n) = umulhi(x, floor(2^32 / n) + 1), exact while x * n < 2^32 (x < 2^11 here)

@@ -348,6 +348,8 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Tiles are walked from the last m-block down: when the projection follows the gather,
+  // the most recently written rows of e_t are the ones still in L2.
   const int num_m = (args.N + kBM - 1) / kBM;
   const int num_n = args.Dcols / BN;
   const int num_tiles = num_m * num_n;
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s holds a load nobody has consumed yet (error path)
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
+        const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
             ok = false;
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       bool ok = true;
       uint32_t issued = 0;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
+        const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
         const int n0 = n_blk * BN, m0 = m_blk * kBM;
         const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
         for (int j = 0; j < kSub; ++j, ++seq) {
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       const int stage = pair;
       // rows and sign words of tokens (64 half + lane) and (+32) of one k-block
       auto hash_rows = [&](int tile, int kb, uint32_t& ra, uint32_t& rb, uint64_t& sa, uint64_t& sb) {
-        const int m0 = (tile / num_n) * kBM;
+        const int m0 = ((num_tiles - 1 - tile) / num_n) * kBM;
         const ItemConst& it = s_ic[kb];
         const int64_t ta = static_cast<int64_t>(m0) + 64 * half + lane, tb = ta + 32;
         uint64_t hs;
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     int pending = -1;             // slot whose TMA store may still be reading (thread epi == 0)
     const int tpb = args.d / BN;  // tiles per branch (context gate)
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const int m_blk = tile / num_n, n_blk = tile - (tile / num_n) * num_n;
+      const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
       if (!mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort)) {
         ok = false;
         break;
