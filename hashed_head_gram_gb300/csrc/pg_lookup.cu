@@ -109,7 +109,6 @@ struct GatherGeom {
   int tb;               // tokens per batch
   int per_tok;          // chunks (or NF4 tasks) per token
   uint32_t tok_magic;   // floor(c / per_tok) = umulhi(c, tok_magic)
-  uint32_t items_magic; // floor(p / items) = umulhi(p, items_magic)
   uint32_t rc;          // 16-byte chunks per stored row (multi-head f32/bf16), or per row (flat)
   uint32_t rc_magic;
   uint32_t row_bytes;
@@ -156,7 +155,7 @@ __device__ __forceinline__ void hash_batch(const ItemConst* __restrict__ ic, con
   const int items = ITEMS ? ITEMS : g.items;
   const int tb = ITEMS ? TB : g.tb;
   if (p >= tb * items) return;
-  const int s = ITEMS ? p / ITEMS : static_cast<int>(__umulhi(static_cast<uint32_t>(p), g.items_magic));
+  const int s = p / items;  // once per lane and batch
   const int item = p - s * items;
   const int64_t tok = batch * tb + s;
   if (tok >= g.N) return;
@@ -212,13 +211,16 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
   for (int64_t batch = first; batch < g.nbatch; batch += nwarps) {
     const uint32_t* rows = s_rows_all[warp][cur];
     const uint64_t* signs = s_signs_all[warp][cur];
-    // ---- phase B, issue: loads of this batch's chunks
+    // a batch is streamed in rounds of 32 * NCH chunks (one round unless a token's e_t
+    // is wider than a round)
+    for (int base = 0; base < chunks; base += 32 * NCH) {
+    // ---- phase B, issue: loads of this round's chunks
     uint4 v[NCH];
     uint32_t bits[NCH];
     uint32_t aux[NCH];   // NF4: scale bits
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
-      const uint32_t c = lane + 32 * i;
+      const uint32_t c = base + lane + 32 * i;
       if (c < static_cast<uint32_t>(chunks)) {
         const uint32_t s = CT ? c / PT : __umulhi(c, g.tok_magic);
         const uint32_t cc = c - s * per_tok;
@@ -249,13 +251,13 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
     }
     // ---- phase A of the next batch while the loads are in flight
     const int64_t next = batch + nwarps;
-    if (next < g.nbatch)
+    if (base == 0 && next < g.nbatch)
       hash_batch<ITEMS, TBC>(s_ic, g, P.mode, next, lane, tokens, canon_map, P.vocab, s_rows_all[warp][cur ^ 1],
                              s_signs_all[warp][cur ^ 1], err);
     // ---- phase B, finish: dequantise, sign, (sum), store
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
-      const uint32_t c = lane + 32 * i;
+      const uint32_t c = base + lane + 32 * i;
       if (c >= static_cast<uint32_t>(chunks)) continue;
       const uint32_t s = CT ? c / PT : __umulhi(c, g.tok_magic);
       const uint32_t cc = c - s * per_tok;
@@ -327,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
             make_uint4(f.z << 16, f.z & 0xFFFF0000u, f.w << 16, f.w & 0xFFFF0000u);
       }
     }
+    }  // rounds
     __syncwarp();
     cur ^= 1;
   }
@@ -449,12 +452,11 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   if (g.per_tok < 2) return PG_ERR_UNSUPPORTED;  // 16-byte flat rows: no workload uses them
   // a warp batch: tb tokens whose (token, item) pairs fit the 32 lanes and whose chunks
   // fit 8 per lane
-  const int tb = batch_tokens(g.per_tok, items);
-  if (tb < 1) return PG_ERR_UNSUPPORTED;  // one token's row bytes exceed a batch
+  int tb = batch_tokens(g.per_tok, items);
+  if (tb < 1) tb = 1;  // a token wider than one round: streamed in several rounds
   g.tb = tb;
-  // floor(x / n) = umulhi(x, floor(2^32 / n) + 1), exact while x * n < 2^32 (x < 2^11 here)
+  // floor(x / n) = umulhi(x, floor(2^32 / n) + 1), exact while x * n < 2^32 (x, n < 2^16 here)
   g.tok_magic = static_cast<uint32_t>((1ull << 32) / static_cast<uint32_t>(g.per_tok) + 1ull);
-  g.items_magic = static_cast<uint32_t>((1ull << 32) / static_cast<uint32_t>(items) + 1ull);
   g.rc_magic = g.rc == 1u ? 0u : static_cast<uint32_t>((1ull << 32) / g.rc + 1ull);
   g.row_bytes = geo.row_bytes;
   g.e_bytes = geo.e_width * (out_dtype == PG_F32 ? 4u : 2u);

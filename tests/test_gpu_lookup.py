@@ -171,3 +171,67 @@ def test_gather_is_causal(cuda):
     assert np.array_equal(outs[0][0, :120], outs[1][0, :120])
     assert np.array_equal(outs[0][1], outs[1][1])
     assert not np.array_equal(outs[0][0, 120:], outs[1][0, 120:])
+
+
+# Layouts other than the workloads' (so the runtime-geometry gather runs): head counts,
+# widths, slots, order sets and dtypes the compile-time variants do not cover.
+OTHER_LAYOUTS = [
+    dict(mode=W.MODE_PAGEGRAM, K=4, S=2, r=32, dt=W.DT_BF16, orders=[2, 3], pages=[37, 31]),
+    dict(mode=W.MODE_PAGEGRAM, K=16, S=1, r=64, dt=W.DT_BF16, orders=[2, 3], pages=[11, 13]),
+    dict(mode=W.MODE_ENGRAM, K=3, S=1, r=128, dt=W.DT_BF16, orders=[1, 2, 4], rows=None),
+    dict(mode=W.MODE_ENGRAM, K=8, S=1, r=64, dt=W.DT_F32, orders=[2], rows=None),
+    dict(mode=W.MODE_PAGEGRAM, K=4, S=15, r=64, dt=W.DT_NF4, orders=[2, 3, 4], pages=[7, 5, 3]),
+    dict(mode=W.MODE_FLAT, K=1, S=1, r=512, dt=W.DT_BF16, orders=[2, 3, 4], rows=[[211], [199], [197]]),
+    dict(mode=W.MODE_FLAT, K=1, S=1, r=128, dt=W.DT_F32, orders=[3], rows=[[101]]),
+    dict(mode=W.MODE_ENGRAM, K=2, S=1, r=1024, dt=W.DT_BF16, orders=[2, 3], rows=None),
+]
+
+
+@pytest.mark.parametrize("lay", range(len(OTHER_LAYOUTS)))
+def test_gather_other_layouts(cuda, lay):
+    pg = _pg()
+    d = dict(OTHER_LAYOUTS[lay])
+    rows = d.pop("rows", None)
+    if d["mode"] == W.MODE_ENGRAM:
+        pr = W.largest_primes(997, len(d["orders"]) * d["K"])
+        rows = [pr[i * d["K"]:(i + 1) * d["K"]] for i in range(len(d["orders"]))]
+    spec = W.TableSpec("t", d["mode"], K=d["K"], S=d["S"], r=d["r"], row_dtype=d["dt"], orders=d["orders"],
+                       pages=d.get("pages", []), rows=rows or [], hash_seed=0xC0FFEE + lay)
+    w = W.shrink(W.make_workload(2), B=3, L=211)
+    tokens = W.make_tokens(w)
+    table = torch.randint(-128, 128, (spec.table_rows, spec.r), dtype=torch.int8,
+                          generator=torch.Generator().manual_seed(lay))
+    if spec.row_dtype == W.DT_NF4:
+        table = torch.randint(0, 256, (spec.table_rows, 34), dtype=torch.uint8,
+                              generator=torch.Generator().manual_seed(lay))
+        table[:, 33] = 0x3C     # scale 1.0 .. 1.99: keeps the fp16 scale finite
+    else:
+        table = (table.float() / 64).to(torch.float32 if spec.row_dtype == W.DT_F32 else torch.bfloat16)
+    out_dtypes = [orc.F32] if spec.row_dtype == W.DT_F32 else [orc.BF16, orc.F32]
+    desc = pg.table_desc(spec, w.vocab)
+    for od in out_dtypes:
+        ref = oracle_e(spec, tokens, None, w.vocab, table, od)
+        e = torch.empty(w.N, spec.e_width, dtype=torch.float32 if od == orc.F32 else torch.bfloat16, device=cuda)
+        pg.gather_sign_concat(desc, torch.from_numpy(tokens).to(cuda), table.to(cuda), e, od)
+        got = e.cpu().numpy().view(np.uint32) if od == orc.F32 else bits16(e)
+        assert np.array_equal(got, ref.view(np.uint32) if od == orc.F32 else ref), (lay, od)
+
+
+def test_nf4_levels_on_the_gpu_match_the_oracle(cuda):
+    # One row per code value with scale 1.0: the GPU's level table, read back through the
+    # gather, equals the oracle's (each side holds its own copy of the NF4 levels).
+    pg = _pg()
+    spec = W.TableSpec("t", W.MODE_PAGEGRAM, K=1, S=1, r=64, row_dtype=W.DT_NF4, orders=[1], pages=[1],
+                       hash_seed=3)
+    tab = torch.zeros(1, 34, dtype=torch.uint8)
+    tab[0, :32] = torch.tensor([(2 * i % 16) | (((2 * i + 1) % 16) << 4) for i in range(32)], dtype=torch.uint8)
+    tab[0, 32:] = torch.tensor([0x00, 0x3C], dtype=torch.uint8)   # fp16 1.0, little-endian
+    tokens = np.array([[5]], np.int32)
+    e = torch.empty(1, 64, dtype=torch.float32, device=cuda)
+    pg.gather_sign_concat(pg.table_desc(spec, 16), torch.from_numpy(tokens).to(cuda), tab.to(cuda), e, orc.F32)
+    _, _, signs, _ = orc.index(spec, tokens, None, 16)
+    lv = orc.nf4_levels()
+    bits = (signs[0, 0, 0, 0] >> np.arange(64, dtype=np.uint64)) & np.uint64(1)
+    want = np.where(bits == 1, -1.0, 1.0).astype(np.float32) * lv[np.arange(64) % 16]
+    assert np.array_equal(np.abs(e.cpu().numpy()[0]), np.abs(want))
+    assert np.array_equal(e.cpu().numpy()[0].view(np.uint32), want.view(np.uint32))
