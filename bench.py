@@ -155,25 +155,31 @@ class Pipeline:
         self.table = W.make_table(w, spec, dev)
         dn = self.dn = W.make_dense(w, dev)
         self.N, self.din, self.d = w.N, spec.e_width, w.d
-        self.e = torch.empty(self.N, self.din, dtype=torch.bfloat16, device=dev)
+        self.tdt = torch.float32 if w.dtype == W.DT_F32 else torch.bfloat16
+        self.pdt = pg.F32 if w.dtype == W.DT_F32 else pg.BF16
+        self.e = torch.empty(self.N, self.din, dtype=self.tdt, device=dev)
         if w.gate == W.GATE_SCALAR:
-            self.out = torch.empty(self.N, self.d, dtype=torch.bfloat16, device=dev)
+            self.out = torch.empty(self.N, self.d, dtype=self.tdt, device=dev)
             self.x_host = dn["x"].cpu().pin_memory()
+        elif w.gate == W.GATE_NONE:
+            self.out = torch.empty(self.N, self.d, dtype=self.tdt, device=dev)
         else:
             self.v = torch.empty(self.N, self.d, dtype=torch.bfloat16, device=dev)
             self.alpha = torch.empty(w.M, self.N, device=dev)
             nws = pg.workspace_size(self.N, self.din, self.d, w.M, pg.BF16, pg.GATE_CONTEXT)
             self.ws = torch.empty(nws // 4, device=dev)
             self.H0 = dn["H"].clone()
-        self.out_host = torch.empty(self.N, self.d, dtype=torch.bfloat16).pin_memory()
+        self.out_host = torch.empty(self.N, self.d, dtype=self.tdt).pin_memory()
 
     def gather(self):
-        self.pg.gather_sign_concat(self.desc, self.tokens, self.table, self.e, self.pg.BF16, canon_map=self.cmap)
+        self.pg.gather_sign_concat(self.desc, self.tokens, self.table, self.e, self.pdt, canon_map=self.cmap)
 
     def project(self):
         pg, w, dn = self.pg, self.w, self.dn
         if w.gate == self.W.GATE_SCALAR:
-            pg.project_gate(self.e, dn["W"], self.d, pg.GATE_SCALAR, self.out, pg.BF16, g=w.g, x_resid=dn["x"])
+            pg.project_gate(self.e, dn["W"], self.d, pg.GATE_SCALAR, self.out, self.pdt, g=w.g, x_resid=dn["x"])
+        elif w.gate == self.W.GATE_NONE:
+            pg.project_gate(self.e, dn["W"], self.d, pg.GATE_NONE, self.out, self.pdt)
         else:
             pg.project_gate(self.e, dn["W"], self.d, pg.GATE_CONTEXT, self.v, pg.BF16, M=w.M, h=dn["H"],
                             gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=self.alpha,
@@ -196,9 +202,12 @@ class Pipeline:
 
     def can_fuse(self):
         sp = self.spec
-        return sp.mode != self.W.MODE_FLAT and sp.row_dtype == self.W.DT_BF16 and sp.r == 64
+        return (sp.mode != self.W.MODE_FLAT and sp.row_dtype == self.W.DT_BF16 and sp.r == 64
+                and self.w.gate != self.W.GATE_NONE)
 
     def stages(self, fused=True):
+        if self.w.cfg_id == 4:   # the 20B NF4 table: the lookup ends at e_t
+            return [("gather_sign_concat", self.gather)]
         if fused and self.can_fuse():
             st = [("lookup_project_gate", self.fused)]
         else:
@@ -208,7 +217,9 @@ class Pipeline:
         return st
 
     def result_tensor(self):
-        return self.out if self.w.gate == self.W.GATE_SCALAR else self.dn["H"]
+        if self.w.cfg_id == 4:
+            return self.e
+        return self.dn["H"] if self.w.gate == self.W.GATE_CONTEXT else self.out
 
     # algorithmic work per launch ("Roofline")
     def algorithmic(self, name):
@@ -216,7 +227,7 @@ class Pipeline:
         if name == "gather_sign_concat":
             # 2K rows x row bytes (sector-rounded for NF4) + token ID + e_t write, per token
             rb = self.spec.row_bytes if self.spec.row_dtype != self.W.DT_NF4 else 64
-            per = len(self.spec.orders) * self.spec.K * rb + 4 + din * 2
+            per = len(self.spec.orders) * self.spec.K * rb + 4 + din * self.e.element_size()
             return "hbm", per * N
         if name in ("project_gate", "lookup_project_gate"):
             cols = d * (1 + w.M)
@@ -239,11 +250,14 @@ def compulsory_gather_bytes(p) -> float:
     cand = first.unsqueeze(1) + span
     cand = cand[cand <= last.unsqueeze(1)]
     distinct = int(torch.unique(cand).numel())
-    return distinct * 32.0 + p.N * 4 + p.N * p.din * 2
+    return distinct * 32.0 + p.N * 4 + p.N * p.din * p.e.element_size()
 
 
 def flush_l2(buf):
+    """Untimed L2 flush between steps: write a buffer larger than L2, then read it back so
+    the written lines are written back here, not inside the next timed kernel."""
     buf.add_(1)
+    buf.sum(dtype=buf.dtype)
 
 
 def time_stages(stages, steps, stream, flush):
@@ -282,7 +296,7 @@ def run_gpu(args):
             fn()
         flush_l2(flush)
     torch.cuda.synchronize()
-    if p.w.gate != p.W.GATE_SCALAR:
+    if p.w.gate == p.W.GATE_CONTEXT:
         p.dn["H"].copy_(p.H0)
     torch.cuda.synchronize()
 
@@ -304,7 +318,8 @@ def run_gpu(args):
     e2e_ms = []
     h2d = p.tokens_host.numel() * 4 + (p.x_host.numel() * 2 if hasattr(p, "x_host") else 0)
     res = p.result_tensor()
-    res_host = p.out_host if res.numel() == p.out_host.numel() else torch.empty_like(res, device="cpu").pin_memory()
+    res_host = (p.out_host if res.shape == p.out_host.shape and res.dtype == p.out_host.dtype
+                else torch.empty_like(res, device="cpu").pin_memory())
     barrier(world)
     torch.cuda.synchronize()
     e2e_steps = max(1, min(args.steps, 200))
@@ -390,7 +405,10 @@ def run_gpu(args):
             "wall_s_timed_loop": round(t_wall, 4),
         }
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+            if p.spec.table_bytes > (8 << 30):
+                line["cpu_baseline"] = None   # the table does not fit the host-side oracle leg
+            else:
+                line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -402,7 +420,8 @@ def run_gpu(args):
 # time of the capture; reported only while the source is unchanged (profiles/ holds the
 # captures).
 TRAFFIC = {
-    (2, "project_gate"): ("pg_project.cu", "4e43ae96596eb2d3", 309.778944e6),
+    (2, "gather_sign_concat"): ("pg_lookup.cu", "363776ab493496dd", 184.213760e6),
+    (2, "project_gate"): ("pg_project.cu", "d29deff114d94a64", 309.707008e6),
 }
 
 
@@ -425,12 +444,16 @@ def workload_config(w, world):
     t = w.tables[0]
     desc = {2: "PageGram 200M-parameter bf16 table: P_n = 48,823 / 48,821 pages, K=8, S=4, r=64; "
                "Zipf(1.1) IDs over 50,304; W_V 1024->768; scalar gate g=0.5",
+            4: "20B-parameter PageGram table in NF4 (34-byte rows, 10.6 GB): P_n = 4,882,811 / 4,882,789, K=8, "
+               "S=4; Zipf(1.05) over 128,000 IDs folded to 98,010; gather + NF4 dequant + sign + concat",
+            1: "tiny fp32 PageGram table (P_n=64, K=8, S=4, r=64); 4096 uniform IDs over 1024; fp32 W_V 1024->256",
             5: "Engram-27B-shaped module: 16 prime subtables ~2.2266M rows, r=80, bf16; Zipf(1.05) over 128k "
                "with canonical folding; fused W_V + 4 W_K (1280 -> 12800); RMSNorm-sigmoid gate; causal "
                "depthwise conv k=4 dilation 3 + SiLU + residual into 4 branches of d=2560"}.get(w.cfg_id, w.name)
     return {"workload": f"{w.name} (config {w.cfg_id}): {desc}", "batch": f"{w.B}x{w.L}", "tokens_per_gpu": w.N,
             "table_bytes": t.table_bytes, "parallelism": f"dp{world} (independent batches, no collective)",
-            "l2": "flushed between timed steps (256 MiB write); table and activations > L2"}
+            "l2": "flushed between timed steps (256 MiB written, then read back, untimed); "
+                  "table and activations > L2"}
 
 
 # ---------------------------------------------------------------- CPU oracle legs
@@ -456,9 +479,13 @@ def _oracle_sample(cfg: int, ntok: int):
     t0 = time.perf_counter()
     canon, rows, signs, bad = orc.index(spec, tok, cmap, w.vocab, which)
     rowdata = orc.fetch_rows(table, rows)
-    e = orc.assemble(spec, rows, rowdata, signs, orc.BF16)
-    ef = orc.bf16_bits_to_f64(e)
-    if w.gate == W.GATE_SCALAR:
+    e = orc.assemble(spec, rows, rowdata, signs, orc.F32 if spec.row_dtype == W.DT_F32 else orc.BF16)
+    if w.cfg_id == 4:   # the lookup ends at e_t
+        return time.perf_counter() - t0, len(which)
+    ef = e.astype(np.float64) if spec.row_dtype == W.DT_F32 else orc.bf16_bits_to_f64(e)
+    if w.gate == W.GATE_NONE:
+        dense.project(ef, dn["W"])
+    elif w.gate == W.GATE_SCALAR:
         v = dense.project(ef, dn["W"])
         dense.scalar_gate(dn["x"][:len(which)], v, w.g)
     else:
@@ -506,7 +533,9 @@ def _cpu_dense(w):
 def cpu_baseline(cfg: int, seconds: float):
     """The oracle as it stands on the host cores, on a bounded sample of the workload."""
     dt, n = _oracle_sample(cfg, 1024)                     # calibration
-    want = int(max(1024, min(1 << 16, n * seconds / max(dt, 1e-3))))
+    w = __import__("hashed_head_gram_gb300.workloads", fromlist=["x"]).make_workload(cfg)
+    cap = 8192 if w.gate == 2 else 1 << 16   # the host copy of the branch states holds 8192 tokens
+    want = int(max(1024, min(cap, n * seconds / max(dt, 1e-3))))
     dt, n = _oracle_sample(cfg, want)
     return {"value": round(n / dt, 1), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"first {n} tokens of the workload batch; C stages single-threaded, numpy fp64 "
@@ -547,7 +576,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 5])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--path", choices=["two_kernel", "fused"], default="two_kernel",
                     help="two_kernel: pg_gather_sign_concat + pg_project_gate; fused: pg_lookup_project_gate "
                          "(r = 64 bf16 tables); the other one is timed too and reported as other_path")
