@@ -1,0 +1,100 @@
+"""Single-kernel runs on a workload's shapes, for timing and profiling one kernel at a time.
+
+    python -m hashed_head_gram_gb300.kernel_cases {gather,project,conv} --config C [--iters N]
+
+Inputs are synthetic and seeded (the conv and projection cases need no table, so they
+hold at most a few GB on the device); each launch goes through the C ABI exactly as the
+benchmark's. Prints the median CUDA-event time per launch (L2 flushed between launches,
+untimed) and the achieved rate.
+"""
+from __future__ import annotations
+
+import argparse
+import statistics
+
+import torch
+
+from . import pg
+from . import workloads as W
+
+
+def _flush(buf):
+    buf.add_(1)
+    buf.sum(dtype=buf.dtype)
+
+
+def _time(fn, iters: int, dev) -> float:
+    flush = torch.zeros(64 << 20, dtype=torch.int32, device=dev)
+    fn()
+    _flush(flush)
+    torch.cuda.synchronize()
+    marks = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        _flush(flush)
+        marks.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in marks) * 1e3
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("kernel", choices=["gather", "project", "conv"])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--iters", type=int, default=20)
+    args = ap.parse_args(argv)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.make_workload(args.config)
+    spec = w.tables[0]
+    g = torch.Generator(device=dev).manual_seed(12345)
+    dt = torch.float32 if w.dtype == W.DT_F32 else torch.bfloat16
+    code = pg.F32 if w.dtype == W.DT_F32 else pg.BF16
+    N, din, d, M = w.N, spec.e_width, w.d, w.M
+    if args.kernel == "gather":
+        desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+        tokens = torch.from_numpy(W.make_tokens(w)).to(dev)
+        cm = W.make_canon_map(w)
+        cm = None if cm is None else torch.from_numpy(cm.view("int32")).to(dev)
+        table = W.make_table(w, spec, dev)
+        e = torch.empty(N, din, dtype=dt, device=dev)
+        us = _time(lambda: pg.gather_sign_concat(desc, tokens, table, e, code, canon_map=cm), args.iters, dev)
+        rb = spec.row_bytes if spec.row_dtype != W.DT_NF4 else 64
+        byts = N * (len(spec.orders) * spec.K * rb + 4 + din * e.element_size())
+        print(f"gather_sign_concat config {w.cfg_id}: {us:.1f} us, {byts / us / 1e3:.0f} GB/s (algorithmic)")
+    elif args.kernel == "project":
+        e = (torch.randint(-128, 128, (N, din), device=dev, generator=g).float() / 64).to(dt)
+        Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(dt)
+        v = torch.empty(N, d, dtype=dt, device=dev)
+        if w.gate == W.GATE_CONTEXT:
+            H = torch.randn(M, N, d, device=dev, generator=g).to(dt)
+            one = torch.ones(d, device=dev)
+            alpha = torch.empty(M, N, device=dev)
+            ws = torch.empty(pg.workspace_size(N, din, d, M, code, pg.GATE_CONTEXT) // 4, device=dev)
+            fn = lambda: pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, v, code, M=M, h=H, gamma_h=one, gamma_k=one,
+                                         alpha_out=alpha, workspace=ws)
+        elif w.gate == W.GATE_SCALAR:
+            x = torch.randn(N, d, device=dev, generator=g).to(dt)
+            fn = lambda: pg.project_gate(e, Wm, d, pg.GATE_SCALAR, v, code, g=w.g, x_resid=x)
+        else:
+            fn = lambda: pg.project_gate(e, Wm, d, pg.GATE_NONE, v, code)
+        us = _time(fn, args.iters, dev)
+        print(f"project_gate config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * (1 + M) * d / us / 1e6:.1f} TFLOP/s")
+    else:
+        if w.gate != W.GATE_CONTEXT:
+            raise SystemExit("the conv runs in the context-gated module (config 5)")
+        v = torch.randn(N, d, device=dev, generator=g).to(dt)
+        alpha = torch.rand(M, N, device=dev, generator=g)
+        gc = torch.ones(d, device=dev)
+        cw = torch.randn(d, w.conv_kernel, device=dev, generator=g) * 0.25
+        H = torch.randn(M, N, d, device=dev, generator=g).to(dt)
+        us = _time(lambda: pg.conv_residual(w.B, w.L, d, M, code, v, alpha, gc, cw, H, dilation=w.dilation,
+                                            eps=w.eps), args.iters, dev)
+        byts = N * d * v.element_size() * (1 + 2 * M)
+        print(f"conv_residual config {w.cfg_id}: {us:.1f} us, {byts / us / 1e3:.0f} GB/s")
+
+
+if __name__ == "__main__":
+    main()
