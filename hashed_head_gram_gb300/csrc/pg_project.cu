@@ -63,20 +63,71 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Acquire at cluster scope: for barriers that threads of the peer CTA arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after ~1 s
 
 // Waits for the phase of `parity` to complete; false after the time limit or when
 // another role of the CTA has already given up (`abort`).
+template <bool CLUSTER = false>
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (poll()) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// ---- CTA pairs (cluster of 2): rank 0 issues the M = 256 MMAs for both CTAs
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs; release/acquire orders shared-memory work across the pair.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the pair.
+__device__ __forceinline__ uint32_t pair_addr(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -88,23 +139,46 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Load into this CTA's shared memory; completion is counted on `bar_cluster`, which may be
+// the barrier of the other CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// TMEM allocation: one warp of the CTA, or one warp of each CTA of a pair (PAIR).
+template <bool PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -115,21 +189,52 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) (+)= A(smem desc) x B(smem desc)^T, bf16 in, fp32 accumulate.
+// D(tmem) (+)= A(smem desc) x B(smem desc)^T, bf16 in, fp32 accumulate. PAIR: M = 256 rows
+// over the two CTAs (each holds 128 rows of A and half of B's rows at the same offsets,
+// and 128 rows of D in its TMEM).
+template <bool PAIR>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
-// Arrives once on `bar` when all previously issued tcgen05.mma of this thread complete.
+// Arrives once on `bar` when all previously issued tcgen05.mma of this thread complete;
+// PAIR: on the barrier at that offset in both CTAs.
+template <bool PAIR>
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
+  if constexpr (PAIR)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// As umma_commit, on this CTA's barrier only.
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_local(uint32_t bar) {
+  if constexpr (PAIR)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
 }
 
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets row (lane base + i).
@@ -215,7 +320,8 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 w, float* f) {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 4;          // shared-memory ring of a single-CTA tile (48 KB per stage)
+constexpr int kStagesPair = 6;      // of a CTA pair's tile (32 KB per stage and CTA)
 constexpr int kGemmThreads = 224;   // 7 warps: A/B producer, MMA, operand producer, 4 x epilogue
 constexpr int kFusedThreads = 480;  // + 8 gather warps producing the A operand
 constexpr int kGatherWarp0 = 7;
@@ -227,6 +333,9 @@ constexpr int kFusedItems = 32;     // (order, head) items of the fused kernel
 
 template <bool GATHER>
 __host__ __device__ constexpr int epi_stages() { return GATHER ? 3 : 4; }
+
+template <bool PAIR>
+__host__ __device__ constexpr int gemm_stages() { return PAIR ? kStagesPair : kStages; }
 
 // What the gather warps of the fused kernel need (empty in the plain GEMM).
 struct FusedGather {
@@ -262,9 +371,10 @@ struct GemmArgs {
   int* err_word;
 };
 
+template <int S>
 struct GemmBarriers {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[S];
+  uint64_t empty[S];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t epi_full[kEpiStagesMax];   // operand sub-tile landed (or slot handed over)
@@ -275,10 +385,11 @@ struct GemmBarriers {
   int abort;
 };
 
-template <int BN, bool GATHER>
+template <int BN, bool GATHER, bool PAIR>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 /* alignment slack */ + kStages * (kABytes + BN * kBK * 2) + epi_stages<GATHER>() * kEpiBytes +
-         sizeof(GemmBarriers) + (GATHER ? kFusedItems * sizeof(ItemConst) : 0);
+  return 1024 /* alignment slack */ + gemm_stages<PAIR>() * (kABytes + (PAIR ? BN / 2 : BN) * kBK * 2) +
+         epi_stages<GATHER>() * kEpiBytes + sizeof(GemmBarriers<gemm_stages<PAIR>()>) +
+         (GATHER ? kFusedItems * sizeof(ItemConst) : 0);
 }
 
 // Epilogue operands and results move through 128 x 32 bf16 sub-tiles (64 bytes per row)
@@ -291,39 +402,51 @@ __device__ __forceinline__ uint32_t epi_offset(int row, int chunk) {
 // GATHER: the A operand (e_t) is not read from global memory; 8 gather warps build each
 // 128 x 64 A tile in shared memory from the table (k-block kb = head (o, k) of r = 64),
 // exactly as pg_gather_sign_concat would have written it.
-template <int BN, int GATE, bool GATHER>
+// PAIR: a cluster of two CTAs computes 256 x BN tiles. Each CTA stages its 128 rows of A
+// and BN/2 rows of B; both CTAs' copies count on rank 0's `full` barrier, rank 0 issues
+// M = 256 MMAs (rows 128 r .. 128 r + 127 accumulate in CTA r's TMEM) and its commits
+// arrive on the barriers of both CTAs; each CTA runs the epilogue of its own 128 rows.
+template <int BN, int GATE, bool GATHER, bool PAIR>
 __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
                    const __grid_constant__ CUtensorMap map_v, const GemmArgs args,
                    const __grid_constant__ typename GatherParam<GATHER>::type gat) {
+  static_assert(!(GATHER && PAIR), "the fused gather runs on single-CTA tiles");
+  constexpr int kSt = gemm_stages<PAIR>();
   constexpr int kEpiStages = epi_stages<GATHER>();
-  constexpr int kBBytes = BN * kBK * 2;
-  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN);
+  constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of W this CTA stages per k-block
+  constexpr int kBBytes = kBRows * kBK * 2;
+  constexpr int kTileM = PAIR ? 2 * kBM : kBM;  // output rows of a tile
+  constexpr uint32_t kIdesc = idesc_bf16(kTileM, BN);
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr int kSub = BN / kEpiCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
-  uint8_t* sE = sB + kStages * kBBytes;
-  GemmBarriers* bars = reinterpret_cast<GemmBarriers*>(sE + kEpiStages * kEpiBytes);
+  uint8_t* sB = smem + kSt * kABytes;
+  uint8_t* sE = sB + kSt * kBBytes;
+  GemmBarriers<kSt>* bars = reinterpret_cast<GemmBarriers<kSt>*>(sE + kEpiStages * kEpiBytes);
   ItemConst* s_ic = reinterpret_cast<ItemConst*>(bars + 1);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // work units: CTAs, or CTA pairs
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const int unit = PAIR ? static_cast<int>(cluster_index()) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(cluster_count()) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       // the TMA expect-tx arrival, plus the 64 gather threads that build the A tile
       mbar_init(smem_u32(&bars->full[s]), GATHER ? 1 + 64 : 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&bars->tmem_full[a]), 1);
-      mbar_init(smem_u32(&bars->tmem_empty[a]), 4 * 32);
+      mbar_init(smem_u32(&bars->tmem_empty[a]), (PAIR ? 2 : 1) * 4 * 32);  // every epilogue thread
     }
     for (int s = 0; s < kEpiStages; ++s) {
       mbar_init(smem_u32(&bars->epi_full[s]), 1);
@@ -336,8 +459,8 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish<PAIR>();
   }
   if constexpr (GATHER) {
     if (threadIdx.x >= 32 * kGatherWarp0 && threadIdx.x - 32 * kGatherWarp0 < gat.P.O * gat.P.H)
@@ -345,12 +468,13 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers and TMEM exist before any remote use
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
   // Tiles are walked from the last m-block down: when the projection follows the gather,
   // the most recently written rows of e_t are the ones still in L2.
-  const int num_m = (args.N + kBM - 1) / kBM;
+  const int num_m = (args.N + kTileM - 1) / kTileM;
   const int num_n = args.Dcols / BN;
   const int num_tiles = num_m * num_n;
   const int num_kb = args.Din / kBK;
@@ -364,7 +488,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s holds a load nobody has consumed yet (error path)
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < num_tiles && ok; tile += units) {
         const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
@@ -372,11 +496,20 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
             break;
           }
           const uint32_t full = smem_u32(&bars->full[stage]);
-          mbar_expect_tx(full, GATHER ? kBBytes : kABytes + kBBytes);
-          if (!GATHER) tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
-          tma_load_2d(smem_u32(sB + stage * kBBytes), &map_b, full, kb * kBK, n_blk * BN);
+          if constexpr (PAIR) {
+            if (rank == 0) mbar_expect_tx(full, 2 * (kABytes + kBBytes));
+            const uint32_t full0 = pair_addr(full, 0);
+            tma_load_2d_pair(smem_u32(sA + stage * kABytes), &map_a, full0, kb * kBK,
+                             m_blk * kTileM + static_cast<int>(rank) * kBM);
+            tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &map_b, full0, kb * kBK,
+                             n_blk * BN + static_cast<int>(rank) * kBRows);
+          } else {
+            mbar_expect_tx(full, GATHER ? kBBytes : kABytes + kBBytes);
+            if (!GATHER) tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
+            tma_load_2d(smem_u32(sB + stage * kBBytes), &map_b, full, kb * kBK, n_blk * BN);
+          }
           issued |= 1u << stage;
-          if (++stage == kStages) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
@@ -385,9 +518,10 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       if (!ok) {
         atomicOr(args.err_word, 1);
         *abort = 1;
-        // Let copies already in flight land before the CTA can exit (bounded).
-        for (int s = 0; s < kStages; ++s)
-          if (issued & (1u << s)) {
+        // Let copies already in flight land before the CTA can exit (bounded; a pair's
+        // copies count on rank 0's barriers and are waited for at the end instead).
+        for (int s = 0; s < kSt; ++s)
+          if (!PAIR && (issued & (1u << s))) {
             const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(smem_u32(&bars->full[s]), par) && globaltimer() - t0 < kWaitLimitNs) {
@@ -397,21 +531,21 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        if (!mbar_wait(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort)) {
+      for (int tile = unit; tile < num_tiles && ok; tile += units) {
+        if (!mbar_wait<PAIR>(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(smem_u32(&bars->full[stage]), phase, abort)) {
+          if (!mbar_wait<PAIR>(smem_u32(&bars->full[stage]), phase, abort)) {
             ok = false;
             break;
           }
@@ -420,15 +554,15 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
           const uint64_t b0 = sw128_desc(smem_u32(sB + stage * kBBytes));
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // advance 16 elements = 32 bytes = 2 units
-            umma_bf16(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc, (kb | k) != 0);
-          umma_commit(smem_u32(&bars->empty[stage]));
-          if (++stage == kStages) {
+            umma_bf16<PAIR>(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc, (kb | k) != 0);
+          umma_commit<PAIR>(smem_u32(&bars->empty[stage]));
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&bars->tmem_full[acc]));
+        umma_commit<PAIR>(smem_u32(&bars->tmem_full[acc]));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -437,7 +571,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
         *abort = 1;
       }
       // Every MMA this thread issued has finished before TMEM can be released.
-      umma_commit(smem_u32(&bars->mma_done));
+      umma_commit_local<PAIR>(smem_u32(&bars->mma_done));
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(smem_u32(&bars->mma_done), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
@@ -450,10 +584,11 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       uint32_t seq = 0;
       bool ok = true;
       uint32_t issued = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < num_tiles && ok; tile += units) {
         const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
-        const int n0 = n_blk * BN, m0 = m_blk * kBM;
+        const int n0 = n_blk * BN, m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
         const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
+        if (m0 >= args.N) continue;  // this CTA's rows of the tile lie past the last token
         for (int j = 0; j < kSub; ++j, ++seq) {
           const int slot = static_cast<int>(seq % kEpiStages);
           const uint32_t ph = (seq / kEpiStages) & 1u;
@@ -590,14 +725,15 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     bool ok = true;
     int pending = -1;             // slot whose TMA store may still be reading (thread epi == 0)
     const int tpb = args.d / BN;  // tiles per branch (context gate)
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int tile = unit; tile < num_tiles && ok; tile += units) {
       const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
       if (!mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int m0 = m_blk * kBM;
+      const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+      const bool rows_here = m0 < args.N;  // (the operand producer skips the same tiles)
       const int row = m0 + row_in_tile;
       const bool live = row < args.N;
       const int n0 = n_blk * BN;
@@ -606,7 +742,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       const int kc = is_k ? n0 - (m_br + 1) * args.d : 0;
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
-      for (int j = 0; j < kSub; ++j, ++seq) {
+      for (int j = 0; rows_here && j < kSub; ++j, ++seq) {
         const int slot = static_cast<int>(seq % kEpiStages);
         const uint32_t ph = (seq / kEpiStages) & 1u;
         if (!mbar_wait(smem_u32(&bars->epi_full[slot]), ph, abort)) {
@@ -683,7 +819,10 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       }
       if (!ok) break;
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
+      if constexpr (PAIR)
+        mbar_arrive_cluster(pair_addr(smem_u32(&bars->tmem_empty[acc]), 0));
+      else
+        mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
       if (is_k && live) {
         float* p = args.partials + (static_cast<size_t>(m_br * tpb + kc / BN) * 3) * args.N + row;
         p[0] = s_hk;
@@ -705,9 +844,20 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) {
+    // After an error, copies this CTA issued may still be landing: they count on rank 0's
+    // barriers, so give them time (bounded) before the pair can leave.
+    if (threadIdx.x == 0 && *abort) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 2000000ull) {
+      }
+    }
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while the other may still reach its shared memory or TMEM
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc<PAIR>(tmem, kTmemCols);
   }
 }
 
@@ -858,12 +1008,12 @@ struct GemmPtrs {
   void* v;
 };
 
-template <int BN, int GATE, bool GATHER = false>
+template <int BN, int GATE, bool GATHER = false, bool PAIR = false>
 pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
                     const typename GatherParam<GATHER>::type& gat = {}) {
   CUtensorMap ma, mb, mx, mh, mv;
   if ((!GATHER && !make_map(&ma, ptr.e, a.N, a.Din, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-      !make_map(&mb, ptr.W, a.Dcols, a.Din, kBK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mb, ptr.W, a.Dcols, a.Din, kBK, PAIR ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mv, ptr.v, a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
   // maps that this launch does not use alias the output map (never read)
@@ -875,22 +1025,47 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
   if (GATE == PG_GATE_CONTEXT &&
       !make_map(&mh, ptr.h, static_cast<uint64_t>(a.M) * a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
-  auto kern = tc_gemm_kernel<BN, GATE, GATHER>;
-  const size_t smem = gemm_smem_bytes<BN, GATHER>();
+  auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR>;
+  const size_t smem = gemm_smem_bytes<BN, GATHER, PAIR>();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return cuda_fail(err);
+  if constexpr (PAIR) {
+    // persistent: one CTA pair per co-resident cluster slot, at most one per 256 x BN tile
+    const int tiles = ((a.N + 2 * kBM - 1) / (2 * kBM)) * (a.Dcols / BN);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2u * static_cast<unsigned>(tiles));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int slots = 0;
+    err = cudaOccupancyMaxActiveClusters(&slots, kern, &cfg);
+    if (err != cudaSuccess) return cuda_fail(err);
+    if (slots < 1) return PG_ERR_DEVICE;
+    const int clusters = tiles < slots ? tiles : slots;
+    cfg.gridDim = dim3(2u * static_cast<unsigned>(clusters));
+    err = cudaLaunchKernelEx(&cfg, kern, ma, mb, mx, mh, mv, a, gat);
+    if (err != cudaSuccess) return cuda_fail(err);
+    return after_launch(1);
+  }
   const int tiles = ((a.N + kBM - 1) / kBM) * (a.Dcols / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
   kern<<<grid, GATHER ? kFusedThreads : kGemmThreads, smem, stream>>>(ma, mb, mx, mh, mv, a, gat);
   return after_launch(1);
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 pg_status dispatch_tc(int gate, const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream) {
-  if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE>(ptr, a, stream);
-  if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR>(ptr, a, stream);
-  return launch_tc<BN, PG_GATE_CONTEXT>(ptr, a, stream);
+  if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE, false, PAIR>(ptr, a, stream);
+  if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR, false, PAIR>(ptr, a, stream);
+  return launch_tc<BN, PG_GATE_CONTEXT, false, PAIR>(ptr, a, stream);
 }
 
 template <int BN>
@@ -998,8 +1173,9 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
     if (!workspace || workspace_bytes < need) return PG_ERR_WORKSPACE;
     if (!aligned16(workspace) || !aligned16(gamma_h) || !aligned16(gamma_k)) return PG_ERR_ALIGN;
   }
-  pg_status st = bn == 256 ? dispatch_tc<256>(gate_kind, ptrs, a, stream)
-                           : dispatch_tc<128>(gate_kind, ptrs, a, stream);
+  // 256-column tiles run on CTA pairs (256 x 256 per pair), 128-column ones on single CTAs
+  pg_status st = bn == 256 ? dispatch_tc<256, true>(gate_kind, ptrs, a, stream)
+                           : dispatch_tc<128, false>(gate_kind, ptrs, a, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
   const int64_t total = static_cast<int64_t>(M) * N;
   alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(

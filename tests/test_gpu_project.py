@@ -40,7 +40,10 @@ def test_simt_fp32_projection_config1(cuda):
     assert rel_l2(to_f64(out), dense.scalar_gate(x.double().numpy(), ref, 0.5)) <= F32_TOL
 
 
-@pytest.mark.parametrize("N,Din,d", [(429, 1024, 768), (128, 64, 128), (1000, 1280, 256), (77, 192, 384)])
+# d % 256 == 0 runs 256 x 256 tiles on CTA pairs: N = 429 and 1000 end in a ragged second
+# half, N = 640 in a pair whose second CTA has no rows at all; d = 128 / 384 run single CTAs.
+@pytest.mark.parametrize("N,Din,d", [(429, 1024, 768), (128, 64, 128), (1000, 1280, 256), (77, 192, 384),
+                                     (640, 512, 512)])
 def test_tcgen05_projection(cuda, N, Din, d):
     pg = _pg()
     e = _e_bf16(N, Din, 4)
@@ -60,7 +63,8 @@ def test_tcgen05_projection(cuda, N, Din, d):
     assert rel_l2(to_f64(out), dense.scalar_gate(x.double().numpy(), ref, 0.5)) <= BF16_TOL
 
 
-@pytest.mark.parametrize("N,Din,d,M", [(300, 1280, 2560, 4), (129, 128, 256, 2), (64, 64, 384, 1)])
+@pytest.mark.parametrize("N,Din,d,M", [(300, 1280, 2560, 4), (129, 128, 256, 2), (64, 64, 384, 1),
+                                       (384, 256, 512, 2)])
 def test_tcgen05_context_gate(cuda, N, Din, d, M):
     pg = _pg()
     e = _e_bf16(N, Din, 7)
