@@ -78,20 +78,29 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after ~1 s
 
-// Waits for the phase of `parity` to complete; false after the time limit or when
-// another role of the CTA has already given up (`abort`).
-template <bool CLUSTER = false>
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  if (poll()) return true;
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+  return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+
+template <bool CLUSTER>
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
   const uint64_t t0 = globaltimer();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
-      if (poll()) return true;
+      if (mbar_poll<CLUSTER>(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// Waits for the phase of `parity` to complete; false after the time limit or when
+// another role of the CTA has already given up (`abort`). The first poll is inline: the
+// MMA issuer runs one wait per 512 tensor-core cycles and a call costs it a large share.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_poll<CLUSTER>(bar, parity) || mbar_wait_slow<CLUSTER>(bar, parity, abort);
 }
 
 // ---- CTA pairs (cluster of 2): rank 0 issues the M = 256 MMAs for both CTAs
