@@ -421,7 +421,7 @@ def run_gpu(args):
 # captures).
 TRAFFIC = {
     (2, "gather_sign_concat"): ("pg_lookup.cu", "363776ab493496dd", 184.213760e6),
-    (2, "project_gate"): ("pg_project.cu", "d29deff114d94a64", 309.707008e6),
+    (2, "project_gate"): ("pg_project.cu", "32db704fcfaa0396", 310.721792e6),
     (5, "conv_residual"): ("pg_conv.cu", "f87b93f460b8b792", 1500.525568e6),
 }
 
