@@ -11,6 +11,8 @@
 //            contiguous bytes of e_t and 4 whole 128-byte rows of one page (PageGram: all K
 //            rows of an order lie in one K*S-row page block, PageGram report section 3.1);
 //   phase A of the warp's next batch runs while phase B's loads are in flight.
+//   NF4 rows (34 bytes) take their own kernel: windows copied into shared memory by
+//   cp.async three batches ahead, dequantised from there (see gather_nf4_kernel).
 // Sources: PageGram report sections 2.1, 2.2, 3.1, 3.3; Engram notes (arXiv 2601.07372)
 // section 3.2.
 #include <cuda_bf16.h>
@@ -114,6 +116,7 @@ struct GatherGeom {
   uint32_t row_bytes;
   uint32_t e_bytes;     // bytes of one token's e_t
   int64_t nbatch;
+  uint64_t table_bytes; // NF4: bytes of the table (the last rows' 16-byte windows stop there)
 };
 
 __device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
@@ -124,11 +127,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
   return v;
 }
 
-__device__ __forceinline__ uint16_t ldg_u16(const void* ptr) {
-  uint16_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(ptr));
-  return v;
-}
 
 
 // XOR masks that negate 4 fp32 from 4 sign bits.
@@ -189,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
   const uint32_t rc = CT ? RC : g.rc;
   constexpr int kWarpsPerBlock = kThreads / 32;
   __shared__ ItemConst s_ic[kMaxItems];
-  __shared__ float s_nf4[16];
   // per warp, double-buffered: rows [2][32], sign words [2][kMaxSignWords]
   __shared__ uint32_t s_rows_all[kWarpsPerBlock][2][32];
   __shared__ uint64_t s_signs_all[kWarpsPerBlock][2][kMaxSignWords];
@@ -197,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x < g.items) init_item_const(s_ic[threadIdx.x], P, seed, threadIdx.x);
-  if (ROWT == PG_NF4 && threadIdx.x < 16) s_nf4[threadIdx.x] = __uint_as_float(c_nf4_bits[threadIdx.x]);
   __syncthreads();
 
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
@@ -217,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
     // ---- phase B, issue: loads of this round's chunks
     uint4 v[NCH];
     uint32_t bits[NCH];
-    uint32_t aux[NCH];   // NF4: scale bits
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
       const uint32_t c = base + lane + 32 * i;
@@ -229,13 +224,6 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
             // chunk cc of the d-wide row, for every order: loaded and summed at use
             v[i] = make_uint4(0, 0, 0, 0);
             bits[i] = 0;
-          } else if constexpr (ROWT == PG_NF4) {
-            const uint32_t it = cc >> 3, piece = cc & 7u;
-            const uint8_t* rowp = table + static_cast<uint64_t>(rows[s * items + it]) * 34u;
-            v[i].x = static_cast<uint32_t>(ldg_u16(rowp + 4 * piece)) |
-                     (static_cast<uint32_t>(ldg_u16(rowp + 4 * piece + 2)) << 16);
-            aux[i] = ldg_u16(rowp + 32);
-            bits[i] = static_cast<uint32_t>(signs[(s * items + it) * g.W] >> (piece * 8)) & 0xFFu;
           } else {
             constexpr int E = ROWT == PG_F32 ? 4 : 8;
             const uint32_t it = CT ? cc / RC : (rc == 1u ? cc : __umulhi(cc, g.rc_magic));
@@ -298,25 +286,6 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
               make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
                          pack_bf16(acc[6], acc[7]));
         }
-      } else if constexpr (ROWT == PG_NF4) {
-        const float scale = __half2float(__ushort_as_half(static_cast<unsigned short>(aux[i])));
-        float x[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float val = s_nf4[(v[i].x >> (4 * q)) & 15u] * scale;
-          x[q] = ((bits[i] >> q) & 1u) ? -val : val;
-        }
-        if constexpr (OUTT == PG_F32) {
-          uint8_t* dst = out_tok + cc * 32u;
-          *reinterpret_cast<uint4*>(dst) = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
-                                                      __float_as_uint(x[2]), __float_as_uint(x[3]));
-          *reinterpret_cast<uint4*>(dst + 16) = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
-                                                           __float_as_uint(x[6]), __float_as_uint(x[7]));
-        } else {
-          *reinterpret_cast<uint4*>(out_tok + cc * 16u) =
-              make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                         pack_bf16(x[6], x[7]));
-        }
       } else if constexpr (ROWT == PG_F32) {
         *reinterpret_cast<uint4*>(out_tok + cc * 16u) = xor4(v[i], f32_sign_mask(bits[i]));
       } else if constexpr (OUTT == PG_BF16) {
@@ -335,6 +304,132 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
   }
 }
 
+// ------------------------------------------------------------------ K2, NF4 rows
+
+// A 34-byte NF4 row starts at an even byte offset o = 34 row mod 16, so it lies inside the
+// three aligned 16-byte chunks [34 row - o, 34 row - o + 48). Each warp batch (32 rows)
+// copies those windows into the warp's shared-memory ring with cp.async (no registers
+// held while the rows are in flight) kNf4Depth batches ahead, then dequantises from shared
+// memory: the same task mapping and output stores as the bf16 path (one lane per 8
+// elements, 16 bytes of e_t per lane and 512 contiguous bytes per warp store).
+constexpr int kNf4Window = 48;
+constexpr int kNf4Depth = 3;
+
+struct Nf4Slot {
+  uint8_t rows[32][kNf4Window];
+  uint64_t sign[32];
+  uint8_t off[32];
+};
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int OUTT, int ITEMS>
+__global__ void __launch_bounds__(kThreads, 4) gather_nf4_kernel(
+    const __grid_constant__ HashParams P, uint64_t seed, const GatherGeom g, const int32_t* __restrict__ tokens,
+    const uint32_t* __restrict__ canon_map, const uint8_t* __restrict__ table, uint8_t* __restrict__ e_out,
+    int32_t* err) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int TBC = ITEMS > 0 ? batch_tokens(ITEMS * 8, ITEMS) : 1;
+  const int items = ITEMS > 0 ? ITEMS : g.items;
+  const int tb = ITEMS > 0 ? TBC : g.tb;
+  const int per_tok = items * 8;
+  const int tasks = tb * per_tok;  // <= 32 * 8
+  __shared__ ItemConst s_ic[kMaxItems];
+  __shared__ float s_nf4[16];
+  __shared__ __align__(16) Nf4Slot s_ring[kWarps][kNf4Depth];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < g.items) init_item_const(s_ic[threadIdx.x], P, seed, threadIdx.x);
+  if (threadIdx.x < 16) s_nf4[threadIdx.x] = __uint_as_float(c_nf4_bits[threadIdx.x]);
+  __syncthreads();
+
+  // phase A of a batch: lane p hashes row p of the batch, stores its sign word and window
+  // offset, and starts the copy of its window
+  auto stage = [&](int64_t batch, Nf4Slot& sl) {
+    const int p = lane;
+    if (p < tb * items) {
+      const int s = p / items, item = p - (p / items) * items;
+      const int64_t tok = batch * tb + s;
+      if (tok < g.N) {
+        const uint32_t t = fastmod(static_cast<uint32_t>(tok), g.fm_L, g.L);
+        uint64_t hs;
+        const uint32_t row = item_row(s_ic[item], P.mode, tokens, canon_map, P.vocab, tok, t, err, &hs);
+        const uint64_t start = static_cast<uint64_t>(row) * 34u;
+        const uint32_t off = static_cast<uint32_t>(start & 15u);
+        sl.sign[p] = mix64(hs + kGolden);
+        sl.off[p] = static_cast<uint8_t>(off);
+        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sl.rows[p]));
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const uint64_t c = start - off + 16u * k;
+          if (c < g.table_bytes) {
+            const uint64_t left = g.table_bytes - c;
+            cp_async16_zfill(dst + 16 * k, table + c, left < 16u ? static_cast<uint32_t>(left) : 16u);
+          }
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+#pragma unroll
+  for (int d = 0; d < kNf4Depth; ++d) {
+    const int64_t b = first + d * nwarps;
+    if (b < g.nbatch) stage(b, s_ring[warp][d]);
+    else cp_async_commit();
+  }
+  int slot = 0;
+  for (int64_t batch = first; batch < g.nbatch; batch += nwarps) {
+    cp_async_wait<kNf4Depth - 1>();  // this lane's copies for `batch` have landed
+    __syncwarp();                    // ... and every other lane's
+    const Nf4Slot& sl = s_ring[warp][slot];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = lane + 32 * i;
+      if (c >= tasks) continue;
+      const int s = ITEMS > 0 ? c / (ITEMS * 8) : c / per_tok;
+      const int cc = c - s * per_tok;
+      const int64_t tok = batch * tb + s;
+      if (tok >= g.N) continue;
+      const int p = s * items + (cc >> 3), piece = cc & 7;
+      const uint8_t* w = sl.rows[p] + sl.off[p];
+      const uint32_t codes = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(w + 4 * piece)) |
+                             (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(w + 4 * piece + 2)) << 16);
+      const float scale = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(w + 32)));
+      const uint32_t bits = static_cast<uint32_t>(sl.sign[p] >> (8 * piece)) & 0xFFu;
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float val = s_nf4[(codes >> (4 * q)) & 15u] * scale;
+        x[q] = ((bits >> q) & 1u) ? -val : val;
+      }
+      uint8_t* out_tok = e_out + static_cast<uint64_t>(tok) * g.e_bytes;
+      if constexpr (OUTT == PG_F32) {
+        uint8_t* dst = out_tok + cc * 32u;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                                                    __float_as_uint(x[2]), __float_as_uint(x[3]));
+        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
+                                                         __float_as_uint(x[6]), __float_as_uint(x[7]));
+      } else {
+        *reinterpret_cast<uint4*>(out_tok + cc * 16u) =
+            make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+      }
+    }
+    __syncwarp();  // every lane is done with the slot before it is refilled
+    const int64_t next = batch + kNf4Depth * nwarps;
+    if (next < g.nbatch) stage(next, s_ring[warp][slot]);
+    else cp_async_commit();
+    slot = slot + 1 == kNf4Depth ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
 using GatherFn = void (*)(const HashParams, uint64_t, const GatherGeom, const int32_t*, const uint32_t*,
                           const uint8_t*, uint8_t*, int32_t*);
 
@@ -349,8 +444,8 @@ GatherFn pick_layout(int row_dtype, int out_dtype, bool flat) {
   if (row_dtype == PG_F32 && out_dtype == PG_F32) return gather_kernel<PG_F32, PG_F32, false, RC, ITEMS>;
   if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return gather_kernel<PG_BF16, PG_BF16, false, RC, ITEMS>;
   if (row_dtype == PG_BF16 && out_dtype == PG_F32) return gather_kernel<PG_BF16, PG_F32, false, RC, ITEMS>;
-  if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_kernel<PG_NF4, PG_BF16, false, RC, ITEMS>;
-  if (row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_kernel<PG_NF4, PG_F32, false, RC, ITEMS>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_nf4_kernel<PG_BF16, 0>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_nf4_kernel<PG_F32, 0>;
   return nullptr;
 }
 
@@ -363,8 +458,8 @@ GatherFn pick_gather(int row_dtype, int out_dtype, bool flat, uint32_t rc, int i
   if (!flat && items == 16) {
     if (rc == 8 && bb) return gather_kernel<PG_BF16, PG_BF16, false, 8, 16>;
     if (rc == 8 && bf) return gather_kernel<PG_BF16, PG_F32, false, 8, 16>;
-    if (rc == 8 && row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_kernel<PG_NF4, PG_BF16, false, 8, 16>;
-    if (rc == 8 && row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_kernel<PG_NF4, PG_F32, false, 8, 16>;
+    if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return gather_nf4_kernel<PG_BF16, 16>;
+    if (row_dtype == PG_NF4 && out_dtype == PG_F32) return gather_nf4_kernel<PG_F32, 16>;
     if (rc == 10 && bb) return gather_kernel<PG_BF16, PG_BF16, false, 10, 16>;
     if (rc == 16 && ff) return gather_kernel<PG_F32, PG_F32, false, 16, 16>;
   }
@@ -461,6 +556,7 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   g.row_bytes = geo.row_bytes;
   g.e_bytes = geo.e_width * (out_dtype == PG_F32 ? 4u : 2u);
   g.nbatch = (N + tb - 1) / tb;
+  g.table_bytes = table_bytes;
 
   const int nsm = sm_count();
   if (nsm == 0) return cuda_fail(cudaGetLastError());
