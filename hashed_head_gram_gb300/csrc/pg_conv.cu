@@ -7,7 +7,8 @@
 //
 // Since u = alpha v, RMSNorm(u) = f v gamma with the per-(branch, position) scalar
 // f = alpha / sqrt(alpha^2 mean(v^2) + eps). A block owns runs of kRun positions of one
-// sequence (persistent grid) and d/8 threads, thread i owning channels [8i, 8i+8):
+// sequence (persistent grid) and d/CPT threads, thread i owning channels [CPT i, CPT i + CPT)
+// (CPT = 4 up to d = 3072, else 8):
 //   1. one warp per position reduces sum(v^2) over the run and its causal halo;
 //   2. f and alpha per (branch, position) go to shared memory;
 //   3. every thread walks its positions by residue class mod dil (so the 4 taps form a
@@ -17,6 +18,8 @@
 // DRAM traffic per token: v once (2d bytes; the taps re-read it from L1/L2) and H read +
 // written once per branch (2 * M * 2d bytes).
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "pg_internal.cuh"
 
@@ -29,18 +32,16 @@ constexpr int kMaxBranches = 8;
 constexpr int kMaxPos = kRun + kMaxHalo;
 constexpr int kTaps = 4;
 
-template <typename T>
-struct Vec8;
+// CPT consecutive channels of one row: load / unpack to fp32 / pack and store.
+template <typename T, int CPT>
+struct VecN;
 
 template <>
-struct Vec8<__nv_bfloat16> {
+struct VecN<__nv_bfloat16, 8> {
   using Raw = uint4;
   static __device__ __forceinline__ Raw zero() { return make_uint4(0, 0, 0, 0); }
   static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
-  }
-  static __device__ __forceinline__ Raw load_rw(const __nv_bfloat16* p) {
-    return *reinterpret_cast<const uint4*>(p);
   }
   static __device__ __forceinline__ void unpack(const Raw& w, float* f) {
     f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
@@ -60,16 +61,30 @@ struct Vec8<__nv_bfloat16> {
 };
 
 template <>
-struct Vec8<float> {
+struct VecN<__nv_bfloat16, 4> {
+  using Raw = uint2;
+  static __device__ __forceinline__ Raw zero() { return make_uint2(0, 0); }
+  static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) {
+    return __ldg(reinterpret_cast<const uint2*>(p));
+  }
+  static __device__ __forceinline__ void unpack(const Raw& w, float* f) {
+    f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* f) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
+    *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+};
+
+template <>
+struct VecN<float, 8> {
   struct Raw {
     float4 a, b;
   };
   static __device__ __forceinline__ Raw zero() { return Raw{make_float4(0, 0, 0, 0), make_float4(0, 0, 0, 0)}; }
   static __device__ __forceinline__ Raw load(const float* p) {
     return Raw{__ldg(reinterpret_cast<const float4*>(p)), __ldg(reinterpret_cast<const float4*>(p + 4))};
-  }
-  static __device__ __forceinline__ Raw load_rw(const float* p) {
-    return Raw{*reinterpret_cast<const float4*>(p), *reinterpret_cast<const float4*>(p + 4)};
   }
   static __device__ __forceinline__ void unpack(const Raw& r, float* f) {
     f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
@@ -81,12 +96,41 @@ struct Vec8<float> {
   }
 };
 
+template <>
+struct VecN<float, 4> {
+  using Raw = float4;
+  static __device__ __forceinline__ Raw zero() { return make_float4(0, 0, 0, 0); }
+  static __device__ __forceinline__ Raw load(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+  static __device__ __forceinline__ void unpack(const Raw& r, float* f) {
+    f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float* f) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+
 // Asynchronous 16-byte global -> shared copies of one thread (L1 bypassed); a thread
 // waits only for its own copies, so no block-wide barrier is involved.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
                "l"(gmem)
                : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+// One thread's asynchronous copy of BYTES (8, 16 or 32) contiguous bytes.
+template <int BYTES>
+__device__ __forceinline__ void cp_async_bytes(void* smem, const void* gmem) {
+  if constexpr (BYTES == 8) {
+    cp_async8(smem, gmem);
+  } else {
+#pragma unroll
+    for (int k = 0; k < BYTES / 16; ++k)
+      cp_async16(static_cast<uint8_t*>(smem) + 16 * k, static_cast<const uint8_t*>(gmem) + 16 * k);
+  }
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -127,35 +171,37 @@ __device__ __forceinline__ uint64_t silu2(uint64_t c) {
   return mul2(c, fma2(pk(0.5f, 0.5f), pk(t0, t1), pk(0.5f, 0.5f)));
 }
 
-// PF: positions of H prefetched ahead of the one being computed (per thread, cp.async).
-template <typename T, int MB, int PF>
-__global__ void __launch_bounds__(512) conv_residual_kernel(
+// PF: positions of H prefetched ahead of the one being computed (per thread, cp.async);
+// CPT: channels per thread (4 gives twice the warps of 8 at half the registers each).
+template <typename T, int MB, int PF, int CPT>
+__global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
     int L, int d, int M_rt, int64_t N, const T* __restrict__ v, const float* __restrict__ alpha,
     const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks, int dil, float eps,
     T* __restrict__ H, int runs_per_seq, int total_runs) {
   constexpr int MMAX = MB > 0 ? MB : kMaxBranches;
   const int M = MB > 0 ? MB : M_rt;
-  __shared__ float s_ms[kMaxPos];
+  __shared__ float s_ms[kMaxPos];  // sum(v^2) per position of the run
   __shared__ float s_f[MMAX][kMaxPos];
   __shared__ float s_a[MMAX][kMaxPos];
-  // H prefetch ring: [PF][M][threads] chunks of 8 channels (16 B bf16 / 32 B fp32)
+  // H prefetch ring: [PF][M][threads] chunks of CPT channels
   extern __shared__ __align__(16) uint8_t s_ring[];
-  using Raw = typename Vec8<T>::Raw;
+  using Vec = VecN<T, CPT>;
+  using Raw = typename Vec::Raw;
   Raw* ring = reinterpret_cast<Raw*>(s_ring);
-  auto ring_at = [&](int slot, int m) -> Raw* { return ring + (slot * MMAX + m) * blockDim.x + threadIdx.x; };
-
-  const int c0 = threadIdx.x * 8;
-  const bool active = c0 < d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  const int chunks = d >> 3;
+  auto ring_at = [&](int slot, int m) -> Raw* { return ring + (slot * MMAX + m) * blockDim.x + threadIdx.x; };
+
+  const int c0 = threadIdx.x * CPT;
+  const bool active = c0 < d;
+  const int chunks8 = d >> 3;
   const int halo = (ks - 1) * dil;
   const float inv_d = 1.0f / static_cast<float>(d);
 
   // conv taps with the RMSNorm gain folded in: wg[j][q] = w[c0+q, j] * gamma[c0+q]
-  float wg[kTaps][8];
+  float wg[kTaps][CPT];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < CPT; ++q) {
     const float g = active ? gamma_c[c0 + q] : 0.f;
 #pragma unroll
     for (int j = 0; j < kTaps; ++j) wg[j][q] = (active && j < ks) ? conv_w[(c0 + q) * ks + j] * g : 0.f;
@@ -169,27 +215,30 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
     const int npos = t1 - p0;
     const int64_t seq0 = static_cast<int64_t>(b) * L;
 
-    // 1. mean(v^2) per position, one warp per position
+    // 1. sum(v^2) per position, one warp per position (16-byte loads, unrolled so each
+    //    lane has several of its row's loads in flight)
     for (int i = warp; i < npos; i += nwarps) {
       const T* row = v + (seq0 + p0 + i) * d;
       float s = 0.f;
-      for (int q = lane; q < chunks; q += 32) {
+#pragma unroll 4
+      for (int q = lane; q < chunks8; q += 32) {
         float x[8];
-        Vec8<T>::unpack(Vec8<T>::load(row + 8 * q), x);
+        VecN<T, 8>::unpack(VecN<T, 8>::load(row + 8 * q), x);
 #pragma unroll
         for (int k = 0; k < 8; ++k) s = fmaf(x[k], x[k], s);
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (lane == 0) s_ms[i] = s * inv_d;
+      if (lane == 0) s_ms[i] = s;
     }
     __syncthreads();
+
     // 2. alpha and f = alpha / sqrt(alpha^2 mean(v^2) + eps) per (branch, position)
     for (int idx = threadIdx.x; idx < M * npos; idx += blockDim.x) {
       const int m = idx / npos, i = idx - (idx / npos) * npos;
       const float a = alpha[m * N + seq0 + p0 + i];
       s_a[m][i] = a;
-      s_f[m][i] = a * rsqrtf(a * a * s_ms[i] + eps);
+      s_f[m][i] = a * rsqrtf(a * a * (s_ms[i] * inv_d) + eps);
     }
     __syncthreads();
 
@@ -208,8 +257,7 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
             if (m >= M) continue;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(H + (m * N + seq0 + t) * d + c0);
             uint8_t* dst = reinterpret_cast<uint8_t*>(ring_at(slot, m));
-#pragma unroll
-            for (int k = 0; k < static_cast<int>(sizeof(Raw) / 16); ++k) cp_async16(dst + 16 * k, src + 16 * k);
+            cp_async_bytes<static_cast<int>(sizeof(Raw))>(dst, src);
           }
         }
         ++pi;
@@ -225,33 +273,34 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
     for (int i = 0; i < PF; ++i) prefetch_next();
     int s = 0;  // sequence index of the position being computed
     for (int r = 0; r < dil && t0 + r < t1; ++r) {
-      float win[kTaps][8];  // v at t - j dil, zero before the start of the sequence
+      float win[kTaps][CPT];  // v at t - j dil, zero before the start of the sequence
 #pragma unroll
       for (int j = 0; j < kTaps; ++j) {
         const int p = t0 + r - j * dil;
         if (active && j < ks && p >= 0) {
-          Vec8<T>::unpack(Vec8<T>::load(v + (seq0 + p) * d + c0), win[j]);
+          Vec::unpack(Vec::load(v + (seq0 + p) * d + c0), win[j]);
         } else {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) win[j][q] = 0.f;
+          for (int q = 0; q < CPT; ++q) win[j][q] = 0.f;
         }
       }
       for (int t = t0 + r; t < t1; t += dil, ++s) {
         const bool has_next = active && t + dil < t1;
-        Raw nxt = Vec8<T>::zero();
-        if (has_next) nxt = Vec8<T>::load(v + (seq0 + t + dil) * d + c0);   // next window row, early
+        Raw nxt = Vec::zero();
+        if (has_next) nxt = Vec::load(v + (seq0 + t + dil) * d + c0);   // next window row, early
         cp_async_wait<PF - 1>();   // this thread's copies for position t have landed
         if (active) {
           const int slot = s % PF;
-          uint64_t prod[kTaps][4];   // (w[:, j] gamma) * v_{t - j dil}, packed pairs
+          constexpr int kPairs = CPT / 2;
+          uint64_t prod[kTaps][kPairs];   // (w[:, j] gamma) * v_{t - j dil}, packed pairs
 #pragma unroll
           for (int j = 0; j < kTaps; ++j)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < kPairs; ++q)
               prod[j][q] = mul2(pk(wg[j][2 * q], wg[j][2 * q + 1]), pk(win[j][2 * q], win[j][2 * q + 1]));
-          uint64_t vt[4];
+          uint64_t vt[kPairs];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) vt[q] = pk(win[0][2 * q], win[0][2 * q + 1]);
+          for (int q = 0; q < kPairs; ++q) vt[q] = pk(win[0][2 * q], win[0][2 * q + 1]);
 #pragma unroll
           for (int m = 0; m < MMAX; ++m) {
             if (m >= M) continue;
@@ -264,17 +313,17 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
             }
             const float a = s_a[m][t - p0];
             const uint64_t aa = pk(a, a);
-            float h[8];
-            Vec8<T>::unpack(*ring_at(slot, m), h);
+            float h[CPT];
+            Vec::unpack(*ring_at(slot, m), h);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kPairs; ++q) {
               uint64_t c = mul2(fj[0], prod[0][q]);
 #pragma unroll
               for (int j = 1; j < kTaps; ++j) c = fma2(fj[j], prod[j][q], c);
               const uint64_t y = fma2(aa, vt[q], silu2(c));           // SiLU(c) + alpha v_t
               upk(add2(pk(h[2 * q], h[2 * q + 1]), y), h[2 * q], h[2 * q + 1]);
             }
-            Vec8<T>::store(H + (m * N + seq0 + t) * d + c0, h);
+            Vec::store(H + (m * N + seq0 + t) * d + c0, h);
           }
         }
         prefetch_next();
@@ -282,8 +331,8 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
 #pragma unroll
         for (int j = kTaps - 1; j > 0; --j)
 #pragma unroll
-          for (int q = 0; q < 8; ++q) win[j][q] = win[j - 1][q];
-        Vec8<T>::unpack(nxt, win[0]);
+          for (int q = 0; q < CPT; ++q) win[j][q] = win[j - 1][q];
+        Vec::unpack(nxt, win[0]);
       }
     }
     cp_async_wait<0>();
@@ -294,13 +343,15 @@ __global__ void __launch_bounds__(512) conv_residual_kernel(
 template <typename T>
 pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, const float* gamma_c,
                  const float* conv_w, int ks, int dil, float eps, void* H, cudaStream_t stream) {
-  const int threads = ((d / 8) + 31) / 32 * 32;
+  // 4 channels per thread up to d = 3072 (768 threads), else 8 (up to 1024 threads)
+  const int cpt = d / 4 <= 768 ? 4 : 8;
+  const int threads = ((d / cpt) + 31) / 32 * 32;
   const int runs_per_seq = (L + kRun - 1) / kRun;
   const int64_t total = static_cast<int64_t>(B) * runs_per_seq;
   if (total >= (1ll << 31)) return PG_ERR_SHAPE;
   const int64_t N = static_cast<int64_t>(B) * L;
   auto run = [&](auto kern, int mmax, int pf) -> pg_status {
-    const size_t ring = static_cast<size_t>(pf) * mmax * threads * (sizeof(T) * 8);
+    const size_t ring = static_cast<size_t>(pf) * mmax * threads * (sizeof(T) * cpt);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring));
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
@@ -314,15 +365,20 @@ pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, 
     return after_launch(1);
   };
   // prefetch depth: 4 positions while the ring fits in 192 KB of shared memory, else 1
-  const bool deep = 4ull * (M == 1 || M == 2 || M == 4 ? M : kMaxBranches) * threads * sizeof(T) * 8 <= (192u << 10);
-  switch (M) {
-    case 1: return deep ? run(conv_residual_kernel<T, 1, 4>, 1, 4) : run(conv_residual_kernel<T, 1, 1>, 1, 1);
-    case 2: return deep ? run(conv_residual_kernel<T, 2, 4>, 2, 4) : run(conv_residual_kernel<T, 2, 1>, 2, 1);
-    case 4: return deep ? run(conv_residual_kernel<T, 4, 4>, 4, 4) : run(conv_residual_kernel<T, 4, 1>, 4, 1);
-    default:
-      return deep ? run(conv_residual_kernel<T, 0, 4>, kMaxBranches, 4)
-                  : run(conv_residual_kernel<T, 0, 1>, kMaxBranches, 1);
-  }
+  const int mm = M == 1 || M == 2 || M == 4 ? M : kMaxBranches;
+  const bool deep = 4ull * mm * threads * sizeof(T) * cpt <= (192u << 10);
+  auto pick = [&](auto cpt_c) -> pg_status {
+    constexpr int C = decltype(cpt_c)::value;
+    switch (M) {
+      case 1: return deep ? run(conv_residual_kernel<T, 1, 4, C>, 1, 4) : run(conv_residual_kernel<T, 1, 1, C>, 1, 1);
+      case 2: return deep ? run(conv_residual_kernel<T, 2, 4, C>, 2, 4) : run(conv_residual_kernel<T, 2, 1, C>, 2, 1);
+      case 4: return deep ? run(conv_residual_kernel<T, 4, 4, C>, 4, 4) : run(conv_residual_kernel<T, 4, 1, C>, 4, 1);
+      default:
+        return deep ? run(conv_residual_kernel<T, 0, 4, C>, kMaxBranches, 4)
+                    : run(conv_residual_kernel<T, 0, 1, C>, kMaxBranches, 1);
+    }
+  };
+  return cpt == 4 ? pick(std::integral_constant<int, 4>()) : pick(std::integral_constant<int, 8>());
 }
 
 }  // namespace

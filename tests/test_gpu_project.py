@@ -124,8 +124,11 @@ def _conv_case(B, L, d, M, seed, zero_w=False, dtype=torch.bfloat16):
     return v, alpha, gc, w, H
 
 
+# d <= 3072 runs 4 channels per thread, larger d 8 (d = 8192: 1024 threads); M = 3 takes the
+# runtime-branch-count kernel
 @pytest.mark.parametrize("B,L,d,M,dtype", [(2, 75, 2560, 4, torch.bfloat16), (3, 16, 64, 2, torch.bfloat16),
-                                           (1, 40, 256, 3, torch.float32), (2, 9, 512, 1, torch.bfloat16)])
+                                           (1, 40, 256, 3, torch.float32), (2, 9, 512, 1, torch.bfloat16),
+                                           (1, 37, 4608, 2, torch.bfloat16), (1, 20, 8192, 1, torch.float32)])
 def test_conv_residual(cuda, B, L, d, M, dtype):
     pg = _pg()
     v, alpha, gc, w, H = _conv_case(B, L, d, M, 14, dtype=dtype)
