@@ -422,7 +422,8 @@ def run_gpu(args):
 TRAFFIC = {
     (2, "gather_sign_concat"): ("pg_lookup.cu", "363776ab493496dd", 184.213760e6),
     (2, "project_gate"): ("pg_project.cu", "32db704fcfaa0396", 310.721792e6),
-    (5, "conv_residual"): ("pg_conv.cu", "f87b93f460b8b792", 1500.525568e6),
+    (4, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 190.3e6),
+    (5, "conv_residual"): ("pg_conv.cu", "dd5069ec32c6d52b", 1504.91392e6),
 }
 
 
