@@ -32,6 +32,10 @@ if ROOT not in sys.path:
 METRIC = "N-gram memory lookup tokens/s (1 GB300) and % of HBM / tensor roofline"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The fp32 projection runs on the FP32 FMA pipes, not the tensor cores: its peak is derived
+# from the unit counts, 152 SMs x 128 FP32 lanes x 2 flop per FMA x 2.07 GHz (maximum SM
+# clock), and reported as an ALU bound.
+FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 # ---------------------------------------------------------------- rank / sharding helpers
@@ -231,7 +235,7 @@ class Pipeline:
             return "hbm", per * N
         if name in ("project_gate", "lookup_project_gate"):
             cols = d * (1 + w.M)
-            return "tensor", 2.0 * N * din * cols
+            return ("alu" if w.dtype == self.W.DT_F32 else "tensor"), 2.0 * N * din * cols
         # conv: read v, read + write H for every branch
         return "hbm", N * (d * 2 + 2 * w.M * d * 2)
 
@@ -350,6 +354,8 @@ def run_gpu(args):
     traffic = traffic_of(args.config, dom)
     if bound == "hbm":
         achieved, peak, unit = work / dur_s / 1e9, float(peaks["hbm_gbs"]), "GB/s"
+    elif bound == "alu":
+        achieved, peak, unit = work / dur_s / 1e12, round(FP32_FFMA_TFLOPS, 1), "TFLOP/s"
     else:
         achieved, peak, unit = work / dur_s / 1e12, float(peaks["bf16_tflops"]), "TFLOP/s"
     kernels = {}
@@ -359,6 +365,9 @@ def run_gpu(args):
         if b == "hbm":
             kernels[name] = {"ms": round(ms, 5), "GB/s": round(wk / (ms / 1e3) / 1e9, 1),
                              "frac_hbm": round(wk / (ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
+        elif b == "alu":
+            kernels[name] = {"ms": round(ms, 5), "TFLOP/s": round(wk / (ms / 1e3) / 1e12, 1),
+                             "frac_fp32_ffma": round(wk / (ms / 1e3) / 1e12 / FP32_FFMA_TFLOPS, 4)}
         else:
             kernels[name] = {"ms": round(ms, 5), "TFLOP/s": round(wk / (ms / 1e3) / 1e12, 1),
                              "frac_tensor": round(wk / (ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]), 4)}
@@ -389,7 +398,8 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(step_ms), 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if p.w.dtype == p.W.DT_F32 else "bf16",
             "data": "synthetic: seeded Zipf token IDs, int8/64 table values, N(0,0.02) weights, N(0,1) states",
             "config": workload_config(p.w, world),
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -397,7 +407,8 @@ def run_gpu(args):
             "gpu_launches": launches,
             "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})"},
+                         "peak_source": ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz" if bound == "alu"
+                                         else f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})")},
             "kernels": kernels,
             "path": args.path if p.can_fuse() else "two_kernel",
             "other_path": other,
@@ -420,10 +431,13 @@ def run_gpu(args):
 # time of the capture; reported only while the source is unchanged (profiles/ holds the
 # captures).
 TRAFFIC = {
-    (2, "gather_sign_concat"): ("pg_lookup.cu", "363776ab493496dd", 184.213760e6),
-    (2, "project_gate"): ("pg_project.cu", "32db704fcfaa0396", 310.721792e6),
+    (2, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 180.541696e6),
+    (2, "project_gate"): ("pg_project.cu", "19495a9a1d30483f", 307.746048e6),
+    (2, "lookup_project_gate"): ("pg_project.cu", "19495a9a1d30483f", 274.214912e6),
     (4, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 190.3e6),
-    (5, "conv_residual"): ("pg_conv.cu", "dd5069ec32c6d52b", 1504.91392e6),
+    (5, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 142.978816e6),
+    (5, "project_gate"): ("pg_project.cu", "19495a9a1d30483f", 1088.25984e6),
+    (5, "conv_residual"): ("pg_conv.cu", "dd5069ec32c6d52b", 1501.8176e6),
 }
 
 

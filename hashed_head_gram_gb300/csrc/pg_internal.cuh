@@ -65,4 +65,16 @@ struct HashParams {
 
 void fill_hash_params(const pg_table_desc* d, const Geometry& g, HashParams* p);
 
+// ---------------------------------------------------------------- projections without tensor cores
+
+// fp32 out[N, d] = e[N, Din] W[d, Din]^T, plus x + g * out for the scalar gate
+// (pg_project_simt.cu). One launch.
+pg_status launch_simt_f32(int N, int Din, int d, int gate_kind, const float* e, const float* W, float g,
+                          const float* x, float* out, cudaStream_t stream);
+
+// W == NULL: out = e, or x + g e for the scalar gate, over n elements of dtype (n % 8 == 0,
+// 16-byte aligned). One launch.
+pg_status launch_identity_gate(int64_t n, int dtype, int gate_kind, const void* e, const void* x, float g,
+                               void* out, cudaStream_t stream);
+
 }  // namespace pg

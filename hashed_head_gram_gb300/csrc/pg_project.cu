@@ -14,7 +14,7 @@
 //   warps 2..5  epilogue: tcgen05.ld 32x32b (thread = output row), gate math, stores;
 //               context-gate tiles reduce per-row partial sums instead of storing
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
-// fp32: a register-tiled SIMT FFMA GEMM (fp32 tolerance 1e-5 rules out TF32).
+// fp32 and W == NULL: pg_project_simt.cu.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -892,91 +892,6 @@ __global__ void __launch_bounds__(256) alpha_finalize_kernel(const float* __rest
   alpha[idx] = 1.0f / (1.0f + expf(-s));
 }
 
-// ==================================================================== fp32 SIMT GEMM
-
-constexpr int kSimtTile = 64;
-constexpr int kSimtK = 16;
-
-// out[N, Dout] = A[N, Din] B[Dout, Din]^T (+ gate); 256 threads, 4x4 outputs each.
-template <int GATE>
-__global__ void __launch_bounds__(256) simt_gemm_f32_kernel(const float* __restrict__ A,
-                                                            const float* __restrict__ Bw, int N,
-                                                            int Din, int Dout, const float* __restrict__ x,
-                                                            float g, float* __restrict__ out) {
-  __shared__ float As[kSimtK][kSimtTile + 4];
-  __shared__ float Bs[kSimtK][kSimtTile + 4];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int m0 = blockIdx.y * kSimtTile, n0 = blockIdx.x * kSimtTile;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < Din; k0 += kSimtK) {
-    for (int i = threadIdx.x; i < kSimtTile * kSimtK; i += 256) {
-      const int r = i / kSimtK, kk = i - (i / kSimtK) * kSimtK;
-      As[kk][r] = (m0 + r < N && k0 + kk < Din) ? A[static_cast<size_t>(m0 + r) * Din + k0 + kk] : 0.f;
-      Bs[kk][r] = (n0 + r < Dout && k0 + kk < Din) ? Bw[static_cast<size_t>(n0 + r) * Din + k0 + kk] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < kSimtK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = As[kk][ty + 16 * i];
-        b[i] = Bs[kk][tx + 16 * i];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = m0 + ty + 16 * i, c = n0 + tx + 16 * j;
-      if (r < N && c < Dout) {
-        const size_t off = static_cast<size_t>(r) * Dout + c;
-        out[off] = GATE == PG_GATE_SCALAR ? fmaf(g, acc[i][j], x[off]) : acc[i][j];
-      }
-    }
-}
-
-// ==================================================================== identity projection
-
-// W == NULL (Din == d): v = e, or x + g e for the scalar gate; 8 elements per thread.
-template <typename T, int GATE>
-__global__ void __launch_bounds__(256) identity_gate_kernel(const T* __restrict__ e, const T* __restrict__ x,
-                                                            float g, T* __restrict__ out, int64_t n) {
-  for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 8; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x * 8) {
-    if constexpr (sizeof(T) == 2) {
-      const uint4 ev = *reinterpret_cast<const uint4*>(e + i);
-      float ef[8], o[8];
-      unpack_bf16x8(ev, ef);
-      if (GATE == PG_GATE_SCALAR) {
-        float xf[8];
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(x + i), xf);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) o[q] = fmaf(g, ef[q], xf[q]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) o[q] = ef[q];
-      }
-      *reinterpret_cast<uint4*>(out + i) = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]),
-                                                      pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        out[i + q] = GATE == PG_GATE_SCALAR ? fmaf(g, e[i + q], x[i + q]) : e[i + q];
-    }
-  }
-}
-
 // ==================================================================== host side
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1126,35 +1041,13 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   if (!W) {  // identity projection: a flat table's e_t is already d wide
     if (Din != d) return PG_ERR_SHAPE;
     if (d % 8) return PG_ERR_UNSUPPORTED;
-    const int64_t n = static_cast<int64_t>(N) * d;
-    const int64_t want = (n / 8 + 255) / 256;
-    const int blocks = static_cast<int>(want < sm_count() * 8ll ? want : sm_count() * 8ll);
-    if (dtype == PG_BF16) {
-      auto* eb = static_cast<const __nv_bfloat16*>(e);
-      auto* xb = static_cast<const __nv_bfloat16*>(x_resid);
-      auto* ob = static_cast<__nv_bfloat16*>(v_out);
-      if (gate_kind == PG_GATE_SCALAR) identity_gate_kernel<__nv_bfloat16, PG_GATE_SCALAR><<<blocks, 256, 0, stream>>>(eb, xb, g, ob, n);
-      else identity_gate_kernel<__nv_bfloat16, PG_GATE_NONE><<<blocks, 256, 0, stream>>>(eb, xb, g, ob, n);
-    } else {
-      auto* ef = static_cast<const float*>(e);
-      auto* xf = static_cast<const float*>(x_resid);
-      auto* of = static_cast<float*>(v_out);
-      if (gate_kind == PG_GATE_SCALAR) identity_gate_kernel<float, PG_GATE_SCALAR><<<blocks, 256, 0, stream>>>(ef, xf, g, of, n);
-      else identity_gate_kernel<float, PG_GATE_NONE><<<blocks, 256, 0, stream>>>(ef, xf, g, of, n);
-    }
-    return after_launch(1);
+    return launch_identity_gate(static_cast<int64_t>(N) * d, dtype, gate_kind, e, x_resid, g, v_out, stream);
   }
 
   if (dtype == PG_F32) {
     if (gate_kind == PG_GATE_CONTEXT) return PG_ERR_UNSUPPORTED;
-    dim3 grid((d + kSimtTile - 1) / kSimtTile, (N + kSimtTile - 1) / kSimtTile);
-    auto* A = static_cast<const float*>(e);
-    auto* B = static_cast<const float*>(W);
-    auto* x = static_cast<const float*>(x_resid);
-    auto* out = static_cast<float*>(v_out);
-    if (gate_kind == PG_GATE_SCALAR) simt_gemm_f32_kernel<PG_GATE_SCALAR><<<grid, 256, 0, stream>>>(A, B, N, Din, d, x, g, out);
-    else simt_gemm_f32_kernel<PG_GATE_NONE><<<grid, 256, 0, stream>>>(A, B, N, Din, d, x, g, out);
-    return after_launch(1);
+    return launch_simt_f32(N, Din, d, gate_kind, static_cast<const float*>(e), static_cast<const float*>(W), g,
+                           static_cast<const float*>(x_resid), static_cast<float*>(v_out), stream);
   }
 
   // bf16 tensor-core path
