@@ -432,11 +432,11 @@ def run_gpu(args):
 # captures).
 TRAFFIC = {
     (2, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 180.541696e6),
-    (2, "project_gate"): ("pg_project.cu", "19495a9a1d30483f", 307.746048e6),
-    (2, "lookup_project_gate"): ("pg_project.cu", "19495a9a1d30483f", 274.214912e6),
+    (2, "project_gate"): ("pg_project.cu", "429cd1a9337dc7c2", 307.035648e6),
+    (2, "lookup_project_gate"): ("pg_project.cu", "429cd1a9337dc7c2", 274.157824e6),
     (4, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 190.3e6),
     (5, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 142.978816e6),
-    (5, "project_gate"): ("pg_project.cu", "19495a9a1d30483f", 1088.25984e6),
+    (5, "project_gate"): ("pg_project.cu", "429cd1a9337dc7c2", 1065.460992e6),
     (5, "conv_residual"): ("pg_conv.cu", "dd5069ec32c6d52b", 1501.8176e6),
 }
 

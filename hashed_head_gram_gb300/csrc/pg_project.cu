@@ -524,6 +524,19 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
           }
         }
       }
+      // Tail: wait until the MMA has released the last fill of every stage. Its commits
+      // arrive asynchronously (on the other CTA of a pair too); none may land after the
+      // CTA has exited. (A stage never filled passes at once.)
+      for (int i = 0; ok && i < kSt; ++i) {
+        if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        if (++stage == kSt) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
       if (!ok) {
         atomicOr(args.err_word, 1);
         *abort = 1;
