@@ -225,6 +225,36 @@ class Pipeline:
             return self.e
         return self.dn["H"] if self.w.gate == self.W.GATE_CONTEXT else self.out
 
+    # The end-to-end loop double-buffers what crosses the host link (token IDs and x in,
+    # the result out; the branch states H, updated in place, for the context gate).
+    def make_slots(self):
+        torch = self.torch
+        base = {"tokens": self.tokens}
+        if hasattr(self, "x_host"):
+            base["x"] = self.dn["x"]
+        if self.w.gate == self.W.GATE_CONTEXT:
+            base["H"] = self.dn["H"]
+        elif self.w.cfg_id == 4:
+            base["e"] = self.e
+        else:
+            base["out"] = self.out
+        other = {k: torch.empty_like(v) for k, v in base.items()}
+        for k in other:
+            other[k].copy_(base[k])
+        self.slots = [base, other]
+
+    def use_slot(self, k):
+        sl = self.slots[k]
+        self.tokens = sl["tokens"]
+        if "x" in sl:
+            self.dn["x"] = sl["x"]
+        if "H" in sl:
+            self.dn["H"] = sl["H"]
+        if "e" in sl:
+            self.e = sl["e"]
+        if "out" in sl:
+            self.out = sl["out"]
+
     # algorithmic work per launch ("Roofline")
     def algorithmic(self, name):
         N, din, d, w = self.N, self.din, self.d, self.w
@@ -318,32 +348,50 @@ def run_gpu(args):
     total_s = reduce_max(sum(step_ms) / 1e3, world)
     value = whole_job_rate(p.N * args.steps, world, total_s)
 
-    # ---- end to end through the C ABI with host buffers
-    e2e_ms = []
+    # ---- end to end through the C ABI with host buffers: every step uploads its token IDs
+    #      (and x) from pinned host memory and reads its whole result back; steps are
+    #      pipelined (uploads on one copy stream, kernels on the launching stream, read-backs
+    #      on another, double-buffered device tensors) as a serving loop would run them
     h2d = p.tokens_host.numel() * 4 + (p.x_host.numel() * 2 if hasattr(p, "x_host") else 0)
-    res = p.result_tensor()
-    res_host = (p.out_host if res.shape == p.out_host.shape and res.dtype == p.out_host.dtype
-                else torch.empty_like(res, device="cpu").pin_memory())
+    p.make_slots()
+    res0 = p.result_tensor()
+    res_hosts = [torch.empty_like(res0, device="cpu").pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    e2e_steps = max(2, min(args.steps, 200))
     barrier(world)
     torch.cuda.synchronize()
-    e2e_steps = max(1, min(args.steps, 200))
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    t_e0, t_e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_e0.record(s_in)
     for i in range(e2e_steps):
-        e0[i].record(stream)
-        p.tokens.copy_(p.tokens_host, non_blocking=True)
-        if hasattr(p, "x_host"):
-            p.dn["x"].copy_(p.x_host, non_blocking=True)
+        k = i % 2
+        sl = p.slots[k]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[k])    # step i-2's kernels are done with slot k's inputs
+            sl["tokens"].copy_(p.tokens_host, non_blocking=True)
+            if "x" in sl:
+                sl["x"].copy_(p.x_host, non_blocking=True)
+            ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        if i >= 2:
+            stream.wait_event(ev_out[k])       # step i-2's result in slot k has been read back
+        p.use_slot(k)
         for _, fn in stages:
             fn()
-        res_host.copy_(res, non_blocking=True)
-        e1[i].record(stream)
-        flush_l2(flush)
+        ev_comp[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[k])
+            res_hosts[k].copy_(p.result_tensor(), non_blocking=True)
+            ev_out[k].record(s_out)
+    t_e1.record(s_out)
     torch.cuda.synchronize()
-    e2e_ms = [e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)]
-    e2e_s = reduce_max(sum(e2e_ms) / 1e3, world)
+    p.use_slot(0)
+    e2e_s = reduce_max(t_e0.elapsed_time(t_e1) / 1e3, world)
     e2e_value = whole_job_rate(p.N * e2e_steps, world, e2e_s)
-    d2h = res.numel() * res.element_size()
+    d2h = res0.numel() * res0.element_size()
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
@@ -403,7 +451,11 @@ def run_gpu(args):
             "data": "synthetic: seeded Zipf token IDs, int8/64 table values, N(0,0.02) weights, N(0,1) states",
             "config": workload_config(p.w, world),
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "how": f"{e2e_steps} steps pipelined: each uploads its inputs from pinned host memory and "
+                           "reads its whole result back; uploads, kernels and read-backs of consecutive steps "
+                           "overlap on three streams (double-buffered device tensors); no L2 flush (inputs "
+                           "> L2 except the tiny workload)"},
             "gpu_launches": launches,
             "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                          "frac": round(achieved / peak, 4), "traffic": traffic,
