@@ -170,6 +170,7 @@ class Pipeline:
         else:
             self.v = torch.empty(self.N, self.d, dtype=torch.bfloat16, device=dev)
             self.alpha = torch.empty(w.M, self.N, device=dev)
+            self.v_ms = torch.empty(self.N, device=dev)  # mean(v^2) per token, projection -> conv
             nws = pg.workspace_size(self.N, self.din, self.d, w.M, pg.BF16, pg.GATE_CONTEXT)
             self.ws = torch.empty(nws // 4, device=dev)
             self.H0 = dn["H"].clone()
@@ -187,12 +188,12 @@ class Pipeline:
         else:
             pg.project_gate(self.e, dn["W"], self.d, pg.GATE_CONTEXT, self.v, pg.BF16, M=w.M, h=dn["H"],
                             gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=self.alpha,
-                            workspace=self.ws)
+                            workspace=self.ws, v_ms_out=self.v_ms)
 
     def conv(self):
         pg, w, dn = self.pg, self.w, self.dn
         pg.conv_residual(w.B, w.L, self.d, w.M, pg.BF16, self.v, self.alpha, dn["gamma_c"], dn["conv_w"], dn["H"],
-                         dilation=w.dilation, eps=w.eps)
+                         dilation=w.dilation, eps=w.eps, v_ms=self.v_ms)
 
     def fused(self):
         pg, w, dn = self.pg, self.w, self.dn

@@ -176,6 +176,7 @@ __device__ __forceinline__ uint64_t silu2(uint64_t c) {
 template <typename T, int MB, int PF, int CPT>
 __global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
     int L, int d, int M_rt, int64_t N, const T* __restrict__ v, const float* __restrict__ alpha,
+    const float* __restrict__ v_ms,
     const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks, int dil, float eps,
     T* __restrict__ H, int runs_per_seq, int total_runs) {
   constexpr int MMAX = MB > 0 ? MB : kMaxBranches;
@@ -215,9 +216,12 @@ __global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
     const int npos = t1 - p0;
     const int64_t seq0 = static_cast<int64_t>(b) * L;
 
-    // 1. sum(v^2) per position, one warp per position (16-byte loads, unrolled so each
-    //    lane has several of its row's loads in flight)
-    for (int i = warp; i < npos; i += nwarps) {
+    // 1. sum(v^2) per position: given (v_ms, the projection's mean(v^2)), or one warp per
+    //    position (16-byte loads, unrolled so each lane has several of its row's loads in
+    //    flight)
+    if (v_ms)
+      for (int i = threadIdx.x; i < npos; i += blockDim.x) s_ms[i] = v_ms[seq0 + p0 + i] * static_cast<float>(d);
+    for (int i = warp; !v_ms && i < npos; i += nwarps) {
       const T* row = v + (seq0 + p0 + i) * d;
       float s = 0.f;
 #pragma unroll 4
@@ -341,8 +345,8 @@ __global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
 }
 
 template <typename T>
-pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, const float* gamma_c,
-                 const float* conv_w, int ks, int dil, float eps, void* H, cudaStream_t stream) {
+pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, const float* v_ms,
+                 const float* gamma_c, const float* conv_w, int ks, int dil, float eps, void* H, cudaStream_t stream) {
   // 4 channels per thread up to d = 3072 (768 threads), else 8 (up to 1024 threads)
   const int cpt = d / 4 <= 768 ? 4 : 8;
   const int threads = ((d / cpt) + 31) / 32 * 32;
@@ -360,8 +364,8 @@ pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, 
     if (per_sm < 1) return PG_ERR_UNSUPPORTED;
     const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
     const int grid = static_cast<int>(total < cap ? total : cap);
-    kern<<<grid, threads, ring, stream>>>(L, d, M, N, static_cast<const T*>(v), alpha, gamma_c, conv_w, ks, dil,
-                                          eps, static_cast<T*>(H), runs_per_seq, static_cast<int>(total));
+    kern<<<grid, threads, ring, stream>>>(L, d, M, N, static_cast<const T*>(v), alpha, v_ms, gamma_c, conv_w, ks,
+                                          dil, eps, static_cast<T*>(H), runs_per_seq, static_cast<int>(total));
     return after_launch(1);
   };
   // prefetch depth: 4 positions while the ring fits in 192 KB of shared memory, else 1
@@ -385,7 +389,7 @@ pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, 
 }  // namespace pg
 
 extern "C" pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M, int32_t dtype,
-                                      const void* v, const float* alpha, const float* gamma_c,
+                                      const void* v, const float* alpha, const float* v_ms, const float* gamma_c,
                                       const float* conv_w, int32_t kernel_size, int32_t dilation,
                                       float eps, void* H, pg_stream_t stream_) {
   using namespace pg;
@@ -399,6 +403,7 @@ extern "C" pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M
   if ((reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(H)) & 15u) return PG_ERR_ALIGN;
   if (sm_count() == 0) return cuda_fail(cudaGetLastError());
   if (dtype == PG_BF16)
-    return launch<__nv_bfloat16>(B, L, d, M, v, alpha, gamma_c, conv_w, kernel_size, dilation, eps, H, stream);
-  return launch<float>(B, L, d, M, v, alpha, gamma_c, conv_w, kernel_size, dilation, eps, H, stream);
+    return launch<__nv_bfloat16>(B, L, d, M, v, alpha, v_ms, gamma_c, conv_w, kernel_size, dilation, eps, H,
+                                 stream);
+  return launch<float>(B, L, d, M, v, alpha, v_ms, gamma_c, conv_w, kernel_size, dilation, eps, H, stream);
 }

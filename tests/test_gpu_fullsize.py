@@ -107,11 +107,12 @@ def test_full_engram27b_module(cuda):
     H0 = H.clone()
     v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
     alpha = torch.empty(M, N, device=cuda)
+    v_ms = torch.empty(N, device=cuda)   # the module as the benchmark runs it: mean(v^2) handed over
     ws = torch.empty(pg.workspace_size(N, din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4, device=cuda)
     pg.project_gate(e, dn["W"], d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=H, gamma_h=dn["gamma_h"],
-                    gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=alpha, workspace=ws)
+                    gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=alpha, workspace=ws, v_ms_out=v_ms)
     pg.conv_residual(w.B, w.L, d, M, pg.BF16, v, alpha, dn["gamma_c"], dn["conv_w"], H, dilation=w.dilation,
-                     eps=w.eps)
+                     eps=w.eps, v_ms=v_ms)
     torch.cuda.synchronize()
     assert pg.device_error() == 0
     Wf = to_f64(dn["W"])

@@ -74,9 +74,11 @@ def test_tcgen05_context_gate(cuda, N, Din, d, M):
     gk = torch.rand(d, generator=_gen(11)) + 0.5
     v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
     alpha = torch.empty(M, N, device=cuda)
+    v_ms = torch.empty(N, device=cuda)
     ws = torch.empty(pg.workspace_size(N, Din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4, device=cuda)
     pg.project_gate(e.to(cuda), Wm.to(cuda), d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=h.to(cuda),
-                    gamma_h=gh.to(cuda), gamma_k=gk.to(cuda), eps=1e-6, alpha_out=alpha, workspace=ws)
+                    gamma_h=gh.to(cuda), gamma_k=gk.to(cuda), eps=1e-6, alpha_out=alpha, workspace=ws,
+                    v_ms_out=v_ms)
     torch.cuda.synchronize()
     assert pg.device_error() == 0
     v_ref, a_ref = dense.engram_gate(e.double().numpy(), Wm.double().numpy(), h.double().numpy(),
@@ -84,6 +86,18 @@ def test_tcgen05_context_gate(cuda, N, Din, d, M):
     assert rel_l2(to_f64(v), v_ref) <= BF16_TOL
     assert rel_l2(to_f64(alpha), a_ref) <= BF16_TOL
     assert np.abs(to_f64(alpha) - a_ref).max() < 1e-3
+    # mean(v^2) of the stored (bf16) v: fp32 sums of exact squares, so ~1e-6 relative
+    ms_stored = (to_f64(v) ** 2).mean(axis=1)
+    assert np.abs(to_f64(v_ms) - ms_stored).max() <= 1e-5 * ms_stored.max()
+    assert rel_l2(to_f64(v_ms), (v_ref ** 2).mean(axis=1)) <= BF16_TOL
+    # the same call without v_ms_out needs no room for it
+    need = M * (d // (256 if d % 256 == 0 else 128)) * 3 * N * 4
+    alpha2 = torch.empty_like(alpha)
+    pg.project_gate(e.to(cuda), Wm.to(cuda), d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=h.to(cuda),
+                    gamma_h=gh.to(cuda), gamma_k=gk.to(cuda), eps=1e-6, alpha_out=alpha2,
+                    workspace=ws[:need // 4])
+    torch.cuda.synchronize()
+    assert torch.equal(alpha, alpha2)
 
 
 def test_context_gate_rejects_small_workspace(cuda):
@@ -93,13 +107,16 @@ def test_context_gate_rejects_small_workspace(cuda):
     Wm = torch.zeros((1 + M) * d, Din, dtype=torch.bfloat16, device=cuda)
     h = torch.zeros(M, N, d, dtype=torch.bfloat16, device=cuda)
     g1 = torch.ones(d, device=cuda)
-    need = pg.workspace_size(N, Din, d, M, pg.BF16, pg.GATE_CONTEXT)
-    ws = torch.empty(need // 4 - 1, device=cuda)
-    with pytest.raises(pg.PgError) as ex:
-        pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, torch.empty(N, d, dtype=torch.bfloat16, device=cuda),
-                        pg.BF16, M=M, h=h, gamma_h=g1, gamma_k=g1, alpha_out=torch.empty(M, N, device=cuda),
-                        workspace=ws)
-    assert ex.value.status == 8
+    need = pg.workspace_size(N, Din, d, M, pg.BF16, pg.GATE_CONTEXT)   # includes the v_ms_out room
+    base = M * (d // 256) * 3 * N * 4
+    assert need == base + (d // 256) * N * 4
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    a = torch.empty(M, N, device=cuda)
+    for nbytes, v_ms in ((base - 4, None), (need - 4, torch.empty(N, device=cuda))):
+        with pytest.raises(pg.PgError) as ex:
+            pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=h, gamma_h=g1, gamma_k=g1, alpha_out=a,
+                            workspace=torch.empty(nbytes // 4, device=cuda), v_ms_out=v_ms)
+        assert ex.value.status == 8
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -129,12 +146,15 @@ def _conv_case(B, L, d, M, seed, zero_w=False, dtype=torch.bfloat16):
 @pytest.mark.parametrize("B,L,d,M,dtype", [(2, 75, 2560, 4, torch.bfloat16), (3, 16, 64, 2, torch.bfloat16),
                                            (1, 40, 256, 3, torch.float32), (2, 9, 512, 1, torch.bfloat16),
                                            (1, 37, 4608, 2, torch.bfloat16), (1, 20, 8192, 1, torch.float32)])
-def test_conv_residual(cuda, B, L, d, M, dtype):
+@pytest.mark.parametrize("given_ms", [False, True])
+def test_conv_residual(cuda, B, L, d, M, dtype, given_ms):
     pg = _pg()
     v, alpha, gc, w, H = _conv_case(B, L, d, M, 14, dtype=dtype)
     Hd = H.to(cuda)
+    # given_ms: mean(v^2) supplied (as pg_project_gate's v_ms_out would), else computed inside
+    v_ms = (v.double() ** 2).mean(dim=1).float().to(cuda) if given_ms else None
     pg.conv_residual(B, L, d, M, pg.dtype_code(dtype), v.to(cuda), alpha.to(cuda), gc.to(cuda), w.to(cuda), Hd,
-                     dilation=3, eps=1e-6)
+                     dilation=3, eps=1e-6, v_ms=v_ms)
     ref = dense.conv_residual(v.double().numpy().reshape(B, L, d), alpha.double().numpy().reshape(M, B, L),
                               gc.double().numpy(), w.double().numpy(), 3, 1e-6,
                               H.double().numpy().reshape(M, B, L, d))
