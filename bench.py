@@ -490,7 +490,7 @@ TRAFFIC = {
     (4, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 190.3e6),
     (5, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 142.978816e6),
     (5, "project_gate"): ("pg_project.cu", "429cd1a9337dc7c2", 1065.460992e6),
-    (5, "conv_residual"): ("pg_conv.cu", "dd5069ec32c6d52b", 1501.8176e6),
+    (5, "conv_residual"): ("pg_conv.cu", "597024b7d69714ca", 1466.725888e6),
 }
 
 

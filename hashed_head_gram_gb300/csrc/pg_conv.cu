@@ -6,20 +6,25 @@
 // the conv to be causal.
 //
 // Since u = alpha v, RMSNorm(u) = f v gamma with the per-(branch, position) scalar
-// f = alpha / sqrt(alpha^2 mean(v^2) + eps). A block owns runs of kRun positions of one
-// sequence (persistent grid) and d/CPT threads, thread i owning channels [CPT i, CPT i + CPT)
-// (CPT = 4 up to d = 3072, else 8):
-//   1. one warp per position reduces sum(v^2) over the run and its causal halo;
-//   2. f and alpha per (branch, position) go to shared memory;
+// f = alpha / sqrt(alpha^2 mean(v^2) + eps). A block owns one channel slice of runs of kRun
+// positions of one sequence (persistent grid), thread i owning channels [4 i, 4 i + 4) of the
+// slice. Slices are 512 channels (4 warps; six blocks fill an SM's 24 warp slots at 80
+// registers) when mean(v^2) is handed over, else up to 3072 (every block then reads whole
+// rows for its sums, so fewer and wider slices):
+//   1. mean(v^2) per position of the run and its causal halo: handed over by the caller
+//      (the projection's epilogue has it), else one warp per position reduces it;
+//   2. per (branch, position) the four tap scalars f_{t - j dil} and alpha_t go to shared
+//      memory as duplicated pairs, so one thread reads all of them with three vector loads;
 //   3. every thread walks its positions by residue class mod dil (so the 4 taps form a
-//      window sliding one row per step): c = sum_j f_{t-j dil} (w[:, j] gamma) v_{t-j dil},
+//      window of rows that rotates by one row per step, held in registers under a 4-way
+//      unrolled walk), c = sum_j f_{t-j dil} (w[:, j] gamma) v_{t-j dil},
 //      H[m, t] += SiLU(c) + alpha_t v_t for all M branches, in packed fp32x2 arithmetic,
 //      with H of the next positions prefetched into shared memory by cp.async.
 // DRAM traffic per token: v once (2d bytes; the taps re-read it from L1/L2) and H read +
 // written once per branch (2 * M * 2d bytes).
 #include <cuda_bf16.h>
 
-#include <type_traits>
+#include <algorithm>
 
 #include "pg_internal.cuh"
 
@@ -161,54 +166,72 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// SiLU(c) = c * sigmoid(c) with sigmoid(c) = (1 + tanh(c/2)) / 2 (one MUFU operation per
-// element), on a packed pair.
-__device__ __forceinline__ uint64_t silu2(uint64_t c) {
-  float c0, c1, t0, t1;
-  upk(mul2(c, pk(0.5f, 0.5f)), c0, c1);
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(c0));
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(c1));
-  return mul2(c, fma2(pk(0.5f, 0.5f), pk(t0, t1), pk(0.5f, 0.5f)));
+// SiLU(c) = c sigmoid(c) = h + h tanh(h) with h = c / 2 (sigmoid(c) = (1 + tanh(c/2)) / 2):
+// from the packed half-argument h, one MUFU operation per element and one packed FMA. The
+// sum acc + SiLU(c) is returned as h tanh(h) + (h + acc).
+__device__ __forceinline__ uint64_t silu2_add(uint64_t h, uint64_t acc) {
+  float h0, h1, t0, t1;
+  upk(h, h0, h1);
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(h0));
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(h1));
+  return fma2(h, pk(t0, t1), add2(h, acc));
 }
 
-// PF: positions of H prefetched ahead of the one being computed (per thread, cp.async);
-// CPT: channels per thread (4 gives twice the warps of 8 at half the registers each).
-template <typename T, int MB, int PF, int CPT>
-__global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
+constexpr int kCpt = 4;             // channels per thread
+constexpr int kMaxThreads = 768;    // so a slice holds at most 3072 channels
+constexpr int kSliceThreads = 128;  // slice width when mean(v^2) is given
+constexpr int kPrefetch = 2;        // positions of H in flight per thread
+
+// PF: positions of H prefetched ahead of the one being computed (per thread, cp.async).
+// The grid is a multiple of `slices`; block b works on channel slice b mod slices.
+template <typename T, int MB, int PF>
+__global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
     int L, int d, int M_rt, int64_t N, const T* __restrict__ v, const float* __restrict__ alpha,
     const float* __restrict__ v_ms,
     const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks, int dil, float eps,
-    T* __restrict__ H, int runs_per_seq, int total_runs) {
+    T* __restrict__ H, int runs_per_seq, int total_runs, int slices) {
   constexpr int MMAX = MB > 0 ? MB : kMaxBranches;
+  constexpr int CPT = kCpt;
   const int M = MB > 0 ? MB : M_rt;
-  __shared__ float s_ms[kMaxPos];  // sum(v^2) per position of the run
-  __shared__ float s_f[MMAX][kMaxPos];
-  __shared__ float s_a[MMAX][kMaxPos];
+  __shared__ float s_ms[kMaxPos];  // mean(v^2) per position of the run and its halo
+  // per (branch, run position t): {f_t, f_t, f_{t-dil}, f_{t-dil}}, {f_{t-2dil} x2, f_{t-3dil} x2},
+  // {alpha_t, alpha_t, -, -}; f is 0 before the start of the sequence and past the kernel size
+  __shared__ __align__(16) float s_tap[MMAX][kRun][12];
   // H prefetch ring: [PF][M][threads] chunks of CPT channels
   extern __shared__ __align__(16) uint8_t s_ring[];
   using Vec = VecN<T, CPT>;
   using Raw = typename Vec::Raw;
+  constexpr int kPairs = CPT / 2;
   Raw* ring = reinterpret_cast<Raw*>(s_ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   auto ring_at = [&](int slot, int m) -> Raw* { return ring + (slot * MMAX + m) * blockDim.x + threadIdx.x; };
 
-  const int c0 = threadIdx.x * CPT;
+  const int c0 = (blockIdx.x % slices) * blockDim.x * CPT + threadIdx.x * CPT;
   const bool active = c0 < d;
   const int chunks8 = d >> 3;
   const int halo = (ks - 1) * dil;
   const float inv_d = 1.0f / static_cast<float>(d);
+  const int64_t branch_stride = N * d;
 
-  // conv taps with the RMSNorm gain folded in: wg[j][q] = w[c0+q, j] * gamma[c0+q]
-  float wg[kTaps][CPT];
+  // conv taps with the RMSNorm gain and SiLU's half-argument folded in, as packed pairs:
+  // wg[j][q] = w[c, j] gamma[c] / 2 for c = c0 + 2q, c0 + 2q + 1
+  uint64_t wg[kTaps][kPairs];
 #pragma unroll
-  for (int q = 0; q < CPT; ++q) {
-    const float g = active ? gamma_c[c0 + q] : 0.f;
+  for (int q = 0; q < kPairs; ++q) {
+    float g[2], w[kTaps][2];
 #pragma unroll
-    for (int j = 0; j < kTaps; ++j) wg[j][q] = (active && j < ks) ? conv_w[(c0 + q) * ks + j] * g : 0.f;
+    for (int e = 0; e < 2; ++e) {
+      const int c = c0 + 2 * q + e;
+      g[e] = active ? 0.5f * gamma_c[c] : 0.f;
+#pragma unroll
+      for (int j = 0; j < kTaps; ++j) w[j][e] = (active && j < ks) ? conv_w[c * ks + j] * g[e] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kTaps; ++j) wg[j][q] = pk(w[j][0], w[j][1]);
   }
 
-  for (int run = blockIdx.x; run < total_runs; run += gridDim.x) {
+  for (int run = blockIdx.x / slices; run < total_runs; run += gridDim.x / slices) {
     const int b = run / runs_per_seq;
     const int t0 = (run - b * runs_per_seq) * kRun;
     const int t1 = min(t0 + kRun, L);
@@ -216,11 +239,10 @@ __global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
     const int npos = t1 - p0;
     const int64_t seq0 = static_cast<int64_t>(b) * L;
 
-    // 1. sum(v^2) per position: given (v_ms, the projection's mean(v^2)), or one warp per
-    //    position (16-byte loads, unrolled so each lane has several of its row's loads in
-    //    flight)
+    // 1. mean(v^2) per position: given (v_ms, the projection's), or one warp per position
+    //    (16-byte loads, unrolled so each lane has several of its row's loads in flight)
     if (v_ms)
-      for (int i = threadIdx.x; i < npos; i += blockDim.x) s_ms[i] = v_ms[seq0 + p0 + i] * static_cast<float>(d);
+      for (int i = threadIdx.x; i < npos; i += blockDim.x) s_ms[i] = v_ms[seq0 + p0 + i];
     for (int i = warp; !v_ms && i < npos; i += nwarps) {
       const T* row = v + (seq0 + p0 + i) * d;
       float s = 0.f;
@@ -233,35 +255,41 @@ __global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (lane == 0) s_ms[i] = s;
+      if (lane == 0) s_ms[i] = s * inv_d;
     }
     __syncthreads();
 
-    // 2. alpha and f = alpha / sqrt(alpha^2 mean(v^2) + eps) per (branch, position)
-    for (int idx = threadIdx.x; idx < M * npos; idx += blockDim.x) {
-      const int m = idx / npos, i = idx - (idx / npos) * npos;
-      const float a = alpha[m * N + seq0 + p0 + i];
-      s_a[m][i] = a;
-      s_f[m][i] = a * rsqrtf(a * a * (s_ms[i] * inv_d) + eps);
+    // 2. tap scalars: f = alpha / sqrt(alpha^2 mean(v^2) + eps) at t - j dil, and alpha_t
+    for (int idx = threadIdx.x; idx < M * kRun * kTaps; idx += blockDim.x) {
+      const int j = idx % kTaps, i = (idx / kTaps) % kRun, m = idx / (kTaps * kRun);
+      const int t = t0 + i, p = t - j * dil;
+      float a = 0.f, f = 0.f;
+      if (t < t1 && j < ks && p >= 0) {
+        a = alpha[m * N + seq0 + p];
+        f = a * rsqrtf(a * a * s_ms[p - p0] + eps);
+      }
+      *reinterpret_cast<float2*>(&s_tap[m][i][2 * j]) = make_float2(f, f);
+      if (j == 0) *reinterpret_cast<float2*>(&s_tap[m][i][8]) = make_float2(a, a);
     }
     __syncthreads();
 
     // 3. conv + SiLU + residual. Positions are walked by residue class mod dil, so the taps
-    //    of t (t, t - dil, t - 2 dil, t - 3 dil) form a window that slides by one row per
-    //    step; H of the next PF positions in walking order is already on its way into this
-    //    thread's ring slots (one cp.async group per position).
+    //    of t (t, t - dil, t - 2 dil, t - 3 dil) are the last four rows of the class: at the
+    //    k-th step the row t - j dil sits in window slot (k - j) mod 4, and the walk is
+    //    unrolled by 4 so every slot index is a constant. H of the next PF positions in
+    //    walking order is already on its way into this thread's ring slots (one cp.async
+    //    group per position).
     int pr = 0, pi = 0, ps = 0;  // prefetch cursor: position t0 + pr + dil * pi, sequence ps
     auto prefetch_next = [&]() {
       if (pr < dil && t0 + pr < t1) {
         if (active) {
           const int t = t0 + pr + dil * pi;
           const int slot = ps % PF;
+          const T* src = H + (seq0 + t) * d + c0;
 #pragma unroll
           for (int m = 0; m < MMAX; ++m) {
             if (m >= M) continue;
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(H + (m * N + seq0 + t) * d + c0);
-            uint8_t* dst = reinterpret_cast<uint8_t*>(ring_at(slot, m));
-            cp_async_bytes<static_cast<int>(sizeof(Raw))>(dst, src);
+            cp_async_bytes<static_cast<int>(sizeof(Raw))>(ring_at(slot, m), src + m * branch_stride);
           }
         }
         ++pi;
@@ -277,66 +305,66 @@ __global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
     for (int i = 0; i < PF; ++i) prefetch_next();
     int s = 0;  // sequence index of the position being computed
     for (int r = 0; r < dil && t0 + r < t1; ++r) {
-      float win[kTaps][CPT];  // v at t - j dil, zero before the start of the sequence
+      uint64_t win[kTaps][kPairs];  // v rows of this residue class, zero before the sequence start
 #pragma unroll
       for (int j = 0; j < kTaps; ++j) {
         const int p = t0 + r - j * dil;
+        float x[CPT];
         if (active && j < ks && p >= 0) {
-          Vec::unpack(Vec::load(v + (seq0 + p) * d + c0), win[j]);
+          Vec::unpack(Vec::load(v + (seq0 + p) * d + c0), x);
         } else {
 #pragma unroll
-          for (int q = 0; q < CPT; ++q) win[j][q] = 0.f;
+          for (int q = 0; q < CPT; ++q) x[q] = 0.f;
         }
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) win[(kTaps - j) % kTaps][q] = pk(x[2 * q], x[2 * q + 1]);
       }
-      for (int t = t0 + r; t < t1; t += dil, ++s) {
-        const bool has_next = active && t + dil < t1;
-        Raw nxt = Vec::zero();
-        if (has_next) nxt = Vec::load(v + (seq0 + t + dil) * d + c0);   // next window row, early
-        cp_async_wait<PF - 1>();   // this thread's copies for position t have landed
-        if (active) {
-          const int slot = s % PF;
-          constexpr int kPairs = CPT / 2;
-          uint64_t prod[kTaps][kPairs];   // (w[:, j] gamma) * v_{t - j dil}, packed pairs
+      int t = t0 + r;
+      while (t < t1) {
 #pragma unroll
-          for (int j = 0; j < kTaps; ++j)
+        for (int k = 0; k < kTaps; ++k) {
+          const bool has_next = active && t + dil < t1;
+          Raw nxt = Vec::zero();
+          if (has_next) nxt = Vec::load(v + (seq0 + t + dil) * d + c0);  // next row of the class, early
+          cp_async_wait<PF - 1>();  // this thread's copies for position t have landed
+          if (active) {
+            const Raw* hr = ring_at(s % PF, 0);
+            T* out = H + (seq0 + t) * d + c0;
+            uint64_t prod[kTaps][kPairs];  // (w[:, j] gamma / 2) * v_{t - j dil}
 #pragma unroll
-            for (int q = 0; q < kPairs; ++q)
-              prod[j][q] = mul2(pk(wg[j][2 * q], wg[j][2 * q + 1]), pk(win[j][2 * q], win[j][2 * q + 1]));
-          uint64_t vt[kPairs];
+            for (int j = 0; j < kTaps; ++j)
 #pragma unroll
-          for (int q = 0; q < kPairs; ++q) vt[q] = pk(win[0][2 * q], win[0][2 * q + 1]);
+              for (int q = 0; q < kPairs; ++q) prod[j][q] = mul2(wg[j][q], win[(k - j + kTaps) % kTaps][q]);
 #pragma unroll
-          for (int m = 0; m < MMAX; ++m) {
-            if (m >= M) continue;
-            uint64_t fj[kTaps];
+            for (int m = 0; m < MMAX; ++m) {
+              if (m >= M) continue;
+              const ulonglong2 f01 = *reinterpret_cast<const ulonglong2*>(&s_tap[m][t - t0][0]);
+              const ulonglong2 f23 = *reinterpret_cast<const ulonglong2*>(&s_tap[m][t - t0][4]);
+              const uint64_t aa = *reinterpret_cast<const uint64_t*>(&s_tap[m][t - t0][8]);
+              float h[CPT];
+              Vec::unpack(hr[m * blockDim.x], h);
 #pragma unroll
-            for (int j = 0; j < kTaps; ++j) {
-              const int p = t - j * dil;
-              const float f = (j < ks && p >= 0) ? s_f[m][p - p0] : 0.f;
-              fj[j] = pk(f, f);
+              for (int q = 0; q < kPairs; ++q) {
+                uint64_t c = mul2(f01.x, prod[0][q]);  // c / 2
+                c = fma2(f01.y, prod[1][q], c);
+                c = fma2(f23.x, prod[2][q], c);
+                c = fma2(f23.y, prod[3][q], c);
+                const uint64_t acc = fma2(aa, win[k][q], pk(h[2 * q], h[2 * q + 1]));  // H + alpha v_t
+                upk(silu2_add(c, acc), h[2 * q], h[2 * q + 1]);
+              }
+              Vec::store(out + m * branch_stride, h);
             }
-            const float a = s_a[m][t - p0];
-            const uint64_t aa = pk(a, a);
-            float h[CPT];
-            Vec::unpack(*ring_at(slot, m), h);
-#pragma unroll
-            for (int q = 0; q < kPairs; ++q) {
-              uint64_t c = mul2(fj[0], prod[0][q]);
-#pragma unroll
-              for (int j = 1; j < kTaps; ++j) c = fma2(fj[j], prod[j][q], c);
-              const uint64_t y = fma2(aa, vt[q], silu2(c));           // SiLU(c) + alpha v_t
-              upk(add2(pk(h[2 * q], h[2 * q + 1]), y), h[2 * q], h[2 * q + 1]);
-            }
-            Vec::store(H + (m * N + seq0 + t) * d + c0, h);
           }
+          prefetch_next();
+          // the slot of v_{t - 3 dil} takes v_{t + dil}
+          float x[CPT];
+          Vec::unpack(nxt, x);
+#pragma unroll
+          for (int q = 0; q < kPairs; ++q) win[(k + 1) % kTaps][q] = pk(x[2 * q], x[2 * q + 1]);
+          t += dil;
+          ++s;
+          if (t >= t1) break;
         }
-        prefetch_next();
-        // slide the window by one row (t -> t + dil)
-#pragma unroll
-        for (int j = kTaps - 1; j > 0; --j)
-#pragma unroll
-          for (int q = 0; q < CPT; ++q) win[j][q] = win[j - 1][q];
-        Vec::unpack(nxt, win[0]);
       }
     }
     cp_async_wait<0>();
@@ -347,42 +375,36 @@ __global__ void __launch_bounds__(CPT == 4 ? 768 : 1024) conv_residual_kernel(
 template <typename T>
 pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, const float* v_ms,
                  const float* gamma_c, const float* conv_w, int ks, int dil, float eps, void* H, cudaStream_t stream) {
-  // 4 channels per thread up to d = 3072 (768 threads), else 8 (up to 1024 threads)
-  const int cpt = d / 4 <= 768 ? 4 : 8;
-  const int threads = ((d / cpt) + 31) / 32 * 32;
+  // channel slices of at most `width` threads * 4 channels, each a multiple of 128 (whole warps)
+  const int width = v_ms ? kSliceThreads : kMaxThreads;
+  const int slices = (d + width * kCpt - 1) / (width * kCpt);
+  const int slice_ch = ((d + slices - 1) / slices + 32 * kCpt - 1) / (32 * kCpt) * (32 * kCpt);
+  const int threads = slice_ch / kCpt;
   const int runs_per_seq = (L + kRun - 1) / kRun;
   const int64_t total = static_cast<int64_t>(B) * runs_per_seq;
   if (total >= (1ll << 31)) return PG_ERR_SHAPE;
   const int64_t N = static_cast<int64_t>(B) * L;
   auto run = [&](auto kern, int mmax, int pf) -> pg_status {
-    const size_t ring = static_cast<size_t>(pf) * mmax * threads * (sizeof(T) * cpt);
+    const size_t ring = static_cast<size_t>(pf) * mmax * threads * (sizeof(T) * kCpt);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring));
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, ring);
     if (e != cudaSuccess) return cuda_fail(e);
     if (per_sm < 1) return PG_ERR_UNSUPPORTED;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
-    const int grid = static_cast<int>(total < cap ? total : cap);
+    const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * per_sm / slices);  // runs in flight
+    const int grid = static_cast<int>((total < cap ? total : cap) * slices);
     kern<<<grid, threads, ring, stream>>>(L, d, M, N, static_cast<const T*>(v), alpha, v_ms, gamma_c, conv_w, ks,
-                                          dil, eps, static_cast<T*>(H), runs_per_seq, static_cast<int>(total));
+                                          dil, eps, static_cast<T*>(H), runs_per_seq, static_cast<int>(total),
+                                          slices);
     return after_launch(1);
   };
-  // prefetch depth: 4 positions while the ring fits in 192 KB of shared memory, else 1
-  const int mm = M == 1 || M == 2 || M == 4 ? M : kMaxBranches;
-  const bool deep = 4ull * mm * threads * sizeof(T) * cpt <= (192u << 10);
-  auto pick = [&](auto cpt_c) -> pg_status {
-    constexpr int C = decltype(cpt_c)::value;
-    switch (M) {
-      case 1: return deep ? run(conv_residual_kernel<T, 1, 4, C>, 1, 4) : run(conv_residual_kernel<T, 1, 1, C>, 1, 1);
-      case 2: return deep ? run(conv_residual_kernel<T, 2, 4, C>, 2, 4) : run(conv_residual_kernel<T, 2, 1, C>, 2, 1);
-      case 4: return deep ? run(conv_residual_kernel<T, 4, 4, C>, 4, 4) : run(conv_residual_kernel<T, 4, 1, C>, 4, 1);
-      default:
-        return deep ? run(conv_residual_kernel<T, 0, 4, C>, kMaxBranches, 4)
-                    : run(conv_residual_kernel<T, 0, 1, C>, kMaxBranches, 1);
-    }
-  };
-  return cpt == 4 ? pick(std::integral_constant<int, 4>()) : pick(std::integral_constant<int, 8>());
+  switch (M) {
+    case 1: return run(conv_residual_kernel<T, 1, kPrefetch>, 1, kPrefetch);
+    case 2: return run(conv_residual_kernel<T, 2, kPrefetch>, 2, kPrefetch);
+    case 4: return run(conv_residual_kernel<T, 4, kPrefetch>, 4, kPrefetch);
+    default: return run(conv_residual_kernel<T, 0, kPrefetch>, kMaxBranches, kPrefetch);
+  }
 }
 
 }  // namespace
