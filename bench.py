@@ -5,9 +5,11 @@
 
 A step is one pass of the whole lookup over one batch of the workload (default:
 the PageGram 200M-parameter bf16 table, 64 x 1024 Zipf(1.1) tokens): canonical IDs,
-n-grams, hashes and rows, gather + sign + concat (pg_gather_sign_concat), then the
-W_V projection with the scalar gate x + g v (pg_project_gate, tcgen05); --path fused
-runs both in one kernel (pg_lookup_project_gate) and the other path is timed too. With
+n-grams, hashes and rows, gather + sign + concat, then the W_V projection with the scalar
+gate x + g v (tcgen05). By default both run in one launch (pg_gather_project_gate: the
+gather on extra warps of the persistent projection, writing e_t ahead of the tiles that
+read it); --path two_kernel runs pg_gather_sign_concat then pg_project_gate, --path fused
+pg_lookup_project_gate; the paths not chosen are timed too. With
 --config 5 the step is the Engram-27B-shaped module (gather, fused W_V + 4 W_K with
 the RMSNorm-sigmoid gate, causal conv + residual).
 
@@ -205,15 +207,45 @@ class Pipeline:
                                    canon_map=self.cmap, M=w.M, h=dn["H"], gamma_h=dn["gamma_h"],
                                    gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=self.alpha, workspace=self.ws)
 
+    def overlap(self):
+        pg, w, dn = self.pg, self.w, self.dn
+        if not hasattr(self, "ws_ov"):
+            n = pg.gather_project_workspace_size(self.N, self.d, w.M, w.gate)
+            self.ws_ov = self.torch.empty((n + 3) // 4, device=self.dev)
+        if w.gate == self.W.GATE_SCALAR:
+            pg.gather_project_gate(self.desc, self.tokens, self.table, self.e, dn["W"], self.d, pg.GATE_SCALAR,
+                                   self.out, self.ws_ov, canon_map=self.cmap, g=w.g, x_resid=dn["x"])
+        elif w.gate == self.W.GATE_NONE:
+            pg.gather_project_gate(self.desc, self.tokens, self.table, self.e, dn["W"], self.d, pg.GATE_NONE,
+                                   self.out, self.ws_ov, canon_map=self.cmap)
+        else:
+            pg.gather_project_gate(self.desc, self.tokens, self.table, self.e, dn["W"], self.d, pg.GATE_CONTEXT,
+                                   self.v, self.ws_ov, canon_map=self.cmap, M=w.M, h=dn["H"],
+                                   gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=self.alpha,
+                                   v_ms_out=self.v_ms)
+
     def can_fuse(self):
         sp = self.spec
         return (sp.mode != self.W.MODE_FLAT and sp.row_dtype == self.W.DT_BF16 and sp.r == 64
-                and self.w.gate != self.W.GATE_NONE)
+                and self.w.gate != self.W.GATE_NONE and self.w.cfg_id != 4)
 
-    def stages(self, fused=True):
+    def can_overlap(self):
+        return self.can_fuse() and self.d % 256 == 0
+
+    def paths(self):
+        """The ways this workload's step can run: the first is the default."""
+        if self.can_overlap():
+            return ["overlap", "two_kernel", "fused"]
+        if self.can_fuse():
+            return ["two_kernel", "fused"]
+        return ["two_kernel"]
+
+    def stages(self, path="two_kernel"):
         if self.w.cfg_id == 4:   # the 20B NF4 table: the lookup ends at e_t
             return [("gather_sign_concat", self.gather)]
-        if fused and self.can_fuse():
+        if path == "overlap":
+            st = [("gather_project_gate", self.overlap)]
+        elif path == "fused":
             st = [("lookup_project_gate", self.fused)]
         else:
             st = [("gather_sign_concat", self.gather), ("project_gate", self.project)]
@@ -264,6 +296,14 @@ class Pipeline:
             rb = self.spec.row_bytes if self.spec.row_dtype != self.W.DT_NF4 else 64
             per = len(self.spec.orders) * self.spec.K * rb + 4 + din * self.e.element_size()
             return "hbm", per * N
+        if name == "gather_project_gate":
+            # one launch doing both kernels' work; its binding roof is HBM (e_t written and
+            # read back, 2K rows, IDs, the epilogue operand and the output: 89 us at the
+            # measured copy rate on the PageGram 200M workload, against 55 us of tensor work)
+            rb = self.spec.row_bytes
+            e_b = din * self.e.element_size()
+            epi = d * 2 * (2 if w.gate == self.W.GATE_SCALAR else 1 + 2 * w.M)
+            return "hbm", (len(self.spec.orders) * self.spec.K * rb + 4 + 2 * e_b + epi) * N
         if name in ("project_gate", "lookup_project_gate"):
             cols = d * (1 + w.M)
             return ("alu" if w.dtype == self.W.DT_F32 else "tensor"), 2.0 * N * din * cols
@@ -323,7 +363,8 @@ def run_gpu(args):
     p = Pipeline(args.config, dev, rank)
     stream = torch.cuda.current_stream()
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    stages = p.stages(fused=args.path == "fused")
+    path = args.path if args.path in p.paths() else p.paths()[0]
+    stages = p.stages(path)
 
     # ---- warm-up
     for _ in range(args.warmup):
@@ -434,13 +475,23 @@ def run_gpu(args):
         kernels["lookup_project_gate"]["GB/s_compulsory"] = round(fb / (f_ms / 1e3) / 1e9, 1)
         kernels["lookup_project_gate"]["frac_hbm_compulsory"] = round(
             fb / (f_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
-    other = None
-    if p.can_fuse():
-        ost = p.stages(fused=args.path != "fused")
+    if "gather_project_gate" in means:
+        # e_t written once and read back by the projection (mostly from L2): table sectors +
+        # IDs + e_t + the epilogue operand in + the output
+        fb = comp + p.N * p.d * 2 * (2 if p.w.gate == p.W.GATE_SCALAR else 1 + 2 * p.w.M)
+        o_ms_ = means["gather_project_gate"]
+        kernels["gather_project_gate"]["compulsory_bytes"] = fb
+        kernels["gather_project_gate"]["GB/s_compulsory"] = round(fb / (o_ms_ / 1e3) / 1e9, 1)
+        kernels["gather_project_gate"]["frac_hbm_compulsory"] = round(
+            fb / (o_ms_ / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+    other = []
+    for op in p.paths():
+        if op == path:
+            continue
+        ost = p.stages(op)
         o_ms = time_stages(ost, max(3, args.steps // 4), stream, flush)
-        other = {"path": "fused" if args.path != "fused" else "two_kernel",
-                 "ms_per_step": round(sum(statistics.mean(x) for x in o_ms), 5),
-                 "kernels": {name: round(statistics.mean(o_ms[j]), 5) for j, (name, _) in enumerate(ost)}}
+        other.append({"path": op, "ms_per_step": round(sum(statistics.mean(x) for x in o_ms), 5),
+                      "kernels": {name: round(statistics.mean(o_ms[j]), 5) for j, (name, _) in enumerate(ost)}})
 
     clocks = clk.summary()
     if rank == 0:
@@ -463,8 +514,8 @@ def run_gpu(args):
                          "peak_source": ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz" if bound == "alu"
                                          else f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})")},
             "kernels": kernels,
-            "path": args.path if p.can_fuse() else "two_kernel",
-            "other_path": other,
+            "path": path,
+            "other_paths": other,
             "clocks": clocks,
             "wall_s_timed_loop": round(t_wall, 4),
         }
@@ -646,9 +697,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--path", choices=["two_kernel", "fused"], default="two_kernel",
-                    help="two_kernel: pg_gather_sign_concat + pg_project_gate; fused: pg_lookup_project_gate "
-                         "(r = 64 bf16 tables); the other one is timed too and reported as other_path")
+    ap.add_argument("--path", choices=["auto", "overlap", "two_kernel", "fused"], default="auto",
+                    help="how the lookup and the projection run: overlap = one launch writing e_t with the "
+                         "gather on extra warps of the projection (pg_gather_project_gate); two_kernel = "
+                         "pg_gather_sign_concat + pg_project_gate; fused = pg_lookup_project_gate (r = 64 bf16 "
+                         "tables); auto = the first that applies, in that order. The others that apply are "
+                         "timed too and reported as other_paths")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

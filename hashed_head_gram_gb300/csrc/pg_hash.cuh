@@ -103,6 +103,15 @@ __device__ __forceinline__ uint4 bf16_sign_mask(uint32_t bits) {
   return m;
 }
 
+// 16 bytes of a table row: read-only, not kept in L1 (rows are rarely reused by one SM).
+__device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
 __device__ __forceinline__ uint4 xor4(uint4 a, uint4 b) {
   return make_uint4(a.x ^ b.x, a.y ^ b.y, a.z ^ b.z, a.w ^ b.w);
 }

@@ -119,14 +119,6 @@ struct GatherGeom {
   uint64_t table_bytes; // NF4: bytes of the table (the last rows' 16-byte windows stop there)
 };
 
-__device__ __forceinline__ uint4 ldg_stream(const void* ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr));
-  return v;
-}
-
 
 
 // XOR masks that negate 4 fp32 from 4 sign bits.

@@ -339,6 +339,11 @@ constexpr int kEpiCols = 32;        // columns per epilogue sub-tile
 constexpr int kEpiStagesMax = 4;    // epilogue shared-memory ring (3 slots in the fused kernel)
 constexpr int kEpiBytes = kBM * kEpiCols * 2;
 constexpr int kFusedItems = 32;     // (order, head) items of the fused kernel
+constexpr int kUnitRows = 512;      // (token, head) rows per work unit of the producing kernel's gather warps
+constexpr int kProduceThreads = 512;  // producing kernel: + 8 gather warps + 1 coordinator warp
+constexpr int kCoordWarp = 15;
+constexpr int kGroupThreads = 9 * 32;  // gather warps + coordinator, on named barrier 1
+constexpr int kReadyTokens = kBM;   // tokens per ready counter (one A tile of one CTA)
 
 template <bool GATHER>
 __host__ __device__ constexpr int epi_stages() { return GATHER ? 3 : 4; }
@@ -356,6 +361,12 @@ struct FusedGather {
   uint32_t L;
   uint64_t fm_L;
   int32_t* err;
+  // producing kernel only: e_t [N, Din] written by the gather warps, per-128-token ready
+  // counters (chunks done) and the chunk claim counter, both zeroed before the launch
+  uint8_t* e_out;
+  uint32_t* ready;
+  uint32_t* claim;
+  int unit_tokens;  // tokens per work unit: the largest power of two <= 128 with unit_tokens * items <= 512
 };
 struct NoGather {};
 template <bool GATHER>
@@ -395,11 +406,32 @@ struct GemmBarriers {
   int abort;
 };
 
-template <int BN, bool GATHER, bool PAIR>
+template <int BN, bool GATHER, bool PAIR, bool PRODUCE>
 constexpr size_t gemm_smem_bytes() {
   return 1024 /* alignment slack */ + gemm_stages<PAIR>() * (kABytes + (PAIR ? BN / 2 : BN) * kBK * 2) +
-         epi_stages<GATHER>() * kEpiBytes + sizeof(GemmBarriers<gemm_stages<PAIR>()>) +
-         (GATHER ? kFusedItems * sizeof(ItemConst) : 0);
+         epi_stages<GATHER || PRODUCE>() * kEpiBytes + sizeof(GemmBarriers<gemm_stages<PAIR>()>) +
+         (GATHER || PRODUCE ? kFusedItems * sizeof(ItemConst) : 0);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait (bounded) until the ready counter reaches `need`: false on abort or time-out.
+__device__ __noinline__ bool wait_ready_slow(const uint32_t* flag, uint32_t need, volatile int* abort) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) >= need) return true;
+    if (*abort || globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+__device__ __forceinline__ bool wait_ready(const uint32_t* flag, uint32_t need, volatile int* abort) {
+  return ld_acquire_gpu(flag) >= need || wait_ready_slow(flag, need, abort);
 }
 
 // Epilogue operands and results move through 128 x 32 bf16 sub-tiles (64 bytes per row)
@@ -416,15 +448,22 @@ __device__ __forceinline__ uint32_t epi_offset(int row, int chunk) {
 // and BN/2 rows of B; both CTAs' copies count on rank 0's `full` barrier, rank 0 issues
 // M = 256 MMAs (rows 128 r .. 128 r + 127 accumulate in CTA r's TMEM) and its commits
 // arrive on the barriers of both CTAs; each CTA runs the epilogue of its own 128 rows.
-template <int BN, int GATE, bool GATHER, bool PAIR>
-__global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
+// PRODUCE: 8 more warps per CTA compute e_t itself (the lookup of pg_gather_sign_concat)
+// into global memory while the tensor cores work: they claim chunks of 8 tokens from a
+// global counter in the order the tiles are walked, write the chunk's e_t rows and count
+// it on its 128-token block's ready counter (release); the A producer waits (acquire,
+// bounded) for a block's count before its first TMA load of that block. Any resident CTA
+// claims and finishes chunks without waiting on anything, so every wait ends.
+template <int BN, int GATE, bool GATHER, bool PAIR, bool PRODUCE = false>
+__global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThreads : kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
                    const __grid_constant__ CUtensorMap map_v, const GemmArgs args,
-                   const __grid_constant__ typename GatherParam<GATHER>::type gat) {
+                   const __grid_constant__ typename GatherParam<GATHER || PRODUCE>::type gat) {
   static_assert(!(GATHER && PAIR), "the fused gather runs on single-CTA tiles");
+  static_assert(!(GATHER && PRODUCE), "one way of making A");
   constexpr int kSt = gemm_stages<PAIR>();
-  constexpr int kEpiStages = epi_stages<GATHER>();
+  constexpr int kEpiStages = epi_stages<GATHER || PRODUCE>();
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of W this CTA stages per k-block
   constexpr int kBBytes = kBRows * kBK * 2;
   constexpr int kTileM = PAIR ? 2 * kBM : kBM;  // output rows of a tile
@@ -472,7 +511,7 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
     tmem_alloc<PAIR>(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish<PAIR>();
   }
-  if constexpr (GATHER) {
+  if constexpr (GATHER || PRODUCE) {
     if (threadIdx.x >= 32 * kGatherWarp0 && threadIdx.x - 32 * kGatherWarp0 < gat.P.O * gat.P.H)
       init_item_const(s_ic[threadIdx.x - 32 * kGatherWarp0], gat.P, gat.seed, threadIdx.x - 32 * kGatherWarp0);
   }
@@ -500,6 +539,21 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
       uint32_t issued = 0;  // bit s: stage s holds a load nobody has consumed yet (error path)
       for (int tile = unit; tile < num_tiles && ok; tile += units) {
         const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
+        if constexpr (PRODUCE) {
+          // this CTA's 128 rows of A must have been written by the gather warps
+          const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+          if (m0 < args.N) {
+            const int rows = min(kBM, args.N - m0);
+            if (!wait_ready(gat.ready + m0 / kReadyTokens,
+                            static_cast<uint32_t>((rows + gat.unit_tokens - 1) / gat.unit_tokens), abort)) {
+              atomicOr(args.err_word, 64);
+              ok = false;
+              break;
+            }
+            // their generic-proxy writes, now visible to this thread, ordered before its TMA reads
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
             ok = false;
@@ -648,8 +702,129 @@ __global__ void __launch_bounds__(GATHER ? kFusedThreads : kGemmThreads, 1)
           }
       }
     }
-  } else if (GATHER && warp >= kGatherWarp0) {
-    if constexpr (GATHER) {
+  } else if ((GATHER || PRODUCE) && warp >= kGatherWarp0) {
+    if constexpr (PRODUCE) {
+      // ---------------------------------------------------------- e_t producers (warps 7..15)
+      // Warps 7..14 gather, as one group, units of T tokens x `items` heads = Hu <= 512
+      // rows of 64 bf16 (128 bytes), T a power of two <= 128 (a unit never spans two ready
+      // counters). Warp w takes rows [64 w, 64 w + 64) of a unit: lane l hashes rows
+      // 64 w + l and 64 w + l + 32 (token p / items, head p mod items), then 8 lanes per row
+      // move its 16-byte pieces, row 64 w + 4 i + (l >> 3) being lane ((4 i + (l >> 3)) mod
+      // 32)'s pair. Warp 15 coordinates: it claims units (in the order the tiles are walked:
+      // last m-block first) one iteration ahead into a 4-slot ring in shared memory, and
+      // counts each unit on its ready counter, after a fence, once every gather warp has
+      // issued its stores. All nine warps meet once per iteration on named barrier 1; with
+      // units k = 0 .. K - 1 handed out (slot K holds -1), both sides pass barriers 0 .. K
+      // and a final one:
+      //   iteration i (barrier i, 1 <= i <= K): the gather warps read unit i from its slot,
+      //   hash it under the loads of unit i - 1, store unit i - 1 and issue the loads of unit
+      //   i; the coordinator has put unit i in its slot before barrier i and counts unit
+      //   i - 2, whose stores were issued before barrier i.
+      __shared__ int64_t s_unit[4];
+      const int items = gat.P.O * gat.P.H;
+      const int T = gat.unit_tokens;
+      const uint32_t nunits = static_cast<uint32_t>((args.N + T - 1) / T);
+      auto group_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kGroupThreads) : "memory"); };
+      if (warp == kCoordWarp) {
+        auto unit_of = [&](uint32_t c) -> int64_t {
+          return (c >= nunits || *abort) ? -1 : static_cast<int64_t>(nunits - 1 - c) * T;
+        };
+        auto publish = [&](int64_t u) {
+          if (lane == 0 && u >= 0) {
+            __threadfence();
+            red_release_gpu_add(gat.ready + u / kReadyTokens, 1u);
+          }
+        };
+        uint32_t pending = 0;  // claim for the next unit (lane 0)
+        int64_t h0 = -1;       // unit 0
+        if (lane == 0) {
+          h0 = unit_of(atomicAdd(gat.claim, 1u));
+          s_unit[0] = h0;
+          if (h0 >= 0) pending = atomicAdd(gat.claim, 1u);
+        }
+        h0 = __shfl_sync(0xffffffffu, h0, 0);
+        __syncwarp();
+        group_sync();  // barrier 0
+        int64_t hm1 = h0, hm2 = -1;  // units i - 1 and i - 2
+        if (h0 >= 0) {
+          for (int i = 1;; ++i) {
+            int64_t val = -1;  // unit i
+            if (lane == 0) {
+              val = unit_of(pending);
+              s_unit[i & 3] = val;
+              if (val >= 0) pending = atomicAdd(gat.claim, 1u);  // used one iteration later
+            }
+            val = __shfl_sync(0xffffffffu, val, 0);
+            __syncwarp();
+            group_sync();  // barrier i
+            publish(hm2);  // unit i - 2
+            hm2 = hm1;
+            hm1 = val;
+            if (val < 0) break;  // K = i
+          }
+        }
+        group_sync();  // final barrier: the stores of unit K - 1 are issued
+        publish(hm2);  // unit K - 1
+      } else {
+        const int gw = warp - kGatherWarp0;
+        const int Hu = T * items;
+        const uint32_t out_row = static_cast<uint32_t>(items) * 128u;
+        const int piece = lane & 7, sub = lane >> 3;
+        uint32_t r[2], off[2];
+        uint64_t sw[2];
+        auto hash = [&](int64_t tok0) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int p = 64 * gw + lane + 32 * j;
+            const int s = p / items;
+            r[j] = 0;
+            sw[j] = 0;
+            off[j] = 0xFFFFFFFFu;  // no row
+            if (tok0 >= 0 && p < Hu && tok0 + s < args.N) {
+              const int it = p - s * items;
+              const int64_t tok = tok0 + s;
+              uint64_t hs;
+              r[j] = item_row(s_ic[it], gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, tok,
+                              fastmod(static_cast<uint32_t>(tok), gat.fm_L, gat.L), gat.err, &hs);
+              sw[j] = mix64(hs + kGolden);
+              off[j] = static_cast<uint32_t>(s) * out_row + static_cast<uint32_t>(it) * 128u;
+            }
+          }
+        };
+        uint4 v[16];
+        uint32_t o[16];
+        auto issue_loads = [&]() {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int src = (4 * i + sub) & 31;
+            const uint32_t row = __shfl_sync(0xffffffffu, i < 8 ? r[0] : r[1], src);
+            o[i] = __shfl_sync(0xffffffffu, i < 8 ? off[0] : off[1], src);
+            v[i] = make_uint4(0, 0, 0, 0);
+            if (o[i] != 0xFFFFFFFFu) v[i] = ldg_stream(gat.table + static_cast<uint64_t>(row) * 128u + piece * 16);
+          }
+        };
+        group_sync();  // barrier 0
+        int64_t cur = s_unit[0];
+        hash(cur);
+        if (cur >= 0) issue_loads();
+        for (int i = 1; cur >= 0; ++i) {
+          const uint64_t sw0 = sw[0], sw1 = sw[1];
+          group_sync();  // barrier i: unit i is in slot i mod 4
+          const int64_t nxt = s_unit[i & 3];
+          hash(nxt);  // under the loads of unit i - 1
+          uint8_t* out = gat.e_out + static_cast<uint64_t>(cur) * out_row + piece * 16;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint64_t w = __shfl_sync(0xffffffffu, q < 8 ? sw0 : sw1, (4 * q + sub) & 31);
+            const uint32_t bits = static_cast<uint32_t>(w >> (8 * piece)) & 0xFFu;
+            if (o[q] != 0xFFFFFFFFu) *reinterpret_cast<uint4*>(out + o[q]) = xor4(v[q], bf16_sign_mask(bits));
+          }
+          if (nxt >= 0) issue_loads();
+          cur = nxt;
+        }
+        group_sync();  // final barrier
+      }
+    } else if constexpr (GATHER) {
       // ---------------------------------------------------------- A-operand gather (warps 7..14)
       // Pair p of warps builds every A tile of ring stage p; warp `half` of the pair covers
       // tokens [64 half, 64 half + 64) of the 128-token block. Lane l hashes tokens l and
@@ -964,9 +1139,9 @@ struct GemmPtrs {
   void* v;
 };
 
-template <int BN, int GATE, bool GATHER = false, bool PAIR = false>
+template <int BN, int GATE, bool GATHER = false, bool PAIR = false, bool PRODUCE = false>
 pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
-                    const typename GatherParam<GATHER>::type& gat = {}) {
+                    const typename GatherParam<GATHER || PRODUCE>::type& gat = {}) {
   CUtensorMap ma, mb, mx, mh, mv;
   if ((!GATHER && !make_map(&ma, ptr.e, a.N, a.Din, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) ||
       !make_map(&mb, ptr.W, a.Dcols, a.Din, kBK, PAIR ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -981,8 +1156,8 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
   if (GATE == PG_GATE_CONTEXT &&
       !make_map(&mh, ptr.h, static_cast<uint64_t>(a.M) * a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
-  auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR>;
-  const size_t smem = gemm_smem_bytes<BN, GATHER, PAIR>();
+  auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR, PRODUCE>;
+  const size_t smem = gemm_smem_bytes<BN, GATHER, PAIR, PRODUCE>();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return cuda_fail(err);
@@ -996,7 +1171,7 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2u * static_cast<unsigned>(tiles));
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(PRODUCE ? kProduceThreads : kGemmThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1022,6 +1197,13 @@ pg_status dispatch_tc(int gate, const GemmPtrs& ptr, const GemmArgs& a, cudaStre
   if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE, false, PAIR>(ptr, a, stream);
   if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR, false, PAIR>(ptr, a, stream);
   return launch_tc<BN, PG_GATE_CONTEXT, false, PAIR>(ptr, a, stream);
+}
+
+pg_status dispatch_produce(int gate, const GemmPtrs& ptr, const GemmArgs& a, const FusedGather& gat,
+                           cudaStream_t stream) {
+  if (gate == PG_GATE_NONE) return launch_tc<256, PG_GATE_NONE, false, true, true>(ptr, a, stream, gat);
+  if (gate == PG_GATE_SCALAR) return launch_tc<256, PG_GATE_SCALAR, false, true, true>(ptr, a, stream, gat);
+  return launch_tc<256, PG_GATE_CONTEXT, false, true, true>(ptr, a, stream, gat);
 }
 
 template <int BN>
@@ -1205,6 +1387,114 @@ extern "C" pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int
   const int64_t total = static_cast<int64_t>(M) * N;
   alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
       a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, nullptr, nullptr);
+  return after_launch(1);
+}
+
+// ==================================================================== lookup + projection, one launch
+
+namespace pg {
+namespace {
+
+// Head of pg_gather_project_gate's workspace: the chunk claim counter, then one ready
+// counter per 128-token block, zeroed by the call before its launch.
+size_t produce_sync_bytes(int64_t N) {
+  const size_t b = static_cast<size_t>(1 + (N + kReadyTokens - 1) / kReadyTokens) * sizeof(uint32_t);
+  return (b + 255) / 256 * 256;
+}
+
+}  // namespace
+}  // namespace pg
+
+extern "C" pg_status pg_gather_project_gate_workspace_size(int32_t N, int32_t d, int32_t M, int32_t gate_kind,
+                                                          size_t* bytes) {
+  if (!bytes) return PG_ERR_NULL;
+  if (N < 0 || d < 1 || M < 0) return PG_ERR_SHAPE;
+  *bytes = pg::produce_sync_bytes(N) + (gate_kind == PG_GATE_CONTEXT ? pg::context_workspace(N, d, M, true) : 0);
+  return PG_OK;
+}
+
+extern "C" pg_status pg_gather_project_gate(const pg_table_desc* desc, const int32_t* tokens, int32_t B,
+                                            int32_t L, const uint32_t* canon_map, const void* table,
+                                            uint64_t table_bytes, void* e_out, int32_t d, int32_t M,
+                                            const void* W, int32_t gate_kind, float g, const void* x_resid,
+                                            const void* h, const float* gamma_h, const float* gamma_k, float eps,
+                                            void* v_out, float* alpha_out, float* v_ms_out, void* workspace,
+                                            size_t workspace_bytes, int32_t* err_index, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  Geometry geo;
+  pg_status st = validate_desc(desc, &geo);
+  if (st != PG_OK) return st;
+  if (desc->hash_kind != PG_HASH_MULXOR || desc->mode == PG_FLAT) return PG_ERR_UNSUPPORTED;
+  if (desc->row_dtype != PG_BF16 || desc->r != kBK) return PG_ERR_UNSUPPORTED;
+  const int items = geo.O * geo.H;
+  if (items > kFusedItems) return PG_ERR_UNSUPPORTED;
+  if (B < 0 || L < 0 || d < 1 || M < 0) return PG_ERR_SHAPE;
+  if (gate_kind < PG_GATE_NONE || gate_kind > PG_GATE_CONTEXT) return PG_ERR_SHAPE;
+  if (gate_kind != PG_GATE_CONTEXT && M != 0) return PG_ERR_SHAPE;
+  if (gate_kind == PG_GATE_CONTEXT && M < 1) return PG_ERR_SHAPE;
+  const int64_t N = static_cast<int64_t>(B) * L;
+  if (N >= (1ll << 31)) return PG_ERR_SHAPE;
+  if (N == 0) return PG_OK;
+  if (!tokens || !table || !W || !v_out || !e_out || !workspace) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_SCALAR && !x_resid) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_CONTEXT && (!h || !gamma_h || !gamma_k || !alpha_out)) return PG_ERR_NULL;
+  if (table_bytes < geo.rows * geo.row_bytes) return PG_ERR_RANGE;
+  if (!aligned16(table) || !aligned16(W) || !aligned16(v_out) || !aligned16(e_out) || !aligned16(workspace) ||
+      (x_resid && !aligned16(x_resid)) || (h && !aligned16(h)))
+    return PG_ERR_ALIGN;
+  if (d % 256 != 0) return PG_ERR_UNSUPPORTED;
+  if (gate_kind == PG_GATE_CONTEXT && static_cast<int64_t>(M) * N >= (1ll << 31)) return PG_ERR_SHAPE;
+  if (sm_count() == 0) return cuda_fail(cudaGetLastError());
+  if (device_cc() != 103 && device_cc() != 100) return PG_ERR_DEVICE;
+  size_t need = 0;
+  pg_gather_project_gate_workspace_size(static_cast<int32_t>(N), d, M, gate_kind, &need);
+  if (workspace_bytes < need) return PG_ERR_WORKSPACE;
+  if (gate_kind == PG_GATE_CONTEXT && (!aligned16(gamma_h) || !aligned16(gamma_k))) return PG_ERR_ALIGN;
+  if (err_index) {
+    if (reinterpret_cast<uintptr_t>(err_index) % 4) return PG_ERR_ALIGN;
+    cudaError_t e = cudaMemsetAsync(err_index, 0xFF, sizeof(int32_t), stream);  // reads as -1
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  const size_t sync_bytes = produce_sync_bytes(N);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sync_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  constexpr int bn = 256;
+  GemmArgs a;
+  a.N = static_cast<int>(N);
+  a.Din = items * kBK;
+  a.Dcols = (gate_kind == PG_GATE_CONTEXT ? (1 + M) : 1) * d;
+  a.d = d;
+  a.M = M;
+  a.g = g;
+  a.gamma_h = gamma_h;
+  a.gamma_k = gamma_k;
+  a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sync_bytes);
+  a.vpart = (gate_kind == PG_GATE_CONTEXT && v_ms_out)
+                ? a.partials + static_cast<size_t>(M) * (d / bn) * 3 * static_cast<size_t>(N)
+                : nullptr;
+  a.err_word = device_error_word();
+  if (!a.err_word) return cuda_fail(cudaGetLastError());
+  FusedGather gat;
+  fill_hash_params(desc, geo, &gat.P);
+  gat.seed = desc->hash_seed;
+  gat.tokens = tokens;
+  gat.canon_map = canon_map;
+  gat.table = static_cast<const uint8_t*>(table);
+  gat.L = static_cast<uint32_t>(L);
+  gat.fm_L = fastmod_constant(gat.L);
+  gat.err = err_index;
+  gat.e_out = static_cast<uint8_t*>(e_out);
+  gat.unit_tokens = 1;
+  while (2 * gat.unit_tokens * items <= kUnitRows && 2 * gat.unit_tokens <= kReadyTokens) gat.unit_tokens *= 2;
+  gat.claim = static_cast<uint32_t*>(workspace);
+  gat.ready = static_cast<uint32_t*>(workspace) + 1;
+  const GemmPtrs ptrs{e_out, W, x_resid, h, v_out};
+  st = dispatch_produce(gate_kind, ptrs, a, gat, stream);
+  if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
+  const int64_t total = static_cast<int64_t>(M) * N;
+  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
+      a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, a.vpart, v_ms_out);
   return after_launch(1);
 }
 

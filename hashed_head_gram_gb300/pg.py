@@ -87,6 +87,11 @@ def _load():
     L.pg_lookup_project_gate.restype = ctypes.c_int
     L.pg_lookup_project_gate.argtypes = [dp, vp, i32, i32, vp, vp, u64, i32, i32, vp, i32, f32, vp, vp, vp, vp,
                                          f32, vp, vp, vp, sz, vp, vp]
+    L.pg_gather_project_gate.restype = ctypes.c_int
+    L.pg_gather_project_gate.argtypes = [dp, vp, i32, i32, vp, vp, u64, vp, i32, i32, vp, i32, f32, vp, vp, vp,
+                                         vp, f32, vp, vp, vp, vp, sz, vp, vp]
+    L.pg_gather_project_gate_workspace_size.restype = ctypes.c_int
+    L.pg_gather_project_gate_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
     L.pg_project_gate_context_noalloc.restype = ctypes.c_int
     L.pg_project_gate_context_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp, vp, vp]
     L.pg_conv_residual.restype = ctypes.c_int
@@ -210,6 +215,34 @@ def lookup_project_gate(desc: TableDesc, tokens: torch.Tensor, table: torch.Tens
            "pg_lookup_project_gate")
 
 
+def gather_project_workspace_size(N: int, d: int, M: int, gate_kind: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.pg_gather_project_gate_workspace_size(N, d, M, gate_kind, ctypes.byref(n)),
+           "pg_gather_project_gate_workspace_size")
+    return n.value
+
+
+def gather_project_gate(desc: TableDesc, tokens: torch.Tensor, table: torch.Tensor, e_out: torch.Tensor,
+                        W: torch.Tensor, d: int, gate_kind: int, v_out: torch.Tensor, workspace: torch.Tensor,
+                        canon_map: Optional[torch.Tensor] = None, M: int = 0, g: float = 0.0,
+                        x_resid: Optional[torch.Tensor] = None, h: Optional[torch.Tensor] = None,
+                        gamma_h: Optional[torch.Tensor] = None, gamma_k: Optional[torch.Tensor] = None,
+                        eps: float = 1e-6, alpha_out: Optional[torch.Tensor] = None,
+                        v_ms_out: Optional[torch.Tensor] = None, err_index: Optional[torch.Tensor] = None,
+                        stream=None):
+    """gather_sign_concat (into e_out) + project_gate in one launch, the lookup overlapped
+    with the tensor-core work."""
+    B, L = tokens.shape
+    nbytes = table.numel() * table.element_size()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pg_gather_project_gate(ctypes.byref(desc), _ptr(tokens), B, L, _ptr(canon_map), _ptr(table),
+                                       nbytes, _ptr(e_out), d, M, _ptr(W), gate_kind, g, _ptr(x_resid), _ptr(h),
+                                       _ptr(gamma_h), _ptr(gamma_k), eps, _ptr(v_out), _ptr(alpha_out),
+                                       _ptr(v_ms_out), _ptr(workspace), ws_bytes, _ptr(err_index),
+                                       _stream(stream)),
+           "pg_gather_project_gate")
+
+
 def project_gate_context_noalloc(e: torch.Tensor, W: torch.Tensor, d: int, M: int, h: torch.Tensor,
                                  gamma_h: torch.Tensor, gamma_k: torch.Tensor, v_out: torch.Tensor,
                                  alpha_out: torch.Tensor, eps: float = 1e-6, stream=None):
@@ -246,6 +279,7 @@ def dtype_code(t: torch.dtype) -> int:
 
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
-           "workspace_size", "project_gate", "lookup_project_gate", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
+           "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
+           "gather_project_gate", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

@@ -259,6 +259,38 @@ pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int32_t* token
                                  pg_stream_t stream);
 
 /*
+ * pg_gather_project_gate -- steps 1-7 in one launch that also writes e_t:
+ * pg_gather_sign_concat(desc, tokens, ..., e_out, PG_BF16) followed by
+ * pg_project_gate(e_out, W, ...), with the lookup of the Engram notes section 3.2 /
+ * PageGram report section 3.1 running on extra warps of the projection's persistent CTA
+ * pairs (Engram notes section 3.4), so that its random row reads overlap the tensor-core
+ * work instead of preceding it. The gather warps claim 8-token chunks of e_t in the order
+ * the projection's tiles consume them and publish each 128-token block on a ready counter
+ * in the workspace; a tile's first load of its rows waits for that count (bounded: a wait
+ * that runs out sets the device error word and the call's results are undefined).
+ *  Tables: PG_ENGRAM or PG_PAGEGRAM mode, PG_BF16 rows, r = 64, O*K <= 32 (Din = O*K*64).
+ *  desc .. table_bytes, err_index   as in pg_gather_sign_concat
+ *  e_out  device [B*L, Din] bf16, 16-byte aligned: e_t, written (the projection's A operand)
+ *  d .. v_ms_out                    as in pg_project_gate with dtype PG_BF16; d % 256 == 0
+ *  workspace  device, 16-byte aligned, >= pg_gather_project_gate_workspace_size() bytes
+ *         (always needed: the ready counters); zeroed in part by the call (one
+ *         cudaMemsetAsync on `stream`) before its kernel.
+ * e_out, v_out, alpha_out and v_ms_out are bit-identical to the two-call sequence. Calls
+ * that share a workspace must be ordered (same stream). B*L == 0 enqueues nothing.
+ */
+pg_status pg_gather_project_gate(const pg_table_desc* desc, const int32_t* tokens, int32_t B, int32_t L,
+                                 const uint32_t* canon_map, const void* table, uint64_t table_bytes,
+                                 void* e_out, int32_t d, int32_t M, const void* W, int32_t gate_kind,
+                                 float g, const void* x_resid, const void* h, const float* gamma_h,
+                                 const float* gamma_k, float eps, void* v_out, float* alpha_out,
+                                 float* v_ms_out, void* workspace, size_t workspace_bytes,
+                                 int32_t* err_index, pg_stream_t stream);
+
+/* Workspace bytes pg_gather_project_gate needs for N = B*L tokens, d, M and gate_kind. */
+pg_status pg_gather_project_gate_workspace_size(int32_t N, int32_t d, int32_t M, int32_t gate_kind,
+                                                size_t* bytes);
+
+/*
  * pg_project_gate_context_noalloc -- the context-gate projection of pg_project_gate
  * (gate PG_GATE_CONTEXT, dtype PG_BF16) for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point: it exists for the host side only.
