@@ -69,21 +69,18 @@ __device__ __forceinline__ void init_item_const(ItemConst& it, const HashParams&
   it.n = P.order_n[o];
 }
 
-// Row of item `it` for token `tok` (position t in its sequence), and the 64-bit sign
-// hash h_{2,o,k} through *hs:
+// Row of item `it` from the canonical IDs c_j of positions t - j (kPad before the start of
+// the sequence; only j < n is read), and the 64-bit sign hash h_{2,o,k} through *hs:
 //   PageGram  base_n + ((H_page mod P_n) K + k) S + (H_head mod S)
 //   Engram    base_{n,k} + H_head mod M_{n,k};   flat  base_n + H_head mod R_n
-__device__ __forceinline__ uint32_t item_row(const ItemConst& it, int mode, const int32_t* __restrict__ tokens,
-                                             const uint32_t* __restrict__ canon_map, uint32_t vocab, int64_t tok,
-                                             uint32_t t, int32_t* err, uint64_t* hs) {
+__device__ __forceinline__ uint32_t item_row_ids(const ItemConst& it, int mode, const uint64_t (&c)[4], uint64_t* hs) {
   uint64_t hp = 0, hh = 0, h2 = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     if (j < it.n) {
-      const uint64_t c = (t >= static_cast<uint32_t>(j)) ? canon_token(tokens, canon_map, vocab, tok - j, err) : kPad;
-      hp ^= c * it.mp[j];
-      hh ^= c * it.mh[j];
-      h2 ^= c * it.ms[j];
+      hp ^= c[j] * it.mp[j];
+      hh ^= c[j] * it.mh[j];
+      h2 ^= c[j] * it.ms[j];
     }
   }
   *hs = h2;
@@ -91,6 +88,17 @@ __device__ __forceinline__ uint32_t item_row(const ItemConst& it, int mode, cons
     return it.base + fastmod(fold32(hp), it.fm_main, it.div_main) * it.stride +
            fastmod(fold32(hh), it.fm_slot, it.slots);
   return it.base + fastmod(fold32(hh), it.fm_main, it.div_main);
+}
+
+// The same for token `tok` (position t in its sequence), reading the IDs it needs.
+__device__ __forceinline__ uint32_t item_row(const ItemConst& it, int mode, const int32_t* __restrict__ tokens,
+                                             const uint32_t* __restrict__ canon_map, uint32_t vocab, int64_t tok,
+                                             uint32_t t, int32_t* err, uint64_t* hs) {
+  uint64_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    c[j] = (j < it.n && t >= static_cast<uint32_t>(j)) ? canon_token(tokens, canon_map, vocab, tok - j, err) : kPad;
+  return item_row_ids(it, mode, c, hs);
 }
 
 // XOR masks that negate 8 packed bf16 (two per 32-bit word) from 8 sign bits.

@@ -358,6 +358,7 @@ constexpr int kProdCoordWarp = 3;
 constexpr int kProdEpiWarp0 = 4;
 constexpr int kProdGatherWarp0 = 8;
 constexpr int kUnitSlots = 4;       // ring of gather units between the coordinator and the gather warps
+constexpr int kCanonStride = 128 + 4;  // per slot: canonical IDs of the unit's tokens and the 3 before
 constexpr int kRegsLight = 40, kRegsEpi = 88, kRegsGather = 192;
 static_assert(kRegsLight + kRegsEpi + 2 * kRegsGather == 4 * 128, "setmaxnreg split must match the launch");
 constexpr int kUnitRows = 8 * 64;  // rows of a gather unit: 64 per gather warp
@@ -436,7 +437,8 @@ template <int BN, bool GATHER, bool PAIR, bool PRODUCE>
 constexpr size_t gemm_smem_bytes() {
   return 1024 /* alignment slack */ + gemm_stages<PAIR>() * (kABytes + (PAIR ? BN / 2 : BN) * kBK * 2) +
          epi_stages<GATHER || PRODUCE>() * kEpiBytes + sizeof(GemmBarriers<gemm_stages<PAIR>()>) +
-         (GATHER || PRODUCE ? kFusedItems * sizeof(ItemConst) : 0);
+         (GATHER || PRODUCE ? kFusedItems * sizeof(ItemConst) : 0) +
+         (PRODUCE ? kUnitSlots * kCanonStride * sizeof(uint32_t) : 0);
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -503,6 +505,8 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
   uint8_t* sE = sB + kSt * kBBytes;
   GemmBarriers<kSt>* bars = reinterpret_cast<GemmBarriers<kSt>*>(sE + kEpiStages * kEpiBytes);
   ItemConst* s_ic = reinterpret_cast<ItemConst*>(bars + 1);
+  // producing kernel: slot u holds at [i] the canonical ID of flat position (unit start - 3 + i)
+  uint32_t* s_canon = reinterpret_cast<uint32_t*>(s_ic + (GATHER || PRODUCE ? kFusedItems : 0));
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -760,39 +764,72 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
         const int T = gat.unit_tokens;
         const uint32_t nunits = static_cast<uint32_t>((args.N + T - 1) / T);
         if (kWG0 && warp == kProdCoordWarp) {
-          if (lane == 0) {
-            auto unit_of = [&](uint32_t c) -> int64_t {
-              return (c >= nunits || *abort) ? -1 : static_cast<int64_t>(nunits - 1 - c) * T;
-            };
-            auto publish = [&](int64_t u) {
-              if (u >= 0) {
-                __threadfence();
-                red_release_gpu_add(gat.ready + u / kReadyTokens, 1u);
+          // lane 0 claims, waits and counts; all lanes stage the canonical IDs of each unit
+          // (the reads of a token happen once, here, ahead of the gather warps)
+          auto publish = [&](int64_t u) {
+            if (u >= 0) {
+              __threadfence();
+              red_release_gpu_add(gat.ready + u / kReadyTokens, 1u);
+            }
+          };
+          bool ok = true;
+          int K = 0;  // units handed out (slot K holds -1)
+          uint32_t pending = 0;
+          if (lane == 0) pending = atomicAdd(gat.claim, 1u);
+          for (int k = 0;; ++k) {
+            const int s = k % kUnitSlots;
+            int64_t val = -1;
+            if (lane == 0) val = (pending >= nunits || *abort) ? -1 : static_cast<int64_t>(nunits - 1 - pending) * T;
+            val = __shfl_sync(0xffffffffu, val, 0);
+            // token IDs of positions val - 3 .. val + T - 1 (issued before the slot is free)
+            constexpr int kStage = (kCanonStride + 31) / 32;
+            int32_t x[kStage];
+#pragma unroll
+            for (int q = 0; q < kStage; ++q) {
+              const int i = lane + 32 * q;
+              const int64_t f = val - 3 + i;
+              x[q] = 0;
+              if (val >= 0 && i < T + 3 && f >= 0 && f < args.N) x[q] = __ldg(gat.tokens + f);
+            }
+            if (k >= kUnitSlots) {
+              // unit k - kUnitSlots: stored by every gather warp, then counted; its slot is free
+              bool waited = true;
+              if (lane == 0) {
+                waited = mbar_wait<false, kRebalance>(smem_u32(&bars->unit_done[s]),
+                                                      static_cast<uint32_t>((k / kUnitSlots - 1) & 1), abort);
+                if (waited) publish(s_unit[s]);
               }
-            };
-            bool ok = true;
-            int K = 0;  // units handed out (slot K holds -1)
-            uint32_t pending = atomicAdd(gat.claim, 1u);
-            for (int k = 0;; ++k) {
-              const int s = k % kUnitSlots;
-              if (k >= kUnitSlots) {
-                // unit k - kUnitSlots: stored by every gather warp, then counted; its slot is free
-                if (!mbar_wait<false, kRebalance>(smem_u32(&bars->unit_done[s]),
-                                                  static_cast<uint32_t>((k / kUnitSlots - 1) & 1), abort)) {
-                  ok = false;
-                  break;
-                }
-                publish(s_unit[s]);
-              }
-              const int64_t val = unit_of(pending);
-              s_unit[s] = val;
-              mbar_arrive(smem_u32(&bars->unit_full[s]));
-              if (val < 0) {
-                K = k;
+              if (!__shfl_sync(0xffffffffu, waited, 0)) {
+                ok = false;
                 break;
               }
-              pending = atomicAdd(gat.claim, 1u);  // needed one unit later
             }
+            // canonical IDs (an out-of-range ID reads as 0 and is reported by its own unit)
+#pragma unroll
+            for (int q = 0; q < kStage; ++q) {
+              const int i = lane + 32 * q;
+              const int64_t f = val - 3 + i;
+              if (val >= 0 && i < T + 3 && f >= 0 && f < args.N) {
+                int32_t id = x[q];
+                if (id < 0 || static_cast<uint32_t>(id) >= gat.P.vocab) {
+                  if (i >= 3 && gat.err) atomicMin(reinterpret_cast<unsigned int*>(gat.err), static_cast<unsigned int>(f));
+                  id = 0;
+                }
+                s_canon[s * kCanonStride + i] = gat.canon_map ? __ldg(gat.canon_map + id) : static_cast<uint32_t>(id);
+              }
+            }
+            __syncwarp();
+            if (lane == 0) {
+              s_unit[s] = val;
+              mbar_arrive(smem_u32(&bars->unit_full[s]));
+              if (val >= 0) pending = atomicAdd(gat.claim, 1u);  // needed one unit later
+            }
+            if (val < 0) {
+              K = k;
+              break;
+            }
+          }
+          if (lane == 0) {
             for (int j = K - kUnitSlots + 1 < 0 ? 0 : K - kUnitSlots + 1; ok && j < K; ++j) {
               const int s = j % kUnitSlots;
               if (!mbar_wait<false, kRebalance>(smem_u32(&bars->unit_done[s]),
@@ -822,7 +859,7 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
           int64_t prev = -1;
           int kprev = 0;
           uint4 vb[NB][kLoads];
-          auto hash = [&](int64_t tok0) {
+          auto hash = [&](int64_t tok0, const uint32_t* cs) {
 #pragma unroll
             for (int j = 0; j < kPairs; ++j) {
               const int p = 64 * gw + lane + 32 * j;
@@ -833,9 +870,13 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
               if (p < Hu && tok0 + s < args.N) {
                 const int it = p - s * items;
                 const int64_t tok = tok0 + s;
-                uint64_t hs;
-                r[j] = item_row(s_ic[it], gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, tok,
-                                fastmod(static_cast<uint32_t>(tok), gat.fm_L, gat.L), gat.err, &hs);
+                const uint32_t t = fastmod(static_cast<uint32_t>(tok), gat.fm_L, gat.L);
+                const uint32_t* ids = cs + 3 + s;  // ids[-j]: position tok - j
+                uint64_t c[4], hs;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                  c[jj] = (jj < s_ic[it].n && t >= static_cast<uint32_t>(jj)) ? ids[-jj] : kPad;
+                r[j] = item_row_ids(s_ic[it], gat.P.mode, c, &hs);
                 sw[j] = mix64(hs + kGolden);
                 off[j] = static_cast<uint32_t>(s) * out_row + static_cast<uint32_t>(it) * 128u;
               }
@@ -881,7 +922,7 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
             }
             const int64_t u = s_unit[s];
             if (u < 0) return false;
-            hash(u);  // under the previous unit's loads
+            hash(u, s_canon + s * kCanonStride);  // under the previous unit's loads
             if constexpr (NB == 2) {
               issue_loads(std::integral_constant<int, b>());
               store_prev(std::integral_constant<int, b ^ 1>());
