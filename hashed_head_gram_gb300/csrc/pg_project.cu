@@ -20,7 +20,6 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
-#include <type_traits>
 
 #include "pg_hash.cuh"
 
@@ -85,7 +84,7 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
 }
 
 template <bool CLUSTER>
-__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
   const uint64_t t0 = globaltimer();
   for (;;) {
 #pragma unroll 1
@@ -95,19 +94,12 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatil
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
-template <bool CLUSTER>
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
-  return mbar_spin<CLUSTER>(bar, parity, abort);
-}
 
 // Waits for the phase of `parity` to complete; false after the time limit or when
 // another role of the CTA has already given up (`abort`). The first poll is inline: the
 // MMA issuer runs one wait per 512 tensor-core cycles and a call costs it a large share.
-// INL: the rest inline too (kernels that change their register count with setmaxnreg
-// cannot call out-of-line code from the reduced roles).
-template <bool CLUSTER = false, bool INL = false>
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  if constexpr (INL) return mbar_poll<CLUSTER>(bar, parity) || mbar_spin<CLUSTER>(bar, parity, abort);
   return mbar_poll<CLUSTER>(bar, parity) || mbar_wait_slow<CLUSTER>(bar, parity, abort);
 }
 
@@ -347,26 +339,16 @@ constexpr int kEpiCols = 32;        // columns per epilogue sub-tile
 constexpr int kEpiStagesMax = 4;    // epilogue shared-memory ring (3 slots in the fused kernel)
 constexpr int kEpiBytes = kBM * kEpiCols * 2;
 constexpr int kFusedItems = 32;     // (order, head) items of the fused kernel
-// Producing kernel (PRODUCE): 16 warps in 4 warpgroups. Warpgroup 0: A/B producer, MMA
-// issuer, epilogue operand producer, gather coordinator; warpgroup 1: the 4 epilogue warps;
-// warpgroups 2-3: 8 gather warps. Without the context gate the registers are rebalanced
-// (setmaxnreg) from 128 per thread at launch to 40 / 88 / 192 / 192: the sum, 512 x 128
-// per warpgroup column, is exactly what the launch holds, and each gather warp then keeps
-// two units' rows (128 rows, 16 KB) of loads in flight instead of one.
+// Producing kernel (PRODUCE): 16 warps. Warps 0-2: A/B producer, MMA issuer, epilogue
+// operand producer; warp 3: gather coordinator; warps 4-7: epilogue; warps 8-15: gather.
 constexpr int kProduceThreads = 512;
 constexpr int kProdCoordWarp = 3;
 constexpr int kProdEpiWarp0 = 4;
 constexpr int kProdGatherWarp0 = 8;
 constexpr int kUnitSlots = 4;       // ring of gather units between the coordinator and the gather warps
 constexpr int kCanonStride = 128 + 4;  // per slot: canonical IDs of the unit's tokens and the 3 before
-constexpr int kRegsLight = 40, kRegsEpi = 88, kRegsGather = 192;
-static_assert(kRegsLight + kRegsEpi + 2 * kRegsGather == 4 * 128, "setmaxnreg split must match the launch");
 constexpr int kUnitRows = 8 * 64;  // rows of a gather unit: 64 per gather warp
 
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 constexpr int kReadyTokens = kBM;   // tokens per ready counter (one A tile of one CTA)
 
 template <bool GATHER>
@@ -488,7 +470,6 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
                    const __grid_constant__ typename GatherParam<GATHER || PRODUCE>::type gat) {
   static_assert(!(GATHER && PAIR), "the fused gather runs on single-CTA tiles");
   static_assert(!(GATHER && PRODUCE), "one way of making A");
-  constexpr bool kRebalance = PRODUCE && GATE != PG_GATE_CONTEXT;  // the context epilogue needs ~160 registers
   constexpr int kSt = gemm_stages<PAIR>();
   constexpr int kEpiStages = epi_stages<GATHER || PRODUCE>();
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of W this CTA stages per k-block
@@ -562,639 +543,598 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
   const int num_tiles = num_m * num_n;
   const int num_kb = args.Din / kBK;
 
-  // Warp roles. With the registers rebalanced, each warpgroup first executes its one
-  // setmaxnreg (all four warps the same instruction), then only its own roles are compiled
-  // into its branch (kWG = its index; -1: every role, nothing rebalanced).
   __shared__ int64_t s_unit[kUnitSlots];  // gather units handed out (producing kernel)
-  auto roles = [&](auto wg_c) {
-    constexpr int kWG = decltype(wg_c)::value;
-    constexpr bool kWG0 = kWG < 0 || kWG == 0, kWG1 = kWG < 0 || kWG == 1, kWG23 = kWG < 0 || kWG >= 2;
-    if (kWG0 && warp == 0) {
-      // ------------------------------------------------------------ A/B TMA producer
-      if (lane == 0) {
-        if (!GATHER) tma_prefetch_map(&map_a);
-        tma_prefetch_map(&map_b);
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        uint32_t issued = 0;  // bit s: stage s holds a load nobody has consumed yet (error path)
-        for (int tile = unit; tile < num_tiles && ok; tile += units) {
-          const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
-          if constexpr (PRODUCE) {
-            // this CTA's 128 rows of A must have been written by the gather warps
-            const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
-            if (m0 < args.N) {
-              const int rows = min(kBM, args.N - m0);
-              if (!wait_ready(gat.ready + m0 / kReadyTokens,
-                              static_cast<uint32_t>((rows + gat.unit_tokens - 1) / gat.unit_tokens), abort)) {
-                atomicOr(args.err_word, 64);
-                ok = false;
-                break;
-              }
-              // their generic-proxy writes, now visible to this thread, ordered before its TMA reads
-              asm volatile("fence.proxy.async.global;" ::: "memory");
-            }
-          }
-          for (int kb = 0; kb < num_kb; ++kb) {
-            if (!mbar_wait<false, kRebalance>(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
+  if (warp == 0) {
+    // ------------------------------------------------------------ A/B TMA producer
+    if (lane == 0) {
+      if (!GATHER) tma_prefetch_map(&map_a);
+      tma_prefetch_map(&map_b);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t issued = 0;  // bit s: stage s holds a load nobody has consumed yet (error path)
+      for (int tile = unit; tile < num_tiles && ok; tile += units) {
+        const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
+        if constexpr (PRODUCE) {
+          // this CTA's 128 rows of A must have been written by the gather warps
+          const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+          if (m0 < args.N) {
+            const int rows = min(kBM, args.N - m0);
+            if (!wait_ready(gat.ready + m0 / kReadyTokens,
+                            static_cast<uint32_t>((rows + gat.unit_tokens - 1) / gat.unit_tokens), abort)) {
+              atomicOr(args.err_word, 64);
               ok = false;
               break;
             }
-            const uint32_t full = smem_u32(&bars->full[stage]);
-            if constexpr (PAIR) {
-              if (rank == 0) mbar_expect_tx(full, 2 * (kABytes + kBBytes));
-              const uint32_t full0 = pair_addr(full, 0);
-              tma_load_2d_pair(smem_u32(sA + stage * kABytes), &map_a, full0, kb * kBK,
-                               m_blk * kTileM + static_cast<int>(rank) * kBM);
-              tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &map_b, full0, kb * kBK,
-                               n_blk * BN + static_cast<int>(rank) * kBRows);
-            } else {
-              mbar_expect_tx(full, GATHER ? kBBytes : kABytes + kBBytes);
-              if (!GATHER) tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
-              tma_load_2d(smem_u32(sB + stage * kBBytes), &map_b, full, kb * kBK, n_blk * BN);
-            }
-            issued |= 1u << stage;
-            if (++stage == kSt) {
-              stage = 0;
-              phase ^= 1u;
-            }
+            // their generic-proxy writes, now visible to this thread, ordered before its TMA reads
+            asm volatile("fence.proxy.async.global;" ::: "memory");
           }
         }
-        // Tail: wait until the MMA has released the last fill of every stage. Its commits
-        // arrive asynchronously (on the other CTA of a pair too); none may land after the
-        // CTA has exited. (A stage never filled passes at once.)
-        for (int i = 0; ok && i < kSt; ++i) {
-          if (!mbar_wait<false, kRebalance>(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
             ok = false;
             break;
           }
+          const uint32_t full = smem_u32(&bars->full[stage]);
+          if constexpr (PAIR) {
+            if (rank == 0) mbar_expect_tx(full, 2 * (kABytes + kBBytes));
+            const uint32_t full0 = pair_addr(full, 0);
+            tma_load_2d_pair(smem_u32(sA + stage * kABytes), &map_a, full0, kb * kBK,
+                             m_blk * kTileM + static_cast<int>(rank) * kBM);
+            tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &map_b, full0, kb * kBK,
+                             n_blk * BN + static_cast<int>(rank) * kBRows);
+          } else {
+            mbar_expect_tx(full, GATHER ? kBBytes : kABytes + kBBytes);
+            if (!GATHER) tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
+            tma_load_2d(smem_u32(sB + stage * kBBytes), &map_b, full, kb * kBK, n_blk * BN);
+          }
+          issued |= 1u << stage;
           if (++stage == kSt) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (!ok) {
-          atomicOr(args.err_word, 1);
-          *abort = 1;
-          // Let copies already in flight land before the CTA can exit (bounded; a pair's
-          // copies count on rank 0's barriers and are waited for at the end instead).
-          for (int s = 0; s < kSt; ++s)
-            if (!PAIR && (issued & (1u << s))) {
-              const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-              const uint64_t t0 = globaltimer();
-              while (!mbar_try_wait(smem_u32(&bars->full[s]), par) && globaltimer() - t0 < kWaitLimitNs) {
-              }
-            }
+      }
+      // Tail: wait until the MMA has released the last fill of every stage. Its commits
+      // arrive asynchronously (on the other CTA of a pair too); none may land after the
+      // CTA has exited. (A stage never filled passes at once.)
+      for (int i = 0; ok && i < kSt; ++i) {
+        if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        if (++stage == kSt) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-    } else if (kWG0 && warp == 1) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0 && rank == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        bool ok = true;
-        for (int tile = unit; tile < num_tiles && ok; tile += units) {
-          if (!mbar_wait<PAIR, kRebalance>(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-          for (int kb = 0; kb < num_kb; ++kb) {
-            if (!mbar_wait<PAIR, kRebalance>(smem_u32(&bars->full[stage]), phase, abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t a0 = sw128_desc(smem_u32(sA + stage * kABytes));
-            const uint64_t b0 = sw128_desc(smem_u32(sB + stage * kBBytes));
-  #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)  // advance 16 elements = 32 bytes = 2 units
-              umma_bf16<PAIR>(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc, (kb | k) != 0);
-            umma_commit<PAIR>(smem_u32(&bars->empty[stage]));
-            if (++stage == kSt) {
-              stage = 0;
-              phase ^= 1u;
+      if (!ok) {
+        atomicOr(args.err_word, 1);
+        *abort = 1;
+        // Let copies already in flight land before the CTA can exit (bounded; a pair's
+        // copies count on rank 0's barriers and are waited for at the end instead).
+        for (int s = 0; s < kSt; ++s)
+          if (!PAIR && (issued & (1u << s))) {
+            const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(&bars->full[s]), par) && globaltimer() - t0 < kWaitLimitNs) {
             }
           }
-          if (!ok) break;
-          umma_commit<PAIR>(smem_u32(&bars->tmem_full[acc]));
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
-        }
-        if (!ok) {
-          atomicOr(args.err_word, 2);
-          *abort = 1;
-        }
-        // Every MMA this thread issued has finished before TMEM can be released.
-        umma_commit_local<PAIR>(smem_u32(&bars->mma_done));
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(smem_u32(&bars->mma_done), 0) && globaltimer() - t0 < kWaitLimitNs) {
-        }
       }
-    } else if (kWG0 && warp == 2) {
-      // ------------------------------------------------------------ epilogue operand producer
-      if (lane == 0) {
-        if (GATE == PG_GATE_SCALAR) tma_prefetch_map(&map_x);
-        if (GATE == PG_GATE_CONTEXT) tma_prefetch_map(&map_h);
-        uint32_t seq = 0;
-        bool ok = true;
-        uint32_t issued = 0;
-        for (int tile = unit; tile < num_tiles && ok; tile += units) {
-          const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
-          const int n0 = n_blk * BN, m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
-          const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
-          if (m0 >= args.N) continue;  // this CTA's rows of the tile lie past the last token
-          for (int j = 0; j < kSub; ++j, ++seq) {
-            const int slot = static_cast<int>(seq % kEpiStages);
-            const uint32_t ph = (seq / kEpiStages) & 1u;
-            if (!mbar_wait<false, kRebalance>(smem_u32(&bars->epi_empty[slot]), ph ^ 1u, abort)) {
-              ok = false;
-              break;
-            }
-            const uint32_t full = smem_u32(&bars->epi_full[slot]);
-            const uint32_t dst = smem_u32(sE + slot * kEpiBytes);
-            if (GATE == PG_GATE_SCALAR) {
-              mbar_expect_tx(full, kEpiBytes);
-              tma_load_2d(dst, &map_x, full, n0 + j * kEpiCols, m0);
-              issued |= 1u << slot;
-            } else if (is_k) {
-              const int m = n0 / args.d - 1;
-              const int kc = n0 - (m + 1) * args.d;
-              mbar_expect_tx(full, kEpiBytes);
-              tma_load_2d(dst, &map_h, full, kc + j * kEpiCols, m * args.N + m0);
-              issued |= 1u << slot;
-            } else {
-              mbar_arrive(full);   // output staging only: hand the free slot over
-            }
-          }
-        }
-        if (!ok) {
-          atomicOr(args.err_word, 8);
-          *abort = 1;
-          for (int s = 0; s < kEpiStages; ++s)
-            if (issued & (1u << s)) {
-              const uint64_t t0 = globaltimer();
-              while (globaltimer() - t0 < kWaitLimitNs / 4 &&
-                     !mbar_try_wait(smem_u32(&bars->epi_full[s]), ((seq - 1 - ((seq - 1 - s) % kEpiStages)) / kEpiStages) & 1u)) {
-              }
-            }
-        }
-      }
-    } else if ((GATHER && warp >= kGatherWarp0) ||
-               (PRODUCE && ((kWG0 && warp == kProdCoordWarp) || (kWG23 && warp >= kProdGatherWarp0)))) {
-      if constexpr (PRODUCE) {
-        // ---------------------------------------------------------- e_t producers (warps 3, 8..15)
-        // Warps 8..15 gather units of T tokens x `items` heads = Hu <= 512 rows of 64 bf16
-        // (128 bytes), T a power of two <= 128 (a unit never spans two ready counters). Warp
-        // w takes rows [64 w, 64 w + 64) of every unit: lane l hashes rows 64 w + l + 32 j
-        // (token p / items, head p mod items), then 8 lanes per row move its 16-byte pieces,
-        // row 64 w + 4 i + (l >> 3) being lane ((4 i + (l >> 3)) mod 32)'s pair i / 8.
-        // Warp 3 coordinates through a ring of kUnitSlots slots in shared memory: unit k goes
-        // into slot k mod kUnitSlots (the claim order is the order the tiles are walked: last
-        // m-block first) and is announced on unit_full[slot]; every gather warp arrives on
-        // unit_done[slot] once its stores of the unit are issued, after which the
-        // coordinator fences, counts the unit on its ready counter and reuses the slot. The
-        // gather warps never wait for one another: each runs its own pipeline (with the
-        // rebalanced registers, two units' loads in flight: unit k's loads are issued before
-        // unit k - 1 is stored). Every wait is a bounded mbarrier wait.
-        const int items = gat.P.O * gat.P.H;
-        const int T = gat.unit_tokens;
-        const uint32_t nunits = static_cast<uint32_t>((args.N + T - 1) / T);
-        if (kWG0 && warp == kProdCoordWarp) {
-          // lane 0 claims, waits and counts; all lanes stage the canonical IDs of each unit
-          // (the reads of a token happen once, here, ahead of the gather warps)
-          auto publish = [&](int64_t u) {
-            if (u >= 0) {
-              __threadfence();
-              red_release_gpu_add(gat.ready + u / kReadyTokens, 1u);
-            }
-          };
-          bool ok = true;
-          int K = 0;  // units handed out (slot K holds -1)
-          uint32_t pending = 0;
-          if (lane == 0) pending = atomicAdd(gat.claim, 1u);
-          for (int k = 0;; ++k) {
-            const int s = k % kUnitSlots;
-            int64_t val = -1;
-            if (lane == 0) val = (pending >= nunits || *abort) ? -1 : static_cast<int64_t>(nunits - 1 - pending) * T;
-            val = __shfl_sync(0xffffffffu, val, 0);
-            // token IDs of positions val - 3 .. val + T - 1 (issued before the slot is free)
-            constexpr int kStage = (kCanonStride + 31) / 32;
-            int32_t x[kStage];
-#pragma unroll
-            for (int q = 0; q < kStage; ++q) {
-              const int i = lane + 32 * q;
-              const int64_t f = val - 3 + i;
-              x[q] = 0;
-              if (val >= 0 && i < T + 3 && f >= 0 && f < args.N) x[q] = __ldg(gat.tokens + f);
-            }
-            if (k >= kUnitSlots) {
-              // unit k - kUnitSlots: stored by every gather warp, then counted; its slot is free
-              bool waited = true;
-              if (lane == 0) {
-                waited = mbar_wait<false, kRebalance>(smem_u32(&bars->unit_done[s]),
-                                                      static_cast<uint32_t>((k / kUnitSlots - 1) & 1), abort);
-                if (waited) publish(s_unit[s]);
-              }
-              if (!__shfl_sync(0xffffffffu, waited, 0)) {
-                ok = false;
-                break;
-              }
-            }
-            // canonical IDs (an out-of-range ID reads as 0 and is reported by its own unit)
-#pragma unroll
-            for (int q = 0; q < kStage; ++q) {
-              const int i = lane + 32 * q;
-              const int64_t f = val - 3 + i;
-              if (val >= 0 && i < T + 3 && f >= 0 && f < args.N) {
-                int32_t id = x[q];
-                if (id < 0 || static_cast<uint32_t>(id) >= gat.P.vocab) {
-                  if (i >= 3 && gat.err) atomicMin(reinterpret_cast<unsigned int*>(gat.err), static_cast<unsigned int>(f));
-                  id = 0;
-                }
-                s_canon[s * kCanonStride + i] = gat.canon_map ? __ldg(gat.canon_map + id) : static_cast<uint32_t>(id);
-              }
-            }
-            __syncwarp();
-            if (lane == 0) {
-              s_unit[s] = val;
-              mbar_arrive(smem_u32(&bars->unit_full[s]));
-              if (val >= 0) pending = atomicAdd(gat.claim, 1u);  // needed one unit later
-            }
-            if (val < 0) {
-              K = k;
-              break;
-            }
-          }
-          if (lane == 0) {
-            for (int j = K - kUnitSlots + 1 < 0 ? 0 : K - kUnitSlots + 1; ok && j < K; ++j) {
-              const int s = j % kUnitSlots;
-              if (!mbar_wait<false, kRebalance>(smem_u32(&bars->unit_done[s]),
-                                                static_cast<uint32_t>((j / kUnitSlots) & 1), abort)) {
-                ok = false;
-                break;
-              }
-              publish(s_unit[s]);
-            }
-            if (!ok) {
-              atomicOr(args.err_word, 128);
-              *abort = 1;
-            }
-          }
-          __syncwarp();
-        } else if (kWG23) {
-          constexpr int kPairs = 2, kLoads = 16;      // 64 rows of this warp per unit
-          constexpr int NB = kRebalance ? 2 : 1;      // units whose loads are in flight
-          const int gw = warp - kProdGatherWarp0;
-          const int Hu = T * items;
-          const uint32_t out_row = static_cast<uint32_t>(items) * 128u;
-          const int piece = lane & 7, sub = lane >> 3;
-          uint32_t r[kPairs], off[kPairs];            // unit being hashed and loaded
-          uint64_t sw[kPairs];
-          uint32_t offp[kPairs];                      // previous unit (loaded, to be stored)
-          uint64_t swp[kPairs];
-          int64_t prev = -1;
-          int kprev = 0;
-          uint4 vb[NB][kLoads];
-          auto hash = [&](int64_t tok0, const uint32_t* cs) {
-#pragma unroll
-            for (int j = 0; j < kPairs; ++j) {
-              const int p = 64 * gw + lane + 32 * j;
-              const int s = p / items;
-              r[j] = 0;
-              sw[j] = 0;
-              off[j] = 0xFFFFFFFFu;  // no row
-              if (p < Hu && tok0 + s < args.N) {
-                const int it = p - s * items;
-                const int64_t tok = tok0 + s;
-                const uint32_t t = fastmod(static_cast<uint32_t>(tok), gat.fm_L, gat.L);
-                const uint32_t* ids = cs + 3 + s;  // ids[-j]: position tok - j
-                uint64_t c[4], hs;
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                  c[jj] = (jj < s_ic[it].n && t >= static_cast<uint32_t>(jj)) ? ids[-jj] : kPad;
-                r[j] = item_row_ids(s_ic[it], gat.P.mode, c, &hs);
-                sw[j] = mix64(hs + kGolden);
-                off[j] = static_cast<uint32_t>(s) * out_row + static_cast<uint32_t>(it) * 128u;
-              }
-            }
-          };
-          auto issue_loads = [&](auto b_c) {
-            constexpr int b = decltype(b_c)::value;
-#pragma unroll
-            for (int i = 0; i < kLoads; ++i) {
-              const int src = (4 * i + sub) & 31;
-              const uint32_t row = __shfl_sync(0xffffffffu, r[i / 8], src);
-              const uint32_t o = __shfl_sync(0xffffffffu, off[i / 8], src);
-              vb[b][i] = make_uint4(0, 0, 0, 0);
-              if (o != 0xFFFFFFFFu) vb[b][i] = ldg_stream(gat.table + static_cast<uint64_t>(row) * 128u + piece * 16);
-            }
-          };
-          // sign-flip and store the previous unit from buffer b, then report it to the coordinator
-          auto store_prev = [&](auto b_c) {
-            constexpr int b = decltype(b_c)::value;
-            if (prev < 0) return;
-            uint8_t* out = gat.e_out + static_cast<uint64_t>(prev) * out_row + piece * 16;
-#pragma unroll
-            for (int q = 0; q < kLoads; ++q) {
-              const int src = (4 * q + sub) & 31;
-              const uint64_t w = __shfl_sync(0xffffffffu, swp[q / 8], src);
-              const uint32_t o = __shfl_sync(0xffffffffu, offp[q / 8], src);
-              const uint32_t bits = static_cast<uint32_t>(w >> (8 * piece)) & 0xFFu;
-              if (o != 0xFFFFFFFFu) *reinterpret_cast<uint4*>(out + o) = xor4(vb[b][q], bf16_sign_mask(bits));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->unit_done[kprev % kUnitSlots]));
-          };
-          bool ok = true;
-          int k = 0;
-          // unit k, its loads into buffer k mod NB; false when the ring says there is no more
-          auto step = [&](auto b_c) -> bool {
-            constexpr int b = decltype(b_c)::value;
-            const int s = k % kUnitSlots;
-            if (!mbar_wait<false, kRebalance>(smem_u32(&bars->unit_full[s]),
-                                              static_cast<uint32_t>((k / kUnitSlots) & 1), abort)) {
-              ok = false;
-              return false;
-            }
-            const int64_t u = s_unit[s];
-            if (u < 0) return false;
-            hash(u, s_canon + s * kCanonStride);  // under the previous unit's loads
-            if constexpr (NB == 2) {
-              issue_loads(std::integral_constant<int, b>());
-              store_prev(std::integral_constant<int, b ^ 1>());
-            } else {
-              static_cast<void>(b);
-              store_prev(std::integral_constant<int, 0>());
-              issue_loads(std::integral_constant<int, 0>());
-            }
-            prev = u;
-            kprev = k;
-#pragma unroll
-            for (int j = 0; j < kPairs; ++j) {
-              offp[j] = off[j];
-              swp[j] = sw[j];
-            }
-            ++k;
-            return true;
-          };
-          for (;;) {
-            if (!step(std::integral_constant<int, 0>())) break;
-            if constexpr (NB == 2) {
-              if (!step(std::integral_constant<int, 1>())) break;
-            }
-          }
-          // the last unit: loaded into buffer (k - 1) mod NB
-          if (ok) {
-            if ((k - 1) % NB == 0) store_prev(std::integral_constant<int, 0>());
-            else store_prev(std::integral_constant<int, NB - 1>());
-          } else {
-            atomicOr(args.err_word, 128);
-            *abort = 1;
-          }
-        }
-      } else if constexpr (GATHER) {
-        // ---------------------------------------------------------- A-operand gather (warps 7..14)
-        // Pair p of warps builds every A tile of ring stage p; warp `half` of the pair covers
-        // tokens [64 half, 64 half + 64) of the 128-token block. Lane l hashes tokens l and
-        // l + 32 of its half for head kb, then 8 lanes per row move 16-byte chunks: chunk
-        // (token, piece) -> A-tile row `token`, physical chunk piece ^ (row & 7) (128-byte
-        // swizzle, the layout the TMA would have written).
-        const int gw = warp - kGatherWarp0;
-        const int pair = gw >> 1, half = gw & 1;
-        const int piece = lane & 7, sub = lane >> 3;
-        const int stage = pair;
-        // rows and sign words of tokens (64 half + lane) and (+32) of one k-block
-        auto hash_rows = [&](int tile, int kb, uint32_t& ra, uint32_t& rb, uint64_t& sa, uint64_t& sb) {
-          const int m0 = ((num_tiles - 1 - tile) / num_n) * kBM;
-          const ItemConst& it = s_ic[kb];
-          const int64_t ta = static_cast<int64_t>(m0) + 64 * half + lane, tb = ta + 32;
-          uint64_t hs;
-          ra = rb = 0;
-          sa = sb = 0;
-          if (ta < args.N) {
-            ra = item_row(it, gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, ta,
-                          fastmod(static_cast<uint32_t>(ta), gat.fm_L, gat.L), gat.err, &hs);
-            sa = mix64(hs + kGolden);
-          }
-          if (tb < args.N) {
-            rb = item_row(it, gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, tb,
-                          fastmod(static_cast<uint32_t>(tb), gat.fm_L, gat.L), gat.err, &hs);
-            sb = mix64(hs + kGolden);
-          }
-        };
-        // this pair's k-blocks: sequence numbers q = pair, pair + 4, ... over the CTA's tiles
-        int tile = blockIdx.x, kb = pair;
-        while (kb >= num_kb && tile < num_tiles) {
-          kb -= num_kb;
-          tile += gridDim.x;
-        }
-        uint32_t q = pair;
-        uint32_t ra, rb;
-        uint64_t sa, sb;
-        if (tile < num_tiles) hash_rows(tile, kb, ra, rb, sa, sb);
-        bool ok = true;
-        while (tile < num_tiles) {
-          // 1. loads of this k-block (they do not need the stage to be free)
-          uint4 v[16];
-  #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int src = 4 * (i & 7) + sub;
-            const uint32_t r = __shfl_sync(0xffffffffu, i < 8 ? ra : rb, src);
-            v[i] = __ldg(reinterpret_cast<const uint4*>(gat.table + static_cast<uint64_t>(r) * 128u + piece * 16));
-          }
-          // 2. hash the next k-block of this pair while the loads are in flight
-          int ntile = tile, nkb = kb + 4;
-          while (nkb >= num_kb && ntile < num_tiles) {
-            nkb -= num_kb;
-            ntile += gridDim.x;
-          }
-          uint32_t na = 0, nb = 0;
-          uint64_t nsa = 0, nsb = 0;
-          if (ntile < num_tiles) hash_rows(ntile, nkb, na, nb, nsa, nsb);
-          // 3. wait for the stage, then sign-flip and store into the swizzled A tile
-          if (!mbar_wait<false, kRebalance>(smem_u32(&bars->empty[stage]), ((q >> 2) & 1u) ^ 1u, abort)) {
-            ok = false;
-            break;
-          }
-          uint8_t* a_tile = sA + stage * kABytes;
-  #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int src = 4 * (i & 7) + sub;
-            const uint64_t sw = __shfl_sync(0xffffffffu, i < 8 ? sa : sb, src);
-            const uint32_t bits = static_cast<uint32_t>(sw >> (8 * piece)) & 0xFFu;
-            const int row = 64 * half + (i < 8 ? 0 : 32) + src;
-            *reinterpret_cast<uint4*>(a_tile + row * 128 + ((piece ^ (row & 7)) << 4)) = xor4(v[i], bf16_sign_mask(bits));
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&bars->full[stage]));
-          tile = ntile;
-          kb = nkb;
-          q += 4;
-          ra = na;
-          rb = nb;
-          sa = nsa;
-          sb = nsb;
-        }
-        if (!ok) {
-          atomicOr(args.err_word, 16);
-          *abort = 1;
-        }
-      }
-    } else if (kWG1) {
-      // ------------------------------------------------------------ epilogue (warps 3..6; 4..7 when PRODUCE)
-      const int epi = threadIdx.x - 32 * (PRODUCE ? kProdEpiWarp0 : 3);
-      const int quarter = warp & 3;  // TMEM lanes this warp may access
-      const int row_in_tile = quarter * 32 + lane;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      uint32_t seq = 0;
       bool ok = true;
-      int pending = -1;             // slot whose TMA store may still be reading (thread epi == 0)
-      const int tpb = args.d / BN;  // tiles per branch (context gate)
       for (int tile = unit; tile < num_tiles && ok; tile += units) {
-        const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
-        if (!mbar_wait<false, kRebalance>(smem_u32(&bars->tmem_full[acc]), acc_phase, abort)) {
+        if (!mbar_wait<PAIR>(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
-        const bool rows_here = m0 < args.N;  // (the operand producer skips the same tiles)
-        const int row = m0 + row_in_tile;
-        const bool live = row < args.N;
-        const int n0 = n_blk * BN;
-        const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
-        const int m_br = is_k ? n0 / args.d - 1 : 0;
-        const int kc = is_k ? n0 - (m_br + 1) * args.d : 0;
-        const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-        float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
-        float s_vv = 0.f;  // context gate, v tiles: sum of the stored (bf16) v^2 of the row
-        for (int j = 0; rows_here && j < kSub; ++j, ++seq) {
-          const int slot = static_cast<int>(seq % kEpiStages);
-          const uint32_t ph = (seq / kEpiStages) & 1u;
-          if (!mbar_wait<false, kRebalance>(smem_u32(&bars->epi_full[slot]), ph, abort)) {
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait<PAIR>(smem_u32(&bars->full[stage]), phase, abort)) {
             ok = false;
             break;
           }
-          uint32_t r[32];
-          tmem_ld32(t_base + static_cast<uint32_t>(j * kEpiCols), r);
-          tmem_ld_wait();
-          uint8_t* slot_p = sE + slot * kEpiBytes;
-          if (is_k) {
-            const float4* gh = reinterpret_cast<const float4*>(args.gamma_h + kc + j * kEpiCols);
-            const float4* gk = reinterpret_cast<const float4*>(args.gamma_k + kc + j * kEpiCols);
-  #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float hf[8];
-              unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_p + epi_offset(row_in_tile, c)), hf);
-              const float4 gh0 = __ldg(gh + 2 * c), gh1 = __ldg(gh + 2 * c + 1);
-              const float4 gk0 = __ldg(gk + 2 * c), gk1 = __ldg(gk + 2 * c + 1);
-              const float ghv[8] = {gh0.x, gh0.y, gh0.z, gh0.w, gh1.x, gh1.y, gh1.z, gh1.w};
-              const float gkv[8] = {gk0.x, gk0.y, gk0.z, gk0.w, gk1.x, gk1.y, gk1.z, gk1.w};
-  #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float kv = __uint_as_float(r[8 * c + i]);
-                s_kk = fmaf(kv, kv, s_kk);
-                s_hh = fmaf(hf[i], hf[i], s_hh);
-                s_hk = fmaf(ghv[i] * gkv[i] * hf[i], kv, s_hk);
-              }
-            }
-          } else {
-  #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint4* p = reinterpret_cast<uint4*>(slot_p + epi_offset(row_in_tile, c));
-              float o[8];
-              if (GATE == PG_GATE_SCALAR) {
-                float xf[8];
-                unpack_bf16x8(*p, xf);
-  #pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = fmaf(args.g, __uint_as_float(r[8 * c + i]), xf[i]);
-              } else {
-  #pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = __uint_as_float(r[8 * c + i]);
-              }
-              const uint4 packed = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
-                                              pack_bf16(o[6], o[7]));
-              *p = packed;
-              if (GATE == PG_GATE_CONTEXT) {
-                float q[8];
-                unpack_bf16x8(packed, q);
-  #pragma unroll
-                for (int i = 0; i < 8; ++i) s_vv = fmaf(q[i], q[i], s_vv);
-              }
-            }
-            fence_proxy_async_smem();
-          }
-          mbar_arrive(smem_u32(&bars->epi_done[slot]));
-          if (epi == 0) {
-            // the slot goes back to the producer once every thread is done with it and,
-            // for outputs, once its TMA store has read it
-            if (!mbar_wait<false, kRebalance>(smem_u32(&bars->epi_done[slot]), ph, abort)) {
-              ok = false;
-              break;
-            }
-            if (!is_k) {
-              tma_store_2d(&map_v, smem_u32(slot_p), n0 + j * kEpiCols, m0);
-              bulk_commit();
-              if (pending >= 0) {   // one store stays in flight; the one before it is done reading
-                bulk_wait_read_all_but_one();
-                mbar_arrive(smem_u32(&bars->epi_empty[pending]));
-              }
-              pending = slot;
-            } else {
-              if (pending >= 0) {
-                bulk_wait_read_all();
-                mbar_arrive(smem_u32(&bars->epi_empty[pending]));
-                pending = -1;
-              }
-              mbar_arrive(smem_u32(&bars->epi_empty[slot]));
-            }
+          tc_fence_after();
+          const uint64_t a0 = sw128_desc(smem_u32(sA + stage * kABytes));
+          const uint64_t b0 = sw128_desc(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // advance 16 elements = 32 bytes = 2 units
+            umma_bf16<PAIR>(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc, (kb | k) != 0);
+          umma_commit<PAIR>(smem_u32(&bars->empty[stage]));
+          if (++stage == kSt) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_fence_before();
-        if constexpr (PAIR)
-          mbar_arrive_cluster(pair_addr(smem_u32(&bars->tmem_empty[acc]), 0));
-        else
-          mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
-        if (is_k && live) {
-          float* p = args.partials + (static_cast<size_t>(m_br * tpb + kc / BN) * 3) * args.N + row;
-          p[0] = s_hk;
-          p[args.N] = s_kk;
-          p[2 * static_cast<size_t>(args.N)] = s_hh;
-        }
-        if (GATE == PG_GATE_CONTEXT && !is_k && live && args.vpart)
-          args.vpart[static_cast<size_t>(n0 / BN) * args.N + row] = s_vv;
+        umma_commit<PAIR>(smem_u32(&bars->tmem_full[acc]));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) {
-        atomicOr(args.err_word, 4);
+        atomicOr(args.err_word, 2);
         *abort = 1;
       }
-      if (epi == 0) {
-        bulk_wait_all();
-        if (pending >= 0) mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+      // Every MMA this thread issued has finished before TMEM can be released.
+      umma_commit_local<PAIR>(smem_u32(&bars->mma_done));
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(smem_u32(&bars->mma_done), 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
     }
-  };
-  if constexpr (kRebalance) {
-    if (warp < 4) {
-      setmaxnreg_dec<kRegsLight>();
-      roles(std::integral_constant<int, 0>());
-    } else if (warp < 8) {
-      setmaxnreg_dec<kRegsEpi>();
-      roles(std::integral_constant<int, 1>());
-    } else {
-      setmaxnreg_inc<kRegsGather>();
-      roles(std::integral_constant<int, 2>());
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ epilogue operand producer
+    if (lane == 0) {
+      if (GATE == PG_GATE_SCALAR) tma_prefetch_map(&map_x);
+      if (GATE == PG_GATE_CONTEXT) tma_prefetch_map(&map_h);
+      uint32_t seq = 0;
+      bool ok = true;
+      uint32_t issued = 0;
+      for (int tile = unit; tile < num_tiles && ok; tile += units) {
+        const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
+        const int n0 = n_blk * BN, m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+        const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
+        if (m0 >= args.N) continue;  // this CTA's rows of the tile lie past the last token
+        for (int j = 0; j < kSub; ++j, ++seq) {
+          const int slot = static_cast<int>(seq % kEpiStages);
+          const uint32_t ph = (seq / kEpiStages) & 1u;
+          if (!mbar_wait(smem_u32(&bars->epi_empty[slot]), ph ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bars->epi_full[slot]);
+          const uint32_t dst = smem_u32(sE + slot * kEpiBytes);
+          if (GATE == PG_GATE_SCALAR) {
+            mbar_expect_tx(full, kEpiBytes);
+            tma_load_2d(dst, &map_x, full, n0 + j * kEpiCols, m0);
+            issued |= 1u << slot;
+          } else if (is_k) {
+            const int m = n0 / args.d - 1;
+            const int kc = n0 - (m + 1) * args.d;
+            mbar_expect_tx(full, kEpiBytes);
+            tma_load_2d(dst, &map_h, full, kc + j * kEpiCols, m * args.N + m0);
+            issued |= 1u << slot;
+          } else {
+            mbar_arrive(full);   // output staging only: hand the free slot over
+          }
+        }
+      }
+      if (!ok) {
+        atomicOr(args.err_word, 8);
+        *abort = 1;
+        for (int s = 0; s < kEpiStages; ++s)
+          if (issued & (1u << s)) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < kWaitLimitNs / 4 &&
+                   !mbar_try_wait(smem_u32(&bars->epi_full[s]), ((seq - 1 - ((seq - 1 - s) % kEpiStages)) / kEpiStages) & 1u)) {
+            }
+          }
+      }
+    }
+  } else if ((GATHER && warp >= kGatherWarp0) ||
+             (PRODUCE && (warp == kProdCoordWarp || warp >= kProdGatherWarp0))) {
+    if constexpr (PRODUCE) {
+      // ---------------------------------------------------------- e_t producers (warps 3, 8..15)
+      // Warps 8..15 gather units of T tokens x `items` heads = Hu <= 512 rows of 64 bf16
+      // (128 bytes), T a power of two <= 128 (a unit never spans two ready counters). Warp
+      // w takes rows [64 w, 64 w + 64) of every unit: lane l hashes rows 64 w + l + 32 j
+      // (token p / items, head p mod items), then 8 lanes per row move its 16-byte pieces,
+      // row 64 w + 4 i + (l >> 3) being lane ((4 i + (l >> 3)) mod 32)'s pair i / 8.
+      // Warp 3 coordinates through a ring of kUnitSlots slots in shared memory: unit k goes
+      // into slot k mod kUnitSlots (the claim order is the order the tiles are walked: last
+      // m-block first) and is announced on unit_full[slot]; every gather warp arrives on
+      // unit_done[slot] once its stores of the unit are issued, after which the
+      // coordinator fences, counts the unit on its ready counter and reuses the slot. The
+      // coordinator also stages each unit's canonical token IDs (and the 3 before it) in its
+      // slot, so a gather warp hashes from shared memory. The gather warps never wait for one
+      // another: each runs its own pipeline, hashing unit k while the loads of unit k - 1 are
+      // in flight. Every wait is a bounded mbarrier wait.
+      const int items = gat.P.O * gat.P.H;
+      const int T = gat.unit_tokens;
+      const uint32_t nunits = static_cast<uint32_t>((args.N + T - 1) / T);
+      if (warp == kProdCoordWarp) {
+        // lane 0 claims, waits and counts; all lanes stage the canonical IDs of each unit
+        // (the reads of a token happen once, here, ahead of the gather warps)
+        auto publish = [&](int64_t u) {
+          if (u >= 0) {
+            __threadfence();
+            red_release_gpu_add(gat.ready + u / kReadyTokens, 1u);
+          }
+        };
+        bool ok = true;
+        int K = 0;  // units handed out (slot K holds -1)
+        uint32_t pending = 0;
+        if (lane == 0) pending = atomicAdd(gat.claim, 1u);
+        for (int k = 0;; ++k) {
+          const int s = k % kUnitSlots;
+          int64_t val = -1;
+          if (lane == 0) val = (pending >= nunits || *abort) ? -1 : static_cast<int64_t>(nunits - 1 - pending) * T;
+          val = __shfl_sync(0xffffffffu, val, 0);
+          // token IDs of positions val - 3 .. val + T - 1 (issued before the slot is free)
+          constexpr int kStage = (kCanonStride + 31) / 32;
+          int32_t x[kStage];
+#pragma unroll
+          for (int q = 0; q < kStage; ++q) {
+            const int i = lane + 32 * q;
+            const int64_t f = val - 3 + i;
+            x[q] = 0;
+            if (val >= 0 && i < T + 3 && f >= 0 && f < args.N) x[q] = __ldg(gat.tokens + f);
+          }
+          if (k >= kUnitSlots) {
+            // unit k - kUnitSlots: stored by every gather warp, then counted; its slot is free
+            bool waited = true;
+            if (lane == 0) {
+              waited = mbar_wait(smem_u32(&bars->unit_done[s]),
+                                                    static_cast<uint32_t>((k / kUnitSlots - 1) & 1), abort);
+              if (waited) publish(s_unit[s]);
+            }
+            if (!__shfl_sync(0xffffffffu, waited, 0)) {
+              ok = false;
+              break;
+            }
+          }
+          // canonical IDs (an out-of-range ID reads as 0 and is reported by its own unit)
+#pragma unroll
+          for (int q = 0; q < kStage; ++q) {
+            const int i = lane + 32 * q;
+            const int64_t f = val - 3 + i;
+            if (val >= 0 && i < T + 3 && f >= 0 && f < args.N) {
+              int32_t id = x[q];
+              if (id < 0 || static_cast<uint32_t>(id) >= gat.P.vocab) {
+                if (i >= 3 && gat.err) atomicMin(reinterpret_cast<unsigned int*>(gat.err), static_cast<unsigned int>(f));
+                id = 0;
+              }
+              s_canon[s * kCanonStride + i] = gat.canon_map ? __ldg(gat.canon_map + id) : static_cast<uint32_t>(id);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            s_unit[s] = val;
+            mbar_arrive(smem_u32(&bars->unit_full[s]));
+            if (val >= 0) pending = atomicAdd(gat.claim, 1u);  // needed one unit later
+          }
+          if (val < 0) {
+            K = k;
+            break;
+          }
+        }
+        if (lane == 0) {
+          for (int j = K - kUnitSlots + 1 < 0 ? 0 : K - kUnitSlots + 1; ok && j < K; ++j) {
+            const int s = j % kUnitSlots;
+            if (!mbar_wait(smem_u32(&bars->unit_done[s]),
+                                              static_cast<uint32_t>((j / kUnitSlots) & 1), abort)) {
+              ok = false;
+              break;
+            }
+            publish(s_unit[s]);
+          }
+          if (!ok) {
+            atomicOr(args.err_word, 128);
+            *abort = 1;
+          }
+        }
+        __syncwarp();
+      } else {
+        constexpr int kPairs = 2, kLoads = 16;      // 64 rows of this warp per unit
+        const int gw = warp - kProdGatherWarp0;
+        const int Hu = T * items;
+        const uint32_t out_row = static_cast<uint32_t>(items) * 128u;
+        const int piece = lane & 7, sub = lane >> 3;
+        uint32_t r[kPairs], off[kPairs];            // unit being hashed and loaded
+        uint64_t sw[kPairs];
+        uint32_t offp[kPairs];                      // previous unit (loaded, to be stored)
+        uint64_t swp[kPairs];
+        int64_t prev = -1;
+        int kprev = 0;
+        uint4 vb[kLoads];
+        auto hash = [&](int64_t tok0, const uint32_t* cs) {
+#pragma unroll
+          for (int j = 0; j < kPairs; ++j) {
+            const int p = 64 * gw + lane + 32 * j;
+            const int s = p / items;
+            r[j] = 0;
+            sw[j] = 0;
+            off[j] = 0xFFFFFFFFu;  // no row
+            if (p < Hu && tok0 + s < args.N) {
+              const int it = p - s * items;
+              const int64_t tok = tok0 + s;
+              const uint32_t t = fastmod(static_cast<uint32_t>(tok), gat.fm_L, gat.L);
+              const uint32_t* ids = cs + 3 + s;  // ids[-j]: position tok - j
+              uint64_t c[4], hs;
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj)
+                c[jj] = (jj < s_ic[it].n && t >= static_cast<uint32_t>(jj)) ? ids[-jj] : kPad;
+              r[j] = item_row_ids(s_ic[it], gat.P.mode, c, &hs);
+              sw[j] = mix64(hs + kGolden);
+              off[j] = static_cast<uint32_t>(s) * out_row + static_cast<uint32_t>(it) * 128u;
+            }
+          }
+        };
+        auto issue_loads = [&]() {
+#pragma unroll
+          for (int i = 0; i < kLoads; ++i) {
+            const int src = (4 * i + sub) & 31;
+            const uint32_t row = __shfl_sync(0xffffffffu, r[i / 8], src);
+            const uint32_t o = __shfl_sync(0xffffffffu, off[i / 8], src);
+            vb[i] = make_uint4(0, 0, 0, 0);
+            if (o != 0xFFFFFFFFu) vb[i] = ldg_stream(gat.table + static_cast<uint64_t>(row) * 128u + piece * 16);
+          }
+        };
+        // sign-flip and store the previous unit, then report it to the coordinator
+        auto store_prev = [&]() {
+          if (prev < 0) return;
+          uint8_t* out = gat.e_out + static_cast<uint64_t>(prev) * out_row + piece * 16;
+#pragma unroll
+          for (int q = 0; q < kLoads; ++q) {
+            const int src = (4 * q + sub) & 31;
+            const uint64_t w = __shfl_sync(0xffffffffu, swp[q / 8], src);
+            const uint32_t o = __shfl_sync(0xffffffffu, offp[q / 8], src);
+            const uint32_t bits = static_cast<uint32_t>(w >> (8 * piece)) & 0xFFu;
+            if (o != 0xFFFFFFFFu) *reinterpret_cast<uint4*>(out + o) = xor4(vb[q], bf16_sign_mask(bits));
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->unit_done[kprev % kUnitSlots]));
+        };
+        // unit k: hashed under the previous unit's loads, then the previous unit is stored
+        // and unit k's loads are issued
+        bool ok = true;
+        for (int k = 0;; ++k) {
+          const int s = k % kUnitSlots;
+          if (!mbar_wait(smem_u32(&bars->unit_full[s]), static_cast<uint32_t>((k / kUnitSlots) & 1), abort)) {
+            ok = false;
+            break;
+          }
+          const int64_t u = s_unit[s];
+          if (u < 0) break;
+          hash(u, s_canon + s * kCanonStride);
+          store_prev();
+          issue_loads();
+          prev = u;
+          kprev = k;
+#pragma unroll
+          for (int j = 0; j < kPairs; ++j) {
+            offp[j] = off[j];
+            swp[j] = sw[j];
+          }
+        }
+        if (ok) {
+          store_prev();  // the last unit
+        } else {
+          atomicOr(args.err_word, 128);
+          *abort = 1;
+        }
+      }
+    } else if constexpr (GATHER) {
+      // ---------------------------------------------------------- A-operand gather (warps 7..14)
+      // Pair p of warps builds every A tile of ring stage p; warp `half` of the pair covers
+      // tokens [64 half, 64 half + 64) of the 128-token block. Lane l hashes tokens l and
+      // l + 32 of its half for head kb, then 8 lanes per row move 16-byte chunks: chunk
+      // (token, piece) -> A-tile row `token`, physical chunk piece ^ (row & 7) (128-byte
+      // swizzle, the layout the TMA would have written).
+      const int gw = warp - kGatherWarp0;
+      const int pair = gw >> 1, half = gw & 1;
+      const int piece = lane & 7, sub = lane >> 3;
+      const int stage = pair;
+      // rows and sign words of tokens (64 half + lane) and (+32) of one k-block
+      auto hash_rows = [&](int tile, int kb, uint32_t& ra, uint32_t& rb, uint64_t& sa, uint64_t& sb) {
+        const int m0 = ((num_tiles - 1 - tile) / num_n) * kBM;
+        const ItemConst& it = s_ic[kb];
+        const int64_t ta = static_cast<int64_t>(m0) + 64 * half + lane, tb = ta + 32;
+        uint64_t hs;
+        ra = rb = 0;
+        sa = sb = 0;
+        if (ta < args.N) {
+          ra = item_row(it, gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, ta,
+                        fastmod(static_cast<uint32_t>(ta), gat.fm_L, gat.L), gat.err, &hs);
+          sa = mix64(hs + kGolden);
+        }
+        if (tb < args.N) {
+          rb = item_row(it, gat.P.mode, gat.tokens, gat.canon_map, gat.P.vocab, tb,
+                        fastmod(static_cast<uint32_t>(tb), gat.fm_L, gat.L), gat.err, &hs);
+          sb = mix64(hs + kGolden);
+        }
+      };
+      // this pair's k-blocks: sequence numbers q = pair, pair + 4, ... over the CTA's tiles
+      int tile = blockIdx.x, kb = pair;
+      while (kb >= num_kb && tile < num_tiles) {
+        kb -= num_kb;
+        tile += gridDim.x;
+      }
+      uint32_t q = pair;
+      uint32_t ra, rb;
+      uint64_t sa, sb;
+      if (tile < num_tiles) hash_rows(tile, kb, ra, rb, sa, sb);
+      bool ok = true;
+      while (tile < num_tiles) {
+        // 1. loads of this k-block (they do not need the stage to be free)
+        uint4 v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int src = 4 * (i & 7) + sub;
+          const uint32_t r = __shfl_sync(0xffffffffu, i < 8 ? ra : rb, src);
+          v[i] = __ldg(reinterpret_cast<const uint4*>(gat.table + static_cast<uint64_t>(r) * 128u + piece * 16));
+        }
+        // 2. hash the next k-block of this pair while the loads are in flight
+        int ntile = tile, nkb = kb + 4;
+        while (nkb >= num_kb && ntile < num_tiles) {
+          nkb -= num_kb;
+          ntile += gridDim.x;
+        }
+        uint32_t na = 0, nb = 0;
+        uint64_t nsa = 0, nsb = 0;
+        if (ntile < num_tiles) hash_rows(ntile, nkb, na, nb, nsa, nsb);
+        // 3. wait for the stage, then sign-flip and store into the swizzled A tile
+        if (!mbar_wait(smem_u32(&bars->empty[stage]), ((q >> 2) & 1u) ^ 1u, abort)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_tile = sA + stage * kABytes;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int src = 4 * (i & 7) + sub;
+          const uint64_t sw = __shfl_sync(0xffffffffu, i < 8 ? sa : sb, src);
+          const uint32_t bits = static_cast<uint32_t>(sw >> (8 * piece)) & 0xFFu;
+          const int row = 64 * half + (i < 8 ? 0 : 32) + src;
+          *reinterpret_cast<uint4*>(a_tile + row * 128 + ((piece ^ (row & 7)) << 4)) = xor4(v[i], bf16_sign_mask(bits));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bars->full[stage]));
+        tile = ntile;
+        kb = nkb;
+        q += 4;
+        ra = na;
+        rb = nb;
+        sa = nsa;
+        sb = nsb;
+      }
+      if (!ok) {
+        atomicOr(args.err_word, 16);
+        *abort = 1;
+      }
     }
   } else {
-    roles(std::integral_constant<int, -1>());
+    // ------------------------------------------------------------ epilogue (warps 3..6; 4..7 when PRODUCE)
+    const int epi = threadIdx.x - 32 * (PRODUCE ? kProdEpiWarp0 : 3);
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t seq = 0;
+    bool ok = true;
+    int pending = -1;             // slot whose TMA store may still be reading (thread epi == 0)
+    const int tpb = args.d / BN;  // tiles per branch (context gate)
+    for (int tile = unit; tile < num_tiles && ok; tile += units) {
+      const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
+      if (!mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+      const bool rows_here = m0 < args.N;  // (the operand producer skips the same tiles)
+      const int row = m0 + row_in_tile;
+      const bool live = row < args.N;
+      const int n0 = n_blk * BN;
+      const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
+      const int m_br = is_k ? n0 / args.d - 1 : 0;
+      const int kc = is_k ? n0 - (m_br + 1) * args.d : 0;
+      const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
+      float s_vv = 0.f;  // context gate, v tiles: sum of the stored (bf16) v^2 of the row
+      for (int j = 0; rows_here && j < kSub; ++j, ++seq) {
+        const int slot = static_cast<int>(seq % kEpiStages);
+        const uint32_t ph = (seq / kEpiStages) & 1u;
+        if (!mbar_wait(smem_u32(&bars->epi_full[slot]), ph, abort)) {
+          ok = false;
+          break;
+        }
+        uint32_t r[32];
+        tmem_ld32(t_base + static_cast<uint32_t>(j * kEpiCols), r);
+        tmem_ld_wait();
+        uint8_t* slot_p = sE + slot * kEpiBytes;
+        if (is_k) {
+          const float4* gh = reinterpret_cast<const float4*>(args.gamma_h + kc + j * kEpiCols);
+          const float4* gk = reinterpret_cast<const float4*>(args.gamma_k + kc + j * kEpiCols);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float hf[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_p + epi_offset(row_in_tile, c)), hf);
+            const float4 gh0 = __ldg(gh + 2 * c), gh1 = __ldg(gh + 2 * c + 1);
+            const float4 gk0 = __ldg(gk + 2 * c), gk1 = __ldg(gk + 2 * c + 1);
+            const float ghv[8] = {gh0.x, gh0.y, gh0.z, gh0.w, gh1.x, gh1.y, gh1.z, gh1.w};
+            const float gkv[8] = {gk0.x, gk0.y, gk0.z, gk0.w, gk1.x, gk1.y, gk1.z, gk1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float kv = __uint_as_float(r[8 * c + i]);
+              s_kk = fmaf(kv, kv, s_kk);
+              s_hh = fmaf(hf[i], hf[i], s_hh);
+              s_hk = fmaf(ghv[i] * gkv[i] * hf[i], kv, s_hk);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4* p = reinterpret_cast<uint4*>(slot_p + epi_offset(row_in_tile, c));
+            float o[8];
+            if (GATE == PG_GATE_SCALAR) {
+              float xf[8];
+              unpack_bf16x8(*p, xf);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] = fmaf(args.g, __uint_as_float(r[8 * c + i]), xf[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] = __uint_as_float(r[8 * c + i]);
+            }
+            const uint4 packed = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+                                            pack_bf16(o[6], o[7]));
+            *p = packed;
+            if (GATE == PG_GATE_CONTEXT) {
+              float q[8];
+              unpack_bf16x8(packed, q);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) s_vv = fmaf(q[i], q[i], s_vv);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(smem_u32(&bars->epi_done[slot]));
+        if (epi == 0) {
+          // the slot goes back to the producer once every thread is done with it and,
+          // for outputs, once its TMA store has read it
+          if (!mbar_wait(smem_u32(&bars->epi_done[slot]), ph, abort)) {
+            ok = false;
+            break;
+          }
+          if (!is_k) {
+            tma_store_2d(&map_v, smem_u32(slot_p), n0 + j * kEpiCols, m0);
+            bulk_commit();
+            if (pending >= 0) {   // one store stays in flight; the one before it is done reading
+              bulk_wait_read_all_but_one();
+              mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+            }
+            pending = slot;
+          } else {
+            if (pending >= 0) {
+              bulk_wait_read_all();
+              mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+              pending = -1;
+            }
+            mbar_arrive(smem_u32(&bars->epi_empty[slot]));
+          }
+        }
+      }
+      if (!ok) break;
+      tc_fence_before();
+      if constexpr (PAIR)
+        mbar_arrive_cluster(pair_addr(smem_u32(&bars->tmem_empty[acc]), 0));
+      else
+        mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
+      if (is_k && live) {
+        float* p = args.partials + (static_cast<size_t>(m_br * tpb + kc / BN) * 3) * args.N + row;
+        p[0] = s_hk;
+        p[args.N] = s_kk;
+        p[2 * static_cast<size_t>(args.N)] = s_hh;
+      }
+      if (GATE == PG_GATE_CONTEXT && !is_k && live && args.vpart)
+        args.vpart[static_cast<size_t>(n0 / BN) * args.N + row] = s_vv;
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      atomicOr(args.err_word, 4);
+      *abort = 1;
+    }
+    if (epi == 0) {
+      bulk_wait_all();
+      if (pending >= 0) mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+    }
   }
 
   tc_fence_before();
