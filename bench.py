@@ -531,30 +531,40 @@ def run_gpu(args):
 
 
 # ncu-measured DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum),
-# keyed by (workload, stage), with the sha256 prefix of the kernel's source file at the
-# time of the capture; reported only while the source is unchanged (profiles/ holds the
-# captures).
+# keyed by (workload, stage), with the sha256 prefix of the kernel's source file followed by
+# the csrc headers (sorted) at the time of the capture; reported only while those sources
+# are unchanged (profiles/ holds the captures).
 TRAFFIC = {
-    (2, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 180.541696e6),
-    (2, "project_gate"): ("pg_project.cu", "429cd1a9337dc7c2", 307.035648e6),
-    (2, "lookup_project_gate"): ("pg_project.cu", "429cd1a9337dc7c2", 274.157824e6),
-    (4, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 190.3e6),
-    (5, "gather_sign_concat"): ("pg_lookup.cu", "10379219b6ed0490", 142.978816e6),
-    (5, "project_gate"): ("pg_project.cu", "429cd1a9337dc7c2", 1065.460992e6),
-    (5, "conv_residual"): ("pg_conv.cu", "597024b7d69714ca", 1466.725888e6),
+    (2, "gather_project_gate"): ("pg_project.cu", "87d912a3653aceaa", 403.794660e6),
+    (2, "gather_sign_concat"): ("pg_lookup.cu", "6f9eea0ec1cf08c5", 180.501931e6),
+    (2, "project_gate"): ("pg_project.cu", "87d912a3653aceaa", 307.011328e6),
+    (2, "lookup_project_gate"): ("pg_project.cu", "87d912a3653aceaa", 274.358613e6),
+    (4, "gather_sign_concat"): ("pg_lookup.cu", "6f9eea0ec1cf08c5", 190.712804e6),
+    (5, "gather_sign_concat"): ("pg_lookup.cu", "6f9eea0ec1cf08c5", 143.373369e6),
+    (5, "project_gate"): ("pg_project.cu", "87d912a3653aceaa", 1071.450283e6),
+    (5, "conv_residual"): ("pg_conv.cu", "e876b26425dfd800", 1463.958414e6),
 }
 
 
-def traffic_of(cfg, stage):
+def source_sha(src):
+    """sha256 prefix of csrc/<src> followed by every csrc header, sorted by name."""
+    import glob
     import hashlib
+    csrc = os.path.join(ROOT, "hashed_head_gram_gb300", "csrc")
+    h = hashlib.sha256()
+    for path in [os.path.join(csrc, src)] + sorted(glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(cfg, stage):
     entry = TRAFFIC.get((cfg, stage))
     if entry is None:
         return None
     src, sha, nbytes = entry
-    path = os.path.join(ROOT, "hashed_head_gram_gb300", "csrc", src)
     try:
-        with open(path, "rb") as f:
-            now = hashlib.sha256(f.read()).hexdigest()[:16]
+        now = source_sha(src)
     except OSError:
         return None
     return nbytes if now == sha else None

@@ -1,6 +1,6 @@
 """Single-kernel runs on a workload's shapes, for timing and profiling one kernel at a time.
 
-    python -m hashed_head_gram_gb300.kernel_cases {gather,project,conv} --config C [--iters N]
+    python -m hashed_head_gram_gb300.kernel_cases {gather,project,gather_project,conv} --config C [--iters N]
 
 Inputs are synthetic and seeded (the conv and projection cases need no table, so they
 hold at most a few GB on the device); each launch goes through the C ABI exactly as the
@@ -20,7 +20,7 @@ from . import workloads as W
 
 def _flush(buf):
     buf.add_(1)
-    buf.sum(dtype=buf.dtype)
+    buf.sum(dtype=buf.dtype)  # read back: the written lines leave L2 here, not in the next launch
 
 
 def _time(fn, iters: int, dev) -> float:
@@ -42,7 +42,7 @@ def _time(fn, iters: int, dev) -> float:
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["gather", "project", "conv"])
+    ap.add_argument("kernel", choices=["gather", "project", "gather_project", "conv"])
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--iters", type=int, default=20)
     args = ap.parse_args(argv)
@@ -64,6 +64,24 @@ def main(argv=None):
         rb = spec.row_bytes if spec.row_dtype != W.DT_NF4 else 64
         byts = N * (len(spec.orders) * spec.K * rb + 4 + din * e.element_size())
         print(f"gather_sign_concat config {w.cfg_id}: {us:.1f} us, {byts / us / 1e3:.0f} GB/s (algorithmic)")
+    elif args.kernel == "gather_project":
+        # lookup + scalar-gated projection in one launch (pg_gather_project_gate)
+        if w.gate != W.GATE_SCALAR:
+            raise SystemExit("the one-launch case runs the scalar-gated workloads (configs 2, 3)")
+        desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+        tokens = torch.from_numpy(W.make_tokens(w)).to(dev)
+        cm = W.make_canon_map(w)
+        cm = None if cm is None else torch.from_numpy(cm.view("int32")).to(dev)
+        table = W.make_table(w, spec, dev)
+        e = torch.empty(N, din, dtype=dt, device=dev)
+        Wm = (torch.randn(d, din, device=dev, generator=g) * 0.02).to(dt)
+        x = torch.randn(N, d, device=dev, generator=g).to(dt)
+        v = torch.empty(N, d, dtype=dt, device=dev)
+        ws = torch.empty(pg.gather_project_workspace_size(N, d, 0, pg.GATE_SCALAR) // 4 + 1, device=dev)
+        us = _time(lambda: pg.gather_project_gate(desc, tokens, table, e, Wm, d, pg.GATE_SCALAR, v, ws, canon_map=cm,
+                                                  g=w.g, x_resid=x), args.iters, dev)
+        print(f"gather_project_gate config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * d / us / 1e6:.1f} TFLOP/s, "
+              f"{N / us:.1f} M tokens/s")
     elif args.kernel == "project":
         e = (torch.randint(-128, 128, (N, din), device=dev, generator=g).float() / 64).to(dt)
         Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(dt)

@@ -128,8 +128,11 @@ uint64_t pg_launch_count(void);
 
 /*
  * Device-side error word of the current device: 0, or the OR of codes of bounded
- * waits that gave up (1 = TMA producer, 2 = MMA issuer, 4 = epilogue). Synchronizes
- * the device. With clear != 0 the word is reset to 0.
+ * waits that gave up in the projection kernels (1 = TMA producer, 2 = MMA issuer,
+ * 4 = epilogue, 8 = epilogue operand producer, 16 = gather warps of
+ * pg_lookup_project_gate, 64 = a tile's wait for its rows of e_t in
+ * pg_gather_project_gate, 128 = that call's gather warps or their coordinator).
+ * Synchronizes the device. With clear != 0 the word is reset to 0.
  */
 pg_status pg_device_error(int32_t* code, int32_t clear);
 
