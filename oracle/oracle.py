@@ -76,6 +76,8 @@ def lib():
         L.orc_f16_to_f32.restype = ctypes.c_float; L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
         L.orc_f32_to_bf16.restype = ctypes.c_uint16; L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
         L.orc_bf16_to_f32.restype = ctypes.c_float; L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        L.orc_f32_to_f16_sat.restype = ctypes.c_uint16; L.orc_f32_to_f16_sat.argtypes = [ctypes.c_float]
+        L.orc_nf4_quantize.restype = None; L.orc_nf4_quantize.argtypes = [vp, i64, vp]
         L.orc_total_rows.restype = u64; L.orc_total_rows.argtypes = [ctypes.POINTER(OrcDesc)]
         L.orc_sign_words.restype = ctypes.c_int; L.orc_sign_words.argtypes = [ctypes.POINTER(OrcDesc)]
         L.orc_heads.restype = ctypes.c_int; L.orc_heads.argtypes = [ctypes.POINTER(OrcDesc)]
@@ -211,3 +213,30 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 def nf4_levels() -> np.ndarray:
     return np.array([lib().orc_nf4_level(c) for c in range(16)], np.float32)
+
+
+def f32_to_f16_sat(x: float) -> int:
+    """fp16 bits of x: round to nearest, ties to even, saturating at +-65504 (R13)."""
+    return int(lib().orc_f32_to_f16_sat(float(x)))
+
+
+def nf4_quantize(x: np.ndarray) -> np.ndarray:
+    """NF4 export (PageGram report 3.3; QLoRA's absmax quantisation, reading R13):
+    x [n, 64] fp32 -> [n, 34] uint8 rows in the R6 layout."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.ndim == 2 and x.shape[1] == 64
+    out = np.zeros((x.shape[0], 34), np.uint8)
+    lib().orc_nf4_quantize(x.ctypes.data, x.shape[0], out.ctypes.data)
+    return out
+
+
+def nf4_dequantize(rows: np.ndarray) -> np.ndarray:
+    """[n, 34] NF4 rows -> [n, 64] fp32 values level[code] * float(scale) (R6)."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint8)
+    lv = nf4_levels()
+    codes = np.empty((rows.shape[0], 64), np.int64)
+    codes[:, 0::2] = rows[:, :32] & 15
+    codes[:, 1::2] = rows[:, :32] >> 4
+    sbits = rows[:, 32].astype(np.uint16) | (rows[:, 33].astype(np.uint16) << 8)
+    scale = np.array([lib().orc_f16_to_f32(int(b)) for b in sbits], np.float32)
+    return (lv[codes] * scale[:, None]).astype(np.float32)

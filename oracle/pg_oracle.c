@@ -45,6 +45,11 @@
  *      level[code] * float(scale) in fp32, then round-to-nearest-even to bf16.
  *  R7  flat mode sums in fp32 in order of increasing n, starting from the first
  *      signed row (acc = s_0*T_0[..]; acc = acc + s_1*T_1[..]).
+ *  R13 NF4 export (QLoRA's absmax quantisation of a 64-wide row): a = max |x_i|;
+ *      scale = a rounded to fp16 (nearest, ties to even; a value that would round
+ *      past 65504 saturates to 65504); s = float(scale). s = 0: every code is the
+ *      exact-zero level (index 7). Otherwise y_i = x_i / s (fp32, correctly rounded)
+ *      and code_i = the k minimising |y_i - level[k]| in fp32, the lowest k on ties.
  *  Toy: flat bigram only, row = (3a + b) mod m on canonical IDs, no row at t=0.
  */
 #include <stdint.h>
@@ -98,6 +103,32 @@ float orc_f16_to_f32(uint16_t h) {
   }
   if (e == 31) return bits_to_f32(sign | 0x7F800000u | (m << 13));
   return bits_to_f32(sign | ((e + 112u) << 23) | (m << 13));
+}
+
+/* binary32 -> binary16, round to nearest, ties to even, from the format definition;
+ * finite values that would round past 65504 (and infinities) saturate to +-65504,
+ * NaN stays NaN. */
+uint16_t orc_f32_to_f16_sat(float f) {
+  const uint32_t u = f32_to_bits(f);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  const uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);
+  if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7BFFu);  /* >= 65520 would round to inf */
+  const uint32_t e = a >> 23;
+  if (e < 113u) {
+    /* below 2^-14: a binary16 subnormal k * 2^-24, k = round(mantissa * 2^(e-126)) */
+    const int sh = 126 - (int)e;
+    if (sh > 24) return sign;
+    const uint32_t mant = (a & 0x7FFFFFu) | 0x800000u;
+    uint32_t k = mant >> sh;
+    const uint32_t rem = mant & ((1u << sh) - 1u), half = 1u << (sh - 1);
+    if (rem > half || (rem == half && (k & 1u))) k += 1u;  /* k = 0x400: smallest normal */
+    return (uint16_t)(sign | k);
+  }
+  uint32_t h = (a >> 13) - ((127u - 15u) << 10);
+  const uint32_t rem = a & 0x1FFFu;
+  if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;
+  return (uint16_t)(sign | h);
 }
 
 /* binary32 -> bfloat16, round to nearest, ties to even (NaN stays NaN). */
@@ -319,4 +350,42 @@ int orc_assemble(const orc_desc* d, int64_t n, const uint32_t* rows, const uint8
     }
   }
   return 0;
+}
+
+/* NF4 export of n rows of 64 fp32 values into 34-byte rows (R6 layout, R13 rule). */
+void orc_nf4_quantize(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t row = 0; row < n; ++row) {
+    const float* xr = x + row * 64;
+    uint8_t* o = out + row * 34;
+    float a = 0.0f;
+    for (int i = 0; i < 64; ++i) {
+      const float v = xr[i] < 0.0f ? -xr[i] : xr[i];
+      if (v > a) a = v;
+    }
+    const uint16_t sbits = orc_f32_to_f16_sat(a);
+    const float s = orc_f16_to_f32(sbits);
+    int code[64];
+    for (int i = 0; i < 64; ++i) {
+      if (s == 0.0f) {
+        code[i] = 7;
+        continue;
+      }
+      const float y = xr[i] / s;
+      int best = 0;
+      float dbest = y - orc_nf4_level(0);
+      if (dbest < 0.0f) dbest = -dbest;
+      for (int k = 1; k < 16; ++k) {
+        float dk = y - orc_nf4_level(k);
+        if (dk < 0.0f) dk = -dk;
+        if (dk < dbest) {
+          dbest = dk;
+          best = k;
+        }
+      }
+      code[i] = best;
+    }
+    for (int i = 0; i < 32; ++i) o[i] = (uint8_t)(code[2 * i] | (code[2 * i + 1] << 4));
+    o[32] = (uint8_t)(sbits & 0xFFu);
+    o[33] = (uint8_t)(sbits >> 8);
+  }
 }
