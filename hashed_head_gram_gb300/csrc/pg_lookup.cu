@@ -470,6 +470,58 @@ pg_status prepare_err(int32_t* err_index, cudaStream_t stream) {
   return e == cudaSuccess ? PG_OK : cuda_fail(e);
 }
 
+// ------------------------------------------------------------------ NF4 export
+
+// NF4 export of 64-wide fp32 head rows into the 34-byte stored rows (PageGram report 3.3:
+// 64 four-bit codes + one fp16 scale; QLoRA's absmax rule). One warp per row, lane l owns
+// elements 2l and 2l+1 and writes byte l; lane 0 writes the scale. Scale = max |x| rounded
+// to fp16 (nearest even), saturating at 65504; codes = the nearest level of x / scale
+// (correctly rounded fp32 division, fp32 distances, the lowest code on ties); a zero scale
+// gives the exact-zero level everywhere.
+__global__ void __launch_bounds__(256) nf4_quantize_kernel(const float* __restrict__ x, int64_t n,
+                                                           uint8_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  float lv[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) lv[k] = __uint_as_float(c_nf4_bits[k]);
+  auto nearest = [&](float y) {
+    int best = 0;
+    float dbest = fabsf(y - lv[0]);
+#pragma unroll
+    for (int k = 1; k < 16; ++k) {
+      const float dk = fabsf(y - lv[k]);
+      if (dk < dbest) {
+        dbest = dk;
+        best = k;
+      }
+    }
+    return best;
+  };
+  for (int64_t row = first; row < n; row += nwarps) {
+    const float2 v = __ldg(reinterpret_cast<const float2*>(x + row * 64) + lane);
+    float a = fmaxf(0.0f, fmaxf(fabsf(v.x), fabsf(v.y)));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    __half h = __float2half_rn(a);
+    if (__hisinf(h)) h = __ushort_as_half(static_cast<unsigned short>(0x7BFFu));
+    const float s = __half2float(h);
+    int c0 = 7, c1 = 7;
+    if (s != 0.0f) {
+      c0 = nearest(__fdiv_rn(v.x, s));
+      c1 = nearest(__fdiv_rn(v.y, s));
+    }
+    uint8_t* o = out + row * 34;
+    o[lane] = static_cast<uint8_t>(c0 | (c1 << 4));
+    if (lane == 0) {
+      const unsigned short sb = __half_as_ushort(h);
+      o[32] = static_cast<uint8_t>(sb & 0xFFu);
+      o[33] = static_cast<uint8_t>(sb >> 8);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace pg
 
@@ -569,6 +621,24 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   fn<<<blocks, kThreads, dyn, stream>>>(P, desc->hash_seed, g, tokens, canon_map,
                                         static_cast<const uint8_t*>(table), static_cast<uint8_t*>(e_out),
                                         err_index);
+  return after_launch(1);
+}
+
+
+pg_status pg_nf4_quantize(const float* x, int64_t nrows, int32_t r, void* out, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (nrows < 0) return PG_ERR_SHAPE;
+  if (r != 64) return PG_ERR_UNSUPPORTED;
+  if (nrows == 0) return PG_OK;
+  if (!x || !out) return PG_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(x) % 8) return PG_ERR_ALIGN;
+  const int nsm = sm_count();
+  if (nsm == 0) return cuda_fail(cudaGetLastError());
+  const int64_t want = (nrows + 7) / 8;  // 8 rows (warps) per block
+  const int64_t cap = static_cast<int64_t>(nsm) * 8;
+  const int blocks = static_cast<int>(want < cap ? want : cap);
+  nf4_quantize_kernel<<<blocks, 256, 0, stream>>>(x, nrows, static_cast<uint8_t*>(out));
   return after_launch(1);
 }
 

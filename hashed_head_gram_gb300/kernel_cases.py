@@ -1,6 +1,6 @@
 """Single-kernel runs on a workload's shapes, for timing and profiling one kernel at a time.
 
-    python -m hashed_head_gram_gb300.kernel_cases {gather,project,gather_project,conv} --config C [--iters N]
+    python -m hashed_head_gram_gb300.kernel_cases {gather,project,gather_project,conv,nf4_export} --config C [--iters N]
 
 Inputs are synthetic and seeded (the conv and projection cases need no table, so they
 hold at most a few GB on the device); each launch goes through the C ABI exactly as the
@@ -42,7 +42,8 @@ def _time(fn, iters: int, dev) -> float:
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["gather", "project", "gather_project", "conv"])
+    ap.add_argument("kernel", choices=["gather", "project", "gather_project", "conv", "nf4_export"])
+    ap.add_argument("--rows", type=int, default=8 << 20, help="nf4_export: fp32 head rows to export")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--iters", type=int, default=20)
     args = ap.parse_args(argv)
@@ -64,6 +65,13 @@ def main(argv=None):
         rb = spec.row_bytes if spec.row_dtype != W.DT_NF4 else 64
         byts = N * (len(spec.orders) * spec.K * rb + 4 + din * e.element_size())
         print(f"gather_sign_concat config {w.cfg_id}: {us:.1f} us, {byts / us / 1e3:.0f} GB/s (algorithmic)")
+    elif args.kernel == "nf4_export":
+        # NF4 export of fp32 head rows (64 wide) into 34-byte rows (pg_nf4_quantize)
+        x = torch.randn(args.rows, 64, device=dev, generator=g)
+        out = torch.empty(args.rows, 34, dtype=torch.uint8, device=dev)
+        us = _time(lambda: pg.nf4_quantize(x, out), args.iters, dev)
+        byts = args.rows * (64 * 4 + 34)
+        print(f"nf4_quantize {args.rows} rows: {us:.1f} us, {byts / us / 1e3:.0f} GB/s, {args.rows / us:.1f} M rows/s")
     elif args.kernel == "gather_project":
         # lookup + scalar-gated projection in one launch (pg_gather_project_gate)
         if w.gate != W.GATE_SCALAR:

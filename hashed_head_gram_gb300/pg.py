@@ -92,6 +92,8 @@ def _load():
                                          vp, f32, vp, vp, vp, vp, sz, vp, vp]
     L.pg_gather_project_gate_workspace_size.restype = ctypes.c_int
     L.pg_gather_project_gate_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
+    L.pg_nf4_quantize.restype = ctypes.c_int
+    L.pg_nf4_quantize.argtypes = [vp, ctypes.c_int64, i32, vp, vp]
     L.pg_project_gate_context_noalloc.restype = ctypes.c_int
     L.pg_project_gate_context_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp, vp, vp]
     L.pg_conv_residual.restype = ctypes.c_int
@@ -243,6 +245,12 @@ def gather_project_gate(desc: TableDesc, tokens: torch.Tensor, table: torch.Tens
            "pg_gather_project_gate")
 
 
+def nf4_quantize(x: torch.Tensor, out: torch.Tensor, stream=None):
+    """NF4 export: x fp32 [n, 64] -> out uint8 [n, 34] (the PG_NF4 row layout)."""
+    n, r = x.shape
+    _check(_lib.pg_nf4_quantize(_ptr(x), n, r, _ptr(out), _stream(stream)), "pg_nf4_quantize")
+
+
 def project_gate_context_noalloc(e: torch.Tensor, W: torch.Tensor, d: int, M: int, h: torch.Tensor,
                                  gamma_h: torch.Tensor, gamma_k: torch.Tensor, v_out: torch.Tensor,
                                  alpha_out: torch.Tensor, eps: float = 1e-6, stream=None):
@@ -280,6 +288,6 @@ def dtype_code(t: torch.dtype) -> int:
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
-           "gather_project_gate", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
+           "gather_project_gate", "nf4_quantize", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

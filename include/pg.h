@@ -183,6 +183,22 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
                                 int32_t* err_index, pg_stream_t stream);
 
 /*
+ * pg_nf4_quantize -- NF4 export of head rows (PageGram report 3.3: deployed rows are 64
+ * four-bit NormalFloat codes + one fp16 scale = 34 bytes; report 9.4, check 5: all-zero
+ * rows stay exact and the error stays within the quantisation bound). Produces tables in
+ * the PG_NF4 row layout that pg_gather_sign_concat reads.
+ *  x      device fp32 [nrows, r], 8-byte aligned; r must be 64 (else PG_ERR_UNSUPPORTED)
+ *  out    device [nrows, 34] bytes, any alignment (PG_NF4 layout: byte i = code of element
+ *         2i | code of element 2i+1 << 4; bytes 32..33 the fp16 scale, little-endian)
+ * Per row: scale = max |x_i| rounded to fp16 (nearest, ties to even; values that would
+ * round past 65504 saturate to 65504); scale 0 gives the exact-zero level (code 7) for
+ * every element; otherwise code_i = the NF4 level nearest to x_i / scale (fp32, correctly
+ * rounded division, fp32 distances, the lowest code on ties). NaN elements do not count
+ * towards the scale and get code 0. nrows == 0 enqueues nothing.
+ */
+pg_status pg_nf4_quantize(const float* x, int64_t nrows, int32_t r, void* out, pg_stream_t stream);
+
+/*
  * Workspace bytes pg_project_gate needs for these arguments (0 when none).
  */
 pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int32_t M,

@@ -216,12 +216,12 @@ def nf4_levels() -> np.ndarray:
 
 
 def f32_to_f16_sat(x: float) -> int:
-    """fp16 bits of x: round to nearest, ties to even, saturating at +-65504 (R13)."""
+    """fp16 bits of x: round to nearest, ties to even, saturating at +-65504 (R15)."""
     return int(lib().orc_f32_to_f16_sat(float(x)))
 
 
 def nf4_quantize(x: np.ndarray) -> np.ndarray:
-    """NF4 export (PageGram report 3.3; QLoRA's absmax quantisation, reading R13):
+    """NF4 export (PageGram report 3.3; QLoRA's absmax quantisation, reading R15):
     x [n, 64] fp32 -> [n, 34] uint8 rows in the R6 layout."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     assert x.ndim == 2 and x.shape[1] == 64

@@ -45,7 +45,7 @@
  *      level[code] * float(scale) in fp32, then round-to-nearest-even to bf16.
  *  R7  flat mode sums in fp32 in order of increasing n, starting from the first
  *      signed row (acc = s_0*T_0[..]; acc = acc + s_1*T_1[..]).
- *  R13 NF4 export (QLoRA's absmax quantisation of a 64-wide row): a = max |x_i|;
+ *  R15 NF4 export (QLoRA's absmax quantisation of a 64-wide row): a = max |x_i|;
  *      scale = a rounded to fp16 (nearest, ties to even; a value that would round
  *      past 65504 saturates to 65504); s = float(scale). s = 0: every code is the
  *      exact-zero level (index 7). Otherwise y_i = x_i / s (fp32, correctly rounded)
@@ -352,7 +352,7 @@ int orc_assemble(const orc_desc* d, int64_t n, const uint32_t* rows, const uint8
   return 0;
 }
 
-/* NF4 export of n rows of 64 fp32 values into 34-byte rows (R6 layout, R13 rule). */
+/* NF4 export of n rows of 64 fp32 values into 34-byte rows (R6 layout, R15 rule). */
 void orc_nf4_quantize(const float* x, int64_t n, uint8_t* out) {
   for (int64_t row = 0; row < n; ++row) {
     const float* xr = x + row * 64;

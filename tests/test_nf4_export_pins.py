@@ -1,7 +1,7 @@
 """Pins of the oracle's NF4 export (PageGram report 3.3 storage format; report 9.4, check 5:
 all-zero rows keep full fidelity and the quantisation error stays within its bound).
 
-The quantiser is QLoRA's absmax rule (reading R13): scale = fp16(max |x|), code = the
+The quantiser is QLoRA's absmax rule (reading R15): scale = fp16(max |x|), code = the
 nearest NF4 level of x / scale. The pins below come from the pages and from mathematics,
 not from retyping the rule: fp16 rounding against numpy's IEEE conversion, the zero row,
 rows built from exact levels, the error bound, idempotence through the stored format.
