@@ -78,6 +78,9 @@ def lib():
         L.orc_bf16_to_f32.restype = ctypes.c_float; L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
         L.orc_f32_to_f16_sat.restype = ctypes.c_uint16; L.orc_f32_to_f16_sat.argtypes = [ctypes.c_float]
         L.orc_nf4_quantize.restype = None; L.orc_nf4_quantize.argtypes = [vp, i64, vp]
+        L.orc_f32_to_e4m3_sat.restype = ctypes.c_uint8; L.orc_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+        L.orc_e4m3_to_f32.restype = ctypes.c_float; L.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        L.orc_fp8_quantize.restype = None; L.orc_fp8_quantize.argtypes = [vp, i64, i64, vp, vp]
         L.orc_total_rows.restype = u64; L.orc_total_rows.argtypes = [ctypes.POINTER(OrcDesc)]
         L.orc_sign_words.restype = ctypes.c_int; L.orc_sign_words.argtypes = [ctypes.POINTER(OrcDesc)]
         L.orc_heads.restype = ctypes.c_int; L.orc_heads.argtypes = [ctypes.POINTER(OrcDesc)]
@@ -240,3 +243,30 @@ def nf4_dequantize(rows: np.ndarray) -> np.ndarray:
     sbits = rows[:, 32].astype(np.uint16) | (rows[:, 33].astype(np.uint16) << 8)
     scale = np.array([lib().orc_f16_to_f32(int(b)) for b in sbits], np.float32)
     return (lv[codes] * scale[:, None]).astype(np.float32)
+
+
+def f32_to_e4m3_sat(x: float) -> int:
+    """OCP FP8 E4M3 bits of x: round to nearest, ties to even, saturating at +-448 (R16)."""
+    return int(lib().orc_f32_to_e4m3_sat(float(x)))
+
+
+def e4m3_to_f32(b: np.ndarray) -> np.ndarray:
+    """Values of E4M3 bytes (exact in fp32)."""
+    table = np.array([lib().orc_e4m3_to_f32(i) for i in range(256)], np.float32)
+    return table[np.asarray(b, np.uint8)]
+
+
+def fp8_quantize(x: np.ndarray):
+    """FP8 projection operand (reading R16, Engram notes 3.4): rows of x [n, cols] fp32 ->
+    (E4M3 bytes [n, cols], fp32 scales [n]) with value ~= e4m3(q) * scale."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n, cols = x.shape
+    q = np.zeros((n, cols), np.uint8)
+    s = np.zeros(n, np.float32)
+    lib().orc_fp8_quantize(x.ctypes.data, n, cols, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def fp8_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """fp64 values e4m3(q) * scale of FP8 rows (both factors exact in fp64)."""
+    return e4m3_to_f32(q).astype(np.float64) * np.asarray(s, np.float64)[:, None]

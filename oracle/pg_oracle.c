@@ -50,6 +50,12 @@
  *      past 65504 saturates to 65504); s = float(scale). s = 0: every code is the
  *      exact-zero level (index 7). Otherwise y_i = x_i / s (fp32, correctly rounded)
  *      and code_i = the k minimising |y_i - level[k]| in fp32, the lowest k on ties.
+ *  R16 FP8 projection operands (Engram notes 3.4: the fused W_V + M W_K GEMM runs in
+ *      FP8): OCP E4M3 (bias 7, no infinities, max 448). A row x of e_t or of W is stored
+ *      as q_i = E4M3(x_i / s) with s = max |x| / 448 (fp32 division; conversion rounds to
+ *      nearest, ties to even, and saturates at +-448); s = 0 stores zeros. The product of
+ *      two E4M3 values is exact in fp32, so the GEMM on the stored values is defined up to
+ *      the order of its fp32 sums; out[t, c] = s_e[t] s_w[c] sum_k q_e[t,k] q_w[c,k].
  *  Toy: flat bigram only, row = (3a + b) mod m on canonical IDs, no row at t=0.
  */
 #include <stdint.h>
@@ -387,5 +393,56 @@ void orc_nf4_quantize(const float* x, int64_t n, uint8_t* out) {
     for (int i = 0; i < 32; ++i) o[i] = (uint8_t)(code[2 * i] | (code[2 * i + 1] << 4));
     o[32] = (uint8_t)(sbits & 0xFFu);
     o[33] = (uint8_t)(sbits >> 8);
+  }
+}
+
+/* binary32 -> OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, S.1111.111 = NaN, max finite 448), round to nearest, ties to even, from the
+ * format definition; values that would round past 448 saturate to +-448, NaN stays NaN. */
+uint8_t orc_f32_to_e4m3_sat(float f) {
+  const uint32_t u = f32_to_bits(f);
+  const uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+  const uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint8_t)(sign | 0x7Fu);
+  if (a > 0x43E80000u) return (uint8_t)(sign | 0x7Eu);  /* > 464: would round to 480 */
+  const uint32_t e = a >> 23;
+  if (e < 121u) {
+    /* below 2^-6: a subnormal k * 2^-9, k = round(mantissa * 2^(e-141)) */
+    const int sh = 141 - (int)e;
+    if (sh > 24) return sign;
+    const uint32_t mant = (a & 0x7FFFFFu) | 0x800000u;
+    uint32_t k = mant >> sh;
+    const uint32_t rem = mant & ((1u << sh) - 1u), half = 1u << (sh - 1);
+    if (rem > half || (rem == half && (k & 1u))) k += 1u;  /* k = 8: smallest normal */
+    return (uint8_t)(sign | k);
+  }
+  uint32_t h = (a >> 20) - ((127u - 7u) << 3);
+  const uint32_t rem = a & 0xFFFFFu;
+  if (rem > 0x80000u || (rem == 0x80000u && (h & 1u))) h += 1u;
+  return (uint8_t)(sign | h);
+}
+
+/* OCP FP8 E4M3 -> binary32 (exact). */
+float orc_e4m3_to_f32(uint8_t b) {
+  const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
+  float v;
+  if (e == 15u && m == 7u) return bits_to_f32(0x7FC00000u);
+  if (e == 0u) v = (float)m * bits_to_f32(0x3B000000u); /* m * 2^-9 */
+  else v = bits_to_f32(((e + 120u) << 23) | (m << 20));
+  return (b & 0x80u) ? -v : v;
+}
+
+/* FP8 rows (R16): n rows of `cols` fp32 values -> E4M3 bytes [n, cols] and scales [n]. */
+void orc_fp8_quantize(const float* x, int64_t n, int64_t cols, uint8_t* q, float* scale) {
+  for (int64_t row = 0; row < n; ++row) {
+    const float* xr = x + row * cols;
+    float a = 0.0f;
+    for (int64_t i = 0; i < cols; ++i) {
+      const float v = xr[i] < 0.0f ? -xr[i] : xr[i];
+      if (v > a) a = v;
+    }
+    const float s = a / 448.0f;
+    scale[row] = s;
+    for (int64_t i = 0; i < cols; ++i) q[row * cols + i] = s == 0.0f ? 0u : orc_f32_to_e4m3_sat(xr[i] / s);
   }
 }
