@@ -198,13 +198,21 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) (+)= A(smem desc) x B(smem desc)^T, bf16 in, fp32 accumulate. PAIR: M = 256 rows
-// over the two CTAs (each holds 128 rows of A and half of B's rows at the same offsets,
-// and 128 rows of D in its TMEM).
-template <bool PAIR>
+// D(tmem) (+)= A(smem desc) x B(smem desc)^T, bf16 (FP8: E4M3) in, fp32 accumulate. PAIR:
+// M = 256 rows over the two CTAs (each holds 128 rows of A and half of B's rows at the same
+// offsets, and 128 rows of D in its TMEM). One instruction covers 32 bytes of K: 16 bf16
+// or 32 E4M3 elements.
+template <bool PAIR, bool FP8 = false>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  if constexpr (PAIR)
+  if constexpr (FP8 && PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else if constexpr (PAIR)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -313,6 +321,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B E4M3 (format 0 at bits 7-9, 10-12), both
+// K-major, N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -396,6 +410,8 @@ struct GemmArgs {
   const float* gamma_k;      // [d]
   float* partials;           // [M, d/BN, 3, N] (context gate)
   float* vpart;              // [d/BN, N] row sums of v^2 per v tile (context gate, or null)
+  const float* sa;           // FP8: per-row scales of e [N]
+  const float* sw;           // FP8: per-row scales of W [Dcols]
   int* err_word;
 };
 
@@ -462,7 +478,7 @@ __device__ __forceinline__ uint32_t epi_offset(int row, int chunk) {
 // it on its 128-token block's ready counter (release); the A producer waits (acquire,
 // bounded) for a block's count before its first TMA load of that block. Any resident CTA
 // claims and finishes chunks without waiting on anything, so every wait ends.
-template <int BN, int GATE, bool GATHER, bool PAIR, bool PRODUCE = false>
+template <int BN, int GATE, bool GATHER, bool PAIR, bool PRODUCE = false, bool FP8 = false>
 __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThreads : kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
@@ -470,20 +486,26 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
                    const __grid_constant__ typename GatherParam<GATHER || PRODUCE>::type gat) {
   static_assert(!(GATHER && PAIR), "the fused gather runs on single-CTA tiles");
   static_assert(!(GATHER && PRODUCE), "one way of making A");
-  constexpr int kSt = gemm_stages<PAIR>();
+  static_assert(!FP8 || (PAIR && !GATHER && !PRODUCE), "FP8 operands: the plain CTA-pair kernel");
+  constexpr int kKB = FP8 ? 2 * kBK : kBK;  // elements of a 128-byte k-block row
+  // FP8: stages of two k-blocks (8 MMAs per barrier wait: an E4M3 k-block is half the tensor
+  // time of a bf16 one, and the single issuing thread's per-wait overhead would set the pace)
+  constexpr int kSubK = FP8 ? 2 : 1;
+  constexpr int kSt = gemm_stages<PAIR>() / kSubK;
   constexpr int kEpiStages = epi_stages<GATHER || PRODUCE>();
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of W this CTA stages per k-block
   constexpr int kBBytes = kBRows * kBK * 2;
+  constexpr int kAStage = kABytes * kSubK, kBStage = kBBytes * kSubK;
   constexpr int kTileM = PAIR ? 2 * kBM : kBM;  // output rows of a tile
-  constexpr uint32_t kIdesc = idesc_bf16(kTileM, BN);
+  constexpr uint32_t kIdesc = FP8 ? idesc_e4m3(kTileM, BN) : idesc_bf16(kTileM, BN);
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr int kSub = BN / kEpiCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kSt * kABytes;
-  uint8_t* sE = sB + kSt * kBBytes;
+  uint8_t* sB = smem + kSt * kAStage;
+  uint8_t* sE = sB + kSt * kBStage;
   GemmBarriers<kSt>* bars = reinterpret_cast<GemmBarriers<kSt>*>(sE + kEpiStages * kEpiBytes);
   ItemConst* s_ic = reinterpret_cast<ItemConst*>(bars + 1);
   // producing kernel: slot u holds at [i] the canonical ID of flat position (unit start - 3 + i)
@@ -541,7 +563,7 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
   const int num_m = (args.N + kTileM - 1) / kTileM;
   const int num_n = args.Dcols / BN;
   const int num_tiles = num_m * num_n;
-  const int num_kb = args.Din / kBK;
+  const int num_kb = args.Din / (kKB * kSubK);  // stages per tile
 
   __shared__ int64_t s_unit[kUnitSlots];  // gather units handed out (producing kernel)
   if (warp == 0) {
@@ -577,12 +599,15 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
           }
           const uint32_t full = smem_u32(&bars->full[stage]);
           if constexpr (PAIR) {
-            if (rank == 0) mbar_expect_tx(full, 2 * (kABytes + kBBytes));
+            if (rank == 0) mbar_expect_tx(full, 2 * (kAStage + kBStage));
             const uint32_t full0 = pair_addr(full, 0);
-            tma_load_2d_pair(smem_u32(sA + stage * kABytes), &map_a, full0, kb * kBK,
-                             m_blk * kTileM + static_cast<int>(rank) * kBM);
-            tma_load_2d_pair(smem_u32(sB + stage * kBBytes), &map_b, full0, kb * kBK,
-                             n_blk * BN + static_cast<int>(rank) * kBRows);
+#pragma unroll
+            for (int sb = 0; sb < kSubK; ++sb) {
+              tma_load_2d_pair(smem_u32(sA + stage * kAStage + sb * kABytes), &map_a, full0, (kb * kSubK + sb) * kKB,
+                               m_blk * kTileM + static_cast<int>(rank) * kBM);
+              tma_load_2d_pair(smem_u32(sB + stage * kBStage + sb * kBBytes), &map_b, full0, (kb * kSubK + sb) * kKB,
+                               n_blk * BN + static_cast<int>(rank) * kBRows);
+            }
           } else {
             mbar_expect_tx(full, GATHER ? kBBytes : kABytes + kBBytes);
             if (!GATHER) tma_load_2d(smem_u32(sA + stage * kABytes), &map_a, full, kb * kBK, m_blk * kBM);
@@ -643,11 +668,14 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
             break;
           }
           tc_fence_after();
-          const uint64_t a0 = sw128_desc(smem_u32(sA + stage * kABytes));
-          const uint64_t b0 = sw128_desc(smem_u32(sB + stage * kBBytes));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)  // advance 16 elements = 32 bytes = 2 units
-            umma_bf16<PAIR>(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc, (kb | k) != 0);
+          for (int sb = 0; sb < kSubK; ++sb) {
+            const uint64_t a0 = sw128_desc(smem_u32(sA + stage * kAStage + sb * kABytes));
+            const uint64_t b0 = sw128_desc(smem_u32(sB + stage * kBStage + sb * kBBytes));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)  // advance 32 bytes = 2 units (16 bf16 or 32 E4M3)
+              umma_bf16<PAIR, FP8>(d_tmem, a0 + 2u * k, b0 + 2u * k, kIdesc, (kb | sb | k) != 0);
+          }
           umma_commit<PAIR>(smem_u32(&bars->empty[stage]));
           if (++stage == kSt) {
             stage = 0;
@@ -975,7 +1003,7 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
           ok = false;
           break;
         }
-        uint8_t* a_tile = sA + stage * kABytes;
+        uint8_t* a_tile = sA + stage * kAStage;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int src = 4 * (i & 7) + sub;
@@ -1038,6 +1066,19 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
         uint32_t r[32];
         tmem_ld32(t_base + static_cast<uint32_t>(j * kEpiCols), r);
         tmem_ld_wait();
+        if constexpr (FP8) {
+          // out = s_e[row] s_w[col] sum_k q_e q_w
+          const float sr = live ? __ldg(args.sa + row) : 0.f;
+          const float4* sc = reinterpret_cast<const float4*>(args.sw + n0 + j * kEpiCols);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 c4 = __ldg(sc + q);
+            r[4 * q + 0] = __float_as_uint(__uint_as_float(r[4 * q + 0]) * sr * c4.x);
+            r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) * sr * c4.y);
+            r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) * sr * c4.z);
+            r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) * sr * c4.w);
+          }
+        }
         uint8_t* slot_p = sE + slot * kEpiBytes;
         if (is_k) {
           const float4* gh = reinterpret_cast<const float4*>(args.gamma_h + kc + j * kEpiCols);
@@ -1203,16 +1244,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (row-major), box [box_rows, box_cols].
+// 2-D bf16 (bytes1: 1-byte elements, E4M3) tensor [rows, cols] (row-major), box [box_rows, box_cols].
 bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
-              uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+              uint32_t box_rows, CUtensorMapSwizzle swizzle, bool bytes1 = false) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {cols * (bytes1 ? 1 : 2)};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+  CUresult r = enc(map, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(ptr), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -1226,12 +1268,13 @@ struct GemmPtrs {
   void* v;
 };
 
-template <int BN, int GATE, bool GATHER = false, bool PAIR = false, bool PRODUCE = false>
+template <int BN, int GATE, bool GATHER = false, bool PAIR = false, bool PRODUCE = false, bool FP8 = false>
 pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
                     const typename GatherParam<GATHER || PRODUCE>::type& gat = {}) {
   CUtensorMap ma, mb, mx, mh, mv;
-  if ((!GATHER && !make_map(&ma, ptr.e, a.N, a.Din, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-      !make_map(&mb, ptr.W, a.Dcols, a.Din, kBK, PAIR ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  constexpr uint32_t kBox = FP8 ? 2 * kBK : kBK;  // a 128-byte row of elements
+  if ((!GATHER && !make_map(&ma, ptr.e, a.N, a.Din, kBox, kBM, CU_TENSOR_MAP_SWIZZLE_128B, FP8)) ||
+      !make_map(&mb, ptr.W, a.Dcols, a.Din, kBox, PAIR ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B, FP8) ||
       !make_map(&mv, ptr.v, a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
   // maps that this launch does not use alias the output map (never read)
@@ -1243,7 +1286,7 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
   if (GATE == PG_GATE_CONTEXT &&
       !make_map(&mh, ptr.h, static_cast<uint64_t>(a.M) * a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
-  auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR, PRODUCE>;
+  auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR, PRODUCE, FP8>;
   const size_t smem = gemm_smem_bytes<BN, GATHER, PAIR, PRODUCE>();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -1284,6 +1327,12 @@ pg_status dispatch_tc(int gate, const GemmPtrs& ptr, const GemmArgs& a, cudaStre
   if (gate == PG_GATE_NONE) return launch_tc<BN, PG_GATE_NONE, false, PAIR>(ptr, a, stream);
   if (gate == PG_GATE_SCALAR) return launch_tc<BN, PG_GATE_SCALAR, false, PAIR>(ptr, a, stream);
   return launch_tc<BN, PG_GATE_CONTEXT, false, PAIR>(ptr, a, stream);
+}
+
+pg_status dispatch_fp8(int gate, const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream) {
+  if (gate == PG_GATE_NONE) return launch_tc<256, PG_GATE_NONE, false, true, false, true>(ptr, a, stream);
+  if (gate == PG_GATE_SCALAR) return launch_tc<256, PG_GATE_SCALAR, false, true, false, true>(ptr, a, stream);
+  return launch_tc<256, PG_GATE_CONTEXT, false, true, false, true>(ptr, a, stream);
 }
 
 pg_status dispatch_produce(int gate, const GemmPtrs& ptr, const GemmArgs& a, const FusedGather& gat,
@@ -1378,6 +1427,7 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   if (gate_kind == PG_GATE_CONTEXT && static_cast<int64_t>(M) * N >= (1ll << 31)) return PG_ERR_SHAPE;
   const GemmPtrs ptrs{e, W, x_resid, h, v_out};
   a.err_word = device_error_word();
+  a.sa = a.sw = nullptr;
   if (!a.err_word) return cuda_fail(cudaGetLastError());
   if (gate_kind == PG_GATE_CONTEXT) {
     const size_t need = context_workspace(N, d, M, v_ms_out != nullptr);
@@ -1387,6 +1437,62 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   // 256-column tiles run on CTA pairs (256 x 256 per pair), 128-column ones on single CTAs
   pg_status st = bn == 256 ? dispatch_tc<256, true>(gate_kind, ptrs, a, stream)
                            : dispatch_tc<128, false>(gate_kind, ptrs, a, stream);
+  if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
+  const int64_t total = static_cast<int64_t>(M) * N;
+  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
+      a.partials, M, d / bn, N, d, eps, alpha_out, a.vpart, v_ms_out);
+  return after_launch(1);
+}
+
+
+pg_status pg_project_gate_fp8(int32_t N, int32_t Din, int32_t d, int32_t M, const void* e_q, const float* e_scale,
+                              const void* W_q, const float* W_scale, int32_t gate_kind, float g,
+                              const void* x_resid, const void* h, const float* gamma_h, const float* gamma_k,
+                              float eps, void* v_out, float* alpha_out, float* v_ms_out, void* workspace,
+                              size_t workspace_bytes, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (N < 0 || Din < 1 || d < 1 || M < 0) return PG_ERR_SHAPE;
+  if (gate_kind < PG_GATE_NONE || gate_kind > PG_GATE_CONTEXT) return PG_ERR_SHAPE;
+  if (gate_kind != PG_GATE_CONTEXT && M != 0) return PG_ERR_SHAPE;
+  if (gate_kind == PG_GATE_CONTEXT && M < 1) return PG_ERR_SHAPE;
+  if (N == 0) return PG_OK;
+  if (!e_q || !e_scale || !W_q || !W_scale || !v_out) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_SCALAR && !x_resid) return PG_ERR_NULL;
+  if (gate_kind == PG_GATE_CONTEXT && (!h || !gamma_h || !gamma_k || !alpha_out)) return PG_ERR_NULL;
+  if (Din % (4 * kBK) != 0 || d % 256 != 0) return PG_ERR_UNSUPPORTED;  // stages of two 128-byte k-blocks
+  if (!aligned16(e_q) || !aligned16(W_q) || !aligned16(v_out) || !aligned16(W_scale) ||
+      (reinterpret_cast<uintptr_t>(e_scale) % 4) || (x_resid && !aligned16(x_resid)) || (h && !aligned16(h)))
+    return PG_ERR_ALIGN;
+  if (static_cast<int64_t>(N) * (d > Din ? d : Din) >= (1ll << 40)) return PG_ERR_SHAPE;
+  if (gate_kind == PG_GATE_CONTEXT && static_cast<int64_t>(M) * N >= (1ll << 31)) return PG_ERR_SHAPE;
+  if (sm_count() == 0) return cuda_fail(cudaGetLastError());
+  if (device_cc() != 103 && device_cc() != 100) return PG_ERR_DEVICE;
+  constexpr int bn = 256;
+  GemmArgs a;
+  a.N = N;
+  a.Din = Din;
+  a.Dcols = (gate_kind == PG_GATE_CONTEXT ? (1 + M) : 1) * d;
+  a.d = d;
+  a.M = M;
+  a.g = g;
+  a.gamma_h = gamma_h;
+  a.gamma_k = gamma_k;
+  a.partials = static_cast<float*>(workspace);
+  a.vpart = (gate_kind == PG_GATE_CONTEXT && v_ms_out)
+                ? static_cast<float*>(workspace) + static_cast<size_t>(M) * (d / bn) * 3 * static_cast<size_t>(N)
+                : nullptr;
+  a.err_word = device_error_word();
+  if (!a.err_word) return cuda_fail(cudaGetLastError());
+  a.sa = e_scale;
+  a.sw = W_scale;
+  if (gate_kind == PG_GATE_CONTEXT) {
+    const size_t need = context_workspace(N, d, M, v_ms_out != nullptr);
+    if (!workspace || workspace_bytes < need) return PG_ERR_WORKSPACE;
+    if (!aligned16(workspace) || !aligned16(gamma_h) || !aligned16(gamma_k)) return PG_ERR_ALIGN;
+  }
+  const GemmPtrs ptrs{e_q, W_q, x_resid, h, v_out};
+  pg_status st = dispatch_fp8(gate_kind, ptrs, a, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
   const int64_t total = static_cast<int64_t>(M) * N;
   alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
@@ -1457,6 +1563,7 @@ extern "C" pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int
   a.partials = static_cast<float*>(workspace);
   a.vpart = nullptr;
   a.err_word = device_error_word();
+  a.sa = a.sw = nullptr;
   if (!a.err_word) return cuda_fail(cudaGetLastError());
   FusedGather gat;
   fill_hash_params(desc, geo, &gat.P);
@@ -1561,6 +1668,7 @@ extern "C" pg_status pg_gather_project_gate(const pg_table_desc* desc, const int
                 ? a.partials + static_cast<size_t>(M) * (d / bn) * 3 * static_cast<size_t>(N)
                 : nullptr;
   a.err_word = device_error_word();
+  a.sa = a.sw = nullptr;
   if (!a.err_word) return cuda_fail(cudaGetLastError());
   FusedGather gat;
   fill_hash_params(desc, geo, &gat.P);

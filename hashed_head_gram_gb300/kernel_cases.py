@@ -1,6 +1,6 @@
 """Single-kernel runs on a workload's shapes, for timing and profiling one kernel at a time.
 
-    python -m hashed_head_gram_gb300.kernel_cases {gather,project,gather_project,conv,nf4_export} --config C [--iters N]
+    python -m hashed_head_gram_gb300.kernel_cases {gather,project,project_fp8,gather_project,conv,nf4_export} --config C [--iters N]
 
 Inputs are synthetic and seeded (the conv and projection cases need no table, so they
 hold at most a few GB on the device); each launch goes through the C ABI exactly as the
@@ -42,7 +42,7 @@ def _time(fn, iters: int, dev) -> float:
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["gather", "project", "gather_project", "conv", "nf4_export"])
+    ap.add_argument("kernel", choices=["gather", "project", "project_fp8", "gather_project", "conv", "nf4_export"])
     ap.add_argument("--rows", type=int, default=8 << 20, help="nf4_export: fp32 head rows to export")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--iters", type=int, default=20)
@@ -90,6 +90,33 @@ def main(argv=None):
                                                   g=w.g, x_resid=x), args.iters, dev)
         print(f"gather_project_gate config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * d / us / 1e6:.1f} TFLOP/s, "
               f"{N / us:.1f} M tokens/s")
+    elif args.kernel == "project_fp8":
+        # the projection on E4M3 operands (pg_fp8_quantize of e and W, then pg_project_gate_fp8);
+        # timed: the projection alone, and the quantisation of e that a step adds to it
+        e = (torch.randint(-128, 128, (N, din), device=dev, generator=g).float() / 64).to(torch.bfloat16)
+        Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        qe = torch.empty(N, din, dtype=torch.uint8, device=dev)
+        se = torch.empty(N, device=dev)
+        qw = torch.empty((1 + M) * d, din, dtype=torch.uint8, device=dev)
+        sw = torch.empty((1 + M) * d, device=dev)
+        pg.fp8_quantize(Wm, qw, sw)
+        v = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+        quant = lambda: pg.fp8_quantize(e, qe, se)
+        quant()
+        if w.gate == W.GATE_CONTEXT:
+            H = torch.randn(M, N, d, device=dev, generator=g).to(torch.bfloat16)
+            one = torch.ones(d, device=dev)
+            alpha = torch.empty(M, N, device=dev)
+            ws = torch.empty(pg.workspace_size(N, din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4, device=dev)
+            fn = lambda: pg.project_gate_fp8(qe, se, qw, sw, d, pg.GATE_CONTEXT, v, M=M, h=H, gamma_h=one,
+                                             gamma_k=one, alpha_out=alpha, workspace=ws)
+        else:
+            x = torch.randn(N, d, device=dev, generator=g).to(torch.bfloat16)
+            fn = lambda: pg.project_gate_fp8(qe, se, qw, sw, d, pg.GATE_SCALAR, v, g=w.g, x_resid=x)
+        us = _time(fn, args.iters, dev)
+        uq = _time(quant, args.iters, dev)
+        print(f"project_gate_fp8 config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * (1 + M) * d / us / 1e6:.1f} "
+              f"TFLOP/s; fp8_quantize of e: {uq:.1f} us")
     elif args.kernel == "project":
         e = (torch.randint(-128, 128, (N, din), device=dev, generator=g).float() / 64).to(dt)
         Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(dt)

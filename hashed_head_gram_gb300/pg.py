@@ -92,6 +92,11 @@ def _load():
                                          vp, f32, vp, vp, vp, vp, sz, vp, vp]
     L.pg_gather_project_gate_workspace_size.restype = ctypes.c_int
     L.pg_gather_project_gate_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
+    L.pg_fp8_quantize.restype = ctypes.c_int
+    L.pg_fp8_quantize.argtypes = [vp, i32, ctypes.c_int64, ctypes.c_int64, vp, vp, vp]
+    L.pg_project_gate_fp8.restype = ctypes.c_int
+    L.pg_project_gate_fp8.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, i32, f32, vp, vp, vp, vp, f32, vp, vp,
+                                      vp, vp, sz, vp]
     L.pg_nf4_quantize.restype = ctypes.c_int
     L.pg_nf4_quantize.argtypes = [vp, ctypes.c_int64, i32, vp, vp]
     L.pg_project_gate_context_noalloc.restype = ctypes.c_int
@@ -245,6 +250,29 @@ def gather_project_gate(desc: TableDesc, tokens: torch.Tensor, table: torch.Tens
            "pg_gather_project_gate")
 
 
+def fp8_quantize(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, stream=None):
+    """E4M3 rows with absmax/448 scales: x [rows, cols] fp32 or bf16 -> q uint8, scale fp32 [rows]."""
+    rows, cols = x.shape
+    _check(_lib.pg_fp8_quantize(_ptr(x), dtype_code(x.dtype), rows, cols, _ptr(q), _ptr(scale), _stream(stream)),
+           "pg_fp8_quantize")
+
+
+def project_gate_fp8(e_q: torch.Tensor, e_scale: torch.Tensor, W_q: torch.Tensor, W_scale: torch.Tensor, d: int,
+                     gate_kind: int, v_out: torch.Tensor, M: int = 0, g: float = 0.0,
+                     x_resid: Optional[torch.Tensor] = None, h: Optional[torch.Tensor] = None,
+                     gamma_h: Optional[torch.Tensor] = None, gamma_k: Optional[torch.Tensor] = None,
+                     eps: float = 1e-6, alpha_out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, v_ms_out: Optional[torch.Tensor] = None,
+                     stream=None):
+    """project_gate on E4M3 operands (pg_fp8_quantize's output)."""
+    N, Din = e_q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pg_project_gate_fp8(N, Din, d, M, _ptr(e_q), _ptr(e_scale), _ptr(W_q), _ptr(W_scale), gate_kind, g,
+                                    _ptr(x_resid), _ptr(h), _ptr(gamma_h), _ptr(gamma_k), eps, _ptr(v_out),
+                                    _ptr(alpha_out), _ptr(v_ms_out), _ptr(workspace), ws_bytes, _stream(stream)),
+           "pg_project_gate_fp8")
+
+
 def nf4_quantize(x: torch.Tensor, out: torch.Tensor, stream=None):
     """NF4 export: x fp32 [n, 64] -> out uint8 [n, 34] (the PG_NF4 row layout)."""
     n, r = x.shape
@@ -288,6 +316,6 @@ def dtype_code(t: torch.dtype) -> int:
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
-           "gather_project_gate", "nf4_quantize", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
+           "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

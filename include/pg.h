@@ -257,6 +257,34 @@ pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M, int32_t d
                            int32_t dilation, float eps, void* H, pg_stream_t stream);
 
 /*
+ * FP8 operands of the fused projection (Engram notes 3.4: W_V and the M W_K run in FP8).
+ *
+ * pg_fp8_quantize -- rows of x [rows, cols] (dtype PG_F32 or PG_BF16, 16-byte aligned,
+ * cols % 8 == 0) -> OCP E4M3 codes q [rows, cols] (1 byte each, 16-byte aligned) and one
+ * fp32 scale per row (scale [rows], 4-byte aligned): scale = max |x| / 448 (fp32 division),
+ * q_i = E4M3(x_i / scale) rounded to nearest, ties to even, saturating at +-448; a row
+ * whose max |x| is 0 gets scale 0 and zero codes. NaN elements are outside the contract.
+ */
+pg_status pg_fp8_quantize(const void* x, int32_t dtype, int64_t rows, int64_t cols, void* q,
+                          float* scale, pg_stream_t stream);
+
+/*
+ * pg_project_gate_fp8 -- pg_project_gate (dtype PG_BF16 outputs and gates) on E4M3
+ * operands: v = diag(e_scale) (e_q W_q^T) diag(W_scale) with e_q [N, Din] and W_q
+ * [(1+M)*d, Din] from pg_fp8_quantize, fp32 accumulation on the tensor cores
+ * (tcgen05.mma kind::f8f6f4, CTA pairs), then exactly pg_project_gate's gate epilogue.
+ *  e_q, W_q     device E4M3 bytes, 16-byte aligned; Din % 256 == 0; d % 256 == 0
+ *  e_scale      device fp32 [N] (4-byte aligned); W_scale device fp32 [(1+M)*d] (16-byte aligned)
+ *  the rest     as pg_project_gate (workspace: pg_project_gate_workspace_size with PG_BF16)
+ */
+pg_status pg_project_gate_fp8(int32_t N, int32_t Din, int32_t d, int32_t M, const void* e_q,
+                              const float* e_scale, const void* W_q, const float* W_scale,
+                              int32_t gate_kind, float g, const void* x_resid, const void* h,
+                              const float* gamma_h, const float* gamma_k, float eps, void* v_out,
+                              float* alpha_out, float* v_ms_out, void* workspace,
+                              size_t workspace_bytes, pg_stream_t stream);
+
+/*
  * pg_lookup_project_gate -- steps 1-7 in one kernel: pg_gather_sign_concat followed by
  * pg_project_gate, without writing e_t to memory. The projection is the fused W_V (+ M
  * W_K) GEMM of the Engram notes section 3.4 fed straight by the lookup of section 3.2 /
