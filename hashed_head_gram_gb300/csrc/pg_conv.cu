@@ -72,6 +72,8 @@ struct VecN<__nv_bfloat16, 4> {
   static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) {
     return __ldg(reinterpret_cast<const uint2*>(p));
   }
+  // coherent load, for memory the same kernel also writes
+  static __device__ __forceinline__ Raw load_rw(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
   static __device__ __forceinline__ void unpack(const Raw& w, float* f) {
     f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
     f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
@@ -106,6 +108,7 @@ struct VecN<float, 4> {
   using Raw = float4;
   static __device__ __forceinline__ Raw zero() { return make_float4(0, 0, 0, 0); }
   static __device__ __forceinline__ Raw load(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+  static __device__ __forceinline__ Raw load_rw(const float* p) { return *reinterpret_cast<const float4*>(p); }
   static __device__ __forceinline__ void unpack(const Raw& r, float* f) {
     f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
   }
@@ -177,6 +180,29 @@ __device__ __forceinline__ uint64_t silu2_add(uint64_t h, uint64_t acc) {
   return fma2(h, pk(t0, t1), add2(h, acc));
 }
 
+// f = alpha / sqrt(alpha^2 mean(v^2) + eps), the RMSNorm factor of u = alpha v, with every
+// rounding spelled out so the full-sequence and the decode kernel compute the same value.
+__device__ __forceinline__ float tap_scale(float a, float ms, float eps) {
+  return __fmul_rn(a, rsqrtf(__fmaf_rn(__fmul_rn(a, a), ms, eps)));
+}
+
+// mean(v^2) of one d-wide row by one warp: lane l sums the squares of 8-element groups
+// l, l + 32, ... in order (one FMA each), then the lanes' sums are added in an xor tree.
+template <typename T>
+__device__ __forceinline__ float row_mean_square(const T* __restrict__ row, int chunks8, float inv_d, int lane) {
+  float s = 0.f;
+#pragma unroll 4
+  for (int q = lane; q < chunks8; q += 32) {
+    float x[8];
+    VecN<T, 8>::unpack(VecN<T, 8>::load(row + 8 * q), x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s = __fmaf_rn(x[k], x[k], s);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
+  return __fmul_rn(s, inv_d);
+}
+
 constexpr int kCpt = 4;             // channels per thread
 constexpr int kMaxThreads = 768;    // so a slice holds at most 3072 channels
 constexpr int kSliceThreads = 128;  // slice width when mean(v^2) is given
@@ -244,18 +270,8 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
     if (v_ms)
       for (int i = threadIdx.x; i < npos; i += blockDim.x) s_ms[i] = v_ms[seq0 + p0 + i];
     for (int i = warp; !v_ms && i < npos; i += nwarps) {
-      const T* row = v + (seq0 + p0 + i) * d;
-      float s = 0.f;
-#pragma unroll 4
-      for (int q = lane; q < chunks8; q += 32) {
-        float x[8];
-        VecN<T, 8>::unpack(VecN<T, 8>::load(row + 8 * q), x);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) s = fmaf(x[k], x[k], s);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (lane == 0) s_ms[i] = s * inv_d;
+      const float s = row_mean_square(v + (seq0 + p0 + i) * d, chunks8, inv_d, lane);
+      if (lane == 0) s_ms[i] = s;
     }
     __syncthreads();
 
@@ -266,7 +282,7 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
       float a = 0.f, f = 0.f;
       if (t < t1 && j < ks && p >= 0) {
         a = alpha[m * N + seq0 + p];
-        f = a * rsqrtf(a * a * s_ms[p - p0] + eps);
+        f = tap_scale(a, s_ms[p - p0], eps);
       }
       *reinterpret_cast<float2*>(&s_tap[m][i][2 * j]) = make_float2(f, f);
       if (j == 0) *reinterpret_cast<float2*>(&s_tap[m][i][8]) = make_float2(a, a);
@@ -372,6 +388,176 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
   }
 }
 
+// ------------------------------------------------------------------ streaming decode
+
+// Position t = pos[b] - 1 of each sequence. Block (b, slice) owns 512 channels of sequence
+// b, thread i channels [4 i, 4 i + 4) of the slice. The inputs that do not depend on t (v_t,
+// H of the M branches, the conv taps) are requested first, while thread 0 reads pos; the
+// tap scalars of the earlier positions then come from the ring (slot p mod D holds v_p,
+// alpha_{:, p}, mean(v_p^2)). Every product, FMA and the SiLU are the full-sequence
+// kernel's, in its order, so H gets the same update. The ring has one slot more than the
+// taps reach, so the slot of t, written here (v by each thread for its channels, the
+// scalars by slice 0), is read by no block of this launch.
+constexpr int kDecodeThreads = 128;
+
+template <typename T, int MB>
+__global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
+    int B, int d, int M_rt, int slices, const T* __restrict__ v, const float* __restrict__ alpha,
+    const float* __restrict__ v_ms, const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks,
+    int dil, float eps, const int32_t* __restrict__ pos, T* __restrict__ ring_v, float* __restrict__ ring_a,
+    float* __restrict__ ring_ms, int D, T* __restrict__ H, int* err_word) {
+  constexpr int MMAX = MB > 0 ? MB : kMaxBranches;
+  const int M = MB > 0 ? MB : M_rt;
+  using Vec = VecN<T, kCpt>;
+  constexpr int kPairs = kCpt / 2;
+  __shared__ float s_f[kMaxBranches][kTaps];
+  __shared__ float s_a[kMaxBranches];
+  __shared__ float s_ms_t;
+  __shared__ int s_t;
+  const int b = blockIdx.x / slices, slice = blockIdx.x - (blockIdx.x / slices) * slices;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = (slice * kDecodeThreads + threadIdx.x) * kCpt;
+  const bool active = c0 < d;
+  const int64_t row_b = static_cast<int64_t>(b) * d;
+
+  // 1. what does not depend on t: v_t, H, the taps; t itself and mean(v_t^2)
+  if (threadIdx.x == 0) {
+    s_t = pos[b] - 1;
+    if (v_ms) s_ms_t = v_ms[b];
+  }
+  typename Vec::Raw vt = Vec::zero();
+  typename Vec::Raw hraw[MMAX];
+  uint64_t wg[kTaps][kPairs];
+  if (active) {
+    vt = Vec::load(v + row_b + c0);
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m)
+      if (m < M) hraw[m] = Vec::load_rw(H + (static_cast<int64_t>(m) * B + b) * d + c0);
+#pragma unroll
+    for (int q = 0; q < kPairs; ++q) {
+      float g[2], w[kTaps][2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = c0 + 2 * q + e;
+        g[e] = 0.5f * gamma_c[c];
+#pragma unroll
+        for (int j = 0; j < kTaps; ++j) w[j][e] = j < ks ? conv_w[c * ks + j] * g[e] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kTaps; ++j) wg[j][q] = pk(w[j][0], w[j][1]);
+    }
+  }
+  if (!v_ms && warp == 0) {
+    const float s = row_mean_square(v + row_b, d >> 3, 1.0f / static_cast<float>(d), lane);
+    if (lane == 0) s_ms_t = s;
+  }
+  __syncthreads();
+  const int t = s_t;
+  if (t < 0) {  // pos[b] < 1: no token consumed to apply the conv to
+    if (threadIdx.x == 0 && slice == 0 && err_word) atomicOr(err_word, 512);
+    return;
+  }
+  // 2. tap scalars f_{t - j dil} (0 before the start and past the kernel size) and alpha_t
+  if (threadIdx.x < M * kTaps) {
+    const int j = threadIdx.x % kTaps, m = threadIdx.x / kTaps;
+    const int p = t - j * dil;
+    float a = 0.f, f = 0.f;
+    if (j < ks && p >= 0) {
+      float ms;
+      if (j == 0) {
+        a = alpha[static_cast<int64_t>(m) * B + b];
+        ms = s_ms_t;
+      } else {
+        const int64_t slot = static_cast<int64_t>(b) * D + p % D;
+        a = ring_a[slot * M + m];
+        ms = ring_ms[slot];
+      }
+      f = tap_scale(a, ms, eps);
+    }
+    s_f[m][j] = f;
+    if (j == 0) s_a[m] = a;
+  }
+  __syncthreads();
+  // 3. conv + SiLU + residual, then v_t into slot t mod D
+  if (active) {
+    uint64_t x[kTaps][kPairs];
+#pragma unroll
+    for (int j = 0; j < kTaps; ++j) {
+      const int p = t - j * dil;
+      float xf[kCpt];
+      if (j == 0) {
+        Vec::unpack(vt, xf);
+      } else if (j < ks && p >= 0) {
+        Vec::unpack(Vec::load_rw(ring_v + (static_cast<int64_t>(b) * D + p % D) * d + c0), xf);
+      } else {
+#pragma unroll
+        for (int q = 0; q < kCpt; ++q) xf[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < kPairs; ++q) x[j][q] = pk(xf[2 * q], xf[2 * q + 1]);
+    }
+    uint64_t prod[kTaps][kPairs];
+#pragma unroll
+    for (int j = 0; j < kTaps; ++j)
+#pragma unroll
+      for (int q = 0; q < kPairs; ++q) prod[j][q] = mul2(wg[j][q], x[j][q]);
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m) {
+      if (m >= M) continue;
+      const uint64_t f0 = pk(s_f[m][0], s_f[m][0]), f1 = pk(s_f[m][1], s_f[m][1]);
+      const uint64_t f2 = pk(s_f[m][2], s_f[m][2]), f3 = pk(s_f[m][3], s_f[m][3]);
+      const uint64_t aa = pk(s_a[m], s_a[m]);
+      float h[kCpt];
+      Vec::unpack(hraw[m], h);
+#pragma unroll
+      for (int q = 0; q < kPairs; ++q) {
+        uint64_t c = mul2(f0, prod[0][q]);  // c / 2
+        c = fma2(f1, prod[1][q], c);
+        c = fma2(f2, prod[2][q], c);
+        c = fma2(f3, prod[3][q], c);
+        const uint64_t acc = fma2(aa, x[0][q], pk(h[2 * q], h[2 * q + 1]));  // H + alpha v_t
+        upk(silu2_add(c, acc), h[2 * q], h[2 * q + 1]);
+      }
+      Vec::store(H + (static_cast<int64_t>(m) * B + b) * d + c0, h);
+    }
+    if (D > 0) {
+      float xf[kCpt];
+      Vec::unpack(vt, xf);
+      Vec::store(ring_v + (static_cast<int64_t>(b) * D + t % D) * d + c0, xf);
+    }
+  }
+  // 4. the scalars of position t into its slot
+  if (D > 0 && slice == 0 && threadIdx.x < M) {
+    const int64_t slot = static_cast<int64_t>(b) * D + t % D;
+    ring_a[slot * M + threadIdx.x] = s_a[threadIdx.x];
+    if (threadIdx.x == 0) ring_ms[slot] = s_ms_t;
+  }
+}
+
+template <typename T, int MB>
+pg_status launch_decode(const pg_decode_state* st, const void* v, const float* alpha, const float* v_ms,
+                        const float* gamma_c, const float* conv_w, float eps, void* H, cudaStream_t stream) {
+  const int slices = (st->d + kDecodeThreads * kCpt - 1) / (kDecodeThreads * kCpt);
+  const int64_t blocks = static_cast<int64_t>(st->B) * slices;
+  if (blocks >= (1ll << 31)) return PG_ERR_SHAPE;
+  decode_conv_kernel<T, MB><<<static_cast<unsigned>(blocks), kDecodeThreads, 0, stream>>>(
+      st->B, st->d, st->M, slices, static_cast<const T*>(v), alpha, v_ms, gamma_c, conv_w, st->kernel_size,
+      st->dilation, eps, st->pos, static_cast<T*>(st->ring_v), st->ring_alpha, st->ring_ms, st->depth,
+      static_cast<T*>(H), device_error_word());
+  return after_launch(1);
+}
+
+template <typename T>
+pg_status dispatch_decode(const pg_decode_state* st, const void* v, const float* alpha, const float* v_ms,
+                          const float* gamma_c, const float* conv_w, float eps, void* H, cudaStream_t stream) {
+  switch (st->M) {
+    case 1: return launch_decode<T, 1>(st, v, alpha, v_ms, gamma_c, conv_w, eps, H, stream);
+    case 2: return launch_decode<T, 2>(st, v, alpha, v_ms, gamma_c, conv_w, eps, H, stream);
+    case 4: return launch_decode<T, 4>(st, v, alpha, v_ms, gamma_c, conv_w, eps, H, stream);
+    default: return launch_decode<T, 0>(st, v, alpha, v_ms, gamma_c, conv_w, eps, H, stream);
+  }
+}
+
 template <typename T>
 pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, const float* v_ms,
                  const float* gamma_c, const float* conv_w, int ks, int dil, float eps, void* H, cudaStream_t stream) {
@@ -428,4 +614,19 @@ extern "C" pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M
     return launch<__nv_bfloat16>(B, L, d, M, v, alpha, v_ms, gamma_c, conv_w, kernel_size, dilation, eps, H,
                                  stream);
   return launch<float>(B, L, d, M, v, alpha, v_ms, gamma_c, conv_w, kernel_size, dilation, eps, H, stream);
+}
+
+extern "C" pg_status pg_decode_conv_residual(const pg_decode_state* state, const void* v, const float* alpha,
+                                             const float* v_ms, const float* gamma_c, const float* conv_w, float eps,
+                                             void* H, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const pg_status st = decode_state_check(state, true);
+  if (st != PG_OK) return st;
+  if (!v || !alpha || !gamma_c || !conv_w || !H) return PG_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(H)) & 15u) return PG_ERR_ALIGN;
+  if (sm_count() == 0) return cuda_fail(cudaGetLastError());
+  if (state->dtype == PG_BF16)
+    return dispatch_decode<__nv_bfloat16>(state, v, alpha, v_ms, gamma_c, conv_w, eps, H, stream);
+  return dispatch_decode<float>(state, v, alpha, v_ms, gamma_c, conv_w, eps, H, stream);
 }

@@ -65,6 +65,12 @@ struct HashParams {
 
 void fill_hash_params(const pg_table_desc* d, const Geometry& g, HashParams* p);
 
+// ---------------------------------------------------------------- streaming decode state
+
+// PG_OK when `st` is a state pg_decode_state_init could have written (geometry in range,
+// parts present and aligned); need_conv also requires the conv part (M >= 1).
+pg_status decode_state_check(const pg_decode_state* st, bool need_conv);
+
 // ---------------------------------------------------------------- projections without tensor cores
 
 // fp32 out[N, d] = e[N, Din] W[d, Din]^T, plus x + g * out for the scalar gate

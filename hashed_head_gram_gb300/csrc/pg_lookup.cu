@@ -522,6 +522,169 @@ __global__ void __launch_bounds__(256) nf4_quantize_kernel(const float* __restri
   }
 }
 
+// ------------------------------------------------------------------ streaming decode lookup
+
+// One new token per sequence. A warp owns sequence b: with t = pos[b], the window is the
+// token's canonical ID (c_0) and, for 1 <= j <= t, the ID ring's slot (t - j) mod 4 (kPad
+// before the start of the sequence: the same window item_row reads from a [B, L] batch).
+// Lanes < items hash one (order, head) item each; the warp then walks the token's e_t in
+// the gather kernels' units (16-byte chunks of a stored row; NF4: 8-element pieces) with
+// their arithmetic, so e_t is bit-identical to pg_gather_sign_concat's. The ring slot of t
+// and pos (t + 1) are written last, by lane 0, after every lane's reads (no other warp
+// touches b).
+constexpr int kDecodeWarps = 8;
+
+template <int ROWT, int OUTT, bool FLAT>
+__global__ void __launch_bounds__(kDecodeWarps * 32) decode_lookup_kernel(
+    const __grid_constant__ HashParams P, uint64_t seed, const GatherGeom g, int B,
+    const int32_t* __restrict__ tokens, const uint32_t* __restrict__ canon_map, const uint8_t* __restrict__ table,
+    int32_t* __restrict__ pos, uint32_t* __restrict__ ids, uint8_t* __restrict__ e_out, int32_t* err,
+    int* err_word) {
+  __shared__ ItemConst s_ic[kMaxItems];
+  __shared__ float s_nf4[16];
+  __shared__ uint32_t s_rows[kDecodeWarps][kMaxItems];
+  __shared__ uint64_t s_signs[kDecodeWarps][kMaxSignWords];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < g.items) init_item_const(s_ic[threadIdx.x], P, seed, threadIdx.x);
+  if (threadIdx.x < 16) s_nf4[threadIdx.x] = __uint_as_float(c_nf4_bits[threadIdx.x]);
+  __syncthreads();
+  const int items = g.items;
+  const int nw = gridDim.x * kDecodeWarps;
+  for (int b = blockIdx.x * kDecodeWarps + warp; b < B; b += nw) {
+    // pos, the token (then its canonical ID) and the four ring slots are read at once
+    int t = 0;
+    uint32_t c0 = 0, slot_id = 0;
+    if (lane < 4) slot_id = ids[4 * static_cast<int64_t>(b) + lane];
+    if (lane == 0) {
+      t = pos[b];
+      c0 = canon_token(tokens, canon_map, P.vocab, b, err);
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    c0 = __shfl_sync(0xffffffffu, c0, 0);
+    if (t < 0) {  // not a position any call writes: the sequence is left as it is
+      if (lane == 0 && err_word) atomicOr(err_word, 512);
+      continue;
+    }
+    uint64_t c[4];
+    c[0] = c0;
+#pragma unroll
+    for (int j = 1; j < 4; ++j) {
+      const uint32_t id = __shfl_sync(0xffffffffu, slot_id, (t - j) & 3);
+      c[j] = t >= j ? id : kPad;
+    }
+    if (lane < items) {
+      uint64_t hs;
+      s_rows[warp][lane] = item_row_ids(s_ic[lane], P.mode, c, &hs);
+      for (int q = 0; q < g.W; ++q) s_signs[warp][lane * g.W + q] = mix64(hs + kGolden * static_cast<uint64_t>(q + 1));
+    }
+    __syncwarp();
+    const uint32_t* rows = s_rows[warp];
+    const uint64_t* signs = s_signs[warp];
+    uint8_t* out_tok = e_out + static_cast<uint64_t>(b) * g.e_bytes;
+    for (int cc = lane; cc < g.per_tok; cc += 32) {
+      if constexpr (ROWT == PG_NF4) {
+        // piece cc & 7 of item cc >> 3: codes of elements 8 piece .. 8 piece + 7, the row's scale
+        const int it = cc >> 3, piece = cc & 7;
+        const uint8_t* w = table + static_cast<uint64_t>(rows[it]) * 34u;
+        const uint32_t codes = static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t*>(w + 4 * piece))) |
+                               (static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t*>(w + 4 * piece + 2)))
+                                << 16);
+        const float scale = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const uint16_t*>(w + 32))));
+        const uint32_t bits = static_cast<uint32_t>(signs[it * g.W] >> (8 * piece)) & 0xFFu;
+        float x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float val = s_nf4[(codes >> (4 * q)) & 15u] * scale;
+          x[q] = ((bits >> q) & 1u) ? -val : val;
+        }
+        if constexpr (OUTT == PG_F32) {
+          uint8_t* dst = out_tok + cc * 32u;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                                                      __float_as_uint(x[2]), __float_as_uint(x[3]));
+          *reinterpret_cast<uint4*>(dst + 16) = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
+                                                           __float_as_uint(x[6]), __float_as_uint(x[7]));
+        } else {
+          *reinterpret_cast<uint4*>(out_tok + cc * 16u) = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                                                     pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+        }
+      } else {
+        constexpr int E = ROWT == PG_F32 ? 4 : 8;  // elements per 16-byte chunk
+        if constexpr (FLAT) {
+          // chunk cc of the d-wide row of every order, signed and summed in order
+          float acc[E];
+          for (int o = 0; o < items; ++o) {
+            const uint4 x4 = ldg_stream(table + static_cast<uint64_t>(rows[o]) * g.row_bytes + cc * 16u);
+            const uint32_t e0 = cc * E;
+            const uint32_t bb = static_cast<uint32_t>(signs[o * g.W + (e0 >> 6)] >> (e0 & 63)) & ((1u << E) - 1u);
+            float x[E];
+            if constexpr (ROWT == PG_F32) {
+              const uint4 f = xor4(x4, f32_sign_mask(bb));
+              x[0] = __uint_as_float(f.x); x[1] = __uint_as_float(f.y);
+              x[2] = __uint_as_float(f.z); x[3] = __uint_as_float(f.w);
+            } else {
+              const uint4 f = xor4(x4, bf16_sign_mask(bb));
+              x[0] = bf16_lo(f.x); x[1] = bf16_hi(f.x); x[2] = bf16_lo(f.y); x[3] = bf16_hi(f.y);
+              x[4] = bf16_lo(f.z); x[5] = bf16_hi(f.z); x[6] = bf16_lo(f.w); x[7] = bf16_hi(f.w);
+            }
+#pragma unroll
+            for (int q = 0; q < E; ++q) acc[q] = (o == 0) ? x[q] : __fadd_rn(acc[q], x[q]);
+          }
+          if constexpr (OUTT == PG_F32) {
+#pragma unroll
+            for (int q = 0; q < E; q += 4)
+              *reinterpret_cast<uint4*>(out_tok + (cc * E + q) * 4u) =
+                  make_uint4(__float_as_uint(acc[q]), __float_as_uint(acc[q + 1]), __float_as_uint(acc[q + 2]),
+                             __float_as_uint(acc[q + 3]));
+          } else {
+            *reinterpret_cast<uint4*>(out_tok + cc * 16u) =
+                make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                           pack_bf16(acc[6], acc[7]));
+          }
+        } else {
+          const uint32_t it = cc / g.rc, piece = cc - it * g.rc;
+          const uint4 v = ldg_stream(table + static_cast<uint64_t>(rows[it]) * g.row_bytes + piece * 16u);
+          const uint32_t e0 = piece * E;
+          const uint32_t bb = static_cast<uint32_t>(signs[it * g.W + (e0 >> 6)] >> (e0 & 63)) & ((1u << E) - 1u);
+          if constexpr (ROWT == PG_F32) {
+            *reinterpret_cast<uint4*>(out_tok + cc * 16u) = xor4(v, f32_sign_mask(bb));
+          } else if constexpr (OUTT == PG_BF16) {
+            *reinterpret_cast<uint4*>(out_tok + cc * 16u) = xor4(v, bf16_sign_mask(bb));
+          } else {
+            const uint4 f = xor4(v, bf16_sign_mask(bb));
+            uint8_t* dst = out_tok + cc * 32u;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(f.x << 16, f.x & 0xFFFF0000u, f.y << 16, f.y & 0xFFFF0000u);
+            *reinterpret_cast<uint4*>(dst + 16) =
+                make_uint4(f.z << 16, f.z & 0xFFFF0000u, f.w << 16, f.w & 0xFFFF0000u);
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane is done with s_rows / s_signs and has read pos and the ring
+    if (lane == 0) {
+      ids[4 * static_cast<int64_t>(b) + (t & 3)] = c0;
+      pos[b] = t + 1;
+    }
+  }
+}
+
+using DecodeFn = void (*)(const HashParams, uint64_t, const GatherGeom, int, const int32_t*, const uint32_t*,
+                          const uint8_t*, int32_t*, uint32_t*, uint8_t*, int32_t*, int*);
+
+DecodeFn pick_decode(int row_dtype, int out_dtype, bool flat) {
+  if (flat) {
+    if (row_dtype == PG_F32 && out_dtype == PG_F32) return decode_lookup_kernel<PG_F32, PG_F32, true>;
+    if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return decode_lookup_kernel<PG_BF16, PG_BF16, true>;
+    if (row_dtype == PG_BF16 && out_dtype == PG_F32) return decode_lookup_kernel<PG_BF16, PG_F32, true>;
+    return nullptr;
+  }
+  if (row_dtype == PG_F32 && out_dtype == PG_F32) return decode_lookup_kernel<PG_F32, PG_F32, false>;
+  if (row_dtype == PG_BF16 && out_dtype == PG_BF16) return decode_lookup_kernel<PG_BF16, PG_BF16, false>;
+  if (row_dtype == PG_BF16 && out_dtype == PG_F32) return decode_lookup_kernel<PG_BF16, PG_F32, false>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_BF16) return decode_lookup_kernel<PG_NF4, PG_BF16, false>;
+  if (row_dtype == PG_NF4 && out_dtype == PG_F32) return decode_lookup_kernel<PG_NF4, PG_F32, false>;
+  return nullptr;
+}
+
 }  // namespace
 }  // namespace pg
 
@@ -639,6 +802,54 @@ pg_status pg_nf4_quantize(const float* x, int64_t nrows, int32_t r, void* out, p
   const int64_t cap = static_cast<int64_t>(nsm) * 8;
   const int blocks = static_cast<int>(want < cap ? want : cap);
   nf4_quantize_kernel<<<blocks, 256, 0, stream>>>(x, nrows, static_cast<uint8_t*>(out));
+  return after_launch(1);
+}
+
+pg_status pg_decode_lookup(const pg_table_desc* desc, const pg_decode_state* state, const int32_t* tokens,
+                           const uint32_t* canon_map, const void* table, uint64_t table_bytes, void* e_out,
+                           int32_t out_dtype, int32_t* err_index, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  Geometry geo;
+  pg_status st = validate_desc(desc, &geo);
+  if (st != PG_OK) return st;
+  if (desc->hash_kind != PG_HASH_MULXOR) return PG_ERR_UNSUPPORTED;
+  st = decode_state_check(state, false);
+  if (st != PG_OK) return st;
+  if (!tokens || !table || !e_out) return PG_ERR_NULL;
+  if (table_bytes < geo.rows * geo.row_bytes) return PG_ERR_RANGE;
+  if (reinterpret_cast<uintptr_t>(table) % 16 || reinterpret_cast<uintptr_t>(e_out) % 16) return PG_ERR_ALIGN;
+  if (out_dtype != PG_F32 && out_dtype != PG_BF16) return PG_ERR_DTYPE;
+  const bool flat = desc->mode == PG_FLAT;
+  const int items = geo.O * geo.H;
+  if (items > kMaxItems || items * geo.W > kMaxSignWords) return PG_ERR_UNSUPPORTED;
+  if (desc->row_dtype != PG_NF4 && geo.row_bytes % 16) return PG_ERR_UNSUPPORTED;
+  DecodeFn fn = pick_decode(desc->row_dtype, out_dtype, flat);
+  if (!fn) return desc->row_dtype == PG_F32 && out_dtype == PG_BF16 ? PG_ERR_DTYPE : PG_ERR_UNSUPPORTED;
+
+  GatherGeom g{};
+  g.N = state->B;
+  g.items = items;
+  g.W = geo.W;
+  g.rc = desc->row_dtype == PG_NF4 ? 8u : geo.row_bytes / 16u;
+  g.per_tok = flat ? static_cast<int>(g.rc) : items * static_cast<int>(g.rc);
+  g.row_bytes = geo.row_bytes;
+  g.e_bytes = geo.e_width * (out_dtype == PG_F32 ? 4u : 2u);
+  g.table_bytes = table_bytes;
+
+  const int nsm = sm_count();
+  if (nsm == 0) return cuda_fail(cudaGetLastError());
+  st = prepare_err(err_index, stream);
+  if (st != PG_OK) return st;
+  HashParams P;
+  fill_hash_params(desc, geo, &P);
+  const int64_t want = (static_cast<int64_t>(state->B) + kDecodeWarps - 1) / kDecodeWarps;
+  const int64_t cap = static_cast<int64_t>(nsm) * 8;
+  const int blocks = static_cast<int>(want < cap ? want : cap);
+  fn<<<blocks, kDecodeWarps * 32, 0, stream>>>(P, desc->hash_seed, g, state->B, tokens, canon_map,
+                                               static_cast<const uint8_t*>(table), state->pos, state->ids,
+                                               static_cast<uint8_t*>(e_out), err_index,
+                                               device_error_word());
   return after_launch(1);
 }
 

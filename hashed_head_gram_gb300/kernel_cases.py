@@ -1,6 +1,6 @@
 """Single-kernel runs on a workload's shapes, for timing and profiling one kernel at a time.
 
-    python -m hashed_head_gram_gb300.kernel_cases {gather,project,project_fp8,gather_project,conv,nf4_export} --config C [--iters N]
+    python -m hashed_head_gram_gb300.kernel_cases {gather,project,project_fp8,gather_project,conv,nf4_export,decode} --config C [--iters N]
 
 Inputs are synthetic and seeded (the conv and projection cases need no table, so they
 hold at most a few GB on the device); each launch goes through the C ABI exactly as the
@@ -42,7 +42,9 @@ def _time(fn, iters: int, dev) -> float:
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("kernel", choices=["gather", "project", "project_fp8", "gather_project", "conv", "nf4_export"])
+    ap.add_argument("kernel", choices=["gather", "project", "project_fp8", "gather_project", "conv", "nf4_export",
+                                       "decode"])
+    ap.add_argument("--batch", default="1,16,256,4096", help="decode: sequences per step (comma list)")
     ap.add_argument("--rows", type=int, default=8 << 20, help="nf4_export: fp32 head rows to export")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--iters", type=int, default=20)
@@ -54,6 +56,9 @@ def main(argv=None):
     dt = torch.float32 if w.dtype == W.DT_F32 else torch.bfloat16
     code = pg.F32 if w.dtype == W.DT_F32 else pg.BF16
     N, din, d, M = w.N, spec.e_width, w.d, w.M
+    if args.kernel == "decode":
+        _decode(w, args, dev, g)
+        return
     if args.kernel == "gather":
         desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
         tokens = torch.from_numpy(W.make_tokens(w)).to(dev)
@@ -148,6 +153,80 @@ def main(argv=None):
                                             eps=w.eps, v_ms=v_ms), args.iters, dev)
         byts = N * d * v.element_size() * (1 + 2 * M)
         print(f"conv_residual config {w.cfg_id}: {us:.1f} us, {byts / us / 1e3:.0f} GB/s")
+
+
+def _decode(w, args, dev, g):
+    """Streaming decode steps, one token per sequence: pg_decode_lookup, the projection
+    (N = B) and, in the context-gated module, pg_decode_conv_residual. Timed per step
+    (eager, L2 flushed between steps) and as a CUDA graph of 16 consecutive steps replayed
+    back to back (the table rows stay cold, W and the state stay in L2 as in serving)."""
+    spec = w.tables[0]
+    d, M, din = w.d, w.M, spec.e_width
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    cm = W.make_canon_map(w)
+    cm = None if cm is None else torch.from_numpy(cm.view("int32")).to(dev)
+    table = W.make_table(w, spec, dev)
+    Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    steps = 16
+    for B in [int(x) for x in args.batch.split(",")]:
+        tokens = torch.randint(0, w.vocab, (steps, B), device=dev, generator=g, dtype=torch.int32)
+        e = torch.empty(B, din, dtype=torch.bfloat16, device=dev)
+        v = torch.empty(B, d, dtype=torch.bfloat16, device=dev)
+        ctx = w.gate == W.GATE_CONTEXT
+        state = pg.DecodeState(B, d=d if ctx else 0, M=M if ctx else 0, dtype=pg.BF16, kernel_size=w.conv_kernel,
+                               dilation=w.dilation, device=dev)
+        if ctx:
+            H = torch.randn(M, B, d, device=dev, generator=g).to(torch.bfloat16)
+            one = torch.ones(d, device=dev)
+            cw = torch.randn(d, w.conv_kernel, device=dev, generator=g) * 0.25
+            alpha = torch.empty(M, B, device=dev)
+            v_ms = torch.empty(B, device=dev)
+            ws = torch.empty(pg.workspace_size(B, din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4 + 4, device=dev)
+            calls = [
+                lambda s: pg.decode_lookup(desc, state, tokens[s], table, e, pg.BF16, canon_map=cm),
+                lambda s: pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=H, gamma_h=one, gamma_k=one,
+                                          alpha_out=alpha, workspace=ws, v_ms_out=v_ms),
+                lambda s: pg.decode_conv_residual(state, v, alpha, one, cw, H, eps=w.eps, v_ms=v_ms),
+            ]
+            names = ["decode_lookup", "project_gate(context)", "decode_conv_residual"]
+        else:
+            x = torch.randn(B, d, device=dev, generator=g).to(torch.bfloat16)
+            gate = pg.GATE_SCALAR if w.gate == W.GATE_SCALAR else pg.GATE_NONE
+            calls = [
+                lambda s: pg.decode_lookup(desc, state, tokens[s], table, e, pg.BF16, canon_map=cm),
+                lambda s: pg.project_gate(e, Wm, d, gate, v, pg.BF16, g=w.g,
+                                          x_resid=x if gate == pg.GATE_SCALAR else None),
+            ]
+            names = ["decode_lookup", "project_gate"]
+        step = lambda s=0: [c(s) for c in calls]
+        eager = _time(step, args.iters, dev)
+        parts = [_time(lambda c=c: c(0), args.iters, dev) for c in calls]
+        # a graph of `steps` consecutive steps
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for s in range(steps):
+                step(s)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for s in range(steps):
+                step(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, args.iters // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        per_step = a.elapsed_time(b) * 1e3 / (reps * steps)
+        if pg.device_error() != 0:
+            raise SystemExit("device error word set")
+        print(f"decode config {w.cfg_id} B={B}: eager step {eager:.1f} us ({' + '.join(f'{n} {u:.1f}' for n, u in zip(names, parts))}); "
+              f"graph {per_step:.1f} us/step, {B / per_step:.3f} M tokens/s")
 
 
 if __name__ == "__main__":

@@ -59,6 +59,24 @@ class TableDesc(ctypes.Structure):
     ]
 
 
+class DecodeStateC(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("M", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("kernel_size", ctypes.c_int32),
+        ("dilation", ctypes.c_int32),
+        ("depth", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("pos", ctypes.c_void_p),
+        ("ids", ctypes.c_void_p),
+        ("ring_v", ctypes.c_void_p),
+        ("ring_alpha", ctypes.c_void_p),
+        ("ring_ms", ctypes.c_void_p),
+    ]
+
+
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"libpg.so is not built ({_LIB_PATH}); run `python -m hashed_head_gram_gb300.build`")
@@ -101,6 +119,17 @@ def _load():
     L.pg_nf4_quantize.argtypes = [vp, ctypes.c_int64, i32, vp, vp]
     L.pg_project_gate_context_noalloc.restype = ctypes.c_int
     L.pg_project_gate_context_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, f32, vp, vp, vp]
+    sp = ctypes.POINTER(DecodeStateC)
+    L.pg_decode_state_size.restype = ctypes.c_int
+    L.pg_decode_state_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(u64)]
+    L.pg_decode_state_init.restype = ctypes.c_int
+    L.pg_decode_state_init.argtypes = [sp, vp, u64, i32, i32, i32, i32, i32, i32, vp]
+    L.pg_decode_reset.restype = ctypes.c_int
+    L.pg_decode_reset.argtypes = [sp, vp, i32, vp]
+    L.pg_decode_lookup.restype = ctypes.c_int
+    L.pg_decode_lookup.argtypes = [dp, sp, vp, vp, vp, u64, vp, i32, vp, vp]
+    L.pg_decode_conv_residual.restype = ctypes.c_int
+    L.pg_decode_conv_residual.argtypes = [sp, vp, vp, vp, vp, vp, f32, vp, vp]
     L.pg_conv_residual.restype = ctypes.c_int
     L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp]
     return L
@@ -300,6 +329,83 @@ def conv_residual(B: int, L: int, d: int, M: int, dtype: int, v: torch.Tensor, a
            "pg_conv_residual")
 
 
+def decode_state_size(B: int, d: int = 0, M: int = 0, dtype: int = BF16, kernel_size: int = 4,
+                      dilation: int = 3) -> int:
+    n = ctypes.c_uint64()
+    _check(_lib.pg_decode_state_size(B, d, M, dtype, kernel_size, dilation, ctypes.byref(n)),
+           "pg_decode_state_size")
+    return n.value
+
+
+class DecodeState:
+    """A decode state and the device buffer it lives in (pg_decode_state_init zeroes it:
+    B empty sequences). `pos`, `ids`, `ring_v`, `ring_alpha` and `ring_ms` are views of the
+    buffer's parts, for inspection and for restarting sequences by hand."""
+
+    def __init__(self, B: int, d: int = 0, M: int = 0, dtype: int = BF16, kernel_size: int = 4,
+                 dilation: int = 3, device=None, stream=None):
+        nbytes = decode_state_size(B, d, M, dtype, kernel_size, dilation)
+        self.buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or torch.device("cuda"))
+        base = (-self.buf.data_ptr()) % 256
+        self.mem = self.buf[base:base + nbytes]
+        self.c = DecodeStateC()
+        _check(_lib.pg_decode_state_init(ctypes.byref(self.c), _ptr(self.mem), nbytes, B, d, M, dtype, kernel_size,
+                                         dilation, _stream(stream)), "pg_decode_state_init")
+
+    def _part(self, ptr, count, dtype):
+        if not ptr or count == 0:
+            return None
+        off = ptr - self.mem.data_ptr()
+        nbytes = count * torch.empty(0, dtype=dtype).element_size()
+        return self.mem[off:off + nbytes].view(dtype)
+
+    @property
+    def pos(self):
+        return self._part(self.c.pos, self.c.B, torch.int32)
+
+    @property
+    def ids(self):
+        return self._part(self.c.ids, self.c.B * 4, torch.int32).view(self.c.B, 4)
+
+    @property
+    def ring_v(self):
+        t = self._part(self.c.ring_v, self.c.B * self.c.depth * self.c.d,
+                       torch.float32 if self.c.dtype == F32 else torch.bfloat16)
+        return None if t is None else t.view(self.c.B, self.c.depth, self.c.d)
+
+    @property
+    def ring_alpha(self):
+        t = self._part(self.c.ring_alpha, self.c.B * self.c.depth * self.c.M, torch.float32)
+        return None if t is None else t.view(self.c.B, self.c.depth, self.c.M)
+
+    @property
+    def ring_ms(self):
+        t = self._part(self.c.ring_ms, self.c.B * self.c.depth, torch.float32)
+        return None if t is None else t.view(self.c.B, self.c.depth)
+
+
+def decode_reset(state: DecodeState, slots: torch.Tensor, stream=None):
+    _check(_lib.pg_decode_reset(ctypes.byref(state.c), _ptr(slots), slots.numel(), _stream(stream)),
+           "pg_decode_reset")
+
+
+def decode_lookup(desc: TableDesc, state: DecodeState, tokens: torch.Tensor, table: torch.Tensor,
+                  e_out: torch.Tensor, out_dtype: int, canon_map: Optional[torch.Tensor] = None,
+                  err_index: Optional[torch.Tensor] = None, stream=None):
+    nbytes = table.numel() * table.element_size()
+    _check(_lib.pg_decode_lookup(ctypes.byref(desc), ctypes.byref(state.c), _ptr(tokens), _ptr(canon_map),
+                                 _ptr(table), nbytes, _ptr(e_out), out_dtype, _ptr(err_index), _stream(stream)),
+           "pg_decode_lookup")
+
+
+def decode_conv_residual(state: DecodeState, v: torch.Tensor, alpha: torch.Tensor, gamma_c: torch.Tensor,
+                         conv_w: torch.Tensor, H: torch.Tensor, eps: float = 1e-6,
+                         v_ms: Optional[torch.Tensor] = None, stream=None):
+    _check(_lib.pg_decode_conv_residual(ctypes.byref(state.c), _ptr(v), _ptr(alpha), _ptr(v_ms), _ptr(gamma_c),
+                                        _ptr(conv_w), eps, _ptr(H), _stream(stream)),
+           "pg_decode_conv_residual")
+
+
 def launch_count() -> int:
     return int(_lib.pg_launch_count())
 
@@ -316,6 +422,8 @@ def dtype_code(t: torch.dtype) -> int:
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
-           "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual", "launch_count", "device_error", "lib",
+           "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual",
+           "decode_state_size", "DecodeState", "decode_reset", "decode_lookup", "decode_conv_residual",
+           "launch_count", "device_error", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

@@ -131,7 +131,9 @@ uint64_t pg_launch_count(void);
  * waits that gave up in the projection kernels (1 = TMA producer, 2 = MMA issuer,
  * 4 = epilogue, 8 = epilogue operand producer, 16 = gather warps of
  * pg_lookup_project_gate, 64 = a tile's wait for its rows of e_t in
- * pg_gather_project_gate, 128 = that call's gather warps or their coordinator).
+ * pg_gather_project_gate, 128 = that call's gather warps or their coordinator), and
+ * of decode-state checks (256 = pg_decode_reset met a slot outside [0, B), 512 = a
+ * decode call met a position it cannot take; that sequence was skipped, left unchanged).
  * Synchronizes the device. With clear != 0 the word is reset to 0.
  */
 pg_status pg_device_error(int32_t* code, int32_t clear);
@@ -370,6 +372,110 @@ pg_status pg_project_gate_context_noalloc(int32_t N, int32_t Din, int32_t d, int
                                           const void* e, const void* W, const void* h,
                                           const float* gamma_h, const float* gamma_k, float eps,
                                           void* v_out, float* alpha_out, pg_stream_t stream);
+
+/*
+ * Streaming decode (one new token per sequence and call).
+ *
+ * Each sequence's lookup reads only its suffix n-gram (the last max(orders) - 1 canonical
+ * IDs and the new one), and the causal conv reads only the inputs of the last
+ * (kernel_size - 1) * dilation positions. Both are known before the step runs, since
+ * addressing depends on the token IDs alone (Engram notes 3.5; PageGram report 3.3 on
+ * prefetching). A decode state keeps exactly that per sequence, so a step over B
+ * sequences costs B tokens' lookups, not a re-run of the prefix. A sequence's outputs at
+ * position t equal those of the full-sequence calls at position t: pg_decode_lookup's e_t
+ * is bit-identical to pg_gather_sign_concat's, and pg_decode_conv_residual's update of H
+ * is bit-identical to pg_conv_residual's when given the same v, alpha and v_ms.
+ *
+ * State layout (device memory, carved from one caller-owned buffer by pg_decode_state_init):
+ *   pos         int32  [B]        tokens of the sequence consumed so far
+ *   ids         uint32 [B][4]     canonical ID of position p in slot p mod 4
+ *   ring_v      dtype  [B][D][d]  v of position p in slot p mod D
+ *   ring_alpha  fp32   [B][D][M]  alpha[m] of position p in slot p mod D
+ *   ring_ms     fp32   [B][D]     mean(v_p^2) in slot p mod D
+ * with D = (kernel_size - 1) * dilation + 1 (0 when kernel_size == 1): the conv inputs of
+ * the last D - 1 positions, which the next output reads (9 for kernel 4, dilation 3), and
+ * the slot the current position's input goes to, so that no block of a launch reads a
+ * slot another block of it writes. Slots of positions before the start of a sequence are
+ * never read, so an all-zero state (what pg_decode_state_init writes) is B empty
+ * sequences, and setting pos[b] = 0 (pg_decode_reset) restarts sequence b. Sequences
+ * advance independently: each reads its own pos, so a batch may hold sequences at
+ * different positions.
+ *
+ * One decode step, on one stream:
+ *   pg_decode_lookup                 -- consumes token b at t = pos[b]; pos[b] = t + 1
+ *   pg_project_gate(N = B, ...)      -- the projection and gate of these tokens
+ *   pg_decode_conv_residual          -- context-gate (multi-branch) path: position pos[b] - 1
+ */
+typedef struct {
+  int32_t B;            /* sequences */
+  int32_t d;            /* conv channels (model width); 0 when the state has no conv part */
+  int32_t M;            /* branches; 0 when the state has no conv part */
+  int32_t dtype;        /* PG_BF16 or PG_F32: dtype of v and ring_v */
+  int32_t kernel_size;  /* 1..4 */
+  int32_t dilation;     /* 1..8 */
+  int32_t depth;        /* D above, filled in by pg_decode_state_init */
+  int32_t reserved;
+  int32_t* pos;
+  uint32_t* ids;
+  void* ring_v;
+  float* ring_alpha;
+  float* ring_ms;
+} pg_decode_state;
+
+/*
+ * Bytes of the device buffer a decode state needs (host-only arithmetic; every part
+ * starts on a 256-byte boundary). M == 0 (with d == 0) sizes a lookup-only state.
+ * PG_ERR_SHAPE / PG_ERR_DTYPE for arguments outside the ranges above.
+ */
+pg_status pg_decode_state_size(int32_t B, int32_t d, int32_t M, int32_t dtype, int32_t kernel_size,
+                               int32_t dilation, uint64_t* bytes);
+
+/*
+ * Fills *state with the geometry and the pointers of its parts inside `buffer` (device,
+ * 256-byte aligned, >= pg_decode_state_size bytes, owned by the caller and used by the
+ * state until the caller frees it) and zeroes the buffer on `stream` (B empty sequences).
+ */
+pg_status pg_decode_state_init(pg_decode_state* state, void* buffer, uint64_t buffer_bytes, int32_t B,
+                               int32_t d, int32_t M, int32_t dtype, int32_t kernel_size, int32_t dilation,
+                               pg_stream_t stream);
+
+/*
+ * Restarts the listed sequences: pos[slots[i]] = 0 for i < n (slots: device int32 [n]).
+ * A slot outside [0, B) is skipped and reported as device error bit 256.
+ */
+pg_status pg_decode_reset(const pg_decode_state* state, const int32_t* slots, int32_t n, pg_stream_t stream);
+
+/*
+ * pg_decode_lookup -- steps 1-6 for one new token per sequence: tokens device int32 [B]
+ * (token b continues sequence b at position t = pos[b]); e_out device [B, width] as
+ * pg_gather_sign_concat's (out_dtype PG_F32 or PG_BF16; NF4 tables dequantised).
+ * Writes ids[b][t mod 4] = the token's canonical ID and pos[b] = t + 1. Orders up to 4
+ * (the ID ring holds the 3 IDs before t). Descriptor, table and err_index as in
+ * pg_gather_sign_concat (err_index gets the smallest b whose token is out of range; that
+ * token reads as ID 0). Multiply-XOR hashing only. A negative pos[b] is reported as
+ * device error bit 512 and sequence b is skipped (e_out row, ids and pos left as they are).
+ */
+pg_status pg_decode_lookup(const pg_table_desc* desc, const pg_decode_state* state, const int32_t* tokens,
+                           const uint32_t* canon_map, const void* table, uint64_t table_bytes, void* e_out,
+                           int32_t out_dtype, int32_t* err_index, pg_stream_t stream);
+
+/*
+ * pg_decode_conv_residual -- step 8 for the position t = pos[b] - 1 of each sequence (the
+ * token the step's pg_decode_lookup consumed):
+ *   u = alpha[m, b] v_b;  z = RMSNorm(u) with gamma_c;
+ *   c = sum_{j < kernel_size} conv_w[:, j] * z_{t - j*dilation}  (terms before t = 0 are 0;
+ *       the earlier z come from the state's ring)
+ *   H[m, b] <- H[m, b] + SiLU(c) + u
+ * and stores v_b, alpha[:, b] and mean(v_b^2) in ring slot t mod D. pos is not changed.
+ *  v  device [B, d] (state dtype, 16-byte aligned); alpha device fp32 [M, B];
+ *  v_ms  optional device fp32 [B] (pg_project_gate's v_ms_out); computed from v when NULL
+ *  gamma_c, conv_w  device fp32 [d], [d, kernel_size]; H device [M, B, d] (state dtype)
+ *  The state must have a conv part (M >= 1, d % 8 == 0, d <= 8192). pos[b] < 1 is
+ *  reported as device error bit 512 and sequence b is skipped (H and the ring unchanged).
+ */
+pg_status pg_decode_conv_residual(const pg_decode_state* state, const void* v, const float* alpha,
+                                  const float* v_ms, const float* gamma_c, const float* conv_w, float eps,
+                                  void* H, pg_stream_t stream);
 
 #ifdef __cplusplus
 }

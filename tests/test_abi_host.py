@@ -116,3 +116,62 @@ def test_workspace_size_query(pg):
     # per (branch, 256-column tile) partial sums, + the v tiles' row sums that v_ms_out needs
     assert pg.workspace_size(32768, 1280, 2560, 4, pg.BF16, pg.GATE_CONTEXT) == (4 * 10 * 3 + 10) * 32768 * 4
     assert pg.workspace_size(65536, 1024, 768, 0, pg.BF16, pg.GATE_SCALAR) == 0
+
+
+def test_decode_state_layout_matches_the_header(pg, tmp_path):
+    src = tmp_path / "ds.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "pg.h"\n'
+                   'int main(void){printf("%zu %zu %zu %zu\\n", sizeof(pg_decode_state),'
+                   ' offsetof(pg_decode_state, pos), offsetof(pg_decode_state, ring_v),'
+                   ' offsetof(pg_decode_state, ring_ms)); return 0;}\n')
+    exe = tmp_path / "ds"
+    subprocess.check_call(["gcc", "-I" + os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    size, pos_off, rv_off, rms_off = map(int, subprocess.check_output([str(exe)]).split())
+    T = pg.DecodeStateC
+    assert ctypes.sizeof(T) == size and T.pos.offset == pos_off
+    assert T.ring_v.offset == rv_off and T.ring_ms.offset == rms_off
+
+
+def test_decode_state_size_arithmetic(pg):
+    # parts pos [B] i32, ids [B][4] u32, ring_v [B][R][d], ring_alpha [B][R][M] f32,
+    # ring_ms [B][R] f32, each rounded up to 256 bytes; R = (kernel - 1) * dilation + 1
+    up = lambda x: (x + 255) // 256 * 256
+    assert pg.decode_state_size(5) == up(20) + up(80)                      # lookup only
+    B, d, M, R = 3, 2560, 4, 10                                             # Engram-27B module
+    assert pg.decode_state_size(B, d, M, pg.BF16, 4, 3) == (
+        up(4 * B) + up(16 * B) + up(B * R * d * 2) + up(B * R * M * 4) + up(B * R * 4))
+    assert pg.decode_state_size(2, 64, 1, pg.F32, 4, 8) == up(8) + up(32) + up(2 * 25 * 64 * 4) + up(2 * 25 * 4) * 2
+    assert pg.decode_state_size(2, 64, 1, pg.F32, 1, 3) == up(8) + up(32)   # kernel 1: no ring
+
+
+def test_decode_state_validation(pg):
+    L = pg.lib()
+    n = ctypes.c_uint64()
+    assert L.pg_decode_state_size(0, 0, 0, pg.BF16, 4, 3, ctypes.byref(n)) == 2      # B < 1
+    assert L.pg_decode_state_size(2, 12, 1, pg.BF16, 4, 3, ctypes.byref(n)) == 2     # d % 8
+    assert L.pg_decode_state_size(2, 16, 0, pg.BF16, 4, 3, ctypes.byref(n)) == 2     # d without M
+    assert L.pg_decode_state_size(2, 16, 9, pg.BF16, 4, 3, ctypes.byref(n)) == 2     # M > 8
+    assert L.pg_decode_state_size(2, 16, 1, pg.NF4, 4, 3, ctypes.byref(n)) == 3      # dtype
+    assert L.pg_decode_state_size(2, 16, 1, pg.BF16, 5, 3, ctypes.byref(n)) == 2     # kernel > 4
+    assert L.pg_decode_state_size(2, 16, 1, pg.BF16, 4, 9, ctypes.byref(n)) == 2     # dilation > 8
+    assert L.pg_decode_state_size(2, 16, 1, pg.BF16, 4, 3, None) == 1
+    assert L.pg_decode_state_init(None, None, 0, 2, 0, 0, pg.BF16, 4, 3, None) == 1
+    st = pg.DecodeStateC()
+    assert L.pg_decode_state_init(ctypes.byref(st), ctypes.c_void_p(256), 16, 2, 0, 0, pg.BF16, 4, 3, None) == 8
+    assert L.pg_decode_state_init(ctypes.byref(st), ctypes.c_void_p(260), 4096, 2, 0, 0, pg.BF16, 4, 3, None) == 5
+    # calls check the state before anything else: missing parts, a conv call on a
+    # lookup-only state, a ring depth that disagrees with the conv
+    spec = W.make_workload(2).tables[0]
+    d = pg.table_desc(spec, 50304)
+    st = pg.DecodeStateC(B=2, d=0, M=0, dtype=pg.BF16, kernel_size=4, dilation=3, depth=0)
+    assert L.pg_decode_lookup(ctypes.byref(d), ctypes.byref(st), None, None, None, 0, None, 1, None, None) == 1
+    st.pos, st.ids = 256, 512
+    assert L.pg_decode_conv_residual(ctypes.byref(st), None, None, None, None, None, 1e-6, None, None) == 2
+    st = pg.DecodeStateC(B=2, d=64, M=1, dtype=pg.BF16, kernel_size=4, dilation=3, depth=9, pos=256, ids=512)
+    assert L.pg_decode_conv_residual(ctypes.byref(st), None, None, None, None, None, 1e-6, None, None) == 2
+    st.depth = 10
+    assert L.pg_decode_conv_residual(ctypes.byref(st), None, None, None, None, None, 1e-6, None, None) == 1
+    ok = pg.DecodeStateC(B=2, d=0, M=0, dtype=pg.BF16, kernel_size=4, dilation=3, depth=0, pos=256, ids=512)
+    assert L.pg_decode_reset(ctypes.byref(ok), None, -1, None) == 2
+    assert L.pg_decode_reset(ctypes.byref(ok), None, 0, None) == 0
+    assert L.pg_decode_reset(ctypes.byref(ok), None, 3, None) == 1
