@@ -390,14 +390,17 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
 
 // ------------------------------------------------------------------ streaming decode
 
-// Position t = pos[b] - 1 of each sequence. Block (b, slice) owns 512 channels of sequence
-// b, thread i channels [4 i, 4 i + 4) of the slice. The inputs that do not depend on t (v_t,
-// H of the M branches, the conv taps) are requested first, while thread 0 reads pos; the
-// tap scalars of the earlier positions then come from the ring (slot p mod D holds v_p,
-// alpha_{:, p}, mean(v_p^2)). Every product, FMA and the SiLU are the full-sequence
-// kernel's, in its order, so H gets the same update. The ring has one slot more than the
-// taps reach, so the slot of t, written here (v by each thread for its channels, the
-// scalars by slice 0), is read by no block of this launch.
+// Position t = pos[b] - 1 of each sequence. A persistent grid of blocks, block i owning
+// channel slice i mod slices (512 channels, thread j channels [4 j, 4 j + 4)) of every
+// (gridDim / slices)-th sequence: the conv taps are loaded once per block, and each
+// sequence's pos is read one sequence ahead. Per sequence, every thread issues at once
+// what the output needs: v_t, H of the M branches, the earlier inputs from the ring (slot
+// p mod D holds v_p, alpha_{:, p}, mean(v_p^2)) and, in threads < 4 M, the tap scalars;
+// one barrier publishes the scalars (double-buffered by processed sequence, so the next
+// sequence's writes never meet this one's reads). Every product, FMA and the SiLU are the
+// full-sequence kernel's, in its order, so H gets the same update. The ring has one slot
+// more than the taps reach, so the slot of t, written here (v by each thread for its
+// channels, the scalars by slice 0), is read by no block of this launch.
 constexpr int kDecodeThreads = 128;
 
 template <typename T, int MB>
@@ -410,127 +413,131 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
   const int M = MB > 0 ? MB : M_rt;
   using Vec = VecN<T, kCpt>;
   constexpr int kPairs = kCpt / 2;
-  __shared__ float s_f[kMaxBranches][kTaps];
-  __shared__ float s_a[kMaxBranches];
-  __shared__ float s_ms_t;
-  __shared__ int s_t;
-  const int b = blockIdx.x / slices, slice = blockIdx.x - (blockIdx.x / slices) * slices;
+  __shared__ float s_f[2][kMaxBranches][kTaps];
+  __shared__ float s_a[2][kMaxBranches];
+  __shared__ float s_ms_t[2];
+  const int slice = blockIdx.x % slices;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c0 = (slice * kDecodeThreads + threadIdx.x) * kCpt;
   const bool active = c0 < d;
-  const int64_t row_b = static_cast<int64_t>(b) * d;
+  const int bstride = gridDim.x / slices;
 
-  // 1. what does not depend on t: v_t, H, the taps; t itself and mean(v_t^2)
-  if (threadIdx.x == 0) {
-    s_t = pos[b] - 1;
-    if (v_ms) s_ms_t = v_ms[b];
-  }
-  typename Vec::Raw vt = Vec::zero();
-  typename Vec::Raw hraw[MMAX];
+  // conv taps with the RMSNorm gain and SiLU's half-argument folded in (as the full kernel)
   uint64_t wg[kTaps][kPairs];
-  if (active) {
-    vt = Vec::load(v + row_b + c0);
 #pragma unroll
-    for (int m = 0; m < MMAX; ++m)
-      if (m < M) hraw[m] = Vec::load_rw(H + (static_cast<int64_t>(m) * B + b) * d + c0);
+  for (int q = 0; q < kPairs; ++q) {
+    float g[2], w[kTaps][2];
 #pragma unroll
-    for (int q = 0; q < kPairs; ++q) {
-      float g[2], w[kTaps][2];
+    for (int e = 0; e < 2; ++e) {
+      const int c = c0 + 2 * q + e;
+      g[e] = active ? 0.5f * gamma_c[c] : 0.f;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int c = c0 + 2 * q + e;
-        g[e] = 0.5f * gamma_c[c];
-#pragma unroll
-        for (int j = 0; j < kTaps; ++j) w[j][e] = j < ks ? conv_w[c * ks + j] * g[e] : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < kTaps; ++j) wg[j][q] = pk(w[j][0], w[j][1]);
+      for (int j = 0; j < kTaps; ++j) w[j][e] = (active && j < ks) ? conv_w[c * ks + j] * g[e] : 0.f;
     }
-  }
-  if (!v_ms && warp == 0) {
-    const float s = row_mean_square(v + row_b, d >> 3, 1.0f / static_cast<float>(d), lane);
-    if (lane == 0) s_ms_t = s;
-  }
-  __syncthreads();
-  const int t = s_t;
-  if (t < 0) {  // pos[b] < 1: no token consumed to apply the conv to
-    if (threadIdx.x == 0 && slice == 0 && err_word) atomicOr(err_word, 512);
-    return;
-  }
-  // 2. tap scalars f_{t - j dil} (0 before the start and past the kernel size) and alpha_t
-  if (threadIdx.x < M * kTaps) {
-    const int j = threadIdx.x % kTaps, m = threadIdx.x / kTaps;
-    const int p = t - j * dil;
-    float a = 0.f, f = 0.f;
-    if (j < ks && p >= 0) {
-      float ms;
-      if (j == 0) {
-        a = alpha[static_cast<int64_t>(m) * B + b];
-        ms = s_ms_t;
-      } else {
-        const int64_t slot = static_cast<int64_t>(b) * D + p % D;
-        a = ring_a[slot * M + m];
-        ms = ring_ms[slot];
-      }
-      f = tap_scale(a, ms, eps);
-    }
-    s_f[m][j] = f;
-    if (j == 0) s_a[m] = a;
-  }
-  __syncthreads();
-  // 3. conv + SiLU + residual, then v_t into slot t mod D
-  if (active) {
-    uint64_t x[kTaps][kPairs];
 #pragma unroll
-    for (int j = 0; j < kTaps; ++j) {
+    for (int j = 0; j < kTaps; ++j) wg[j][q] = pk(w[j][0], w[j][1]);
+  }
+
+  int b = blockIdx.x / slices;
+  int t_next = b < B ? pos[b] - 1 : 0;
+  int buf = 0;  // scalar buffer of the next processed sequence
+  for (; b < B; b += bstride) {
+    const int t = t_next;
+    if (b + bstride < B) t_next = pos[b + bstride] - 1;
+    if (t < 0) {  // pos[b] < 1: no consumed token to apply the conv to (uniform in the block)
+      if (threadIdx.x == 0 && slice == 0 && err_word) atomicOr(err_word, 512);
+      continue;
+    }
+    const int64_t row_b = static_cast<int64_t>(b) * d;
+    // 1. tap scalars f_{t - j dil} (0 before the start and past the kernel size) and alpha_t;
+    //    mean(v_t^2) handed over, or reduced by warp 0 as the full kernel does
+    float ms_own = 0.f;  // threads < 4 M (all in warp 0) read it
+    if (!v_ms && warp == 0) ms_own = row_mean_square(v + row_b, d >> 3, 1.0f / static_cast<float>(d), lane);
+    if (threadIdx.x < M * kTaps) {
+      const int j = threadIdx.x % kTaps, m = threadIdx.x / kTaps;
       const int p = t - j * dil;
-      float xf[kCpt];
-      if (j == 0) {
+      float a = 0.f, f = 0.f;
+      if (j < ks && p >= 0) {
+        float ms;
+        if (j == 0) {
+          a = alpha[static_cast<int64_t>(m) * B + b];
+          ms = v_ms ? v_ms[b] : ms_own;  // the xor tree leaves the same sum in every lane of warp 0
+        } else {
+          const int64_t slot = static_cast<int64_t>(b) * D + p % D;
+          a = ring_a[slot * M + m];
+          ms = ring_ms[slot];
+        }
+        f = tap_scale(a, ms, eps);
+      }
+      s_f[buf][m][j] = f;
+      if (j == 0) s_a[buf][m] = a;
+      if (threadIdx.x == 0) s_ms_t[buf] = v_ms ? v_ms[b] : ms_own;
+    }
+    // 2. the channels' operands
+    typename Vec::Raw vt = Vec::zero();
+    typename Vec::Raw hraw[MMAX];
+    uint64_t x[kTaps][kPairs];
+    if (active) {
+      vt = Vec::load(v + row_b + c0);
+#pragma unroll
+      for (int m = 0; m < MMAX; ++m)
+        if (m < M) hraw[m] = Vec::load_rw(H + (static_cast<int64_t>(m) * B + b) * d + c0);
+#pragma unroll
+      for (int j = 0; j < kTaps; ++j) {
+        const int p = t - j * dil;
+        float xf[kCpt];
+        if (j == 0) {
+          Vec::unpack(vt, xf);
+        } else if (j < ks && p >= 0) {
+          Vec::unpack(Vec::load_rw(ring_v + (static_cast<int64_t>(b) * D + p % D) * d + c0), xf);
+        } else {
+#pragma unroll
+          for (int q = 0; q < kCpt; ++q) xf[q] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) x[j][q] = pk(xf[2 * q], xf[2 * q + 1]);
+      }
+    }
+    __syncthreads();
+    // 3. conv + SiLU + residual, then v_t into slot t mod D
+    if (active) {
+      uint64_t prod[kTaps][kPairs];
+#pragma unroll
+      for (int j = 0; j < kTaps; ++j)
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) prod[j][q] = mul2(wg[j][q], x[j][q]);
+#pragma unroll
+      for (int m = 0; m < MMAX; ++m) {
+        if (m >= M) continue;
+        const uint64_t f0 = pk(s_f[buf][m][0], s_f[buf][m][0]), f1 = pk(s_f[buf][m][1], s_f[buf][m][1]);
+        const uint64_t f2 = pk(s_f[buf][m][2], s_f[buf][m][2]), f3 = pk(s_f[buf][m][3], s_f[buf][m][3]);
+        const uint64_t aa = pk(s_a[buf][m], s_a[buf][m]);
+        float h[kCpt];
+        Vec::unpack(hraw[m], h);
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) {
+          uint64_t c = mul2(f0, prod[0][q]);  // c / 2
+          c = fma2(f1, prod[1][q], c);
+          c = fma2(f2, prod[2][q], c);
+          c = fma2(f3, prod[3][q], c);
+          const uint64_t acc = fma2(aa, x[0][q], pk(h[2 * q], h[2 * q + 1]));  // H + alpha v_t
+          upk(silu2_add(c, acc), h[2 * q], h[2 * q + 1]);
+        }
+        Vec::store(H + (static_cast<int64_t>(m) * B + b) * d + c0, h);
+      }
+      if (D > 0) {
+        float xf[kCpt];
         Vec::unpack(vt, xf);
-      } else if (j < ks && p >= 0) {
-        Vec::unpack(Vec::load_rw(ring_v + (static_cast<int64_t>(b) * D + p % D) * d + c0), xf);
-      } else {
-#pragma unroll
-        for (int q = 0; q < kCpt; ++q) xf[q] = 0.f;
+        Vec::store(ring_v + (static_cast<int64_t>(b) * D + t % D) * d + c0, xf);
       }
-#pragma unroll
-      for (int q = 0; q < kPairs; ++q) x[j][q] = pk(xf[2 * q], xf[2 * q + 1]);
     }
-    uint64_t prod[kTaps][kPairs];
-#pragma unroll
-    for (int j = 0; j < kTaps; ++j)
-#pragma unroll
-      for (int q = 0; q < kPairs; ++q) prod[j][q] = mul2(wg[j][q], x[j][q]);
-#pragma unroll
-    for (int m = 0; m < MMAX; ++m) {
-      if (m >= M) continue;
-      const uint64_t f0 = pk(s_f[m][0], s_f[m][0]), f1 = pk(s_f[m][1], s_f[m][1]);
-      const uint64_t f2 = pk(s_f[m][2], s_f[m][2]), f3 = pk(s_f[m][3], s_f[m][3]);
-      const uint64_t aa = pk(s_a[m], s_a[m]);
-      float h[kCpt];
-      Vec::unpack(hraw[m], h);
-#pragma unroll
-      for (int q = 0; q < kPairs; ++q) {
-        uint64_t c = mul2(f0, prod[0][q]);  // c / 2
-        c = fma2(f1, prod[1][q], c);
-        c = fma2(f2, prod[2][q], c);
-        c = fma2(f3, prod[3][q], c);
-        const uint64_t acc = fma2(aa, x[0][q], pk(h[2 * q], h[2 * q + 1]));  // H + alpha v_t
-        upk(silu2_add(c, acc), h[2 * q], h[2 * q + 1]);
-      }
-      Vec::store(H + (static_cast<int64_t>(m) * B + b) * d + c0, h);
+    // 4. the scalars of position t into its slot
+    if (D > 0 && slice == 0 && threadIdx.x < M) {
+      const int64_t slot = static_cast<int64_t>(b) * D + t % D;
+      ring_a[slot * M + threadIdx.x] = s_a[buf][threadIdx.x];
+      if (threadIdx.x == 0) ring_ms[slot] = s_ms_t[buf];
     }
-    if (D > 0) {
-      float xf[kCpt];
-      Vec::unpack(vt, xf);
-      Vec::store(ring_v + (static_cast<int64_t>(b) * D + t % D) * d + c0, xf);
-    }
-  }
-  // 4. the scalars of position t into its slot
-  if (D > 0 && slice == 0 && threadIdx.x < M) {
-    const int64_t slot = static_cast<int64_t>(b) * D + t % D;
-    ring_a[slot * M + threadIdx.x] = s_a[threadIdx.x];
-    if (threadIdx.x == 0) ring_ms[slot] = s_ms_t;
+    buf ^= 1;
   }
 }
 
@@ -538,9 +545,15 @@ template <typename T, int MB>
 pg_status launch_decode(const pg_decode_state* st, const void* v, const float* alpha, const float* v_ms,
                         const float* gamma_c, const float* conv_w, float eps, void* H, cudaStream_t stream) {
   const int slices = (st->d + kDecodeThreads * kCpt - 1) / (kDecodeThreads * kCpt);
-  const int64_t blocks = static_cast<int64_t>(st->B) * slices;
-  if (blocks >= (1ll << 31)) return PG_ERR_SHAPE;
-  decode_conv_kernel<T, MB><<<static_cast<unsigned>(blocks), kDecodeThreads, 0, stream>>>(
+  auto kern = decode_conv_kernel<T, MB>;
+  int per_sm = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (per_sm < 1) return PG_ERR_UNSUPPORTED;
+  // sequences in flight: as many as fill the SMs' block slots, at most B
+  const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * per_sm / slices);
+  const int64_t blocks = std::min<int64_t>(st->B, cap) * slices;
+  kern<<<static_cast<unsigned>(blocks), kDecodeThreads, 0, stream>>>(
       st->B, st->d, st->M, slices, static_cast<const T*>(v), alpha, v_ms, gamma_c, conv_w, st->kernel_size,
       st->dilation, eps, st->pos, static_cast<T*>(st->ring_v), st->ring_alpha, st->ring_ms, st->depth,
       static_cast<T*>(H), device_error_word());

@@ -270,3 +270,25 @@ def fp8_quantize(x: np.ndarray):
 def fp8_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """fp64 values e4m3(q) * scale of FP8 rows (both factors exact in fp64)."""
     return e4m3_to_f32(q).astype(np.float64) * np.asarray(s, np.float64)[:, None]
+
+
+# ------------------------------------------------------------------ correlated collisions
+
+def collision_counts(rows: np.ndarray) -> Tuple[int, np.ndarray]:
+    """Head-collision counts over a set of distinct n-grams of one order (PageGram report
+    3.2, measured in 6.1): rows [n, K] holds each n-gram's K head rows. Over all unordered
+    pairs {i, j}: shared[k] = #pairs whose head-0 rows are equal and whose head-k rows are
+    equal; shared[0] = pairs0 = #pairs colliding on head 0. The mean number of further
+    heads a head-0 collision shares is sum(shared[1:]) / pairs0, which the report derives
+    as (K - 1) / S for PageGram and which is about (K - 1) / M_{n,k} for independent
+    Engram-style subtables. Definition written out: for each head k, count the equal
+    (row_0, row_k) keys and add C(c, 2) for every key seen c times."""
+    r = np.asarray(rows).astype(np.uint64)
+    n, K = r.shape
+    shared = np.zeros(K, np.int64)
+    for k in range(K):
+        key = (r[:, 0] << np.uint64(32)) | r[:, k]
+        _, c = np.unique(key, return_counts=True)
+        c = c.astype(np.int64)
+        shared[k] = int((c * (c - 1) // 2).sum())
+    return int(shared[0]), shared

@@ -151,6 +151,54 @@ def test_bucket_loads_are_poisson_like():
         assert 27.0 < stat < 100.0, (k, stat)   # chi^2(60): 0.05th..99.95th percentile
 
 
+def _brute_force_pairs(r):
+    """Every unordered pair compared directly: [K] counts of pairs equal on head 0 and k."""
+    n, K = r.shape
+    out = np.zeros(K, np.int64)
+    for i in range(n):
+        for j in range(i + 1, n):
+            if r[i, 0] == r[j, 0]:
+                out += (r[i] == r[j]).astype(np.int64)
+    return out
+
+
+@pytest.mark.parametrize("n,K,hi,seed", [(0, 8, 5, 1), (1, 8, 5, 2), (60, 8, 4, 3), (300, 3, 7, 4),
+                                         (250, 16, 2, 5), (400, 8, 40, 6)])
+def test_collision_counts_equal_brute_force(n, K, hi, seed):
+    # small value ranges so that pairs collide often, on head 0 and on the others
+    rng = np.random.default_rng(seed)
+    r = rng.integers(0, hi, (n, K)).astype(np.uint32)
+    r[:, 0] += np.uint32(0xFFFFFF00)              # high bits in use: keys must not alias
+    pairs0, shared = orc.collision_counts(r)
+    bf = _brute_force_pairs(r)
+    assert pairs0 == bf[0] and np.array_equal(shared, bf)
+
+
+def test_collision_counts_closed_forms():
+    n = 37
+    same = np.tile(np.arange(8, dtype=np.uint32), (n, 1))
+    pairs0, shared = orc.collision_counts(same)
+    assert pairs0 == n * (n - 1) // 2 and (shared == pairs0).all()          # all pairs, all heads
+    distinct = np.arange(n * 8, dtype=np.uint32).reshape(n, 8)
+    assert orc.collision_counts(distinct)[0] == 0
+    # two groups on head 0 (sizes 3 and 4); head 1 splits the second group 2 + 2
+    r = np.array([[5, 1], [5, 2], [5, 3], [9, 7], [9, 7], [9, 8], [9, 8]], np.uint32)
+    pairs0, shared = orc.collision_counts(r)
+    assert pairs0 == 3 + 6 and shared[1] == 2
+
+
+@pytest.mark.parametrize("S", [1, 4, 15])
+def test_collision_counts_on_pagegram_rows(S):
+    # through the hash: the report's (K - 1) / S law (3.2) and S = 1's full overlap
+    sp = spec(W.MODE_PAGEGRAM, K=8, S=S, pages=(3, 3))
+    rows, _ = rows_at_last(sp, all_bigrams(96), 96)
+    pairs0, shared = orc.collision_counts(rows[:, 0, :])
+    if S == 1:
+        assert (shared == pairs0).all()
+    mean = shared[1:].sum() / pairs0
+    assert abs(mean - 7 / S) < 6 * np.sqrt(7 * (1 / S) * (1 - 1 / S) / pairs0) * 3 + 1e-3, (mean, S)
+
+
 @pytest.mark.parametrize("S,expect", [(4, 7 / 4), (15, 7 / 15)])
 def test_pagegram_extra_shared_heads(S, expect):
     # Given two n-grams collide on head 0, the other K-1 heads collide w.p. 1/S
