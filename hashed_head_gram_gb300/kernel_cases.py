@@ -1,6 +1,6 @@
 """Single-kernel runs on a workload's shapes, for timing and profiling one kernel at a time.
 
-    python -m hashed_head_gram_gb300.kernel_cases {gather,project,project_fp8,gather_project,conv,nf4_export,decode} --config C [--iters N]
+    python -m hashed_head_gram_gb300.kernel_cases {gather,project,project_fp8,gather_project,conv,nf4_export,decode,slots} --config C [--iters N]
 
 Inputs are synthetic and seeded (the conv and projection cases need no table, so they
 hold at most a few GB on the device); each launch goes through the C ABI exactly as the
@@ -43,7 +43,7 @@ def _time(fn, iters: int, dev) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("kernel", choices=["gather", "project", "project_fp8", "gather_project", "conv", "nf4_export",
-                                       "decode"])
+                                       "decode", "slots"])
     ap.add_argument("--batch", default="1,16,256,4096", help="decode: sequences per step (comma list)")
     ap.add_argument("--rows", type=int, default=8 << 20, help="nf4_export: fp32 head rows to export")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
@@ -58,6 +58,9 @@ def main(argv=None):
     N, din, d, M = w.N, spec.e_width, w.d, w.M
     if args.kernel == "decode":
         _decode(w, args, dev, g)
+        return
+    if args.kernel == "slots":
+        _slots(args, dev, g)
         return
     if args.kernel == "gather":
         desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
@@ -227,6 +230,45 @@ def _decode(w, args, dev, g):
             raise SystemExit("device error word set")
         print(f"decode config {w.cfg_id} B={B}: eager step {eager:.1f} us ({' + '.join(f'{n} {u:.1f}' for n, u in zip(names, parts))}); "
               f"graph {per_step:.1f} us/step, {B / per_step:.3f} M tokens/s")
+
+
+def _slots(args, dev, g):
+    """The PageGram report's slot sweep S in {1, 4, 8, 15, 60} on workload 2 (200M-parameter
+    bf16 table, P_n chosen so the budget stays fixed): the lookup (pg_gather_sign_concat)
+    and the one-launch lookup + projection (pg_gather_project_gate) timed per S, and the
+    correlated-collision statistic (pg_collision_counts over 4M distinct bigrams) next to
+    its (K - 1) / S expectation."""
+    w = W.make_workload(2)
+    tokens = torch.from_numpy(W.make_tokens(w)).to(dev)
+    N, d = w.N, w.d
+    e = torch.empty(N, 1024, dtype=torch.bfloat16, device=dev)
+    Wm = (torch.randn(d, 1024, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    x = torch.randn(N, d, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(pg.gather_project_workspace_size(N, d, 0, pg.GATE_SCALAR) // 4 + 1, device=dev)
+    n = 4_000_000
+    for S in W.SLOT_SWEEP:
+        spec = W.pagegram_slots(S)
+        desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+        table = W.make_table(w, spec, dev)
+        ug = _time(lambda: pg.gather_sign_concat(desc, tokens, table, e, pg.BF16), args.iters, dev)
+        uf = _time(lambda: pg.gather_project_gate(desc, tokens, table, e, Wm, d, pg.GATE_SCALAR, v, ws, g=w.g,
+                                                  x_resid=x), args.iters, dev)
+        grams = torch.from_numpy(W.distinct_ngrams(n, 2, w.vocab, seed=100 + S)).to(dev)
+        rows = torch.empty(2 * n, 2, spec.K, dtype=torch.int32, device=dev)
+        pg.canon_hash(desc, grams, rows)
+        span = spec.pages[0] * spec.K * S
+        cws = torch.empty(pg.collision_workspace_size(n, span), dtype=torch.uint8, device=dev)
+        counts = torch.empty(spec.K, dtype=torch.int64, device=dev)
+        uc = _time(lambda: pg.collision_counts(rows.view(-1)[2 * spec.K:], n, spec.K, 4 * spec.K, 0, span, counts,
+                                               cws), 3, dev)
+        c = counts.cpu().tolist()
+        del table
+        if pg.device_error() != 0:
+            raise SystemExit("device error word set")
+        print(f"S={S:2d} P_n={spec.pages}: gather {ug:.1f} us ({N / ug:.0f} M tok/s), gather+project one launch "
+              f"{uf:.1f} us ({N / uf:.0f} M tok/s); collisions over {n} bigrams: {c[0]} head-0 pairs, "
+              f"extra shared heads {sum(c[1:]) / max(c[0], 1):.4f} (K-1)/S = {7 / S:.4f}; counted in {uc:.0f} us")
 
 
 if __name__ == "__main__":

@@ -130,6 +130,10 @@ def _load():
     L.pg_decode_lookup.argtypes = [dp, sp, vp, vp, vp, u64, vp, i32, vp, vp]
     L.pg_decode_conv_residual.restype = ctypes.c_int
     L.pg_decode_conv_residual.argtypes = [sp, vp, vp, vp, vp, vp, f32, vp, vp]
+    L.pg_collision_counts_workspace_size.restype = ctypes.c_int
+    L.pg_collision_counts_workspace_size.argtypes = [ctypes.c_int64, u32, ctypes.POINTER(sz)]
+    L.pg_collision_counts.restype = ctypes.c_int
+    L.pg_collision_counts.argtypes = [vp, ctypes.c_int64, i32, ctypes.c_int64, u32, u32, vp, vp, sz, vp]
     L.pg_conv_residual.restype = ctypes.c_int
     L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp]
     return L
@@ -406,6 +410,22 @@ def decode_conv_residual(state: DecodeState, v: torch.Tensor, alpha: torch.Tenso
            "pg_decode_conv_residual")
 
 
+def collision_workspace_size(n: int, row0_span: int) -> int:
+    b = ctypes.c_size_t()
+    _check(_lib.pg_collision_counts_workspace_size(n, row0_span, ctypes.byref(b)),
+           "pg_collision_counts_workspace_size")
+    return b.value
+
+
+def collision_counts(rows: torch.Tensor, n: int, K: int, stride: int, row0_lo: int, row0_span: int,
+                     counts_out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """rows: int32 view of the uint32 head rows (n-gram i, head k at i * stride + k);
+    counts_out: int64 [K] (uint64 counts); workspace: >= collision_workspace_size bytes."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pg_collision_counts(_ptr(rows), n, K, stride, row0_lo, row0_span, _ptr(counts_out),
+                                    _ptr(workspace), ws_bytes, _stream(stream)), "pg_collision_counts")
+
+
 def launch_count() -> int:
     return int(_lib.pg_launch_count())
 
@@ -424,6 +444,6 @@ __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
            "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual",
            "decode_state_size", "DecodeState", "decode_reset", "decode_lookup", "decode_conv_residual",
-           "launch_count", "device_error", "lib",
+           "collision_workspace_size", "collision_counts", "launch_count", "device_error", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

@@ -196,6 +196,36 @@ def make_workload(cfg_id: int) -> Workload:
     raise ValueError(f"unknown workload {cfg_id}")
 
 
+# PageGram report section 4 evaluates S in {1, 4, 8, 15, 60} at a fixed table size.
+SLOT_SWEEP = (1, 4, 8, 15, 60)
+
+
+def pagegram_slots(S: int) -> TableSpec:
+    """Workload 2's 200M-parameter PageGram table with S slots per head and page. The
+    budget P_n K S r stays that of S = 4 (48,823 and 48,821 pages, report section 4): P_n
+    are the two largest primes <= 48,823 * 4 / S, which for S = 4 are the report's."""
+    base = make_workload(2).tables[0]
+    return dataclasses.replace(base, S=S, pages=largest_primes((48823 * 4) // S, 2))
+
+
+def distinct_ngrams(n: int, order: int, vocab: int, seed: int) -> np.ndarray:
+    """n distinct n-grams, int32 [n, order]: the first n points of the base-m grid over
+    `order` digits (m = the least integer with m ** order >= n), digit j mapped through
+    its own seeded injection of [0, m) into [0, vocab)."""
+    m = max(1, int(round(n ** (1.0 / order))))
+    while m ** order < n:
+        m += 1
+    if m > vocab:
+        raise ValueError("vocabulary too small for that many distinct n-grams")
+    rng = np.random.default_rng(np.random.SeedSequence([BASE_SEED, 0x5EED, n, order, seed]))
+    i = np.arange(n, dtype=np.int64)
+    out = np.empty((n, order), np.int32)
+    for j in range(order):
+        digit = (i // m ** (order - 1 - j)) % m
+        out[:, j] = rng.choice(vocab, size=m, replace=False)[digit]
+    return out
+
+
 def shrink(w: Workload, B: int, L: int) -> Workload:
     """Same tables and weights shape, fewer tokens (for oracle-sized tests)."""
     return dataclasses.replace(w, B=B, L=L)

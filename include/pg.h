@@ -133,7 +133,9 @@ uint64_t pg_launch_count(void);
  * pg_lookup_project_gate, 64 = a tile's wait for its rows of e_t in
  * pg_gather_project_gate, 128 = that call's gather warps or their coordinator), and
  * of decode-state checks (256 = pg_decode_reset met a slot outside [0, B), 512 = a
- * decode call met a position it cannot take; that sequence was skipped, left unchanged).
+ * decode call met a position it cannot take; that sequence was skipped, left unchanged),
+ * and of pg_collision_counts (1024 = a head-0 row outside the given span, or a head-0
+ * group too large to compare pairwise; those n-grams or pairs were left out).
  * Synchronizes the device. With clear != 0 the word is reset to 0.
  */
 pg_status pg_device_error(int32_t* code, int32_t clear);
@@ -476,6 +478,31 @@ pg_status pg_decode_lookup(const pg_table_desc* desc, const pg_decode_state* sta
 pg_status pg_decode_conv_residual(const pg_decode_state* state, const void* v, const float* alpha,
                                   const float* v_ms, const float* gamma_c, const float* conv_w, float eps,
                                   void* H, pg_stream_t stream);
+
+/*
+ * Correlated collisions (PageGram report 3.2, measured in 6.1): two n-grams that share a
+ * page collide on each head with probability 1/S, so a pair colliding on head 0 shares
+ * (K - 1)/S further heads on average; independent Engram-style subtables give about
+ * 1/M_{n,k} per head.
+ *
+ * pg_collision_counts -- over n DISTINCT n-grams of one order, whose head rows are
+ * rows[i * stride + k] (device uint32, k < K <= 16; e.g. pg_canon_hash's rows_out at one
+ * position and order, stride = O * H times the positions per n-gram):
+ *   counts_out[k] = number of unordered pairs {i, j} with equal head-0 rows and equal
+ *   head-k rows (counts_out[0]: pairs colliding on head 0)   -- device uint64 [K]
+ * so that sum_{k >= 1} counts_out[k] / counts_out[0] is the mean number of further shared
+ * heads. Every head-0 row must lie in [row0_lo, row0_lo + row0_span) (the order's head-0
+ * rows: PageGram base_n + [0, P_n K S), Engram the subtable of (n, 0)); one outside is
+ * left out and reported as device error bit 1024, as is a head-0 group of more than 1024
+ * n-grams (its pairs are left out). workspace: device, 256-byte aligned, at least
+ * pg_collision_counts_workspace_size bytes. Counts are exact integers, independent of
+ * scheduling. n == 0 writes zero counts.
+ */
+pg_status pg_collision_counts_workspace_size(int64_t n, uint32_t row0_span, size_t* bytes);
+
+pg_status pg_collision_counts(const uint32_t* rows, int64_t n, int32_t K, int64_t stride, uint32_t row0_lo,
+                              uint32_t row0_span, uint64_t* counts_out, void* workspace, size_t workspace_bytes,
+                              pg_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -175,3 +175,19 @@ def test_decode_state_validation(pg):
     assert L.pg_decode_reset(ctypes.byref(ok), None, -1, None) == 2
     assert L.pg_decode_reset(ctypes.byref(ok), None, 0, None) == 0
     assert L.pg_decode_reset(ctypes.byref(ok), None, 3, None) == 1
+
+
+def test_collision_counts_host_checks(pg):
+    L = pg.lib()
+    b = ctypes.c_size_t()
+    assert L.pg_collision_counts_workspace_size(10, 0, ctypes.byref(b)) == 2          # empty span
+    assert L.pg_collision_counts_workspace_size(-1, 5, ctypes.byref(b)) == 2
+    assert L.pg_collision_counts_workspace_size(10, 5000, None) == 1
+    assert L.pg_collision_counts_workspace_size(10, 5000, ctypes.byref(b)) == 0
+    assert b.value >= 4 * (5000 + 5001 + 10)                                         # cursors, offsets, indices
+    assert L.pg_collision_counts(None, 10, 0, 8, 0, 100, None, None, 0, None) == 2      # K < 1
+    assert L.pg_collision_counts(None, 10, 17, 17, 0, 100, None, None, 0, None) == 2    # K > 16
+    assert L.pg_collision_counts(None, 10, 8, 4, 0, 100, None, None, 0, None) == 2      # stride < K
+    assert L.pg_collision_counts(None, 10, 8, 8, 0, 100, None, None, 0, None) == 1      # no counts
+    assert L.pg_collision_counts(None, 10, 8, 8, 0, 100, ctypes.c_void_p(4), None, 0, None) == 5
+    assert L.pg_collision_counts(None, 10, 8, 8, 0, 100, ctypes.c_void_p(8), None, 0, None) == 1

@@ -1,0 +1,141 @@
+"""Correlated collisions on the GPU (PageGram report 3.2 and 6.1): pg_collision_counts'
+integer pair counts equal the oracle's on the same hashed rows, for PageGram tables of the
+report's slot sweep S in {1, 4, 8, 15, 60} at a fixed 200M-parameter budget and for the
+Engram-style table of the same budget; at millions of distinct n-grams the mean number of
+further shared heads follows (K - 1) / S."""
+import numpy as np
+import pytest
+import torch
+
+from hashed_head_gram_gb300 import workloads as W
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def _pg():
+    from hashed_head_gram_gb300 import pg
+    return pg
+
+
+def _gpu_rows(pg, desc, spec, grams, cuda):
+    """Head rows of every n-gram at its last position: int32 [n * L, O, H] on the GPU."""
+    n, L = grams.shape
+    O, H = len(spec.orders), orc.heads(spec)
+    rows = torch.empty(n * L, O, H, dtype=torch.int32, device=cuda)
+    pg.canon_hash(desc, torch.from_numpy(grams).to(cuda), rows)
+    return rows
+
+
+def _order_span(spec, o):
+    """[lo, lo + span) holding order o's head-0 rows."""
+    if spec.mode == W.MODE_PAGEGRAM:
+        lo = sum(p * spec.K * spec.S for p in spec.pages[:o])
+        return lo, spec.pages[o] * spec.K * spec.S
+    lo = sum(sum(rr) for rr in spec.rows[:o])
+    return lo, spec.rows[o][0]
+
+
+def _gpu_counts(pg, rows, n, L, spec, o, cuda, lo=None, span=None):
+    O, H = len(spec.orders), orc.heads(spec)
+    lo0, span0 = _order_span(spec, o)
+    lo = lo0 if lo is None else lo
+    span = span0 if span is None else span
+    ws = torch.empty(pg.collision_workspace_size(n, span), dtype=torch.uint8, device=cuda)
+    counts = torch.empty(H, dtype=torch.int64, device=cuda)
+    view = rows.view(-1)[(L - 1) * O * H + o * H:]
+    pg.collision_counts(view, n, H, L * O * H, lo, span, counts, ws)
+    torch.cuda.synchronize()
+    return counts.cpu().numpy()
+
+
+def _oracle_counts(spec, grams, vocab, o):
+    _, rows, _, bad = orc.index(spec, grams, None, vocab)
+    assert bad == -1
+    n, L = grams.shape
+    last = rows.reshape(n, L, *rows.shape[1:])[:, -1, o, :]
+    return orc.collision_counts(last)[1], last
+
+
+@pytest.mark.parametrize("S", W.SLOT_SWEEP)
+@pytest.mark.parametrize("o", [0, 1])
+def test_pagegram_counts_match_the_oracle(cuda, S, o):
+    pg = _pg()
+    spec = W.pagegram_slots(S)
+    w = W.make_workload(2)
+    n = 300_000
+    grams = W.distinct_ngrams(n, spec.orders[o], w.vocab, seed=S)
+    desc = pg.table_desc(spec, w.vocab)
+    rows = _gpu_rows(pg, desc, spec, grams, cuda)
+    pg.device_error(clear=True)
+    got = _gpu_counts(pg, rows, n, grams.shape[1], spec, o, cuda)
+    assert pg.device_error() == 0
+    ref, _ = _oracle_counts(spec, grams, w.vocab, o)
+    assert got[0] > 1000
+    assert np.array_equal(got, ref)
+    if S == 1:
+        assert (got == got[0]).all()        # one slot per head: a shared page is every head
+
+
+def test_engram_counts_match_the_oracle(cuda):
+    pg = _pg()
+    w = W.make_workload(3)
+    spec = w.tables[0]
+    n = 400_000
+    grams = W.distinct_ngrams(n, 2, w.vocab, seed=7)
+    desc = pg.table_desc(spec, w.vocab)
+    rows = _gpu_rows(pg, desc, spec, grams, cuda)
+    got = _gpu_counts(pg, rows, n, 2, spec, 0, cuda)
+    ref, _ = _oracle_counts(spec, grams, w.vocab, 0)
+    assert np.array_equal(got, ref)
+
+
+def test_rows_outside_the_span_are_reported_and_left_out(cuda):
+    pg = _pg()
+    spec = W.pagegram_slots(4)
+    w = W.make_workload(2)
+    n = 50_000
+    grams = W.distinct_ngrams(n, 2, w.vocab, seed=11)
+    desc = pg.table_desc(spec, w.vocab)
+    rows = _gpu_rows(pg, desc, spec, grams, cuda)
+    lo, span = _order_span(spec, 0)
+    cut = span // 2
+    pg.device_error(clear=True)
+    got = _gpu_counts(pg, rows, n, 2, spec, 0, cuda, lo=lo, span=cut)
+    assert pg.device_error(clear=True) == 1024
+    _, last = _oracle_counts(spec, grams, w.vocab, 0)
+    keep = last[:, 0].astype(np.int64) - lo < cut
+    assert np.array_equal(got, orc.collision_counts(last[keep])[1])
+
+
+def test_empty_and_single_sets(cuda):
+    pg = _pg()
+    counts = torch.full((8,), 7, dtype=torch.int64, device=cuda)
+    ws = torch.empty(pg.collision_workspace_size(1, 100), dtype=torch.uint8, device=cuda)
+    rows = torch.zeros(8, dtype=torch.int32, device=cuda)
+    pg.collision_counts(rows, 0, 8, 8, 0, 100, counts, ws)
+    torch.cuda.synchronize()
+    assert (counts.cpu() == 0).all()
+    pg.collision_counts(rows, 1, 8, 8, 0, 100, counts, ws)
+    torch.cuda.synchronize()
+    assert (counts.cpu() == 0).all()
+
+
+@pytest.mark.parametrize("S", W.SLOT_SWEEP)
+def test_extra_shared_heads_follow_k_minus_1_over_s(cuda, S):
+    # 4M distinct bigrams: about 4e7 pairs collide on head 0; their mean number of further
+    # shared heads is (K - 1) / S (report 3.2; 0.467 measured at S = 15 in 6.1)
+    pg = _pg()
+    spec = W.pagegram_slots(S)
+    w = W.make_workload(2)
+    n = 4_000_000
+    grams = W.distinct_ngrams(n, 2, w.vocab, seed=100 + S)
+    rows = _gpu_rows(pg, pg.table_desc(spec, w.vocab), spec, grams, cuda)
+    pg.device_error(clear=True)
+    got = _gpu_counts(pg, rows, n, 2, spec, 0, cuda)
+    assert pg.device_error() == 0
+    pairs0 = got[0]
+    head0_rows = spec.pages[0] * spec.S
+    assert abs(pairs0 / (n * (n - 1) / 2 / head0_rows) - 1) < 0.02    # about uniform on head 0
+    mean = got[1:].sum() / pairs0
+    assert abs(mean - 7 / S) <= 0.03 * (7 / S), (S, mean)
