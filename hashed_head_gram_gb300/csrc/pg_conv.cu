@@ -392,19 +392,41 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
 
 // Position t = pos[b] - 1 of each sequence. A persistent grid of blocks, block i owning
 // channel slice i mod slices (512 channels, thread j channels [4 j, 4 j + 4)) of every
-// (gridDim / slices)-th sequence: the conv taps are loaded once per block, and each
-// sequence's pos is read one sequence ahead. Per sequence, every thread issues at once
-// what the output needs: v_t, H of the M branches, the earlier inputs from the ring (slot
-// p mod D holds v_p, alpha_{:, p}, mean(v_p^2)) and, in threads < 4 M, the tap scalars;
-// one barrier publishes the scalars (double-buffered by processed sequence, so the next
-// sequence's writes never meet this one's reads). Every product, FMA and the SiLU are the
-// full-sequence kernel's, in its order, so H gets the same update. The ring has one slot
-// more than the taps reach, so the slot of t, written here (v by each thread for its
-// channels, the scalars by slice 0), is read by no block of this launch.
+// (gridDim / slices)-th sequence; the conv taps are loaded once per block. Operands go
+// through a kStages-deep ring in shared memory filled by cp.async, kStages - 1 sequences
+// ahead of the one being computed (no registers held while they are in flight): each
+// thread copies its chunks of v_t, of H for the M branches and of the ring's earlier
+// inputs (slot p mod D holds v_p, alpha_{:, p}, mean(v_p^2)), threads < 4 (M + 1) the raw
+// tap scalars; the position of a sequence is read one fill earlier still. One barrier per
+// sequence, once the thread's copies of this sequence and the next have landed: it makes
+// both stages visible, frees the stage filled next and publishes this sequence's tap
+// factors f, which threads < 4 M formed from the next-but-current stage's raw scalars in
+// the previous iteration. Every product, FMA and the SiLU are the full-sequence kernel's,
+// in its order, so H gets the same update.
+// The ring has one slot more than the taps reach, so the slot of t, written here (v by
+// each thread for its channels, the scalars by slice 0), is read by no block of this launch.
 constexpr int kDecodeThreads = 128;
+constexpr int kDecodeStages = 4;
+
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+
+template <typename T, int MMAX>
+struct DecodeStage {
+  using Raw = typename VecN<T, kCpt>::Raw;
+  static constexpr int kOps = 1 + MMAX + (kTaps - 1);  // v_t, H of each branch, taps 1..3
+  Raw ops[kOps][kDecodeThreads];
+  float sc[kTaps][MMAX + 1];  // per tap j: alpha of each branch, then mean(v^2) (raw, copied)
+  float f[kTaps][MMAX];       // tap factors f_{t - j dil} of each branch (formed from sc)
+  float ms_t;                 // mean(v_t^2)
+  int t;                      // position of the stage's sequence; < 0: nothing to do
+};
 
 template <typename T, int MB>
-__global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
+__global__ void __launch_bounds__(kDecodeThreads, 6) decode_conv_kernel(
     int B, int d, int M_rt, int slices, const T* __restrict__ v, const float* __restrict__ alpha,
     const float* __restrict__ v_ms, const float* __restrict__ gamma_c, const float* __restrict__ conv_w, int ks,
     int dil, float eps, const int32_t* __restrict__ pos, T* __restrict__ ring_v, float* __restrict__ ring_a,
@@ -412,15 +434,16 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
   constexpr int MMAX = MB > 0 ? MB : kMaxBranches;
   const int M = MB > 0 ? MB : M_rt;
   using Vec = VecN<T, kCpt>;
+  using Raw = typename Vec::Raw;
+  using Stage = DecodeStage<T, MMAX>;
   constexpr int kPairs = kCpt / 2;
-  __shared__ float s_f[2][kMaxBranches][kTaps];
-  __shared__ float s_a[2][kMaxBranches];
-  __shared__ float s_ms_t[2];
+  extern __shared__ __align__(16) uint8_t s_raw[];
+  Stage* stages = reinterpret_cast<Stage*>(s_raw);
   const int slice = blockIdx.x % slices;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int c0 = (slice * kDecodeThreads + threadIdx.x) * kCpt;
   const bool active = c0 < d;
-  const int bstride = gridDim.x / slices;
+  const int b0 = blockIdx.x / slices, bstride = gridDim.x / slices;
 
   // conv taps with the RMSNorm gain and SiLU's half-argument folded in (as the full kernel)
   uint64_t wg[kTaps][kPairs];
@@ -438,58 +461,98 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
     for (int j = 0; j < kTaps; ++j) wg[j][q] = pk(w[j][0], w[j][1]);
   }
 
-  int b = blockIdx.x / slices;
-  int t_next = b < B ? pos[b] - 1 : 0;
-  int buf = 0;  // scalar buffer of the next processed sequence
-  for (; b < B; b += bstride) {
-    const int t = t_next;
-    if (b + bstride < B) t_next = pos[b + bstride] - 1;
+  // the k-th sequence of this block, at position t, into stage `st` (one commit group)
+  auto fill = [&](int k, Stage& st, int t) {
+    const int b = b0 + k * bstride;
+    if (b < B && t >= 0) {
+      if (active) {
+        cp_async_bytes<static_cast<int>(sizeof(Raw))>(&st.ops[0][threadIdx.x], v + static_cast<int64_t>(b) * d + c0);
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m)
+          if (m < M)
+            cp_async_bytes<static_cast<int>(sizeof(Raw))>(&st.ops[1 + m][threadIdx.x],
+                                                          H + (static_cast<int64_t>(m) * B + b) * d + c0);
+#pragma unroll
+        for (int j = 1; j < kTaps; ++j) {
+          const int p = t - j * dil;
+          if (j < ks && p >= 0)
+            cp_async_bytes<static_cast<int>(sizeof(Raw))>(&st.ops[MMAX + j][threadIdx.x],
+                                                          ring_v + (static_cast<int64_t>(b) * D + p % D) * d + c0);
+        }
+      }
+      if (threadIdx.x < kTaps * (M + 1)) {
+        const int j = threadIdx.x / (M + 1), m = threadIdx.x - j * (M + 1);
+        const int p = t - j * dil;
+        if (j < ks && p >= 0) {
+          if (j == 0) {
+            if (m < M) cp_async4(&st.sc[0][m], alpha + static_cast<int64_t>(m) * B + b);
+            else if (v_ms) cp_async4(&st.sc[0][MMAX], v_ms + b);
+          } else {
+            const int64_t slot = static_cast<int64_t>(b) * D + p % D;
+            if (m < M) cp_async4(&st.sc[j][m], ring_a + slot * M + m);
+            else cp_async4(&st.sc[j][MMAX], ring_ms + slot);
+          }
+        }
+      }
+    }
+    if (threadIdx.x == 0) st.t = b < B ? t : -1;
+    cp_async_commit();
+  };
+  auto pos_of = [&](int k) -> int {
+    const int b = b0 + k * bstride;
+    return b < B ? pos[b] - 1 : -1;
+  };
+  // tap factors of the k-th sequence from its stage's raw scalars (warp 0; the stage's
+  // copies have landed and are visible): f = 0 before the start and past the kernel size
+  auto prep = [&](int k, Stage& st) {
+    const int b = b0 + k * bstride;
+    const int t = st.t;
+    if (threadIdx.x >= 32 || b >= B || t < 0) return;
+    // mean(v_t^2): handed over, or reduced by this warp as the full kernel's warp does
+    const float ms = v_ms ? st.sc[0][MMAX]
+                          : row_mean_square(v + static_cast<int64_t>(b) * d, d >> 3, 1.0f / static_cast<float>(d),
+                                            lane);
+    if (threadIdx.x < kTaps * M) {
+      const int j = threadIdx.x / M, m = threadIdx.x - j * M;
+      const bool ok = j < ks && t - j * dil >= 0;
+      st.f[j][m] = ok ? tap_scale(st.sc[j][m], j == 0 ? ms : st.sc[j][MMAX], eps) : 0.f;
+    }
+    if (threadIdx.x == 0) st.ms_t = ms;
+  };
+
+  int tp[kDecodeStages - 1];
+#pragma unroll
+  for (int k = 0; k < kDecodeStages - 1; ++k) tp[k] = pos_of(k);
+#pragma unroll
+  for (int k = 0; k < kDecodeStages - 1; ++k) fill(k, stages[k], tp[k]);
+  int t_pf = pos_of(kDecodeStages - 1);
+  cp_async_wait<kDecodeStages - 2>();  // sequence 0's copies
+  __syncthreads();
+  prep(0, stages[0]);
+
+  for (int k = 0; b0 + k * bstride < B; ++k) {
+    const int b = b0 + k * bstride;
+    Stage& st = stages[k % kDecodeStages];
+    cp_async_wait<kDecodeStages - 3>();  // this thread's copies of sequences k and k + 1 have landed
+    __syncthreads();                     // everyone's; stage k's factors are out; stage k - 1 is free
+    fill(k + kDecodeStages - 1, stages[(k + kDecodeStages - 1) % kDecodeStages], t_pf);
+    t_pf = pos_of(k + kDecodeStages);
+    prep(k + 1, stages[(k + 1) % kDecodeStages]);
+    const int t = st.t;
     if (t < 0) {  // pos[b] < 1: no consumed token to apply the conv to (uniform in the block)
       if (threadIdx.x == 0 && slice == 0 && err_word) atomicOr(err_word, 512);
       continue;
     }
-    const int64_t row_b = static_cast<int64_t>(b) * d;
-    // 1. tap scalars f_{t - j dil} (0 before the start and past the kernel size) and alpha_t;
-    //    mean(v_t^2) handed over, or reduced by warp 0 as the full kernel does
-    float ms_own = 0.f;  // threads < 4 M (all in warp 0) read it
-    if (!v_ms && warp == 0) ms_own = row_mean_square(v + row_b, d >> 3, 1.0f / static_cast<float>(d), lane);
-    if (threadIdx.x < M * kTaps) {
-      const int j = threadIdx.x % kTaps, m = threadIdx.x / kTaps;
-      const int p = t - j * dil;
-      float a = 0.f, f = 0.f;
-      if (j < ks && p >= 0) {
-        float ms;
-        if (j == 0) {
-          a = alpha[static_cast<int64_t>(m) * B + b];
-          ms = v_ms ? v_ms[b] : ms_own;  // the xor tree leaves the same sum in every lane of warp 0
-        } else {
-          const int64_t slot = static_cast<int64_t>(b) * D + p % D;
-          a = ring_a[slot * M + m];
-          ms = ring_ms[slot];
-        }
-        f = tap_scale(a, ms, eps);
-      }
-      s_f[buf][m][j] = f;
-      if (j == 0) s_a[buf][m] = a;
-      if (threadIdx.x == 0) s_ms_t[buf] = v_ms ? v_ms[b] : ms_own;
-    }
-    // 2. the channels' operands
-    typename Vec::Raw vt = Vec::zero();
-    typename Vec::Raw hraw[MMAX];
-    uint64_t x[kTaps][kPairs];
     if (active) {
-      vt = Vec::load(v + row_b + c0);
-#pragma unroll
-      for (int m = 0; m < MMAX; ++m)
-        if (m < M) hraw[m] = Vec::load_rw(H + (static_cast<int64_t>(m) * B + b) * d + c0);
+      uint64_t x[kTaps][kPairs];
 #pragma unroll
       for (int j = 0; j < kTaps; ++j) {
         const int p = t - j * dil;
         float xf[kCpt];
         if (j == 0) {
-          Vec::unpack(vt, xf);
+          Vec::unpack(st.ops[0][threadIdx.x], xf);
         } else if (j < ks && p >= 0) {
-          Vec::unpack(Vec::load_rw(ring_v + (static_cast<int64_t>(b) * D + p % D) * d + c0), xf);
+          Vec::unpack(st.ops[MMAX + j][threadIdx.x], xf);
         } else {
 #pragma unroll
           for (int q = 0; q < kCpt; ++q) xf[q] = 0.f;
@@ -497,10 +560,6 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
 #pragma unroll
         for (int q = 0; q < kPairs; ++q) x[j][q] = pk(xf[2 * q], xf[2 * q + 1]);
       }
-    }
-    __syncthreads();
-    // 3. conv + SiLU + residual, then v_t into slot t mod D
-    if (active) {
       uint64_t prod[kTaps][kPairs];
 #pragma unroll
       for (int j = 0; j < kTaps; ++j)
@@ -509,11 +568,12 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
 #pragma unroll
       for (int m = 0; m < MMAX; ++m) {
         if (m >= M) continue;
-        const uint64_t f0 = pk(s_f[buf][m][0], s_f[buf][m][0]), f1 = pk(s_f[buf][m][1], s_f[buf][m][1]);
-        const uint64_t f2 = pk(s_f[buf][m][2], s_f[buf][m][2]), f3 = pk(s_f[buf][m][3], s_f[buf][m][3]);
-        const uint64_t aa = pk(s_a[buf][m], s_a[buf][m]);
+        const float a_t = st.sc[0][m];
+        const uint64_t f0 = pk(st.f[0][m], st.f[0][m]), f1 = pk(st.f[1][m], st.f[1][m]);
+        const uint64_t f2 = pk(st.f[2][m], st.f[2][m]), f3 = pk(st.f[3][m], st.f[3][m]);
+        const uint64_t aa = pk(a_t, a_t);
         float h[kCpt];
-        Vec::unpack(hraw[m], h);
+        Vec::unpack(st.ops[1 + m][threadIdx.x], h);
 #pragma unroll
         for (int q = 0; q < kPairs; ++q) {
           uint64_t c = mul2(f0, prod[0][q]);  // c / 2
@@ -527,18 +587,18 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_conv_kernel(
       }
       if (D > 0) {
         float xf[kCpt];
-        Vec::unpack(vt, xf);
+        Vec::unpack(st.ops[0][threadIdx.x], xf);
         Vec::store(ring_v + (static_cast<int64_t>(b) * D + t % D) * d + c0, xf);
       }
     }
-    // 4. the scalars of position t into its slot
+    // the scalars of position t into its slot
     if (D > 0 && slice == 0 && threadIdx.x < M) {
       const int64_t slot = static_cast<int64_t>(b) * D + t % D;
-      ring_a[slot * M + threadIdx.x] = s_a[buf][threadIdx.x];
-      if (threadIdx.x == 0) ring_ms[slot] = s_ms_t[buf];
+      ring_a[slot * M + threadIdx.x] = st.sc[0][threadIdx.x];
+      if (threadIdx.x == 0) ring_ms[slot] = st.ms_t;
     }
-    buf ^= 1;
   }
+  cp_async_wait<0>();
 }
 
 template <typename T, int MB>
@@ -546,14 +606,17 @@ pg_status launch_decode(const pg_decode_state* st, const void* v, const float* a
                         const float* gamma_c, const float* conv_w, float eps, void* H, cudaStream_t stream) {
   const int slices = (st->d + kDecodeThreads * kCpt - 1) / (kDecodeThreads * kCpt);
   auto kern = decode_conv_kernel<T, MB>;
+  const size_t smem = sizeof(DecodeStage<T, (MB > 0 ? MB : kMaxBranches)>) * kDecodeStages;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e);
   int per_sm = 0;
-  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, 0);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   if (per_sm < 1) return PG_ERR_UNSUPPORTED;
   // sequences in flight: as many as fill the SMs' block slots, at most B
   const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * per_sm / slices);
   const int64_t blocks = std::min<int64_t>(st->B, cap) * slices;
-  kern<<<static_cast<unsigned>(blocks), kDecodeThreads, 0, stream>>>(
+  kern<<<static_cast<unsigned>(blocks), kDecodeThreads, smem, stream>>>(
       st->B, st->d, st->M, slices, static_cast<const T*>(v), alpha, v_ms, gamma_c, conv_w, st->kernel_size,
       st->dilation, eps, st->pos, static_cast<T*>(st->ring_v), st->ring_alpha, st->ring_ms, st->depth,
       static_cast<T*>(H), device_error_word());

@@ -45,6 +45,8 @@ def main(argv=None):
     ap.add_argument("kernel", choices=["gather", "project", "project_fp8", "gather_project", "conv", "nf4_export",
                                        "decode", "slots"])
     ap.add_argument("--batch", default="1,16,256,4096", help="decode: sequences per step (comma list)")
+    ap.add_argument("--small-table", action="store_true",
+                    help="decode: the table with ~100k-row subtables / pages (for ncu captures)")
     ap.add_argument("--rows", type=int, default=8 << 20, help="nf4_export: fp32 head rows to export")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--iters", type=int, default=20)
@@ -164,6 +166,13 @@ def _decode(w, args, dev, g):
     (eager, L2 flushed between steps) and as a CUDA graph of 16 consecutive steps replayed
     back to back (the table rows stay cold, W and the state stay in L2 as in serving)."""
     spec = w.tables[0]
+    if args.small_table:
+        import dataclasses
+        if spec.mode == W.MODE_PAGEGRAM:
+            spec = dataclasses.replace(spec, pages=W.largest_primes(25000, len(spec.orders)))
+        else:
+            p = W.largest_primes(100000, len(spec.orders) * spec.K)
+            spec = dataclasses.replace(spec, rows=[p[i * spec.K:(i + 1) * spec.K] for i in range(len(spec.orders))])
     d, M, din = w.d, w.M, spec.e_width
     desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
     cm = W.make_canon_map(w)
