@@ -78,6 +78,23 @@ pg_status decode_state_check(const pg_decode_state* st, bool need_conv);
 pg_status launch_simt_f32(int N, int Din, int d, int gate_kind, const float* e, const float* W, float g,
                           const float* x, float* out, cudaStream_t stream);
 
+// bf16 pg_project_gate for N <= kSmallRows rows (decode batches): a W-streaming SIMT kernel
+// over all SMs (pg_project_simt.cu). Context gate: per-row sums per 64-column tile go to
+// partials [M, d / kSmallTile, 3, N] (and vpart [d / kSmallTile, N]) for the alpha finalize
+// pass. Needs d % 64 == 0, Din % 8 == 0, 16-byte aligned e and W. One launch.
+constexpr int kSmallRows = 16;
+constexpr int kSmallTile = 64;
+constexpr size_t kSmallMaxE = 48 * 1024;  // e staged in shared memory: N * Din * 2 bytes at most
+// Whether pg_project_gate (bf16) takes the few-rows kernel: measured on GB300 against the
+// tensor-core path (workloads 2 and 5), it is faster up to 4 rows, slower from 8.
+constexpr int kSmallRowsUsed = 4;
+inline bool use_small_rows(int64_t N, int Din) {
+  return N >= 1 && N <= kSmallRowsUsed && static_cast<size_t>(N) * Din * 2 <= kSmallMaxE;
+}
+pg_status launch_small_rows_bf16(int N, int Din, int d, int M, int gate_kind, const void* e, const void* W, float g,
+                                 const void* x, const void* h, const float* gamma_h, const float* gamma_k, void* out,
+                                 float* partials, float* vpart, cudaStream_t stream);
+
 // W == NULL: out = e, or x + g e for the scalar gate, over n elements of dtype (n % 8 == 0,
 // 16-byte aligned). One launch.
 pg_status launch_identity_gate(int64_t n, int dtype, int gate_kind, const void* e, const void* x, float g,

@@ -1227,6 +1227,59 @@ __global__ void __launch_bounds__(256) alpha_finalize_kernel(const float* __rest
   alpha[idx] = 1.0f / (1.0f + expf(-s));
 }
 
+// The same for few rows (N <= kFinalizeWarpRows): one warp per (branch, row), lane l adding
+// tiles l, l + 32, ... and an xor tree the lanes' sums (fixed order: deterministic), so the
+// partials' round trips run side by side instead of one after another.
+constexpr int kFinalizeWarpRows = 64;
+
+__global__ void __launch_bounds__(256) alpha_finalize_warp_kernel(const float* __restrict__ partials, int M,
+                                                                  int tpb, int N, int d, float eps,
+                                                                  float* __restrict__ alpha,
+                                                                  const float* __restrict__ vpart,
+                                                                  float* __restrict__ v_ms) {
+  const int64_t w = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= static_cast<int64_t>(M) * N) return;  // whole warps
+  const int m = static_cast<int>(w / N);
+  const int row = static_cast<int>(w - static_cast<int64_t>(m) * N);
+  const bool with_v = vpart && m == 0;
+  float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f, s_vv = 0.f;
+  for (int tb = lane; tb < tpb; tb += 32) {
+    const float* p = partials + (static_cast<size_t>(m * tpb + tb) * 3) * N + row;
+    s_hk += p[0];
+    s_kk += p[N];
+    s_hh += p[2 * static_cast<size_t>(N)];
+    if (with_v) s_vv += vpart[static_cast<size_t>(tb) * N + row];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s_hk += __shfl_xor_sync(0xffffffffu, s_hk, o);
+    s_kk += __shfl_xor_sync(0xffffffffu, s_kk, o);
+    s_hh += __shfl_xor_sync(0xffffffffu, s_hh, o);
+    s_vv += __shfl_xor_sync(0xffffffffu, s_vv, o);
+  }
+  if (lane != 0) return;
+  if (with_v) v_ms[row] = s_vv / static_cast<float>(d);
+  const float inv_d = 1.0f / static_cast<float>(d);
+  const float rh = sqrtf(s_hh * inv_d + eps);
+  const float rk = sqrtf(s_kk * inv_d + eps);
+  const float s = s_hk / (rh * rk * sqrtf(static_cast<float>(d)));
+  alpha[w] = 1.0f / (1.0f + expf(-s));
+}
+
+// alpha (and mean(v^2)) from the per-tile sums: a thread per (branch, row), or a warp for few rows.
+pg_status launch_alpha_finalize(const float* partials, int M, int tpb, int N, int d, float eps, float* alpha,
+                                const float* vpart, float* v_ms, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  if (N <= kFinalizeWarpRows)
+    alpha_finalize_warp_kernel<<<static_cast<unsigned>((total * 32 + 255) / 256), 256, 0, stream>>>(
+        partials, M, tpb, N, d, eps, alpha, vpart, v_ms);
+  else
+    alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
+        partials, M, tpb, N, d, eps, alpha, vpart, v_ms);
+  return after_launch(1);
+}
+
 // ==================================================================== host side
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1354,9 +1407,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Context-gate workspace: per-(branch, tile) partial sums [M][d/BN][3][N], then, when
 // mean(v^2) is requested, the v tiles' row sums of v^2 [d/BN][N].
-size_t context_workspace(int64_t N, int d, int M, bool with_v_ms) {
+// Scratch of the context gate's per-row tile sums: [M, d / BN, 3, N] (+ [d / BN, N] for
+// v_ms). The tensor-core kernels sum per BN-column tile; the size query (query = true)
+// also covers the few-rows kernel's 64-column tiles (up to kSmallRowsUsed rows).
+size_t context_workspace(int64_t N, int d, int M, bool with_v_ms, bool query = false) {
   const int bn = (d % 256 == 0) ? 256 : 128;
-  const size_t tiles = static_cast<size_t>(d / bn);
+  const size_t tiles = static_cast<size_t>(
+      query && N <= kSmallRowsUsed && d % kSmallTile == 0 ? d / kSmallTile : d / bn);
   return (static_cast<size_t>(M) * tiles * 3 + (with_v_ms ? tiles : 0)) * static_cast<size_t>(N) * sizeof(float);
 }
 
@@ -1370,7 +1427,7 @@ pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int3
   if (!bytes) return PG_ERR_NULL;
   if (N < 0 || Din < 1 || d < 1 || M < 0) return PG_ERR_SHAPE;
   *bytes = 0;
-  if (gate_kind == PG_GATE_CONTEXT && dtype == PG_BF16) *bytes = pg::context_workspace(N, d, M, true);
+  if (gate_kind == PG_GATE_CONTEXT && dtype == PG_BF16) *bytes = pg::context_workspace(N, d, M, true, true);
   return PG_OK;
 }
 
@@ -1410,6 +1467,23 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   if (device_cc() != 103 && device_cc() != 100) return PG_ERR_DEVICE;
   if (Din % kBK != 0 || d % 128 != 0) return PG_ERR_UNSUPPORTED;
   if (!aligned16(W) || (h && !aligned16(h))) return PG_ERR_ALIGN;
+  if (use_small_rows(N, Din)) {
+    // a few rows (decode): W streamed over every SM by the SIMT kernel; the context gate
+    // takes it when the workspace holds its 64-column tile sums (what the size query gives)
+    if (gate_kind != PG_GATE_CONTEXT)
+      return launch_small_rows_bf16(N, Din, d, M, gate_kind, e, W, g, x_resid, h, gamma_h, gamma_k, v_out, nullptr,
+                                    nullptr, stream);
+    const size_t tiles = static_cast<size_t>(d / kSmallTile);
+    const size_t need = (static_cast<size_t>(M) * tiles * 3 + (v_ms_out ? tiles : 0)) * static_cast<size_t>(N) * 4;
+    if (workspace && workspace_bytes >= need && aligned16(workspace) && aligned16(gamma_h) && aligned16(gamma_k)) {
+      float* part = static_cast<float*>(workspace);
+      float* vpart = v_ms_out ? part + static_cast<size_t>(M) * tiles * 3 * static_cast<size_t>(N) : nullptr;
+      pg_status st = launch_small_rows_bf16(N, Din, d, M, gate_kind, e, W, g, x_resid, h, gamma_h, gamma_k, v_out,
+                                            part, vpart, stream);
+      if (st != PG_OK) return st;
+      return launch_alpha_finalize(part, M, static_cast<int>(tiles), N, d, eps, alpha_out, vpart, v_ms_out, stream);
+    }
+  }
   const int bn = (d % 256 == 0) ? 256 : 128;
   GemmArgs a;
   a.N = N;
@@ -1438,10 +1512,7 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   pg_status st = bn == 256 ? dispatch_tc<256, true>(gate_kind, ptrs, a, stream)
                            : dispatch_tc<128, false>(gate_kind, ptrs, a, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
-  const int64_t total = static_cast<int64_t>(M) * N;
-  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-      a.partials, M, d / bn, N, d, eps, alpha_out, a.vpart, v_ms_out);
-  return after_launch(1);
+  return launch_alpha_finalize(a.partials, M, d / bn, N, d, eps, alpha_out, a.vpart, v_ms_out, stream);
 }
 
 
@@ -1494,10 +1565,7 @@ pg_status pg_project_gate_fp8(int32_t N, int32_t Din, int32_t d, int32_t M, cons
   const GemmPtrs ptrs{e_q, W_q, x_resid, h, v_out};
   pg_status st = dispatch_fp8(gate_kind, ptrs, a, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
-  const int64_t total = static_cast<int64_t>(M) * N;
-  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-      a.partials, M, d / bn, N, d, eps, alpha_out, a.vpart, v_ms_out);
-  return after_launch(1);
+  return launch_alpha_finalize(a.partials, M, d / bn, N, d, eps, alpha_out, a.vpart, v_ms_out, stream);
 }
 
 }  // extern "C"
@@ -1578,10 +1646,7 @@ extern "C" pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int
   st = bn == 256 ? dispatch_fused<256>(gate_kind, ptrs, a, gat, stream)
                  : dispatch_fused<128>(gate_kind, ptrs, a, gat, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
-  const int64_t total = static_cast<int64_t>(M) * N;
-  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-      a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, nullptr, nullptr);
-  return after_launch(1);
+  return launch_alpha_finalize(a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, nullptr, nullptr, stream);
 }
 
 // ==================================================================== lookup + projection, one launch
@@ -1603,7 +1668,7 @@ extern "C" pg_status pg_gather_project_gate_workspace_size(int32_t N, int32_t d,
                                                           size_t* bytes) {
   if (!bytes) return PG_ERR_NULL;
   if (N < 0 || d < 1 || M < 0) return PG_ERR_SHAPE;
-  *bytes = pg::produce_sync_bytes(N) + (gate_kind == PG_GATE_CONTEXT ? pg::context_workspace(N, d, M, true) : 0);
+  *bytes = pg::produce_sync_bytes(N) + (gate_kind == PG_GATE_CONTEXT ? pg::context_workspace(N, d, M, true, true) : 0);
   return PG_OK;
 }
 
@@ -1645,12 +1710,22 @@ extern "C" pg_status pg_gather_project_gate(const pg_table_desc* desc, const int
   pg_gather_project_gate_workspace_size(static_cast<int32_t>(N), d, M, gate_kind, &need);
   if (workspace_bytes < need) return PG_ERR_WORKSPACE;
   if (gate_kind == PG_GATE_CONTEXT && (!aligned16(gamma_h) || !aligned16(gamma_k))) return PG_ERR_ALIGN;
+  const size_t sync_bytes = produce_sync_bytes(N);
+  if (use_small_rows(N, items * kBK)) {
+    // a few rows (decode batches): the two calls themselves, whose projection then runs on
+    // the few-rows kernel; the persistent producing grid would hold a tile of 256 rows
+    st = pg_gather_sign_concat(desc, tokens, B, L, canon_map, table, table_bytes, e_out, PG_BF16, err_index,
+                               stream_);
+    if (st != PG_OK) return st;
+    return pg_project_gate(static_cast<int32_t>(N), items * kBK, d, M, PG_BF16, e_out, W, gate_kind, g, x_resid, h,
+                           gamma_h, gamma_k, eps, v_out, alpha_out, v_ms_out,
+                           static_cast<uint8_t*>(workspace) + sync_bytes, workspace_bytes - sync_bytes, stream_);
+  }
   if (err_index) {
     if (reinterpret_cast<uintptr_t>(err_index) % 4) return PG_ERR_ALIGN;
     cudaError_t e = cudaMemsetAsync(err_index, 0xFF, sizeof(int32_t), stream);  // reads as -1
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  const size_t sync_bytes = produce_sync_bytes(N);
   cudaError_t e = cudaMemsetAsync(workspace, 0, sync_bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   constexpr int bn = 256;
@@ -1687,10 +1762,7 @@ extern "C" pg_status pg_gather_project_gate(const pg_table_desc* desc, const int
   const GemmPtrs ptrs{e_out, W, x_resid, h, v_out};
   st = dispatch_produce(gate_kind, ptrs, a, gat, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
-  const int64_t total = static_cast<int64_t>(M) * N;
-  alpha_finalize_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-      a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, a.vpart, v_ms_out);
-  return after_launch(1);
+  return launch_alpha_finalize(a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, a.vpart, v_ms_out, stream);
 }
 
 // ==================================================================== no-allocation variant

@@ -151,7 +151,194 @@ __global__ void __launch_bounds__(256) identity_gate_kernel(const T* __restrict_
   }
 }
 
+// ---------------------------------------------------------------- bf16, few rows (decode)
+
+// pg_project_gate's bf16 path for N <= kSmallRows rows: out = e W^T over the (1+M) d
+// columns is a matrix-vector product per row, bound by reading W once; tensor-core tiles
+// of 128 / 256 rows would idle and leave W to a few dozen SMs. A block stages e [N, Din]
+// in shared memory and owns `cpb` output columns (for the context gate one 64-column tile
+// of the per-row sums); each warp takes CW of them at a time for all rows. Per 16-byte
+// chunk of the K dimension a lane holds the chunk of each of its columns (streamed past
+// L1, the next chunk's loads issued before the current one is used) and multiplies it
+// with that chunk of every row of e, accumulating CW x NB fp32 dot products that a
+// butterfly of shuffles completes. The gate is then applied to the block's results in
+// shared memory; for the context gate each row's tile sums (sum gh gk h k, sum k^2,
+// sum h^2, and sum v^2 of the stored v) are added in column order into the layout the
+// alpha finalize pass reads.
+template <int NB>
+struct SmallCols {
+  static constexpr int CW = NB <= 8 ? 4 : 2;  // columns per warp and pass
+};
+
+__device__ __forceinline__ uint4 ldg_stream16(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
+template <int NB, int GATE>
+__global__ void __launch_bounds__(512) small_rows_bf16_kernel(
+    const __nv_bfloat16* __restrict__ e, const __nv_bfloat16* __restrict__ W, int N, int Din, int d, int cpb,
+    float g, const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ h,
+    const float* __restrict__ gamma_h, const float* __restrict__ gamma_k, __nv_bfloat16* __restrict__ out,
+    float* __restrict__ partials, float* __restrict__ vpart) {
+  constexpr int CW = SmallCols<NB>::CW;
+  __shared__ float s_res[kSmallTile][NB];
+  __shared__ float s_q[4][NB][kSmallTile];  // per column: h gh gk k, k^2, h^2; v^2
+  extern __shared__ __align__(16) uint4 s_e[];  // e, [N][Din / 8] chunks of 8
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int c0 = blockIdx.x * cpb;
+  const int chunks = Din >> 3;
+  for (int i = threadIdx.x; i < N * chunks; i += blockDim.x) s_e[i] = __ldg(reinterpret_cast<const uint4*>(e) + i);
+  __syncthreads();
+  for (int pc = warp * CW; pc < cpb; pc += nwarps * CW) {
+    float acc[CW][NB];
+#pragma unroll
+    for (int c = 0; c < CW; ++c)
+#pragma unroll
+      for (int n = 0; n < NB; ++n) acc[c][n] = 0.f;
+    const __nv_bfloat16* wrow = W + static_cast<size_t>(c0 + pc) * Din;
+    uint4 cur[CW], nxt[CW];
+    int kc = lane;
+    if (kc < chunks) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c) cur[c] = ldg_stream16(wrow + static_cast<size_t>(c) * Din + kc * 8);
+    }
+    while (kc < chunks) {
+      const int kn = kc + 32;
+      if (kn < chunks) {
+#pragma unroll
+        for (int c = 0; c < CW; ++c) nxt[c] = ldg_stream16(wrow + static_cast<size_t>(c) * Din + kn * 8);
+      }
+      float wf[CW][8];
+#pragma unroll
+      for (int c = 0; c < CW; ++c) unpack_bf16x8(cur[c], wf[c]);
+#pragma unroll
+      for (int n = 0; n < NB; ++n) {
+        if (n >= N) break;
+        float ef[8];
+        unpack_bf16x8(s_e[n * chunks + kc], ef);
+#pragma unroll
+        for (int c = 0; c < CW; ++c)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[c][n] = fmaf(wf[c][i], ef[i], acc[c][n]);
+      }
+#pragma unroll
+      for (int c = 0; c < CW; ++c) cur[c] = nxt[c];
+      kc = kn;
+    }
+#pragma unroll
+    for (int c = 0; c < CW; ++c)
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[c][n] += __shfl_xor_sync(0xffffffffu, acc[c][n], o);
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c)
+#pragma unroll
+        for (int n = 0; n < NB; ++n) s_res[pc + c][n] = acc[c][n];
+    }
+  }
+  __syncthreads();
+  const bool is_k = GATE == PG_GATE_CONTEXT && c0 >= d;
+  const int m_br = is_k ? c0 / d - 1 : 0;
+  const int kc0 = is_k ? c0 - (m_br + 1) * d : 0;
+  for (int idx = threadIdx.x; idx < cpb * NB; idx += blockDim.x) {
+    const int c = idx % cpb, n = idx / cpb;
+    if (n >= N) continue;
+    const float a = s_res[c][n];
+    if (is_k) {
+      const float hf = __bfloat162float(h[(static_cast<size_t>(m_br) * N + n) * d + kc0 + c]);
+      s_q[0][n][c] = gamma_h[kc0 + c] * gamma_k[kc0 + c] * hf * a;
+      s_q[1][n][c] = a * a;
+      s_q[2][n][c] = hf * hf;
+    } else {
+      float o = a;
+      if (GATE == PG_GATE_SCALAR) o = fmaf(g, a, __bfloat162float(x[static_cast<size_t>(n) * d + c0 + c]));
+      const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+      out[static_cast<size_t>(n) * d + c0 + c] = ob;
+      if (GATE == PG_GATE_CONTEXT) {
+        const float q = __bfloat162float(ob);
+        s_q[3][n][c] = q * q;
+      }
+    }
+  }
+  if (GATE != PG_GATE_CONTEXT) return;
+  __syncthreads();
+  if (threadIdx.x < N) {
+    const int n = threadIdx.x;
+    const int tpb = d / kSmallTile;
+    if (is_k) {
+      float hk = 0.f, kk = 0.f, hh = 0.f;
+      for (int c = 0; c < kSmallTile; ++c) {
+        hk += s_q[0][n][c];
+        kk += s_q[1][n][c];
+        hh += s_q[2][n][c];
+      }
+      float* p = partials + (static_cast<size_t>(m_br * tpb + kc0 / kSmallTile) * 3) * N + n;
+      p[0] = hk;
+      p[N] = kk;
+      p[2 * static_cast<size_t>(N)] = hh;
+    } else if (vpart) {
+      float vv = 0.f;
+      for (int c = 0; c < kSmallTile; ++c) vv += s_q[3][n][c];
+      vpart[static_cast<size_t>(c0 / kSmallTile) * N + n] = vv;
+    }
+  }
+}
+
+template <int NB>
+pg_status launch_small_nb(int N, int Din, int d, int M, int gate_kind, const void* e, const void* W, float g,
+                          const void* x, const void* h, const float* gamma_h, const float* gamma_k, void* out,
+                          float* partials, float* vpart, cudaStream_t stream) {
+  constexpr int CW = SmallCols<NB>::CW;
+  const int dcols = (gate_kind == PG_GATE_CONTEXT ? 1 + M : 1) * d;
+  // context: one 64-column tile of the per-row sums per block, a warp per CW columns (16
+  // warps); otherwise as few columns per block as spread W over about every SM
+  int warps = 16, cpb = kSmallTile;
+  if (gate_kind != PG_GATE_CONTEXT) {
+    const int want = dcols / (CW * sm_count());
+    warps = want < 1 ? 1 : (want > 8 ? 8 : want);
+    while (kSmallTile % (warps * CW)) --warps;
+    cpb = warps * CW;
+  }
+  const unsigned blocks = static_cast<unsigned>(dcols / cpb);
+  const size_t smem = static_cast<size_t>(N) * Din * sizeof(__nv_bfloat16);
+  const auto* ep = static_cast<const __nv_bfloat16*>(e);
+  const auto* wp = static_cast<const __nv_bfloat16*>(W);
+  const auto* xp = static_cast<const __nv_bfloat16*>(x);
+  const auto* hp = static_cast<const __nv_bfloat16*>(h);
+  auto* op = static_cast<__nv_bfloat16*>(out);
+  auto run = [&](auto kern) -> pg_status {
+    // e may need more than the default 48 KB of dynamic shared memory next to the static part
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kSmallMaxE));
+    if (err != cudaSuccess) return cuda_fail(err);
+    kern<<<blocks, warps * 32, smem, stream>>>(ep, wp, N, Din, d, cpb, g, xp, hp, gamma_h, gamma_k, op, partials,
+                                               vpart);
+    return after_launch(1);
+  };
+  if (gate_kind == PG_GATE_CONTEXT) return run(small_rows_bf16_kernel<NB, PG_GATE_CONTEXT>);
+  if (gate_kind == PG_GATE_SCALAR) return run(small_rows_bf16_kernel<NB, PG_GATE_SCALAR>);
+  return run(small_rows_bf16_kernel<NB, PG_GATE_NONE>);
+}
+
 }  // namespace
+
+pg_status launch_small_rows_bf16(int N, int Din, int d, int M, int gate_kind, const void* e, const void* W, float g,
+                                 const void* x, const void* h, const float* gamma_h, const float* gamma_k, void* out,
+                                 float* partials, float* vpart, cudaStream_t stream) {
+  if (N < 1 || N > kSmallRows || d % kSmallTile || Din % 8) return PG_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(N) * Din * sizeof(__nv_bfloat16) > kSmallMaxE) return PG_ERR_UNSUPPORTED;
+  if (N <= 1) return launch_small_nb<1>(N, Din, d, M, gate_kind, e, W, g, x, h, gamma_h, gamma_k, out, partials, vpart, stream);
+  if (N <= 2) return launch_small_nb<2>(N, Din, d, M, gate_kind, e, W, g, x, h, gamma_h, gamma_k, out, partials, vpart, stream);
+  if (N <= 4) return launch_small_nb<4>(N, Din, d, M, gate_kind, e, W, g, x, h, gamma_h, gamma_k, out, partials, vpart, stream);
+  if (N <= 8) return launch_small_nb<8>(N, Din, d, M, gate_kind, e, W, g, x, h, gamma_h, gamma_k, out, partials, vpart, stream);
+  return launch_small_nb<16>(N, Din, d, M, gate_kind, e, W, g, x, h, gamma_h, gamma_k, out, partials, vpart, stream);
+}
 
 pg_status launch_simt_f32(int N, int Din, int d, int gate_kind, const float* e, const float* W, float g,
                           const float* x, float* out, cudaStream_t stream) {

@@ -223,8 +223,10 @@ pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int3
  *                     gamma_k for k; fp32 [d]); h device [M, N, d]; alpha_out fp32 [M, N]
  *  dtype  PG_F32: fp32 SIMT FFMA path (gates NONE and SCALAR).
  *         PG_BF16: tcgen05 tensor-core path, fp32 accumulation, bf16 results; requires
- *         Din % 64 == 0, d % 128 == 0, 16-byte aligned e and W. Identity (W == NULL)
- *         works for both dtypes.
+ *         Din % 64 == 0, d % 128 == 0, 16-byte aligned e and W. A few rows (decode
+ *         batches of up to 4) run a SIMT kernel that streams W over every SM instead (a tensor-core tile's 128 / 256 rows would
+ *         idle); the context gate takes it when the workspace is the size query's.
+ *         Identity (W == NULL) works for both dtypes.
  *  v_ms_out  context gate, bf16 path only, optional (may be NULL): device fp32 [N],
  *             mean(v_t^2) over the d values of v_out as stored (bf16), the factor the
  *             RMSNorm of pg_conv_residual needs; computed in the projection's epilogue
@@ -232,7 +234,9 @@ pg_status pg_project_gate_workspace_size(int32_t N, int32_t Din, int32_t d, int3
  *  workspace  device, >= pg_project_gate_workspace_size() bytes, 16-byte aligned
  *             (only the context gate uses it; its contents are scratch). The query
  *             includes the room v_ms_out needs; without v_ms_out, M * (d / BN) * 3 * N * 4
- *             bytes suffice (BN = 256 if d % 256 == 0, else 128).
+ *             bytes suffice (BN = 256 if d % 256 == 0, else 128; the query uses BN = 64
+ *             for N <= 4, which the few-rows kernel needs, and smaller workspaces send
+ *             those calls to the tensor-core path).
  * N == 0 enqueues nothing. x_resid / h / v_out must not overlap e or W.
  */
 pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t dtype,
@@ -299,7 +303,9 @@ pg_status pg_project_gate_fp8(int32_t N, int32_t Din, int32_t d, int32_t M, cons
  *  desc .. table_bytes, err_index   as in pg_gather_sign_concat
  *  d .. workspace_bytes             as in pg_project_gate with dtype PG_BF16
  * Results are bit-identical to the two-call sequence (same values, same accumulation
- * order). B*L == 0 enqueues nothing.
+ * order) except for the few tokens (up to 4) whose two-call
+ * projection runs on the few-rows kernel, which this call matches within the
+ * projection's tolerance. B*L == 0 enqueues nothing.
  */
 pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int32_t* tokens, int32_t B, int32_t L,
                                  const uint32_t* canon_map, const void* table, uint64_t table_bytes,
@@ -326,8 +332,9 @@ pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int32_t* token
  *  workspace  device, 16-byte aligned, >= pg_gather_project_gate_workspace_size() bytes
  *         (always needed: the ready counters); zeroed in part by the call (one
  *         cudaMemsetAsync on `stream`) before its kernel.
- * e_out, v_out, alpha_out and v_ms_out are bit-identical to the two-call sequence. Calls
- * that share a workspace must be ordered (same stream). B*L == 0 enqueues nothing.
+ * e_out, v_out, alpha_out and v_ms_out are bit-identical to the two-call sequence (for
+ * the few tokens that take the few-rows projection the call runs those two calls). Calls that share a workspace must be ordered
+ * (same stream). B*L == 0 enqueues nothing.
  */
 pg_status pg_gather_project_gate(const pg_table_desc* desc, const int32_t* tokens, int32_t B, int32_t L,
                                  const uint32_t* canon_map, const void* table, uint64_t table_bytes,

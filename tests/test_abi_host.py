@@ -116,6 +116,9 @@ def test_workspace_size_query(pg):
     # per (branch, 256-column tile) partial sums, + the v tiles' row sums that v_ms_out needs
     assert pg.workspace_size(32768, 1280, 2560, 4, pg.BF16, pg.GATE_CONTEXT) == (4 * 10 * 3 + 10) * 32768 * 4
     assert pg.workspace_size(65536, 1024, 768, 0, pg.BF16, pg.GATE_SCALAR) == 0
+    # up to 4 rows (decode batches): the few-rows kernel's 64-column tile sums
+    assert pg.workspace_size(4, 1280, 2560, 4, pg.BF16, pg.GATE_CONTEXT) == (4 * 40 * 3 + 40) * 4 * 4
+    assert pg.workspace_size(5, 1280, 2560, 4, pg.BF16, pg.GATE_CONTEXT) == (4 * 10 * 3 + 10) * 5 * 4
 
 
 def test_decode_state_layout_matches_the_header(pg, tmp_path):

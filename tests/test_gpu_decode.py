@@ -366,3 +366,44 @@ def test_decode_steps_of_the_pagegram_scalar_path_match_the_oracle(cuda):
         got = np.stack([to_f64(o) for o in outs], axis=1).reshape(B * T, d)
         assert rel_l2(got, ref) <= BF16_TOL, cfg
         assert (state.pos.cpu() == T).all()
+
+
+@pytest.mark.parametrize("cfg", [2, 4, 5])
+def test_decode_lookup_on_the_full_tables(cuda, cfg):
+    # the full-size tables (PageGram 200M bf16, PageGram 20B NF4, Engram-27B bf16 with its
+    # canonical folding), 4096 sequences per call at staggered positions: sequence b starts
+    # lag = b mod 3 steps late (until then it is fed a filler token and restarted after the
+    # step, so it stays empty); sampled sequences' e_t are checked bit for bit
+    pg = _pg()
+    w = W.make_workload(cfg)
+    spec = w.tables[0]
+    B, T = 4096, 5
+    ww = W.shrink(w, B=B, L=T)
+    tokens, cmap = W.make_tokens(ww), W.make_canon_map(ww)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    table = W.make_table(w, spec, cuda)
+    state = pg.DecodeState(B)
+    lag = np.arange(B) % 3
+    cm = canon_tensor(cmap, cuda)
+    err = torch.empty(1, dtype=torch.int32, device=cuda)
+    outs = []
+    for step in range(T + 2):
+        t_of = step - lag
+        tok = np.where((t_of >= 0) & (t_of < T), tokens[np.arange(B), np.clip(t_of, 0, T - 1)], 0).astype(np.int32)
+        e = torch.empty(B, spec.e_width, dtype=torch.bfloat16, device=cuda)
+        pg.decode_lookup(desc, state, torch.from_numpy(tok).to(cuda), table, e, orc.BF16, canon_map=cm, err_index=err)
+        assert err.item() == -1
+        idle = np.flatnonzero(t_of < 0).astype(np.int32)
+        if idle.size:
+            pg.decode_reset(state, torch.from_numpy(idle).to(cuda))
+        outs.append(e)
+    torch.cuda.synchronize()
+    assert pg.device_error() == 0
+    assert np.array_equal(state.pos.cpu().numpy(), T + 2 - lag)
+    rng = np.random.default_rng(cfg)
+    sample = np.concatenate([[0, 1, 2, B - 1, B - 2, B - 3], rng.integers(0, B, 42)])
+    which = np.array([b * T + t for b in sample for t in range(T)], np.int64)
+    ref = oracle_e(spec, tokens, cmap, w.vocab, table, orc.BF16, which=which).reshape(len(sample), T, -1)
+    for i, b in enumerate(sample):
+        for t in range(T):
+            assert np.array_equal(bits16(outs[t + lag[b]][b]), ref[i, t]), (b, t)

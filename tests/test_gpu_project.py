@@ -195,3 +195,64 @@ def test_zero_conv_is_the_identity_path(cuda):
     ref = alpha.double().numpy()[..., None] * v.double().numpy()[None]
     assert np.array_equal(to_f64(Hd), (alpha[..., None] * v[None]).double().numpy())  # fp32 u = alpha * v
     assert rel_l2(to_f64(Hd), ref) <= 1e-7
+
+
+# ------------------------------------------------------------------ few rows (decode batches)
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 13, 16])
+@pytest.mark.parametrize("Din,d", [(1024, 768), (1280, 2560), (256, 128)])
+def test_few_rows_scalar_and_none_gates(cuda, N, Din, d):
+    # up to 4 rows take the W-streaming SIMT kernel, more the tensor-core path: both sides
+    pg = _pg()
+    e = _e_bf16(N, Din, 90 + N)
+    Wm = (torch.randn(d, Din, generator=_gen(91)) * 0.02).to(torch.bfloat16)
+    x = torch.randn(N, d, generator=_gen(92)).to(torch.bfloat16)
+    ref = dense.project(e.double().numpy(), Wm.double().numpy())
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    pg.project_gate(e.to(cuda), Wm.to(cuda), d, pg.GATE_NONE, v, pg.BF16)
+    out = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    pg.project_gate(e.to(cuda), Wm.to(cuda), d, pg.GATE_SCALAR, out, pg.BF16, g=0.5, x_resid=x.to(cuda))
+    torch.cuda.synchronize()
+    assert rel_l2(to_f64(v), ref) <= BF16_TOL
+    assert rel_l2(to_f64(out), dense.scalar_gate(x.double().numpy(), ref, 0.5)) <= BF16_TOL
+    # each output is one fp32 dot product (error <= Din 2^-24 sum |e W|) rounded once to bf16
+    # (relative error <= 2^-8)
+    s_abs = dense.project(np.abs(e.double().numpy()), np.abs(Wm.double().numpy()))
+    bound = 2.0 ** -8 * np.abs(ref) + 1.01 * Din * 2.0 ** -24 * s_abs * (1 + 2.0 ** -8)
+    assert np.all(np.abs(to_f64(v) - ref) <= bound)
+
+
+@pytest.mark.parametrize("N", [1, 3, 8, 16])
+@pytest.mark.parametrize("Din,d,M", [(1280, 2560, 4), (256, 256, 2), (512, 128, 1)])
+def test_few_rows_context_gate(cuda, N, Din, d, M):
+    pg = _pg()
+    e = _e_bf16(N, Din, 95 + N)
+    Wm = (torch.randn((1 + M) * d, Din, generator=_gen(96)) * 0.02).to(torch.bfloat16)
+    h = torch.randn(M, N, d, generator=_gen(97)).to(torch.bfloat16)
+    gh = torch.rand(d, generator=_gen(98)) + 0.5
+    gk = torch.rand(d, generator=_gen(99)) + 0.5
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    alpha = torch.empty(M, N, device=cuda)
+    v_ms = torch.empty(N, device=cuda)
+    ws = torch.empty(pg.workspace_size(N, Din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4, device=cuda)
+    pg.project_gate(e.to(cuda), Wm.to(cuda), d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=h.to(cuda), gamma_h=gh.to(cuda),
+                    gamma_k=gk.to(cuda), eps=1e-6, alpha_out=alpha, workspace=ws, v_ms_out=v_ms)
+    torch.cuda.synchronize()
+    assert pg.device_error() == 0
+    v_ref, a_ref = dense.engram_gate(e.double().numpy(), Wm.double().numpy(), h.double().numpy(),
+                                     gh.double().numpy(), gk.double().numpy(), 1e-6, M)
+    assert rel_l2(to_f64(v), v_ref) <= BF16_TOL
+    assert np.abs(to_f64(alpha) - a_ref).max() < 1e-3
+    ms_stored = (to_f64(v) ** 2).mean(axis=1)
+    assert np.abs(to_f64(v_ms) - ms_stored).max() <= 1e-5 * ms_stored.max()
+    # a workspace of the 256-column size sends the call to the tensor-core path: same values
+    # within the tolerance (other accumulation order)
+    small_ws = torch.empty(M * (d // (256 if d % 256 == 0 else 128)) * 3 * N + 4, device=cuda)
+    v2 = torch.empty_like(v)
+    alpha2 = torch.empty_like(alpha)
+    pg.project_gate(e.to(cuda), Wm.to(cuda), d, pg.GATE_CONTEXT, v2, pg.BF16, M=M, h=h.to(cuda), gamma_h=gh.to(cuda),
+                    gamma_k=gk.to(cuda), eps=1e-6, alpha_out=alpha2, workspace=small_ws)
+    torch.cuda.synchronize()
+    assert rel_l2(to_f64(v2), v_ref) <= BF16_TOL
+    assert np.abs(to_f64(alpha2) - a_ref).max() < 1e-3
+
