@@ -181,6 +181,63 @@ class Pipeline:
     def gather(self):
         self.pg.gather_sign_concat(self.desc, self.tokens, self.table, self.e, self.pdt, canon_map=self.cmap)
 
+    def decode(self, B: int, steps: int = 16, reps: int = 8):
+        """Streaming decode on this workload's table and weights: B sequences, one token
+        each per step (pg_decode_lookup, the projection with N = B, and in the context-gated
+        module pg_decode_conv_residual). `steps` consecutive steps captured in a CUDA graph and
+        replayed `reps` times back to back; returns microseconds per step."""
+        torch, pg, W, w, dn = self.torch, self.pg, self.W, self.w, self.dn
+        tok = torch.from_numpy(W.make_tokens(W.shrink(w, B=B, L=steps)).T.copy()).to(self.dev)   # [steps, B]
+        ctx = w.gate == W.GATE_CONTEXT
+        st = pg.DecodeState(B, d=self.d if ctx else 0, M=w.M if ctx else 0, dtype=pg.BF16,
+                            kernel_size=w.conv_kernel, dilation=w.dilation, device=self.dev)
+        e = torch.empty(B, self.din, dtype=torch.bfloat16, device=self.dev)
+        v = torch.empty(B, self.d, dtype=torch.bfloat16, device=self.dev)
+        if ctx:
+            H = dn["H"][:, :B].contiguous() if B <= w.N else torch.zeros(w.M, B, self.d, dtype=torch.bfloat16,
+                                                                          device=self.dev)
+            alpha = torch.empty(w.M, B, device=self.dev)
+            v_ms = torch.empty(B, device=self.dev)
+            ws = torch.empty(pg.workspace_size(B, self.din, self.d, w.M, pg.BF16, pg.GATE_CONTEXT) // 4 + 4,
+                             device=self.dev)
+        else:
+            x = dn["x"][:B].contiguous() if "x" in dn and B <= w.N else torch.zeros(B, self.d, dtype=torch.bfloat16,
+                                                                                   device=self.dev)
+
+        def step(s):
+            pg.decode_lookup(self.desc, st, tok[s], self.table, e, pg.BF16, canon_map=self.cmap)
+            if ctx:
+                pg.project_gate(e, dn["W"], self.d, pg.GATE_CONTEXT, v, pg.BF16, M=w.M, h=H, gamma_h=dn["gamma_h"],
+                                gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=alpha, workspace=ws, v_ms_out=v_ms)
+                pg.decode_conv_residual(st, v, alpha, dn["gamma_c"], dn["conv_w"], H, eps=w.eps, v_ms=v_ms)
+            elif w.gate == W.GATE_SCALAR:
+                pg.project_gate(e, dn["W"], self.d, pg.GATE_SCALAR, v, pg.BF16, g=w.g, x_resid=x)
+            else:
+                pg.project_gate(e, dn["W"], self.d, pg.GATE_NONE, v, pg.BF16)
+
+        side = torch.cuda.Stream(device=self.dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for s in range(steps):
+                step(s)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for s in range(steps):
+                step(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if pg.device_error() != 0:
+            raise RuntimeError("device error word set during the decode measurement")
+        return a.elapsed_time(b) * 1e3 / (reps * steps)
+
     def project(self):
         pg, w, dn = self.pg, self.w, self.dn
         if w.gate == self.W.GATE_SCALAR:
@@ -493,6 +550,12 @@ def run_gpu(args):
         other.append({"path": op, "ms_per_step": round(sum(statistics.mean(x) for x in o_ms), 5),
                       "kernels": {name: round(statistics.mean(o_ms[j]), 5) for j, (name, _) in enumerate(ost)}})
 
+    decode = []
+    if p.w.dtype == p.W.DT_BF16:
+        for B in sorted({1, p.w.B, 4096}):
+            us = p.decode(B)
+            decode.append({"sequences": B, "us_per_step": round(us, 2), "tokens_per_s": round(B / us * 1e6, 1)})
+
     clocks = clk.summary()
     if rank == 0:
         line = {
@@ -516,6 +579,11 @@ def run_gpu(args):
             "kernels": kernels,
             "path": path,
             "other_paths": other,
+            "decode": {"steps": decode,
+                       "how": "streaming decode, one token per sequence and step, on the same table and weights "
+                              "(decode lookup -> projection with N = sequences -> decode conv where the module has "
+                              "one); 16 consecutive steps in one CUDA graph replayed back to back, no L2 flush "
+                              "(table rows cold, W and the state warm, as in serving); not part of value"},
             "clocks": clocks,
             "wall_s_timed_loop": round(t_wall, 4),
         }
