@@ -139,3 +139,37 @@ def test_extra_shared_heads_follow_k_minus_1_over_s(cuda, S):
     assert abs(pairs0 / (n * (n - 1) / 2 / head0_rows) - 1) < 0.02    # about uniform on head 0
     mean = got[1:].sum() / pairs0
     assert abs(mean - 7 / S) <= 0.03 * (7 / S), (S, mean)
+
+
+@pytest.mark.parametrize("S", W.SLOT_SWEEP)
+def test_slot_sweep_lookup_and_one_launch_parity(cuda, S):
+    # every table of the sweep at full size (200M parameters) on workload 2's 64 x 1024
+    # tokens: the lookup bit for bit at sampled tokens, the one-launch lookup + projection
+    # writing the same e_t and the scalar-gated output within the bf16 tolerance
+    from oracle import dense
+    from tests._helpers import BF16_TOL, bits16, oracle_e, rel_l2, to_f64
+    pg = _pg()
+    w = W.make_workload(2)
+    spec = W.pagegram_slots(S)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    tokens = W.make_tokens(w)
+    tok = torch.from_numpy(tokens).to(cuda)
+    table = W.make_table(w, spec, cuda)
+    dn = W.make_dense(w, cuda)
+    e = torch.empty(w.N, spec.e_width, dtype=torch.bfloat16, device=cuda)
+    pg.gather_sign_concat(desc, tok, table, e, pg.BF16)
+    e1 = torch.empty_like(e)
+    out = torch.empty(w.N, w.d, dtype=torch.bfloat16, device=cuda)
+    ws = torch.empty(pg.gather_project_workspace_size(w.N, w.d, 0, pg.GATE_SCALAR) // 4 + 1, device=cuda)
+    pg.gather_project_gate(desc, tok, table, e1, dn["W"], w.d, pg.GATE_SCALAR, out, ws, g=w.g, x_resid=dn["x"])
+    torch.cuda.synchronize()
+    assert pg.device_error() == 0
+    assert torch.equal(e.view(torch.int16), e1.view(torch.int16))
+    rng = np.random.default_rng(S)
+    which = np.concatenate([[0, 1, 2, w.L - 1, w.N - 1], rng.integers(0, w.N, 91)]).astype(np.int64)
+    ref = oracle_e(spec, tokens, None, w.vocab, table, orc.BF16, which=which)
+    idx = torch.from_numpy(which).to(cuda)
+    assert np.array_equal(bits16(e[idx]), ref)
+    v_ref = dense.project(orc.bf16_bits_to_f64(ref), to_f64(dn["W"]))
+    x = to_f64(dn["x"][idx])
+    assert rel_l2(to_f64(out[idx]), dense.scalar_gate(x, v_ref, w.g)) <= BF16_TOL
