@@ -191,18 +191,34 @@ __global__ void __launch_bounds__(512) small_rows_bf16_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int c0 = blockIdx.x * cpb;
   const int chunks = Din >> 3;
+  const bool is_k = GATE == PG_GATE_CONTEXT && c0 >= d;
+  const int m_br = is_k ? c0 / d - 1 : 0;
+  const int kc0 = is_k ? c0 - (m_br + 1) * d : 0;
+  // the epilogue's own inputs (context gate, k tiles: h and the two gains of the thread's
+  // first (column, row)) and the first K chunk of W are requested before e is staged
+  float ep_h = 0.f, ep_g = 0.f;
+  if (is_k && threadIdx.x < cpb * N) {
+    const int c = threadIdx.x % cpb, n = threadIdx.x / cpb;
+    ep_h = __bfloat162float(h[(static_cast<size_t>(m_br) * N + n) * d + kc0 + c]);
+    ep_g = gamma_h[kc0 + c] * gamma_k[kc0 + c];
+  }
+  uint4 cur[CW], nxt[CW];
+  int pc = warp * CW;
+  if (pc < cpb && lane < chunks) {
+#pragma unroll
+    for (int c = 0; c < CW; ++c) cur[c] = ldg_stream16(W + static_cast<size_t>(c0 + pc + c) * Din + lane * 8);
+  }
   for (int i = threadIdx.x; i < N * chunks; i += blockDim.x) s_e[i] = __ldg(reinterpret_cast<const uint4*>(e) + i);
   __syncthreads();
-  for (int pc = warp * CW; pc < cpb; pc += nwarps * CW) {
+  for (bool first = true; pc < cpb; pc += nwarps * CW, first = false) {
     float acc[CW][NB];
 #pragma unroll
     for (int c = 0; c < CW; ++c)
 #pragma unroll
       for (int n = 0; n < NB; ++n) acc[c][n] = 0.f;
     const __nv_bfloat16* wrow = W + static_cast<size_t>(c0 + pc) * Din;
-    uint4 cur[CW], nxt[CW];
     int kc = lane;
-    if (kc < chunks) {
+    if (!first && kc < chunks) {
 #pragma unroll
       for (int c = 0; c < CW; ++c) cur[c] = ldg_stream16(wrow + static_cast<size_t>(c) * Din + kc * 8);
     }
@@ -243,16 +259,15 @@ __global__ void __launch_bounds__(512) small_rows_bf16_kernel(
     }
   }
   __syncthreads();
-  const bool is_k = GATE == PG_GATE_CONTEXT && c0 >= d;
-  const int m_br = is_k ? c0 / d - 1 : 0;
-  const int kc0 = is_k ? c0 - (m_br + 1) * d : 0;
   for (int idx = threadIdx.x; idx < cpb * NB; idx += blockDim.x) {
     const int c = idx % cpb, n = idx / cpb;
     if (n >= N) continue;
     const float a = s_res[c][n];
     if (is_k) {
-      const float hf = __bfloat162float(h[(static_cast<size_t>(m_br) * N + n) * d + kc0 + c]);
-      s_q[0][n][c] = gamma_h[kc0 + c] * gamma_k[kc0 + c] * hf * a;
+      const bool pre = idx == static_cast<int>(threadIdx.x);  // this (column, row) was prefetched
+      const float hf = pre ? ep_h : __bfloat162float(h[(static_cast<size_t>(m_br) * N + n) * d + kc0 + c]);
+      const float gg = pre ? ep_g : gamma_h[kc0 + c] * gamma_k[kc0 + c];
+      s_q[0][n][c] = gg * hf * a;
       s_q[1][n][c] = a * a;
       s_q[2][n][c] = hf * hf;
     } else {
