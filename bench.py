@@ -550,6 +550,32 @@ def run_gpu(args):
         other.append({"path": op, "ms_per_step": round(sum(statistics.mean(x) for x in o_ms), 5),
                       "kernels": {name: round(statistics.mean(o_ms[j]), 5) for j, (name, _) in enumerate(ost)}})
 
+    # ---- the no-reuse control: the same path on uniform IDs (Zipf workloads only)
+    control = None
+    if p.w.zipf_s is not None:
+        import torch as _t
+        zipf_tokens = p.tokens.clone()
+        p.tokens.copy_(_t.from_numpy(p.W.make_tokens(p.w, rank=rank, uniform=True)).to(dev))
+        u_ms = time_stages(stages, max(3, args.steps // 4), stream, flush)
+        u_means = {name: statistics.mean(u_ms[j]) for j, (name, _) in enumerate(stages)}
+        u_step = sum(u_means.values())
+        comp_u = compulsory_gather_bytes(p)
+        if dom == "gather_project_gate":
+            comp_u += p.N * p.d * 2 * (2 if p.w.gate == p.W.GATE_SCALAR else 1 + 2 * p.w.M)
+        b_u, work_u = p.algorithmic(dom)
+        ck = {"ms": round(u_means[dom], 5)}
+        if b_u == "hbm":
+            ck["frac_hbm"] = round(work_u / (u_means[dom] / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+            if dom in ("gather_sign_concat", "gather_project_gate"):
+                ck["compulsory_bytes"] = comp_u
+                ck["frac_hbm_compulsory"] = round(comp_u / (u_means[dom] / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+        control = {"ids": "i.i.d. uniform over the vocabulary (no reuse: the compulsory bytes approach the "
+                          "algorithmic ones)", "ms_per_step": round(u_step, 5),
+                   "tokens_per_s": round(whole_job_rate(p.N, world, reduce_max(u_step / 1e3, world)), 1),
+                   "kernels": {dom: ck}}
+        p.tokens.copy_(zipf_tokens)
+        del zipf_tokens
+
     decode = []
     if p.w.dtype == p.W.DT_BF16:
         for B in sorted({1, p.w.B, 4096}):
@@ -579,6 +605,7 @@ def run_gpu(args):
             "kernels": kernels,
             "path": path,
             "other_paths": other,
+            "uniform_ids_control": control,
             "decode": {"steps": decode,
                        "how": "streaming decode, one token per sequence and step, on the same table and weights "
                               "(decode lookup -> projection with N = sequences -> decode conv where the module has "

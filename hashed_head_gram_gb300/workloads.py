@@ -242,14 +242,18 @@ def zipf_ids(rng: np.random.Generator, V: int, s: float, n: int) -> np.ndarray:
     return np.minimum(np.searchsorted(cdf, u, side="right"), V - 1).astype(np.int32)
 
 
-def make_tokens(w: Workload, rank: int = 0) -> np.ndarray:
-    """int32 [B, L] token IDs. `rank` offsets the stream for data-parallel shards."""
+def make_tokens(w: Workload, rank: int = 0, uniform: bool = False) -> np.ndarray:
+    """int32 [B, L] token IDs. `rank` offsets the stream for data-parallel shards;
+    `uniform` draws i.i.d. uniform IDs instead of the workload's Zipf stream (the
+    no-reuse control: almost every row of the batch distinct)."""
     ss = _children(w.cfg_id)["tokens"]
     if rank:
         ss = np.random.SeedSequence([ss.entropy, 7919 * rank])
+    if uniform:
+        ss = np.random.SeedSequence([ss.entropy, 0x0C0FFEE])
     rng = np.random.Generator(np.random.PCG64(ss))
     n = w.B * w.L
-    if w.zipf_s is None:
+    if w.zipf_s is None or uniform:
         ids = rng.integers(0, w.vocab, n, dtype=np.int64).astype(np.int32)
     else:
         ids = zipf_ids(rng, w.vocab, w.zipf_s, n)
