@@ -247,6 +247,7 @@ def _conv_inputs(B, T, d, M, ks, seed, dtype):
     (4, 7, 64, 1, 2, 1, torch.float32),
     (1, 5, 8192, 3, 1, 3, torch.bfloat16),
     (2, 12, 768, 8, 3, 2, torch.float32),
+    (2, 13, 256, 8, 4, 3, torch.bfloat16),     # 4 taps x (8 + 1) = 36 tap scalars per sequence
 ])
 @pytest.mark.parametrize("given_ms", [False, True])
 def test_decode_conv_is_bit_identical_to_the_full_conv(cuda, B, T, d, M, ks, dil, dtype, given_ms):
