@@ -173,3 +173,21 @@ def test_slot_sweep_lookup_and_one_launch_parity(cuda, S):
     v_ref = dense.project(orc.bf16_bits_to_f64(ref), to_f64(dn["W"]))
     x = to_f64(dn["x"][idx])
     assert rel_l2(to_f64(out[idx]), dense.scalar_gate(x, v_ref, w.g)) <= BF16_TOL
+
+
+def test_per_head_collision_rate_is_the_same_across_layouts(cuda):
+    # PageGram report 3.2: at a fixed budget each head has the same number of rows in both
+    # layouts (P_n S for PageGram, M_{n,k} for the Engram-style subtables), so a pair of
+    # n-grams collides on a given head equally often; 4M distinct bigrams, head 0
+    pg = _pg()
+    n = 4_000_000
+    rates = {}
+    for name, w, spec in (("pagegram", W.make_workload(2), W.pagegram_slots(4)),
+                          ("engram", W.make_workload(3), W.make_workload(3).tables[0])):
+        grams = W.distinct_ngrams(n, 2, w.vocab, seed=500)
+        rows = _gpu_rows(pg, pg.table_desc(spec, w.vocab), spec, grams, cuda)
+        got = _gpu_counts(pg, rows, n, 2, spec, 0, cuda)
+        head_rows = spec.pages[0] * spec.S if spec.mode == W.MODE_PAGEGRAM else spec.rows[0][0]
+        rates[name] = got[0] / (n * (n - 1) / 2) * head_rows     # 1 for an ideal hash
+    assert abs(rates["pagegram"] - 1) < 0.02 and abs(rates["engram"] - 1) < 0.02, rates
+    assert abs(rates["pagegram"] / rates["engram"] - 1) < 0.02, rates
