@@ -42,6 +42,11 @@ FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 # ---------------------------------------------------------------- rank / sharding helpers
 
+# Nominal GB300 figures, reported beside the measured peaks: HBM3e 7.9 TB/s, dense bf16
+# 2.25 PFLOP/s; the FP32 FMA peak of the ALU-bound path is already the derived one.
+NOMINAL_PEAK = {"hbm": 7900.0, "tensor": 2250.0, "alu": FP32_FFMA_TFLOPS}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -600,6 +605,7 @@ def run_gpu(args):
             "gpu_launches": launches,
             "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                          "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "frac_nominal": round(achieved / NOMINAL_PEAK[bound], 4),
                          "peak_source": ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz" if bound == "alu"
                                          else f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})")},
             "kernels": kernels,
