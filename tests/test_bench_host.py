@@ -1,0 +1,41 @@
+"""bench.py's host-side bookkeeping (no GPU): the recorded per-kernel DRAM traffic is
+reported only while the kernel's sources are the ones it was captured on, and the
+roofline peaks it divides by."""
+import json
+import os
+import shutil
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_traffic_is_reported_only_for_the_captured_sources(tmp_path, monkeypatch):
+    (cfg, stage), (src, sha, nbytes) = next(iter(bench.TRAFFIC.items()))
+    now = bench.source_sha(src)
+    assert len(now) == 16 and all(c in "0123456789abcdef" for c in now)
+    assert bench.traffic_of(cfg, stage) == (nbytes if now == sha else None)
+    assert bench.traffic_of(99, "no such stage") is None
+    # a changed header changes every kernel's hash: the figure is withdrawn
+    csrc = os.path.join(ROOT, "hashed_head_gram_gb300", "csrc")
+    copy = tmp_path / "repo"
+    shutil.copytree(csrc, copy / "hashed_head_gram_gb300" / "csrc")
+    monkeypatch.setattr(bench, "ROOT", str(copy))
+    assert bench.source_sha(src) == now
+    hdr = copy / "hashed_head_gram_gb300" / "csrc" / "pg_internal.cuh"
+    hdr.write_text(hdr.read_text() + "\n// changed\n")
+    assert bench.source_sha(src) != now
+    monkeypatch.setitem(bench.TRAFFIC, (cfg, stage), (src, now, nbytes))   # captured on the old sources
+    assert bench.traffic_of(cfg, stage) is None
+
+
+def test_peaks_measured_and_nominal():
+    peaks, where = bench.load_peaks()
+    assert float(peaks["hbm_gbs"]) > 1000 and float(peaks["bf16_tflops"]) > 100
+    assert bench.NOMINAL_PEAK["hbm"] == 7900.0 and bench.NOMINAL_PEAK["tensor"] == 2250.0
+    assert abs(bench.NOMINAL_PEAK["alu"] - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+
+
+def test_whole_job_rate_counts_every_rank():
+    assert bench.whole_job_rate(1000, 1, 2.0) == 500.0
+    assert bench.whole_job_rate(1000, 4, 2.0) == 2000.0
