@@ -194,3 +194,39 @@ def test_collision_counts_host_checks(pg):
     assert L.pg_collision_counts(None, 10, 8, 8, 0, 100, None, None, 0, None) == 1      # no counts
     assert L.pg_collision_counts(None, 10, 8, 8, 0, 100, ctypes.c_void_p(4), None, 0, None) == 5
     assert L.pg_collision_counts(None, 10, 8, 8, 0, 100, ctypes.c_void_p(8), None, 0, None) == 1
+
+
+def test_a_c_program_uses_the_library_through_the_header(pg, tmp_path):
+    # the boundary is plain C: a C99 program that includes pg.h and links libpg.so runs the
+    # host-side calls (no GPU needed for these)
+    src = tmp_path / "use_pg.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "pg.h"
+int main(void) {
+  pg_table_desc d;
+  memset(&d, 0, sizeof d);
+  d.abi_version = PG_ABI_VERSION; d.hash_version = PG_HASH_VERSION;
+  d.mode = PG_PAGEGRAM; d.hash_kind = PG_HASH_MULXOR;
+  d.num_orders = 2; d.orders[0] = 2; d.orders[1] = 3;
+  d.K = 8; d.S = 4; d.r = 64; d.pages[0] = 48823; d.pages[1] = 48821;
+  d.row_dtype = PG_BF16; d.vocab = 50304; d.canon_vocab = 50304;
+  uint64_t rows = 0; uint32_t rb = 0, ew = 0;
+  pg_status st = pg_table_geometry(&d, &rows, &rb, &ew);
+  uint64_t state_bytes = 0;
+  pg_status st2 = pg_decode_state_size(64, 2560, 4, PG_BF16, 4, 3, &state_bytes);
+  pg_status st3 = pg_gather_sign_concat(&d, NULL, 2, 3, NULL, NULL, 0, NULL, PG_BF16, NULL, NULL);
+  printf("%d %llu %u %u %d %llu %d %s\n", (int)st, (unsigned long long)rows, rb, ew, (int)st2,
+         (unsigned long long)state_bytes, (int)st3, pg_status_str(PG_ERR_NULL));
+  return 0;
+}
+""")
+    lib_dir = os.path.join(ROOT, "hashed_head_gram_gb300")
+    exe = tmp_path / "use_pg"
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I" + os.path.join(ROOT, "include"), str(src),
+                           "-L" + lib_dir, "-l:libpg.so", "-Wl,-rpath," + lib_dir, "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split(maxsplit=7)
+    assert out[0] == "0" and int(out[1]) == (48823 + 48821) * 8 * 4 and out[2] == "128" and out[3] == "1024"
+    assert out[4] == "0" and int(out[5]) == pg.decode_state_size(64, 2560, 4, pg.BF16, 4, 3)
+    assert out[6] == "1" and out[7].strip() == pg.lib().pg_status_str(1).decode()
