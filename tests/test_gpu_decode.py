@@ -408,3 +408,51 @@ def test_decode_lookup_on_the_full_tables(cuda, cfg):
     for i, b in enumerate(sample):
         for t in range(T):
             assert np.array_equal(bits16(outs[t + lag[b]][b]), ref[i, t]), (b, t)
+
+
+@pytest.mark.parametrize("B", [2, 8])
+def test_decode_steps_of_the_full_engram_module(cuda, B):
+    # the Engram-27B module at full size (5.7 GB table, W 12,800 x 1,280) decoded the way
+    # bench.py times it: 2 sequences take the few-rows projection, 8 the tensor-core one
+    pg = _pg()
+    w = W.make_workload(5)
+    spec = w.tables[0]
+    T = 5
+    ww = W.shrink(w, B=B, L=T)
+    tokens, cmap = W.make_tokens(ww), W.make_canon_map(ww)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    table = W.make_table(w, spec, cuda)
+    dn = W.make_dense(ww, "cpu")
+    d, M, Din = w.d, w.M, spec.e_width
+    H = dn["H"].reshape(M, B, T, d)
+    Wd, cw = dn["W"].to(cuda), dn["conv_w"].to(cuda)
+    g1 = torch.ones(d, device=cuda)
+    state = pg.DecodeState(B, d=d, M=M, dtype=pg.BF16)
+    ws = torch.empty(pg.workspace_size(B, Din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4 + 4, device=cuda)
+    cm = canon_tensor(cmap, cuda)
+    vs, als, Hs = [], [], []
+    for t in range(T):
+        e = torch.empty(B, Din, dtype=torch.bfloat16, device=cuda)
+        pg.decode_lookup(desc, state, torch.from_numpy(tokens[:, t].copy()).to(cuda), table, e, orc.BF16, canon_map=cm)
+        Ht = H[:, :, t].contiguous().to(cuda)
+        v = torch.empty(B, d, dtype=torch.bfloat16, device=cuda)
+        alpha = torch.empty(M, B, device=cuda)
+        v_ms = torch.empty(B, device=cuda)
+        pg.project_gate(e, Wd, d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=Ht, gamma_h=g1, gamma_k=g1, eps=w.eps,
+                        alpha_out=alpha, workspace=ws, v_ms_out=v_ms)
+        pg.decode_conv_residual(state, v, alpha, g1, cw, Ht, eps=w.eps, v_ms=v_ms)
+        vs.append(v), als.append(alpha), Hs.append(Ht)
+    torch.cuda.synchronize()
+    assert pg.device_error() == 0
+    e_ref = orc.bf16_bits_to_f64(oracle_e(spec, tokens, cmap, w.vocab, table, orc.BF16))       # [B*T, Din]
+    v_ref, a_ref = dense.engram_gate(e_ref, dn["W"].double().numpy(), H.double().numpy().reshape(M, B * T, d),
+                                     np.ones(d), np.ones(d), w.eps, M)
+    H_ref = dense.conv_residual(v_ref.reshape(B, T, d), a_ref.reshape(M, B, T), np.ones(d),
+                                dn["conv_w"].double().numpy(), w.dilation, w.eps, H.double().numpy())
+    v_got = np.stack([to_f64(x) for x in vs], axis=1)
+    a_got = np.stack([to_f64(x) for x in als], axis=2)
+    H_got = np.stack([to_f64(x) for x in Hs], axis=2)
+    assert rel_l2(v_got, v_ref.reshape(B, T, d)) <= BF16_TOL
+    assert np.abs(a_got - a_ref.reshape(M, B, T)).max() < 2e-3
+    assert rel_l2(H_got, H_ref) <= BF16_TOL
+    assert rel_l2(H_got - H.double().numpy(), H_ref - H.double().numpy()) <= 5e-2
