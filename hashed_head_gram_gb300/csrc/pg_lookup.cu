@@ -23,13 +23,13 @@
 namespace pg {
 namespace {
 
-// NF4 levels: normal quantiles at evenly spaced probabilities (7 negative, exact zero,
-// 8 positive; outermost probability 1 - (1/30 + 1/32)/2), scaled to [-1, 1]; the
-// QLoRA NormalFloat-4 construction (PageGram report 3.3 names the data type).
+// NF4 levels: QLoRA's NormalFloat-4 values as printed in its paper (Dettmers et al. 2023,
+// Appendix E; the PageGram report, section 3.3, names the data type): normal quantiles at
+// evenly spaced probabilities (7 negative, exact zero, 8 positive), scaled to [-1, 1].
 __constant__ uint32_t c_nf4_bits[16] = {
-    0xbf800000u, 0xbf3239b1u, 0xbf066b2eu, 0xbeca329eu, 0xbe91a24bu, 0xbe3d353du,
-    0xbdba7869u, 0x00000000u, 0x3da2fb01u, 0x3e24cadfu, 0x3e7c04dau, 0x3ead0336u,
-    0x3ee1a4b5u, 0x3f1007a9u, 0x3f3913b0u, 0x3f800000u};
+    0xbf800000u, 0xbf3239b1u, 0xbf066b30u, 0xbeca32a0u, 0xbe91a24du, 0xbe3d353fu,
+    0xbdba7871u, 0x00000000u, 0x3da2faffu, 0x3e24cae3u, 0x3e7c04ddu, 0x3ead033au,
+    0x3ee1a4b8u, 0x3f1007abu, 0x3f3913b3u, 0x3f800000u};
 
 
 

@@ -84,14 +84,16 @@ typedef struct {
 
 /* ------------------------------------------------------------ number formats */
 
-/* NF4 levels: normal quantiles at evenly spaced probabilities, 7 negative, an
- * exact zero and 8 positive, outermost probability 1 - (1/30 + 1/32)/2 on both
- * sides, scaled so the extremes are -1 and +1 (the QLoRA NormalFloat-4 idea,
- * derived by oracle/nf4_levels.py). fp32 bit patterns. */
+/* NF4 levels: the 16 values of QLoRA's NormalFloat-4 data type as its paper prints
+ * them (Dettmers et al. 2023, Appendix E), which the PageGram report (section 3.3) names
+ * as the row format. They are normal quantiles at evenly spaced probabilities, 7
+ * negative, an exact zero and 8 positive, outermost probability ~0.9677083, scaled so
+ * the extremes are -1 and +1 (oracle/nf4_levels.py re-derives them to within 2 fp32
+ * ulps). fp32 bit patterns. */
 static const uint32_t ORC_NF4_BITS[16] = {
-    0xbf800000u, 0xbf3239b1u, 0xbf066b2eu, 0xbeca329eu, 0xbe91a24bu, 0xbe3d353du,
-    0xbdba7869u, 0x00000000u, 0x3da2fb01u, 0x3e24cadfu, 0x3e7c04dau, 0x3ead0336u,
-    0x3ee1a4b5u, 0x3f1007a9u, 0x3f3913b0u, 0x3f800000u};
+    0xbf800000u, 0xbf3239b1u, 0xbf066b30u, 0xbeca32a0u, 0xbe91a24du, 0xbe3d353fu,
+    0xbdba7871u, 0x00000000u, 0x3da2faffu, 0x3e24cae3u, 0x3e7c04ddu, 0x3ead033au,
+    0x3ee1a4b8u, 0x3f1007abu, 0x3f3913b3u, 0x3f800000u};
 
 static float bits_to_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
 static uint32_t f32_to_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }

@@ -377,7 +377,26 @@ def test_nf4_format_arithmetic_and_levels():
     assert 8 * 15 * 34 == int(g["page_bytes_S15"]) and 8 * 4 * 34 == int(g["page_bytes_S4"])
     lv = orc.nf4_levels()
     assert (np.diff(lv) > 0).all() and lv[0] == -1 and lv[7] == 0 and lv[15] == 1
-    assert (lv == derive_levels()).all()
+
+
+def test_nf4_levels_are_qlora_published_table():
+    # the 16 NF4 values printed in the QLoRA paper (Appendix E), each to the precision it is
+    # printed with: the oracle's fp32 levels are those values rounded to fp32, bit for bit
+    pub = np.array([float(r[0]) for r in _golden_rows("nf4_levels_qlora.txt")])
+    assert pub.shape == (16,)
+    lv = orc.nf4_levels()
+    assert (lv.view(np.uint32) == pub.astype(np.float32).view(np.uint32)).all()
+    # and a plain restatement of the construction (normal quantiles, exact fp64 outer
+    # probability) lands within 2 fp32 ulps of them: a wrong outer probability, a wrong
+    # 7/8 split or a missing normalisation would move a level by >= 1e-3
+    d = derive_levels().astype(np.float64)
+    assert np.abs(d - pub).max() <= 2e-7
+    # symmetric-type control: the same quantiles with an 8/8 split (no exact zero) differ
+    # from the table by far more than the tolerance above
+    from scipy.stats import norm
+    delta = 1.0 - 0.5 * (1.0 / 30.0 + 1.0 / 32.0)
+    sym = norm.ppf(np.linspace(1 - delta, delta, 16))
+    assert np.abs(sym / sym.max() - pub).max() > 1e-2
 
 
 def test_nf4_decode_special_rows():
