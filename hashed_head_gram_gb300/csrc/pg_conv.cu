@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "pg_internal.cuh"
 
@@ -170,13 +171,22 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
 }
 
 // SiLU(c) = c sigmoid(c) = h + h tanh(h) with h = c / 2 (sigmoid(c) = (1 + tanh(c/2)) / 2):
-// from the packed half-argument h, one MUFU operation per element and one packed FMA. The
-// sum acc + SiLU(c) is returned as h tanh(h) + (h + acc).
+// from the packed half-argument h, one tanh per element and one packed FMA. The sum
+// acc + SiLU(c) is returned as h tanh(h) + (h + acc). Stored in bf16, the outputs take the
+// hardware approximation (tanh.approx, one MUFU operation, relative error ~2^-11: far inside
+// the bf16 rounding of H); stored in fp32 they take CUDA's tanhf (a few ulp), since the
+// approximation alone would put the fp32 result above a 1e-5 relative error.
+template <typename T>
 __device__ __forceinline__ uint64_t silu2_add(uint64_t h, uint64_t acc) {
   float h0, h1, t0, t1;
   upk(h, h0, h1);
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(h0));
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(h1));
+  if constexpr (std::is_same<T, float>::value) {
+    t0 = tanhf(h0);
+    t1 = tanhf(h1);
+  } else {
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t0) : "f"(h0));
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t1) : "f"(h1));
+  }
   return fma2(h, pk(t0, t1), add2(h, acc));
 }
 
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
                 c = fma2(f23.x, prod[2][q], c);
                 c = fma2(f23.y, prod[3][q], c);
                 const uint64_t acc = fma2(aa, win[k][q], pk(h[2 * q], h[2 * q + 1]));  // H + alpha v_t
-                upk(silu2_add(c, acc), h[2 * q], h[2 * q + 1]);
+                upk(silu2_add<T>(c, acc), h[2 * q], h[2 * q + 1]);
               }
               Vec::store(out + m * branch_stride, h);
             }
@@ -581,7 +591,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 6) decode_conv_kernel(
           c = fma2(f2, prod[2][q], c);
           c = fma2(f3, prod[3][q], c);
           const uint64_t acc = fma2(aa, x[0][q], pk(h[2 * q], h[2 * q + 1]));  // H + alpha v_t
-          upk(silu2_add(c, acc), h[2 * q], h[2 * q + 1]);
+          upk(silu2_add<T>(c, acc), h[2 * q], h[2 * q + 1]);
         }
         Vec::store(H + (static_cast<int64_t>(m) * B + b) * d + c0, h);
       }

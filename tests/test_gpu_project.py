@@ -158,11 +158,11 @@ def test_conv_residual(cuda, B, L, d, M, dtype, given_ms):
     ref = dense.conv_residual(v.double().numpy().reshape(B, L, d), alpha.double().numpy().reshape(M, B, L),
                               gc.double().numpy(), w.double().numpy(), 3, 1e-6,
                               H.double().numpy().reshape(M, B, L, d))
-    tol = BF16_TOL if dtype == torch.bfloat16 else F32_TOL * 10
+    tol = BF16_TOL if dtype == torch.bfloat16 else F32_TOL
     assert rel_l2(to_f64(Hd).reshape(M, B, L, d), ref) <= tol
     # the update itself (H_new - H) is also close: a stricter view of the same output
     upd = to_f64(Hd).reshape(M, B, L, d) - H.double().numpy().reshape(M, B, L, d)
-    assert rel_l2(upd, ref - H.double().numpy().reshape(M, B, L, d)) <= (5e-2 if dtype == torch.bfloat16 else 1e-4)
+    assert rel_l2(upd, ref - H.double().numpy().reshape(M, B, L, d)) <= (5e-2 if dtype == torch.bfloat16 else F32_TOL)
 
 
 def test_zero_table_leaves_H_bit_identical(cuda):
