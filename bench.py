@@ -2,20 +2,23 @@
 """Benchmark of the hashed multi-head N-gram lookup on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--config C]
+                    [--workloads all|C,C,...] [--path auto|overlap|two_kernel|fused]
+    python bench.py --kernel {gather,project,project_fp8,gather_project,conv,nf4_export,decode,slots} --config C
 
-A step is one pass of the whole lookup over one batch of the workload (default:
-the PageGram 200M-parameter bf16 table, 64 x 1024 Zipf(1.1) tokens): canonical IDs,
-n-grams, hashes and rows, gather + sign + concat, then the W_V projection with the scalar
-gate x + g v (tcgen05). By default both run in one launch (pg_gather_project_gate: the
-gather on extra warps of the persistent projection, writing e_t ahead of the tiles that
-read it); --path two_kernel runs pg_gather_sign_concat then pg_project_gate, --path fused
-pg_lookup_project_gate; the paths not chosen are timed too. With
---config 5 the step is the Engram-27B-shaped module (gather, fused W_V + 4 W_K with
-the RMSNorm-sigmoid gate, causal conv + residual).
+A step is one pass of the whole lookup over one batch of a workload. The headline
+(--config, default 5) is the Engram-27B-shaped module, 8 x 4096 Zipf tokens: canonical
+IDs, n-grams, hashes and rows, gather + sign + concat (pg_gather_sign_concat), the fused
+W_V + 4 W_K projection with the RMSNorm-sigmoid gate (tcgen05; pg_project_gate), the
+causal depthwise conv + SiLU + residual into the 4 branch states (pg_conv_residual). The
+other four workloads are measured in the same run (same method, at least 100 timed
+steps) and reported under "workloads": the tiny fp32 tables, the PageGram 200M bf16
+table (lookup + projection + scalar gate in one launch, pg_gather_project_gate), the
+Engram-style 200M table and the 20B NF4 table (the lookup alone).
 
 Rank 0 prints one JSON line. Under torchrun each rank runs its own batch (seeded by
 rank; no collective on the data path) and the timing is the max over ranks.
 --impl reference times the CPU oracle on the host cores instead (rank 0 only).
+--kernel runs one kernel at a time on a workload's shapes (timing and profiling).
 """
 from __future__ import annotations
 
@@ -38,14 +41,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from the unit counts, 152 SMs x 128 FP32 lanes x 2 flop per FMA x 2.07 GHz (maximum SM
 # clock), and reported as an ALU bound.
 FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-
-
-# ---------------------------------------------------------------- rank / sharding helpers
+ALL_WORKLOADS = (1, 2, 3, 4, 5)
+EXTRA_MIN_STEPS = 100          # timed steps of the workloads besides the headline
 
 # Nominal GB300 figures, reported beside the measured peaks: HBM3e 7.9 TB/s, dense bf16
 # 2.25 PFLOP/s; the FP32 FMA peak of the ALU-bound path is already the derived one.
 NOMINAL_PEAK = {"hbm": 7900.0, "tensor": 2250.0, "alu": FP32_FFMA_TFLOPS}
 
+
+# ---------------------------------------------------------------- rank / sharding helpers
 
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -143,6 +147,9 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- the GPU path
 
+GATHER_KERNELS = ("gather_sign_concat", "gather_project_gate", "lookup_project_gate")
+
+
 class Pipeline:
     """Resident inputs and outputs of one workload; step() launches the whole path."""
 
@@ -158,6 +165,7 @@ class Pipeline:
         spec = self.spec = w.tables[0]
         self.desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
         self.dev = dev
+        self.rank = rank
         tokens = W.make_tokens(w, rank=rank)
         self.tokens_host = torch.from_numpy(tokens).pin_memory()
         self.tokens = self.tokens_host.to(dev)
@@ -181,7 +189,6 @@ class Pipeline:
             nws = pg.workspace_size(self.N, self.din, self.d, w.M, pg.BF16, pg.GATE_CONTEXT)
             self.ws = torch.empty(nws // 4, device=dev)
             self.H0 = dn["H"].clone()
-        self.out_host = torch.empty(self.N, self.d, dtype=self.tdt).pin_memory()
 
     def gather(self):
         self.pg.gather_sign_concat(self.desc, self.tokens, self.table, self.e, self.pdt, canon_map=self.cmap)
@@ -350,34 +357,63 @@ class Pipeline:
         if "out" in sl:
             self.out = sl["out"]
 
-    # algorithmic work per launch ("Roofline")
+    def epilogue_bytes(self):
+        """Per token: the projection's epilogue operand in and result out (scalar gate: x in,
+        out; context gate: h of every branch in, v out)."""
+        w = self.w
+        if w.gate == self.W.GATE_SCALAR:
+            return self.d * 2 * 2
+        if w.gate == self.W.GATE_CONTEXT:
+            return self.d * 2 * (1 + w.M)
+        return self.d * 2
+
+    def weight_bytes(self):
+        return (1 + self.w.M) * self.d * self.din * (4 if self.w.dtype == self.W.DT_F32 else 2)
+
     def algorithmic(self, name):
+        """(bound, work per launch) with no reuse counted: every row read from HBM as often as
+        the method addresses it (sector-rounded for the 34-byte NF4 rows)."""
         N, din, d, w = self.N, self.din, self.d, self.w
+        rows = len(self.spec.orders) * (1 if self.spec.mode == self.W.MODE_FLAT else self.spec.K)
+        rb = self.spec.row_bytes if self.spec.row_dtype != self.W.DT_NF4 else 64
+        e_b = din * self.e.element_size()
         if name == "gather_sign_concat":
-            # 2K rows x row bytes (sector-rounded for NF4) + token ID + e_t write, per token
-            rb = self.spec.row_bytes if self.spec.row_dtype != self.W.DT_NF4 else 64
-            per = len(self.spec.orders) * self.spec.K * rb + 4 + din * self.e.element_size()
-            return "hbm", per * N
+            # 2K rows + token ID + e_t write, per token
+            return "hbm", (rows * rb + 4 + e_b) * N
         if name == "gather_project_gate":
-            # one launch doing both kernels' work; its binding roof is HBM (e_t written and
-            # read back, 2K rows, IDs, the epilogue operand and the output: 89 us at the
-            # measured copy rate on the PageGram 200M workload, against 55 us of tensor work)
-            rb = self.spec.row_bytes
-            e_b = din * self.e.element_size()
-            epi = d * 2 * (2 if w.gate == self.W.GATE_SCALAR else 1 + 2 * w.M)
-            return "hbm", (len(self.spec.orders) * self.spec.K * rb + 4 + 2 * e_b + epi) * N
-        if name in ("project_gate", "lookup_project_gate"):
+            # one launch doing the lookup and the projection: rows, ID, e_t written once, the
+            # epilogue operand and the output (e_t's read-back by the tiles is the split's own
+            # cost, not the method's, and comes mostly from L2); its binding roof is HBM
+            return "hbm", (rows * rb + 4 + e_b + self.epilogue_bytes()) * N + self.weight_bytes()
+        if name == "lookup_project_gate":
+            return "hbm", (rows * rb + 4 + self.epilogue_bytes()) * N + self.weight_bytes()
+        if name == "project_gate":
             cols = d * (1 + w.M)
             return ("alu" if w.dtype == self.W.DT_F32 else "tensor"), 2.0 * N * din * cols
         # conv: read v, read + write H for every branch
         return "hbm", N * (d * 2 + 2 * w.M * d * 2)
 
+    def compulsory(self, name, table_sectors_bytes):
+        """Lower bound on a kernel's DRAM bytes: the distinct 32-byte table sectors the batch
+        touches, token IDs, e_t written (where it leaves the kernel), the epilogue operand and
+        output, and W."""
+        N = self.N
+        e_b = self.din * self.e.element_size()
+        if name == "gather_sign_concat":
+            return table_sectors_bytes + N * 4 + N * e_b
+        if name == "gather_project_gate":
+            return table_sectors_bytes + N * (4 + e_b + self.epilogue_bytes()) + self.weight_bytes()
+        if name == "lookup_project_gate":
+            return table_sectors_bytes + N * (4 + self.epilogue_bytes()) + self.weight_bytes()
+        return None
 
-def compulsory_gather_bytes(p) -> float:
-    """Distinct 32-byte table sectors the batch touches (rows from pg_canon_hash on
-    the GPU) + token IDs + the e_t write: a lower bound on the gather's DRAM traffic."""
+
+def table_sector_bytes(p) -> float:
+    """Distinct 32-byte table sectors the batch touches (rows from pg_canon_hash on the
+    GPU), in bytes."""
     torch, pg = p.torch, p.pg
-    rows = torch.empty(p.N, len(p.spec.orders), p.spec.K, dtype=torch.int32, device=p.dev)
+    heads = 1 if p.spec.mode == p.W.MODE_FLAT else p.spec.K
+    rows = torch.empty(p.N, len(p.spec.orders), heads, dtype=torch.int32, device=p.dev)
     pg.canon_hash(p.desc, p.tokens, rows, canon_map=p.cmap)
     r = rows.view(-1).to(torch.int64) & 0xFFFFFFFF
     rb = p.spec.row_bytes
@@ -386,8 +422,13 @@ def compulsory_gather_bytes(p) -> float:
     span = torch.arange((rb + 31) // 32 + 1, device=p.dev)
     cand = first.unsqueeze(1) + span
     cand = cand[cand <= last.unsqueeze(1)]
-    distinct = int(torch.unique(cand).numel())
-    return distinct * 32.0 + p.N * 4 + p.N * p.din * p.e.element_size()
+    return float(torch.unique(cand).numel()) * 32.0
+
+
+def compulsory_gather_bytes(p) -> float:
+    """Distinct 32-byte table sectors + token IDs + the e_t write: a lower bound on the
+    gather's DRAM traffic."""
+    return p.compulsory("gather_sign_concat", table_sector_bytes(p))
 
 
 def flush_l2(buf):
@@ -411,29 +452,90 @@ def time_stages(stages, steps, stream, flush):
     return [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)] for j in range(len(stages))]
 
 
-def run_gpu(args):
+def warm(stages, n, flush):
     import torch
+    for _ in range(n):
+        for _, fn in stages:
+            fn()
+        flush_l2(flush)
+    torch.cuda.synchronize()
 
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", torch.cuda.current_device())
+
+def kernel_entry(p, name, ms, peaks, comp_sectors):
+    """Per-kernel rates: no-reuse algorithmic rate and fraction, plus the compulsory-byte
+    fraction for the gathering kernels."""
+    b, wk = p.algorithmic(name)
+    s = ms / 1e3
+    if b == "hbm":
+        out = {"ms": round(ms, 5), "GB/s": round(wk / s / 1e9, 1),
+               "frac_hbm": round(wk / s / 1e9 / float(peaks["hbm_gbs"]), 4)}
+        cb = p.compulsory(name, comp_sectors)
+        if cb is not None:
+            out["frac_hbm"] = round(wk / s / 1e9 / float(peaks["hbm_gbs"]), 4)
+            out["frac_hbm_note"] = "no-reuse bytes (every addressed row from HBM): can exceed 1 under Zipf reuse"
+            out["compulsory_bytes"] = cb
+            out["GB/s_compulsory"] = round(cb / s / 1e9, 1)
+            out["frac_hbm_compulsory"] = round(cb / s / 1e9 / float(peaks["hbm_gbs"]), 4)
+        return out
+    if b == "alu":
+        return {"ms": round(ms, 5), "TFLOP/s": round(wk / s / 1e12, 1),
+                "frac_fp32_ffma": round(wk / s / 1e12 / FP32_FFMA_TFLOPS, 4)}
+    return {"ms": round(ms, 5), "TFLOP/s": round(wk / s / 1e12, 1),
+            "frac_tensor_burst": round(wk / s / 1e12 / float(peaks["bf16_tflops"]), 4),
+            "frac_tensor_sustained": round(wk / s / 1e12 / float(peaks.get("bf16_tflops_sustained",
+                                                                            peaks["bf16_tflops"])), 4)}
+
+
+def roofline_of(p, name, ms, peaks, peak_src, comp_sectors, cfg):
+    """The roofline object of one kernel: achieved = its algorithmic bytes (compulsory
+    bytes for the gathering kernels: distinct table sectors, IDs, e_t, epilogue operands)
+    or flops per launch / its mean CUDA-event duration."""
+    bound, work = p.algorithmic(name)
+    s = ms / 1e3
+    out = {"bound": bound, "kernel": name}
+    if bound == "hbm":
+        cb = p.compulsory(name, comp_sectors)
+        byts = cb if cb is not None else work
+        peak = float(peaks["hbm_gbs"])
+        out.update(achieved=round(byts / s / 1e9, 2), peak=peak, unit="GB/s", frac=round(byts / s / 1e9 / peak, 4),
+                   bytes_per_launch=byts,
+                   basis=("compulsory bytes: distinct 32-byte table sectors + IDs + e_t + epilogue operands + W"
+                          if cb is not None else "algorithmic bytes (each read and written once)"),
+                   peak_source=f"{peak_src} (hbm_gbs: STREAM-style copy)")
+        if cb is not None:
+            out["achieved_no_reuse"] = round(work / s / 1e9, 2)
+            out["frac_no_reuse"] = round(work / s / 1e9 / peak, 4)
+    elif bound == "alu":
+        achieved = work / s / 1e12
+        out.update(achieved=round(achieved, 2), peak=round(FP32_FFMA_TFLOPS, 1), unit="TFLOP/s",
+                   frac=round(achieved / FP32_FFMA_TFLOPS, 4),
+                   peak_source="derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz")
+    else:
+        achieved = work / s / 1e12
+        sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        out.update(achieved=round(achieved, 2), peak=sus, unit="TFLOP/s", frac=round(achieved / sus, 4),
+                   frac_burst=round(achieved / float(peaks["bf16_tflops"]), 4), peak_burst=float(peaks["bf16_tflops"]),
+                   peak_source=f"{peak_src} (bf16_tflops_sustained: cuBLAS bf16 back to back under the power cap; "
+                               "the kernel runs inside a step of several launches)")
+    out["frac_nominal"] = round(out["achieved"] / NOMINAL_PEAK[bound], 4)
+    out["traffic"] = traffic_of(cfg, name)
+    return out
+
+
+def measure_workload(cfg, args, dev, rank, world, steps, headline):
+    """Times one workload's step (device-resident inputs), its alternative paths, the
+    uniform-ID control, streaming decode and the end-to-end loop; returns a dict."""
+    import torch
     from hashed_head_gram_gb300 import pg
 
-    p = Pipeline(args.config, dev, rank)
+    p = Pipeline(cfg, dev, rank)
     stream = torch.cuda.current_stream()
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     path = args.path if args.path in p.paths() else p.paths()[0]
     stages = p.stages(path)
 
     # ---- warm-up
-    for _ in range(args.warmup):
-        for _, fn in stages:
-            fn()
-        flush_l2(flush)
-    torch.cuda.synchronize()
+    warm(stages, args.warmup, flush)
     if p.w.gate == p.W.GATE_CONTEXT:
         p.dn["H"].copy_(p.H0)
     torch.cuda.synchronize()
@@ -444,13 +546,13 @@ def run_gpu(args):
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t_wall = time.perf_counter()
-        stage_ms = time_stages(stages, args.steps, stream, flush)
+        stage_ms = time_stages(stages, steps, stream, flush)
         t_wall = time.perf_counter() - t_wall
     barrier(world)
     launches = pg.launch_count() - launches0
-    step_ms = [sum(stage_ms[j][i] for j in range(len(stages))) for i in range(args.steps)]
+    step_ms = [sum(stage_ms[j][i] for j in range(len(stages))) for i in range(steps)]
     total_s = reduce_max(sum(step_ms) / 1e3, world)
-    value = whole_job_rate(p.N * args.steps, world, total_s)
+    value = whole_job_rate(p.N * steps, world, total_s)
 
     # ---- end to end through the C ABI with host buffers: every step uploads its token IDs
     #      (and x) from pinned host memory and reads its whole result back; steps are
@@ -464,7 +566,7 @@ def run_gpu(args):
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
-    e2e_steps = max(2, min(args.steps, 200))
+    e2e_steps = max(2, min(steps, 200))
     barrier(world)
     torch.cuda.synchronize()
     t_e0, t_e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -496,135 +598,125 @@ def run_gpu(args):
     e2e_s = reduce_max(t_e0.elapsed_time(t_e1) / 1e3, world)
     e2e_value = whole_job_rate(p.N * e2e_steps, world, e2e_s)
     d2h = res0.numel() * res0.element_size()
+    del res_hosts
 
-    # ---- roofline of the dominant kernel
+    # ---- per-kernel rates and the roofline of the dominant kernel
     peaks, peak_src = load_peaks()
     means = {name: statistics.mean(stage_ms[j]) for j, (name, _) in enumerate(stages)}
     dom = max(means, key=means.get)
-    bound, work = p.algorithmic(dom)
-    dur_s = means[dom] / 1e3
-    traffic = traffic_of(args.config, dom)
-    if bound == "hbm":
-        achieved, peak, unit = work / dur_s / 1e9, float(peaks["hbm_gbs"]), "GB/s"
-    elif bound == "alu":
-        achieved, peak, unit = work / dur_s / 1e12, round(FP32_FFMA_TFLOPS, 1), "TFLOP/s"
-    else:
-        achieved, peak, unit = work / dur_s / 1e12, float(peaks["bf16_tflops"]), "TFLOP/s"
-    kernels = {}
-    for j, (name, _) in enumerate(stages):
-        b, wk = p.algorithmic(name)
-        ms = means[name]
-        if b == "hbm":
-            kernels[name] = {"ms": round(ms, 5), "GB/s": round(wk / (ms / 1e3) / 1e9, 1),
-                             "frac_hbm": round(wk / (ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
-        elif b == "alu":
-            kernels[name] = {"ms": round(ms, 5), "TFLOP/s": round(wk / (ms / 1e3) / 1e12, 1),
-                             "frac_fp32_ffma": round(wk / (ms / 1e3) / 1e12 / FP32_FFMA_TFLOPS, 4)}
-        else:
-            kernels[name] = {"ms": round(ms, 5), "TFLOP/s": round(wk / (ms / 1e3) / 1e12, 1),
-                             "frac_tensor": round(wk / (ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]), 4)}
-    comp = compulsory_gather_bytes(p)
-    if "gather_sign_concat" in means:
-        g_ms = means["gather_sign_concat"]
-        kernels["gather_sign_concat"]["compulsory_bytes"] = comp
-        kernels["gather_sign_concat"]["frac_hbm_compulsory"] = round(
-            comp / (g_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
-    if "lookup_project_gate" in means:
-        # e_t never reaches memory: table sectors + IDs + the epilogue operand in + the output
-        fb = comp - p.N * p.din * 2 + p.N * p.d * 2 * (2 if p.w.gate == p.W.GATE_SCALAR else 1 + 2 * p.w.M)
-        f_ms = means["lookup_project_gate"]
-        kernels["lookup_project_gate"]["compulsory_bytes"] = fb
-        kernels["lookup_project_gate"]["GB/s_compulsory"] = round(fb / (f_ms / 1e3) / 1e9, 1)
-        kernels["lookup_project_gate"]["frac_hbm_compulsory"] = round(
-            fb / (f_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
-    if "gather_project_gate" in means:
-        # e_t written once and read back by the projection (mostly from L2): table sectors +
-        # IDs + e_t + the epilogue operand in + the output
-        fb = comp + p.N * p.d * 2 * (2 if p.w.gate == p.W.GATE_SCALAR else 1 + 2 * p.w.M)
-        o_ms_ = means["gather_project_gate"]
-        kernels["gather_project_gate"]["compulsory_bytes"] = fb
-        kernels["gather_project_gate"]["GB/s_compulsory"] = round(fb / (o_ms_ / 1e3) / 1e9, 1)
-        kernels["gather_project_gate"]["frac_hbm_compulsory"] = round(
-            fb / (o_ms_ / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+    sectors = table_sector_bytes(p)
+    kernels = {name: kernel_entry(p, name, ms, peaks, sectors) for name, ms in means.items()}
+    roofline = roofline_of(p, dom, means[dom], peaks, peak_src, sectors, cfg)
+    if dom != "gather_sign_concat" and "gather_sign_concat" in means:
+        kernels["gather_sign_concat"]["roofline"] = roofline_of(p, "gather_sign_concat", means["gather_sign_concat"],
+                                                                peaks, peak_src, sectors, cfg)
+
+    # ---- the other paths of this workload, each warmed up and timed over the same steps
     other = []
     for op in p.paths():
         if op == path:
             continue
         ost = p.stages(op)
-        o_ms = time_stages(ost, max(3, args.steps // 4), stream, flush)
-        other.append({"path": op, "ms_per_step": round(sum(statistics.mean(x) for x in o_ms), 5),
-                      "kernels": {name: round(statistics.mean(o_ms[j]), 5) for j, (name, _) in enumerate(ost)}})
+        warm(ost, args.warmup, flush)
+        o_ms = time_stages(ost, steps, stream, flush)
+        om = {name: statistics.mean(o_ms[j]) for j, (name, _) in enumerate(ost)}
+        other.append({"path": op, "ms_per_step": round(sum(om.values()), 5),
+                      "kernels": {name: kernel_entry(p, name, ms, peaks, sectors) for name, ms in om.items()}})
+    if p.w.gate == p.W.GATE_CONTEXT:
+        p.dn["H"].copy_(p.H0)
 
     # ---- the no-reuse control: the same path on uniform IDs (Zipf workloads only)
     control = None
     if p.w.zipf_s is not None:
-        import torch as _t
         zipf_tokens = p.tokens.clone()
-        p.tokens.copy_(_t.from_numpy(p.W.make_tokens(p.w, rank=rank, uniform=True)).to(dev))
-        u_ms = time_stages(stages, max(3, args.steps // 4), stream, flush)
+        p.tokens.copy_(torch.from_numpy(p.W.make_tokens(p.w, rank=rank, uniform=True)).to(dev))
+        warm(stages, args.warmup, flush)
+        u_ms = time_stages(stages, steps, stream, flush)
         u_means = {name: statistics.mean(u_ms[j]) for j, (name, _) in enumerate(stages)}
-        u_step = sum(u_means.values())
-        comp_u = compulsory_gather_bytes(p)
-        if dom == "gather_project_gate":
-            comp_u += p.N * p.d * 2 * (2 if p.w.gate == p.W.GATE_SCALAR else 1 + 2 * p.w.M)
-        b_u, work_u = p.algorithmic(dom)
-        ck = {"ms": round(u_means[dom], 5)}
-        if b_u == "hbm":
-            ck["frac_hbm"] = round(work_u / (u_means[dom] / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
-            if dom in ("gather_sign_concat", "gather_project_gate"):
-                ck["compulsory_bytes"] = comp_u
-                ck["frac_hbm_compulsory"] = round(comp_u / (u_means[dom] / 1e3) / 1e9 / float(peaks["hbm_gbs"]), 4)
+        u_sectors = table_sector_bytes(p)
         control = {"ids": "i.i.d. uniform over the vocabulary (no reuse: the compulsory bytes approach the "
-                          "algorithmic ones)", "ms_per_step": round(u_step, 5),
-                   "tokens_per_s": round(whole_job_rate(p.N, world, reduce_max(u_step / 1e3, world)), 1),
-                   "kernels": {dom: ck}}
+                          "algorithmic ones)", "ms_per_step": round(sum(u_means.values()), 5),
+                   "tokens_per_s": round(whole_job_rate(p.N, world, reduce_max(sum(u_means.values()) / 1e3, world)), 1),
+                   "kernels": {name: kernel_entry(p, name, ms, peaks, u_sectors) for name, ms in u_means.items()}}
         p.tokens.copy_(zipf_tokens)
         del zipf_tokens
+        if p.w.gate == p.W.GATE_CONTEXT:
+            p.dn["H"].copy_(p.H0)
 
     decode = []
     if p.w.dtype == p.W.DT_BF16:
         for B in sorted({1, p.w.B, 4096}):
             us = p.decode(B)
             decode.append({"sequences": B, "us_per_step": round(us, 2), "tokens_per_s": round(B / us * 1e6, 1)})
+    if pg.device_error() != 0:
+        raise RuntimeError(f"device error word set: {pg.device_error()}")
 
-    clocks = clk.summary()
+    out = {
+        "value": round(value, 1), "unit": "tokens/s", "steps": steps, "ms_per_step": round(statistics.mean(step_ms), 5),
+        "dtype": "f32" if p.w.dtype == p.W.DT_F32 else "bf16",
+        "config": workload_config(p.w, world),
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": f"{e2e_steps} steps pipelined: each uploads its inputs from pinned host memory and "
+                       "reads its whole result back; uploads, kernels and read-backs of consecutive steps "
+                       "overlap on three streams (double-buffered device tensors); no L2 flush (inputs "
+                       "> L2 except the tiny workload)"},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "kernels": kernels,
+        "path": path,
+        "other_paths": other,
+        "uniform_ids_control": control,
+        "decode": {"steps": decode,
+                   "how": "streaming decode, one token per sequence and step, on the same table and weights "
+                          "(decode lookup -> projection with N = sequences -> decode conv where the module has "
+                          "one); 16 consecutive steps in one CUDA graph replayed back to back, no L2 flush "
+                          "(table rows cold, W and the state warm, as in serving); not part of value"},
+        "clocks": clk.summary(),
+        "wall_s_timed_loop": round(t_wall, 4),
+    }
+    del p, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_gpu(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    head = measure_workload(args.config, args, dev, rank, world, args.steps, headline=True)
+    extras = {}
+    for cfg in args.extra:
+        extras[str(cfg)] = measure_workload(cfg, args, dev, rank, world, max(args.steps, EXTRA_MIN_STEPS),
+                                            headline=False)
+
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(step_ms), 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if p.w.dtype == p.W.DT_F32 else "bf16",
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
             "data": "synthetic: seeded Zipf token IDs, int8/64 table values, N(0,0.02) weights, N(0,1) states",
-            "config": workload_config(p.w, world),
-            "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
-                    "how": f"{e2e_steps} steps pipelined: each uploads its inputs from pinned host memory and "
-                           "reads its whole result back; uploads, kernels and read-backs of consecutive steps "
-                           "overlap on three streams (double-buffered device tensors); no L2 flush (inputs "
-                           "> L2 except the tiny workload)"},
-            "gpu_launches": launches,
-            "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                         "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "frac_nominal": round(achieved / NOMINAL_PEAK[bound], 4),
-                         "peak_source": ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz" if bound == "alu"
-                                         else f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})")},
-            "kernels": kernels,
-            "path": path,
-            "other_paths": other,
-            "uniform_ids_control": control,
-            "decode": {"steps": decode,
-                       "how": "streaming decode, one token per sequence and step, on the same table and weights "
-                              "(decode lookup -> projection with N = sequences -> decode conv where the module has "
-                              "one); 16 consecutive steps in one CUDA graph replayed back to back, no L2 flush "
-                              "(table rows cold, W and the state warm, as in serving); not part of value"},
-            "clocks": clocks,
-            "wall_s_timed_loop": round(t_wall, 4),
+            "config": head["config"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+            "roofline": head["roofline"], "clocks": head["clocks"],
         }
+        for k in ("kernels", "path", "other_paths", "uniform_ids_control", "decode", "wall_s_timed_loop"):
+            line[k] = head[k]
+        if extras:
+            line["workloads"] = extras
+            line["workloads_how"] = (f"the other workloads, each timed like the headline over max(steps, "
+                                     f"{EXTRA_MIN_STEPS}) steps after the same warm-up; not part of value")
         if world == 1 and not args.no_cpu_baseline:
-            if p.spec.table_bytes > (8 << 30):
-                line["cpu_baseline"] = None   # the table does not fit the host-side oracle leg
-            else:
-                line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+            cpu = cpu_baselines([args.config] + list(args.extra), args.cpu_seconds)
+            line["cpu_baseline"] = cpu.get(args.config)
+            for cfg in args.extra:
+                extras[str(cfg)]["cpu_baseline"] = cpu.get(cfg)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -671,155 +763,642 @@ def traffic_of(cfg, stage):
     return nbytes if now == sha else None
 
 
+WORKLOAD_DESC = {
+    1: "tiny fp32 PageGram table (P_n=64, K=8, S=4, r=64); 4096 uniform IDs over 1024; fp32 W_V 1024->256",
+    2: "PageGram 200M-parameter bf16 table: P_n = 48,823 / 48,821 pages, K=8, S=4, r=64; Zipf(1.1) IDs over "
+       "50,304; W_V 1024->768; scalar gate g=0.5",
+    3: "Engram-style 200M-parameter bf16 table: 16 prime subtables ~195k rows, r=64; same tokens as the PageGram "
+       "200M workload; W_V 1024->768; scalar gate g=0.5",
+    4: "20B-parameter PageGram table in NF4 (34-byte rows, 10.6 GB): P_n = 4,882,811 / 4,882,789, K=8, S=4; "
+       "Zipf(1.05) over 128,000 IDs folded to 98,010; gather + NF4 dequant + sign + concat",
+    5: "Engram-27B-shaped module: 16 prime subtables ~2.2266M rows, r=80, bf16 (5.7 GB); Zipf(1.05) over 128k "
+       "with canonical folding; fused W_V + 4 W_K (1280 -> 12800); RMSNorm-sigmoid gate; causal depthwise conv "
+       "k=4 dilation 3 + SiLU + residual into 4 branches of d=2560",
+}
+
+
 def workload_config(w, world):
     t = w.tables[0]
-    desc = {2: "PageGram 200M-parameter bf16 table: P_n = 48,823 / 48,821 pages, K=8, S=4, r=64; "
-               "Zipf(1.1) IDs over 50,304; W_V 1024->768; scalar gate g=0.5",
-            4: "20B-parameter PageGram table in NF4 (34-byte rows, 10.6 GB): P_n = 4,882,811 / 4,882,789, K=8, "
-               "S=4; Zipf(1.05) over 128,000 IDs folded to 98,010; gather + NF4 dequant + sign + concat",
-            1: "tiny fp32 PageGram table (P_n=64, K=8, S=4, r=64); 4096 uniform IDs over 1024; fp32 W_V 1024->256",
-            5: "Engram-27B-shaped module: 16 prime subtables ~2.2266M rows, r=80, bf16; Zipf(1.05) over 128k "
-               "with canonical folding; fused W_V + 4 W_K (1280 -> 12800); RMSNorm-sigmoid gate; causal "
-               "depthwise conv k=4 dilation 3 + SiLU + residual into 4 branches of d=2560"}.get(w.cfg_id, w.name)
-    return {"workload": f"{w.name} (config {w.cfg_id}): {desc}", "batch": f"{w.B}x{w.L}", "tokens_per_gpu": w.N,
+    return {"workload": f"{w.name} (config {w.cfg_id}): {WORKLOAD_DESC.get(w.cfg_id, w.name)}",
+            "batch": f"{w.B}x{w.L}", "tokens_per_gpu": w.N,
             "table_bytes": t.table_bytes, "parallelism": f"dp{world} (independent batches, no collective)",
             "l2": "flushed between timed steps (256 MiB written, then read back, untimed); "
                   "table and activations > L2"}
 
 
 # ---------------------------------------------------------------- CPU oracle legs
+#
+# The oracle, as it stands, on the host cores: every stage of the path over a bounded
+# sample of a workload (the first n tokens of its batch: the prefix of the first sequence,
+# or whole sequences), each stage timed on its own. With T threads the sample is split
+# into T contiguous token ranges run concurrently (the C stages and numpy's fp64 kernels
+# release the GIL; BLAS is held to one thread per range); the conv's ranges start 9
+# positions early so every output sees its full causal window.
 
-def _oracle_sample(cfg: int, ntok: int):
-    """Runs the oracle over the first `ntok` tokens of the workload; returns seconds."""
-    import numpy as np
-    import torch
-
-    from hashed_head_gram_gb300 import workloads as W
-    from oracle import dense, oracle as orc
-
-    w = W.make_workload(cfg)
-    spec = w.tables[0]
-    tokens = W.make_tokens(w)
-    cmap = W.make_canon_map(w)
-    L = w.L
-    nseq = max(1, (ntok + L - 1) // L)
-    tok = tokens[:nseq]
-    which = np.arange(min(ntok, nseq * L), dtype=np.int64)
-    table = _cpu_table(w, spec)
-    dn = _cpu_dense(w)
-    t0 = time.perf_counter()
-    canon, rows, signs, bad = orc.index(spec, tok, cmap, w.vocab, which)
-    rowdata = orc.fetch_rows(table, rows)
-    e = orc.assemble(spec, rows, rowdata, signs, orc.F32 if spec.row_dtype == W.DT_F32 else orc.BF16)
-    if w.cfg_id == 4:   # the lookup ends at e_t
-        return time.perf_counter() - t0, len(which)
-    ef = e.astype(np.float64) if spec.row_dtype == W.DT_F32 else orc.bf16_bits_to_f64(e)
-    if w.gate == W.GATE_NONE:
-        dense.project(ef, dn["W"])
-    elif w.gate == W.GATE_SCALAR:
-        v = dense.project(ef, dn["W"])
-        dense.scalar_gate(dn["x"][:len(which)], v, w.g)
-    else:
-        v, a = dense.engram_gate(ef, dn["W"], dn["H"][:, :len(which)], dn["gh"], dn["gk"], w.eps, w.M)
-        n = len(which) // L * L
-        if n:
-            dense.conv_residual(v[:n].reshape(-1, L, w.d), a[:, :n].reshape(w.M, -1, L), dn["gc"], dn["cw"],
-                                w.dilation, w.eps, dn["H"][:, :n].reshape(w.M, -1, L, w.d))
-    return time.perf_counter() - t0, len(which)
+def host_cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
 
 
-_CPU_CACHE = {}
+class OracleLeg:
+    """Inputs of one workload's CPU leg, prepared once; run() times one pass."""
 
+    TABLE_MATERIALISE_BYTES = 1 << 30
 
-def _cpu_table(w, spec):
-    """Host copy of the table rows. The table tensor is generated on the CPU with the
-    same seeded generator kind the tests use (only the rows are needed)."""
-    import numpy as np
-    from hashed_head_gram_gb300 import workloads as W
-    key = ("t", w.cfg_id)
-    if key not in _CPU_CACHE:
-        if spec.table_bytes > (8 << 30):
-            raise RuntimeError("table too large for the CPU baseline leg")
-        t = W.make_table(w, spec, "cpu")
-        _CPU_CACHE[key] = t.view(__import__("torch").uint8).reshape(spec.table_rows, spec.row_bytes).numpy()
-    return _CPU_CACHE[key]
+    def __init__(self, cfg: int, threads: int):
+        import numpy as np
+        import torch
 
+        from hashed_head_gram_gb300 import workloads as W
+        from oracle import dense, oracle as orc
 
-def _cpu_dense(w):
-    from hashed_head_gram_gb300 import workloads as W
-    key = ("d", w.cfg_id)
-    if key not in _CPU_CACHE:
-        dn = W.make_dense(w, "cpu")
-        out = {"W": dn["W"].double().numpy()}
+        self.np, self.W, self.orc, self.dense = np, W, orc, dense
+        w = self.w = W.make_workload(cfg)
+        self.spec = w.tables[0]
+        self.threads = threads
+        self.tokens = W.make_tokens(w)
+        self.cmap = W.make_canon_map(w)
+        self.pool = None
+        if threads > 1:
+            from concurrent.futures import ThreadPoolExecutor
+            self.pool = ThreadPoolExecutor(threads)
+        spec = self.spec
+        if spec.table_bytes <= self.TABLE_MATERIALISE_BYTES:
+            t = W.make_table(w, spec, "cpu")
+            self.table = t.view(torch.uint8).reshape(spec.table_rows, spec.row_bytes).numpy()
+            self.table_note = "the whole table in host memory"
+        else:
+            self.table = None
+            self.table_note = ("the sample's distinct rows in a compact host table (row ids remapped between the "
+                               "index and gather stages, untimed): the full table does not fit the leg")
+        self.dn_t = W.make_dense(w, "cpu")
+        self.n = 0
+
+    def prepare(self, n: int):
+        """Sample = the first n tokens (n <= L: a prefix of sequence 0; else whole sequences)."""
+        np, w = self.np, self.w
+        n = max(1, min(n, w.N))
+        if n > w.L:
+            n = n // w.L * w.L
+        self.n = n
+        self.nseq = (n + w.L - 1) // w.L
+        self.tok = np.ascontiguousarray(self.tokens[:self.nseq])
+        parts = np.array_split(np.arange(n, dtype=np.int64), self.threads)
+        self.which = [p for p in parts if len(p)]
+        if self.table is None:
+            _, rows, _, _ = self.orc.index(self.spec, self.tok, self.cmap, self.w.vocab, np.arange(n, dtype=np.int64))
+            flat = rows.reshape(-1)
+            self.uniq = np.unique(flat[flat != self.orc.NO_ROW])
+            rng = np.random.default_rng(self.w.cfg_id)
+            rb = self.spec.row_bytes
+            if self.spec.row_dtype == self.W.DT_NF4:
+                ct = rng.integers(0, 256, (len(self.uniq), rb), dtype=np.uint8)
+                sc = (1.0 + rng.integers(0, 1024, len(self.uniq)) / 1024.0).astype(np.float16).view(np.uint8)
+                ct[:, 32:34] = sc.reshape(-1, 2)
+            else:
+                q = rng.integers(-128, 128, (len(self.uniq), self.spec.r)).astype(np.float32) / 64
+                bits = q.view(np.uint32) if self.spec.row_dtype == self.W.DT_F32 else \
+                    (q.view(np.uint32) >> 16).astype(np.uint16)
+                ct = np.ascontiguousarray(bits).view(np.uint8).reshape(len(self.uniq), rb)
+            self.compact = ct
+        dn, M, d = self.dn_t, w.M, w.d
+        self.Wd = dn["W"].double().numpy()
         if "x" in dn:
-            out["x"] = dn["x"].double().numpy()
+            self.x = dn["x"][:n].double().numpy()
         if "H" in dn:
-            out.update(H=dn["H"][:, :8192].double().numpy(), gh=dn["gamma_h"].double().numpy(),
-                       gk=dn["gamma_k"].double().numpy(), gc=dn["gamma_c"].double().numpy(),
-                       cw=dn["conv_w"].double().numpy())
-        _CPU_CACHE[key] = out
-    return _CPU_CACHE[key]
+            self.H = dn["H"][:, :n].double().numpy()
+            self.gh, self.gk = dn["gamma_h"].double().numpy(), dn["gamma_k"].double().numpy()
+            self.gc, self.cw = dn["gamma_c"].double().numpy(), dn["conv_w"].double().numpy()
+        return n
+
+    def _map(self, fn, items):
+        return list(self.pool.map(fn, items)) if self.pool is not None else [fn(x) for x in items]
+
+    def run(self):
+        """One pass of every stage over the sample; returns {stage: seconds}."""
+        np, orc, dense, w, spec = self.np, self.orc, self.dense, self.w, self.spec
+        t = {}
+        t0 = time.perf_counter()
+        idx = self._map(lambda wh: orc.index(spec, self.tok, self.cmap, w.vocab, wh), self.which)
+        t["index"] = time.perf_counter() - t0
+        rows = [r for (_, r, _, _) in idx]
+        table = self.table
+        if table is None:   # remap to the compact table (untimed: not the oracle's work)
+            table = self.compact
+            remapped = []
+            for r in rows:
+                rr = np.full(r.shape, orc.NO_ROW, np.uint32)
+                ok = r != orc.NO_ROW
+                rr[ok] = np.searchsorted(self.uniq, r[ok]).astype(np.uint32)
+                remapped.append(rr)
+            rows = remapped
+        odt = orc.F32 if spec.row_dtype == self.W.DT_F32 else orc.BF16
+        t0 = time.perf_counter()
+        es = self._map(lambda a: orc.assemble(spec, a[0], orc.fetch_rows(table, a[0]), a[1][2], odt),
+                       list(zip(rows, idx)))
+        t["gather"] = time.perf_counter() - t0
+        if w.cfg_id == 4:   # the lookup ends at e_t
+            return t
+        ctx = w.gate == self.W.GATE_CONTEXT
+
+        def dense_part(a):
+            e, wh = a
+            ef = e.astype(np.float64) if odt == orc.F32 else orc.bf16_bits_to_f64(e)
+            if w.gate == self.W.GATE_NONE:
+                return dense.project(ef, self.Wd)
+            if w.gate == self.W.GATE_SCALAR:
+                return dense.scalar_gate(self.x[wh[0]:wh[-1] + 1], dense.project(ef, self.Wd), w.g)
+            return dense.engram_gate(ef, self.Wd, self.H[:, wh[0]:wh[-1] + 1], self.gh, self.gk, w.eps, w.M)
+
+        t0 = time.perf_counter()
+        res = self._map(dense_part, list(zip(es, self.which)))
+        t["project_gate"] = time.perf_counter() - t0
+        if not ctx:
+            return t
+        v = np.concatenate([r[0] for r in res])
+        alpha = np.concatenate([r[1] for r in res], axis=1)
+        segs = conv_segments(self.n, w.L, self.threads, (w.conv_kernel - 1) * w.dilation)
+        t0 = time.perf_counter()
+        self._map(lambda sg: conv_range(dense, sg, v, alpha, self.gc, self.cw, w.dilation, w.eps, self.H), segs)
+        t["conv"] = time.perf_counter() - t0
+        return t
 
 
-def cpu_baseline(cfg: int, seconds: float):
-    """The oracle as it stands on the host cores, on a bounded sample of the workload."""
-    dt, n = _oracle_sample(cfg, 1024)                     # calibration
-    w = __import__("hashed_head_gram_gb300.workloads", fromlist=["x"]).make_workload(cfg)
-    cap = 8192 if w.gate == 2 else 1 << 16   # the host copy of the branch states holds 8192 tokens
-    want = int(max(1024, min(cap, n * seconds / max(dt, 1e-3))))
-    dt, n = _oracle_sample(cfg, want)
-    return {"value": round(n / dt, 1), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {n} tokens of the workload batch; C stages single-threaded, numpy fp64 "
-                      f"projection/gate on the BLAS thread pool (up to {os.cpu_count()} cores); {dt:.2f} s"}
+def conv_segments(n, L, threads, halo):
+    """Token ranges for the conv over the first n flat tokens of sequences of length L:
+    each sequence split into enough pieces for `threads` workers; (a0, a, b) = the piece
+    [a, b) computed from a0 = max(sequence start, a - halo), so that every output in it
+    sees its whole causal window."""
+    import numpy as np
+    nseq = (n + L - 1) // L
+    per_seq = max(1, -(-threads // nseq))
+    segs = []
+    for s in range(nseq):
+        lo, hi = s * L, min(n, (s + 1) * L)
+        for piece in np.array_split(np.arange(lo, hi), per_seq):
+            if len(piece):
+                a = int(piece[0])
+                segs.append((max(lo, a - halo), a, int(piece[-1]) + 1))
+    return segs
+
+
+def conv_range(dense, seg, v, alpha, gc, cw, dilation, eps, H):
+    """The oracle's conv + residual over one (a0, a, b) range of flat tokens: H + Y at [a, b)."""
+    a0, a, b = seg
+    out = dense.conv_residual(v[a0:b][None], alpha[:, a0:b][:, None], gc, cw, dilation, eps, H[:, a0:b][:, None])
+    return out[:, 0, a - a0:]
+
+
+def _leg_summary(leg, passes, stat=statistics.median):
+    """tokens/s per stage and for the whole path (per-token time = the sum of the stages')."""
+    n = leg.n
+    stages = {k: stat([p[k] for p in passes]) for k in passes[0]}
+    total = sum(stages.values())
+    return {"value": round(n / total, 1), "unit": "tokens/s", "threads": leg.threads,
+            "stages_tokens_per_s": {k: round(n / s, 1) for k, s in stages.items()},
+            "sample_tokens": n, "passes": len(passes), "seconds_per_pass": round(total, 3)}
+
+
+def oracle_leg(cfg: int, threads: int, seconds: float):
+    """Sized sample (about `seconds` per pass after a 64-token calibration), one warm pass,
+    then the median of a few passes."""
+    leg = OracleLeg(cfg, threads)
+    leg.prepare(64 * threads)
+    leg.run()
+    cal = leg.run()
+    per_tok = sum(cal.values()) / leg.n
+    cap = 16384 if leg.w.gate == leg.W.GATE_CONTEXT else 65536
+    leg.prepare(int(min(cap, max(64 * threads, seconds / max(per_tok, 1e-9)))))
+    leg.run()
+    passes = [leg.run() for _ in range(3)]
+    out = _leg_summary(leg, passes)
+    out["table"] = leg.table_note
+    return out
+
+
+def run_oracle_legs(args):
+    """Child process of cpu_baselines(): BLAS is held to one thread by the environment the
+    parent set before this interpreter started."""
+    res = {}
+    for cfg in [int(c) for c in args.oracle_legs.split(",")]:
+        res[cfg] = oracle_leg(cfg, args.threads, args.cpu_seconds)
+    print(json.dumps(res), flush=True)
+
+
+def _one_thread_env(threads):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+              "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["PG_ORACLE_THREADS"] = str(threads)
+    env.pop("CUDA_VISIBLE_DEVICES", None)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    return env
+
+
+def cpu_baselines(cfgs, seconds):
+    """The oracle on the host cores for each workload, at 1 thread and at nproc threads, in
+    child processes (BLAS threads fixed at start-up; no GPU)."""
+    nproc = os.cpu_count() or 1
+    model = host_cpu_model()
+    out = {}
+    legs = {}
+    for threads in sorted({1, nproc}):
+        cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--oracle-legs",
+               ",".join(str(c) for c in cfgs), "--threads", str(threads), "--cpu-seconds", str(seconds)]
+        r = subprocess.run(cmd, capture_output=True, text=True, env=_one_thread_env(threads), timeout=1800)
+        if r.returncode != 0:
+            raise RuntimeError(f"oracle leg failed ({threads} threads):\n{r.stderr[-3000:]}")
+        legs[threads] = {int(k): v for k, v in json.loads(r.stdout.strip().splitlines()[-1]).items()}
+    for cfg in cfgs:
+        one, many = legs[1][cfg], legs[nproc][cfg]
+        out[cfg] = {"value": many["value"], "unit": "tokens/s", "cores": nproc, "kind": "oracle",
+                    "threads_1": one, "threads_nproc": many, "cpu_model": model,
+                    "sample": (f"first {many['sample_tokens']} tokens of the workload batch ({one['sample_tokens']} "
+                               f"at 1 thread); every stage of the path "
+                               f"({', '.join(many['stages_tokens_per_s'])}) timed on its own, median of 3 passes, "
+                               f"whole-path rate from the summed per-token times; {many['table']}")}
+    return out
 
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands on the host cores (nproc threads by
+    default), one pass over a bounded sample of the workload per step."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    dt1, n1 = _oracle_sample(args.config, 256)
-    budget = 60.0                                         # seconds for the whole run
-    per_step = max(64, min(1 << 14, int(n1 * budget / max((args.steps + args.warmup) * dt1, 1e-6))))
+    threads = args.threads or (os.cpu_count() or 1)
+    leg = OracleLeg(args.config, threads)
+    leg.prepare(64 * threads)
+    leg.run()
+    cal = leg.run()
+    per_tok = sum(cal.values()) / leg.n
+    budget = 90.0                                         # seconds for the warm-up and timed steps
+    per_step = budget / (args.steps + args.warmup)
+    cap = 16384 if leg.w.gate == leg.W.GATE_CONTEXT else 65536
+    leg.prepare(int(min(cap, max(64, per_step / max(per_tok, 1e-9)))))
     for _ in range(args.warmup):
-        _oracle_sample(args.config, per_step)
-    total_t, total_n = 0.0, 0
-    for _ in range(args.steps):
-        dt, n = _oracle_sample(args.config, per_step)
-        total_t += dt
-        total_n += n
-    value = total_n / total_t
+        leg.run()
+    passes = [leg.run() for _ in range(args.steps)]
+    total_t = sum(sum(p.values()) for p in passes)
+    value = leg.n * args.steps / total_t
+    summ = _leg_summary(leg, passes, stat=statistics.mean)
     from hashed_head_gram_gb300 import workloads as W
     w = W.make_workload(args.config)
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_t / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (same seeded workload as the GPU arm)", "config": workload_config(w, 1),
-            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": os.cpu_count(),
-                             "kind": "oracle",
-                             "sample": f"{per_step} tokens per step from the workload batch"},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "cpu_model": host_cpu_model(), "stages_tokens_per_s": summ["stages_tokens_per_s"],
+                             "sample": f"{leg.n} tokens per step (the first of the workload batch), every stage "
+                                       f"of the path on {threads} threads; {leg.table_note}"},
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- single-kernel cases
+
+def _kflush(buf):
+    buf.add_(1)
+    buf.sum(dtype=buf.dtype)  # read back: the written lines leave L2 here, not in the next launch
+
+
+def _ktime(fn, iters: int, dev) -> float:
+    """Median CUDA-event time (us) of fn over `iters` launches, L2 flushed between them."""
+    import torch
+    flush = torch.zeros(64 << 20, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        fn()
+        _kflush(flush)
+    torch.cuda.synchronize()
+    marks = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        _kflush(flush)
+        marks.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in marks) * 1e3
+
+
+def run_kernel_case(args):
+    """One kernel at a time on a workload's shapes, through the C ABI exactly as the
+    benchmark launches it (the conv and projection cases need no table, so they hold at
+    most a few GB on the device). Prints the median time per launch and the rate."""
+    import torch
+
+    from hashed_head_gram_gb300 import pg, workloads as W
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.make_workload(args.config)
+    spec = w.tables[0]
+    g = torch.Generator(device=dev).manual_seed(12345)
+    dt = torch.float32 if w.dtype == W.DT_F32 else torch.bfloat16
+    code = pg.F32 if w.dtype == W.DT_F32 else pg.BF16
+    N, din, d, M = w.N, spec.e_width, w.d, w.M
+    kind = args.kernel
+    if kind == "decode":
+        _kernel_decode(w, args, dev, g)
+        return
+    if kind == "slots":
+        _kernel_slots(args, dev, g)
+        return
+    if kind in ("gather", "gather_project"):
+        if args.table_rows_scale < 1.0:
+            spec = _scaled_spec(W, spec, args.table_rows_scale)
+        desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+        tokens = torch.from_numpy(W.make_tokens(w)).to(dev)
+        cm = W.make_canon_map(w)
+        cm = None if cm is None else torch.from_numpy(cm.view("int32")).to(dev)
+        table = W.make_table(w, spec, dev)
+        e = torch.empty(N, din, dtype=dt, device=dev)
+    if kind == "gather":
+        us = _ktime(lambda: pg.gather_sign_concat(desc, tokens, table, e, code, canon_map=cm), args.iters, dev)
+        rb = spec.row_bytes if spec.row_dtype != W.DT_NF4 else 64
+        heads = 1 if spec.mode == W.MODE_FLAT else spec.K
+        byts = N * (len(spec.orders) * heads * rb + 4 + din * e.element_size())
+        print(f"gather_sign_concat config {w.cfg_id} (table {spec.table_bytes / 1e9:.2f} GB): {us:.1f} us, "
+              f"{byts / us / 1e3:.0f} GB/s (no-reuse bytes)")
+    elif kind == "nf4_export":
+        x = torch.randn(args.rows, 64, device=dev, generator=g)
+        out = torch.empty(args.rows, 34, dtype=torch.uint8, device=dev)
+        us = _ktime(lambda: pg.nf4_quantize(x, out), args.iters, dev)
+        byts = args.rows * (64 * 4 + 34)
+        print(f"nf4_quantize {args.rows} rows: {us:.1f} us, {byts / us / 1e3:.0f} GB/s, {args.rows / us:.1f} M rows/s")
+    elif kind == "gather_project":
+        if w.gate != W.GATE_SCALAR:
+            raise SystemExit("the one-launch case runs the scalar-gated workloads (configs 2, 3)")
+        Wm = (torch.randn(d, din, device=dev, generator=g) * 0.02).to(dt)
+        x = torch.randn(N, d, device=dev, generator=g).to(dt)
+        v = torch.empty(N, d, dtype=dt, device=dev)
+        ws = torch.empty(pg.gather_project_workspace_size(N, d, 0, pg.GATE_SCALAR) // 4 + 1, device=dev)
+        us = _ktime(lambda: pg.gather_project_gate(desc, tokens, table, e, Wm, d, pg.GATE_SCALAR, v, ws, canon_map=cm,
+                                                   g=w.g, x_resid=x), args.iters, dev)
+        print(f"gather_project_gate config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * d / us / 1e6:.1f} TFLOP/s, "
+              f"{N / us:.1f} M tokens/s")
+    elif kind == "project_fp8":
+        e = (torch.randint(-128, 128, (N, din), device=dev, generator=g).float() / 64).to(torch.bfloat16)
+        Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        qe = torch.empty(N, din, dtype=torch.uint8, device=dev)
+        se = torch.empty(N, device=dev)
+        qw = torch.empty((1 + M) * d, din, dtype=torch.uint8, device=dev)
+        sw = torch.empty((1 + M) * d, device=dev)
+        pg.fp8_quantize(Wm, qw, sw)
+        v = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+        quant = lambda: pg.fp8_quantize(e, qe, se)
+        quant()
+        if w.gate == W.GATE_CONTEXT:
+            H = torch.randn(M, N, d, device=dev, generator=g).to(torch.bfloat16)
+            one = torch.ones(d, device=dev)
+            alpha = torch.empty(M, N, device=dev)
+            ws = torch.empty(pg.workspace_size(N, din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4, device=dev)
+            fn = lambda: pg.project_gate_fp8(qe, se, qw, sw, d, pg.GATE_CONTEXT, v, M=M, h=H, gamma_h=one,
+                                             gamma_k=one, alpha_out=alpha, workspace=ws)
+        else:
+            x = torch.randn(N, d, device=dev, generator=g).to(torch.bfloat16)
+            fn = lambda: pg.project_gate_fp8(qe, se, qw, sw, d, pg.GATE_SCALAR, v, g=w.g, x_resid=x)
+        us = _ktime(fn, args.iters, dev)
+        uq = _ktime(quant, args.iters, dev)
+        print(f"project_gate_fp8 config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * (1 + M) * d / us / 1e6:.1f} "
+              f"TFLOP/s; fp8_quantize of e: {uq:.1f} us")
+    elif kind == "project":
+        e = (torch.randint(-128, 128, (N, din), device=dev, generator=g).float() / 64).to(dt)
+        Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(dt)
+        v = torch.empty(N, d, dtype=dt, device=dev)
+        if w.gate == W.GATE_CONTEXT:
+            H = torch.randn(M, N, d, device=dev, generator=g).to(dt)
+            one = torch.ones(d, device=dev)
+            alpha = torch.empty(M, N, device=dev)
+            ws = torch.empty(pg.workspace_size(N, din, d, M, code, pg.GATE_CONTEXT) // 4, device=dev)
+            fn = lambda: pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, v, code, M=M, h=H, gamma_h=one, gamma_k=one,
+                                         alpha_out=alpha, workspace=ws)
+        elif w.gate == W.GATE_SCALAR:
+            x = torch.randn(N, d, device=dev, generator=g).to(dt)
+            fn = lambda: pg.project_gate(e, Wm, d, pg.GATE_SCALAR, v, code, g=w.g, x_resid=x)
+        else:
+            fn = lambda: pg.project_gate(e, Wm, d, pg.GATE_NONE, v, code)
+        us = _ktime(fn, args.iters, dev)
+        print(f"project_gate config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * (1 + M) * d / us / 1e6:.1f} TFLOP/s")
+    elif kind == "conv":
+        if w.gate != W.GATE_CONTEXT:
+            raise SystemExit("the conv runs in the context-gated module (config 5)")
+        v = torch.randn(N, d, device=dev, generator=g).to(dt)
+        alpha = torch.rand(M, N, device=dev, generator=g)
+        gc = torch.ones(d, device=dev)
+        cw = torch.randn(d, w.conv_kernel, device=dev, generator=g) * 0.25
+        H = torch.randn(M, N, d, device=dev, generator=g).to(dt)
+        v_ms = (v.float() ** 2).mean(dim=1)  # as the projection hands it over in the module
+        us = _ktime(lambda: pg.conv_residual(w.B, w.L, d, M, code, v, alpha, gc, cw, H, dilation=w.dilation,
+                                             eps=w.eps, v_ms=v_ms), args.iters, dev)
+        byts = N * d * v.element_size() * (1 + 2 * M)
+        print(f"conv_residual config {w.cfg_id}: {us:.1f} us, {byts / us / 1e3:.0f} GB/s")
+    if pg.device_error() != 0:
+        raise SystemExit("device error word set")
+
+
+def _scaled_spec(W, spec, scale):
+    """The workload's table with its page / subtable counts scaled down (same layout and
+    row format): for captures that must hold only a few GB on the device."""
+    import dataclasses
+    if spec.mode == W.MODE_PAGEGRAM:
+        return dataclasses.replace(spec, pages=W.largest_primes(int(spec.pages[0] * scale), len(spec.orders)))
+    p = W.largest_primes(int(spec.rows[0][0] * scale), len(spec.orders) * spec.K)
+    return dataclasses.replace(spec, rows=[p[i * spec.K:(i + 1) * spec.K] for i in range(len(spec.orders))])
+
+
+def _kernel_decode(w, args, dev, g):
+    """Streaming decode steps, one token per sequence: pg_decode_lookup, the projection
+    (N = B) and, in the context-gated module, pg_decode_conv_residual. Timed per step
+    (eager, L2 flushed between steps) and as a CUDA graph of 16 consecutive steps replayed
+    back to back (the table rows stay cold, W and the state stay in L2 as in serving)."""
+    import torch
+
+    from hashed_head_gram_gb300 import pg, workloads as W
+
+    spec = w.tables[0]
+    if args.small_table:
+        import dataclasses
+        if spec.mode == W.MODE_PAGEGRAM:
+            spec = dataclasses.replace(spec, pages=W.largest_primes(25000, len(spec.orders)))
+        else:
+            p = W.largest_primes(100000, len(spec.orders) * spec.K)
+            spec = dataclasses.replace(spec, rows=[p[i * spec.K:(i + 1) * spec.K] for i in range(len(spec.orders))])
+    d, M, din = w.d, w.M, spec.e_width
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    cm = W.make_canon_map(w)
+    cm = None if cm is None else torch.from_numpy(cm.view("int32")).to(dev)
+    table = W.make_table(w, spec, dev)
+    Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    steps = 16
+    for B in [int(x) for x in args.batch.split(",")]:
+        tokens = torch.randint(0, w.vocab, (steps, B), device=dev, generator=g, dtype=torch.int32)
+        e = torch.empty(B, din, dtype=torch.bfloat16, device=dev)
+        v = torch.empty(B, d, dtype=torch.bfloat16, device=dev)
+        ctx = w.gate == W.GATE_CONTEXT
+        state = pg.DecodeState(B, d=d if ctx else 0, M=M if ctx else 0, dtype=pg.BF16, kernel_size=w.conv_kernel,
+                               dilation=w.dilation, device=dev)
+        if ctx:
+            H = torch.randn(M, B, d, device=dev, generator=g).to(torch.bfloat16)
+            one = torch.ones(d, device=dev)
+            cw = torch.randn(d, w.conv_kernel, device=dev, generator=g) * 0.25
+            alpha = torch.empty(M, B, device=dev)
+            v_ms = torch.empty(B, device=dev)
+            ws = torch.empty(pg.workspace_size(B, din, d, M, pg.BF16, pg.GATE_CONTEXT) // 4 + 4, device=dev)
+            calls = [
+                lambda s: pg.decode_lookup(desc, state, tokens[s], table, e, pg.BF16, canon_map=cm),
+                lambda s: pg.project_gate(e, Wm, d, pg.GATE_CONTEXT, v, pg.BF16, M=M, h=H, gamma_h=one, gamma_k=one,
+                                          alpha_out=alpha, workspace=ws, v_ms_out=v_ms),
+                lambda s: pg.decode_conv_residual(state, v, alpha, one, cw, H, eps=w.eps, v_ms=v_ms),
+            ]
+            names = ["decode_lookup", "project_gate(context)", "decode_conv_residual"]
+        else:
+            x = torch.randn(B, d, device=dev, generator=g).to(torch.bfloat16)
+            gate = pg.GATE_SCALAR if w.gate == W.GATE_SCALAR else pg.GATE_NONE
+            calls = [
+                lambda s: pg.decode_lookup(desc, state, tokens[s], table, e, pg.BF16, canon_map=cm),
+                lambda s: pg.project_gate(e, Wm, d, gate, v, pg.BF16, g=w.g,
+                                          x_resid=x if gate == pg.GATE_SCALAR else None),
+            ]
+            names = ["decode_lookup", "project_gate"]
+        step = lambda s=0: [c(s) for c in calls]
+        eager = _ktime(step, args.iters, dev)
+        parts = [_ktime(lambda c=c: c(0), args.iters, dev) for c in calls]
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for s in range(steps):
+                step(s)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for s in range(steps):
+                step(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, args.iters // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        per_step = a.elapsed_time(b) * 1e3 / (reps * steps)
+        if pg.device_error() != 0:
+            raise SystemExit("device error word set")
+        print(f"decode config {w.cfg_id} B={B}: eager step {eager:.1f} us "
+              f"({' + '.join(f'{n} {u:.1f}' for n, u in zip(names, parts))}); "
+              f"graph {per_step:.1f} us/step, {B / per_step:.3f} M tokens/s")
+
+
+def _kernel_slots(args, dev, g):
+    """The PageGram report's slot sweep S in {1, 4, 8, 15, 60} on the PageGram 200M
+    workload (bf16 table, P_n chosen so the budget stays fixed): the lookup and the
+    one-launch lookup + projection timed per S, and the correlated-collision statistic
+    (pg_collision_counts over 4M distinct bigrams) next to its (K - 1) / S expectation."""
+    import torch
+
+    from hashed_head_gram_gb300 import pg, workloads as W
+
+    w = W.make_workload(2)
+    tokens = torch.from_numpy(W.make_tokens(w)).to(dev)
+    N, d = w.N, w.d
+    e = torch.empty(N, 1024, dtype=torch.bfloat16, device=dev)
+    Wm = (torch.randn(d, 1024, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    x = torch.randn(N, d, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(pg.gather_project_workspace_size(N, d, 0, pg.GATE_SCALAR) // 4 + 1, device=dev)
+    n = 4_000_000
+    for S in W.SLOT_SWEEP:
+        spec = W.pagegram_slots(S)
+        desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+        table = W.make_table(w, spec, dev)
+        ug = _ktime(lambda: pg.gather_sign_concat(desc, tokens, table, e, pg.BF16), args.iters, dev)
+        uf = _ktime(lambda: pg.gather_project_gate(desc, tokens, table, e, Wm, d, pg.GATE_SCALAR, v, ws, g=w.g,
+                                                   x_resid=x), args.iters, dev)
+        grams = torch.from_numpy(W.distinct_ngrams(n, 2, w.vocab, seed=100 + S)).to(dev)
+        rows = torch.empty(2 * n, 2, spec.K, dtype=torch.int32, device=dev)
+        pg.canon_hash(desc, grams, rows)
+        span = spec.pages[0] * spec.K * S
+        cws = torch.empty(pg.collision_workspace_size(n, span), dtype=torch.uint8, device=dev)
+        counts = torch.empty(spec.K, dtype=torch.int64, device=dev)
+        uc = _ktime(lambda: pg.collision_counts(rows.view(-1)[2 * spec.K:], n, spec.K, 4 * spec.K, 0, span, counts,
+                                                cws), 3, dev)
+        c = counts.cpu().tolist()
+        del table
+        if pg.device_error() != 0:
+            raise SystemExit("device error word set")
+        print(f"S={S:2d} P_n={spec.pages}: gather {ug:.1f} us ({N / ug:.0f} M tok/s), gather+project one launch "
+              f"{uf:.1f} us ({N / uf:.0f} M tok/s); collisions over {n} bigrams: {c[0]} head-0 pairs, "
+              f"extra shared heads {sum(c[1:]) / max(c[0], 1):.4f} (K-1)/S = {7 / S:.4f}; counted in {uc:.0f} us")
+
+
+# ---------------------------------------------------------------- entry
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=list(ALL_WORKLOADS),
+                    help="the headline workload (default 5, the Engram-27B-shaped module)")
+    ap.add_argument("--workloads", default="all",
+                    help="'all' (the headline and the other four) or a comma list of workloads to measure besides "
+                         "the headline ('none' for the headline alone)")
     ap.add_argument("--path", choices=["auto", "overlap", "two_kernel", "fused"], default="auto",
                     help="how the lookup and the projection run: overlap = one launch writing e_t with the "
                          "gather on extra warps of the projection (pg_gather_project_gate); two_kernel = "
                          "pg_gather_sign_concat + pg_project_gate; fused = pg_lookup_project_gate (r = 64 bf16 "
                          "tables); auto = the first that applies, in that order. The others that apply are "
                          "timed too and reported as other_paths")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=1.0,
+                    help="CPU oracle legs: seconds of work per timed pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--threads", type=int, default=0, help="reference arm: host threads (default: all cores)")
+    ap.add_argument("--oracle-legs", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--kernel", choices=["gather", "project", "project_fp8", "gather_project", "conv", "nf4_export",
+                                         "decode", "slots"], default=None,
+                    help="time one kernel on the workload's shapes instead of the benchmark")
+    ap.add_argument("--iters", type=int, default=20, help="--kernel: timed launches")
+    ap.add_argument("--batch", default="1,16,256,4096", help="--kernel decode: sequences per step (comma list)")
+    ap.add_argument("--small-table", action="store_true",
+                    help="--kernel decode: the table with ~100k-row subtables / pages (for ncu captures)")
+    ap.add_argument("--table-rows-scale", type=float, default=1.0,
+                    help="--kernel gather / gather_project: scale the table's pages / subtable rows (for ncu "
+                         "captures of a few GB)")
+    ap.add_argument("--rows", type=int, default=8 << 20, help="--kernel nf4_export: fp32 head rows to export")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.oracle_legs:
+        run_oracle_legs(args)
+        return
+    if args.kernel:
+        run_kernel_case(args)
+        return
+    if args.workloads == "all":
+        args.extra = [c for c in ALL_WORKLOADS if c != args.config]
+    elif args.workloads == "none":
+        args.extra = []
+    else:
+        args.extra = [int(c) for c in args.workloads.split(",") if int(c) != args.config]
     if args.impl == "reference":
+        if not os.environ.get("PG_ORACLE_THREADS"):
+            # one BLAS thread per token range: the environment must be set before numpy loads
+            env = _one_thread_env(args.threads or (os.cpu_count() or 1))
+            for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                      "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+                os.environ[k] = env[k]
         run_reference(args)
     else:
         run_gpu(args)

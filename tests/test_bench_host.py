@@ -39,3 +39,30 @@ def test_peaks_measured_and_nominal():
 def test_whole_job_rate_counts_every_rank():
     assert bench.whole_job_rate(1000, 1, 2.0) == 500.0
     assert bench.whole_job_rate(1000, 4, 2.0) == 2000.0
+
+
+def test_oracle_conv_ranges_reproduce_the_whole_sequences():
+    # the CPU leg splits the conv over token ranges that start `halo` positions early;
+    # stitched together they equal the oracle's conv over whole sequences
+    import numpy as np
+    from oracle import dense
+    rng = np.random.default_rng(3)
+    L, nseq, d, M, dil, k = 37, 3, 16, 2, 3, 4
+    n = L * nseq
+    v = rng.standard_normal((n, d))
+    alpha = rng.random((M, n))
+    H = rng.standard_normal((M, n, d))
+    gc, cw = rng.random(d) + 0.5, rng.standard_normal((d, k)) * 0.25
+    ref = dense.conv_residual(v.reshape(nseq, L, d), alpha.reshape(M, nseq, L), gc, cw, dil, 1e-6,
+                              H.reshape(M, nseq, L, d)).reshape(M, n, d)
+    for threads in (1, 2, 5, 16):
+        segs = bench.conv_segments(n, L, threads, (k - 1) * dil)
+        covered = np.concatenate([np.arange(a, b) for _, a, b in segs])
+        assert (np.sort(covered) == np.arange(n)).all()
+        got = np.zeros_like(ref)
+        for sg in segs:
+            got[:, sg[1]:sg[2]] = bench.conv_range(dense, sg, v, alpha, gc, cw, dil, 1e-6, H)
+        assert np.allclose(got, ref, rtol=0, atol=1e-12)
+    # a prefix of one sequence (n < L)
+    segs = bench.conv_segments(20, L, 4, (k - 1) * dil)
+    assert segs[0] == (0, 0, 5) and all(a0 == max(0, a - 9) for a0, a, _ in segs)
