@@ -368,8 +368,11 @@ pg_status pg_gather_project_gate_workspace_size(int32_t N, int32_t d, int32_t M,
  *    BN = 256 if d % 256 == 0 else 128, exceeds PG_NOALLOC_SCRATCH_BYTES (at d = 2560,
  *    M = 4: N <= 34,952 tokens); nothing is enqueued then;
  *  - the first call on a device looks up the scratch array's device address on that
- *    device (cudaGetSymbolAddress, with the device current); make that first call before
- *    any stream capture;
+ *    device (cudaGetSymbolAddress, with the device current). With lazy module loading
+ *    (the CUDA default) that lookup may also be what loads the library's device code
+ *    on that device, the 16 MiB array with it; so make the first call at start-up,
+ *    before any stream capture, where a one-time load is acceptable;
+ *  - devices with an ordinal of 64 or more are not served: PG_ERR_DEVICE;
  *  - every call on a device shares the one array and overwrites all of the scratch it
  *    uses before reading it (no part has to start at zero); calls whose kernels overlap
  *    on the GPU (other streams, other host threads) race on it and must be ordered by

@@ -31,8 +31,10 @@ def test_noalloc_matches_the_workspace_entry_point_on_consecutive_calls(cuda):
     from hashed_head_gram_gb300 import pg
     lib = pg.lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    # the larger call first: the second call must not see its leftovers
-    for N, Din, d, M, seed in [(700, 1280, 2560, 4, 21), (129, 256, 384, 2, 22)]:
+    # the larger call first: the later calls must not see its leftovers. N <= 4 runs the
+    # few-rows kernel (64-column partial sums) through the same scratch.
+    for N, Din, d, M, seed in [(700, 1280, 2560, 4, 21), (129, 256, 384, 2, 22), (1, 1280, 2560, 4, 23),
+                               (4, 1280, 2560, 4, 24), (3, 256, 384, 2, 25)]:
         e, W, h, gh, gk = _case(N, Din, d, M, seed, cuda)
         v_ref = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
         a_ref = torch.empty(M, N, device=cuda)
@@ -67,3 +69,24 @@ def test_noalloc_refuses_requests_beyond_its_scratch(cuda):
                                                  _p(a), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert pg.STATUS[status] == "PG_ERR_SCRATCH_LIMIT"
     assert pg.launch_count() == before
+
+
+def test_noalloc_takes_no_device_memory(cuda):
+    # after a first call (which may load the library's device code, scratch array
+    # included), further calls leave the device's free memory unchanged
+    from hashed_head_gram_gb300 import pg
+    lib = pg.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    N, Din, d, M = 512, 1280, 2560, 4
+    e, W, h, gh, gk = _case(N, Din, d, M, 31, cuda)
+    v = torch.empty(N, d, dtype=torch.bfloat16, device=cuda)
+    a = torch.empty(M, N, device=cuda)
+    args = (N, Din, d, M, _p(e), _p(W), _p(h), _p(gh), _p(gk), 1e-6, _p(v), _p(a), stream)
+    assert lib.pg_project_gate_context_noalloc(*args) == 0
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        assert lib.pg_project_gate_context_noalloc(*args) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert pg.device_error() == 0
