@@ -458,6 +458,26 @@ __device__ __forceinline__ bool wait_ready(const uint32_t* flag, uint32_t need, 
   }
 }
 
+// Self-test of the two bounded waits every tcgen05 kernel here relies on: one thread
+// waits on an mbarrier phase that nothing completes, then on a ready counter that nothing
+// raises (the caller's zeroed word). Each wait must give up after its limit (~1 s) and the
+// kernel reports it through the device error word (2048: the mbarrier wait, 4096: the
+// counter wait) and returns; no copy, MMA or TMEM is involved.
+constexpr int kErrSelftestBarrier = 2048;
+constexpr int kErrSelftestCounter = 4096;
+
+__global__ void __launch_bounds__(32) wait_selftest_kernel(const uint32_t* __restrict__ flag, int* err_word) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  volatile int* abort = &abort_flag;
+  if (!mbar_wait(smem_u32(&bar), 0u, abort)) atomicOr(err_word, kErrSelftestBarrier);
+  if (!wait_ready(flag, 1u, abort)) atomicOr(err_word, kErrSelftestCounter);
+}
+
 // Epilogue operands and results move through 128 x 32 bf16 sub-tiles (64 bytes per row)
 // written / read by TMA with 64-byte swizzle: 16-byte chunk c of row r sits at
 // r * 64 + ((c ^ ((r >> 1) & 3)) * 16), so the 32 rows of a warp hit every bank.
@@ -1763,6 +1783,19 @@ extern "C" pg_status pg_gather_project_gate(const pg_table_desc* desc, const int
   st = dispatch_produce(gate_kind, ptrs, a, gat, stream);
   if (st != PG_OK || gate_kind != PG_GATE_CONTEXT) return st;
   return launch_alpha_finalize(a.partials, M, d / bn, static_cast<int>(N), d, eps, alpha_out, a.vpart, v_ms_out, stream);
+}
+
+// ==================================================================== self-test of the bounded waits
+
+extern "C" pg_status pg_selftest_bounded_waits(uint32_t* zero_word, pg_stream_t stream) {
+  if (!zero_word) return PG_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(zero_word) % 4) return PG_ERR_ALIGN;
+  int* err = pg::device_error_word();
+  if (!err) return pg::cuda_fail(cudaGetLastError());
+  cudaError_t e = cudaMemsetAsync(zero_word, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return pg::cuda_fail(e);
+  pg::wait_selftest_kernel<<<1, 32, 0, stream>>>(zero_word, err);
+  return pg::after_launch(1);
 }
 
 // ==================================================================== no-allocation variant

@@ -136,6 +136,8 @@ def _load():
     L.pg_collision_counts.argtypes = [vp, ctypes.c_int64, i32, ctypes.c_int64, u32, u32, vp, vp, sz, vp]
     L.pg_conv_residual.restype = ctypes.c_int
     L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp]
+    L.pg_selftest_bounded_waits.restype = ctypes.c_int
+    L.pg_selftest_bounded_waits.argtypes = [vp, vp]
     return L
 
 
@@ -436,6 +438,13 @@ def device_error(clear: bool = False) -> int:
     return code.value
 
 
+def selftest_bounded_waits(zero_word: torch.Tensor, stream=None):
+    """zero_word: a 4-byte device tensor (set to 0 by the call). Afterwards (about 2 s on
+    the device) the device error word holds 2048 | 4096 when both waits gave up as they
+    should."""
+    _check(_lib.pg_selftest_bounded_waits(_ptr(zero_word), _stream(stream)), "pg_selftest_bounded_waits")
+
+
 def dtype_code(t: torch.dtype) -> int:
     return {torch.float32: F32, torch.bfloat16: BF16}[t]
 
@@ -444,6 +453,6 @@ __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
            "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual",
            "decode_state_size", "DecodeState", "decode_reset", "decode_lookup", "decode_conv_residual",
-           "collision_workspace_size", "collision_counts", "launch_count", "device_error", "lib",
+           "collision_workspace_size", "collision_counts", "launch_count", "device_error", "selftest_bounded_waits", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

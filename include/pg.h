@@ -135,10 +135,26 @@ uint64_t pg_launch_count(void);
  * of decode-state checks (256 = pg_decode_reset met a slot outside [0, B), 512 = a
  * decode call met a position it cannot take; that sequence was skipped, left unchanged),
  * and of pg_collision_counts (1024 = a head-0 row outside the given span, or a head-0
- * group too large to compare pairwise; those n-grams or pairs were left out).
+ * group too large to compare pairwise; those n-grams or pairs were left out), and of
+ * pg_selftest_bounded_waits (2048, 4096).
  * Synchronizes the device. With clear != 0 the word is reset to 0.
  */
 pg_status pg_device_error(int32_t* code, int32_t clear);
+
+/*
+ * pg_selftest_bounded_waits -- checks, on the current device, that the bounded waits the
+ * tensor-core kernels use give up and report instead of hanging. The pages have no
+ * counterpart: this is failure handling of this library.
+ *
+ * One thread waits on an mbarrier phase that nothing completes, then on a ready counter
+ * that nothing raises (*zero_word, set to 0 by the call on `stream`); each wait gives up
+ * after about one second and ORs its code into the device error word (2048 = the mbarrier
+ * wait, 4096 = the counter wait), so a correct run leaves 2048 | 4096 there after about
+ * two seconds. No copy, tensor-core operation or TMEM is involved, and the device stays
+ * usable. zero_word: caller-owned device memory, 4 bytes, 4-byte aligned.
+ * PG_ERR_NULL / PG_ERR_ALIGN for a bad zero_word; PG_ERR_CUDA if the launch fails.
+ */
+pg_status pg_selftest_bounded_waits(uint32_t* zero_word, pg_stream_t stream);
 
 /*
  * Table geometry of a descriptor: number of stored rows (the table's first
