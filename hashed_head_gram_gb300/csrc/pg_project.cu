@@ -159,6 +159,13 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Plain (non-tensor) bulk copy global -> this CTA's shared memory, counted on `bar`; both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -332,6 +339,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+  return f;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// the two bf16 of a 32-bit word as an fp32 pair (low half first)
+__device__ __forceinline__ uint64_t bf16x2_as_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
 __device__ __forceinline__ void unpack_bf16x8(uint4 w, float* f) {
   f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
   f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
@@ -431,10 +463,15 @@ struct GemmBarriers {
   int abort;
 };
 
-template <int BN, bool GATHER, bool PAIR, bool PRODUCE>
+// Per epilogue slot, the column vectors of its sub-tile staged beside the operand: gamma_h,
+// gamma_k (context gate, k tiles) and FP8's per-column scales, 32 fp32 each.
+constexpr int kVecBytes = kEpiStagesMax * 3 * kEpiCols * 4;
+
+template <int BN, bool GATHER, bool PAIR, bool PRODUCE, bool VEC>
 constexpr size_t gemm_smem_bytes() {
   return 1024 /* alignment slack */ + gemm_stages<PAIR>() * (kABytes + (PAIR ? BN / 2 : BN) * kBK * 2) +
-         epi_stages<GATHER || PRODUCE>() * kEpiBytes + sizeof(GemmBarriers<gemm_stages<PAIR>()>) +
+         epi_stages<GATHER || PRODUCE>() * kEpiBytes + (VEC ? kVecBytes : 0) +
+         sizeof(GemmBarriers<gemm_stages<PAIR>()>) +
          (GATHER || PRODUCE ? kFusedItems * sizeof(ItemConst) : 0) +
          (PRODUCE ? kUnitSlots * kCanonStride * sizeof(uint32_t) : 0);
 }
@@ -526,7 +563,9 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSt * kAStage;
   uint8_t* sE = sB + kSt * kBStage;
-  GemmBarriers<kSt>* bars = reinterpret_cast<GemmBarriers<kSt>*>(sE + kEpiStages * kEpiBytes);
+  constexpr bool kVec = GATE == PG_GATE_CONTEXT || FP8;
+  float* s_vec = reinterpret_cast<float*>(sE + kEpiStages * kEpiBytes);  // [slot][gamma_h, gamma_k, scale][32]
+  GemmBarriers<kSt>* bars = reinterpret_cast<GemmBarriers<kSt>*>(sE + kEpiStages * kEpiBytes + (kVec ? kVecBytes : 0));
   ItemConst* s_ic = reinterpret_cast<ItemConst*>(bars + 1);
   // producing kernel: slot u holds at [i] the canonical ID of flat position (unit start - 3 + i)
   uint32_t* s_canon = reinterpret_cast<uint32_t*>(s_ic + (GATHER || PRODUCE ? kFusedItems : 0));
@@ -739,18 +778,23 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
           }
           const uint32_t full = smem_u32(&bars->epi_full[slot]);
           const uint32_t dst = smem_u32(sE + slot * kEpiBytes);
-          if (GATE == PG_GATE_SCALAR) {
-            mbar_expect_tx(full, kEpiBytes);
-            tma_load_2d(dst, &map_x, full, n0 + j * kEpiCols, m0);
-            issued |= 1u << slot;
-          } else if (is_k) {
-            const int m = n0 / args.d - 1;
-            const int kc = n0 - (m + 1) * args.d;
-            mbar_expect_tx(full, kEpiBytes);
-            tma_load_2d(dst, &map_h, full, kc + j * kEpiCols, m * args.N + m0);
-            issued |= 1u << slot;
-          } else {
+          float* vec = s_vec + slot * 3 * kEpiCols;
+          const uint32_t tx = (GATE == PG_GATE_SCALAR || is_k ? kEpiBytes : 0) + (is_k ? 2 * kEpiCols * 4 : 0) +
+                              (FP8 ? kEpiCols * 4 : 0);
+          if (tx == 0) {
             mbar_arrive(full);   // output staging only: hand the free slot over
+          } else {
+            mbar_expect_tx(full, tx);
+            if (GATE == PG_GATE_SCALAR) tma_load_2d(dst, &map_x, full, n0 + j * kEpiCols, m0);
+            if (is_k) {
+              const int m = n0 / args.d - 1;
+              const int kc = n0 - (m + 1) * args.d;
+              tma_load_2d(dst, &map_h, full, kc + j * kEpiCols, m * args.N + m0);
+              bulk_load(smem_u32(vec), args.gamma_h + kc + j * kEpiCols, kEpiCols * 4, full);
+              bulk_load(smem_u32(vec + kEpiCols), args.gamma_k + kc + j * kEpiCols, kEpiCols * 4, full);
+            }
+            if (FP8) bulk_load(smem_u32(vec + 2 * kEpiCols), args.sw + n0 + j * kEpiCols, kEpiCols * 4, full);
+            issued |= 1u << slot;
           }
         }
       }
@@ -1074,7 +1118,10 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
       const int m_br = is_k ? n0 / args.d - 1 : 0;
       const int kc = is_k ? n0 - (m_br + 1) * args.d : 0;
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
+      // context gate, k tiles: sums over the row's columns of g h k, k^2 and h^2 (g = gamma_h
+      // gamma_k), as fp32 pairs (even, odd column) in two interleaved sets; FP8: k without the
+      // row scale s_e, which multiplies the sums once at the end
+      uint64_t a_hk[2] = {0ull, 0ull}, a_kk[2] = {0ull, 0ull}, a_hh[2] = {0ull, 0ull};
       float s_vv = 0.f;  // context gate, v tiles: sum of the stored (bf16) v^2 of the row
       for (int j = 0; rows_here && j < kSub; ++j, ++seq) {
         const int slot = static_cast<int>(seq % kEpiStages);
@@ -1086,37 +1133,52 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
         uint32_t r[32];
         tmem_ld32(t_base + static_cast<uint32_t>(j * kEpiCols), r);
         tmem_ld_wait();
+        const float* vec = s_vec + slot * 3 * kEpiCols;
         if constexpr (FP8) {
+          const float4* sc = reinterpret_cast<const float4*>(vec + 2 * kEpiCols);  // s_w of the columns
+          if (is_k) {  // s_w[col] here, s_e[row] on the finished sums
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 c4 = sc[q];
+              r[4 * q + 0] = __float_as_uint(__uint_as_float(r[4 * q + 0]) * c4.x);
+              r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) * c4.y);
+              r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) * c4.z);
+              r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) * c4.w);
+            }
+          } else {
           // out = s_e[row] s_w[col] sum_k q_e q_w
           const float sr = live ? __ldg(args.sa + row) : 0.f;
-          const float4* sc = reinterpret_cast<const float4*>(args.sw + n0 + j * kEpiCols);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 c4 = __ldg(sc + q);
+            const float4 c4 = sc[q];
             r[4 * q + 0] = __float_as_uint(__uint_as_float(r[4 * q + 0]) * sr * c4.x);
             r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) * sr * c4.y);
             r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) * sr * c4.z);
             r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) * sr * c4.w);
           }
+          }
         }
         uint8_t* slot_p = sE + slot * kEpiBytes;
         if (is_k) {
-          const float4* gh = reinterpret_cast<const float4*>(args.gamma_h + kc + j * kEpiCols);
-          const float4* gk = reinterpret_cast<const float4*>(args.gamma_k + kc + j * kEpiCols);
+          const float4* gh = reinterpret_cast<const float4*>(vec);
+          const float4* gk = reinterpret_cast<const float4*>(vec + kEpiCols);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            float hf[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4*>(slot_p + epi_offset(row_in_tile, c)), hf);
-            const float4 gh0 = __ldg(gh + 2 * c), gh1 = __ldg(gh + 2 * c + 1);
-            const float4 gk0 = __ldg(gk + 2 * c), gk1 = __ldg(gk + 2 * c + 1);
-            const float ghv[8] = {gh0.x, gh0.y, gh0.z, gh0.w, gh1.x, gh1.y, gh1.z, gh1.w};
-            const float gkv[8] = {gk0.x, gk0.y, gk0.z, gk0.w, gk1.x, gk1.y, gk1.z, gk1.w};
+            const uint4 hw = *reinterpret_cast<const uint4*>(slot_p + epi_offset(row_in_tile, c));
+            const float4 gh0 = gh[2 * c], gh1 = gh[2 * c + 1];
+            const float4 gk0 = gk[2 * c], gk1 = gk[2 * c + 1];
+            const uint64_t g2[4] = {f2_mul(f2_pack(gh0.x, gh0.y), f2_pack(gk0.x, gk0.y)),
+                                    f2_mul(f2_pack(gh0.z, gh0.w), f2_pack(gk0.z, gk0.w)),
+                                    f2_mul(f2_pack(gh1.x, gh1.y), f2_pack(gk1.x, gk1.y)),
+                                    f2_mul(f2_pack(gh1.z, gh1.w), f2_pack(gk1.z, gk1.w))};
+            const uint64_t h2[4] = {bf16x2_as_f2(hw.x), bf16x2_as_f2(hw.y), bf16x2_as_f2(hw.z), bf16x2_as_f2(hw.w)};
+            const int set = c & 1;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float kv = __uint_as_float(r[8 * c + i]);
-              s_kk = fmaf(kv, kv, s_kk);
-              s_hh = fmaf(hf[i], hf[i], s_hh);
-              s_hk = fmaf(ghv[i] * gkv[i] * hf[i], kv, s_hk);
+            for (int i = 0; i < 4; ++i) {
+              const uint64_t k2 = f2_pack(__uint_as_float(r[8 * c + 2 * i]), __uint_as_float(r[8 * c + 2 * i + 1]));
+              a_kk[set] = f2_fma(k2, k2, a_kk[set]);
+              a_hh[set] = f2_fma(h2[i], h2[i], a_hh[set]);
+              a_hk[set] = f2_fma(f2_mul(g2[i], h2[i]), k2, a_hk[set]);
             }
           }
         } else {
@@ -1178,6 +1240,17 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
       else
         mbar_arrive(smem_u32(&bars->tmem_empty[acc]));
       if (is_k && live) {
+        const float2 hk0 = f2_unpack(a_hk[0]), hk1 = f2_unpack(a_hk[1]);
+        const float2 kk0 = f2_unpack(a_kk[0]), kk1 = f2_unpack(a_kk[1]);
+        const float2 hh0 = f2_unpack(a_hh[0]), hh1 = f2_unpack(a_hh[1]);
+        float s_hk = (hk0.x + hk0.y) + (hk1.x + hk1.y);
+        float s_kk = (kk0.x + kk0.y) + (kk1.x + kk1.y);
+        const float s_hh = (hh0.x + hh0.y) + (hh1.x + hh1.y);
+        if constexpr (FP8) {
+          const float sr = __ldg(args.sa + row);
+          s_hk *= sr;
+          s_kk *= sr * sr;
+        }
         float* p = args.partials + (static_cast<size_t>(m_br * tpb + kc / BN) * 3) * args.N + row;
         p[0] = s_hk;
         p[args.N] = s_kk;
@@ -1360,7 +1433,8 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
       !make_map(&mh, ptr.h, static_cast<uint64_t>(a.M) * a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
   auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR, PRODUCE, FP8>;
-  const size_t smem = gemm_smem_bytes<BN, GATHER, PAIR, PRODUCE>();
+  constexpr size_t smem = gemm_smem_bytes<BN, GATHER, PAIR, PRODUCE, GATE == PG_GATE_CONTEXT || FP8>();
+  static_assert(smem <= 232448, "dynamic shared memory above the 227 KB a CTA may hold");
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return cuda_fail(err);
