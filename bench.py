@@ -41,12 +41,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from the unit counts, 152 SMs x 128 FP32 lanes x 2 flop per FMA x 2.07 GHz (maximum SM
 # clock), and reported as an ALU bound.
 FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+FP8_OVER_BF16 = 4.5 / 2.25     # nominal dense FP8 / bf16 tensor rates of GB300
 ALL_WORKLOADS = (1, 2, 3, 4, 5)
 EXTRA_MIN_STEPS = 100          # timed steps of the workloads besides the headline
 
 # Nominal GB300 figures, reported beside the measured peaks: HBM3e 7.9 TB/s, dense bf16
 # 2.25 PFLOP/s; the FP32 FMA peak of the ALU-bound path is already the derived one.
-NOMINAL_PEAK = {"hbm": 7900.0, "tensor": 2250.0, "alu": FP32_FFMA_TFLOPS}
+NOMINAL_PEAK = {"hbm": 7900.0, "tensor": 2250.0, "tensor_fp8": 4500.0, "alu": FP32_FFMA_TFLOPS}
 
 
 # ---------------------------------------------------------------- rank / sharding helpers
@@ -193,6 +194,31 @@ class Pipeline:
     def gather(self):
         self.pg.gather_sign_concat(self.desc, self.tokens, self.table, self.e, self.pdt, canon_map=self.cmap)
 
+    def fp8_ready(self):
+        """E4M3 operands of the FP8 path: W quantised once (a weight), buffers for e_t's codes."""
+        if hasattr(self, "qe"):
+            return
+        torch, dn = self.torch, self.dn
+        self.qe = torch.empty(self.N, self.din, dtype=torch.uint8, device=self.dev)
+        self.se = torch.empty(self.N, device=self.dev)
+        self.qw = torch.empty(dn["W"].shape, dtype=torch.uint8, device=self.dev)
+        self.sw = torch.empty(dn["W"].shape[0], device=self.dev)
+        self.pg.fp8_quantize(dn["W"], self.qw, self.sw)
+        torch.cuda.synchronize()
+
+    def gather_q8(self):
+        self.pg.gather_sign_concat_e4m3(self.desc, self.tokens, self.table, self.qe, self.se, canon_map=self.cmap)
+
+    def project_fp8(self):
+        pg, w, dn = self.pg, self.w, self.dn
+        if w.gate == self.W.GATE_SCALAR:
+            pg.project_gate_fp8(self.qe, self.se, self.qw, self.sw, self.d, pg.GATE_SCALAR, self.out, g=w.g,
+                                x_resid=dn["x"])
+        else:
+            pg.project_gate_fp8(self.qe, self.se, self.qw, self.sw, self.d, pg.GATE_CONTEXT, self.v, M=w.M,
+                                h=dn["H"], gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"], eps=w.eps,
+                                alpha_out=self.alpha, workspace=self.ws, v_ms_out=self.v_ms)
+
     def decode(self, B: int, steps: int = 16, reps: int = 8):
         """Streaming decode on this workload's table and weights: B sequences, one token
         each per step (pg_decode_lookup, the projection with N = B, and in the context-gated
@@ -301,19 +327,30 @@ class Pipeline:
     def can_overlap(self):
         return self.can_fuse() and self.d % 256 == 0
 
+    def can_fp8(self):
+        sp = self.spec
+        return (sp.mode != self.W.MODE_FLAT and sp.row_dtype == self.W.DT_BF16 and sp.r in (64, 80)
+                and self.w.gate != self.W.GATE_NONE and self.d % 256 == 0 and self.din % 256 == 0)
+
     def paths(self):
-        """The ways this workload's step can run: the first is the default."""
+        """The ways this workload's step can run: the first is the default (bf16)."""
+        out = ["two_kernel"]
         if self.can_overlap():
-            return ["overlap", "two_kernel", "fused"]
-        if self.can_fuse():
-            return ["two_kernel", "fused"]
-        return ["two_kernel"]
+            out = ["overlap", "two_kernel", "fused"]
+        elif self.can_fuse():
+            out = ["two_kernel", "fused"]
+        if self.can_fp8():
+            out.append("fp8")
+        return out
 
     def stages(self, path="two_kernel"):
         if self.w.cfg_id == 4:   # the 20B NF4 table: the lookup ends at e_t
             return [("gather_sign_concat", self.gather)]
         if path == "overlap":
             st = [("gather_project_gate", self.overlap)]
+        elif path == "fp8":
+            self.fp8_ready()
+            st = [("gather_sign_concat_e4m3", self.gather_q8), ("project_gate_fp8", self.project_fp8)]
         elif path == "fused":
             st = [("lookup_project_gate", self.fused)]
         else:
@@ -387,6 +424,11 @@ class Pipeline:
             return "hbm", (rows * rb + 4 + e_b + self.epilogue_bytes()) * N + self.weight_bytes()
         if name == "lookup_project_gate":
             return "hbm", (rows * rb + 4 + self.epilogue_bytes()) * N + self.weight_bytes()
+        if name == "gather_sign_concat_e4m3":
+            # 2K rows + token ID + E4M3 e_t (1 byte per element) + its fp32 scale, per token
+            return "hbm", (rows * rb + 4 + din + 4) * N
+        if name == "project_gate_fp8":
+            return "tensor_fp8", 2.0 * N * din * d * (1 + w.M)
         if name == "project_gate":
             cols = d * (1 + w.M)
             return ("alu" if w.dtype == self.W.DT_F32 else "tensor"), 2.0 * N * din * cols
@@ -405,6 +447,8 @@ class Pipeline:
             return table_sectors_bytes + N * (4 + e_b + self.epilogue_bytes()) + self.weight_bytes()
         if name == "lookup_project_gate":
             return table_sectors_bytes + N * (4 + self.epilogue_bytes()) + self.weight_bytes()
+        if name == "gather_sign_concat_e4m3":
+            return table_sectors_bytes + N * (4 + self.din + 4)
         return None
 
 
@@ -480,6 +524,12 @@ def kernel_entry(p, name, ms, peaks, comp_sectors):
     if b == "alu":
         return {"ms": round(ms, 5), "TFLOP/s": round(wk / s / 1e12, 1),
                 "frac_fp32_ffma": round(wk / s / 1e12 / FP32_FFMA_TFLOPS, 4)}
+    if b == "tensor_fp8":
+        # FP8 peak = the measured bf16 peak x the nominal FP8 / bf16 ratio (4.5 / 2.25)
+        return {"ms": round(ms, 5), "TFLOP/s": round(wk / s / 1e12, 1),
+                "frac_tensor_fp8_burst": round(wk / s / 1e12 / (FP8_OVER_BF16 * float(peaks["bf16_tflops"])), 4),
+                "frac_tensor_fp8_sustained": round(wk / s / 1e12 / (FP8_OVER_BF16 * float(
+                    peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))), 4)}
     return {"ms": round(ms, 5), "TFLOP/s": round(wk / s / 1e12, 1),
             "frac_tensor_burst": round(wk / s / 1e12 / float(peaks["bf16_tflops"]), 4),
             "frac_tensor_sustained": round(wk / s / 1e12 / float(peaks.get("bf16_tflops_sustained",
@@ -512,9 +562,11 @@ def roofline_of(p, name, ms, peaks, peak_src, comp_sectors, cfg):
                    peak_source="derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz")
     else:
         achieved = work / s / 1e12
-        sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        ratio = FP8_OVER_BF16 if bound == "tensor_fp8" else 1.0   # FP8: measured bf16 x nominal ratio
+        sus = ratio * float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
         out.update(achieved=round(achieved, 2), peak=sus, unit="TFLOP/s", frac=round(achieved / sus, 4),
-                   frac_burst=round(achieved / float(peaks["bf16_tflops"]), 4), peak_burst=float(peaks["bf16_tflops"]),
+                   frac_burst=round(achieved / (ratio * float(peaks["bf16_tflops"])), 4),
+                   peak_burst=ratio * float(peaks["bf16_tflops"]),
                    peak_source=f"{peak_src} (bf16_tflops_sustained: cuBLAS bf16 back to back under the power cap; "
                                "the kernel runs inside a step of several launches)")
     out["frac_nominal"] = round(out["achieved"] / NOMINAL_PEAK[bound], 4)
@@ -653,7 +705,8 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
 
     out = {
         "value": round(value, 1), "unit": "tokens/s", "steps": steps, "ms_per_step": round(statistics.mean(step_ms), 5),
-        "dtype": "f32" if p.w.dtype == p.W.DT_F32 else "bf16",
+        "dtype": "f32" if p.w.dtype == p.W.DT_F32 else ("e4m3 projection operands, bf16 outputs" if path == "fp8"
+                                                        else "bf16"),
         "config": workload_config(p.w, world),
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -1355,12 +1408,13 @@ def main(argv=None):
     ap.add_argument("--workloads", default="all",
                     help="'all' (the headline and the other four) or a comma list of workloads to measure besides "
                          "the headline ('none' for the headline alone)")
-    ap.add_argument("--path", choices=["auto", "overlap", "two_kernel", "fused"], default="auto",
+    ap.add_argument("--path", choices=["auto", "overlap", "two_kernel", "fused", "fp8"], default="auto",
                     help="how the lookup and the projection run: overlap = one launch writing e_t with the "
                          "gather on extra warps of the projection (pg_gather_project_gate); two_kernel = "
                          "pg_gather_sign_concat + pg_project_gate; fused = pg_lookup_project_gate (r = 64 bf16 "
-                         "tables); auto = the first that applies, in that order. The others that apply are "
-                         "timed too and reported as other_paths")
+                         "tables); fp8 = pg_gather_sign_concat_e4m3 + pg_project_gate_fp8 (E4M3 operands); auto = "
+                         "the first bf16 path that applies, in that order. The others that apply are timed too "
+                         "and reported as other_paths")
     ap.add_argument("--cpu-seconds", type=float, default=1.0,
                     help="CPU oracle legs: seconds of work per timed pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")

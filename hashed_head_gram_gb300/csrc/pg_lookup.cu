@@ -17,6 +17,7 @@
 // section 3.2.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "pg_hash.cuh"
 
@@ -291,6 +292,139 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
       }
     }
     }  // rounds
+    __syncwarp();
+    cur ^= 1;
+  }
+}
+
+// ------------------------------------------------------------------ K2, E4M3 output
+
+// The gather with the FP8 projection's operand as its output (Engram notes section 3.4:
+// the fused projection runs in FP8): e_t of bf16 rows, quantised per token as
+// pg_fp8_quantize does it, q_i = E4M3(x_i / s) with s = max |x| / 448 (correctly rounded
+// fp32 division, round to nearest even, saturating; s = 0 stores zeros), so codes and
+// scales equal pg_gather_sign_concat (bf16) followed by pg_fp8_quantize bit for bit. The
+// batch, hash and load phases are the bf16 gather's; a warp batch holds whole tokens in
+// registers, so each token's max |x| is a warp reduction over the bf16 magnitudes (as
+// 15-bit patterns, whose integer order is their numeric order; NaN patterns left out).
+template <int RC, int ITEMS>
+__global__ void __launch_bounds__(kThreads, 3) gather_e4m3_kernel(
+    const __grid_constant__ HashParams P, uint64_t seed, const GatherGeom g, const int32_t* __restrict__ tokens,
+    const uint32_t* __restrict__ canon_map, const uint8_t* __restrict__ table, uint8_t* __restrict__ q_out,
+    float* __restrict__ scale_out, int32_t* err) {
+  constexpr int PT = ITEMS * RC;
+  constexpr int TBC = batch_tokens(PT, ITEMS);
+  constexpr int NCH = (TBC * PT + 31) / 32;
+  static_assert(TBC == 1 || PT % 32 == 0, "a lane's chunks of one step belong to one token");
+  constexpr int kWarpsPerBlock = kThreads / 32;
+  constexpr int E = 8;  // bf16 elements per 16-byte chunk
+  __shared__ ItemConst s_ic[kMaxItems];
+  __shared__ uint32_t s_rows_all[kWarpsPerBlock][2][32];
+  __shared__ uint64_t s_signs_all[kWarpsPerBlock][2][kMaxSignWords];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x < g.items) init_item_const(s_ic[threadIdx.x], P, seed, threadIdx.x);
+  __syncthreads();
+
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
+  if (first < g.nbatch)
+    hash_batch<ITEMS, TBC>(s_ic, g, P.mode, first, lane, tokens, canon_map, P.vocab, s_rows_all[warp][0],
+                           s_signs_all[warp][0], err);
+  __syncwarp();
+  int cur = 0;
+  for (int64_t batch = first; batch < g.nbatch; batch += nwarps) {
+    const uint32_t* rows = s_rows_all[warp][cur];
+    const uint64_t* signs = s_signs_all[warp][cur];
+    uint4 v[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const uint32_t c = lane + 32 * i;
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (c < static_cast<uint32_t>(TBC * PT)) {
+        const uint32_t sidx = c / PT, cc = c - sidx * PT;
+        if (batch * TBC + sidx < g.N) {
+          const uint32_t it = cc / RC, piece = cc - it * RC;
+          v[i] = ldg_stream(table + static_cast<uint64_t>(rows[sidx * ITEMS + it]) * (RC * 16u) + piece * 16u);
+        }
+      }
+    }
+    const int64_t next = batch + nwarps;
+    if (next < g.nbatch)
+      hash_batch<ITEMS, TBC>(s_ic, g, P.mode, next, lane, tokens, canon_map, P.vocab, s_rows_all[warp][cur ^ 1],
+                             s_signs_all[warp][cur ^ 1], err);
+    // sign, then each token's largest magnitude
+    uint32_t amax[TBC];
+#pragma unroll
+    for (int t = 0; t < TBC; ++t) amax[t] = 0u;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const uint32_t c = lane + 32 * i;
+      const uint32_t sidx = c / PT, cc = c - sidx * PT;
+      if (c >= static_cast<uint32_t>(TBC * PT)) continue;
+      const uint32_t it = cc / RC, piece = cc - it * RC;
+      const uint32_t e0 = piece * E;
+      const uint32_t bits =
+          static_cast<uint32_t>(signs[(sidx * ITEMS + it) * g.W + (e0 >> 6)] >> (e0 & 63)) & ((1u << E) - 1u);
+      v[i] = xor4(v[i], bf16_sign_mask(bits));
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t m = 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t lo = w[q] & 0x7FFFu, hi = (w[q] >> 16) & 0x7FFFu;
+        m = max(m, lo > 0x7F80u ? 0u : lo);
+        m = max(m, hi > 0x7F80u ? 0u : hi);
+      }
+      const int t = TBC == 1 ? 0 : static_cast<int>((32 * i) / PT);  // PT % 32 == 0 when TBC > 1
+      amax[t] = max(amax[t], m);
+    }
+    // scale s, and its correctly rounded reciprocal for the quotients (Markstein's division:
+    // q0 = RN(x y), r = x - q0 s exactly by an fma, q = RN(q0 + r y) is RN(x / s) when
+    // y = RN(1 / s) and nothing underflows). For s in [2^-90, 2^125] every quotient that can
+    // reach a nonzero E4M3 code (|x / s| >= 2^-10) has a normal remainder; outside it the
+    // quotients take the plain correctly rounded division.
+    float scl[TBC], rcp[TBC];
+    bool fast[TBC];
+#pragma unroll
+    for (int t = 0; t < TBC; ++t) {
+      const uint32_t m = __reduce_max_sync(0xffffffffu, amax[t]);
+      scl[t] = __fdiv_rn(__uint_as_float(m << 16), 448.0f);
+      rcp[t] = __frcp_rn(scl[t]);
+      fast[t] = scl[t] >= 0x1p-90f && scl[t] <= 0x1p125f;
+      const int64_t tok = batch * TBC + t;
+      if (lane == 0 && tok < g.N) scale_out[tok] = scl[t];
+    }
+    // codes, 8 per chunk (8 contiguous bytes of the token's row)
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const uint32_t c = lane + 32 * i;
+      if (c >= static_cast<uint32_t>(TBC * PT)) continue;
+      const uint32_t sidx = c / PT, cc = c - sidx * PT;
+      const int64_t tok = batch * TBC + sidx;
+      if (tok >= g.N) continue;
+      const int t = TBC == 1 ? 0 : static_cast<int>((32 * i) / PT);
+      const float sc = scl[t], y = rcp[t];
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t out[2] = {0u, 0u};
+      if (sc != 0.0f) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // the pair of elements in word q
+          float2 z = make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u));
+          if (fast[t]) {
+            const float q0 = __fmul_rn(z.x, y), q1 = __fmul_rn(z.y, y);
+            const float r0 = __fmaf_rn(-q0, sc, z.x), r1 = __fmaf_rn(-q1, sc, z.y);
+            z.x = r0 == 0.0f ? q0 : __fmaf_rn(r0, y, q0);
+            z.y = r1 == 0.0f ? q1 : __fmaf_rn(r1, y, q1);
+          } else {
+            z.x = __fdiv_rn(z.x, sc);
+            z.y = __fdiv_rn(z.y, sc);
+          }
+          const uint32_t b2 = __nv_cvt_float2_to_fp8x2(z, __NV_SATFINITE, __NV_E4M3);  // z.x in the low byte
+          out[q / 2] |= b2 << (16 * (q % 2));
+        }
+      }
+      *reinterpret_cast<uint2*>(q_out + static_cast<uint64_t>(tok) * (PT * E) + cc * E) = make_uint2(out[0], out[1]);
+    }
     __syncwarp();
     cur ^= 1;
   }
@@ -787,6 +921,67 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   return after_launch(1);
 }
 
+
+pg_status pg_gather_sign_concat_e4m3(const pg_table_desc* desc, const int32_t* tokens, int32_t B, int32_t L,
+                                     const uint32_t* canon_map, const void* table, uint64_t table_bytes,
+                                     uint8_t* q_out, float* scale_out, int32_t* err_index, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  Geometry geo;
+  pg_status st = validate_desc(desc, &geo);
+  if (st != PG_OK) return st;
+  if (desc->hash_kind != PG_HASH_MULXOR) return PG_ERR_UNSUPPORTED;
+  if (B < 0 || L < 0) return PG_ERR_SHAPE;
+  const int64_t N = static_cast<int64_t>(B) * L;
+  if (N >= (1ll << 31)) return PG_ERR_SHAPE;
+  if (N == 0) return PG_OK;
+  if (!tokens || !table || !q_out || !scale_out) return PG_ERR_NULL;
+  if (table_bytes < geo.rows * geo.row_bytes) return PG_ERR_RANGE;
+  if (reinterpret_cast<uintptr_t>(table) % 16 || reinterpret_cast<uintptr_t>(q_out) % 16 ||
+      reinterpret_cast<uintptr_t>(scale_out) % 4)
+    return PG_ERR_ALIGN;
+  if (desc->row_dtype != PG_BF16) return PG_ERR_DTYPE;
+  const int items = geo.O * geo.H;
+  const uint32_t rc = geo.row_bytes / 16u;
+  using E4Fn = void (*)(const HashParams, uint64_t, const GatherGeom, const int32_t*, const uint32_t*,
+                        const uint8_t*, uint8_t*, float*, int32_t*);
+  E4Fn fn = nullptr;
+  if (desc->mode != PG_FLAT && items == 16 && rc == 8) fn = gather_e4m3_kernel<8, 16>;
+  if (desc->mode != PG_FLAT && items == 16 && rc == 10) fn = gather_e4m3_kernel<10, 16>;
+  if (!fn) return PG_ERR_UNSUPPORTED;  // the layouts of the projected workloads (r = 64, 80; 16 heads)
+
+  GatherGeom g{};
+  g.N = N;
+  g.L = static_cast<uint32_t>(L);
+  g.fm_L = fastmod_constant(g.L);
+  g.items = items;
+  g.W = geo.W;
+  g.rc = rc;
+  g.per_tok = items * static_cast<int>(rc);
+  g.tb = batch_tokens(g.per_tok, items);
+  g.row_bytes = geo.row_bytes;
+  g.e_bytes = geo.e_width;
+  g.nbatch = (N + g.tb - 1) / g.tb;
+  g.table_bytes = table_bytes;
+  const int nsm = sm_count();
+  if (nsm == 0) return cuda_fail(cudaGetLastError());
+  st = prepare_err(err_index, stream);
+  if (st != PG_OK) return st;
+  HashParams P;
+  fill_hash_params(desc, geo, &P);
+  if (g.tb * items * geo.W > kMaxSignWords) return PG_ERR_UNSUPPORTED;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(fn),
+                                                                kThreads, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t cap = static_cast<int64_t>(nsm) * per_sm;
+  const int64_t want = (g.nbatch + kThreads / 32 - 1) / (kThreads / 32);
+  const int blocks = static_cast<int>(want < cap ? want : cap);
+  fn<<<blocks, kThreads, 0, stream>>>(P, desc->hash_seed, g, tokens, canon_map, static_cast<const uint8_t*>(table),
+                                      q_out, scale_out, err_index);
+  return after_launch(1);
+}
 
 pg_status pg_nf4_quantize(const float* x, int64_t nrows, int32_t r, void* out, pg_stream_t stream_) {
   using namespace pg;

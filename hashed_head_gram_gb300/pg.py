@@ -110,6 +110,8 @@ def _load():
                                          vp, f32, vp, vp, vp, vp, sz, vp, vp]
     L.pg_gather_project_gate_workspace_size.restype = ctypes.c_int
     L.pg_gather_project_gate_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
+    L.pg_gather_sign_concat_e4m3.restype = ctypes.c_int
+    L.pg_gather_sign_concat_e4m3.argtypes = [dp, vp, i32, i32, vp, vp, u64, vp, vp, vp, vp]
     L.pg_fp8_quantize.restype = ctypes.c_int
     L.pg_fp8_quantize.argtypes = [vp, i32, ctypes.c_int64, ctypes.c_int64, vp, vp, vp]
     L.pg_project_gate_fp8.restype = ctypes.c_int
@@ -216,6 +218,17 @@ def gather_sign_concat(desc: TableDesc, tokens: torch.Tensor, table: torch.Tenso
     _check(_lib.pg_gather_sign_concat(ctypes.byref(desc), _ptr(tokens), B, L, _ptr(canon_map), _ptr(table),
                                       nbytes, _ptr(e_out), out_dtype, _ptr(err_index), _stream(stream)),
            "pg_gather_sign_concat")
+
+
+def gather_sign_concat_e4m3(desc: TableDesc, tokens: torch.Tensor, table: torch.Tensor, q_out: torch.Tensor,
+                            scale_out: torch.Tensor, canon_map: Optional[torch.Tensor] = None,
+                            err_index: Optional[torch.Tensor] = None, stream=None):
+    """q_out: uint8 [B*L, e_width] E4M3 codes; scale_out: fp32 [B*L]."""
+    B, L = tokens.shape
+    nbytes = table.numel() * table.element_size()
+    _check(_lib.pg_gather_sign_concat_e4m3(ctypes.byref(desc), _ptr(tokens), B, L, _ptr(canon_map), _ptr(table),
+                                           nbytes, _ptr(q_out), _ptr(scale_out), _ptr(err_index), _stream(stream)),
+           "pg_gather_sign_concat_e4m3")
 
 
 def workspace_size(N: int, Din: int, d: int, M: int, dtype: int, gate_kind: int) -> int:
@@ -450,6 +463,7 @@ def dtype_code(t: torch.dtype) -> int:
 
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
+           "gather_sign_concat_e4m3",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
            "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual",
            "decode_state_size", "DecodeState", "decode_reset", "decode_lookup", "decode_conv_residual",

@@ -293,6 +293,23 @@ pg_status pg_fp8_quantize(const void* x, int32_t dtype, int64_t rows, int64_t co
                           float* scale, pg_stream_t stream);
 
 /*
+ * pg_gather_sign_concat_e4m3 -- steps 1-7 of pg_gather_sign_concat with the FP8 projection's
+ * operand as output: each token's e_t row (bf16 table rows, signed and concatenated exactly
+ * as pg_gather_sign_concat writes it in bf16) quantised as pg_fp8_quantize does it, in the
+ * same kernel (Engram notes 3.4: the fused projection runs in FP8, so e_t need not exist in
+ * bf16). q_out and scale_out equal pg_gather_sign_concat(out_dtype = PG_BF16) followed by
+ * pg_fp8_quantize(dtype = PG_BF16) bit for bit.
+ *  q_out     device [B*L, O*K*r] E4M3 codes, 16-byte aligned
+ *  scale_out device fp32 [B*L], 4-byte aligned
+ *  other arguments, err_index and errors as pg_gather_sign_concat; PG_ERR_DTYPE unless the
+ *  table holds bf16 rows; PG_ERR_UNSUPPORTED for layouts other than 16 (order, head) items
+ *  of r = 64 or r = 80 (Engram or PageGram mode).
+ */
+pg_status pg_gather_sign_concat_e4m3(const pg_table_desc* desc, const int32_t* tokens, int32_t B, int32_t L,
+                                     const uint32_t* canon_map, const void* table, uint64_t table_bytes,
+                                     uint8_t* q_out, float* scale_out, int32_t* err_index, pg_stream_t stream);
+
+/*
  * pg_project_gate_fp8 -- pg_project_gate (dtype PG_BF16 outputs and gates) on E4M3
  * operands: v = diag(e_scale) (e_q W_q^T) diag(W_scale) with e_q [N, Din] and W_q
  * [(1+M)*d, Din] from pg_fp8_quantize, fp32 accumulation on the tensor cores

@@ -116,3 +116,86 @@ def test_fp8_rejects_what_it_does_not_cover(cuda):
         pg.fp8_quantize(torch.zeros(4, 12, device=cuda), torch.empty(4, 12, dtype=torch.uint8, device=cuda),
                         torch.empty(4, device=cuda))
     assert ex.value.status == 6
+
+
+# ---- E4M3 e_t straight from the gather (pg_gather_sign_concat_e4m3)
+
+def _e4m3_case(cfg, B, L, small=True):
+    from tests._helpers import shrink_table
+    from hashed_head_gram_gb300 import workloads as W
+    w = W.shrink(W.make_workload(cfg), B=B, L=L)
+    spec = shrink_table(w.tables[0]) if small else w.tables[0]
+    return w, spec, W.make_tokens(w), W.make_canon_map(w)
+
+
+@pytest.mark.parametrize("cfg,B,L", [(2, 3, 517), (3, 2, 301), (5, 3, 517), (5, 1, 1), (2, 1, 3)])
+def test_gather_e4m3_matches_oracle_and_the_two_calls(cuda, cfg, B, L):
+    from tests._helpers import canon_tensor, oracle_e
+    from hashed_head_gram_gb300 import workloads as W
+    pg = _pg()
+    w, spec, tokens, cmap = _e4m3_case(cfg, B, L)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    table = W.make_table(w, spec, "cpu")
+    N, D = w.N, spec.e_width
+    # the oracle: e_t in bf16, then E4M3 codes and scales of each row
+    e_ref = oracle_e(spec, tokens, cmap, w.vocab, table, orc.BF16)
+    q_ref, s_ref = orc.fp8_quantize(orc.bf16_bits_to_f64(e_ref).astype(np.float32))
+    tok = torch.from_numpy(tokens).to(cuda)
+    cm = canon_tensor(cmap, cuda)
+    td = table.to(cuda)
+    q = torch.full((N, D), 0xA5, dtype=torch.uint8, device=cuda)
+    s = torch.full((N,), float("nan"), device=cuda)
+    err = torch.empty(1, dtype=torch.int32, device=cuda)
+    pg.gather_sign_concat_e4m3(desc, tok, td, q, s, canon_map=cm, err_index=err)
+    torch.cuda.synchronize()
+    assert err.item() == -1 and pg.device_error() == 0
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    # and the same bytes as pg_gather_sign_concat (bf16) followed by pg_fp8_quantize
+    e = torch.empty(N, D, dtype=torch.bfloat16, device=cuda)
+    pg.gather_sign_concat(desc, tok, td, e, orc.BF16, canon_map=cm)
+    q2, s2 = _quantize_gpu(pg, e, cuda)
+    assert torch.equal(q, q2) and torch.equal(s.view(torch.int32), s2.view(torch.int32))
+
+
+def test_gather_e4m3_zero_rows_and_rejections(cuda):
+    from hashed_head_gram_gb300 import workloads as W
+    pg = _pg()
+    w, spec, tokens, cmap = _e4m3_case(5, 2, 40)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    table = torch.zeros(spec.table_rows, spec.r, dtype=torch.bfloat16)   # e_t = 0: scale 0, codes 0
+    q = torch.full((w.N, spec.e_width), 7, dtype=torch.uint8, device=cuda)
+    s = torch.full((w.N,), 1.0, device=cuda)
+    pg.gather_sign_concat_e4m3(desc, torch.from_numpy(tokens).to(cuda), table.to(cuda), q, s,
+                               canon_map=None if cmap is None else torch.from_numpy(cmap.view(np.int32)).to(cuda))
+    torch.cuda.synchronize()
+    assert int(q.max().item()) == 0 and float(s.abs().max().item()) == 0.0
+    # NF4 rows and the tiny fp32 table are outside this entry point
+    w4, spec4, tok4, _ = _e4m3_case(4, 1, 8)
+    with pytest.raises(pg.PgError, match="DTYPE"):
+        pg.gather_sign_concat_e4m3(pg.table_desc(spec4, w4.vocab, w4.canon_vocab), torch.from_numpy(tok4).to(cuda),
+                                   torch.zeros(spec4.table_rows, 34, dtype=torch.uint8, device=cuda),
+                                   torch.empty(8, spec4.e_width, dtype=torch.uint8, device=cuda),
+                                   torch.empty(8, device=cuda))
+
+
+@pytest.mark.parametrize("scale_exp", [-130, -120, -100, -90, -80, -60, 0, 60, 120])
+def test_gather_e4m3_extreme_magnitudes(cuda, scale_exp):
+    # rows of very different magnitudes, up to scales whose reciprocal leaves the normal
+    # range (the kernel then divides plainly); codes and scales still equal the oracle's
+    from tests._helpers import canon_tensor, oracle_e
+    pg = _pg()
+    w, spec, tokens, cmap = _e4m3_case(5, 2, 77)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    g = _gen(900 + scale_exp)
+    vals = torch.randn(spec.table_rows, spec.r, generator=g) * torch.exp(torch.randn(spec.table_rows, 1, generator=g))
+    table = (vals * (2.0 ** scale_exp)).to(torch.bfloat16)
+    e_ref = oracle_e(spec, tokens, cmap, w.vocab, table, orc.BF16)
+    q_ref, s_ref = orc.fp8_quantize(orc.bf16_bits_to_f64(e_ref).astype(np.float32))
+    q = torch.empty(w.N, spec.e_width, dtype=torch.uint8, device=cuda)
+    s = torch.empty(w.N, device=cuda)
+    pg.gather_sign_concat_e4m3(desc, torch.from_numpy(tokens).to(cuda), table.to(cuda), q, s,
+                               canon_map=canon_tensor(cmap, cuda))
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
