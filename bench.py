@@ -287,6 +287,16 @@ class Pipeline:
                             gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"], eps=w.eps, alpha_out=self.alpha,
                             workspace=self.ws, v_ms_out=self.v_ms)
 
+    def project_conv(self):
+        """The context-gated projection and the conv + residual in one launch."""
+        pg, w, dn = self.pg, self.w, self.dn
+        if not hasattr(self, "ws_pc"):
+            n = pg.project_gate_conv_workspace_size(self.N, self.d, w.M)
+            self.ws_pc = self.torch.empty((n + 3) // 4, device=self.dev)
+        pg.project_gate_conv(w.B, w.L, self.e, dn["W"], self.d, w.M, dn["H"], dn["gamma_h"], dn["gamma_k"],
+                             dn["gamma_c"], dn["conv_w"], self.v, self.alpha, self.ws_pc, dilation=w.dilation,
+                             eps=w.eps, v_ms_out=self.v_ms)
+
     def conv(self):
         pg, w, dn = self.pg, self.w, self.dn
         pg.conv_residual(w.B, w.L, self.d, w.M, pg.BF16, self.v, self.alpha, dn["gamma_c"], dn["conv_w"], dn["H"],
@@ -332,9 +342,15 @@ class Pipeline:
         return (sp.mode != self.W.MODE_FLAT and sp.row_dtype == self.W.DT_BF16 and sp.r in (64, 80)
                 and self.w.gate != self.W.GATE_NONE and self.d % 256 == 0 and self.din % 256 == 0)
 
+    def can_conv_fuse(self):
+        return (self.w.gate == self.W.GATE_CONTEXT and self.w.dtype == self.W.DT_BF16 and self.d % 256 == 0
+                and self.din % 64 == 0)
+
     def paths(self):
         """The ways this workload's step can run: the first is the default (bf16)."""
         out = ["two_kernel"]
+        if self.can_conv_fuse():
+            out = ["two_kernel", "conv_fused"]
         if self.can_overlap():
             out = ["overlap", "two_kernel", "fused"]
         elif self.can_fuse():
@@ -348,6 +364,8 @@ class Pipeline:
             return [("gather_sign_concat", self.gather)]
         if path == "overlap":
             st = [("gather_project_gate", self.overlap)]
+        elif path == "conv_fused":
+            return [("gather_sign_concat", self.gather), ("project_gate_conv", self.project_conv)]
         elif path == "fp8":
             self.fp8_ready()
             st = [("gather_sign_concat_e4m3", self.gather_q8), ("project_gate_fp8", self.project_fp8)]
@@ -429,7 +447,7 @@ class Pipeline:
             return "hbm", (rows * rb + 4 + din + 4) * N
         if name == "project_gate_fp8":
             return "tensor_fp8", 2.0 * N * din * d * (1 + w.M)
-        if name == "project_gate":
+        if name in ("project_gate", "project_gate_conv"):
             cols = d * (1 + w.M)
             return ("alu" if w.dtype == self.W.DT_F32 else "tensor"), 2.0 * N * din * cols
         # conv: read v, read + write H for every branch
@@ -1241,6 +1259,22 @@ def run_kernel_case(args):
             fn = lambda: pg.project_gate(e, Wm, d, pg.GATE_NONE, v, code)
         us = _ktime(fn, args.iters, dev)
         print(f"project_gate config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * (1 + M) * d / us / 1e6:.1f} TFLOP/s")
+    elif kind == "project_conv":
+        if w.gate != W.GATE_CONTEXT:
+            raise SystemExit("the projection + conv runs in the context-gated module (config 5)")
+        e = (torch.randint(-128, 128, (N, din), device=dev, generator=g).float() / 64).to(dt)
+        Wm = (torch.randn((1 + M) * d, din, device=dev, generator=g) * 0.02).to(dt)
+        v = torch.empty(N, d, dtype=dt, device=dev)
+        H = torch.randn(M, N, d, device=dev, generator=g).to(dt)
+        one = torch.ones(d, device=dev)
+        cw = torch.randn(d, w.conv_kernel, device=dev, generator=g) * 0.25
+        alpha = torch.empty(M, N, device=dev)
+        v_ms = torch.empty(N, device=dev)
+        ws = torch.empty(pg.project_gate_conv_workspace_size(N, d, M) // 4 + 1, device=dev)
+        us = _ktime(lambda: pg.project_gate_conv(w.B, w.L, e, Wm, d, M, H, one, one, one, cw, v, alpha, ws,
+                                                 dilation=w.dilation, eps=w.eps, v_ms_out=v_ms), args.iters, dev)
+        print(f"project_gate_conv config {w.cfg_id}: {us:.1f} us, {2.0 * N * din * (1 + M) * d / us / 1e6:.1f} "
+              f"TFLOP/s (projection flops)")
     elif kind == "conv":
         if w.gate != W.GATE_CONTEXT:
             raise SystemExit("the conv runs in the context-gated module (config 5)")
@@ -1408,7 +1442,7 @@ def main(argv=None):
     ap.add_argument("--workloads", default="all",
                     help="'all' (the headline and the other four) or a comma list of workloads to measure besides "
                          "the headline ('none' for the headline alone)")
-    ap.add_argument("--path", choices=["auto", "overlap", "two_kernel", "fused", "fp8"], default="auto",
+    ap.add_argument("--path", choices=["auto", "overlap", "two_kernel", "fused", "fp8", "conv_fused"], default="auto",
                     help="how the lookup and the projection run: overlap = one launch writing e_t with the "
                          "gather on extra warps of the projection (pg_gather_project_gate); two_kernel = "
                          "pg_gather_sign_concat + pg_project_gate; fused = pg_lookup_project_gate (r = 64 bf16 "
@@ -1420,7 +1454,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--threads", type=int, default=0, help="reference arm: host threads (default: all cores)")
     ap.add_argument("--oracle-legs", default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--kernel", choices=["gather", "project", "project_fp8", "gather_project", "conv", "nf4_export",
+    ap.add_argument("--kernel", choices=["gather", "project", "project_fp8", "project_conv", "gather_project", "conv",
+                                         "nf4_export",
                                          "decode", "slots"], default=None,
                     help="time one kernel on the workload's shapes instead of the benchmark")
     ap.add_argument("--iters", type=int, default=20, help="--kernel: timed launches")

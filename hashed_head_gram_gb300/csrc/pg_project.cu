@@ -21,6 +21,7 @@
 
 #include <mutex>
 
+#include "pg_conv_math.cuh"
 #include "pg_hash.cuh"
 
 namespace pg {
@@ -287,6 +288,22 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
+// 3-D tensor copies (the conv's branch-state tiles: [M, N, d] with rows clipped per branch).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until all but the most recent committed bulk store group have read shared memory.
@@ -396,6 +413,25 @@ constexpr int kCanonStride = 128 + 4;  // per slot: canonical IDs of the unit's 
 constexpr int kUnitRows = 8 * 64;  // rows of a gather unit: 64 per gather warp
 
 constexpr int kReadyTokens = kBM;   // tokens per ready counter (one A tile of one CTA)
+// Projection + conv in one launch (CONV): GEMM operand stages (5: room for the conv ring),
+// the lag of the conv items behind the GEMM tiles (in m-blocks), the largest causal halo
+// (kernel_size - 1) * dilation, and the conv warps' ring: per stage a 16-column sub-tile of
+// H and of v (128 rows each, 32-byte swizzle), v's halo rows before it and the packed taps
+// of its 8 column pairs.
+constexpr int kStagesConv = 5;
+constexpr int kConvLag = 2;
+constexpr int kConvMaxHalo = 24;
+constexpr int kConvCols = 16;
+constexpr int kConvTileBytes = kBM * kConvCols * 2;              // 4096
+constexpr int kConvHaloBytes = kConvMaxHalo * kConvCols * 2;     // 768
+constexpr int kConvTapBytes = (kConvCols / 2) * 4 * 8;           // 256
+constexpr int kConvStageBytes = 2 * kConvTileBytes + kConvHaloBytes + kConvTapBytes;  // 9216
+constexpr int kConvStages = 3;
+constexpr int kConvRows = kBM + kConvMaxHalo;  // f and alpha rows of a conv item
+constexpr int kConvWarp0 = 7;      // warps 7..14 compute the conv (row x 8-column chunk), warp 15 streams its operands
+constexpr int kConvCompute = 256;  // conv compute threads
+constexpr int kConvThreads = 512;
+constexpr int kErrConvWait = 16384;
 
 template <bool GATHER>
 __host__ __device__ constexpr int epi_stages() { return GATHER ? 3 : 4; }
@@ -445,6 +481,16 @@ struct GemmArgs {
   const float* sa;           // FP8: per-row scales of e [N]
   const float* sw;           // FP8: per-row scales of W [Dcols]
   int* err_word;
+  // CONV: the causal conv + residual behind the tiles
+  uint32_t* done = nullptr;        // [m-blocks] CTA-tiles of each m-block finished and published
+  const uint64_t* conv_taps = nullptr;  // [d / 2][4] fp32 pairs w[c, j] gamma_c[c] / 2, c = 2p, 2p + 1
+  float* alpha_out = nullptr;      // [M, N]
+  float* v_ms_out = nullptr;       // [N] or null
+  float eps = 0.f;
+  int L = 1;                       // sequence length
+  int ks = 0;                      // conv kernel size (<= 4)
+  int dil = 1;                     // dilation
+  int halo = 0;                    // (ks - 1) * dil
 };
 
 template <int S>
@@ -459,6 +505,10 @@ struct GemmBarriers {
   uint64_t mma_done;
   uint64_t unit_full[kUnitSlots];  // producing kernel: gather unit announced in its slot
   uint64_t unit_done[kUnitSlots];  // producing kernel: every gather warp stored its share of it
+  uint64_t pub;                    // CONV: the 128 epilogue threads finished a GEMM tile
+  uint64_t conv_sync;              // CONV: the conv threads wrote a conv item's f and alpha
+  uint64_t cfull[kConvStages];     // CONV: a conv sub-tile's operands landed
+  uint64_t cdone[kConvStages];     // CONV: the conv threads updated the stage's H
   uint32_t tmem_base;
   int abort;
 };
@@ -467,11 +517,15 @@ struct GemmBarriers {
 // gamma_k (context gate, k tiles) and FP8's per-column scales, 32 fp32 each.
 constexpr int kVecBytes = kEpiStagesMax * 3 * kEpiCols * 4;
 
-template <int BN, bool GATHER, bool PAIR, bool PRODUCE, bool VEC>
+template <bool PAIR, bool CONV>
+__host__ __device__ constexpr int stages_of() { return CONV ? kStagesConv : gemm_stages<PAIR>(); }
+
+template <int BN, bool GATHER, bool PAIR, bool PRODUCE, bool VEC, bool CONV = false>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 /* alignment slack */ + gemm_stages<PAIR>() * (kABytes + (PAIR ? BN / 2 : BN) * kBK * 2) +
+  return 1024 /* alignment slack */ + stages_of<PAIR, CONV>() * (kABytes + (PAIR ? BN / 2 : BN) * kBK * 2) +
          epi_stages<GATHER || PRODUCE>() * kEpiBytes + (VEC ? kVecBytes : 0) +
-         sizeof(GemmBarriers<gemm_stages<PAIR>()>) +
+         (CONV ? 512 + kConvStages * kConvStageBytes + 2 * 2 * kConvRows * sizeof(float) : 0) +
+         sizeof(GemmBarriers<stages_of<PAIR, CONV>()>) +
          (GATHER || PRODUCE ? kFusedItems * sizeof(ItemConst) : 0) +
          (PRODUCE ? kUnitSlots * kCanonStride * sizeof(uint32_t) : 0);
 }
@@ -515,6 +569,52 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(const uint32_t* __res
   if (!wait_ready(flag, 1u, abort)) atomicOr(err_word, kErrSelftestCounter);
 }
 
+// The context gate of (branch m, row) from the per-tile partial sums of the projection's
+// epilogue (sum gh gk h k, sum k^2, sum h^2 per 256-column tile), summed in tile order:
+// alpha = sigmoid(RMSNorm(h) . RMSNorm(k) / sqrt(d)); and mean(v^2) from the per-tile sums
+// of the stored v. Plain loads: the conv items read sums this launch wrote.
+__device__ __forceinline__ float gate_alpha(const float* partials, int m, int tpb, int N, int d, float eps,
+                                            int row) {
+  float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
+  for (int t0 = 0; t0 < tpb; t0 += 16) {  // 16 tiles' loads in flight, then added in tile order
+    float a[16], b[16], c[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      a[u] = b[u] = c[u] = 0.f;
+      if (t0 + u < tpb) {
+        const float* p = partials + (static_cast<size_t>(m * tpb + t0 + u) * 3) * N + row;
+        a[u] = p[0];
+        b[u] = p[N];
+        c[u] = p[2 * static_cast<size_t>(N)];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (t0 + u < tpb) {
+        s_hk += a[u];
+        s_kk += b[u];
+        s_hh += c[u];
+      }
+  }
+  const float inv_d = 1.0f / static_cast<float>(d);
+  const float rh = sqrtf(__fmaf_rn(s_hh, inv_d, eps));
+  const float rk = sqrtf(__fmaf_rn(s_kk, inv_d, eps));
+  const float s = s_hk / (rh * rk * sqrtf(static_cast<float>(d)));
+  return 1.0f / (1.0f + expf(-s));
+}
+__device__ __forceinline__ float row_mean_sq(const float* vpart, int tpb, int N, int d, int row) {
+  float s_vv = 0.f;
+  for (int t0 = 0; t0 < tpb; t0 += 16) {
+    float a[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) a[u] = t0 + u < tpb ? vpart[static_cast<size_t>(t0 + u) * N + row] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (t0 + u < tpb) s_vv += a[u];
+  }
+  return s_vv / static_cast<float>(d);
+}
+
 // Epilogue operands and results move through 128 x 32 bf16 sub-tiles (64 bytes per row)
 // written / read by TMA with 64-byte swizzle: 16-byte chunk c of row r sits at
 // r * 64 + ((c ^ ((r >> 1) & 3)) * 16), so the 32 rows of a warp hit every bank.
@@ -535,20 +635,37 @@ __device__ __forceinline__ uint32_t epi_offset(int row, int chunk) {
 // it on its 128-token block's ready counter (release); the A producer waits (acquire,
 // bounded) for a block's count before its first TMA load of that block. Any resident CTA
 // claims and finishes chunks without waiting on anything, so every wait ends.
-template <int BN, int GATE, bool GATHER, bool PAIR, bool PRODUCE = false, bool FP8 = false>
-__global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThreads : kGemmThreads, 1)
+//
+// CONV: the same kernel (CTA pairs, context gate) also runs the causal conv + SiLU +
+// residual of pg_conv_residual, as "conv items" interleaved with the GEMM tiles: the pair's
+// work list walks the m-blocks in ascending order and, kConvLag m-blocks behind the GEMM
+// tiles, takes for each m-block M * d / BN conv items (branch, 256-column block) of the same
+// 256 x 256 shape. A conv item's branch-state tile was read as h by the k tiles of its
+// m-block moments earlier, so its H comes mostly from L2. Each CTA's epilogue publishes a
+// finished GEMM tile on its m-block's counter (release, after its v stores completed);
+// a conv item waits (acquire, bounded) until the counters of its m-block and the one before
+// (the causal halo) are full, forms alpha and the RMSNorm tap factors of its rows from the
+// partial sums, and updates H with the arithmetic of pg_conv_residual (shared header), so
+// H, alpha and mean(v^2) are bit-identical to pg_project_gate followed by pg_conv_residual.
+// Every wait is on work that appears earlier in the list, which every pair walks in order:
+// the earliest waiting item always depends on GEMM tiles only, so all waits end.
+template <int BN, int GATE, bool GATHER, bool PAIR, bool PRODUCE = false, bool FP8 = false, bool CONV = false>
+__global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThreads : CONV ? kConvThreads : kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_h,
                    const __grid_constant__ CUtensorMap map_v, const GemmArgs args,
-                   const __grid_constant__ typename GatherParam<GATHER || PRODUCE>::type gat) {
+                   const __grid_constant__ typename GatherParam<GATHER || PRODUCE>::type gat,
+                   const __grid_constant__ CUtensorMap map_h3, const __grid_constant__ CUtensorMap map_vh) {
   static_assert(!(GATHER && PAIR), "the fused gather runs on single-CTA tiles");
   static_assert(!(GATHER && PRODUCE), "one way of making A");
   static_assert(!FP8 || (PAIR && !GATHER && !PRODUCE), "FP8 operands: the plain CTA-pair kernel");
+  static_assert(!CONV || (PAIR && GATE == PG_GATE_CONTEXT && !GATHER && !PRODUCE && BN == 256),
+                "the conv behind the tiles: plain CTA pairs, context gate");
   constexpr int kKB = FP8 ? 2 * kBK : kBK;  // elements of a 128-byte k-block row
   // FP8: stages of two k-blocks (8 MMAs per barrier wait: an E4M3 k-block is half the tensor
   // time of a bf16 one, and the single issuing thread's per-wait overhead would set the pace)
   constexpr int kSubK = FP8 ? 2 : 1;
-  constexpr int kSt = gemm_stages<PAIR>() / kSubK;
+  constexpr int kSt = stages_of<PAIR, CONV>() / kSubK;
   constexpr int kEpiStages = epi_stages<GATHER || PRODUCE>();
   constexpr int kBRows = PAIR ? BN / 2 : BN;  // rows of W this CTA stages per k-block
   constexpr int kBBytes = kBRows * kBK * 2;
@@ -565,7 +682,13 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
   uint8_t* sE = sB + kSt * kBStage;
   constexpr bool kVec = GATE == PG_GATE_CONTEXT || FP8;
   float* s_vec = reinterpret_cast<float*>(sE + kEpiStages * kEpiBytes);  // [slot][gamma_h, gamma_k, scale][32]
-  GemmBarriers<kSt>* bars = reinterpret_cast<GemmBarriers<kSt>*>(sE + kEpiStages * kEpiBytes + (kVec ? kVecBytes : 0));
+  // CONV: per pair of epilogue slots the halo rows of v, the taps and gamma_c; then f and
+  // alpha of a conv item's rows, double-buffered by item
+  uint8_t* s_conv = sE + kEpiStages * kEpiBytes + (kVec ? kVecBytes : 0) + (CONV ? 512 : 0);  // 1024-aligned
+  float* s_cf = reinterpret_cast<float*>(s_conv + kConvStages * kConvStageBytes);  // [2][kConvRows]
+  float* s_ca = s_cf + 2 * kConvRows;                                               // [2][kConvRows]
+  GemmBarriers<kSt>* bars = reinterpret_cast<GemmBarriers<kSt>*>(
+      CONV ? reinterpret_cast<uint8_t*>(s_ca + 2 * kConvRows) : s_conv);
   ItemConst* s_ic = reinterpret_cast<ItemConst*>(bars + 1);
   // producing kernel: slot u holds at [i] the canonical ID of flat position (unit start - 3 + i)
   uint32_t* s_canon = reinterpret_cast<uint32_t*>(s_ic + (GATHER || PRODUCE ? kFusedItems : 0));
@@ -594,6 +717,12 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
       mbar_init(smem_u32(&bars->epi_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars->mma_done), 1);
+    mbar_init(smem_u32(&bars->pub), 4 * 32);
+    mbar_init(smem_u32(&bars->conv_sync), kConvCompute);
+    for (int s = 0; s < kConvStages; ++s) {
+      mbar_init(smem_u32(&bars->cfull[s]), 1);
+      mbar_init(smem_u32(&bars->cdone[s]), kConvCompute);
+    }
     for (int s = 0; s < kUnitSlots; ++s) {
       mbar_init(smem_u32(&bars->unit_full[s]), 1);
       mbar_init(smem_u32(&bars->unit_done[s]), kProduceThreads / 32 - kProdGatherWarp0);
@@ -623,6 +752,39 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
   const int num_n = args.Dcols / BN;
   const int num_tiles = num_m * num_n;
   const int num_kb = args.Din / (kKB * kSubK);  // stages per tile
+  // The pair's work list. CONV: stage s holds the GEMM tiles of m-block s (s < num_m) and
+  // then the conv items of m-block s - lag (s >= lag); otherwise the GEMM tiles, last
+  // m-block first.
+  const int num_c = CONV ? args.M * (args.d / BN) : 0;  // conv items per m-block
+  const int num_items = num_tiles + num_m * num_c;
+  auto item_of = [&](int i, bool& conv, int& m_blk, int& n_blk) {
+    if constexpr (!CONV) {
+      const int rt = num_tiles - 1 - i;
+      conv = false;
+      m_blk = rt / num_n;
+      n_blk = rt - m_blk * num_n;
+    } else {
+      const int lag = kConvLag < num_m ? kConvLag : num_m;
+      const int a_end = lag * num_n;
+      const int per = num_n + num_c;
+      const int b_end = a_end + (num_m - lag) * per;
+      if (i < a_end) {
+        conv = false;
+        m_blk = i / num_n;
+        n_blk = i - m_blk * num_n;
+      } else if (i < b_end) {
+        const int r = i - a_end, st = r / per, o = r - st * per;
+        conv = o >= num_n;
+        m_blk = conv ? st : lag + st;
+        n_blk = conv ? o - num_n : o;
+      } else {
+        const int r = i - b_end;
+        conv = true;
+        m_blk = num_m - lag + r / num_c;
+        n_blk = r - (r / num_c) * num_c;
+      }
+    }
+  };
 
   __shared__ int64_t s_unit[kUnitSlots];  // gather units handed out (producing kernel)
   if (warp == 0) {
@@ -634,8 +796,11 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
       uint32_t phase = 0;
       bool ok = true;
       uint32_t issued = 0;  // bit s: stage s holds a load nobody has consumed yet (error path)
-      for (int tile = unit; tile < num_tiles && ok; tile += units) {
-        const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
+      for (int tile = unit; tile < num_items && ok; tile += units) {
+        bool conv_item;
+        int m_blk, n_blk;
+        item_of(tile, conv_item, m_blk, n_blk);
+        if (conv_item) continue;  // no tensor-core operands
         if constexpr (PRODUCE) {
           // this CTA's 128 rows of A must have been written by the gather warps
           const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
@@ -714,7 +879,13 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = unit; tile < num_tiles && ok; tile += units) {
+      for (int tile = unit; tile < num_items && ok; tile += units) {
+        if constexpr (CONV) {
+          bool conv_item;
+          int mb_, nb_;
+          item_of(tile, conv_item, mb_, nb_);
+          if (conv_item) continue;
+        }
         if (!mbar_wait<PAIR>(smem_u32(&bars->tmem_empty[acc]), acc_phase ^ 1u, abort)) {
           ok = false;
           break;
@@ -764,11 +935,14 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
       uint32_t seq = 0;
       bool ok = true;
       uint32_t issued = 0;
-      for (int tile = unit; tile < num_tiles && ok; tile += units) {
-        const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
+      for (int tile = unit; tile < num_items && ok; tile += units) {
+        bool conv_item;
+        int m_blk, n_blk;
+        item_of(tile, conv_item, m_blk, n_blk);
         const int n0 = n_blk * BN, m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
         const bool is_k = GATE == PG_GATE_CONTEXT && n0 >= args.d;
         if (m0 >= args.N) continue;  // this CTA's rows of the tile lie past the last token
+        if (conv_item) continue;  // conv items run on the conv warps
         for (int j = 0; j < kSub; ++j, ++seq) {
           const int slot = static_cast<int>(seq % kEpiStages);
           const uint32_t ph = (seq / kEpiStages) & 1u;
@@ -1091,6 +1265,212 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
         *abort = 1;
       }
     }
+  } else if (CONV && warp >= kConvWarp0) {
+    if constexpr (CONV) {
+      // ------------------------------------------------------------ conv warps (7..11)
+      // The conv items of the pair's work list, in order. Warp 11's lane 0 streams each
+      // item's 16 sub-tiles of 16 columns (H of the branch, v of the item's rows and of the
+      // causal halo before them, the packed taps) through a kConvStages-deep ring once the
+      // item's m-blocks are published, and writes every updated sub-tile of H back; warps
+      // 7..10 (thread = row) first form the item's alpha and tap factors from the partial
+      // sums, then update the sub-tiles in place with pg_conv_residual's arithmetic.
+      const int tpbk = args.d / BN;
+      constexpr int kSubs = BN / kConvCols;  // sub-tiles per conv item
+      auto sw32 = [](int row, int chunk) -> uint32_t {  // 32-byte rows, 32-byte swizzle
+        return static_cast<uint32_t>(row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4));
+      };
+      if (warp == kConvWarp0 + kConvCompute / 32) {
+        if (lane == 0) {
+          tma_prefetch_map(&map_h3);
+          tma_prefetch_map(&map_x);
+          if (args.halo > 0) tma_prefetch_map(&map_vh);
+          uint32_t k = 0;  // conv sub-tiles issued
+          bool ok = true;
+          int st_r0[kConvStages], st_br[kConvStages], st_col[kConvStages];
+          for (int tile = unit; tile < num_items && ok; tile += units) {
+            bool cv;
+            int m_blk, n_blk;
+            item_of(tile, cv, m_blk, n_blk);
+            if (!cv) continue;
+            const int r0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+            if (r0 >= args.N) continue;  // (the compute warps skip the same items)
+            const int br = n_blk / tpbk, cb = n_blk - br * tpbk;
+            // v of this m-block and of the one before is written by this launch's v tiles
+            if (!wait_ready(args.done + m_blk, 2u * num_n, abort) ||
+                (m_blk > 0 && !wait_ready(args.done + m_blk - 1, 2u * num_n, abort))) {
+              atomicOr(args.err_word, kErrConvWait);
+              ok = false;
+              break;
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            for (int j = 0; j < kSubs; ++j, ++k) {
+              const int s = static_cast<int>(k % kConvStages);
+              const uint32_t use = k / kConvStages;
+              uint8_t* stg = s_conv + s * kConvStageBytes;
+              if (use > 0) {
+                // the compute warps are done with the sub-tile this stage held: write it back,
+                // and let the store read the stage before it is refilled
+                if (!mbar_wait(smem_u32(&bars->cdone[s]), (use - 1) & 1u, abort)) {
+                  ok = false;
+                  break;
+                }
+                tma_store_3d(&map_h3, smem_u32(stg), st_col[s], st_r0[s], st_br[s]);
+                bulk_commit();
+                bulk_wait_read_all();
+              }
+              const uint32_t full = smem_u32(&bars->cfull[s]);
+              const int col = cb * BN + j * kConvCols;
+              mbar_expect_tx(full, 2 * kConvTileBytes + args.halo * kConvCols * 2 + kConvTapBytes);
+              tma_load_3d(smem_u32(stg), &map_h3, full, col, r0, br);
+              tma_load_2d(smem_u32(stg + kConvTileBytes), &map_x, full, col, r0);
+              if (args.halo > 0) tma_load_2d(smem_u32(stg + 2 * kConvTileBytes), &map_vh, full, col, r0 - args.halo);
+              bulk_load(smem_u32(stg + 2 * kConvTileBytes + kConvHaloBytes), args.conv_taps + (col / 2) * 4,
+                        kConvTapBytes, full);
+              st_r0[s] = r0;
+              st_br[s] = br;
+              st_col[s] = col;
+            }
+          }
+          // the last fills: written back once computed
+          for (uint32_t q = k > kConvStages ? k - kConvStages : 0; ok && q < k; ++q) {
+            const int s = static_cast<int>(q % kConvStages);
+            if (!mbar_wait(smem_u32(&bars->cdone[s]), (q / kConvStages) & 1u, abort)) {
+              ok = false;
+              break;
+            }
+            tma_store_3d(&map_h3, smem_u32(s_conv + s * kConvStageBytes), st_col[s], st_r0[s], st_br[s]);
+            bulk_commit();
+          }
+          bulk_wait_all();
+          if (!ok) {
+            atomicOr(args.err_word, 32);
+            *abort = 1;
+            // let the loads already issued land before the CTA can exit (bounded)
+            for (uint32_t q = k > kConvStages ? k - kConvStages : 0; q < k; ++q) {
+              const uint64_t t0 = globaltimer();
+              while (!mbar_try_wait(smem_u32(&bars->cfull[q % kConvStages]), (q / kConvStages) & 1u) &&
+                     globaltimer() - t0 < kWaitLimitNs / 4) {
+              }
+            }
+          }
+        }
+      } else {
+        const int cth = threadIdx.x - 32 * kConvWarp0;
+        const int ct = cth & (kBM - 1);  // this thread's row of the item
+        const int chunk = cth >> 7;      // and its 8 columns of every 16-column sub-tile
+        const int halo = args.halo, dil = args.dil, ks = args.ks;
+        uint32_t k = 0, sync_phase = 0;
+        int cbuf = 0;
+        bool ok = true;
+        for (int tile = unit; tile < num_items && ok; tile += units) {
+          bool cv;
+          int m_blk, n_blk;
+          item_of(tile, cv, m_blk, n_blk);
+          if (!cv) continue;
+          const int r0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+          if (r0 >= args.N) continue;
+          const int br = n_blk / tpbk;
+          // the partial sums of this m-block and of the one before are complete
+          if (!wait_ready(args.done + m_blk, 2u * num_n, abort) ||
+              (m_blk > 0 && !wait_ready(args.done + m_blk - 1, 2u * num_n, abort))) {
+            atomicOr(args.err_word, kErrConvWait);
+            ok = false;
+            break;
+          }
+          // alpha and the tap factor f = alpha / sqrt(alpha^2 mean(v^2) + eps) of the rows
+          // [r0 - halo, r0 + 128), formed as the alpha finalize and pg_conv_residual form them;
+          // the items of column block 0 also write alpha and mean(v^2) out
+          const int cb = n_blk - br * tpbk;
+          float* cf = s_cf + cbuf * kConvRows;
+          float* ca = s_ca + cbuf * kConvRows;
+          cbuf ^= 1;
+          for (int i = cth; i < kBM + halo; i += kConvCompute) {
+            const int p = r0 - halo + i;
+            float a = 0.f, f = 0.f;
+            if (p >= 0 && p < args.N) {
+              a = gate_alpha(args.partials, br, tpbk, args.N, args.d, args.eps, p);
+              const float ms = row_mean_sq(args.vpart, tpbk, args.N, args.d, p);
+              f = tap_scale(a, ms, args.eps);
+              if (cb == 0 && i >= halo) {
+                args.alpha_out[static_cast<size_t>(br) * args.N + p] = a;
+                if (br == 0 && args.v_ms_out) args.v_ms_out[p] = ms;
+              }
+            }
+            cf[i] = f;
+            ca[i] = a;
+          }
+          mbar_arrive(smem_u32(&bars->conv_sync));
+          if (!mbar_wait(smem_u32(&bars->conv_sync), sync_phase, abort)) {
+            ok = false;
+            break;
+          }
+          sync_phase ^= 1u;
+          // this thread's row t: its four tap factors (zero before the start of its sequence
+          // and past the kernel size) and alpha_t
+          const int tpos = (r0 + ct) % args.L;
+          bool tap_ok[4];
+          float fj[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            tap_ok[jj] = jj < ks && tpos >= jj * dil;
+            fj[jj] = tap_ok[jj] ? cf[halo + ct - jj * dil] : 0.f;
+          }
+          const uint64_t f0 = pk(fj[0], fj[0]), f1 = pk(fj[1], fj[1]), f2 = pk(fj[2], fj[2]), f3 = pk(fj[3], fj[3]);
+          const float at = ca[halo + ct];
+          const uint64_t aa = pk(at, at);
+          for (int j = 0; j < kSubs; ++j, ++k) {
+            const int s = static_cast<int>(k % kConvStages);
+            if (!mbar_wait(smem_u32(&bars->cfull[s]), (k / kConvStages) & 1u, abort)) {
+              ok = false;
+              break;
+            }
+            uint8_t* stg = s_conv + s * kConvStageBytes;  // H, overwritten by H + Y
+            const uint8_t* vs = stg + kConvTileBytes;     // v of the item's rows
+            const uint8_t* vh = stg + 2 * kConvTileBytes;  // v of the halo rows
+            const uint64_t* taps = reinterpret_cast<const uint64_t*>(stg + 2 * kConvTileBytes + kConvHaloBytes);
+            {
+              const int c = chunk;  // 16-byte chunk c: columns 8c .. 8c + 7 of the sub-tile
+              uint4 vr[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const int rr = ct - jj * dil;
+                if (!tap_ok[jj])
+                  vr[jj] = make_uint4(0, 0, 0, 0);
+                else if (rr >= 0)
+                  vr[jj] = *reinterpret_cast<const uint4*>(vs + sw32(rr, c));
+                else
+                  vr[jj] = *reinterpret_cast<const uint4*>(vh + (halo + rr) * (kConvCols * 2) + c * 16);
+              }
+              float h[8];
+              unpack_bf16x8(*reinterpret_cast<const uint4*>(stg + sw32(ct, c)), h);
+              const uint32_t vw[4][4] = {{vr[0].x, vr[0].y, vr[0].z, vr[0].w}, {vr[1].x, vr[1].y, vr[1].z, vr[1].w},
+                                         {vr[2].x, vr[2].y, vr[2].z, vr[2].w}, {vr[3].x, vr[3].y, vr[3].z, vr[3].w}};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {  // columns 8c + 2q, 8c + 2q + 1
+                const uint64_t* wq = taps + (4 * c + q) * 4;
+                uint64_t prod[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) prod[jj] = mul2(wq[jj], bf16x2_as_f2(vw[jj][q]));
+                uint64_t cc = mul2(f0, prod[0]);  // c / 2
+                cc = fma2(f1, prod[1], cc);
+                cc = fma2(f2, prod[2], cc);
+                cc = fma2(f3, prod[3], cc);
+                const uint64_t accv = fma2(aa, bf16x2_as_f2(vw[0][q]), pk(h[2 * q], h[2 * q + 1]));  // H + alpha v_t
+                upk(silu2_add<__nv_bfloat16>(cc, accv), h[2 * q], h[2 * q + 1]);
+              }
+              *reinterpret_cast<uint4*>(stg + sw32(ct, c)) =
+                  make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
+            }
+            fence_proxy_async_smem();  // the stage's H is read next by the TMA store
+            mbar_arrive(smem_u32(&bars->cdone[s]));
+          }
+        }
+        if (!ok) {
+          atomicOr(args.err_word, 32);
+          *abort = 1;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue (warps 3..6; 4..7 when PRODUCE)
     const int epi = threadIdx.x - 32 * (PRODUCE ? kProdEpiWarp0 : 3);
@@ -1102,8 +1482,12 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
     bool ok = true;
     int pending = -1;             // slot whose TMA store may still be reading (thread epi == 0)
     const int tpb = args.d / BN;  // tiles per branch (context gate)
-    for (int tile = unit; tile < num_tiles && ok; tile += units) {
-      const int rt = num_tiles - 1 - tile; const int m_blk = rt / num_n, n_blk = rt - (rt / num_n) * num_n;
+    uint32_t pub_phase = 0;  // CONV: tile publication barrier
+    for (int tile = unit; tile < num_items && ok; tile += units) {
+      bool conv_item;
+      int m_blk, n_blk;
+      item_of(tile, conv_item, m_blk, n_blk);
+      if (conv_item) continue;  // conv items run on the conv warps
       if (!mbar_wait(smem_u32(&bars->tmem_full[acc]), acc_phase, abort)) {
         ok = false;
         break;
@@ -1258,6 +1642,26 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
       }
       if (GATE == PG_GATE_CONTEXT && !is_k && live && args.vpart)
         args.vpart[static_cast<size_t>(n0 / BN) * args.N + row] = s_vv;
+      if constexpr (CONV) {
+        // publish this CTA's share of the tile on its m-block's counter once its partial
+        // sums are visible and its v stores complete
+        __threadfence();
+        mbar_arrive(smem_u32(&bars->pub));
+        if (epi == 0) {
+          if (!mbar_wait(smem_u32(&bars->pub), pub_phase, abort)) {
+            ok = false;
+          } else {
+            bulk_wait_all();
+            if (pending >= 0) {
+              mbar_arrive(smem_u32(&bars->epi_empty[pending]));
+              pending = -1;
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            red_release_gpu_add(args.done + m_blk, 1u);
+          }
+        }
+        pub_phase ^= 1u;
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -1290,6 +1694,22 @@ __global__ void __launch_bounds__(PRODUCE ? kProduceThreads : GATHER ? kFusedThr
   }
 }
 
+// The conv taps with the RMSNorm gain and SiLU's half-argument folded in, as pg_conv_residual
+// forms them: out[p][j] = (w[c, j] gamma_c[c] / 2, w[c + 1, j] gamma_c[c + 1] / 2), c = 2p,
+// zero for j >= kernel_size.
+__global__ void __launch_bounds__(256) conv_taps_kernel(const float* __restrict__ conv_w,
+                                                        const float* __restrict__ gamma_c, int d, int ks,
+                                                        uint64_t* __restrict__ out) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (d / 2) * 4) return;
+  const int p = idx >> 2, j = idx & 3;
+  const int c0 = 2 * p, c1 = 2 * p + 1;
+  const float g0 = 0.5f * gamma_c[c0], g1 = 0.5f * gamma_c[c1];
+  const float w0 = j < ks ? conv_w[c0 * ks + j] * g0 : 0.f;
+  const float w1 = j < ks ? conv_w[c1 * ks + j] * g1 : 0.f;
+  out[idx] = pk(w0, w1);
+}
+
 // alpha[m, t] from the per-tile partial sums (summed in tile order: deterministic).
 // With vpart, threads of branch 0 also write mean(v^2) of their row (tile order: deterministic).
 __global__ void __launch_bounds__(256) alpha_finalize_kernel(const float* __restrict__ partials, int M,
@@ -1301,23 +1721,8 @@ __global__ void __launch_bounds__(256) alpha_finalize_kernel(const float* __rest
   if (idx >= static_cast<int64_t>(M) * N) return;
   const int m = static_cast<int>(idx / N);
   const int row = static_cast<int>(idx - static_cast<int64_t>(m) * N);
-  if (vpart && m == 0) {
-    float s_vv = 0.f;
-    for (int tb = 0; tb < tpb; ++tb) s_vv += vpart[static_cast<size_t>(tb) * N + row];
-    v_ms[row] = s_vv / static_cast<float>(d);
-  }
-  float s_hk = 0.f, s_kk = 0.f, s_hh = 0.f;
-  for (int tb = 0; tb < tpb; ++tb) {
-    const float* p = partials + (static_cast<size_t>(m * tpb + tb) * 3) * N + row;
-    s_hk += p[0];
-    s_kk += p[N];
-    s_hh += p[2 * static_cast<size_t>(N)];
-  }
-  const float inv_d = 1.0f / static_cast<float>(d);
-  const float rh = sqrtf(s_hh * inv_d + eps);
-  const float rk = sqrtf(s_kk * inv_d + eps);
-  const float s = s_hk / (rh * rk * sqrtf(static_cast<float>(d)));
-  alpha[idx] = 1.0f / (1.0f + expf(-s));
+  if (vpart && m == 0) v_ms[row] = row_mean_sq(vpart, tpb, N, d, row);
+  alpha[idx] = gate_alpha(partials, m, tpb, N, d, eps, row);
 }
 
 // The same for few rows (N <= kFinalizeWarpRows): one warp per (branch, row), lane l adding
@@ -1406,6 +1811,21 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, u
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor [z, rows, cols] (row-major), box [1, box_rows, box_cols]: rows clipped per z.
+bool make_map_3d(CUtensorMap* map, const void* ptr, uint64_t zs, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                 uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, zs};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 struct GemmPtrs {
   const void* e;
   const void* W;
@@ -1414,10 +1834,11 @@ struct GemmPtrs {
   void* v;
 };
 
-template <int BN, int GATE, bool GATHER = false, bool PAIR = false, bool PRODUCE = false, bool FP8 = false>
+template <int BN, int GATE, bool GATHER = false, bool PAIR = false, bool PRODUCE = false, bool FP8 = false,
+          bool CONV = false>
 pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
                     const typename GatherParam<GATHER || PRODUCE>::type& gat = {}) {
-  CUtensorMap ma, mb, mx, mh, mv;
+  CUtensorMap ma, mb, mx, mh, mv, mh3, mvh;
   constexpr uint32_t kBox = FP8 ? 2 * kBK : kBK;  // a 128-byte row of elements
   if ((!GATHER && !make_map(&ma, ptr.e, a.N, a.Din, kBox, kBM, CU_TENSOR_MAP_SWIZZLE_128B, FP8)) ||
       !make_map(&mb, ptr.W, a.Dcols, a.Din, kBox, PAIR ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B, FP8) ||
@@ -1432,15 +1853,25 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
   if (GATE == PG_GATE_CONTEXT &&
       !make_map(&mh, ptr.h, static_cast<uint64_t>(a.M) * a.N, a.d, kEpiCols, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
     return PG_ERR_UNSUPPORTED;
-  auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR, PRODUCE, FP8>;
-  constexpr size_t smem = gemm_smem_bytes<BN, GATHER, PAIR, PRODUCE, GATE == PG_GATE_CONTEXT || FP8>();
+  mh3 = mv;
+  mvh = mv;
+  if (CONV) {  // the conv warps' tiles: H per branch (stores clipped at each branch's last row), v, v's halo
+    if (!make_map_3d(&mh3, ptr.h, a.M, a.N, a.d, kConvCols, kBM, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map(&mx, ptr.v, a.N, a.d, kConvCols, kBM, CU_TENSOR_MAP_SWIZZLE_32B))
+      return PG_ERR_UNSUPPORTED;
+    if (a.halo > 0 && !make_map(&mvh, ptr.v, a.N, a.d, kConvCols, a.halo, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return PG_ERR_UNSUPPORTED;
+  }
+  auto kern = tc_gemm_kernel<BN, GATE, GATHER, PAIR, PRODUCE, FP8, CONV>;
+  constexpr size_t smem = gemm_smem_bytes<BN, GATHER, PAIR, PRODUCE, GATE == PG_GATE_CONTEXT || FP8, CONV>();
   static_assert(smem <= 232448, "dynamic shared memory above the 227 KB a CTA may hold");
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return cuda_fail(err);
   if constexpr (PAIR) {
     // persistent: one CTA pair per co-resident cluster slot, at most one per 256 x BN tile
-    const int tiles = ((a.N + 2 * kBM - 1) / (2 * kBM)) * (a.Dcols / BN);
+    const int mblocks = (a.N + 2 * kBM - 1) / (2 * kBM);
+    const int tiles = mblocks * (a.Dcols / BN) + (CONV ? mblocks * a.M * (a.d / BN) : 0);  // work items
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -1448,7 +1879,7 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2u * static_cast<unsigned>(tiles));
-    cfg.blockDim = dim3(PRODUCE ? kProduceThreads : kGemmThreads);
+    cfg.blockDim = dim3(PRODUCE ? kProduceThreads : CONV ? kConvThreads : kGemmThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1459,13 +1890,13 @@ pg_status launch_tc(const GemmPtrs& ptr, const GemmArgs& a, cudaStream_t stream,
     if (slots < 1) return PG_ERR_DEVICE;
     const int clusters = tiles < slots ? tiles : slots;
     cfg.gridDim = dim3(2u * static_cast<unsigned>(clusters));
-    err = cudaLaunchKernelEx(&cfg, kern, ma, mb, mx, mh, mv, a, gat);
+    err = cudaLaunchKernelEx(&cfg, kern, ma, mb, mx, mh, mv, a, gat, mh3, mvh);
     if (err != cudaSuccess) return cuda_fail(err);
     return after_launch(1);
   }
   const int tiles = ((a.N + kBM - 1) / kBM) * (a.Dcols / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  kern<<<grid, GATHER ? kFusedThreads : kGemmThreads, smem, stream>>>(ma, mb, mx, mh, mv, a, gat);
+  kern<<<grid, GATHER ? kFusedThreads : kGemmThreads, smem, stream>>>(ma, mb, mx, mh, mv, a, gat, mh3, mvh);
   return after_launch(1);
 }
 
@@ -1609,6 +2040,81 @@ pg_status pg_project_gate(int32_t N, int32_t Din, int32_t d, int32_t M, int32_t 
   return launch_alpha_finalize(a.partials, M, d / bn, N, d, eps, alpha_out, a.vpart, v_ms_out, stream);
 }
 
+
+pg_status pg_project_gate_conv_workspace_size(int32_t N, int32_t d, int32_t M, size_t* bytes) {
+  if (!bytes) return PG_ERR_NULL;
+  if (N < 0 || d < 1 || M < 1) return PG_ERR_SHAPE;
+  const size_t sync = (static_cast<size_t>((N + 255) / 256) * sizeof(uint32_t) + 255) / 256 * 256;
+  const size_t taps = (static_cast<size_t>(d / 2) * 4 * sizeof(uint64_t) + 255) / 256 * 256;
+  *bytes = sync + taps + pg::context_workspace(N, d, M, true);
+  return PG_OK;
+}
+
+pg_status pg_project_gate_conv(int32_t B, int32_t L, int32_t Din, int32_t d, int32_t M, const void* e,
+                               const void* W, void* H, const float* gamma_h, const float* gamma_k,
+                               const float* gamma_c, const float* conv_w, int32_t kernel_size, int32_t dilation,
+                               float eps, void* v_out, float* alpha_out, float* v_ms_out, void* workspace,
+                               size_t workspace_bytes, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (B < 0 || L < 1 || Din < 1 || d < 1 || M < 1) return PG_ERR_SHAPE;
+  if (kernel_size < 1 || kernel_size > 4 || dilation < 1 || dilation > 8) return PG_ERR_SHAPE;
+  const int64_t N64 = static_cast<int64_t>(B) * L;
+  if (N64 >= (1ll << 31)) return PG_ERR_SHAPE;
+  const int N = static_cast<int>(N64);
+  if (N == 0) return PG_OK;
+  if (!e || !W || !H || !gamma_h || !gamma_k || !gamma_c || !conv_w || !v_out || !alpha_out || !workspace)
+    return PG_ERR_NULL;
+  if (Din % kBK != 0 || d % 256 != 0) return PG_ERR_UNSUPPORTED;
+  if (!aligned16(e) || !aligned16(W) || !aligned16(H) || !aligned16(v_out) || !aligned16(gamma_h) ||
+      !aligned16(gamma_k) || !aligned16(gamma_c) || !aligned16(conv_w) || !aligned16(workspace) ||
+      reinterpret_cast<uintptr_t>(alpha_out) % 4 || reinterpret_cast<uintptr_t>(v_ms_out) % 4)
+    return PG_ERR_ALIGN;
+  if (static_cast<int64_t>(N) * (d > Din ? d : Din) >= (1ll << 40)) return PG_ERR_SHAPE;
+  if (static_cast<int64_t>(M) * N >= (1ll << 31)) return PG_ERR_SHAPE;
+  size_t need = 0;
+  pg_status st = pg_project_gate_conv_workspace_size(N, d, M, &need);
+  if (st != PG_OK) return st;
+  if (workspace_bytes < need) return PG_ERR_WORKSPACE;
+  if (sm_count() == 0) return cuda_fail(cudaGetLastError());
+  if (device_cc() != 103 && device_cc() != 100) return PG_ERR_DEVICE;
+  constexpr int bn = 256;
+  const size_t sync = (static_cast<size_t>((N + 255) / 256) * sizeof(uint32_t) + 255) / 256 * 256;
+  const size_t taps_bytes = need - sync - context_workspace(N, d, M, true);
+  GemmArgs a;
+  a.N = N;
+  a.Din = Din;
+  a.Dcols = (1 + M) * d;
+  a.d = d;
+  a.M = M;
+  a.g = 0.f;
+  a.gamma_h = gamma_h;
+  a.gamma_k = gamma_k;
+  a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sync + taps_bytes);
+  a.vpart = a.partials + static_cast<size_t>(M) * (d / bn) * 3 * static_cast<size_t>(N);
+  a.sa = a.sw = nullptr;
+  a.err_word = device_error_word();
+  if (!a.err_word) return cuda_fail(cudaGetLastError());
+  a.done = static_cast<uint32_t*>(workspace);
+  uint64_t* taps = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + sync);
+  a.conv_taps = taps;
+  a.alpha_out = alpha_out;
+  a.v_ms_out = v_ms_out;
+  a.eps = eps;
+  a.L = L;
+  a.ks = kernel_size;
+  a.dil = dilation;
+  a.halo = (kernel_size - 1) * dilation;
+  if (a.halo > kConvMaxHalo) return PG_ERR_UNSUPPORTED;
+  cudaError_t err = cudaMemsetAsync(workspace, 0, sync, stream);  // the m-blocks' counters
+  if (err != cudaSuccess) return cuda_fail(err);
+  const int ntaps = (d / 2) * 4;
+  conv_taps_kernel<<<(ntaps + 255) / 256, 256, 0, stream>>>(conv_w, gamma_c, d, kernel_size, taps);
+  st = after_launch(1);
+  if (st != PG_OK) return st;
+  const GemmPtrs ptrs{e, W, nullptr, H, v_out};
+  return launch_tc<256, PG_GATE_CONTEXT, false, true, false, false, true>(ptrs, a, stream);
+}
 
 pg_status pg_project_gate_fp8(int32_t N, int32_t Din, int32_t d, int32_t M, const void* e_q, const float* e_scale,
                               const void* W_q, const float* W_scale, int32_t gate_kind, float g,

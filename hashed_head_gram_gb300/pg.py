@@ -112,6 +112,11 @@ def _load():
     L.pg_gather_project_gate_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.POINTER(sz)]
     L.pg_gather_sign_concat_e4m3.restype = ctypes.c_int
     L.pg_gather_sign_concat_e4m3.argtypes = [dp, vp, i32, i32, vp, vp, u64, vp, vp, vp, vp]
+    L.pg_project_gate_conv_workspace_size.restype = ctypes.c_int
+    L.pg_project_gate_conv_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+    L.pg_project_gate_conv.restype = ctypes.c_int
+    L.pg_project_gate_conv.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp, vp,
+                                       vp, sz, vp]
     L.pg_fp8_quantize.restype = ctypes.c_int
     L.pg_fp8_quantize.argtypes = [vp, i32, ctypes.c_int64, ctypes.c_int64, vp, vp, vp]
     L.pg_project_gate_fp8.restype = ctypes.c_int
@@ -218,6 +223,26 @@ def gather_sign_concat(desc: TableDesc, tokens: torch.Tensor, table: torch.Tenso
     _check(_lib.pg_gather_sign_concat(ctypes.byref(desc), _ptr(tokens), B, L, _ptr(canon_map), _ptr(table),
                                       nbytes, _ptr(e_out), out_dtype, _ptr(err_index), _stream(stream)),
            "pg_gather_sign_concat")
+
+
+def project_gate_conv_workspace_size(N: int, d: int, M: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.pg_project_gate_conv_workspace_size(N, d, M, ctypes.byref(n)), "pg_project_gate_conv_workspace_size")
+    return n.value
+
+
+def project_gate_conv(B: int, L: int, e: torch.Tensor, W: torch.Tensor, d: int, M: int, H: torch.Tensor,
+                      gamma_h: torch.Tensor, gamma_k: torch.Tensor, gamma_c: torch.Tensor, conv_w: torch.Tensor,
+                      v_out: torch.Tensor, alpha_out: torch.Tensor, workspace: torch.Tensor, dilation: int = 3,
+                      eps: float = 1e-6, v_ms_out: Optional[torch.Tensor] = None, stream=None):
+    """Context-gated projection + causal conv + residual in one launch; H [M, B*L, d] updated
+    in place (it is also the gate's h)."""
+    ks = conv_w.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pg_project_gate_conv(B, L, e.shape[1], d, M, _ptr(e), _ptr(W), _ptr(H), _ptr(gamma_h), _ptr(gamma_k),
+                                     _ptr(gamma_c), _ptr(conv_w), ks, dilation, eps, _ptr(v_out), _ptr(alpha_out),
+                                     _ptr(v_ms_out), _ptr(workspace), ws_bytes, _stream(stream)),
+           "pg_project_gate_conv")
 
 
 def gather_sign_concat_e4m3(desc: TableDesc, tokens: torch.Tensor, table: torch.Tensor, q_out: torch.Tensor,
@@ -463,7 +488,7 @@ def dtype_code(t: torch.dtype) -> int:
 
 
 __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash", "gather_sign_concat",
-           "gather_sign_concat_e4m3",
+           "gather_sign_concat_e4m3", "project_gate_conv", "project_gate_conv_workspace_size",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
            "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual",
            "decode_state_size", "DecodeState", "decode_reset", "decode_lookup", "decode_conv_residual",

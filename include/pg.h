@@ -136,7 +136,8 @@ uint64_t pg_launch_count(void);
  * decode call met a position it cannot take; that sequence was skipped, left unchanged),
  * and of pg_collision_counts (1024 = a head-0 row outside the given span, or a head-0
  * group too large to compare pairwise; those n-grams or pairs were left out), and of
- * pg_selftest_bounded_waits (2048, 4096).
+ * pg_selftest_bounded_waits (2048, 4096), and of pg_project_gate_conv (16384 = a conv item's wait
+ * for the tiles of its m-blocks).
  * Synchronizes the device. With clear != 0 the word is reset to 0.
  */
 pg_status pg_device_error(int32_t* code, int32_t clear);
@@ -279,6 +280,31 @@ pg_status pg_conv_residual(int32_t B, int32_t L, int32_t d, int32_t M, int32_t d
                            const void* v, const float* alpha, const float* v_ms,
                            const float* gamma_c, const float* conv_w, int32_t kernel_size,
                            int32_t dilation, float eps, void* H, pg_stream_t stream);
+
+/*
+ * pg_project_gate_conv -- the context-gated projection and the causal conv + residual in one
+ * launch: pg_project_gate(gate_kind = PG_GATE_CONTEXT, dtype = PG_BF16, h = H) followed by
+ * pg_conv_residual(v, alpha, v_ms, gamma_c, conv_w, kernel_size, dilation, eps, H), with H
+ * read as the gate's h and updated in place (Engram notes 3.3, 3.4, 3.1: alpha from
+ * RMSNorm(h) . RMSNorm(k), then Y = SiLU(Conv1D(RMSNorm(alpha v))) + alpha v, H += Y).
+ * The conv runs behind the projection's tiles in the same persistent kernel, so each
+ * tile of H is read once from HBM for both steps. v_out, alpha_out, v_ms_out and H are
+ * bit-identical to the two calls.
+ *  e [B*L, Din], W [(1+M) d, Din], H [M, B*L, d]: device bf16, 16-byte aligned
+ *  gamma_h, gamma_k, gamma_c [d], conv_w [d, kernel_size]: device fp32, 16-byte aligned
+ *  v_out [B*L, d] bf16; alpha_out [M, B*L] fp32; v_ms_out [B*L] fp32 or NULL
+ *  workspace: pg_project_gate_conv_workspace_size bytes, 16-byte aligned (the call zeroes
+ *  its head, per-m-block counters, on `stream` before the launch)
+ *  Din % 64 == 0, d % 256 == 0; kernel_size in [1, 4], dilation in [1, 8],
+ *  (kernel_size - 1) * dilation <= 24. PG_ERR_WORKSPACE for a short workspace. A wait of a
+ *  conv item for its m-blocks that gives up sets device error bit 16384.
+ */
+pg_status pg_project_gate_conv_workspace_size(int32_t N, int32_t d, int32_t M, size_t* bytes);
+pg_status pg_project_gate_conv(int32_t B, int32_t L, int32_t Din, int32_t d, int32_t M, const void* e,
+                               const void* W, void* H, const float* gamma_h, const float* gamma_k,
+                               const float* gamma_c, const float* conv_w, int32_t kernel_size, int32_t dilation,
+                               float eps, void* v_out, float* alpha_out, float* v_ms_out, void* workspace,
+                               size_t workspace_bytes, pg_stream_t stream);
 
 /*
  * FP8 operands of the fused projection (Engram notes 3.4: W_V and the M W_K run in FP8).
