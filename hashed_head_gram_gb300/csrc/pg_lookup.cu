@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include "pg_conv_math.cuh"
 #include "pg_hash.cuh"
 
 namespace pg {
@@ -529,22 +530,26 @@ __global__ void __launch_bounds__(kThreads, 4) gather_nf4_kernel(
                              (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(w + 4 * piece + 2)) << 16);
       const float scale = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(w + 32)));
       const uint32_t bits = static_cast<uint32_t>(sl.sign[p] >> (8 * piece)) & 0xFFu;
+      // level * scale in fp32 pairs; the sign goes on after rounding (round-to-nearest is
+      // symmetric, so the result is the rounding of the signed product)
+      const uint64_t sc2 = pk(scale, scale);
       float x[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float val = s_nf4[(codes >> (4 * q)) & 15u] * scale;
-        x[q] = ((bits >> q) & 1u) ? -val : val;
-      }
+      for (int q = 0; q < 8; q += 2)
+        upk(mul2(pk(s_nf4[(codes >> (4 * q)) & 15u], s_nf4[(codes >> (4 * q + 4)) & 15u]), sc2), x[q], x[q + 1]);
       uint8_t* out_tok = e_out + static_cast<uint64_t>(tok) * g.e_bytes;
       if constexpr (OUTT == PG_F32) {
         uint8_t* dst = out_tok + cc * 32u;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
-                                                    __float_as_uint(x[2]), __float_as_uint(x[3]));
-        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
-                                                         __float_as_uint(x[6]), __float_as_uint(x[7]));
+        *reinterpret_cast<uint4*>(dst) = xor4(make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                                                         __float_as_uint(x[2]), __float_as_uint(x[3])),
+                                              f32_sign_mask(bits & 15u));
+        *reinterpret_cast<uint4*>(dst + 16) = xor4(make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
+                                                              __float_as_uint(x[6]), __float_as_uint(x[7])),
+                                                   f32_sign_mask(bits >> 4));
       } else {
         *reinterpret_cast<uint4*>(out_tok + cc * 16u) =
-            make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+            xor4(make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7])),
+                 bf16_sign_mask(bits));
       }
     }
     __syncwarp();  // every lane is done with the slot before it is refilled
