@@ -219,11 +219,12 @@ class Pipeline:
                                 h=dn["H"], gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"], eps=w.eps,
                                 alpha_out=self.alpha, workspace=self.ws, v_ms_out=self.v_ms)
 
-    def decode(self, B: int, steps: int = 16, reps: int = 8):
+    def decode(self, B: int, steps: int = 16, reps: int = 8, one_launch: bool = False):
         """Streaming decode on this workload's table and weights: B sequences, one token
         each per step (pg_decode_lookup, the projection with N = B, and in the context-gated
-        module pg_decode_conv_residual). `steps` consecutive steps captured in a CUDA graph and
-        replayed `reps` times back to back; returns microseconds per step."""
+        module pg_decode_conv_residual; with one_launch, pg_decode_step, B <= 8). `steps`
+        consecutive steps captured in a CUDA graph and replayed `reps` times back to back;
+        returns microseconds per step."""
         torch, pg, W, w, dn = self.torch, self.pg, self.W, self.w, self.dn
         tok = torch.from_numpy(W.make_tokens(W.shrink(w, B=B, L=steps)).T.copy()).to(self.dev)   # [steps, B]
         ctx = w.gate == W.GATE_CONTEXT
@@ -242,7 +243,22 @@ class Pipeline:
             x = dn["x"][:B].contiguous() if "x" in dn and B <= w.N else torch.zeros(B, self.d, dtype=torch.bfloat16,
                                                                                    device=self.dev)
 
+        if one_launch:
+            ws1 = torch.zeros((pg.decode_step_workspace_size(B, self.d, w.M if ctx else 0) + 3) // 4,
+                              dtype=torch.int32, device=self.dev)
+
         def step(s):
+            if one_launch:
+                if ctx:
+                    pg.decode_step(self.desc, st, tok[s], self.table, dn["W"], self.d, pg.GATE_CONTEXT, v, ws1,
+                                   canon_map=self.cmap, H=H, gamma_h=dn["gamma_h"], gamma_k=dn["gamma_k"],
+                                   gamma_c=dn["gamma_c"], conv_w=dn["conv_w"], eps=w.eps, alpha_out=alpha,
+                                   v_ms_out=v_ms)
+                else:
+                    gate = pg.GATE_SCALAR if w.gate == W.GATE_SCALAR else pg.GATE_NONE
+                    pg.decode_step(self.desc, st, tok[s], self.table, dn["W"], self.d, gate, v, ws1,
+                                   canon_map=self.cmap, g=w.g, x_resid=x if gate == pg.GATE_SCALAR else None)
+                return
             pg.decode_lookup(self.desc, st, tok[s], self.table, e, pg.BF16, canon_map=self.cmap)
             if ctx:
                 pg.project_gate(e, dn["W"], self.d, pg.GATE_CONTEXT, v, pg.BF16, M=w.M, h=H, gamma_h=dn["gamma_h"],
@@ -715,9 +731,14 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
 
     decode = []
     if p.w.dtype == p.W.DT_BF16 and not args.quick:
-        for B in sorted({1, p.w.B, 4096}):
+        for B in sorted({1, 4, p.w.B, 4096}):
             us = p.decode(B)
-            decode.append({"sequences": B, "us_per_step": round(us, 2), "tokens_per_s": round(B / us * 1e6, 1)})
+            entry = {"sequences": B, "us_per_step": round(us, 2), "tokens_per_s": round(B / us * 1e6, 1)}
+            if B <= 8 and p.d % 8 == 0:
+                one = p.decode(B, one_launch=True)
+                entry.update({"one_launch_us_per_step": round(one, 2),
+                              "one_launch_tokens_per_s": round(B / one * 1e6, 1)})
+            decode.append(entry)
     if pg.device_error() != 0:
         raise RuntimeError(f"device error word set: {pg.device_error()}")
 
@@ -741,8 +762,10 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
         "decode": {"steps": decode,
                    "how": "streaming decode, one token per sequence and step, on the same table and weights "
                           "(decode lookup -> projection with N = sequences -> decode conv where the module has "
-                          "one); 16 consecutive steps in one CUDA graph replayed back to back, no L2 flush "
-                          "(table rows cold, W and the state warm, as in serving); not part of value"},
+                          "one: us_per_step; up to 8 sequences also the whole step as one launch, "
+                          "pg_decode_step: one_launch_us_per_step); 16 consecutive steps in one CUDA graph "
+                          "replayed back to back, no L2 flush (table rows cold, W and the state warm, as in "
+                          "serving); not part of value"},
         "clocks": clk.summary(),
         "wall_s_timed_loop": round(t_wall, 4),
     }
@@ -1382,6 +1405,34 @@ def _kernel_decode(w, args, dev, g):
         print(f"decode config {w.cfg_id} B={B}: eager step {eager:.1f} us "
               f"({' + '.join(f'{n} {u:.1f}' for n, u in zip(names, parts))}); "
               f"graph {per_step:.1f} us/step, {B / per_step:.3f} M tokens/s")
+        if B <= 8:
+            # the same step as one launch (pg_decode_step)
+            ws1 = torch.zeros((pg.decode_step_workspace_size(B, d, M if ctx else 0) + 3) // 4, dtype=torch.int32,
+                              device=dev)
+            if ctx:
+                one_call = lambda s: pg.decode_step(desc, state, tokens[s], table, Wm, d, pg.GATE_CONTEXT, v, ws1,
+                                                    canon_map=cm, H=H, gamma_h=one, gamma_k=one, gamma_c=one,
+                                                    conv_w=cw, eps=w.eps, alpha_out=alpha, v_ms_out=v_ms)
+            else:
+                one_call = lambda s: pg.decode_step(desc, state, tokens[s], table, Wm, d, gate, v, ws1, canon_map=cm,
+                                                    g=w.g, x_resid=x if gate == pg.GATE_SCALAR else None)
+            eager1 = _ktime(lambda: one_call(0), args.iters, dev)
+            graph1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph1):
+                for s in range(steps):
+                    one_call(s)
+            graph1.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(reps):
+                graph1.replay()
+            b.record()
+            torch.cuda.synchronize()
+            per1 = a.elapsed_time(b) * 1e3 / (reps * steps)
+            if pg.device_error() != 0:
+                raise SystemExit("device error word set")
+            print(f"decode config {w.cfg_id} B={B}: one launch (pg_decode_step) eager {eager1:.1f} us; "
+                  f"graph {per1:.1f} us/step, {B / per1:.3f} M tokens/s")
 
 
 def _kernel_slots(args, dev, g):

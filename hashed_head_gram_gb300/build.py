@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpg.so")
-SOURCES = ["pg_abi.cu", "pg_lookup.cu", "pg_project.cu", "pg_project_simt.cu", "pg_fp8.cu", "pg_conv.cu", "pg_decode.cu", "pg_stats.cu"]
+SOURCES = ["pg_abi.cu", "pg_lookup.cu", "pg_project.cu", "pg_project_simt.cu", "pg_fp8.cu", "pg_conv.cu", "pg_decode.cu",
+           "pg_decode_step.cu", "pg_stats.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -11,7 +11,7 @@ namespace pg {
 __device__ __forceinline__ uint32_t fold32(uint64_t h) { return static_cast<uint32_t>(h ^ (h >> 32)); }
 
 // Odd multiplier m_{kind,o,k,j} of hash_version 1.
-__device__ __forceinline__ uint64_t multiplier(uint64_t seed, int kind, int o, int k, int j) {
+__host__ __device__ __forceinline__ uint64_t multiplier(uint64_t seed, int kind, int o, int k, int j) {
   const uint64_t fid = static_cast<uint64_t>(((kind * 4 + o) * 64 + k) * 4 + j);
   return mix64(seed + kGolden * (1ull + fid)) | 1ull;
 }
@@ -51,7 +51,8 @@ struct ItemConst {
   int32_t pad;
 };
 
-__device__ __forceinline__ void init_item_const(ItemConst& it, const HashParams& P, uint64_t seed, int item) {
+__host__ __device__ __forceinline__ void init_item_const(ItemConst& it, const HashParams& P, uint64_t seed,
+                                                         int item) {
   const int o = item / P.H, k = item - (item / P.H) * P.H;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {

@@ -65,6 +65,15 @@ struct HashParams {
 
 void fill_hash_params(const pg_table_desc* d, const Geometry& g, HashParams* p);
 
+// err_index (optional, device int32): set to -1 on `stream` before a lookup lowers it to
+// the smallest offending index with an unsigned atomicMin (0xFFFFFFFF reads as -1).
+inline pg_status prepare_err(int32_t* err_index, cudaStream_t stream) {
+  if (!err_index) return PG_OK;
+  if (reinterpret_cast<uintptr_t>(err_index) % 4) return PG_ERR_ALIGN;
+  cudaError_t e = cudaMemsetAsync(err_index, 0xFF, sizeof(int32_t), stream);
+  return e == cudaSuccess ? PG_OK : cuda_fail(e);
+}
+
 // ---------------------------------------------------------------- streaming decode state
 
 // PG_OK when `st` is a state pg_decode_state_init could have written (geometry in range,

@@ -77,6 +77,26 @@ class DecodeStateC(ctypes.Structure):
     ]
 
 
+
+class DecodeStepArgsC(ctypes.Structure):
+    _fields_ = [
+        ("W", ctypes.c_void_p),
+        ("d", ctypes.c_int32),
+        ("gate_kind", ctypes.c_int32),
+        ("g", ctypes.c_float),
+        ("eps", ctypes.c_float),
+        ("x_resid", ctypes.c_void_p),
+        ("H", ctypes.c_void_p),
+        ("gamma_h", ctypes.c_void_p),
+        ("gamma_k", ctypes.c_void_p),
+        ("gamma_c", ctypes.c_void_p),
+        ("conv_w", ctypes.c_void_p),
+        ("e_out", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("alpha_out", ctypes.c_void_p),
+        ("v_ms_out", ctypes.c_void_p),
+    ]
+
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(f"libpg.so is not built ({_LIB_PATH}); run `python -m hashed_head_gram_gb300.build`")
@@ -137,6 +157,10 @@ def _load():
     L.pg_decode_lookup.argtypes = [dp, sp, vp, vp, vp, u64, vp, i32, vp, vp]
     L.pg_decode_conv_residual.restype = ctypes.c_int
     L.pg_decode_conv_residual.argtypes = [sp, vp, vp, vp, vp, vp, f32, vp, vp]
+    L.pg_decode_step_workspace_size.restype = ctypes.c_int
+    L.pg_decode_step_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(u64)]
+    L.pg_decode_step.restype = ctypes.c_int
+    L.pg_decode_step.argtypes = [dp, sp, vp, vp, vp, u64, ctypes.POINTER(DecodeStepArgsC), vp, u64, vp, vp]
     L.pg_collision_counts_workspace_size.restype = ctypes.c_int
     L.pg_collision_counts_workspace_size.argtypes = [ctypes.c_int64, u32, ctypes.POINTER(sz)]
     L.pg_collision_counts.restype = ctypes.c_int
@@ -449,6 +473,30 @@ def decode_conv_residual(state: DecodeState, v: torch.Tensor, alpha: torch.Tenso
                                         _ptr(conv_w), eps, _ptr(H), _stream(stream)),
            "pg_decode_conv_residual")
 
+
+
+def decode_step_workspace_size(B: int, d: int, M: int = 0) -> int:
+    b = ctypes.c_uint64()
+    _check(_lib.pg_decode_step_workspace_size(B, d, M, ctypes.byref(b)), "pg_decode_step_workspace_size")
+    return b.value
+
+
+def decode_step(desc: TableDesc, state: DecodeState, tokens: torch.Tensor, table: torch.Tensor, W: torch.Tensor,
+                d: int, gate_kind: int, out: torch.Tensor, workspace: torch.Tensor, canon_map: Optional[torch.Tensor] = None,
+                g: float = 1.0, x_resid: Optional[torch.Tensor] = None, H: Optional[torch.Tensor] = None,
+                gamma_h: Optional[torch.Tensor] = None, gamma_k: Optional[torch.Tensor] = None,
+                gamma_c: Optional[torch.Tensor] = None, conv_w: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                e_out: Optional[torch.Tensor] = None, alpha_out: Optional[torch.Tensor] = None,
+                v_ms_out: Optional[torch.Tensor] = None, err_index: Optional[torch.Tensor] = None, stream=None):
+    """pg_decode_step: one decode step (lookup, projection, gate and, for the context gate,
+    the conv) in one launch. `workspace` must be zero before its first use."""
+    a = DecodeStepArgsC(_ptr(W), d, gate_kind, g, eps, _ptr(x_resid), _ptr(H), _ptr(gamma_h), _ptr(gamma_k),
+                        _ptr(gamma_c), _ptr(conv_w), _ptr(e_out), _ptr(out), _ptr(alpha_out), _ptr(v_ms_out))
+    nbytes = table.numel() * table.element_size()
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(_lib.pg_decode_step(ctypes.byref(desc), ctypes.byref(state.c), _ptr(tokens), _ptr(canon_map), _ptr(table),
+                               nbytes, ctypes.byref(a), _ptr(workspace), wbytes, _ptr(err_index), _stream(stream)),
+           "pg_decode_step")
 
 def collision_workspace_size(n: int, row0_span: int) -> int:
     b = ctypes.c_size_t()

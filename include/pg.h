@@ -137,7 +137,8 @@ uint64_t pg_launch_count(void);
  * and of pg_collision_counts (1024 = a head-0 row outside the given span, or a head-0
  * group too large to compare pairwise; those n-grams or pairs were left out), and of
  * pg_selftest_bounded_waits (2048, 4096), and of pg_project_gate_conv (16384 = a conv item's wait
- * for the tiles of its m-blocks).
+ * for the tiles of its m-blocks), and of pg_decode_step (32768 = a block's wait at the grid
+ * barrier, 65536 = a wait for a row of W).
  * Synchronizes the device. With clear != 0 the word is reset to 0.
  */
 pg_status pg_device_error(int32_t* code, int32_t clear);
@@ -547,6 +548,68 @@ pg_status pg_decode_lookup(const pg_table_desc* desc, const pg_decode_state* sta
 pg_status pg_decode_conv_residual(const pg_decode_state* state, const void* v, const float* alpha,
                                   const float* v_ms, const float* gamma_c, const float* conv_w, float eps,
                                   void* H, pg_stream_t stream);
+
+/*
+ * One decode step in one launch, for a few sequences (B <= 8): pg_decode_lookup, the
+ * projection with its gate (pg_project_gate with N = B) and, for the context gate,
+ * pg_decode_conv_residual, as one kernel. Addressing depends on the token IDs alone
+ * (Engram notes 3.5), so every block computes the step's e_t; each block then owns a range
+ * of the d channels, streams its rows of W and runs the conv on the same channels. The
+ * context gate's sums over all d channels (alpha, mean(v^2)) meet once at a grid barrier:
+ * every block publishes partial sums to the workspace and reduces all of them in one
+ * order, so every block uses the same alpha.
+ *
+ * Results: e_t (e_out, optional) bit-identical to pg_decode_lookup's; out, alpha_out,
+ * v_ms_out and the update of H equal the three calls' within rounding (the dot products
+ * and the gate's sums are added in another order; given the same v, alpha and mean(v^2)
+ * the conv rounds every step as pg_decode_conv_residual does). The state advances as in
+ * pg_decode_lookup + pg_decode_conv_residual: ids, pos, and for the context gate the ring.
+ * A sequence with pos[b] < 0 is skipped (device error bit 512): its rows of e_out, out,
+ * alpha_out, H and the state are left as they are.
+ */
+typedef struct {
+  const void* W;          /* bf16 [(1 + M) d, Din] (context gate; M = state->M) or [d, Din]:
+                             pg_project_gate's W; 16-byte aligned; Din = the table's e_t width */
+  int32_t d;              /* output width (context gate: state->d) */
+  int32_t gate_kind;      /* PG_GATE_NONE, PG_GATE_SCALAR or PG_GATE_CONTEXT */
+  float g;                /* scalar gate: out = x_resid + g (e W^T) */
+  float eps;              /* context gate: RMSNorm epsilon (gate and conv) */
+  const void* x_resid;    /* scalar gate: bf16 [B, d] */
+  void* H;                /* context gate: bf16 [M, B, d], the gate's h and, updated in place,
+                             the branch states the conv adds to */
+  const float* gamma_h;   /* context gate: fp32 [d] each */
+  const float* gamma_k;
+  const float* gamma_c;   /* context gate: conv RMSNorm gain, fp32 [d] */
+  const float* conv_w;    /* context gate: fp32 [d, kernel_size] */
+  void* e_out;            /* optional bf16 [B, Din], 16-byte aligned */
+  void* out;              /* bf16 [B, d]: v (context gate) or the gated output */
+  float* alpha_out;       /* optional fp32 [M, B] (context gate) */
+  float* v_ms_out;        /* optional fp32 [B]: mean(v^2) (context gate) */
+} pg_decode_step_args;
+
+/*
+ * Workspace bytes of pg_decode_step for B sequences (1..8), width d and M branches (0 for
+ * the scalar or no gate) on the current device (its SM count sets the block count).
+ */
+pg_status pg_decode_step_workspace_size(int32_t B, int32_t d, int32_t M, uint64_t* bytes);
+
+/*
+ * pg_decode_step -- desc, state, tokens, canon_map, table, table_bytes and err_index as in
+ * pg_decode_lookup (rows bf16, or NF4 in the multi-head modes; e_t in bf16), B = state->B
+ * <= 8; the context gate needs a bf16 state with a conv part (d and M as in args). The
+ * workspace (device, 16-byte aligned, >= pg_decode_step_workspace_size bytes, owned by the
+ * caller) must be zero before its first use (its first word is the grid barrier's counter:
+ * every call flips its bit 31 and leaves the other bits as they were). Calls that share a
+ * workspace must be ordered (one stream). Needs one block per SM resident at once (the grid barrier): PG_ERR_UNSUPPORTED
+ * when the shapes leave no room for it (Din > 4096, more than 64 channels per SM). A block
+ * that waits more than ~1 s at the grid barrier, or for a row of W, gives up and sets device
+ * error bit 32768 or 65536; the step's outputs are then undefined. PG_ERR_WORKSPACE when it
+ * is too small.
+ */
+pg_status pg_decode_step(const pg_table_desc* desc, const pg_decode_state* state, const int32_t* tokens,
+                         const uint32_t* canon_map, const void* table, uint64_t table_bytes,
+                         const pg_decode_step_args* args, void* workspace, uint64_t workspace_bytes,
+                         int32_t* err_index, pg_stream_t stream);
 
 /*
  * Correlated collisions (PageGram report 3.2, measured in 6.1): two n-grams that share a
