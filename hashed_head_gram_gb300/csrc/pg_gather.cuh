@@ -62,21 +62,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // items hash one (order, head) item each into s_rows / s_signs (the warp's own); the warp
 // then walks the token's e_t in the gather kernels' units (16-byte chunks of a stored row;
 // NF4: 8-element pieces) with their arithmetic, so e_t (written to out_tok, global or shared
-// memory) is bit-identical to pg_gather_sign_concat's. Returns t and the canonical ID in
-// *c0_out, after a __syncwarp (every lane has read pos and the ring and is done with s_rows);
-// the caller then writes ids[b][t mod 4] and pos[b]. A negative t is reported as device
-// error bit 512 and nothing is written.
-template <int ROWT, int OUTT, bool FLAT>
-__device__ __forceinline__ int decode_token_lookup(const HashParams& P, const GatherGeom& g,
-                                                   const ItemConst* __restrict__ s_ic, const float* s_nf4,
-                                                   uint32_t* s_rows, uint64_t* s_signs, int b, int lane,
+// memory) is bit-identical to pg_gather_sign_concat's. The gather ends with a __syncwarp
+// (every lane has read pos and the ring and is done with s_rows); the caller then writes
+// ids[b][t mod 4] and pos[b]. A negative t is reported as device error bit 512 and nothing
+// is written.
+
+// The window of sequence b's new token, by one warp: returns t = pos[b] and the token's
+// canonical ID in *c0_out (both in every lane), lanes < 4 the ID ring's slot `lane` in
+// *slot_out. Only loads: the hash constants are not needed yet.
+__device__ __forceinline__ int decode_token_window(const HashParams& P, int b, int lane,
                                                    const int32_t* __restrict__ tokens,
-                                                   const uint32_t* __restrict__ canon_map,
-                                                   const uint8_t* __restrict__ table, const int32_t* pos,
-                                                   const uint32_t* ids, uint8_t* out_tok, int32_t* err,
-                                                   int* err_word, uint32_t* c0_out) {
-  const int items = g.items;
-  // pos, the token (then its canonical ID) and the four ring slots are read at once
+                                                   const uint32_t* __restrict__ canon_map, const int32_t* pos,
+                                                   const uint32_t* ids, int32_t* err, uint32_t* c0_out,
+                                                   uint32_t* slot_out) {
   int t = 0;
   uint32_t c0 = 0, slot_id = 0;
   if (lane < 4) slot_id = ids[4 * static_cast<int64_t>(b) + lane];
@@ -84,9 +82,21 @@ __device__ __forceinline__ int decode_token_lookup(const HashParams& P, const Ga
     t = pos[b];
     c0 = canon_token(tokens, canon_map, P.vocab, b, err);
   }
-  t = __shfl_sync(0xffffffffu, t, 0);
-  c0 = __shfl_sync(0xffffffffu, c0, 0);
-  *c0_out = c0;
+  *c0_out = __shfl_sync(0xffffffffu, c0, 0);
+  *slot_out = slot_id;
+  return __shfl_sync(0xffffffffu, t, 0);
+}
+
+// The hashes and the gather of sequence b from its window (t, c0, the lanes' ID ring
+// slots). Returns t.
+template <int ROWT, int OUTT, bool FLAT>
+__device__ __forceinline__ int decode_token_gather(const HashParams& P, const GatherGeom& g,
+                                                   const ItemConst* __restrict__ s_ic, const float* s_nf4,
+                                                   uint32_t* s_rows, uint64_t* s_signs, int lane, int t,
+                                                   uint32_t c0, uint32_t slot_id,
+                                                   const uint8_t* __restrict__ table, uint8_t* out_tok,
+                                                   int* err_word) {
+  const int items = g.items;
   if (t < 0) {  // not a position any call writes: the sequence is left as it is
     if (lane == 0 && err_word) atomicOr(err_word, 512);
     return t;
@@ -185,6 +195,22 @@ __device__ __forceinline__ int decode_token_lookup(const HashParams& P, const Ga
   }
   __syncwarp();  // every lane is done with s_rows / s_signs and has read pos and the ring
   return t;
+}
+
+// Both parts: returns t and the canonical ID in *c0_out.
+template <int ROWT, int OUTT, bool FLAT>
+__device__ __forceinline__ int decode_token_lookup(const HashParams& P, const GatherGeom& g,
+                                                   const ItemConst* __restrict__ s_ic, const float* s_nf4,
+                                                   uint32_t* s_rows, uint64_t* s_signs, int b, int lane,
+                                                   const int32_t* __restrict__ tokens,
+                                                   const uint32_t* __restrict__ canon_map,
+                                                   const uint8_t* __restrict__ table, const int32_t* pos,
+                                                   const uint32_t* ids, uint8_t* out_tok, int32_t* err,
+                                                   int* err_word, uint32_t* c0_out) {
+  uint32_t slot_id;
+  const int t = decode_token_window(P, b, lane, tokens, canon_map, pos, ids, err, c0_out, &slot_id);
+  return decode_token_gather<ROWT, OUTT, FLAT>(P, g, s_ic, s_nf4, s_rows, s_signs, lane, t, *c0_out, slot_id,
+                                               table, out_tok, err_word);
 }
 
 }  // namespace

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libpg.so.
 #pragma once
 
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,6 +20,9 @@ pg_status after_launch(int n);
 // Streaming multiprocessor count and compute capability of the current device.
 int sm_count();
 int device_cc();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Device address of this library's device-side error word (current device).
 int* device_error_word();

@@ -1780,21 +1780,6 @@ pg_status launch_alpha_finalize(const float* partials, int M, int tpb, int N, in
 
 // ==================================================================== host side
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // 2-D bf16 (bytes1: 1-byte elements, E4M3) tensor [rows, cols] (row-major), box [box_rows, box_cols].
 bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
               uint32_t box_rows, CUtensorMapSwizzle swizzle, bool bytes1 = false) {
@@ -2426,3 +2411,22 @@ extern "C" pg_status pg_project_gate_context_noalloc(int32_t N, int32_t Din, int
   return pg_project_gate(N, Din, d, M, PG_BF16, e, W, PG_GATE_CONTEXT, 0.0f, nullptr, h, gamma_h, gamma_k,
                          eps, v_out, alpha_out, nullptr, scratch, PG_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+namespace pg {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace pg
