@@ -42,6 +42,7 @@
 
 #include <algorithm>
 
+#include "pg_async.cuh"
 #include "pg_conv_math.cuh"
 #include "pg_gather.cuh"
 #include "pg_internal.cuh"
@@ -59,49 +60,8 @@ constexpr int kStepMaxCh = 64;     // channels per block (d <= 64 x blocks)
 constexpr int kStepTaps = 4;
 constexpr int kErrStepWait = 32768;  // device error bit: a block gave up waiting at the grid barrier
 constexpr int kErrStepCopy = 65536;  // device error bit: a tile of W did not land in time
-constexpr uint64_t kStepWaitNs = 1000000000ull;  // bounded waits give up after ~1 s
 
 // ---------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `parity`: false after the time limit.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
-  if (bar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = now_ns();
-  while (!bar_try_wait(bar, parity))
-    if (now_ns() - t0 > kStepWaitNs) return false;
-  return true;
-}
-
-// One arrival on `bar` that also makes its current phase expect `bytes` of copies.
-__device__ __forceinline__ void bar_expect(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
 
 // Box (x, y, z) of the 3-D tensor `map` into shared `dst`, counted on `bar` when it lands.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
@@ -335,7 +295,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const __gr
   // hash constants
   if (lane == 0) {
     bar_init(my_bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    bar_init_fence();
     if (sp.split) issue_box(warp * 80);
     else if (warp < nbox) issue_box(warp * kStepBoxCols);
   }
@@ -498,7 +458,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const __gr
         box_mma(j * kStepBoxCols);
         __syncwarp();  // every lane is done with the slot: it takes the warp's next box
         if (lane == 0 && j + kStepWarps < nbox) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          fence_async_smem();
           issue_box((j + kStepWarps) * kStepBoxCols);
         }
       }
@@ -612,7 +572,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const __gr
       if (((ld_acquire_u32(sp.counter) ^ old) & 0x80000000u) == 0u) {
         const uint64_t t0 = now_ns();
         while (((ld_acquire_u32(sp.counter) ^ old) & 0x80000000u) == 0u) {
-          if (now_ns() - t0 > kStepWaitNs) {
+          if (now_ns() - t0 > kAsyncWaitNs) {
             atomicOr(sp.err_word, kErrStepWait);
             s_abort = 1;
             break;
