@@ -216,7 +216,7 @@ __device__ __forceinline__ void step_sum_partials(const float* partials, int PQ,
 
 // ---------------------------------------------------------------- the kernel
 
-template <int GATE>
+template <int GATE, int ROWS>
 __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const __grid_constant__ HashParams P,
                                                                       const __grid_constant__ StepParams sp) {
   __shared__ ItemConst s_ic[kMaxItems];
@@ -331,10 +331,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const __gr
     const int b = warp;
     uint8_t* e_tok = s_e + static_cast<uint32_t>(b) * rs;
     int* ew = blk == 0 ? sp.err_word : nullptr;
-    if (sp.rows == kRowsNf4)
+    if constexpr (ROWS == kRowsNf4)
       decode_token_gather<PG_NF4, PG_BF16, false>(P, sp.g, s_ic, s_nf4, s_rows[b], s_signs[b], lane, t_b, c0_b,
                                                   slot_b, sp.table, e_tok, ew);
-    else if (sp.rows == kRowsBf16Flat)
+    else if constexpr (ROWS == kRowsBf16Flat)
       decode_token_gather<PG_BF16, PG_BF16, true>(P, sp.g, s_ic, s_nf4, s_rows[b], s_signs[b], lane, t_b, c0_b,
                                                   slot_b, sp.table, e_tok, ew);
     else
@@ -655,10 +655,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const __gr
 
 using StepFn = void (*)(const HashParams, const StepParams);
 
-StepFn pick_step(int gate) {
-  if (gate == PG_GATE_CONTEXT) return decode_step_kernel<PG_GATE_CONTEXT>;
-  if (gate == PG_GATE_SCALAR) return decode_step_kernel<PG_GATE_SCALAR>;
-  return decode_step_kernel<PG_GATE_NONE>;
+template <int ROWS>
+StepFn pick_step_rows(int gate) {
+  if (gate == PG_GATE_CONTEXT) return decode_step_kernel<PG_GATE_CONTEXT, ROWS>;
+  if (gate == PG_GATE_SCALAR) return decode_step_kernel<PG_GATE_SCALAR, ROWS>;
+  return decode_step_kernel<PG_GATE_NONE, ROWS>;
+}
+
+// One instantiation per (gate, row type): a kernel holds one lookup variant only (its code
+// is read once per launch, so its size shows up as instruction-fetch stalls).
+StepFn pick_step(int gate, int rows) {
+  if (rows == kRowsNf4) return pick_step_rows<kRowsNf4>(gate);
+  if (rows == kRowsBf16Flat) return pick_step_rows<kRowsBf16Flat>(gate);
+  return pick_step_rows<kRowsBf16>(gate);
 }
 
 // Blocks of a step: one per SM, at most one per channel.
@@ -789,7 +798,7 @@ pg_status pg_decode_step(const pg_table_desc* desc, const pg_decode_state* state
   sp.err = err_index;
   sp.err_word = device_error_word();
 
-  StepFn fn = pick_step(gate);
+  StepFn fn = pick_step(gate, sp.rows);
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, fn);
   if (e != cudaSuccess) return cuda_fail(e);
