@@ -354,3 +354,45 @@ def test_decode_step_of_the_full_engram_module(cuda, B):
     H0 = m.H.double().numpy()
     assert rel_l2(H_got, H_ref) <= BF16_TOL
     assert rel_l2(H_got - H0, H_ref - H0) <= 5e-2
+
+
+def _layout_case(name):
+    """Context-gate modules over other table layouts: e_t widths 768 (flat rows: 12 W boxes
+    for 16 warps), 1024 (PageGram bf16 and NF4 rows: one box per warp) and 2048 (16 heads:
+    two boxes per warp, the second refilling the first's slot)."""
+    import dataclasses
+    w5 = W.make_workload(5)
+    if name == "pagegram_bf16":
+        spec = shrink_table(W.make_workload(2).tables[0])
+        return dataclasses.replace(w5, tables=[spec], d=512, M=2), spec
+    if name == "pagegram_nf4":
+        spec = shrink_table(W.make_workload(4).tables[0])
+        return dataclasses.replace(w5, tables=[spec], d=768, M=3), spec
+    if name == "flat_bf16":
+        spec = shrink_table(W.make_workload(3).tables[1])
+        return dataclasses.replace(w5, tables=[spec], d=256, M=1), spec
+    spec = dataclasses.replace(shrink_table(W.make_workload(2).tables[0]), K=16)   # 2 x 16 heads of 64
+    return dataclasses.replace(w5, tables=[spec], d=1024, M=4), spec
+
+
+@pytest.mark.parametrize("name,B", [("pagegram_bf16", 5), ("pagegram_nf4", 2), ("flat_bf16", 7), ("wide", 3)])
+def test_decode_step_context_gate_over_other_layouts(cuda, name, B):
+    pg = _pg()
+    w, spec = _layout_case(name)
+    T = 11
+    m = Module(w, spec, B, T, 230 + B, cuda)
+    assert m.Din in (768, 1024, 2048)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
+    pg.device_error(clear=True)
+    e, v, al, ms, H, state = m.run_step(pg, desc, cuda)
+    assert pg.device_error() == 0
+    e_ref, v_ref, a_ref, H_ref = m.oracle()
+    for t in range(T):
+        assert np.array_equal(bits16(e[t]), np.ascontiguousarray(e_ref[:, t])), t
+    assert rel_l2(to_f64(v).transpose(1, 0, 2), v_ref) <= BF16_TOL
+    assert np.abs(to_f64(al).transpose(1, 2, 0) - a_ref).max() < 2e-3
+    H_got = to_f64(H).transpose(1, 2, 0, 3)
+    H0 = m.H.double().numpy()
+    assert rel_l2(H_got, H_ref) <= BF16_TOL
+    assert rel_l2(H_got - H0, H_ref - H0) <= 5e-2
+    assert (state.pos.cpu() == T).all()
