@@ -27,12 +27,36 @@ constexpr int kSimtTile = 64;   // 64 x 64 outputs per block
 constexpr int kSimtK = 32;      // k-tile depth
 constexpr int kSimtThreads = 128;
 
+// Cluster rank and distributed shared memory (the split-K sums of a tile's CTAs).
+__device__ __forceinline__ uint32_t simt_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void simt_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(const void* local, uint32_t rank) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+
 // out[N, Dout] = A[N, Din] B[Dout, Din]^T (+ gate). 128 threads, thread (ty, tx) owns rows
 // ty*8 .. ty*8+7 and columns tx*4 .. tx*4+3 of the 64 x 64 tile (8 x 4 fp32 accumulators);
 // per k step it reads 8 A values and 4 B values from shared memory (3 vector loads for 32
 // FMAs). 32-deep k-tiles are double-buffered: the next tile's global loads are in registers while
 // the current one is multiplied. Out-of-range rows, columns and k read as zero.
-template <int GATE>
+// KS > 1: a cluster of KS CTAs per tile splits K (CTA z takes k-tiles z, z + KS, ...); each
+// writes its partial tile to its shared memory and CTA r adds rows 64 r / KS .. of all
+// KS partials in rank order through distributed shared memory (deterministic) and stores
+// them: KS times the CTAs of a 64 x 64 grid, so small problems fill the SMs.
+template <int GATE, int KS>
 __global__ void __launch_bounds__(kSimtThreads) simt_gemm_f32_kernel(const float* __restrict__ A,
                                                                     const float* __restrict__ Bw, int N,
                                                                     int Din, int Dout, const float* __restrict__ x,
@@ -80,13 +104,14 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_f32_kernel(const float
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  load_tile(0);
+  const int kz = KS > 1 ? static_cast<int>(simt_cluster_rank()) : 0;
+  load_tile(kz * kSimtK);
   store_tile(0);
   __syncthreads();
   int buf = 0;
-  for (int k0 = 0; k0 < Din; k0 += kSimtK) {
-    const bool more = k0 + kSimtK < Din;
-    if (more) load_tile(k0 + kSimtK);
+  for (int k0 = kz * kSimtK; k0 < Din; k0 += KS * kSimtK) {
+    const bool more = k0 + KS * kSimtK < Din;
+    if (more) load_tile(k0 + KS * kSimtK);
 #pragma unroll
     for (int kk = 0; kk < kSimtK; ++kk) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 8]);
@@ -105,18 +130,55 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_f32_kernel(const float
       buf ^= 1;
     }
   }
+  if constexpr (KS == 1) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = m0 + ty * 8 + i;
-    if (r >= N) continue;
+    for (int i = 0; i < 8; ++i) {
+      const int r = m0 + ty * 8 + i;
+      if (r >= N) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = n0 + tx * 4 + j;
-      if (c < Dout) {
-        const size_t off = static_cast<size_t>(r) * Dout + c;
-        out[off] = GATE == PG_GATE_SCALAR ? fmaf(g, acc[i][j], x[off]) : acc[i][j];
+      for (int j = 0; j < 4; ++j) {
+        const int c = n0 + tx * 4 + j;
+        if (c < Dout) {
+          const size_t off = static_cast<size_t>(r) * Dout + c;
+          out[off] = GATE == PG_GATE_SCALAR ? fmaf(g, acc[i][j], x[off]) : acc[i][j];
+        }
       }
     }
+  } else {
+    // the partial tile [64][64] in this CTA's shared memory (the A / B buffers are free)
+    float* part = &As[0][0][0];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<float4*>(part + (ty * 8 + i) * kSimtTile + tx * 4) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    simt_cluster_sync();
+    constexpr int kRows = kSimtTile / KS;  // rows this CTA adds and stores
+    for (int q = threadIdx.x; q < kRows * (kSimtTile / 4); q += kSimtThreads) {
+      const int rr = kz * kRows + q / (kSimtTile / 4), c4 = (q % (kSimtTile / 4)) * 4;
+      float4 sum = ld_dsmem_f4(part + rr * kSimtTile + c4, 0);
+#pragma unroll
+      for (int z = 1; z < KS; ++z) {
+        const float4 p4 = ld_dsmem_f4(part + rr * kSimtTile + c4, z);
+        sum.x += p4.x;
+        sum.y += p4.y;
+        sum.z += p4.z;
+        sum.w += p4.w;
+      }
+      const int r = m0 + rr;
+      if (r < N) {
+        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = n0 + c4 + j;
+          if (c < Dout) {
+            const size_t off = static_cast<size_t>(r) * Dout + c;
+            out[off] = GATE == PG_GATE_SCALAR ? fmaf(g, sv[j], x[off]) : sv[j];
+          }
+        }
+      }
+    }
+    simt_cluster_sync();  // no CTA leaves while another reads its partial tile
   }
 }
 
@@ -355,13 +417,45 @@ pg_status launch_small_rows_bf16(int N, int Din, int d, int M, int gate_kind, co
   return launch_small_nb<16>(N, Din, d, M, gate_kind, e, W, g, x, h, gamma_h, gamma_k, out, partials, vpart, stream);
 }
 
+namespace {
+
+template <int GATE, int KS>
+pg_status launch_simt_ks(int N, int Din, int d, const float* e, const float* W, float g, const float* x, float* out,
+                         cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((d + kSimtTile - 1) / kSimtTile, (N + kSimtTile - 1) / kSimtTile, KS);
+  cfg.blockDim = dim3(kSimtThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = KS;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, simt_gemm_f32_kernel<GATE, KS>, e, W, N, Din, d, x, g, out);
+  if (err != cudaSuccess) return cuda_fail(err);
+  return after_launch(1);
+}
+
+}  // namespace
+
 pg_status launch_simt_f32(int N, int Din, int d, int gate_kind, const float* e, const float* W, float g,
                           const float* x, float* out, cudaStream_t stream) {
+  // split K over a cluster of 4 (or 2) CTAs per tile when the tiles alone leave SMs idle
+  const int64_t tiles = static_cast<int64_t>((d + kSimtTile - 1) / kSimtTile) * ((N + kSimtTile - 1) / kSimtTile);
+  const int64_t fill = 4ll * sm_count();
+  if (Din >= 4 * 2 * kSimtK && tiles * 2 < fill)
+    return gate_kind == PG_GATE_SCALAR ? launch_simt_ks<PG_GATE_SCALAR, 4>(N, Din, d, e, W, g, x, out, stream)
+                                       : launch_simt_ks<PG_GATE_NONE, 4>(N, Din, d, e, W, g, x, out, stream);
+  if (Din >= 2 * 2 * kSimtK && tiles < fill)
+    return gate_kind == PG_GATE_SCALAR ? launch_simt_ks<PG_GATE_SCALAR, 2>(N, Din, d, e, W, g, x, out, stream)
+                                       : launch_simt_ks<PG_GATE_NONE, 2>(N, Din, d, e, W, g, x, out, stream);
   dim3 grid((d + kSimtTile - 1) / kSimtTile, (N + kSimtTile - 1) / kSimtTile);
   if (gate_kind == PG_GATE_SCALAR)
-    simt_gemm_f32_kernel<PG_GATE_SCALAR><<<grid, kSimtThreads, 0, stream>>>(e, W, N, Din, d, x, g, out);
+    simt_gemm_f32_kernel<PG_GATE_SCALAR, 1><<<grid, kSimtThreads, 0, stream>>>(e, W, N, Din, d, x, g, out);
   else
-    simt_gemm_f32_kernel<PG_GATE_NONE><<<grid, kSimtThreads, 0, stream>>>(e, W, N, Din, d, x, g, out);
+    simt_gemm_f32_kernel<PG_GATE_NONE, 1><<<grid, kSimtThreads, 0, stream>>>(e, W, N, Din, d, x, g, out);
   return after_launch(1);
 }
 
