@@ -503,6 +503,43 @@ def table_sector_bytes(p) -> float:
     return float(torch.unique(cand).numel()) * 32.0
 
 
+def library_row_gather(p, steps, flush) -> dict:
+    """The same rows the lookup reads, gathered by a library kernel: torch.index_select of
+    the batch's row indices (from pg_canon_hash, computed before the timed region) out of the
+    same table into a dense buffer, L2 flushed between launches. Random row reads plus a
+    dense write, without hashing, signs, dequantisation or the flat sum: a measured
+    reference for what random row reads cost on this GPU."""
+    torch, pg = p.torch, p.pg
+    heads = 1 if p.spec.mode == p.W.MODE_FLAT else p.spec.K
+    rows = torch.empty(p.N, len(p.spec.orders), heads, dtype=torch.int32, device=p.dev)
+    pg.canon_hash(p.desc, p.tokens, rows, canon_map=p.cmap)
+    idx = rows.view(-1).to(torch.int64) & 0xFFFFFFFF
+    rb = p.spec.row_bytes
+    wide = torch.int64 if rb % 8 == 0 else torch.int16
+    tab = p.table.view(torch.uint8).view(-1)[: p.spec.table_rows * rb].view(wide).view(p.spec.table_rows, -1)
+    out = torch.empty(idx.numel(), tab.shape[1], dtype=wide, device=p.dev)
+    fn = lambda: torch.index_select(tab, 0, idx, out=out)
+    for _ in range(3):
+        fn()
+        flush_l2(flush)
+    ms = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        flush_l2(flush)
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    t = statistics.mean(x.elapsed_time(y) for x, y in ms)
+    n = idx.numel()
+    del out, tab, idx, rows
+    return {"ms": round(t, 5), "rows_per_s": round(n / (t / 1e3), 1), "rows": n, "row_bytes": rb,
+            "GB/s_read_plus_write": round(2.0 * n * rb / (t / 1e3) / 1e9, 1),
+            "how": "torch.index_select of the batch's rows (indices from pg_canon_hash) into a dense buffer, "
+                   f"{steps} launches, L2 flushed between them: reads every addressed row, writes it once"}
+
+
 def compulsory_gather_bytes(p) -> float:
     """Distinct 32-byte table sectors + token IDs + the e_t write: a lower bound on the
     gather's DRAM traffic."""
@@ -696,6 +733,7 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
     if dom != "gather_sign_concat" and "gather_sign_concat" in means:
         kernels["gather_sign_concat"]["roofline"] = roofline_of(p, "gather_sign_concat", means["gather_sign_concat"],
                                                                 peaks, peak_src, sectors, cfg)
+    library_gather = None if args.quick else library_row_gather(p, steps, flush)
 
     # ---- the other paths of this workload, each warmed up and timed over the same steps
     other = []
@@ -759,6 +797,7 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
         "path": path,
         "other_paths": other,
         "uniform_ids_control": control,
+        "library_row_gather": library_gather,
         "decode": {"steps": decode,
                    "how": "streaming decode, one token per sequence and step, on the same table and weights "
                           "(decode lookup -> projection with N = sequences -> decode conv where the module has "
@@ -800,7 +839,8 @@ def run_gpu(args):
             "config": head["config"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
             "roofline": head["roofline"], "clocks": head["clocks"],
         }
-        for k in ("kernels", "path", "other_paths", "uniform_ids_control", "decode", "wall_s_timed_loop"):
+        for k in ("kernels", "path", "other_paths", "uniform_ids_control", "library_row_gather", "decode",
+                  "wall_s_timed_loop"):
             line[k] = head[k]
         if extras:
             line["workloads"] = extras

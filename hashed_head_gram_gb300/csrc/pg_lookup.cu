@@ -87,6 +87,53 @@ __global__ void __launch_bounds__(256) canon_hash_kernel(
 
 // ------------------------------------------------------------------ K2: fused gather
 
+// The IDs of a warp batch (tb consecutive tokens from flat position tb * batch) are loaded
+// ahead of the batch, once per warp: lane q < tb + 3 holds the token at flat position
+// tb * batch - 3 + q, which covers every n-gram window of the batch (n <= 4). Its raw ID is
+// read first and its canonical ID from that later, each load in flight while the warp
+// works on an earlier batch; the hashing lanes then take their n-gram's IDs by shuffles.
+// tb <= kMaxBatchTokens keeps the window within the 32 lanes.
+constexpr int kMaxBatchTokens = 32 - 3;
+
+__device__ __forceinline__ bool window_has(const GatherGeom& g, int tb, int64_t batch, int lane) {
+  const int64_t f = batch * tb - 3 + lane;
+  return batch < g.nbatch && lane < tb + 3 && f >= 0 && f < g.N;
+}
+
+__device__ __forceinline__ int32_t window_raw_id(const GatherGeom& g, int tb, const int32_t* __restrict__ tokens,
+                                                 int64_t batch, int lane) {
+  return window_has(g, tb, batch, lane) ? __ldg(tokens + (batch * tb - 3 + lane)) : 0;
+}
+
+// The canonical ID of raw ID x at this lane's window position (kPad where there is none).
+// An out-of-range ID reads as ID 0 and is reported by the batch that owns its position.
+__device__ __forceinline__ uint32_t window_canon_id(const GatherGeom& g, int tb, uint32_t vocab,
+                                                    const uint32_t* __restrict__ canon_map, int64_t batch, int lane,
+                                                    int32_t x, int32_t* err) {
+  if (!window_has(g, tb, batch, lane)) return kPad;
+  if (x < 0 || static_cast<uint32_t>(x) >= vocab) {
+    if (err && lane >= 3)
+      atomicMin(reinterpret_cast<unsigned int*>(err), static_cast<unsigned int>(batch * tb - 3 + lane));
+    x = 0;
+  }
+  return canon_map ? __ldg(canon_map + x) : static_cast<uint32_t>(x);
+}
+
+// Row and sign hash of (token s of the batch, item `ic`) from the window's canonical IDs
+// `cid`. Every lane of the warp calls it (shuffles); `valid` lanes get the row.
+__device__ __forceinline__ uint32_t window_row(const ItemConst& ic, int mode, const GatherGeom& g, int64_t tok, int s,
+                                               uint32_t cid, bool valid, uint64_t* hs) {
+  uint64_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) c[j] = __shfl_sync(0xffffffffu, cid, s - j + 3);
+  if (!valid) return 0u;
+  const uint32_t t = fastmod(static_cast<uint32_t>(tok), g.fm_L, g.L);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (!(j < ic.n && t >= static_cast<uint32_t>(j))) c[j] = kPad;
+  return item_row_ids(ic, mode, c, hs);
+}
+
 constexpr int kThreads = 256;       // threads per gather block
 constexpr int kChunksPerThread = 8; // 16-byte chunks (or NF4 tasks) per lane per warp batch
 
@@ -128,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
   constexpr int PT = CT ? (FLAT ? RC : ITEMS * RC) : 1;
   constexpr int TBC = CT ? batch_tokens(PT, ITEMS) : 1;
   constexpr int NCH = CT ? (TBC * PT + 31) / 32 : kChunksPerThread;
+  static_assert(TBC <= kMaxBatchTokens, "the batch's ID window fits the lanes");
   const int per_tok = CT ? PT : g.per_tok;
   const int items = CT ? ITEMS : g.items;
   const int tb = CT ? TBC : g.tb;
@@ -143,17 +191,48 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
   if (threadIdx.x < g.items) init_item_const(s_ic[threadIdx.x], P, seed, threadIdx.x);
   __syncthreads();
 
+  // phase A of a batch: lane p = (token s, item) hashes its row and sign words from the
+  // window's canonical IDs `cid` (no loads)
+  auto hash_to = [&](int64_t batch, uint32_t cid, uint32_t* s_rows, uint64_t* s_signs) {
+    const int p = lane;
+    const int s = p < tb * items ? p / items : 0;
+    const int item = p - s * items;
+    const int64_t tok = batch * tb + s;
+    const bool valid = batch < g.nbatch && p < tb * items && tok < g.N;
+    uint64_t hs;
+    const uint32_t row = window_row(s_ic[valid ? item : 0], P.mode, g, tok, s, cid, valid, &hs);
+    if (valid) {
+      s_rows[p] = row;
+      for (int q = 0; q < g.W; ++q) s_signs[p * g.W + q] = mix64(hs + kGolden * static_cast<uint64_t>(q + 1));
+    }
+  };
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
-  if (first < g.nbatch)
+  // IDs: raw IDs two batches ahead of the one hashed, canonical IDs one ahead. Batches of
+  // one token keep per-lane ID reads instead (each hashing lane reads its n-gram's IDs while
+  // the previous batch's rows are in flight): there the window's bookkeeping costs more
+  // issue slots than the reads' latency, which the row loads hide (measured).
+  constexpr bool kWindow = !CT || TBC > 1;
+  int32_t raw_ahead = 0;
+  uint32_t cid_ahead = kPad;
+  if constexpr (kWindow) {
+    raw_ahead = window_raw_id(g, tb, tokens, first, lane);
+    const int32_t raw1 = window_raw_id(g, tb, tokens, first + nwarps, lane);
+    const uint32_t cid0 = window_canon_id(g, tb, P.vocab, canon_map, first, lane, raw_ahead, err);
+    cid_ahead = window_canon_id(g, tb, P.vocab, canon_map, first + nwarps, lane, raw1, err);
+    raw_ahead = window_raw_id(g, tb, tokens, first + 2 * nwarps, lane);
+    hash_to(first, cid0, s_rows_all[warp][0], s_signs_all[warp][0]);
+  } else if (first < g.nbatch) {
     hash_batch<ITEMS, TBC>(s_ic, g, P.mode, first, lane, tokens, canon_map, P.vocab, s_rows_all[warp][0],
                            s_signs_all[warp][0], err);
+  }
   __syncwarp();
   const int chunks = tb * per_tok;
   int cur = 0;
   for (int64_t batch = first; batch < g.nbatch; batch += nwarps) {
     const uint32_t* rows = s_rows_all[warp][cur];
     const uint64_t* signs = s_signs_all[warp][cur];
+    uint32_t cid_next = kPad;
     // a batch is streamed in rounds of 32 * NCH chunks (one round unless a token's e_t
     // is wider than a round)
     for (int base = 0; base < chunks; base += 32 * NCH) {
@@ -184,11 +263,17 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
         }
       }
     }
-    // ---- phase A of the next batch while the loads are in flight
-    const int64_t next = batch + nwarps;
-    if (base == 0 && next < g.nbatch)
-      hash_batch<ITEMS, TBC>(s_ic, g, P.mode, next, lane, tokens, canon_map, P.vocab, s_rows_all[warp][cur ^ 1],
-                             s_signs_all[warp][cur ^ 1], err);
+    // ---- IDs of later batches, then phase A of the next batch, while the loads are in flight
+    if constexpr (kWindow) {
+      if (base == 0) {
+        cid_next = window_canon_id(g, tb, P.vocab, canon_map, batch + 2 * nwarps, lane, raw_ahead, err);
+        raw_ahead = window_raw_id(g, tb, tokens, batch + 3 * nwarps, lane);
+        hash_to(batch + nwarps, cid_ahead, s_rows_all[warp][cur ^ 1], s_signs_all[warp][cur ^ 1]);
+      }
+    } else if (base == 0 && batch + nwarps < g.nbatch) {
+      hash_batch<ITEMS, TBC>(s_ic, g, P.mode, batch + nwarps, lane, tokens, canon_map, P.vocab,
+                             s_rows_all[warp][cur ^ 1], s_signs_all[warp][cur ^ 1], err);
+    }
     // ---- phase B, finish: dequantise, sign, (sum), store
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
@@ -248,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, (RC > 0 && ITEMS > 0) ? 3 : 2) gathe
     }  // rounds
     __syncwarp();
     cur ^= 1;
+    cid_ahead = cid_next;
   }
 }
 
@@ -387,11 +473,15 @@ __global__ void __launch_bounds__(kThreads, 3) gather_e4m3_kernel(
 // ------------------------------------------------------------------ K2, NF4 rows
 
 // A 34-byte NF4 row starts at an even byte offset o = 34 row mod 16, so it lies inside the
-// three aligned 16-byte chunks [34 row - o, 34 row - o + 48). Each warp batch (32 rows)
-// copies those windows into the warp's shared-memory ring with cp.async (no registers
-// held while the rows are in flight) kNf4Depth batches ahead, then dequantises from shared
-// memory: the same task mapping and output stores as the bf16 path (one lane per 8
-// elements, 16 bytes of e_t per lane and 512 contiguous bytes per warp store).
+// three aligned 16-byte chunks [34 row - o, 34 row - o + 48). Each warp batch (tb tokens,
+// tb * items <= 32 rows) copies those windows into the warp's shared-memory ring with
+// cp.async (no registers held while the rows are in flight) kNf4Depth batches ahead, then
+// dequantises from shared memory: the same task mapping and output stores as the bf16 path
+// (one lane per 8 elements, 16 bytes of e_t per lane and 512 contiguous bytes per warp
+// store).
+// The IDs a batch hashes are loaded ahead too (window_raw_id two iterations before the
+// batch is staged, window_canon_id one iteration before), so no load sits between a
+// batch's dequantisation and the copies of the batch staged after it.
 constexpr int kNf4Window = 48;
 constexpr int kNf4Depth = 3;
 
@@ -415,8 +505,9 @@ __global__ void __launch_bounds__(kThreads, 4) gather_nf4_kernel(
     int32_t* err) {
   constexpr int kWarps = kThreads / 32;
   constexpr int TBC = ITEMS > 0 ? batch_tokens(ITEMS * 8, ITEMS) : 1;
+  static_assert(ITEMS == 0 || TBC <= kMaxBatchTokens, "the batch's ID window fits the lanes");
   const int items = ITEMS > 0 ? ITEMS : g.items;
-  const int tb = ITEMS > 0 ? TBC : g.tb;
+  const int tb = ITEMS > 0 ? TBC : g.tb;  // <= kMaxBatchTokens (host)
   const int per_tok = items * 8;
   const int tasks = tb * per_tok;  // <= 32 * 8
   __shared__ ItemConst s_ic[kMaxItems];
@@ -427,29 +518,33 @@ __global__ void __launch_bounds__(kThreads, 4) gather_nf4_kernel(
   if (threadIdx.x < 16) s_nf4[threadIdx.x] = __uint_as_float(c_nf4_bits[threadIdx.x]);
   __syncthreads();
 
-  // phase A of a batch: lane p hashes row p of the batch, stores its sign word and window
-  // offset, and starts the copy of its window
-  auto stage = [&](int64_t batch, Nf4Slot& sl) {
+  auto raw_id = [&](int64_t batch) { return window_raw_id(g, tb, tokens, batch, lane); };
+  auto canon_id = [&](int64_t batch, int32_t x) {
+    return window_canon_id(g, tb, P.vocab, canon_map, batch, lane, x, err);
+  };
+
+  // a batch: lane p hashes row p from the window's canonical IDs `cid`, stores its sign
+  // word and window offset, and starts the copy of its window
+  auto stage = [&](int64_t batch, Nf4Slot& sl, uint32_t cid) {
     const int p = lane;
-    if (p < tb * items) {
-      const int s = p / items, item = p - (p / items) * items;
-      const int64_t tok = batch * tb + s;
-      if (tok < g.N) {
-        const uint32_t t = fastmod(static_cast<uint32_t>(tok), g.fm_L, g.L);
-        uint64_t hs;
-        const uint32_t row = item_row(s_ic[item], P.mode, tokens, canon_map, P.vocab, tok, t, err, &hs);
-        const uint64_t start = static_cast<uint64_t>(row) * 34u;
-        const uint32_t off = static_cast<uint32_t>(start & 15u);
-        sl.sign[p] = mix64(hs + kGolden);
-        sl.off[p] = static_cast<uint8_t>(off);
-        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sl.rows[p]));
+    const int s = p < tb * items ? p / items : 0;
+    const int item = p - s * items;
+    const int64_t tok = batch * tb + s;
+    const bool valid = batch < g.nbatch && p < tb * items && tok < g.N;
+    uint64_t hs;
+    const uint32_t row = window_row(s_ic[valid ? item : 0], P.mode, g, tok, s, cid, valid, &hs);
+    if (valid) {
+      const uint64_t start = static_cast<uint64_t>(row) * 34u;
+      const uint32_t off = static_cast<uint32_t>(start & 15u);
+      sl.sign[p] = mix64(hs + kGolden);
+      sl.off[p] = static_cast<uint8_t>(off);
+      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(sl.rows[p]));
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const uint64_t c = start - off + 16u * k;
-          if (c < g.table_bytes) {
-            const uint64_t left = g.table_bytes - c;
-            cp_async16_zfill(dst + 16 * k, table + c, left < 16u ? static_cast<uint32_t>(left) : 16u);
-          }
+      for (int k = 0; k < 3; ++k) {
+        const uint64_t ch = start - off + 16u * k;
+        if (ch < g.table_bytes) {
+          const uint64_t left = g.table_bytes - ch;
+          cp_async16_zfill(dst + 16 * k, table + ch, left < 16u ? static_cast<uint32_t>(left) : 16u);
         }
       }
     }
@@ -458,17 +553,27 @@ __global__ void __launch_bounds__(kThreads, 4) gather_nf4_kernel(
 
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  // prologue: IDs of the first kNf4Depth + 2 batches, canonical IDs of the first
+  // kNf4Depth + 1, the first kNf4Depth batches staged
+  int32_t raw[kNf4Depth + 2];
+  uint32_t cid[kNf4Depth + 1];
 #pragma unroll
-  for (int d = 0; d < kNf4Depth; ++d) {
-    const int64_t b = first + d * nwarps;
-    if (b < g.nbatch) stage(b, s_ring[warp][d]);
-    else cp_async_commit();
-  }
+  for (int d = 0; d < kNf4Depth + 2; ++d) raw[d] = raw_id(first + d * nwarps);
+#pragma unroll
+  for (int d = 0; d < kNf4Depth + 1; ++d) cid[d] = canon_id(first + d * nwarps, raw[d]);
+#pragma unroll
+  for (int d = 0; d < kNf4Depth; ++d) stage(first + d * nwarps, s_ring[warp][d], cid[d]);
+  uint32_t cid_ahead = cid[kNf4Depth];      // canonical IDs of batch + kNf4Depth * nwarps
+  int32_t raw_ahead = raw[kNf4Depth + 1];   // raw IDs of batch + (kNf4Depth + 1) * nwarps
   int slot = 0;
   for (int64_t batch = first; batch < g.nbatch; batch += nwarps) {
+    // IDs for later batches, in flight during this batch's dequantisation
+    const uint32_t cid_next = canon_id(batch + (kNf4Depth + 1) * nwarps, raw_ahead);
+    raw_ahead = raw_id(batch + (kNf4Depth + 2) * nwarps);
     cp_async_wait<kNf4Depth - 1>();  // this lane's copies for `batch` have landed
     __syncwarp();                    // ... and every other lane's
     const Nf4Slot& sl = s_ring[warp][slot];
+    const uint8_t* sign_bytes = reinterpret_cast<const uint8_t*>(sl.sign);  // byte j: bits 8 j .. 8 j + 7
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int c = lane + 32 * i;
@@ -482,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 4) gather_nf4_kernel(
       const uint32_t codes = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(w + 4 * piece)) |
                              (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(w + 4 * piece + 2)) << 16);
       const float scale = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(w + 32)));
-      const uint32_t bits = static_cast<uint32_t>(sl.sign[p] >> (8 * piece)) & 0xFFu;
+      const uint32_t bits = sign_bytes[8 * p + piece];
       // level * scale in fp32 pairs; the sign goes on after rounding (round-to-nearest is
       // symmetric, so the result is the rounding of the signed product)
       const uint64_t sc2 = pk(scale, scale);
@@ -506,9 +611,8 @@ __global__ void __launch_bounds__(kThreads, 4) gather_nf4_kernel(
       }
     }
     __syncwarp();  // every lane is done with the slot before it is refilled
-    const int64_t next = batch + kNf4Depth * nwarps;
-    if (next < g.nbatch) stage(next, s_ring[warp][slot]);
-    else cp_async_commit();
+    stage(batch + kNf4Depth * nwarps, s_ring[warp][slot], cid_ahead);
+    cid_ahead = cid_next;
     slot = slot + 1 == kNf4Depth ? 0 : slot + 1;
   }
   cp_async_wait<0>();
@@ -730,6 +834,7 @@ pg_status pg_gather_sign_concat(const pg_table_desc* desc, const int32_t* tokens
   // fit 8 per lane
   int tb = batch_tokens(g.per_tok, items);
   if (tb < 1) tb = 1;  // a token wider than one round: streamed in several rounds
+  if (tb > kMaxBatchTokens) tb = kMaxBatchTokens;  // the batch's ID window fits the lanes
   g.tb = tb;
   // floor(x / n) = umulhi(x, floor(2^32 / n) + 1), exact while x * n < 2^32 (x, n < 2^16 here)
   g.tok_magic = static_cast<uint32_t>((1ull << 32) / static_cast<uint32_t>(g.per_tok) + 1ull);

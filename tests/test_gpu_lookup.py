@@ -104,22 +104,24 @@ def test_toy_hash_on_the_gpu(cuda):
         assert rows.cpu().numpy().view(np.uint32)[1:].tolist() == [5, 3]
 
 
-def test_out_of_range_tokens_are_reported_and_clamped(cuda):
+@pytest.mark.parametrize("cfg", [2, 5, 4])  # two-token batches, one-token batches, NF4 rows
+def test_out_of_range_tokens_are_reported_and_clamped(cuda, cfg):
     pg = _pg()
-    w, spec, tokens, cmap = _inputs(2, 0, B=4, L=100)
+    w, spec, tokens, cmap = _inputs(cfg, 0, B=4, L=100)
     tokens = tokens.copy()
     tokens[2, 50] = w.vocab + 5
     tokens[3, 7] = -1
-    desc = pg.table_desc(spec, w.vocab)
+    desc = pg.table_desc(spec, w.vocab, w.canon_vocab)
     table = W.make_table(w, spec, "cpu")
     e = torch.empty(w.N, spec.e_width, dtype=torch.bfloat16, device=cuda)
     err = torch.empty(1, dtype=torch.int32, device=cuda)
-    pg.gather_sign_concat(desc, torch.from_numpy(tokens).to(cuda), table.to(cuda), e, orc.BF16, err_index=err)
+    pg.gather_sign_concat(desc, torch.from_numpy(tokens).to(cuda), table.to(cuda), e, orc.BF16,
+                          canon_map=canon_tensor(cmap, cuda), err_index=err)
     torch.cuda.synchronize()
     assert err.item() == 2 * 100 + 50
     # tokens whose windows avoid the bad IDs still match the oracle
     good = np.array([i for i in range(w.N) if not (250 <= i <= 252 or 307 <= i <= 309)])
-    ref = oracle_e(spec, tokens.clip(0, w.vocab - 1), None, w.vocab, table, orc.BF16, which=good)
+    ref = oracle_e(spec, tokens.clip(0, w.vocab - 1), cmap, w.vocab, table, orc.BF16, which=good)
     assert np.array_equal(bits16(e)[good], ref)
 
 
