@@ -503,41 +503,55 @@ def table_sector_bytes(p) -> float:
     return float(torch.unique(cand).numel()) * 32.0
 
 
-def library_row_gather(p, steps, flush) -> dict:
-    """The same rows the lookup reads, gathered by a library kernel: torch.index_select of
-    the batch's row indices (from pg_canon_hash, computed before the timed region) out of the
-    same table into a dense buffer, L2 flushed between launches. Random row reads plus a
-    dense write, without hashing, signs, dequantisation or the flat sum: a measured
-    reference for what random row reads cost on this GPU."""
+def row_references(p, steps, flush) -> dict:
+    """The rows the lookup reads, moved by themselves: pg_row_copy (the same row indices,
+    from pg_canon_hash before the timed region, the same 16-byte loads, a dense write of each
+    row's 16-byte-aligned window; no hashing, signs, dequantisation or concatenation) and
+    torch.index_select of the same rows (a library gather). Each timed over `steps`
+    launches with the L2 flushed between them."""
     torch, pg = p.torch, p.pg
     heads = 1 if p.spec.mode == p.W.MODE_FLAT else p.spec.K
     rows = torch.empty(p.N, len(p.spec.orders), heads, dtype=torch.int32, device=p.dev)
     pg.canon_hash(p.desc, p.tokens, rows, canon_map=p.cmap)
-    idx = rows.view(-1).to(torch.int64) & 0xFFFFFFFF
+    rows = rows.view(-1)
+    n = rows.numel()
     rb = p.spec.row_bytes
+    wb = pg.row_copy_window(rb)
+    ob = max(wb, p.e.element_size() * (p.spec.r if p.spec.mode != p.W.MODE_FLAT else p.din))  # e_t bytes per row
+    out = torch.empty(n, ob, dtype=torch.uint8, device=p.dev)
+    idx = rows.to(torch.int64) & 0xFFFFFFFF
     wide = torch.int64 if rb % 8 == 0 else torch.int16
     tab = p.table.view(torch.uint8).view(-1)[: p.spec.table_rows * rb].view(wide).view(p.spec.table_rows, -1)
-    out = torch.empty(idx.numel(), tab.shape[1], dtype=wide, device=p.dev)
-    fn = lambda: torch.index_select(tab, 0, idx, out=out)
-    for _ in range(3):
-        fn()
-        flush_l2(flush)
-    ms = []
-    for _ in range(steps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        flush_l2(flush)
-        ms.append((a, b))
-    torch.cuda.synchronize()
-    t = statistics.mean(x.elapsed_time(y) for x, y in ms)
-    n = idx.numel()
-    del out, tab, idx, rows
-    return {"ms": round(t, 5), "rows_per_s": round(n / (t / 1e3), 1), "rows": n, "row_bytes": rb,
-            "GB/s_read_plus_write": round(2.0 * n * rb / (t / 1e3) / 1e9, 1),
-            "how": "torch.index_select of the batch's rows (indices from pg_canon_hash) into a dense buffer, "
-                   f"{steps} launches, L2 flushed between them: reads every addressed row, writes it once"}
+    sel = torch.empty(n, tab.shape[1], dtype=wide, device=p.dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+            flush_l2(flush)
+        ms = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            flush_l2(flush)
+            ms.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(x.elapsed_time(y) for x, y in ms)
+
+    t_copy = timed(lambda: pg.row_copy(p.table, rb, rows, out, ob))
+    t_sel = timed(lambda: torch.index_select(tab, 0, idx, out=sel))
+    del out, sel, tab, idx, rows
+    return {
+        "rows": n, "row_bytes": rb,
+        "row_copy": {"ms": round(t_copy, 5), "rows_per_s": round(n / (t_copy / 1e3), 1), "window_bytes": wb,
+                     "out_row_bytes": ob, "GB/s_read_plus_write": round(n * (wb + ob) / (t_copy / 1e3) / 1e9, 1),
+                     "how": f"pg_row_copy of the batch's rows (indices from pg_canon_hash): each row's "
+                            f"{wb}-byte aligned window read with 16-byte loads and written densely as a {ob}-byte "
+                            f"row (the lookup's output bytes per row), {steps} launches, L2 flushed between them"},
+        "torch_index_select": {"ms": round(t_sel, 5), "rows_per_s": round(n / (t_sel / 1e3), 1),
+                               "how": "torch.index_select of the same rows into a dense buffer (library gather)"},
+    }
 
 
 def compulsory_gather_bytes(p) -> float:
@@ -736,7 +750,7 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
     if dom != "gather_sign_concat" and "gather_sign_concat" in means:
         kernels["gather_sign_concat"]["roofline"] = roofline_of(p, "gather_sign_concat", means["gather_sign_concat"],
                                                                 peaks, peak_src, sectors, cfg)
-    library_gather = None if args.quick else library_row_gather(p, steps, flush)
+    rows_ref = None if args.quick else row_references(p, steps, flush)
 
     # ---- the other paths of this workload, each warmed up and timed over the same steps
     other = []
@@ -751,6 +765,14 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
                       "kernels": {name: kernel_entry(p, name, ms, peaks, sectors) for name, ms in om.items()}})
     if p.w.gate == p.W.GATE_CONTEXT:
         p.dn["H"].copy_(p.H0)
+    if rows_ref is not None:  # the gather kernel (default or two-kernel path) against its rows moved alone
+        g_ms = means.get("gather_sign_concat")
+        for op in other:
+            if g_ms is None and "gather_sign_concat" in op["kernels"]:
+                g_ms = op["kernels"]["gather_sign_concat"]["ms"]
+        if g_ms is not None:
+            rows_ref["gather_sign_concat_ms"] = round(g_ms, 5)
+            rows_ref["gather_over_row_copy"] = round(g_ms / rows_ref["row_copy"]["ms"], 3)
 
     # ---- the no-reuse control: the same path on uniform IDs (Zipf workloads only)
     control = None
@@ -800,7 +822,7 @@ def measure_workload(cfg, args, dev, rank, world, steps, headline):
         "path": path,
         "other_paths": other,
         "uniform_ids_control": control,
-        "library_row_gather": library_gather,
+        "rows_moved_alone": rows_ref,
         "decode": {"steps": decode,
                    "how": "streaming decode, one token per sequence and step, on the same table and weights "
                           "(decode lookup -> projection with N = sequences -> decode conv where the module has "
@@ -842,7 +864,7 @@ def run_gpu(args):
             "config": head["config"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
             "roofline": head["roofline"], "clocks": head["clocks"],
         }
-        for k in ("kernels", "path", "other_paths", "uniform_ids_control", "library_row_gather", "decode",
+        for k in ("kernels", "path", "other_paths", "uniform_ids_control", "rows_moved_alone", "decode",
                   "wall_s_timed_loop"):
             line[k] = head[k]
         if extras:

@@ -13,6 +13,9 @@
 //   4. per (head k, bucket): every pair of the bucket compared on head k; a warp holds 32
 //      buckets of one head, sums its counts and adds them with one atomic.
 // The counts are integers and do not depend on the order a bucket was filled in.
+//
+// pg_row_copy (diagnostic): the rows a lookup reads, moved and nothing else, to measure
+// what that access pattern costs on its own.
 #include <algorithm>
 
 #include "pg_internal.cuh"
@@ -179,10 +182,94 @@ __global__ void pair_kernel(const uint32_t* __restrict__ rows, int64_t stride, i
   }
 }
 
+// ---------------------------------------------------------------- row copy (diagnostic)
+
+// Output row i holds ocpr 16-byte chunks: the first cpr are the 16-byte-aligned window that
+// holds row rows[i] of the table, the rest zeros (so the written bytes can match a lookup's
+// output row); window chunks not wholly inside the table are written as zeros.
+// Consecutive threads take consecutive output chunks (a warp: 512 contiguous bytes, rows
+// read with the lookup kernels' 16-byte non-L1-allocating loads); kCopyUnroll chunks per
+// thread in flight. c / ocpr by Lemire's direct division (ocpr_div = ceil(2^64 / ocpr),
+// exact for 32-bit c; ocpr == 1 takes c itself). chunks < 2^31, so base + kCopyUnroll
+// threads' strides stays below 2^32.
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(256) row_copy_kernel(const uint8_t* __restrict__ table, uint64_t table_bytes,
+                                                       uint32_t row_bytes, uint32_t cpr, uint32_t ocpr,
+                                                       uint64_t ocpr_div, const uint32_t* __restrict__ rows,
+                                                       uint32_t chunks, uint8_t* __restrict__ out) {
+  const uint32_t nthreads = gridDim.x * blockDim.x;
+  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < chunks; base += nthreads * kCopyUnroll) {
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const uint32_t c = base + u * nthreads;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (c < chunks) {
+        const uint32_t i = ocpr == 1 ? c : static_cast<uint32_t>(__umul64hi(ocpr_div, c));  // c / ocpr
+        const uint32_t piece = c - i * ocpr;
+        if (piece < cpr) {
+          const uint64_t at = (static_cast<uint64_t>(rows[i]) * row_bytes & ~15ull) + 16ull * piece;
+          if (at + 16 <= table_bytes) {
+            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                         : "l"(table + at));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const uint32_t c = base + u * nthreads;
+      if (c < chunks) *reinterpret_cast<uint4*>(out + 16ull * c) = v[u];
+    }
+  }
+}
+
 }  // namespace
 }  // namespace pg
 
 extern "C" {
+
+pg_status pg_row_copy_window(uint32_t row_bytes, uint32_t* window_bytes) {
+  if (!window_bytes) return PG_ERR_NULL;
+  if (row_bytes == 0 || row_bytes > 4096) return PG_ERR_SHAPE;
+  // a row starts at a multiple of gcd(row_bytes, 16) within its first chunk
+  uint32_t g = 16;
+  while (row_bytes % g) g >>= 1;
+  *window_bytes = (row_bytes + (16 - g) + 15) / 16 * 16;
+  return PG_OK;
+}
+
+pg_status pg_row_copy(const void* table, uint64_t table_bytes, uint32_t row_bytes, const uint32_t* rows, int64_t n,
+                      void* out, uint32_t out_row_bytes, pg_stream_t stream_) {
+  using namespace pg;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint32_t wb = 0;
+  pg_status st = pg_row_copy_window(row_bytes, &wb);
+  if (st != PG_OK) return st;
+  if (out_row_bytes == 0) out_row_bytes = wb;
+  if (out_row_bytes < wb || out_row_bytes % 16 || out_row_bytes > 65536) return PG_ERR_SHAPE;
+  const uint32_t cpr = wb / 16, ocpr = out_row_bytes / 16;
+  if (n < 0 || static_cast<uint64_t>(n) * ocpr >= (1ull << 31)) return PG_ERR_SHAPE;
+  if (n == 0) return PG_OK;
+  if (!table || !rows || !out) return PG_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(table) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+      reinterpret_cast<uintptr_t>(rows) % 4)
+    return PG_ERR_ALIGN;
+  const int nsm = sm_count();
+  if (nsm == 0) return cuda_fail(cudaGetLastError());
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_copy_kernel, 256, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const uint32_t chunks = static_cast<uint32_t>(n * ocpr);
+  const int64_t want = (static_cast<int64_t>(chunks) + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(nsm) * std::max(per_sm, 1);
+  const int grid = static_cast<int>(std::min(want, cap));
+  row_copy_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(table), table_bytes, row_bytes, cpr, ocpr,
+                                            ~0ull / ocpr + 1ull, rows, chunks, static_cast<uint8_t*>(out));
+  return after_launch(1);
+}
 
 pg_status pg_collision_counts_workspace_size(int64_t n, uint32_t row0_span, size_t* bytes) {
   if (!bytes) return PG_ERR_NULL;

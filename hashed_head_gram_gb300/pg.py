@@ -169,6 +169,10 @@ def _load():
     L.pg_conv_residual.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp]
     L.pg_selftest_bounded_waits.restype = ctypes.c_int
     L.pg_selftest_bounded_waits.argtypes = [vp, vp]
+    L.pg_row_copy_window.restype = ctypes.c_int
+    L.pg_row_copy_window.argtypes = [u32, ctypes.POINTER(u32)]
+    L.pg_row_copy.restype = ctypes.c_int
+    L.pg_row_copy.argtypes = [vp, u64, u32, vp, ctypes.c_int64, vp, u32, vp]
     return L
 
 
@@ -531,6 +535,21 @@ def selftest_bounded_waits(zero_word: torch.Tensor, stream=None):
     _check(_lib.pg_selftest_bounded_waits(_ptr(zero_word), _stream(stream)), "pg_selftest_bounded_waits")
 
 
+def row_copy_window(row_bytes: int) -> int:
+    w = ctypes.c_uint32()
+    _check(_lib.pg_row_copy_window(row_bytes, ctypes.byref(w)), "pg_row_copy_window")
+    return w.value
+
+
+def row_copy(table: torch.Tensor, row_bytes: int, rows: torch.Tensor, out: torch.Tensor, out_row_bytes: int = 0,
+             stream=None):
+    """Diagnostic: out [n, out_row_bytes or row_copy_window(row_bytes)] bytes = the windows of
+    the table rows `rows` (int32 view of uint32 indices, n = rows.numel()), zero-padded."""
+    nbytes = table.numel() * table.element_size()
+    _check(_lib.pg_row_copy(_ptr(table), nbytes, row_bytes, _ptr(rows), rows.numel(), _ptr(out), out_row_bytes,
+                            _stream(stream)), "pg_row_copy")
+
+
 def dtype_code(t: torch.dtype) -> int:
     return {torch.float32: F32, torch.bfloat16: BF16}[t]
 
@@ -540,6 +559,7 @@ __all__ = ["PgError", "TableDesc", "table_desc", "table_geometry", "canon_hash",
            "workspace_size", "project_gate", "lookup_project_gate", "gather_project_workspace_size",
            "gather_project_gate", "nf4_quantize", "fp8_quantize", "project_gate_fp8", "project_gate_context_noalloc", "conv_residual",
            "decode_state_size", "DecodeState", "decode_reset", "decode_lookup", "decode_conv_residual",
-           "collision_workspace_size", "collision_counts", "launch_count", "device_error", "selftest_bounded_waits", "lib",
+           "collision_workspace_size", "collision_counts", "launch_count", "device_error", "selftest_bounded_waits",
+           "row_copy_window", "row_copy", "lib",
            "FLAT", "ENGRAM", "PAGEGRAM", "F32", "BF16", "NF4", "GATE_NONE", "GATE_SCALAR", "GATE_CONTEXT",
            "HASH_MULXOR", "HASH_TOY", "PG_NO_ROW"]

@@ -636,6 +636,31 @@ pg_status pg_collision_counts(const uint32_t* rows, int64_t n, int32_t K, int64_
                               uint32_t row0_span, uint64_t* counts_out, void* workspace, size_t workspace_bytes,
                               pg_stream_t stream);
 
+/*
+ * Diagnostic, no counterpart on the pages: the memory access pattern of a lookup on its
+ * own. pg_row_copy moves the rows a gather reads -- the same row indices, the same 16-byte
+ * loads, a dense write -- without hashing, signs, dequantisation or concatenation, so the
+ * time a gather takes can be set beside the time its rows alone take to move.
+ *
+ * pg_row_copy_window -- *window_bytes = the bytes copied per row: the 16-byte chunks that
+ * hold a row of row_bytes bytes (row_bytes itself when it is a multiple of 16; 48 for the
+ * 34-byte NF4 rows). row_bytes in [1, 4096], else PG_ERR_SHAPE.
+ *
+ * pg_row_copy -- output row i (out_row_bytes bytes at out + i * out_row_bytes; device,
+ * 16-byte aligned) = the aligned window of `table` (device, 16-byte aligned, table_bytes
+ * long) holding row rows[i] (device uint32 [n], 4-byte aligned; the row starts at byte
+ * rows[i] * row_bytes), followed by zeros up to out_row_bytes: out_row_bytes = 0 takes the
+ * window's size; otherwise a multiple of 16, at least the window and at most 65536 (a
+ * lookup's output row, e.g. 128 bytes of bf16 e_t per 34-byte NF4 row), else PG_ERR_SHAPE.
+ * A 16-byte chunk of a window that is not wholly inside the table (a row index past the
+ * end) is written as zeros. n * out_row_bytes / 16 < 2^31, else PG_ERR_SHAPE; n == 0
+ * enqueues nothing. One launch on `stream`.
+ */
+pg_status pg_row_copy_window(uint32_t row_bytes, uint32_t* window_bytes);
+
+pg_status pg_row_copy(const void* table, uint64_t table_bytes, uint32_t row_bytes, const uint32_t* rows, int64_t n,
+                      void* out, uint32_t out_row_bytes, pg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -196,6 +196,22 @@ def test_collision_counts_host_checks(pg):
     assert L.pg_collision_counts(None, 10, 8, 8, 0, 100, ctypes.c_void_p(8), None, 0, None) == 1
 
 
+def test_row_copy_window_and_host_checks(pg):
+    # the window: the 16-byte chunks that hold a row wherever a row of that size can start
+    for rb, wb in ((128, 128), (160, 160), (16, 16), (34, 48), (2, 16), (3, 32), (24, 32), (4096, 4096)):
+        assert pg.row_copy_window(rb) == wb, rb
+    L = pg.lib()
+    w = ctypes.c_uint32()
+    assert L.pg_row_copy_window(0, ctypes.byref(w)) == 2 and L.pg_row_copy_window(4097, ctypes.byref(w)) == 2
+    assert L.pg_row_copy(None, 0, 128, None, 0, None, 0, None) == 0                 # n = 0: nothing to do
+    assert L.pg_row_copy(None, 1 << 20, 128, None, 10, None, 0, None) == 1           # PG_ERR_NULL
+    assert L.pg_row_copy(None, 1 << 20, 128, None, -1, None, 0, None) == 2           # PG_ERR_SHAPE
+    assert L.pg_row_copy(None, 1 << 20, 128, None, 1 << 28, None, 0, None) == 2      # n * 8 chunks >= 2^31
+    assert L.pg_row_copy(None, 1 << 20, 34, None, 10, None, 32, None) == 2           # output row < window (48)
+    assert L.pg_row_copy(None, 1 << 20, 34, None, 10, None, 136, None) == 2          # not a multiple of 16
+    assert L.pg_row_copy(None, 1 << 20, 34, None, 10, None, 128, None) == 1          # valid sizes, NULL pointers
+
+
 def test_a_c_program_uses_the_library_through_the_header(pg, tmp_path):
     # the boundary is plain C: a C99 program that includes pg.h and links libpg.so runs the
     # host-side calls (no GPU needed for these)

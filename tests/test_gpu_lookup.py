@@ -237,3 +237,34 @@ def test_nf4_levels_on_the_gpu_match_the_oracle(cuda):
     want = np.where(bits == 1, -1.0, 1.0).astype(np.float32) * lv[np.arange(64) % 16]
     assert np.array_equal(np.abs(e.cpu().numpy()[0]), np.abs(want))
     assert np.array_equal(e.cpu().numpy()[0].view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("row_bytes,out_row", [(128, 0), (160, 0), (34, 0), (34, 128), (256, 0), (16, 0), (16, 48)])
+def test_row_copy_moves_each_rows_window(cuda, row_bytes, out_row):
+    # The diagnostic row copy: output row i = the aligned 16-byte window holding row
+    # rows[i], zero-padded to the output row; chunks past the table's end (a row index
+    # beyond it, or the table's ragged tail) are zeros. Checked byte for byte on the host.
+    pg = _pg()
+    g = torch.Generator().manual_seed(row_bytes + out_row)
+    R, n = 1001, 3000
+    table = torch.randint(0, 256, (R * row_bytes + 5,), dtype=torch.uint8, generator=g)
+    rows = torch.randint(0, R, (n,), dtype=torch.int32, generator=g)
+    rows[7] = R + 50
+    rows[8] = R - 1
+    wb = pg.row_copy_window(row_bytes)
+    ob = out_row or wb
+    out = torch.full((n, ob), 7, dtype=torch.uint8, device=cuda)
+    pg.row_copy(table.to(cuda), row_bytes, rows.to(cuda), out, out_row)
+    tb = table.numpy()
+    want = np.zeros((n, ob), np.uint8)
+    for i, r in enumerate(rows.numpy().astype(np.int64)):
+        start = (r * row_bytes) & ~15
+        for c in range(wb // 16):
+            a = start + 16 * c
+            if a + 16 <= tb.size:
+                want[i, 16 * c:16 * c + 16] = tb[a:a + 16]
+    assert np.array_equal(out.cpu().numpy(), want)
+    for i, r in enumerate(rows.numpy()[:64].astype(np.int64)):  # the window holds the row
+        s = r * row_bytes
+        if s + row_bytes <= (tb.size // 16) * 16:
+            assert np.array_equal(want[i, s % 16:s % 16 + row_bytes], tb[s:s + row_bytes])
