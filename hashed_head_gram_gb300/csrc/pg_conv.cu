@@ -19,7 +19,7 @@
 //      window of rows that rotates by one row per step, held in registers under a 4-way
 //      unrolled walk), c = sum_j f_{t-j dil} (w[:, j] gamma) v_{t-j dil},
 //      H[m, t] += SiLU(c) + alpha_t v_t for all M branches, in packed fp32x2 arithmetic,
-//      with H of the next positions prefetched into shared memory by cp.async.
+//      with H and v of the next positions prefetched into shared memory by cp.async.
 // DRAM traffic per token: v once (2d bytes; the taps re-read it from L1/L2) and H read +
 // written once per branch (2 * M * 2d bytes).
 #include <cuda_bf16.h>
@@ -166,7 +166,7 @@ __device__ __forceinline__ float row_mean_square(const T* __restrict__ row, int 
 constexpr int kCpt = 4;             // channels per thread
 constexpr int kMaxThreads = 768;    // so a slice holds at most 3072 channels
 constexpr int kSliceThreads = 128;  // slice width when mean(v^2) is given
-constexpr int kPrefetch = 2;        // positions of H in flight per thread
+constexpr int kPrefetch = 2;        // positions of H and v in flight per thread
 
 // PF: positions of H prefetched ahead of the one being computed (per thread, cp.async).
 // The grid is a multiple of `slices`; block b works on channel slice b mod slices.
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
   // per (branch, run position t): {f_t, f_t, f_{t-dil}, f_{t-dil}}, {f_{t-2dil} x2, f_{t-3dil} x2},
   // {alpha_t, alpha_t, -, -}; f is 0 before the start of the sequence and past the kernel size
   __shared__ __align__(16) float s_tap[MMAX][kRun][12];
-  // H prefetch ring: [PF][M][threads] chunks of CPT channels
+  // operand ring: [PF][MMAX + 1][threads] chunks of CPT channels (H of each branch, then v)
   extern __shared__ __align__(16) uint8_t s_ring[];
   using Vec = VecN<T, CPT>;
   using Raw = typename Vec::Raw;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
   Raw* ring = reinterpret_cast<Raw*>(s_ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  auto ring_at = [&](int slot, int m) -> Raw* { return ring + (slot * MMAX + m) * blockDim.x + threadIdx.x; };
+  auto ring_at = [&](int slot, int m) -> Raw* { return ring + (slot * (MMAX + 1) + m) * blockDim.x + threadIdx.x; };
 
   const int c0 = (blockIdx.x % slices) * blockDim.x * CPT + threadIdx.x * CPT;
   const bool active = c0 < d;
@@ -252,9 +252,9 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
     // 3. conv + SiLU + residual. Positions are walked by residue class mod dil, so the taps
     //    of t (t, t - dil, t - 2 dil, t - 3 dil) are the last four rows of the class: at the
     //    k-th step the row t - j dil sits in window slot (k - j) mod 4, and the walk is
-    //    unrolled by 4 so every slot index is a constant. H of the next PF positions in
-    //    walking order is already on its way into this thread's ring slots (one cp.async
-    //    group per position).
+    //    unrolled by 4 so every slot index is a constant. H and v of the next PF positions in
+    //    walking order are already on their way into this thread's ring slots (one cp.async
+    //    group per position); v_t enters the window from the ring at its step.
     int pr = 0, pi = 0, ps = 0;  // prefetch cursor: position t0 + pr + dil * pi, sequence ps
     auto prefetch_next = [&]() {
       if (pr < dil && t0 + pr < t1) {
@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
             if (m >= M) continue;
             cp_async_bytes<static_cast<int>(sizeof(Raw))>(ring_at(slot, m), src + m * branch_stride);
           }
+          cp_async_bytes<static_cast<int>(sizeof(Raw))>(ring_at(slot, MMAX), v + (seq0 + t) * d + c0);
         }
         ++pi;
         if (t0 + pr + dil * pi >= t1) {
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
     for (int r = 0; r < dil && t0 + r < t1; ++r) {
       uint64_t win[kTaps][kPairs];  // v rows of this residue class, zero before the sequence start
 #pragma unroll
-      for (int j = 0; j < kTaps; ++j) {
+      for (int j = 1; j < kTaps; ++j) {  // v_t itself comes from the ring at its step
         const int p = t0 + r - j * dil;
         float x[CPT];
         if (active && j < ks && p >= 0) {
@@ -299,12 +300,15 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
       while (t < t1) {
 #pragma unroll
         for (int k = 0; k < kTaps; ++k) {
-          const bool has_next = active && t + dil < t1;
-          Raw nxt = Vec::zero();
-          if (has_next) nxt = Vec::load(v + (seq0 + t + dil) * d + c0);  // next row of the class, early
           cp_async_wait<PF - 1>();  // this thread's copies for position t have landed
           if (active) {
             const Raw* hr = ring_at(s % PF, 0);
+            {  // v_t into the window slot of v_{t - 4 dil}
+              float x[CPT];
+              Vec::unpack(hr[MMAX * blockDim.x], x);
+#pragma unroll
+              for (int q = 0; q < kPairs; ++q) win[k][q] = pk(x[2 * q], x[2 * q + 1]);
+            }
             T* out = H + (seq0 + t) * d + c0;
             uint64_t prod[kTaps][kPairs];  // (w[:, j] gamma / 2) * v_{t - j dil}
 #pragma unroll
@@ -332,11 +336,6 @@ __global__ void __launch_bounds__(kMaxThreads) conv_residual_kernel(
             }
           }
           prefetch_next();
-          // the slot of v_{t - 3 dil} takes v_{t + dil}
-          float x[CPT];
-          Vec::unpack(nxt, x);
-#pragma unroll
-          for (int q = 0; q < kPairs; ++q) win[(k + 1) % kTaps][q] = pk(x[2 * q], x[2 * q + 1]);
           t += dil;
           ++s;
           if (t >= t1) break;
@@ -607,7 +606,7 @@ pg_status launch(int B, int L, int d, int M, const void* v, const float* alpha, 
   if (total >= (1ll << 31)) return PG_ERR_SHAPE;
   const int64_t N = static_cast<int64_t>(B) * L;
   auto run = [&](auto kern, int mmax, int pf) -> pg_status {
-    const size_t ring = static_cast<size_t>(pf) * mmax * threads * (sizeof(T) * kCpt);
+    const size_t ring = static_cast<size_t>(pf) * (mmax + 1) * threads * (sizeof(T) * kCpt);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ring));
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
