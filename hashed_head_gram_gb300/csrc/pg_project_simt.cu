@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_f32_kernel(const float
   const int m0 = blockIdx.y * kSimtTile, n0 = blockIdx.x * kSimtTile;
   // global -> register staging: thread loads 8 consecutive k of one A row and of one B row
   const int lr = tid >> 1, lk = (tid & 1) * 16;
-  const bool vec = (Din & 3) == 0;
+  const bool vec = (Din & 3) == 0 && reinterpret_cast<uintptr_t>(A) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(Bw) % 16 == 0;  // 16-byte loads of whole rows
   float ra[16], rb[16];
   auto load_tile = [&](int k0) {
     const int ar = m0 + lr, br = n0 + lr;
@@ -155,6 +156,147 @@ __global__ void __launch_bounds__(kSimtThreads) simt_gemm_f32_kernel(const float
     simt_cluster_sync();
     constexpr int kRows = kSimtTile / KS;  // rows this CTA adds and stores
     for (int q = threadIdx.x; q < kRows * (kSimtTile / 4); q += kSimtThreads) {
+      const int rr = kz * kRows + q / (kSimtTile / 4), c4 = (q % (kSimtTile / 4)) * 4;
+      float4 sum = ld_dsmem_f4(part + rr * kSimtTile + c4, 0);
+#pragma unroll
+      for (int z = 1; z < KS; ++z) {
+        const float4 p4 = ld_dsmem_f4(part + rr * kSimtTile + c4, z);
+        sum.x += p4.x;
+        sum.y += p4.y;
+        sum.z += p4.z;
+        sum.w += p4.w;
+      }
+      const int r = m0 + rr;
+      if (r < N) {
+        const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = n0 + c4 + j;
+          if (c < Dout) {
+            const size_t off = static_cast<size_t>(r) * Dout + c;
+            out[off] = GATE == PG_GATE_SCALAR ? fmaf(g, sv[j], x[off]) : sv[j];
+          }
+        }
+      }
+    }
+    simt_cluster_sync();  // no CTA leaves while another reads its partial tile
+  }
+}
+
+// The same product for 16-byte-aligned operands with Din % 4 == 0: 64 threads per 64 x 64
+// tile, thread (ty, tx) = (tid / 8, tid % 8) owning rows ty*8 .. ty*8+7 and columns
+// tx*8 .. tx*8+7 (8 x 8 fp32 accumulators). The A and B tiles, [64 rows][32 k] each, arrive
+// through a kF32Stages-deep cp.async ring (no registers held in flight; rows and k past the
+// matrix read as zeros); a 16-byte chunk c of row r sits at chunk c ^ ((r / 8) mod 8), so
+// the 8 rows a warp reads at one chunk lie in 8 different bank groups. Per 4-deep k chunk a
+// thread reads its 8 A rows and 8 B rows (16 vector loads) for 256 FMAs, each accumulator
+// summed over k in increasing order. KS > 1: as above, CTA z of the cluster takes k-tiles
+// z, z + KS, ... and CTA r adds rows 64 r / KS .. of the KS partial tiles in rank order.
+constexpr int kF32Threads = 64;
+constexpr int kF32Stages = 3;
+
+__device__ __forceinline__ void f32_cp_async16(float* smem, const float* gmem, bool fill) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(
+                   __cvta_generic_to_shared(smem))),
+               "l"(gmem), "r"(fill ? 16 : 0)
+               : "memory");
+}
+
+template <int GATE, int KS>
+__global__ void __launch_bounds__(kF32Threads) simt_gemm_f32_tiled_kernel(const float* __restrict__ A,
+                                                                          const float* __restrict__ Bw, int N,
+                                                                          int Din, int Dout,
+                                                                          const float* __restrict__ x, float g,
+                                                                          float* __restrict__ out) {
+  __shared__ __align__(16) float As[kF32Stages][kSimtTile][kSimtK];
+  __shared__ __align__(16) float Bs[kF32Stages][kSimtTile][kSimtK];
+  const int tid = threadIdx.x;
+  const int ty = tid >> 3, tx = tid & 7;
+  const int m0 = blockIdx.y * kSimtTile, n0 = blockIdx.x * kSimtTile;
+  const int kz = KS > 1 ? static_cast<int>(simt_cluster_rank()) : 0;
+  const int ntiles = (Din + kSimtK - 1) / kSimtK;
+  const int my_tiles = ntiles > kz ? (ntiles - kz + KS - 1) / KS : 0;  // k-tiles kz, kz + KS, ...
+
+  // k-tile `kt` (global index) into stage `st`: 64 rows x 8 chunks of A and of B, 8 + 8
+  // chunks per thread (row tid / 8 + 8 q, chunk tid % 8)
+  auto load = [&](int kt, int st) {
+    const int k0 = kt * kSimtK;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int r = ty + 8 * q, c = tx, k = k0 + 4 * c;
+      const int pc = c ^ (r >> 3 & 7);
+      const bool ka = k < Din;  // Din % 4 == 0: a chunk is wholly inside K or outside it
+      const bool va = ka && m0 + r < N, vb = ka && n0 + r < Dout;
+      f32_cp_async16(&As[st][r][4 * pc], va ? A + static_cast<size_t>(m0 + r) * Din + k : A, va);
+      f32_cp_async16(&Bs[st][r][4 * pc], vb ? Bw + static_cast<size_t>(n0 + r) * Din + k : Bw, vb);
+    }
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < kF32Stages - 1; ++s) {
+    if (s < my_tiles) load(kz + s * KS, s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int t = 0; t < my_tiles; ++t) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kF32Stages - 2) : "memory");
+    __syncthreads();  // stage t landed for every thread; stage t - 1 is no longer read
+    if (t + kF32Stages - 1 < my_tiles) load(kz + (t + kF32Stages - 1) * KS, (t + kF32Stages - 1) % kF32Stages);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const int st = t % kF32Stages;
+#pragma unroll
+    for (int c = 0; c < kSimtK / 4; ++c) {
+      float4 a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4*>(&As[st][ty * 8 + i][4 * (c ^ ty)]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 b = *reinterpret_cast<const float4*>(&Bs[st][tx * 8 + j][4 * (c ^ tx)]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[i][j] = fmaf(a[i].x, b.x, acc[i][j]);
+          acc[i][j] = fmaf(a[i].y, b.y, acc[i][j]);
+          acc[i][j] = fmaf(a[i].z, b.z, acc[i][j]);
+          acc[i][j] = fmaf(a[i].w, b.w, acc[i][j]);
+        }
+      }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+  if constexpr (KS == 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = m0 + ty * 8 + i;
+      if (r >= N) continue;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = n0 + tx * 8 + j;
+        if (c < Dout) {
+          const size_t off = static_cast<size_t>(r) * Dout + c;
+          out[off] = GATE == PG_GATE_SCALAR ? fmaf(g, acc[i][j], x[off]) : acc[i][j];
+        }
+      }
+    }
+  } else {
+    // the partial tile [64][64] in this CTA's shared memory (the A ring is free)
+    float* part = &As[0][0][0];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      *reinterpret_cast<float4*>(part + (ty * 8 + i) * kSimtTile + tx * 8) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(part + (ty * 8 + i) * kSimtTile + tx * 8 + 4) =
+          make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+    simt_cluster_sync();
+    constexpr int kRows = kSimtTile / KS;  // rows this CTA adds and stores
+    for (int q = threadIdx.x; q < kRows * (kSimtTile / 4); q += kF32Threads) {
       const int rr = kz * kRows + q / (kSimtTile / 4), c4 = (q % (kSimtTile / 4)) * 4;
       float4 sum = ld_dsmem_f4(part + rr * kSimtTile + c4, 0);
 #pragma unroll
@@ -419,6 +561,11 @@ pg_status launch_small_rows_bf16(int N, int Din, int d, int M, int gate_kind, co
 
 namespace {
 
+// The 8 x 8 kernel reads 16-byte chunks of rows: Din % 4 == 0 and 16-byte aligned operands.
+inline bool f32_tiled_ok(int Din, const float* e, const float* W) {
+  return Din % 4 == 0 && reinterpret_cast<uintptr_t>(e) % 16 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0;
+}
+
 template <int GATE, int KS>
 pg_status launch_simt_ks(int N, int Din, int d, const float* e, const float* W, float g, const float* x, float* out,
                          cudaStream_t stream) {
@@ -433,7 +580,11 @@ pg_status launch_simt_ks(int N, int Din, int d, const float* e, const float* W, 
   attr[0].val.clusterDim.z = KS;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, simt_gemm_f32_kernel<GATE, KS>, e, W, N, Din, d, x, g, out);
+  const bool tiled = f32_tiled_ok(Din, e, W);
+  if (tiled) cfg.blockDim = dim3(kF32Threads);
+  const cudaError_t err =
+      tiled ? cudaLaunchKernelEx(&cfg, simt_gemm_f32_tiled_kernel<GATE, KS>, e, W, N, Din, d, x, g, out)
+            : cudaLaunchKernelEx(&cfg, simt_gemm_f32_kernel<GATE, KS>, e, W, N, Din, d, x, g, out);
   if (err != cudaSuccess) return cuda_fail(err);
   return after_launch(1);
 }
@@ -445,17 +596,32 @@ pg_status launch_simt_f32(int N, int Din, int d, int gate_kind, const float* e, 
   // split K over a cluster of 4 (or 2) CTAs per tile when the tiles alone leave SMs idle
   const int64_t tiles = static_cast<int64_t>((d + kSimtTile - 1) / kSimtTile) * ((N + kSimtTile - 1) / kSimtTile);
   const int64_t fill = 4ll * sm_count();
-  if (Din >= 4 * 2 * kSimtK && tiles * 2 < fill)
+  if (f32_tiled_ok(Din, e, W)) {
+    // 4 blocks per SM (registers): the largest split whose CTAs run in one wave (workload
+    // 4096 x 1024 x 256: 2 -> 61 us, 4 -> 64 us)
+    if (Din >= 4 * 2 * kSimtK && tiles * 4 <= fill)
+      return gate_kind == PG_GATE_SCALAR ? launch_simt_ks<PG_GATE_SCALAR, 4>(N, Din, d, e, W, g, x, out, stream)
+                                         : launch_simt_ks<PG_GATE_NONE, 4>(N, Din, d, e, W, g, x, out, stream);
+    if (Din >= 2 * 2 * kSimtK && tiles * 2 <= fill)
+      return gate_kind == PG_GATE_SCALAR ? launch_simt_ks<PG_GATE_SCALAR, 2>(N, Din, d, e, W, g, x, out, stream)
+                                         : launch_simt_ks<PG_GATE_NONE, 2>(N, Din, d, e, W, g, x, out, stream);
+  } else if (Din >= 4 * 2 * kSimtK && tiles * 2 < fill)
     return gate_kind == PG_GATE_SCALAR ? launch_simt_ks<PG_GATE_SCALAR, 4>(N, Din, d, e, W, g, x, out, stream)
                                        : launch_simt_ks<PG_GATE_NONE, 4>(N, Din, d, e, W, g, x, out, stream);
-  if (Din >= 2 * 2 * kSimtK && tiles < fill)
+  else if (Din >= 2 * 2 * kSimtK && tiles < fill)
     return gate_kind == PG_GATE_SCALAR ? launch_simt_ks<PG_GATE_SCALAR, 2>(N, Din, d, e, W, g, x, out, stream)
                                        : launch_simt_ks<PG_GATE_NONE, 2>(N, Din, d, e, W, g, x, out, stream);
   dim3 grid((d + kSimtTile - 1) / kSimtTile, (N + kSimtTile - 1) / kSimtTile);
-  if (gate_kind == PG_GATE_SCALAR)
+  if (f32_tiled_ok(Din, e, W)) {
+    if (gate_kind == PG_GATE_SCALAR)
+      simt_gemm_f32_tiled_kernel<PG_GATE_SCALAR, 1><<<grid, kF32Threads, 0, stream>>>(e, W, N, Din, d, x, g, out);
+    else
+      simt_gemm_f32_tiled_kernel<PG_GATE_NONE, 1><<<grid, kF32Threads, 0, stream>>>(e, W, N, Din, d, x, g, out);
+  } else if (gate_kind == PG_GATE_SCALAR) {
     simt_gemm_f32_kernel<PG_GATE_SCALAR, 1><<<grid, kSimtThreads, 0, stream>>>(e, W, N, Din, d, x, g, out);
-  else
+  } else {
     simt_gemm_f32_kernel<PG_GATE_NONE, 1><<<grid, kSimtThreads, 0, stream>>>(e, W, N, Din, d, x, g, out);
+  }
   return after_launch(1);
 }
 

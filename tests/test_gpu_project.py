@@ -40,6 +40,27 @@ def test_simt_fp32_projection_config1(cuda):
     assert rel_l2(to_f64(out), dense.scalar_gate(x.double().numpy(), ref, 0.5)) <= F32_TOL
 
 
+# fp32 SIMT shapes: split K over clusters of 4 and 2 CTAs and none, K not a multiple of the
+# 32-deep k-tile, ragged rows and columns; Din % 4 != 0 and a W offset by 4 bytes take the
+# kernel with 4-byte loads.
+@pytest.mark.parametrize("N,Din,d,shift", [(1000, 1280, 256, 0), (77, 192, 384, 0), (65, 100, 72, 0),
+                                           (640, 64, 64, 0), (33, 99, 40, 0), (300, 512, 128, 1)])
+def test_simt_fp32_projection_shapes(cuda, N, Din, d, shift):
+    pg = _pg()
+    e = torch.randint(-128, 128, (N, Din), generator=_gen(6)).float() / 64
+    Wv = torch.randn(d, Din, generator=_gen(7)) * 0.02
+    x = torch.randn(N, d, generator=_gen(8))
+    ref = dense.project(e.double().numpy(), Wv.double().numpy())
+    buf = torch.empty(d * Din + shift, device=cuda)
+    wd = buf[shift:].view(d, Din)
+    wd.copy_(Wv.to(cuda))
+    for gate in (pg.GATE_NONE, pg.GATE_SCALAR):
+        out = torch.empty(N, d, device=cuda)
+        pg.project_gate(e.to(cuda), wd, d, gate, out, pg.F32, g=0.5, x_resid=x.to(cuda))
+        want = ref if gate == pg.GATE_NONE else dense.scalar_gate(x.double().numpy(), ref, 0.5)
+        assert rel_l2(to_f64(out), want) <= F32_TOL, gate
+
+
 # d % 256 == 0 runs 256 x 256 tiles on CTA pairs: N = 429 and 1000 end in a ragged second
 # half, N = 640 in a pair whose second CTA has no rows at all; d = 128 / 384 run single CTAs.
 @pytest.mark.parametrize("N,Din,d", [(429, 1024, 768), (128, 64, 128), (1000, 1280, 256), (77, 192, 384),
