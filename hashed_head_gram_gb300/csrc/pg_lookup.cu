@@ -10,7 +10,10 @@
 //            bytes [16c, 16c+16) of its concatenated e_t, so 32 consecutive chunks are 512
 //            contiguous bytes of e_t and 4 whole 128-byte rows of one page (PageGram: all K
 //            rows of an order lie in one K*S-row page block, PageGram report section 3.1);
-//   phase A of the warp's next batch runs while phase B's loads are in flight.
+//   phase A of the warp's next batch runs while phase B's loads are in flight. A batch's
+//   token IDs are read ahead of it by a few lanes (raw IDs two batches ahead, canonical IDs
+//   one ahead) and handed to the hashing lanes by shuffles, so phase A issues no loads
+//   (batches of one token keep per-lane ID reads).
 //   NF4 rows (34 bytes) take their own kernel: windows copied into shared memory by
 //   cp.async three batches ahead, dequantised from there (see gather_nf4_kernel).
 // Sources: PageGram report sections 2.1, 2.2, 3.1, 3.3; Engram notes (arXiv 2601.07372)
