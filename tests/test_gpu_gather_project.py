@@ -59,8 +59,9 @@ def _case(cfg, ti, B, L):
     return w, spec
 
 
+# (8, 128) and (9, 256): token counts that are whole multiples of the ready-counter unit
 @pytest.mark.parametrize("cfg,ti,B,L", [(2, 0, 3, 143), (3, 0, 2, 200), (2, 0, 1, 64), (5, 0, 2, 150),
-                                        (2, 0, 1, 5)])
+                                        (2, 0, 1, 5), (2, 0, 8, 128), (3, 0, 9, 256)])
 def test_scalar_and_none_gates_match_two_calls(cuda, cfg, ti, B, L):
     pg = _pg()
     w, spec = _case(cfg, ti, B, L)
@@ -162,6 +163,22 @@ def test_reports_out_of_range_tokens(cuda):
               None, torch.zeros(d, spec.e_width, dtype=torch.bfloat16, device=cuda), d, pg.GATE_NONE, {}, err=err)
     torch.cuda.synchronize()
     assert err.item() == 140
+
+
+@pytest.mark.parametrize("bad", [[(7, 5)], [(1, 100), (7, 5)], [(6, 0)]])
+def test_reports_the_smallest_out_of_range_position(cuda, bad):
+    # bad IDs in the last sequences of a batch of 8: the smallest flat position is reported
+    pg = _pg()
+    w, spec = _case(2, 0, 8, 128)
+    tokens = W.make_tokens(w).copy()
+    for b, t in bad:
+        tokens[b, t] = w.vocab + 1 + t
+    d = 256
+    err = torch.empty(1, dtype=torch.int32, device=cuda)
+    _one_call(pg, pg.table_desc(spec, w.vocab), spec, torch.from_numpy(tokens).to(cuda), W.make_table(w, spec, cuda),
+              None, torch.zeros(d, spec.e_width, dtype=torch.bfloat16, device=cuda), d, pg.GATE_NONE, {}, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == min(b * 128 + t for b, t in bad)
 
 
 def test_full_pagegram_200M_workload(cuda):
