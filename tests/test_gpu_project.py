@@ -186,6 +186,38 @@ def test_conv_residual(cuda, B, L, d, M, dtype, given_ms):
     assert rel_l2(upd, ref - H.double().numpy().reshape(M, B, L, d)) <= (5e-2 if dtype == torch.bfloat16 else F32_TOL)
 
 
+# sequences of several 32-position runs with a ragged tail, every kernel size and a spread of
+# dilations: the causal window crosses run boundaries (up to 3 * 8 = 24 positions back),
+# M = 8 and M = 3 take the runtime-branch-count kernel
+@pytest.mark.parametrize("ks,dil,B,L,d,M,dtype", [
+    (4, 8, 2, 100, 512, 2, torch.bfloat16),
+    (4, 8, 1, 70, 256, 8, torch.float32),
+    (1, 1, 2, 65, 512, 4, torch.bfloat16),
+    (2, 1, 1, 97, 2560, 4, torch.bfloat16),
+    (3, 2, 3, 33, 128, 3, torch.bfloat16),
+    (2, 5, 2, 64, 768, 1, torch.float32),
+    (3, 7, 1, 150, 1024, 4, torch.bfloat16),
+])
+@pytest.mark.parametrize("given_ms", [False, True])
+def test_conv_residual_kernel_sizes_and_dilations(cuda, ks, dil, B, L, d, M, dtype, given_ms):
+    pg = _pg()
+    v, alpha, gc, w, H = _conv_case(B, L, d, M, 40 + ks * 10 + dil, dtype=dtype)
+    w = w[:, :ks].contiguous()
+    Hd = H.to(cuda)
+    v_ms = (v.double() ** 2).mean(dim=1).float().to(cuda) if given_ms else None
+    pg.conv_residual(B, L, d, M, pg.dtype_code(dtype), v.to(cuda), alpha.to(cuda), gc.to(cuda), w.to(cuda), Hd,
+                     dilation=dil, eps=1e-6, v_ms=v_ms)
+    ref = dense.conv_residual(v.double().numpy().reshape(B, L, d), alpha.double().numpy().reshape(M, B, L),
+                              gc.double().numpy(), w.double().numpy(), dil, 1e-6,
+                              H.double().numpy().reshape(M, B, L, d))
+    assert rel_l2(to_f64(Hd).reshape(M, B, L, d), ref) <= (BF16_TOL if dtype == torch.bfloat16 else F32_TOL)
+    # the first positions of every sequence see only the taps that reach back into it
+    upd = to_f64(Hd).reshape(M, B, L, d) - H.double().numpy().reshape(M, B, L, d)
+    ref_upd = ref - H.double().numpy().reshape(M, B, L, d)
+    head = min(L, (ks - 1) * dil + 1)
+    assert rel_l2(upd[:, :, :head], ref_upd[:, :, :head]) <= (5e-2 if dtype == torch.bfloat16 else F32_TOL)
+
+
 def test_zero_table_leaves_H_bit_identical(cuda):
     # e = 0 -> v = 0, alpha = 1/2 exactly, Y = 0: H is unchanged bit for bit
     # (PageGram report appendix D/E check 3).

@@ -467,20 +467,24 @@ def test_projection_and_gate_against_torch():
     assert np.allclose(dense.scalar_gate(x.numpy(), v, 0.5), (x + 0.5 * vk[:, :d]).numpy())
 
 
-def test_conv_residual_against_torch_conv1d():
+# kernel 4, dilation 3 is the Engram notes' conv; the others cover one tap, dilation 1 and
+# windows that reach past the start of the 23-position sequences (3 * 8 = 24 back)
+@pytest.mark.parametrize("ks,dil", [(4, 3), (1, 1), (2, 1), (3, 2), (2, 5), (4, 8), (3, 7)])
+def test_conv_residual_against_torch_conv1d(ks, dil):
     c = _dense_case()
     B, L, d, M, eps = c["B"], c["L"], c["d"], c["M"], 1e-6
     v = torch.randn(B, L, d, dtype=torch.float64)
     alpha = torch.rand(M, B, L, dtype=torch.float64)
-    got = dense.conv_residual(v.numpy(), alpha.numpy(), c["gc"].numpy(), c["w"].numpy(), 3, eps,
-                              c["H"].numpy())
+    w = c["w"][:, :ks]
+    got = dense.conv_residual(v.numpy(), alpha.numpy(), c["gc"].numpy(), w.numpy(), dil, eps, c["H"].numpy())
+    pad = (ks - 1) * dil
     for m in range(M):
         u = alpha[m][..., None] * v
         z = F.rms_norm(u, (d,), c["gc"], eps)
-        # torch conv1d is a cross-correlation: tap i of the padded input reads
-        # position t - 3*(3 - i), so our tap j = 3 - i.
-        wt = c["w"].flip(1)[:, None, :]
-        conv = F.conv1d(F.pad(z.transpose(1, 2), (9, 0)), wt, groups=d, dilation=3).transpose(1, 2)
+        # torch conv1d is a cross-correlation: tap i of the left-padded input reads
+        # position t - dil * (ks - 1 - i), so our tap j = ks - 1 - i.
+        wt = w.flip(1)[:, None, :]
+        conv = F.conv1d(F.pad(z.transpose(1, 2), (pad, 0)), wt, groups=d, dilation=dil).transpose(1, 2)
         ref = c["H"][m] + F.silu(conv) + u
         assert np.allclose(got[m], ref.numpy(), rtol=1e-12, atol=1e-12)
 
