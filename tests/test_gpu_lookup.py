@@ -186,6 +186,9 @@ OTHER_LAYOUTS = [
     dict(mode=W.MODE_FLAT, K=1, S=1, r=512, dt=W.DT_BF16, orders=[2, 3, 4], rows=[[211], [199], [197]]),
     dict(mode=W.MODE_FLAT, K=1, S=1, r=128, dt=W.DT_F32, orders=[3], rows=[[101]]),
     dict(mode=W.MODE_ENGRAM, K=2, S=1, r=1024, dt=W.DT_BF16, orders=[2, 3], rows=None),
+    # degenerate addressing: one page per order (every n-gram in page 0), one row per order
+    dict(mode=W.MODE_PAGEGRAM, K=8, S=4, r=64, dt=W.DT_BF16, orders=[2, 3], pages=[1, 1]),
+    dict(mode=W.MODE_FLAT, K=1, S=1, r=64, dt=W.DT_BF16, orders=[2, 3], rows=[[1], [1]]),
 ]
 
 
