@@ -381,10 +381,12 @@ pg_status pg_lookup_project_gate(const pg_table_desc* desc, const int32_t* token
  * pg_project_gate(e_out, W, ...), with the lookup of the Engram notes section 3.2 /
  * PageGram report section 3.1 running on extra warps of the projection's persistent CTA
  * pairs (Engram notes section 3.4), so that its random row reads overlap the tensor-core
- * work instead of preceding it. The gather warps claim 8-token chunks of e_t in the order
- * the projection's tiles consume them and publish each 128-token block on a ready counter
- * in the workspace; a tile's first load of its rows waits for that count (bounded: a wait
- * that runs out sets the device error word and the call's results are undefined).
+ * work instead of preceding it. A coordinator warp per CTA claims units of e_t (the most
+ * tokens, a power of two, whose rows number at most 512: 32 tokens at 16 rows per token) in
+ * the order the projection's tiles consume them and hands them to the gather warps; each
+ * finished unit is counted on its 128-token block's ready counter in the workspace, and a
+ * tile's first load of its rows waits for that count (bounded: a wait that runs out sets
+ * the device error word and the call's results are undefined).
  *  Tables: PG_ENGRAM or PG_PAGEGRAM mode, PG_BF16 rows, r = 64, O*K <= 32 (Din = O*K*64).
  *  desc .. table_bytes, err_index   as in pg_gather_sign_concat
  *  e_out  device [B*L, Din] bf16, 16-byte aligned: e_t, written (the projection's A operand)
