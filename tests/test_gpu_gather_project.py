@@ -91,6 +91,42 @@ def test_scalar_and_none_gates_match_two_calls(cuda, cfg, ti, B, L):
     assert rel_l2(to_f64(v1), ref) <= BF16_TOL
 
 
+# heads per token other than the workloads' 16 (units of 32 tokens x 16 rows): 2 heads give
+# units of 128 tokens (256 rows), 12 and 24 units of 32 and 16 tokens (384 rows: the last
+# gather warps of a unit have no rows), 32 units of 16 tokens (Din = 2048, the call's largest)
+@pytest.mark.parametrize("mode,K,orders", [(W.MODE_PAGEGRAM, 1, [2, 3]), (W.MODE_PAGEGRAM, 4, [2, 3, 4]),
+                                           (W.MODE_ENGRAM, 8, [1, 2, 3]), (W.MODE_PAGEGRAM, 16, [2, 3])])
+def test_head_counts_other_than_sixteen(cuda, mode, K, orders):
+    pg = _pg()
+    w = W.shrink(W.make_workload(2), B=2, L=333)
+    base = w.tables[0]
+    if mode == W.MODE_PAGEGRAM:
+        spec = dataclasses.replace(base, K=K, S=4, orders=list(orders), pages=[97, 89, 83][:len(orders)], rows=[])
+    else:
+        pr = W.largest_primes(1999, len(orders) * K)
+        spec = dataclasses.replace(base, mode=W.MODE_ENGRAM, K=K, S=1, orders=list(orders), pages=[],
+                                   rows=[pr[i * K:(i + 1) * K] for i in range(len(orders))])
+    d = 256
+    desc = pg.table_desc(spec, w.vocab)
+    tokens = W.make_tokens(w)
+    table = W.make_table(w, spec, "cpu")
+    g = torch.Generator().manual_seed(5)
+    Wv = (torch.randn(d, spec.e_width, generator=g) * 0.02).to(torch.bfloat16).to(cuda)
+    x = torch.randn(w.N, d, generator=g).to(torch.bfloat16)
+    tok, tab = torch.from_numpy(tokens).to(cuda), table.to(cuda)
+    dn = {"x": x.to(cuda)}
+    e2, v2, _, _ = _two_call(pg, desc, spec, tok, tab, None, Wv, d, pg.GATE_SCALAR, dn)
+    err = torch.empty(1, dtype=torch.int32, device=cuda)
+    e1, v1, _, _ = _one_call(pg, desc, spec, tok, tab, None, Wv, d, pg.GATE_SCALAR, dn, err=err)
+    torch.cuda.synchronize()
+    assert pg.device_error() == 0 and err.item() == -1
+    assert torch.equal(_bits(e1), _bits(e2)) and torch.equal(_bits(v1), _bits(v2))
+    ref_e = oracle_e(spec, tokens, None, w.vocab, table, orc.BF16)
+    assert torch.equal(_bits(e1).cpu(), torch.from_numpy(ref_e.view(np.int16)).reshape(e1.shape))
+    ref = dense.scalar_gate(x.double().numpy(), dense.project(orc.bf16_bits_to_f64(ref_e), to_f64(Wv)), 0.5)
+    assert rel_l2(to_f64(v1), ref) <= BF16_TOL
+
+
 @pytest.mark.parametrize("d,M", [(256, 2), (512, 1)])
 def test_context_gate_matches_two_calls(cuda, d, M):
     pg = _pg()
