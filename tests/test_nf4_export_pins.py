@@ -59,6 +59,21 @@ def test_rows_of_exact_levels_return_their_codes():
         assert (orc.nf4_dequantize(rows) == x).all()
 
 
+def test_exact_ties_between_two_levels_take_the_lower_code():
+    # Reading R15 breaks a tie between two equally near levels toward the lower code. Exact
+    # ties: with the row's absmax 1.0 the scale is fp16(1.0) = 1, and half of the level next
+    # to zero lies exactly half-way between it and the zero level (halving is exact in fp32)
+    lv = orc.nf4_levels()
+    assert lv[7] == 0.0
+    x = np.zeros((1, 64), np.float32)
+    x[0, 0] = 1.0
+    x[0, 1] = lv[8] / np.float32(2)      # between level 7 (zero) and level 8
+    x[0, 2] = lv[6] / np.float32(2)      # between level 6 and level 7 (zero)
+    rows = orc.nf4_quantize(x)
+    assert rows[0, 0] == 15 | (7 << 4)   # codes of elements 0 and 1
+    assert rows[0, 1] & 15 == 6          # element 2
+
+
 @pytest.mark.parametrize("dist", ["normal", "uniform", "heavy", "tiny", "huge", "sparse"])
 def test_error_within_the_quantisation_bound(dist):
     # |x - dequant(x)| <= s * g / 2 + |a - s| (+ fp32 rounding of x / s), with a = max |x|,

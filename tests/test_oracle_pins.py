@@ -292,6 +292,28 @@ def test_rows_depend_exactly_on_the_suffix_window():
     assert (r[0, 2, 1] == r[0, 5, 1]).all() and (r[0, 2, 1] == r[1, 3, 1]).all()
 
 
+def test_positions_before_the_start_are_padding_not_a_token():
+    # The first positions' n-grams reach back past the start of the sequence, and what
+    # stands there is padding: a symbol that is no token. So token x at t = 0 is hashed
+    # unlike x after any real token y, and [y, x] at t = 1 unlike [z, y, x] at t = 2 (every
+    # y, z of a small vocabulary). Sign words are bijective in the n-gram's 64-bit hash,
+    # so they differ exactly when the n-grams do.
+    sp = spec(W.MODE_ENGRAM, K=8, rows=[[101] * 8, [103] * 8])
+    V = 12
+    for x in range(V):
+        _, _, s0, _ = orc.index(sp, np.array([[x]], np.int32), None, V)
+        pairs = np.array([[y, x] for y in range(V)], np.int32)
+        _, _, s1, _ = orc.index(sp, pairs, None, V)
+        s1 = s1.reshape(V, 2, *s1.shape[1:])
+        for y in range(V):
+            assert not np.array_equal(s0[0, 0], s1[y, 1, 0]), (x, y)     # bigram (pad, x) vs (y, x)
+            triples = np.array([[z, y, x] for z in range(V)], np.int32)
+            _, _, s2, _ = orc.index(sp, triples, None, V)
+            s2 = s2.reshape(V, 3, *s2.shape[1:])
+            for z in range(V):
+                assert not np.array_equal(s1[y, 1, 1], s2[z, 2, 1]), (x, y, z)   # (pad, y, x) vs (z, y, x)
+
+
 def test_sequences_do_not_leak_into_each_other():
     sp = spec(W.MODE_PAGEGRAM)
     toks = np.random.default_rng(4).integers(0, 50, (3, 10)).astype(np.int32)
