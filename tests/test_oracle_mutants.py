@@ -67,6 +67,14 @@ C_MUTANTS = [
      "else v = bits_to_f32(((e + 120u) << 23) | (m << 20));",
      "else v = bits_to_f32(((e + 121u) << 23) | (m << 20));"),
     ("FP8 row scale from 240 instead of 448", "const float s = a / 448.0f;", "const float s = a / 240.0f;"),
+    ("the largest out-of-range position reported",
+     "if (bad < 0 || src < bad) bad = src;", "if (bad < 0 || src > bad) bad = src;"),
+    ("Engram head reduced modulo the previous head's subtable size",
+     "% d->rows[o][k];", "% d->rows[o][k > 0 ? k - 1 : 0];"),
+    ("fp16 subnormals scaled by 2^-23", "(float)m * bits_to_f32(0x33800000u)", "(float)m * bits_to_f32(0x34000000u)"),
+    ("NF4 export of a zero row with code 8", "code[i] = 7;", "code[i] = 8;"),
+    ("E4M3 saturating only past 480 (464 .. 480 round to the NaN pattern)",
+     "if (a > 0x43E80000u)", "if (a > 0x43F00000u)"),
 ]
 
 

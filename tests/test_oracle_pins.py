@@ -344,6 +344,11 @@ def test_out_of_range_ids_are_reported():
     toks = np.array([[1, 2, 3], [4, 70, 6]], np.int32)
     _, _, _, bad = orc.index(sp, toks, None, 50)
     assert bad == 4
+    # several: the smallest flat position is the one reported (IDs >= V and negative IDs)
+    toks = np.array([[1, 2, 3], [4, 70, 6], [50, 2, -1]], np.int32)
+    assert orc.index(sp, toks, None, 50)[3] == 4
+    toks[0, 2] = -7
+    assert orc.index(sp, toks, None, 50)[3] == 2
     with pytest.raises(ValueError):
         orc.lookup(sp, toks, None, 50, np.zeros((orc.total_rows(sp), 256), np.uint8), orc.F32)
 
