@@ -93,8 +93,39 @@ def _rmsnorm_sum(z, gamma, eps):
     return z / np.sqrt(np.sum(z * z, axis=-1, keepdims=True) + eps) * np.asarray(gamma, np.float64)
 
 
-def _dense_mutants():
+def _fetch_rows_shifted(table_bytes, rows):
+    flat = rows.reshape(-1)
+    out = np.zeros((flat.size, table_bytes.shape[1]), np.uint8)
+    ok = flat != orc.NO_ROW
+    out[ok] = table_bytes[np.minimum(flat[ok].astype(np.int64) + 1, table_bytes.shape[0] - 1)]
+    return out.reshape(rows.shape + (table_bytes.shape[1],))
+
+
+def _collisions_keyed_on_head_k(rows):
+    r = np.asarray(rows).astype(np.uint64)
+    shared = np.zeros(r.shape[1], np.int64)
+    for k in range(r.shape[1]):
+        _, c = np.unique(r[:, k], return_counts=True)
+        shared[k] = int((c.astype(np.int64) * (c.astype(np.int64) - 1) // 2).sum())
+    return int(shared[0]), shared
+
+
+def _python_mutants():
+    """(what the mistake is, module, attribute, replacement)"""
     rms, proj, conv = dense.rmsnorm, dense.project, dense.conv_residual
+    deq, fp8deq = orc.nf4_dequantize, orc.fp8_dequantize
+    return [
+        ("rows fetched one row further on", orc, "fetch_rows", _fetch_rows_shifted),
+        ("NF4 rows decoded with their nibbles swapped", orc, "nf4_dequantize",
+         lambda rows: deq(np.concatenate([((np.asarray(rows)[:, :32] & 15) << 4) | (np.asarray(rows)[:, :32] >> 4),
+                                          np.asarray(rows)[:, 32:]], axis=1).astype(np.uint8))),
+        ("FP8 rows decoded with the scale applied twice", orc, "fp8_dequantize",
+         lambda q, sc: fp8deq(q, sc) * np.asarray(sc, np.float64)[:, None]),
+        ("head collisions counted on head k alone", orc, "collision_counts", _collisions_keyed_on_head_k),
+    ] + [(what, dense, name, fn) for what, name, fn in _dense_mutants(rms, proj, conv)]
+
+
+def _dense_mutants(rms, proj, conv):
     return [
         ("SiLU as c * sigmoid(-c)", "silu", _silu_negated),
         ("RMSNorm without its gain", "rmsnorm", lambda z, g, eps: rms(z, np.ones_like(np.asarray(g)), eps)),
@@ -142,6 +173,8 @@ PINS = [
     (P.test_causality_of_the_whole_path, {}),
     (P.test_parameter_budgets_match_the_report, {}),
     (P.test_bucket_loads_are_poisson_like, {}),
+    (P.test_collision_counts_equal_brute_force, {"n": 60, "K": 8, "hi": 4, "seed": 3}),
+    (P.test_collision_counts_closed_forms, {}),
     (P.test_collision_counts_on_pagegram_rows, {"S": 4}),
     (P.test_pagegram_extra_shared_heads, {"S": 4, "expect": 7 / 4}),
     (P.test_engram_second_head_recollision_is_about_one_over_M, {}),
@@ -186,8 +219,8 @@ def test_c_oracle_mistake_fails_a_pin(tmp_path, monkeypatch, what, orig, mut):
     assert _first_failing_pin() is not None, f"no pin fails when the oracle has this mistake: {what}"
 
 
-@pytest.mark.parametrize("k", range(8))
-def test_dense_oracle_mistake_fails_a_pin(monkeypatch, k):
-    what, name, fn = _dense_mutants()[k]
-    monkeypatch.setattr(dense, name, fn)
+@pytest.mark.parametrize("k", range(12))
+def test_python_oracle_mistake_fails_a_pin(monkeypatch, k):
+    what, module, name, fn = _python_mutants()[k]
+    monkeypatch.setattr(module, name, fn)
     assert _first_failing_pin() is not None, f"no pin fails when the oracle has this mistake: {what}"
