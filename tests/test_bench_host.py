@@ -66,3 +66,22 @@ def test_oracle_conv_ranges_reproduce_the_whole_sequences():
     # a prefix of one sequence (n < L)
     segs = bench.conv_segments(20, L, 4, (k - 1) * dil)
     assert segs[0] == (0, 0, 5) and all(a0 == max(0, a - 9) for a0, a, _ in segs)
+
+
+def test_reference_arm_prints_one_contract_line():
+    # `bench.py --impl reference` times the CPU oracle on the headline workload and prints one
+    # JSON line with the GPU arm's metric, unit and direction, and no host<->device bytes
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["higher_is_better"] is True and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["value"] > 0 and d["config"]["workload"].startswith("engram27b-module-bf16")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
